@@ -1,0 +1,109 @@
+"""ctypes front end of the float64 C oracle (``ssd_oracle.c``).
+
+TEST INFRASTRUCTURE ONLY -- the CUDA library is checked against this; it is
+never part of the product path.
+
+Definition followed (the op timed by the "kernel_ssd_gpu.json" and
+"kernel_ssd_cpu.json" benchmark records, whose ``scan`` implementation is the
+step-by-step form of the recurrence):
+
+    S_t = exp(la_t) S_{t-1} + k_t v_t^T,  S_{-1} = h0,   out_t = S_t^T q_t
+
+with head h reading group h // (H // G).  Gradients are the exact adjoint of
+the loss <dout, out>.  Inputs are taken as stored (fp32 values widened to
+float64 exactly); all arithmetic is float64.
+"""
+import ctypes
+import os
+
+import numpy as np
+
+from .build import build_oracle
+
+_lib = None
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        path = build_oracle()
+        lib = ctypes.CDLL(path)
+        d = ctypes.POINTER(ctypes.c_double)
+        i64 = ctypes.c_int64
+        lib.ssd_oracle_fwd.argtypes = [d, d, d, d, d, d] + [i64] * 6
+        lib.ssd_oracle_fwd.restype = ctypes.c_int
+        lib.ssd_oracle_bwd.argtypes = [d] * 13 + [i64] * 6
+        lib.ssd_oracle_bwd.restype = ctypes.c_int
+        lib.ssd_oracle_num_threads.argtypes = []
+        lib.ssd_oracle_num_threads.restype = ctypes.c_int
+        _lib = lib
+    return _lib
+
+
+def oracle_threads() -> int:
+    """Threads the oracle's OpenMP loops use (1 without OpenMP)."""
+    return int(_load().ssd_oracle_num_threads())
+
+
+def _f64(x):
+    if x is None:
+        return None
+    if hasattr(x, "detach"):  # torch tensor
+        x = x.detach().cpu().numpy()
+    return np.ascontiguousarray(np.asarray(x, dtype=np.float64))
+
+
+def _ptr(a):
+    if a is None:
+        return ctypes.POINTER(ctypes.c_double)()
+    return a.ctypes.data_as(ctypes.POINTER(ctypes.c_double))
+
+
+def _dims(q, v, la):
+    B, L, G, dk = q.shape
+    H, dv = v.shape[2], v.shape[3]
+    assert v.shape[:2] == (B, L) and la.shape == (B, L, H)
+    assert H % G == 0, "heads must split evenly over groups"
+    return B, L, G, H, dk, dv
+
+
+def ssd_fwd_ref(q, k, v, log_alpha, h0=None):
+    """out [B,L,H,dv] (float64) for q,k [B,L,G,dk], v [B,L,H,dv], log_alpha [B,L,H]."""
+    q, k, v, la, h0 = map(_f64, (q, k, v, log_alpha, h0))
+    B, L, G, H, dk, dv = _dims(q, v, la)
+    assert k.shape == q.shape
+    if h0 is not None:
+        assert h0.shape == (B, H, dk, dv)
+    out = np.zeros((B, L, H, dv), np.float64)
+    rc = _load().ssd_oracle_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(la), _ptr(h0), _ptr(out),
+                                B, L, G, H, dk, dv)
+    if rc:
+        raise RuntimeError(f"oracle fwd failed ({rc})")
+    return out
+
+
+def ssd_bwd_ref(q, k, v, log_alpha, h0, dout, per_head=False):
+    """Gradients of <dout, out>: dict with dq, dk, dv, dlog_alpha, dh0 (float64).
+
+    With ``per_head=True`` also returns dq_heads / dk_heads [B,L,H,dk], the
+    per-head contributions before the sum over the heads of each group.
+    """
+    q, k, v, la, h0, dout = map(_f64, (q, k, v, log_alpha, h0, dout))
+    B, L, G, H, dk, dv = _dims(q, v, la)
+    assert k.shape == q.shape and dout.shape == v.shape
+    r = {
+        "dq": np.zeros((B, L, G, dk)), "dk": np.zeros((B, L, G, dk)),
+        "dv": np.zeros((B, L, H, dv)), "dlog_alpha": np.zeros((B, L, H)),
+        "dh0": np.zeros((B, H, dk, dv)),
+    }
+    dqh = np.zeros((B, L, H, dk)) if per_head else None
+    dkh = np.zeros((B, L, H, dk)) if per_head else None
+    rc = _load().ssd_oracle_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(la), _ptr(h0), _ptr(dout),
+                                _ptr(r["dq"]), _ptr(r["dk"]), _ptr(r["dv"]),
+                                _ptr(r["dlog_alpha"]), _ptr(r["dh0"]), _ptr(dqh), _ptr(dkh),
+                                B, L, G, H, dk, dv)
+    if rc:
+        raise RuntimeError(f"oracle bwd failed ({rc})")
+    if per_head:
+        r["dq_heads"], r["dk_heads"] = dqh, dkh
+    return r

@@ -1,0 +1,66 @@
+"""Seeded synthetic inputs for the SSD scan workloads.
+
+Shared by the tests, the benchmark and the smoke check; it holds no part of
+the scan's arithmetic -- only shapes and random draws.
+
+Workload shapes are the [batch, groups, heads, dk, dv] tuples and sequence
+lengths of the "kernel_ssd_gpu.json" benchmark page (its ``config.configs``
+and ``config.seq_lens`` blocks).  Distributions (not on the pages):
+q, k ~ N(0,1)/sqrt(dk); v ~ N(0,1); log_alpha = -softplus(N(mu,1)) with mu=0
+(mu=-3 for the long-memory workload); h0 ~ 0.1 N(0,1); dout ~ N(0,1).
+Draw order q, k, v, log_alpha, h0, dout from one PCG64 stream per workload.
+"""
+from dataclasses import dataclass
+
+import numpy as np
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    B: int
+    G: int
+    H: int
+    L: int
+    dk: int
+    dv: int
+    chunk: int = 64
+    la_mu: float = 0.0
+    seed: int = 0
+
+    @property
+    def tokens(self) -> int:
+        """Tokens per call as the benchmark pages count them: B * L * H."""
+        return self.B * self.L * self.H
+
+
+# index i gets seed 1000 + i
+WORKLOADS = [
+    Workload("g1h1_d128_L512", 4, 1, 1, 512, 128, 128, seed=1000),
+    Workload("g2h4_dk48_dv40_L2048", 4, 2, 4, 2048, 48, 40, seed=1001),
+    Workload("g2h8_d128_L2048", 4, 2, 8, 2048, 128, 128, seed=1002),
+    Workload("g1h24_dk128_dv64_L8192", 2, 1, 24, 8192, 128, 64, seed=1003),
+    Workload("g2h8_d128_L8192_long", 4, 2, 8, 8192, 128, 128, la_mu=-3.0, seed=1004),
+]
+BY_NAME = {w.name: w for w in WORKLOADS}
+
+
+def _softplus(x):
+    return np.logaddexp(0.0, x)
+
+
+def make_inputs(B, L, G, H, dk, dv, seed, la_mu=0.0, with_h0=True, with_dout=True):
+    """float32 numpy arrays q, k, v, log_alpha, h0, dout (h0/dout None if not asked)."""
+    rng = np.random.default_rng(seed)
+    f32 = np.float32
+    q = (rng.standard_normal((B, L, G, dk)) / np.sqrt(dk)).astype(f32)
+    k = (rng.standard_normal((B, L, G, dk)) / np.sqrt(dk)).astype(f32)
+    v = rng.standard_normal((B, L, H, dv)).astype(f32)
+    la = (-_softplus(rng.standard_normal((B, L, H)) + la_mu)).astype(f32)
+    h0 = (0.1 * rng.standard_normal((B, H, dk, dv))).astype(f32) if with_h0 else None
+    dout = rng.standard_normal((B, L, H, dv)).astype(f32) if with_dout else None
+    return q, k, v, la, h0, dout
+
+
+def workload_inputs(w: Workload, with_h0=True, with_dout=True):
+    return make_inputs(w.B, w.L, w.G, w.H, w.dk, w.dv, w.seed, w.la_mu, with_h0, with_dout)
