@@ -1,0 +1,145 @@
+/*
+ * ssd.h -- C ABI of the GB300 (sm_103a) chunked SSD scan library, libssd.so.
+ *
+ * The operation is the gated linear-attention ("SSD") scan benchmarked by the
+ * "kernel_ssd_gpu.json" and "kernel_ssd_cpu.json" benchmark pages
+ * (https://www.mackelab.org/probjax/benchmarks/, their `results` tables, impl
+ * "chunked", modes "fwd" and "fwd_bwd").  Those pages give only shapes, byte
+ * counts and timings; the recurrence below is the one this library fixes:
+ *
+ *   per batch b, head h, group g = h / (H / G)   (heads split evenly and
+ *   contiguously over the groups)
+ *     S_{-1} = h0[b,h]                                        dk x dv
+ *     S_t    = exp(log_alpha[b,t,h]) * S_{t-1} + k[b,t,g] v[b,t,h]^T
+ *     out[b,t,h,:] = S_t^T q[b,t,g]        (inclusive state, q unscaled)
+ *
+ * ssd_bwd returns the gradients of the scalar <dout, out> with respect to
+ * q, k, v, log_alpha and h0 (the pages' fwd_bwd records return gradients for
+ * all five arguments: their output bytes equal the argument bytes plus a
+ * scalar).  dq and dk are summed over the heads that share a group.
+ *
+ * Layouts: every tensor is contiguous, row-major, fp32, in device memory
+ * (the pages' argument byte counts fix these shapes exactly):
+ *   q, k, dq, dk        [B, L, G, dk]
+ *   v, dv, out, dout    [B, L, H, dv]
+ *   log_alpha, dlog_alpha [B, L, H]
+ *   h0, dh0             [B, H, dk, dv]
+ *
+ * Conventions for every entry point:
+ *   - The caller owns every buffer.  Outputs are fully overwritten (dq and dk
+ *     are not accumulated into).  Inputs are never written.  Outputs must not
+ *     alias inputs or each other.
+ *   - h0 == NULL means a zero initial state; dh0 == NULL means "not wanted".
+ *   - Every pointer must be 16-byte aligned (SSD_ERR_ALIGN otherwise).
+ *   - L == 0 (or B == 0) is a valid empty problem: nothing is launched,
+ *     except that ssd_bwd zero-fills dh0 when it is given.
+ *   - Any L >= 1 is accepted; a last chunk shorter than `chunk` is handled.
+ *   - log_alpha must be finite (a documented precondition that the device
+ *     does not check; use a large negative finite value such as -1e4 for
+ *     "forget everything").
+ *   - Calls are asynchronous on `stream` (NULL = legacy default stream):
+ *     argument checks happen on the host before anything is enqueued; the
+ *     call returns without synchronising.  Temporary device workspace is
+ *     taken with cudaMallocAsync and released with cudaFreeAsync on the same
+ *     stream.  Calls on different streams may run concurrently.
+ *   - No function throws or aborts; each returns an ssd_status code.
+ *
+ * Two arithmetic paths implement the same op (ssd_set_path):
+ *   SSD_PATH_TC   tensor-core path: tcgen05.mma (kind::tf32) with the
+ *                 accumulators in tensor memory; operands rounded to TF32,
+ *                 accumulation in fp32.  Supports chunk == 64,
+ *                 dk, dv multiples of 8 up to 128.
+ *   SSD_PATH_SIMT all-fp32 CUDA-core path.  Supports chunk in {16, 32, 64},
+ *                 1 <= dk, dv <= 128.
+ */
+#ifndef SSD_H_
+#define SSD_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define SSD_API __attribute__((visibility("default")))
+#else
+#define SSD_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Matches the runtime's opaque stream handle (cudaStream_t). */
+typedef struct CUstream_st *ssd_stream_t;
+
+typedef enum ssd_status {
+  SSD_OK = 0,
+  SSD_ERR_ARG = 1,          /* a size <= 0 where >= 1 is needed, H % G != 0,
+                               a required pointer is NULL, or unknown path */
+  SSD_ERR_ALIGN = 2,        /* a pointer is not 16-byte aligned */
+  SSD_ERR_CHUNK = 3,        /* chunk length not supported by the active path */
+  SSD_ERR_UNSUPPORTED = 4,  /* dk / dv outside what the active path supports */
+  SSD_ERR_ALLOC = 5,        /* workspace allocation failed (nothing launched) */
+  SSD_ERR_LAUNCH = 6,       /* a kernel launch failed */
+  SSD_ERR_TIMEOUT = 7,      /* a device-side bounded wait gave up (see
+                               ssd_last_device_error) */
+  SSD_ERR_CUDA = 8          /* another CUDA runtime error (no device, ...) */
+} ssd_status;
+
+typedef enum ssd_path { SSD_PATH_TC = 0, SSD_PATH_SIMT = 1 } ssd_path;
+
+/*
+ * Forward: out = the inclusive-state outputs of the recurrence above.
+ *   q, k       [B,L,G,dk]   read
+ *   v          [B,L,H,dv]   read
+ *   log_alpha  [B,L,H]      read (finite)
+ *   h0         [B,H,dk,dv]  read, or NULL for zeros
+ *   out        [B,L,H,dv]   written
+ *   chunk      the chunk length of the chunked evaluation; results do not
+ *              depend on it beyond rounding.
+ */
+SSD_API int ssd_fwd(const float *q, const float *k, const float *v,
+            const float *log_alpha, const float *h0, float *out,
+            int64_t B, int64_t L, int64_t G, int64_t H, int64_t dk,
+            int64_t dv, int64_t chunk, ssd_stream_t stream);
+
+/*
+ * Backward: gradients of <dout, out>, recomputing every intermediate from the
+ * inputs (nothing is saved by ssd_fwd).
+ *   dout        [B,L,H,dv]   read
+ *   dq, dk      [B,L,G,dk]   written (summed over the heads of each group)
+ *   dv          [B,L,H,dv]   written
+ *   dlog_alpha  [B,L,H]      written
+ *   dh0         [B,H,dk,dv]  written, or NULL when not wanted
+ * h0 may be NULL (zeros).  Other arguments as for ssd_fwd.
+ */
+SSD_API int ssd_bwd(const float *q, const float *k, const float *v,
+            const float *log_alpha, const float *h0, const float *dout,
+            float *dq, float *dk, float *dv, float *dlog_alpha, float *dh0,
+            int64_t B, int64_t L, int64_t G, int64_t H, int64_t dk_dim,
+            int64_t dv_dim, int64_t chunk, ssd_stream_t stream);
+
+/* Select the arithmetic path for later calls in this process (all threads).
+ * Returns SSD_ERR_ARG for an unknown value.  The initial path is SSD_PATH_TC,
+ * or the value of the environment variable SSD_PATH ("tc" / "simt") read at
+ * the first call. */
+SSD_API int ssd_set_path(int path);
+SSD_API int ssd_get_path(void);
+
+/* Static description of a status code; never NULL. */
+SSD_API const char *ssd_strerror(int status);
+
+/* Synchronises `stream`, then reads and clears the library's device error
+ * word on the current device.  Returns SSD_ERR_TIMEOUT when a bounded
+ * device-side wait gave up since the last check (the affected outputs are
+ * then unspecified), SSD_ERR_CUDA when the synchronisation itself failed,
+ * SSD_OK otherwise. */
+SSD_API int ssd_last_device_error(ssd_stream_t stream);
+
+/* Library version as major*10000 + minor*100 + patch. */
+SSD_API int ssd_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SSD_H_ */

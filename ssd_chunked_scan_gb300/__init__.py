@@ -1,0 +1,15 @@
+"""GB300 (sm_103a) chunked SSD scan: a C-ABI CUDA library with a thin binding.
+
+``ssd_chunked_scan_gb300.ssd`` is the binding (it loads libssd.so and raises
+if it is missing); ``ssd_chunked_scan_gb300.inputs`` holds the seeded
+synthetic workloads.  The binding is imported lazily so that the input
+generators work on machines without the built library.
+"""
+
+
+def __getattr__(name):
+    if name in ("ssd_fwd", "ssd_bwd", "ssd_set_path", "ssd_get_path", "ssd_strerror",
+                "ssd_last_device_error", "SSDError", "SSD_PATH_TC", "SSD_PATH_SIMT"):
+        from . import ssd
+        return getattr(ssd, name)
+    raise AttributeError(name)

@@ -1,0 +1,203 @@
+// C ABI of libssd (declared in include/ssd.h): argument checks, workspace,
+// path selection and dispatch.  No kernel arithmetic lives here.
+#include <atomic>
+#include <cstdlib>
+#include <cstring>
+
+#include "../../include/ssd.h"
+#include "common.cuh"
+#include "simt.h"
+#include "tc.h"
+
+namespace {
+
+std::atomic<int> g_path{-1};
+
+int current_path() {
+  int p = g_path.load(std::memory_order_relaxed);
+  if (p < 0) {
+    p = SSD_PATH_SIMT;
+    const char *e = std::getenv("SSD_PATH");
+    if (e && (std::strcmp(e, "tc") == 0 || std::strcmp(e, "TC") == 0)) p = SSD_PATH_TC;
+    int expected = -1;
+    if (!g_path.compare_exchange_strong(expected, p)) p = expected;
+  }
+  return p;
+}
+
+bool misaligned(const void *p) { return p && (reinterpret_cast<uintptr_t>(p) & 15u); }
+
+// Host-side fault injection for tests of the error path: with
+// SSD_FAULT_ALLOC=1 in the environment every workspace request fails before
+// anything is enqueued.
+bool alloc_fault_injected() {
+  const char *e = std::getenv("SSD_FAULT_ALLOC");
+  return e && e[0] == '1';
+}
+
+int check_common(int64_t B, int64_t L, int64_t G, int64_t H, int64_t dk, int64_t dv,
+                 int64_t chunk) {
+  if (B < 0 || L < 0 || G < 1 || H < 1 || dk < 1 || dv < 1 || chunk < 1) return SSD_ERR_ARG;
+  if (H % G != 0) return SSD_ERR_ARG;
+  if (B > 65535 || H > 65535 || G > 65535) return SSD_ERR_UNSUPPORTED;
+  return SSD_OK;
+}
+
+int check_path_shape(int path, int64_t L, int64_t dk, int64_t dv, int64_t chunk) {
+  if (path == SSD_PATH_SIMT) {
+    if (chunk != 16 && chunk != 32 && chunk != 64) return SSD_ERR_CHUNK;
+    if (dk > 128 || dv > 128) return SSD_ERR_UNSUPPORTED;
+  } else {
+    int rc = ssd::tc::check_shape(dk, dv, chunk);
+    if (rc) return rc;
+  }
+  if (ssd::cdiv(L, chunk) > 0x7fffffffLL) return SSD_ERR_UNSUPPORTED;
+  return SSD_OK;
+}
+
+ssd::Geo make_geo(int64_t B, int64_t L, int64_t G, int64_t H, int64_t dk, int64_t dv,
+                  int64_t chunk) {
+  ssd::Geo g;
+  g.B = B; g.L = L; g.G = G; g.H = H; g.dk = dk; g.dv = dv;
+  g.C = (int)chunk;
+  g.N = ssd::cdiv(L, chunk);
+  g.hpg = (int)(H / G);
+  return g;
+}
+
+int from_cuda(cudaError_t e) {
+  if (e == cudaSuccess) return SSD_OK;
+  if (e == cudaErrorMemoryAllocation) return SSD_ERR_ALLOC;
+  if (e == cudaErrorLaunchFailure || e == cudaErrorInvalidConfiguration ||
+      e == cudaErrorLaunchOutOfResources || e == cudaErrorInvalidDeviceFunction ||
+      e == cudaErrorNoKernelImageForDevice || e == cudaErrorInvalidValue)
+    return SSD_ERR_LAUNCH;
+  return SSD_ERR_CUDA;
+}
+
+// Stream-ordered workspace.  The first use on a device raises that device's
+// default memory pool release threshold so freed workspace is kept for the
+// next call instead of being returned to the driver at every synchronisation.
+int ws_alloc(void **p, size_t bytes, cudaStream_t s) {
+  *p = nullptr;
+  if (bytes == 0) return SSD_OK;
+  if (alloc_fault_injected()) return SSD_ERR_ALLOC;
+  static std::atomic<unsigned long long> tuned{0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return SSD_ERR_CUDA;
+  if (dev < 64 && !(tuned.load() & (1ull << dev))) {
+    cudaMemPool_t pool;
+    if (cudaDeviceGetDefaultMemPool(&pool, dev) == cudaSuccess) {
+      uint64_t thr = ~0ull;
+      cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &thr);
+    }
+    tuned.fetch_or(1ull << dev);
+  }
+  cudaError_t e = cudaMallocAsync(p, bytes, s);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    *p = nullptr;
+    return e == cudaErrorMemoryAllocation ? SSD_ERR_ALLOC : from_cuda(e);
+  }
+  return SSD_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int ssd_version(void) { return 100; }
+
+const char *ssd_strerror(int status) {
+  switch (status) {
+    case SSD_OK: return "ok";
+    case SSD_ERR_ARG: return "invalid argument (size, H % G, null pointer or unknown path)";
+    case SSD_ERR_ALIGN: return "pointer not 16-byte aligned";
+    case SSD_ERR_CHUNK: return "chunk length not supported by the active path";
+    case SSD_ERR_UNSUPPORTED: return "shape not supported by the active path";
+    case SSD_ERR_ALLOC: return "workspace allocation failed";
+    case SSD_ERR_LAUNCH: return "kernel launch failed";
+    case SSD_ERR_TIMEOUT: return "a device-side bounded wait timed out";
+    case SSD_ERR_CUDA: return "CUDA runtime error";
+    default: return "unknown status";
+  }
+}
+
+int ssd_set_path(int path) {
+  if (path != SSD_PATH_TC && path != SSD_PATH_SIMT) return SSD_ERR_ARG;
+  g_path.store(path);
+  return SSD_OK;
+}
+
+int ssd_get_path(void) { return current_path(); }
+
+int ssd_fwd(const float *q, const float *k, const float *v, const float *log_alpha,
+            const float *h0, float *out, int64_t B, int64_t L, int64_t G, int64_t H, int64_t dk,
+            int64_t dv, int64_t chunk, ssd_stream_t stream) {
+  int rc = check_common(B, L, G, H, dk, dv, chunk);
+  if (rc) return rc;
+  const int path = current_path();
+  rc = check_path_shape(path, L, dk, dv, chunk);
+  if (rc) return rc;
+  if (B == 0 || L == 0) return SSD_OK;
+  if (!q || !k || !v || !log_alpha || !out) return SSD_ERR_ARG;
+  if (misaligned(q) || misaligned(k) || misaligned(v) || misaligned(log_alpha) ||
+      misaligned(h0) || misaligned(out))
+    return SSD_ERR_ALIGN;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const ssd::Geo g = make_geo(B, L, G, H, dk, dv, chunk);
+  const size_t wsb = path == SSD_PATH_SIMT ? ssd::simt::fwd_workspace_bytes(g)
+                                           : ssd::tc::fwd_workspace_bytes(g);
+  void *ws = nullptr;
+  rc = ws_alloc(&ws, wsb, s);
+  if (rc) return rc;
+  cudaError_t e = path == SSD_PATH_SIMT ? ssd::simt::fwd(q, k, v, log_alpha, h0, out, g, ws, s)
+                                        : ssd::tc::fwd(q, k, v, log_alpha, h0, out, g, ws, s);
+  if (ws) cudaFreeAsync(ws, s);
+  return from_cuda(e);
+}
+
+int ssd_bwd(const float *q, const float *k, const float *v, const float *log_alpha,
+            const float *h0, const float *dout, float *dq, float *dk, float *dv,
+            float *dlog_alpha, float *dh0, int64_t B, int64_t L, int64_t G, int64_t H,
+            int64_t dk_dim, int64_t dv_dim, int64_t chunk, ssd_stream_t stream) {
+  int rc = check_common(B, L, G, H, dk_dim, dv_dim, chunk);
+  if (rc) return rc;
+  const int path = current_path();
+  rc = check_path_shape(path, L, dk_dim, dv_dim, chunk);
+  if (rc) return rc;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (misaligned(q) || misaligned(k) || misaligned(v) || misaligned(log_alpha) ||
+      misaligned(h0) || misaligned(dout) || misaligned(dq) || misaligned(dk) ||
+      misaligned(dv) || misaligned(dlog_alpha) || misaligned(dh0))
+    return SSD_ERR_ALIGN;
+  if (B == 0 || L == 0) {
+    if (dh0 && B > 0)
+      return from_cuda(cudaMemsetAsync(dh0, 0, sizeof(float) * B * H * dk_dim * dv_dim, s));
+    return SSD_OK;
+  }
+  if (!q || !k || !v || !log_alpha || !dout || !dq || !dk || !dv || !dlog_alpha)
+    return SSD_ERR_ARG;
+  const ssd::Geo g = make_geo(B, L, G, H, dk_dim, dv_dim, chunk);
+  const size_t wsb = path == SSD_PATH_SIMT ? ssd::simt::bwd_workspace_bytes(g)
+                                           : ssd::tc::bwd_workspace_bytes(g);
+  void *ws = nullptr;
+  rc = ws_alloc(&ws, wsb, s);
+  if (rc) return rc;
+  cudaError_t e =
+      path == SSD_PATH_SIMT
+          ? ssd::simt::bwd(q, k, v, log_alpha, h0, dout, dq, dk, dv, dlog_alpha, dh0, g, ws, s)
+          : ssd::tc::bwd(q, k, v, log_alpha, h0, dout, dq, dk, dv, dlog_alpha, dh0, g, ws, s);
+  if (ws) cudaFreeAsync(ws, s);
+  return from_cuda(e);
+}
+
+int ssd_last_device_error(ssd_stream_t stream) {
+  cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return SSD_ERR_CUDA;
+  unsigned int word = 0;
+  if (ssd::tc::read_and_clear_error(&word) != cudaSuccess) return SSD_ERR_CUDA;
+  return word ? SSD_ERR_TIMEOUT : SSD_OK;
+}
+
+}  // extern "C"

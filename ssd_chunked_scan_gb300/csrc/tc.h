@@ -1,0 +1,25 @@
+// Host entry points of the tensor-core path (tc.cu).
+#pragma once
+#include "common.cuh"
+
+namespace ssd {
+namespace tc {
+
+// 0 when the tensor-core path supports (dk, dv, chunk), else an ssd_status.
+int check_shape(int64_t dk, int64_t dv, int64_t chunk);
+
+size_t fwd_workspace_bytes(const Geo &g);
+size_t bwd_workspace_bytes(const Geo &g);
+
+cudaError_t fwd(const float *q, const float *k, const float *v, const float *la, const float *h0,
+                float *out, const Geo &g, void *ws, cudaStream_t s);
+cudaError_t bwd(const float *q, const float *k, const float *v, const float *la, const float *h0,
+                const float *dout, float *dq, float *dk, float *dv, float *dla, float *dh0,
+                const Geo &g, void *ws, cudaStream_t s);
+
+// Reads and clears the device error word of the current device (set by a
+// bounded wait that gave up).
+cudaError_t read_and_clear_error(unsigned int *word);
+
+}  // namespace tc
+}  // namespace ssd

@@ -1,0 +1,159 @@
+"""Python binding of libssd (include/ssd.h): argument marshalling only.
+
+Every step of the scan runs in the CUDA library; this module checks tensor
+dtypes / devices / shapes, passes raw device pointers and the current CUDA
+stream through ctypes, and turns a non-zero status into ``SSDError``.  There is
+no fallback: if libssd.so is missing or fails to load, importing this module
+raises.
+"""
+import ctypes
+import os
+
+import torch
+
+_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_lib", "libssd.so")
+
+SSD_OK = 0
+SSD_ERR_ARG = 1
+SSD_ERR_ALIGN = 2
+SSD_ERR_CHUNK = 3
+SSD_ERR_UNSUPPORTED = 4
+SSD_ERR_ALLOC = 5
+SSD_ERR_LAUNCH = 6
+SSD_ERR_TIMEOUT = 7
+SSD_ERR_CUDA = 8
+SSD_PATH_TC = 0
+SSD_PATH_SIMT = 1
+
+EXPORTED = ("ssd_fwd", "ssd_bwd", "ssd_set_path", "ssd_get_path", "ssd_strerror",
+            "ssd_last_device_error", "ssd_version")
+
+
+class SSDError(RuntimeError):
+    def __init__(self, status, where):
+        self.status = status
+        super().__init__(f"{where}: {ssd_strerror(status)} (status {status})")
+
+
+def _load():
+    if not os.path.exists(_LIB_PATH):
+        raise ImportError(f"libssd.so not built at {_LIB_PATH}; run __graft_entry__.build()")
+    lib = ctypes.CDLL(_LIB_PATH)
+    p, i64 = ctypes.c_void_p, ctypes.c_int64
+    lib.ssd_fwd.argtypes = [p] * 6 + [i64] * 7 + [p]
+    lib.ssd_fwd.restype = ctypes.c_int
+    lib.ssd_bwd.argtypes = [p] * 11 + [i64] * 7 + [p]
+    lib.ssd_bwd.restype = ctypes.c_int
+    lib.ssd_set_path.argtypes = [ctypes.c_int]
+    lib.ssd_set_path.restype = ctypes.c_int
+    lib.ssd_get_path.argtypes = []
+    lib.ssd_get_path.restype = ctypes.c_int
+    lib.ssd_strerror.argtypes = [ctypes.c_int]
+    lib.ssd_strerror.restype = ctypes.c_char_p
+    lib.ssd_last_device_error.argtypes = [p]
+    lib.ssd_last_device_error.restype = ctypes.c_int
+    lib.ssd_version.argtypes = []
+    lib.ssd_version.restype = ctypes.c_int
+    return lib
+
+
+LIB = _load()
+
+
+def ssd_strerror(status: int) -> str:
+    return LIB.ssd_strerror(int(status)).decode()
+
+
+def ssd_set_path(path: int) -> None:
+    rc = LIB.ssd_set_path(int(path))
+    if rc:
+        raise SSDError(rc, "ssd_set_path")
+
+
+def ssd_get_path() -> int:
+    return int(LIB.ssd_get_path())
+
+
+def ssd_last_device_error(stream=None) -> int:
+    return int(LIB.ssd_last_device_error(_stream(stream)))
+
+
+def _stream(stream):
+    if stream is None:
+        return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, torch.cuda.Stream):
+        return ctypes.c_void_p(stream.cuda_stream)
+    return ctypes.c_void_p(int(stream))
+
+
+def _ptr(t):
+    return ctypes.c_void_p(0 if t is None else t.data_ptr())
+
+
+def _check(name, t, shape, device):
+    if t is None:
+        return
+    if not isinstance(t, torch.Tensor) or t.dtype != torch.float32:
+        raise TypeError(f"{name} must be a float32 torch tensor")
+    if t.device != device:
+        raise ValueError(f"{name} must be on {device}, got {t.device}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+
+
+def _dims(q, v):
+    if q.dim() != 4 or v.dim() != 4:
+        raise ValueError("q must be [B,L,G,dk] and v [B,L,H,dv]")
+    B, L, G, dk = q.shape
+    H, dv = v.shape[2], v.shape[3]
+    return B, L, G, H, dk, dv
+
+
+def ssd_fwd(q, k, v, log_alpha, h0=None, chunk=64, out=None, stream=None):
+    """out [B,L,H,dv] of the scan for q,k [B,L,G,dk], v [B,L,H,dv], log_alpha [B,L,H]."""
+    B, L, G, H, dk, dv = _dims(q, v)
+    dev = q.device
+    _check("q", q, (B, L, G, dk), dev)
+    _check("k", k, (B, L, G, dk), dev)
+    _check("v", v, (B, L, H, dv), dev)
+    _check("log_alpha", log_alpha, (B, L, H), dev)
+    _check("h0", h0, (B, H, dk, dv), dev)
+    if out is None:
+        out = torch.empty((B, L, H, dv), dtype=torch.float32, device=dev)
+    _check("out", out, (B, L, H, dv), dev)
+    rc = LIB.ssd_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(h0), _ptr(out),
+                     B, L, G, H, dk, dv, int(chunk), _stream(stream))
+    if rc:
+        raise SSDError(rc, "ssd_fwd")
+    return out
+
+
+def ssd_bwd(q, k, v, log_alpha, h0, dout, chunk=64, want_dh0=True, grads=None, stream=None):
+    """Gradients of <dout, out>: dict dq, dk, dv, dlog_alpha, dh0 (dh0 None if not wanted).
+
+    ``grads`` may supply preallocated output tensors under the same keys.
+    """
+    B, L, G, H, dk, dv = _dims(q, v)
+    dev = q.device
+    for n, t, s in (("q", q, (B, L, G, dk)), ("k", k, (B, L, G, dk)), ("v", v, (B, L, H, dv)),
+                    ("log_alpha", log_alpha, (B, L, H)), ("h0", h0, (B, H, dk, dv)),
+                    ("dout", dout, (B, L, H, dv))):
+        _check(n, t, s, dev)
+    shapes = {"dq": (B, L, G, dk), "dk": (B, L, G, dk), "dv": (B, L, H, dv),
+              "dlog_alpha": (B, L, H), "dh0": (B, H, dk, dv)}
+    g = dict(grads or {})
+    for n, s in shapes.items():
+        if n == "dh0" and not want_dh0:
+            g[n] = None
+            continue
+        if g.get(n) is None:
+            g[n] = torch.empty(s, dtype=torch.float32, device=dev)
+        _check(n, g[n], s, dev)
+    rc = LIB.ssd_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(h0), _ptr(dout),
+                     _ptr(g["dq"]), _ptr(g["dk"]), _ptr(g["dv"]), _ptr(g["dlog_alpha"]),
+                     _ptr(g["dh0"]), B, L, G, H, dk, dv, int(chunk), _stream(stream))
+    if rc:
+        raise SSDError(rc, "ssd_bwd")
+    return g

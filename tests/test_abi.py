@@ -1,0 +1,89 @@
+"""The C ABI library: it loads without a GPU, exports every entry point that
+include/ssd.h declares, and rejects bad arguments on the host before touching
+the device (so these run on a CPU-only machine)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+LIB = os.path.join(ROOT, "ssd_chunked_scan_gb300", "_lib", "libssd.so")
+
+
+def _declared():
+    names = set()
+    for h in os.listdir(os.path.join(ROOT, "include")):
+        if h.endswith(".h"):
+            txt = open(os.path.join(ROOT, "include", h)).read()
+            names |= set(re.findall(r"SSD_API\s+[\w\s\*]*?\b(ssd_\w+)\s*\(", txt))
+    return names
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(LIB):
+        from ssd_chunked_scan_gb300.build import build_lib
+        build_lib()
+    l = ctypes.CDLL(LIB)
+    p, i64 = ctypes.c_void_p, ctypes.c_int64
+    l.ssd_fwd.argtypes = [p] * 6 + [i64] * 7 + [p]
+    l.ssd_bwd.argtypes = [p] * 11 + [i64] * 7 + [p]
+    l.ssd_strerror.restype = ctypes.c_char_p
+    return l
+
+
+def test_exports_every_declared_symbol(lib):
+    names = _declared()
+    assert {"ssd_fwd", "ssd_bwd", "ssd_set_path", "ssd_strerror"} <= names
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_strerror_total(lib):
+    for s in range(-1, 12):
+        assert lib.ssd_strerror(s)
+    assert lib.ssd_strerror(0) == b"ok"
+
+
+def _fwd(lib, ptrs=(0x1000,) * 6, B=1, L=8, G=1, H=1, dk=8, dv=8, chunk=64):
+    return lib.ssd_fwd(*[ctypes.c_void_p(x) for x in ptrs], B, L, G, H, dk, dv, chunk, None)
+
+
+def _bwd(lib, ptrs=(0x1000,) * 11, B=1, L=8, G=1, H=1, dk=8, dv=8, chunk=64):
+    return lib.ssd_bwd(*[ctypes.c_void_p(x) for x in ptrs], B, L, G, H, dk, dv, chunk, None)
+
+
+@pytest.mark.parametrize("path", [0, 1])
+def test_host_argument_checks(lib, path):
+    assert lib.ssd_set_path(path) == 0
+    assert _fwd(lib, G=2, H=3) == 1              # H % G != 0
+    assert _fwd(lib, B=-1) == 1
+    assert _fwd(lib, L=-5) == 1
+    assert _fwd(lib, G=0) == 1
+    assert _fwd(lib, dk=0) == 1
+    assert _fwd(lib, chunk=0) == 1
+    assert _fwd(lib, chunk=48) == 3              # no path takes chunk 48
+    assert _fwd(lib, dk=512) == 4
+    assert _fwd(lib, L=0) == 0                   # empty problem: nothing launched
+    assert _fwd(lib, B=0) == 0
+    assert _fwd(lib, ptrs=(0x1000, 0x1000, 0, 0x1000, 0, 0x1000)) == 1   # v NULL
+    assert _fwd(lib, ptrs=(0x1000, 0x1004, 0x1000, 0x1000, 0, 0x1000)) == 2
+    assert _bwd(lib, ptrs=(0x1000,) * 10 + (0x1008,)) == 2
+    assert _bwd(lib, ptrs=(0x1000,) * 5 + (0,) + (0x1000,) * 5) == 1      # dout NULL
+    assert _bwd(lib, L=0, ptrs=(0,) * 11) == 0   # empty, dh0 not wanted
+
+
+def test_set_path(lib):
+    assert lib.ssd_set_path(7) == 1
+    assert lib.ssd_set_path(1) == 0 and lib.ssd_get_path() == 1
+    assert lib.ssd_set_path(0) == 0 and lib.ssd_get_path() == 0
+
+
+def test_injected_workspace_failure_is_reported_before_launch(lib, monkeypatch):
+    # SSD_FAULT_ALLOC=1 makes the workspace request fail on the host; the
+    # call must return SSD_ERR_ALLOC without enqueueing anything
+    monkeypatch.setenv("SSD_FAULT_ALLOC", "1")
+    assert lib.ssd_set_path(1) == 0
+    assert _fwd(lib) == 5
+    assert _bwd(lib) == 5
