@@ -1,0 +1,439 @@
+#!/usr/bin/env python
+"""Throughput of the chunked SSD scan (fwd + bwd) on one or more GPUs.
+
+A step is one forward and one backward pass (ssd_fwd then ssd_bwd, the whole
+hot path) over the g2h8_d128 L=8192 long-memory workload: B=4, G=2, H=8,
+L=8192, dk=dv=128, chunk 64, fp32 storage, seeded synthetic inputs.  The
+metric is tokens/s with tokens = B*L*H per step.  Prints ONE JSON line
+(rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--path tc|simt]
+  python bench.py --impl reference ...   # the float64 CPU oracle, timed on host cores
+
+Under torchrun each rank runs the full workload on its own GPU (the units --
+batch entries and groups -- are independent, so there is no collective on the
+data path); value is the tokens of all ranks over the slowest rank's time.
+"""
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "SSD fwd / fwd_bwd tokens/s (B·L·H) at 1 GB300 and % of roofline vs oracle"
+WORKLOAD = "g2h8_d128_L8192_long"
+# chunked fwd_bwd, g2h8_d128, seq 8192 on the "kernel_ssd_gpu.json" benchmark
+# page (RTX 3090): 11.883 ms per call -> B*L*H / t tokens/s
+PAGE_FWD_BWD_MS = {"g2h8_d128_L8192_long": 11.883, "g2h8_d128_L2048": 3.210,
+                   "g1h24_dk128_dv64_L8192": 10.695, "g1h1_d128_L512": 0.2519,
+                   "g2h4_dk48_dv40_L2048": 0.9683}
+PAGE_FWD_MS = {"g2h8_d128_L8192_long": 4.182, "g2h8_d128_L2048": 1.170,
+               "g1h24_dk128_dv64_L8192": 3.461, "g1h1_d128_L512": 0.08903,
+               "g2h4_dk48_dv40_L2048": 0.3709}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        d = json.load(open(p))
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                "source": "measured"}
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+                "source": "fallback"}
+
+
+# nominal dense tensor rates: tf32 1.1 PF vs bf16 2.25 PF per GPU
+TF32_OVER_BF16 = 1.1 / 2.25
+# FP32 FFMA: 152 SMs x 128 lanes x 2 flop x 2070 MHz (maximum SM clock)
+FP32_TFLOPS = 152 * 128 * 2 * 2.070e9 / 1e12
+
+
+def kernel_costs(w):
+    """Algorithmic bytes and flops per launch of each kernel, and its bound.
+
+    Bytes count each tensor a kernel must read or write once (a group's q / k
+    once, not once per head); flops count multiply-adds as 2, the causal half
+    of each chunk's C x C block, per (b, l) token: QK^T G*C*dk, PV / dP etc.
+    H*C*d, each dk x dv contraction 2*H*dk*dv."""
+    B, L, G, H, dk, dv, C = w.B, w.L, w.G, w.H, w.dk, w.dv, w.chunk
+    N = -(-L // C)
+    f = 4
+    qk = B * L * G * dk * f
+    vv = B * L * H * dv * f
+    la = B * L * H * f
+    st = B * H * N * dk * dv * f
+    h0 = B * H * dk * dv * f
+    BL = B * L
+    c = {}
+    c["simt.chunk_state"] = (qk + vv + la + st, BL * 2 * H * dk * dv, "alu")
+    c["simt.query_state"] = (qk + vv + la + st, BL * 2 * H * dk * dv, "alu")
+    c["simt.state_scan_fwd"] = (2 * st + h0, 2 * B * H * N * dk * dv, "hbm")
+    c["simt.state_scan_rev"] = (2 * st + h0, 2 * B * H * N * dk * dv, "hbm")
+    c["simt.chunk_out"] = (2 * qk + 2 * vv + la + st, BL * (G * C * dk + H * C * dv + 2 * H * dk * dv), "alu")
+    c["simt.chunk_grad"] = (2 * qk + 2 * vv + la + 2 * st + 2 * qk + vv + la,
+                            BL * (G * C * dk + 2 * H * C * (dk + dv) + 6 * H * dk * dv), "alu")
+    c["simt.dla_carry"] = (2 * la, BL * H, "hbm")
+    # tensor-core path
+    c["tc.fwd"] = (2 * qk + vv + la + h0 + vv, BL * (G * C * dk + H * C * dv + 4 * H * dk * dv), "tensor")
+    c["tc.bwd"] = (2 * qk + 2 * vv + la + h0 + 2 * qk + vv + la + h0,
+                   BL * (G * C * dk + 2 * H * C * (dk + dv) + 10 * H * dk * dv), "tensor")
+    return c
+
+
+def step_totals(w):
+    """Minimal bytes and flops of one fwd + bwd step (two calls)."""
+    B, L, G, H, dk, dv, C = w.B, w.L, w.G, w.H, w.dk, w.dv, w.chunk
+    f = 4
+    args = (2 * B * L * G * dk + B * L * H * dv + B * L * H + B * H * dk * dv) * f
+    out = B * L * H * dv * f
+    bytes_fb = 3 * args + 2 * out  # fwd reads args writes out; bwd reads args + dout, writes grads
+    fl_f = B * L * (G * C * dk + H * C * dv + 4 * H * dk * dv)
+    fl_b = B * L * (G * C * dk + 2 * H * C * (dk + dv) + 10 * H * dk * dv)
+    return bytes_fb, fl_f + fl_b, args + out, fl_f
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 100 ms in the background."""
+
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.samples = []
+        self.proc = None
+        self.index = index
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.t = threading.Thread(target=self._read, daemon=True)
+        self.t.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 8:
+                self.samples.append((time.time(), parts))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        inwin = [p for (t, p) in self.samples if t0 <= t <= t1]
+        window = "timed"
+        if not inwin:
+            inwin = [p for (t, p) in self.samples]
+            window = "whole run (timed region shorter than the sampling period)"
+        if not inwin:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(p[0]) for p in inwin if num(p[0]) is not None]
+        mx = [num(p[1]) for p in inwin if num(p[1]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for p in inwin for i in range(4) if p[4 + i].lower() == "active"})
+        pw = [num(p[2]) for p in inwin if num(p[2]) is not None]
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "power_w_max": max(pw) if pw else None, "samples": len(inwin), "window": window}
+
+
+def cpu_oracle_sample(w, min_seconds=10.0, max_reps=4):
+    """Time the float64 oracle (fwd + bwd) on one batch entry of the workload,
+    repeated until min_seconds have passed; returns tokens/s and details."""
+    import numpy as np
+    from oracle import oracle_threads, ssd_bwd_ref, ssd_fwd_ref
+    from ssd_chunked_scan_gb300.inputs import workload_inputs
+    q, k, v, la, h0, dout = workload_inputs(w)
+    sl = lambda x: np.ascontiguousarray(x[:1])
+    q, k, v, la, h0, dout = map(sl, (q, k, v, la, h0, dout))
+    toks, t0, reps = 0, time.perf_counter(), 0
+    while True:
+        ssd_fwd_ref(q, k, v, la, h0)
+        ssd_bwd_ref(q, k, v, la, h0, dout)
+        reps += 1
+        toks += w.L * w.H
+        el = time.perf_counter() - t0
+        if el >= min_seconds or reps >= max_reps:
+            break
+    return {"value": toks / el, "unit": "tokens/s", "cores": oracle_threads(), "kind": "oracle",
+            "sample": f"batch entry 0 of {w.name} (1 x {w.L} x {w.H} heads, all groups), "
+                      f"float64 fwd+bwd, {reps} rep(s), {el:.1f} s"}
+
+
+def run_reference(args, w):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    import numpy as np
+    from oracle import oracle_threads, ssd_bwd_ref, ssd_fwd_ref
+    from ssd_chunked_scan_gb300.inputs import workload_inputs
+    q, k, v, la, h0, dout = workload_inputs(w)
+    # bounded sample: batch entry 0, group 0 and its heads, full sequence
+    hpg = w.H // w.G
+    sq = lambda x: np.ascontiguousarray(x[:1, :, :1])
+    sv = lambda x: np.ascontiguousarray(x[:1, :, :hpg])
+    q, k = sq(q), sq(k)
+    v, la, dout = sv(v), sv(la), sv(dout)
+    h0 = np.ascontiguousarray(h0[:1, :hpg])
+
+    def step():
+        ssd_fwd_ref(q, k, v, la, h0)
+        ssd_bwd_ref(q, k, v, la, h0, dout)
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    el = time.perf_counter() - t0
+    toks = w.L * hpg
+    val = toks * args.steps / el
+    sample = f"batch entry 0, group 0 ({hpg} heads) of {w.name}, full L={w.L}, float64 fwd+bwd per step"
+    line = {"impl": "reference", "metric": METRIC, "value": val, "unit": "tokens/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": el / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "mode": "fwd_bwd", "B": w.B, "G": w.G, "H": w.H,
+                       "L": w.L, "dk": w.dk, "dv": w.dv, "chunk": w.chunk,
+                       "sample_tokens_per_step": toks},
+            "cpu_baseline": {"value": val, "unit": "tokens/s", "cores": oracle_threads(),
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": val, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--path", default=os.environ.get("SSD_BENCH_PATH", "tc"), choices=["tc", "simt"])
+    ap.add_argument("--workload", default=WORKLOAD)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    from ssd_chunked_scan_gb300.inputs import BY_NAME
+    w = BY_NAME[args.workload]
+    if args.impl == "reference":
+        return run_reference(args, w)
+
+    import torch
+    import torch.distributed as dist
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+
+    from ssd_chunked_scan_gb300 import ssd
+    from ssd_chunked_scan_gb300.inputs import workload_inputs
+    ssd.ssd_set_path(ssd.SSD_PATH_TC if args.path == "tc" else ssd.SSD_PATH_SIMT)
+
+    host = [torch.from_numpy(x).pin_memory() for x in workload_inputs(w)]
+    q, k, v, la, h0, dout = [x.to(dev) for x in host]
+    out = torch.empty((w.B, w.L, w.H, w.dv), device=dev)
+    grads = {"dq": torch.empty_like(q), "dk": torch.empty_like(k), "dv": torch.empty_like(v),
+             "dlog_alpha": torch.empty_like(la), "dh0": torch.empty_like(h0)}
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        ssd.ssd_fwd(q, k, v, la, h0, chunk=w.chunk, out=out)
+        ssd.ssd_bwd(q, k, v, la, h0, dout, chunk=w.chunk, grads=grads)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    if ssd.ssd_last_device_error() != 0:
+        raise RuntimeError("device error word set during warm-up")
+
+    # timed region: exactly K steps, inputs (323 MiB + dout 128 MiB) larger than L2
+    barrier()
+    torch.cuda.synchronize(dev)
+    n0 = ssd.ssd_launch_count()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    th0 = time.time()
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    th1 = time.time()
+    barrier()
+    launches = ssd.ssd_launch_count() - n0
+    ms = e0.elapsed_time(e1) / args.steps
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    if ssd.ssd_last_device_error() != 0:
+        raise RuntimeError("device error word set during the timed region")
+
+    # per-kernel device time: the same K steps again with every launch bracketed by events
+    ssd.ssd_trace_reset()
+    ssd.ssd_trace_enable(True)
+    for _ in range(args.steps):
+        step()
+    torch.cuda.synchronize(dev)
+    ssd.ssd_trace_enable(False)
+    trace = ssd.ssd_trace_collect()
+    ssd.ssd_trace_reset()
+    clocks.stop()
+    clk = clocks.summary(th0, th1)
+
+    # fwd alone (context line)
+    torch.cuda.synchronize(dev)
+    f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    f0.record(stream)
+    for _ in range(args.steps):
+        ssd.ssd_fwd(q, k, v, la, h0, chunk=w.chunk, out=out)
+    f1.record(stream)
+    torch.cuda.synchronize(dev)
+    fwd_ms = f0.elapsed_time(f1) / args.steps
+
+    # end to end through the public API: pinned host inputs -> device, fwd+bwd,
+    # out and every gradient -> pinned host, every step
+    e2e = None
+    if not args.no_e2e:
+        h_out = torch.empty(out.shape, pin_memory=True)
+        h_grads = {n: torch.empty(t.shape, pin_memory=True) for n, t in grads.items()}
+        dq_, dk_, dv_, dla_, dh0_ = (torch.empty_like(t) for t in (q, k, v, la, h0))
+        dbufs = [torch.empty_like(t) for t in (q, k, v, la, h0, dout)]
+
+        def e2e_step():
+            for d, hsrc in zip(dbufs, host):
+                d.copy_(hsrc, non_blocking=True)
+            o = ssd.ssd_fwd(*dbufs[:5], chunk=w.chunk, out=out)
+            g = ssd.ssd_bwd(*dbufs, chunk=w.chunk, grads=grads)
+            h_out.copy_(o, non_blocking=True)
+            for n in h_grads:
+                h_grads[n].copy_(g[n], non_blocking=True)
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize(dev)
+        barrier()
+        g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        g0.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        g1.record(stream)
+        torch.cuda.synchronize(dev)
+        barrier()
+        e2e_ms = g0.elapsed_time(g1) / args.steps
+        if world > 1:
+            t = torch.tensor([e2e_ms], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e2e_ms = float(t.item())
+        h2d = sum(x.numel() * x.element_size() for x in host)
+        d2h = h_out.numel() * 4 + sum(x.numel() * x.element_size() for x in h_grads.values())
+        e2e = {"value": w.tokens * world / (e2e_ms / 1e3), "unit": "tokens/s",
+               "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return 0
+
+    peaks = load_peaks()
+    costs = kernel_costs(w)
+    top = max(trace.items(), key=lambda kv: kv[1][1])
+    top_name, (top_n, top_ms) = top
+    per_launch_ms = top_ms / top_n
+    kb, kf, kbound = costs.get(top_name, (None, None, "hbm"))
+    if kbound == "tensor":
+        peak = peaks["bf16_tflops"] * TF32_OVER_BF16
+        ach = kf / (per_launch_ms / 1e3) / 1e12
+        roof = {"bound": "tensor", "achieved": ach, "peak": peak, "unit": "TFLOP/s",
+                "peak_note": f"tf32 = {peaks['source']} bf16 burst x nominal tf32/bf16 ratio"}
+    elif kbound == "alu":
+        ach = kf / (per_launch_ms / 1e3) / 1e12
+        roof = {"bound": "alu", "achieved": ach, "peak": FP32_TFLOPS, "unit": "TFLOP/s",
+                "peak_note": "fp32 FFMA: 152 SMs x 128 lanes x 2 flop x 2070 MHz"}
+    else:
+        ach = kb / (per_launch_ms / 1e3) / 1e9
+        roof = {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "peak_note": f"{peaks['source']} copy bandwidth"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["traffic"] = None
+    roof["kernel"] = top_name
+    roof["kernel_ms_per_launch"] = per_launch_ms
+    roof["alg_bytes_per_launch"] = kb
+    roof["alg_flops_per_launch"] = kf
+
+    bytes_fb, fl_fb, bytes_f, fl_f = step_totals(w)
+    t_hbm = bytes_fb / (peaks["hbm_gbs"] * 1e9)
+    t_tc = fl_fb / (peaks["bf16_tflops"] * TF32_OVER_BF16 * 1e12)
+    step_roof_s = max(t_hbm, t_tc)
+    value = w.tokens * world / (ms / 1e3)
+    page_ms = PAGE_FWD_BWD_MS.get(w.name)
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": (value / (w.tokens / (page_ms / 1e3))) if page_ms else None,
+        "dtype": "tf32" if args.path == "tc" else "f32", "data": "synthetic",
+        "config": {"workload": w.name, "mode": "fwd_bwd", "path": args.path, "B": w.B, "G": w.G,
+                   "H": w.H, "L": w.L, "dk": w.dk, "dv": w.dv, "chunk": w.chunk,
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "l2": "no flush: each step's inputs and outputs (967 MiB) exceed L2"},
+        "roofline": roof,
+        "step_roofline": {"bound": "hbm" if t_hbm >= t_tc else "tensor",
+                          "alg_bytes": bytes_fb, "alg_flops": fl_fb,
+                          "roofline_ms": step_roof_s * 1e3, "frac": step_roof_s * 1e3 / ms},
+        "fwd": {"ms": fwd_ms, "tokens_per_s": w.tokens / (fwd_ms / 1e3),
+                "frac_of_roofline": max(bytes_f / (peaks["hbm_gbs"] * 1e9),
+                                        fl_f / (peaks["bf16_tflops"] * TF32_OVER_BF16 * 1e12)) / (fwd_ms / 1e3)},
+        "kernels": {n: {"launches": c, "ms_total": t, "share": t / sum(x[1] for x in trace.values())}
+                    for n, (c, t) in sorted(trace.items(), key=lambda kv: -kv[1][1])},
+        "gpu_launches": launches,
+        "clocks": clk,
+        "e2e": e2e,
+        "page_context": {"rtx3090_fwd_bwd_ms": page_ms, "rtx3090_fwd_ms": PAGE_FWD_MS.get(w.name)},
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_oracle_sample(w)
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -135,6 +135,23 @@ SSD_API const char *ssd_strerror(int status);
  * SSD_OK otherwise. */
 SSD_API int ssd_last_device_error(ssd_stream_t stream);
 
+/* Launch accounting and tracing (for profiling; not needed for the op).
+ * ssd_launch_count: kernels launched by this library in this process so far.
+ * ssd_trace_enable(1): from now on, bracket every launch with two CUDA events
+ *   on its stream (adds a few microseconds of device time per launch).
+ * ssd_trace_collect: waits for the traced launches, folds them into
+ *   per-kernel totals, returns the number of distinct kernel names (or a
+ *   negated ssd_status on failure).
+ * ssd_trace_get(i, ...): name (NUL-terminated, truncated to name_len),
+ *   launch count and total device milliseconds of kernel i.
+ * ssd_trace_reset: drops all records and totals. */
+SSD_API long long ssd_launch_count(void);
+SSD_API int ssd_trace_enable(int on);
+SSD_API int ssd_trace_collect(void);
+SSD_API int ssd_trace_get(int i, char *name, int name_len, long long *launches,
+                          double *total_ms);
+SSD_API int ssd_trace_reset(void);
+
 /* Library version as major*10000 + minor*100 + patch. */
 SSD_API int ssd_version(void);
 

@@ -54,3 +54,20 @@ __device__ inline void chunk_cumsum64(const float *__restrict__ la, int64_t firs
 }
 
 }  // namespace ssd
+
+namespace ssd {
+// Scope around one kernel launch: counts it and, when tracing is enabled,
+// records CUDA events before and after it on stream s (trace.cu).
+class LaunchTrace {
+ public:
+  LaunchTrace(const char *name, cudaStream_t s);
+  ~LaunchTrace();
+  LaunchTrace(const LaunchTrace &) = delete;
+  LaunchTrace &operator=(const LaunchTrace &) = delete;
+
+ private:
+  const char *name_;
+  cudaStream_t s_;
+  void *a_;
+};
+}  // namespace ssd

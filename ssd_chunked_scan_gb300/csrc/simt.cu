@@ -530,6 +530,7 @@ template <int MA, int NB, bool QUERY>
 static void launch_state(const float *X, const float *Y, const float *la, float *st, float *Adec,
                          const Geo &g, cudaStream_t s) {
   dim3 grid((unsigned)g.N, (unsigned)g.H, (unsigned)g.B);
+  LaunchTrace lt(QUERY ? "simt.query_state" : "simt.chunk_state", s);
   k_chunk_state<MA, NB, QUERY><<<grid, NT, 0, s>>>(X, Y, la, st, Adec, g);
 }
 
@@ -546,6 +547,7 @@ static void dispatch_state(const float *X, const float *Y, const float *la, floa
 static void launch_scan_fwd(float *st, const float *Adec, const float *h0, const Geo &g,
                             cudaStream_t s) {
   dim3 grid((unsigned)(g.B * g.H), (unsigned)cdiv(g.dk * g.dv, NT));
+  LaunchTrace lt("simt.state_scan_fwd", s);
   k_scan_fwd<<<grid, NT, 0, s>>>(st, Adec, h0, g);
 }
 
@@ -564,6 +566,7 @@ cudaError_t fwd(const float *q, const float *k, const float *v, const float *la,
   dispatch_state<false>(k, v, la, st, Adec, g, s);
   launch_scan_fwd(st, Adec, h0, g, s);
   dim3 grid((unsigned)g.N, (unsigned)g.H, (unsigned)g.B);
+  LaunchTrace lt("simt.chunk_out", s);
   if (g.dv > 64) k_chunk_out<2><<<grid, NT, 0, s>>>(q, k, v, la, st, out, g);
   else k_chunk_out<1><<<grid, NT, 0, s>>>(q, k, v, la, st, out, g);
   return cudaGetLastError();
@@ -579,6 +582,7 @@ static cudaError_t launch_grad(const float *q, const float *k, const float *v, c
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
   dim3 grid((unsigned)g.N, (unsigned)g.G, (unsigned)g.B);
+  LaunchTrace lt("simt.chunk_grad", s);
   k_chunk_grad<NBK, NBV><<<grid, NT, smem, s>>>(q, k, v, la, dout, Hst, dXst, dq, dk, dv, dla,
                                                  dcs_sum, g);
   return cudaGetLastError();
@@ -599,6 +603,7 @@ cudaError_t bwd(const float *q, const float *k, const float *v, const float *la,
   dispatch_state<true>(q, dout, la, dXst, nullptr, g, s);
   {
     dim3 grid((unsigned)(g.B * g.H), (unsigned)cdiv(g.dk * g.dv, NT));
+    LaunchTrace lt("simt.state_scan_rev", s);
     k_scan_rev<<<grid, NT, 0, s>>>(dXst, Adec, dh0, g);
   }
   cudaError_t err;
@@ -608,7 +613,10 @@ cudaError_t bwd(const float *q, const float *k, const float *v, const float *la,
   else if (bv) err = launch_grad<1, 2>(q, k, v, la, dout, Hst, dXst, dq, dk, dv, dla, dcs_sum, g, s);
   else err = launch_grad<1, 1>(q, k, v, la, dout, Hst, dXst, dq, dk, dv, dla, dcs_sum, g, s);
   if (err != cudaSuccess) return err;
-  k_dla_carry<<<(unsigned)(g.B * g.H), NT, 0, s>>>(dla, dcs_sum, g);
+  {
+    LaunchTrace lt("simt.dla_carry", s);
+    k_dla_carry<<<(unsigned)(g.B * g.H), NT, 0, s>>>(dla, dcs_sum, g);
+  }
   return cudaGetLastError();
 }
 

@@ -26,7 +26,8 @@ SSD_PATH_TC = 0
 SSD_PATH_SIMT = 1
 
 EXPORTED = ("ssd_fwd", "ssd_bwd", "ssd_set_path", "ssd_get_path", "ssd_strerror",
-            "ssd_last_device_error", "ssd_version")
+            "ssd_last_device_error", "ssd_version", "ssd_launch_count", "ssd_trace_enable",
+            "ssd_trace_collect", "ssd_trace_get", "ssd_trace_reset")
 
 
 class SSDError(RuntimeError):
@@ -54,6 +55,13 @@ def _load():
     lib.ssd_last_device_error.restype = ctypes.c_int
     lib.ssd_version.argtypes = []
     lib.ssd_version.restype = ctypes.c_int
+    lib.ssd_launch_count.argtypes = []
+    lib.ssd_launch_count.restype = ctypes.c_longlong
+    lib.ssd_trace_enable.argtypes = [ctypes.c_int]
+    lib.ssd_trace_collect.argtypes = []
+    lib.ssd_trace_get.argtypes = [ctypes.c_int, ctypes.c_char_p, ctypes.c_int,
+                                  ctypes.POINTER(ctypes.c_longlong), ctypes.POINTER(ctypes.c_double)]
+    lib.ssd_trace_reset.argtypes = []
     return lib
 
 
@@ -76,6 +84,35 @@ def ssd_get_path() -> int:
 
 def ssd_last_device_error(stream=None) -> int:
     return int(LIB.ssd_last_device_error(_stream(stream)))
+
+
+def ssd_launch_count() -> int:
+    """Kernels launched by libssd in this process so far."""
+    return int(LIB.ssd_launch_count())
+
+
+def ssd_trace_enable(on: bool) -> None:
+    LIB.ssd_trace_enable(1 if on else 0)
+
+
+def ssd_trace_reset() -> None:
+    LIB.ssd_trace_reset()
+
+
+def ssd_trace_collect() -> dict:
+    """Per-kernel {name: (launches, total_ms)} of the traced launches so far."""
+    n = LIB.ssd_trace_collect()
+    if n < 0:
+        raise SSDError(-n, "ssd_trace_collect")
+    res = {}
+    buf = ctypes.create_string_buffer(128)
+    for i in range(n):
+        cnt, ms = ctypes.c_longlong(0), ctypes.c_double(0.0)
+        rc = LIB.ssd_trace_get(i, buf, 128, ctypes.byref(cnt), ctypes.byref(ms))
+        if rc:
+            raise SSDError(rc, "ssd_trace_get")
+        res[buf.value.decode()] = (int(cnt.value), float(ms.value))
+    return res
 
 
 def _stream(stream):
