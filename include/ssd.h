@@ -82,7 +82,9 @@ typedef enum ssd_status {
   SSD_ERR_LAUNCH = 6,       /* a kernel launch failed */
   SSD_ERR_TIMEOUT = 7,      /* a device-side bounded wait gave up (see
                                ssd_last_device_error) */
-  SSD_ERR_CUDA = 8          /* another CUDA runtime error (no device, ...) */
+  SSD_ERR_CUDA = 8,         /* another CUDA runtime error (no device, ...) */
+  SSD_ERR_SCRATCH = 9       /* the problem needs more scratch than
+                               ssd_fwd_noalloc's fixed buffer holds */
 } ssd_status;
 
 typedef enum ssd_path { SSD_PATH_TC = 0, SSD_PATH_SIMT = 1 } ssd_path;
@@ -117,6 +119,36 @@ SSD_API int ssd_bwd(const float *q, const float *k, const float *v,
             float *dq, float *dk, float *dv, float *dlog_alpha, float *dh0,
             int64_t B, int64_t L, int64_t G, int64_t H, int64_t dk_dim,
             int64_t dv_dim, int64_t chunk, ssd_stream_t stream);
+
+/*
+ * Allocation-free forward.  The benchmark pages have no counterpart: this
+ * entry point exists for callers that cannot allocate device memory at call
+ * time -- code whose memory is fully reserved up front by a framework's own
+ * caching allocator (so a further cudaMalloc fails), real-time loops that
+ * must not allocate once running, and hooks that run inside an allocator and
+ * so must not call back into it.
+ *
+ * Same arguments, layouts and result as ssd_fwd, always on the all-fp32
+ * CUDA-core path (chunk in {16, 32, 64}, 1 <= dk, dv <= 128), whatever
+ * ssd_set_path selected.  Its scratch is one fixed array of
+ * ssd_fwd_noalloc_scratch_bytes() bytes (32 MiB) that the library holds in
+ * the memory of every GPU on which it is loaded, until the process exits.
+ * The problem must fit: B*H*ceil(L/chunk)*(dk*dv + 1)*4 bytes at most
+ * (for example B*H*L <= 32768 at dk = dv = 128, chunk 64); larger problems
+ * return SSD_ERR_SCRATCH before anything is enqueued.
+ *   - It never calls cudaMalloc, cudaFree or any allocating routine.
+ *   - The first call on a device looks up the array's device address on that
+ *     device; make that first call before any stream capture.
+ *   - Every call on a device shares the one array: calls that overlap on the
+ *     GPU (different streams, or different host threads without ordering)
+ *     race and give wrong results.  Nothing in the array needs clearing;
+ *     each call writes all the scratch it reads.
+ */
+SSD_API int ssd_fwd_noalloc(const float *q, const float *k, const float *v,
+                            const float *log_alpha, const float *h0, float *out,
+                            int64_t B, int64_t L, int64_t G, int64_t H, int64_t dk,
+                            int64_t dv, int64_t chunk, ssd_stream_t stream);
+SSD_API size_t ssd_fwd_noalloc_scratch_bytes(void);
 
 /* Select the arithmetic path for later calls in this process (all threads).
  * Returns SSD_ERR_ARG for an unknown value.  The initial path is SSD_PATH_TC,

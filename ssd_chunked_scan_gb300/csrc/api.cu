@@ -119,6 +119,7 @@ const char *ssd_strerror(int status) {
     case SSD_ERR_LAUNCH: return "kernel launch failed";
     case SSD_ERR_TIMEOUT: return "a device-side bounded wait timed out";
     case SSD_ERR_CUDA: return "CUDA runtime error";
+    case SSD_ERR_SCRATCH: return "problem too large for the fixed scratch of ssd_fwd_noalloc";
     default: return "unknown status";
   }
 }

@@ -22,12 +22,14 @@ SSD_ERR_ALLOC = 5
 SSD_ERR_LAUNCH = 6
 SSD_ERR_TIMEOUT = 7
 SSD_ERR_CUDA = 8
+SSD_ERR_SCRATCH = 9
 SSD_PATH_TC = 0
 SSD_PATH_SIMT = 1
 
 EXPORTED = ("ssd_fwd", "ssd_bwd", "ssd_set_path", "ssd_get_path", "ssd_strerror",
             "ssd_last_device_error", "ssd_version", "ssd_launch_count", "ssd_trace_enable",
-            "ssd_trace_collect", "ssd_trace_get", "ssd_trace_reset")
+            "ssd_trace_collect", "ssd_trace_get", "ssd_trace_reset", "ssd_fwd_noalloc",
+            "ssd_fwd_noalloc_scratch_bytes")
 
 
 class SSDError(RuntimeError):
@@ -62,6 +64,10 @@ def _load():
     lib.ssd_trace_get.argtypes = [ctypes.c_int, ctypes.c_char_p, ctypes.c_int,
                                   ctypes.POINTER(ctypes.c_longlong), ctypes.POINTER(ctypes.c_double)]
     lib.ssd_trace_reset.argtypes = []
+    lib.ssd_fwd_noalloc.argtypes = [p] * 6 + [i64] * 7 + [p]
+    lib.ssd_fwd_noalloc.restype = ctypes.c_int
+    lib.ssd_fwd_noalloc_scratch_bytes.argtypes = []
+    lib.ssd_fwd_noalloc_scratch_bytes.restype = ctypes.c_size_t
     return lib
 
 
@@ -194,3 +200,27 @@ def ssd_bwd(q, k, v, log_alpha, h0, dout, chunk=64, want_dh0=True, grads=None, s
     if rc:
         raise SSDError(rc, "ssd_bwd")
     return g
+
+
+def ssd_fwd_noalloc(q, k, v, log_alpha, h0, out, chunk=64, stream=None):
+    """Forward into a caller-provided ``out`` without any device allocation.
+
+    For callers that cannot allocate device memory at call time (memory fully
+    reserved up front by another allocator, allocation-free real-time loops,
+    allocator hooks).  Runs the all-fp32 path with the library's fixed
+    scratch array; problems that do not fit raise SSDError(SSD_ERR_SCRATCH).
+    Calls that overlap on the GPU share that array and race.
+    """
+    B, L, G, H, dk, dv = _dims(q, v)
+    dev = q.device
+    for n, t, s in (("q", q, (B, L, G, dk)), ("k", k, (B, L, G, dk)), ("v", v, (B, L, H, dv)),
+                    ("log_alpha", log_alpha, (B, L, H)), ("h0", h0, (B, H, dk, dv)),
+                    ("out", out, (B, L, H, dv))):
+        _check(n, t, s, dev)
+    if out is None:
+        raise ValueError("out must be given")
+    rc = LIB.ssd_fwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(h0), _ptr(out),
+                             B, L, G, H, dk, dv, int(chunk), _stream(stream))
+    if rc:
+        raise SSDError(rc, "ssd_fwd_noalloc")
+    return out
