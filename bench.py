@@ -57,7 +57,7 @@ TF32_OVER_BF16 = 1.1 / 2.25
 FP32_TFLOPS = 152 * 128 * 2 * 2.070e9 / 1e12
 
 
-def kernel_costs(w):
+def kernel_costs(w, sms=152):
     """Algorithmic bytes and flops per launch of each kernel, and its bound.
 
     Bytes count each tensor a kernel must read or write once (a group's q / k
@@ -82,11 +82,32 @@ def kernel_costs(w):
     c["simt.chunk_grad"] = (2 * qk + 2 * vv + la + 2 * st + 2 * qk + vv + la,
                             BL * (G * C * dk + 2 * H * C * (dk + dv) + 6 * H * dk * dv), "alu")
     c["simt.dla_carry"] = (2 * la, BL * H, "hbm")
-    # tensor-core path
-    c["tc.fwd"] = (2 * qk + vv + la + h0 + vv, BL * (G * C * dk + H * C * dv + 4 * H * dk * dv), "tensor")
-    c["tc.bwd"] = (2 * qk + 2 * vv + la + h0 + 2 * qk + vv + la + h0,
-                   BL * (G * C * dk + 2 * H * C * (dk + dv) + 10 * H * dk * dv), "tensor")
+    # tensor-core path: per-segment states [B,H,nseg,dk,dv]; every kernel is
+    # bound by HBM traffic at these shapes (arithmetic intensity < 60 FLOP/B)
+    nseg = tc_nseg(w, sms)
+    sst = B * H * nseg * dk * dv * f
+    fw = BL * (G * C * dk + H * C * dv + 4 * H * dk * dv)      # forward pass
+    st2 = BL * 2 * H * dk * dv                                 # one state contraction
+    for n in ("tc.seg_state", "tc.seg_state_dq", "tc.seg_state_dk", "tc.seg_state_dv"):
+        c[n] = (qk + vv + la + sst, st2, "hbm")
+    c["tc.seg_scan"] = (2 * sst + h0, 2 * B * H * nseg * dk * dv, "hbm")
+    c["tc.walk_out"] = (2 * qk + 2 * vv + la + sst, fw, "hbm")
+    c["tc.walk_dv"] = (2 * qk + 2 * vv + la + sst, fw, "hbm")
+    for n in ("tc.walk_dq", "tc.walk_dk"):
+        c[n] = (3 * qk + 2 * vv + 2 * la + sst, fw + BL * H * dk * 2, "hbm")
+    c["tc.dla_intra"] = (2 * qk + 2 * vv + 2 * la, BL * (G * C * dk + H * C * dv + H * C), "hbm")
+    c["tc.dla"] = (4 * la + 2 * sst, BL * H * 4 + 2 * B * H * nseg * dk * dv, "hbm")
     return c
+
+
+def tc_nseg(w, sms=152):
+    """Segments per sequence chosen by the tensor-core path (same rule as tc.cu:
+    enough segments for about four CTAs per SM)."""
+    bh = w.B * w.H
+    want = max(1, -(-4 * sms // bh))
+    Ls = -(-(-(-w.L // want)) // 64) * 64
+    Ls = max(Ls, 64)
+    return -(-w.L // Ls)
 
 
 def step_totals(w):
@@ -239,6 +260,8 @@ def main():
     ap.add_argument("--workload", default=WORKLOAD)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--mode", default="fwd_bwd", choices=["fwd_bwd", "fwd"],
+                    help="fwd times ssd_fwd alone (a step is then one forward pass)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -270,7 +293,8 @@ def main():
 
     def step():
         ssd.ssd_fwd(q, k, v, la, h0, chunk=w.chunk, out=out)
-        ssd.ssd_bwd(q, k, v, la, h0, dout, chunk=w.chunk, grads=grads)
+        if args.mode == "fwd_bwd":
+            ssd.ssd_bwd(q, k, v, la, h0, dout, chunk=w.chunk, grads=grads)
 
     def barrier():
         if world > 1:
@@ -341,10 +365,12 @@ def main():
             for d, hsrc in zip(dbufs, host):
                 d.copy_(hsrc, non_blocking=True)
             o = ssd.ssd_fwd(*dbufs[:5], chunk=w.chunk, out=out)
-            g = ssd.ssd_bwd(*dbufs, chunk=w.chunk, grads=grads)
             h_out.copy_(o, non_blocking=True)
-            for n in h_grads:
-                h_grads[n].copy_(g[n], non_blocking=True)
+            if args.mode == "fwd_bwd":
+                g = ssd.ssd_bwd(*dbufs, chunk=w.chunk, grads=grads)
+                for n in h_grads:
+                    h_grads[n].copy_(g[n], non_blocking=True)
+        fb = args.mode == "fwd_bwd"
         for _ in range(2):
             e2e_step()
         torch.cuda.synchronize(dev)
@@ -361,8 +387,8 @@ def main():
             t = torch.tensor([e2e_ms], device=dev)
             dist.all_reduce(t, op=dist.ReduceOp.MAX)
             e2e_ms = float(t.item())
-        h2d = sum(x.numel() * x.element_size() for x in host)
-        d2h = h_out.numel() * 4 + sum(x.numel() * x.element_size() for x in h_grads.values())
+        h2d = sum(x.numel() * x.element_size() for x in (host if fb else host[:5]))
+        d2h = h_out.numel() * 4 + (sum(x.numel() * x.element_size() for x in h_grads.values()) if fb else 0)
         e2e = {"value": w.tokens * world / (e2e_ms / 1e3), "unit": "tokens/s",
                "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
 
@@ -372,11 +398,13 @@ def main():
         return 0
 
     peaks = load_peaks()
-    costs = kernel_costs(w)
+    costs = kernel_costs(w, torch.cuda.get_device_properties(dev).multi_processor_count)
     top = max(trace.items(), key=lambda kv: kv[1][1])
     top_name, (top_n, top_ms) = top
     per_launch_ms = top_ms / top_n
-    kb, kf, kbound = costs.get(top_name, (None, None, "hbm"))
+    if top_name not in costs:
+        raise KeyError(f"no algorithmic cost entry for kernel {top_name}")
+    kb, kf, kbound = costs[top_name]
     if kbound == "tensor":
         peak = peaks["bf16_tflops"] * TF32_OVER_BF16
         ach = kf / (per_launch_ms / 1e3) / 1e12
@@ -409,7 +437,7 @@ def main():
         "higher_is_better": True, "scaling": "weak",
         "vs_baseline": (value / (w.tokens / (page_ms / 1e3))) if page_ms else None,
         "dtype": "tf32" if args.path == "tc" else "f32", "data": "synthetic",
-        "config": {"workload": w.name, "mode": "fwd_bwd", "path": args.path, "B": w.B, "G": w.G,
+        "config": {"workload": w.name, "mode": args.mode, "path": args.path, "B": w.B, "G": w.G,
                    "H": w.H, "L": w.L, "dk": w.dk, "dv": w.dv, "chunk": w.chunk,
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "l2": "no flush: each step's inputs and outputs (967 MiB) exceed L2"},

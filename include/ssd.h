@@ -46,9 +46,12 @@
  *
  * Two arithmetic paths implement the same op (ssd_set_path):
  *   SSD_PATH_TC   tensor-core path: tcgen05.mma (kind::tf32) with the
- *                 accumulators in tensor memory; operands rounded to TF32,
- *                 accumulation in fp32.  Supports chunk == 64,
- *                 dk, dv multiples of 8 up to 128.
+ *                 accumulators in tensor memory; operands rounded to TF32
+ *                 (to nearest), accumulation and state passing in fp32.
+ *                 Supports chunk == 64, dk and dv multiples of 8 up to 128,
+ *                 B*L < 2^31.  In ssd_bwd the group sums of dq and dk are
+ *                 formed with fp32 atomic adds when H > G, so their last
+ *                 bits may differ from run to run.
  *   SSD_PATH_SIMT all-fp32 CUDA-core path.  Supports chunk in {16, 32, 64},
  *                 1 <= dk, dv <= 128.
  */

@@ -16,9 +16,9 @@ std::atomic<int> g_path{-1};
 int current_path() {
   int p = g_path.load(std::memory_order_relaxed);
   if (p < 0) {
-    p = SSD_PATH_SIMT;
+    p = SSD_PATH_TC;
     const char *e = std::getenv("SSD_PATH");
-    if (e && (std::strcmp(e, "tc") == 0 || std::strcmp(e, "TC") == 0)) p = SSD_PATH_TC;
+    if (e && (std::strcmp(e, "simt") == 0 || std::strcmp(e, "SIMT") == 0)) p = SSD_PATH_SIMT;
     int expected = -1;
     if (!g_path.compare_exchange_strong(expected, p)) p = expected;
   }

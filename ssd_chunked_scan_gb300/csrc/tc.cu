@@ -1,30 +1,1038 @@
-// Tensor-core (tcgen05) path of the chunked SSD scan.
+// Tensor-core path of the chunked SSD scan (tcgen05.mma kind::tf32, fp32
+// accumulators in tensor memory, TMA-fed shared-memory operands).
+//
+// The op is the recurrence S_t = exp(la_t) S_{t-1} + k_t v_t^T, out_t = S_t^T q_t
+// timed as impl "chunked" on the "kernel_ssd_gpu.json" benchmark page.
+//
+// Everything is built from one "scan pass" on operands (q', k', v'):
+//   causal       out'_r = sum_{u<=r} exp(cs_r - cs_u)(q'_r.k'_u) v'_u + exp(cs_r) S^T q'_r
+//   anti-causal  out'_r = sum_{u>=r} exp(cs_u - cs_r)(q'_r.k'_u) v'_u + exp(A_c - cs_r) G^T q'_r
+// (cs the in-chunk inclusive prefix of la, A_c its total; S / G the state
+// entering the chunk from the left / right).  The forward is the causal pass
+// on (q, k, v).  The gradients of <dout, out> are passes too, because the
+// adjoint of a linear scan is a linear scan:
+//   dq_h = causal(q' = dout, k' = v, v' = k, initial state h0^T)
+//   dk_h = anti-causal(q' = v, k' = dout, v' = q)
+//   dv   = anti-causal(q' = k, k' = q, v' = dout), whose leftmost state is dh0
+// and dla_t = sum_{t'>=t} (q_t'.dq_h[t'] - k_t'.dk_h[t']).
+//
+// A pass cuts every (batch, head) sequence into segments of Ls tokens (a
+// multiple of the 64-token chunk) so that B*H*nseg CTAs work at once:
+//   k_seg_state  each segment's zero-initial-state contribution (one contraction)
+//   k_seg_scan   the states entering every segment (sequential over segments)
+//   k_walk       each segment's chunks in order, the running state resident in
+//                tensor memory
+//
+// Operands the tensor cores must see transposed (anything contracted over
+// tokens) are made by the threads from the TMA-loaded tiles: into tensor
+// memory as the A operand (k'^T, v'^T) or into shared memory in the K-major
+// 128-byte-swizzled layout (w * k'^T, P).  Operands written by threads are
+// rounded to TF32 to nearest; TMA-fed ones are truncated by the tensor core.
+#include <algorithm>
+#include <cstring>
+#include <mutex>
+
+#include <cudaTypedefs.h>
+
 #include "../../include/ssd.h"
 #include "common.cuh"
 #include "tc.h"
+#include "tc_common.cuh"
 
 namespace ssd {
 namespace tc {
 
-// Device error word: bit 0 = an mbarrier wait exceeded its iteration limit.
-__device__ unsigned int g_error_word;
+constexpr int C = 64;     // chunk length of the tensor-core path
+constexpr int NTH = 128;  // threads per CTA: one per tensor-memory lane
+
+__host__ __device__ constexpr int rup(int x, int m) { return (x + m - 1) / m * m; }
+__host__ __device__ inline int64_t imin64(int64_t a, int64_t b) { return a < b ? a : b; }
+
+// Inclusive prefix sums of la over n <= 64 tokens starting at `first` (fp64
+// accumulation by warp 0, rounded once to fp32), plus `carry` added before
+// rounding.  Returns (in warp 0) the sum of the n values.
+__device__ inline double warp_cumsum64(const float *__restrict__ la, int64_t first,
+                                       int64_t stride, int n, double carry, float *cs) {
+  const int l = threadIdx.x & 31;
+  double x0 = (2 * l < n) ? (double)la[first + (int64_t)(2 * l) * stride] : 0.0;
+  double x1 = (2 * l + 1 < n) ? (double)la[first + (int64_t)(2 * l + 1) * stride] : 0.0;
+  double pair = x0 + x1, incl = pair;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    double y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (l >= o) incl += y;
+  }
+  const double excl = incl - pair;
+  if (cs) {
+    if (2 * l < n) cs[2 * l] = (float)(carry + excl + x0);
+    if (2 * l + 1 < n) cs[2 * l + 1] = (float)(carry + incl);
+  }
+  return __shfl_sync(0xffffffffu, incl, 31);
+}
+
+// ===========================================================================
+// Geometry of one scan pass on operands (q', k', v').
+struct PassGeo {
+  int64_t B, L, H;
+  int hpg;
+  int dk, dv;          // feature dims of q'/k' and of v' (= out')
+  int dkp, dkn;        // dk rounded up to 32 (TMA column blocks) / 16 (MMA N)
+  int dvp, dvn;        // dv rounded up to 32 / 16
+  int qk_per_head;     // q', k' indexed by head (1) or by group (0)
+  int v_per_head;      // v' indexed by head (1) or by group (0)
+  int Ls, nseg;        // segment length (multiple of C) and segments per sequence
+};
+
+// Output of a walk: out'[b, t, slot, 0:dv] with slot = h (out_slots == H) or
+// h / hpg (out_slots == G, summed over the group's heads by atomic adds);
+// optionally dcs[b, t, h] = y[b, t, h / hpg, :] . (the inter-chunk part of
+// out'_t, the term carried by the state entering the chunk).
+struct OutArgs {
+  float *out;
+  int out_slots;
+  const float *y;
+  float *dcs;
+};
+
+__device__ __forceinline__ int qk_slot(const PassGeo &p, int64_t h) {
+  return (int)(p.qk_per_head ? h : h / p.hpg);
+}
+__device__ __forceinline__ int v_slot(const PassGeo &p, int64_t h) {
+  return (int)(p.v_per_head ? h : h / p.hpg);
+}
+
+// ===========================================================================
+// Segment contraction, the zero-initial-state contribution of one segment:
+//   causal      D = sum_u exp(A_seg - cs_u) k'_u v'_u^T   (evaluated at its end)
+//   anti-causal D = sum_u exp(cs_u) k'_u v'_u^T           (evaluated at its start)
+// with cs the in-segment inclusive prefix of la and A_seg its total (also
+// written).  grid (nseg, H, B), 128 threads.
+// Tensor memory (256 columns): D [0,128), A operand k'^T double-buffered at
+// [128,192) / [192,256).  Shared memory: k' and v' tiles (TMA), and the B
+// operand (sc * v')^T [dvn x 64], K-major.
+template <bool REV>
+__global__ void __launch_bounds__(NTH) k_seg_state(const __grid_constant__ CUtensorMap tmK,
+                                                   const __grid_constant__ CUtensorMap tmV,
+                                                   const float *__restrict__ la,
+                                                   float *__restrict__ states,
+                                                   float *__restrict__ Aseg, PassGeo p) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  const int ncbk = p.dkp / 32, ncbv = p.dvp / 32;
+  uint8_t *Xt = smem;                       // k' tile [64 x dkp]
+  uint8_t *Yt = Xt + ncbk * 8192;           // v' tile [64 x dvp]
+  uint8_t *Bb = Yt + ncbv * 8192;           // (sc v')^T [dvn x 64]
+  float *cs = (float *)(Bb + p.dvn * 256);  // 64
+  float *sc = cs + C;                       // 64
+  __shared__ uint64_t bar_tma, bar_mma;
+  __shared__ uint32_t tmem_base;
+  __shared__ double seg_total;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int64_t seg = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const int64_t bh = b * p.H + h;
+  const int64_t s_begin = seg * (int64_t)p.Ls;
+  const int64_t s_end = imin64(p.L, s_begin + p.Ls);
+  const int nsl = (int)cdiv(s_end - s_begin, C);
+  const int kslot = qk_slot(p, h), vslot = v_slot(p, h);
+  const uint32_t tile_tx = (uint32_t)(ncbk + ncbv) * 8192;
+
+  if (warp == 0) tmem_alloc(&tmem_base, 256);
+  if (tid == 0) {
+    mbar_init(&bar_tma, 1);
+    mbar_init(&bar_mma, 1);
+    fence_mbar_init();
+    prefetch_tmap(&tmK);
+    prefetch_tmap(&tmV);
+  }
+  __syncthreads();
+  auto issue_tma = [&](int n) {
+    const int row = (int)(b * p.L + s_begin + (int64_t)n * C);
+    mbar_expect_tx(&bar_tma, tile_tx);
+    for (int cb = 0; cb < ncbk; ++cb) tma_load_3d(Xt + cb * 8192, &tmK, &bar_tma, cb * 32, kslot, row);
+    for (int cb = 0; cb < ncbv; ++cb) tma_load_3d(Yt + cb * 8192, &tmV, &bar_tma, cb * 32, vslot, row);
+  };
+  if (tid == 0) issue_tma(0);
+  if (warp == 0) {
+    double tot = 0.0;
+    for (int64_t t = s_begin; t < s_end; t += C)
+      tot += warp_cumsum64(la, (b * p.L + t) * p.H + h, p.H, (int)imin64(C, s_end - t), 0.0, nullptr);
+    if (lane == 0) seg_total = tot;
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base;
+  const uint32_t lb = (uint32_t)(warp * 32) << 16;
+  const float Af = (float)seg_total;
+  double carry = 0.0;
+  bool ok = true;
+  int tma_pending = 0;  // slice whose tiles are in flight (tid 0's view)
+
+  for (int n = 0; n < nsl; ++n) {
+    const int64_t t0 = s_begin + (int64_t)n * C;
+    const int len = (int)imin64(C, s_end - t0);
+    if (warp == 0) {
+      const double part = warp_cumsum64(la, (b * p.L + t0) * p.H + h, p.H, len, carry, cs);
+      __syncwarp();
+      for (int u = lane; u < C; u += 32) sc[u] = u < len ? expf(REV ? cs[u] : Af - cs[u]) : 0.f;
+      carry += part;
+    }
+    ok = mbar_wait(&bar_tma, n & 1) && ok;
+    if (n >= 1) ok = mbar_wait(&bar_mma, (n - 1) & 1) && ok;
+    if (tid == 0 && ok) tma_pending = -1;
+    if (__syncthreads_or(!ok)) break;
+    tc_fence_after();
+    const int buf = n & 1;
+    {  // A operand: k'^T, lane i = feature, 64 tokens
+      float v[32];
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+#pragma unroll
+        for (int uu = 0; uu < 32; ++uu) {
+          const int u = half * 32 + uu;
+          v[uu] = (tid < p.dk && u < len) ? tf32r(*(const float *)(Xt + sw128_off(u, tid, C))) : 0.f;
+        }
+        tmem_st32(tmem + lb + 128 + buf * 64 + half * 32, v);
+      }
+    }
+    if (tid < p.dvn) {  // B operand: (sc v')^T, row j = feature
+#pragma unroll 4
+      for (int u = 0; u < C; u += 4) {
+        float f[4];
+#pragma unroll
+        for (int r = 0; r < 4; ++r)
+          f[r] = tid < p.dv ? tf32r(*(const float *)(Yt + sw128_off(u + r, tid, C)) * sc[u + r]) : 0.f;
+        *reinterpret_cast<float4 *>(Bb + sw128_off(tid, u, p.dvn)) = make_float4(f[0], f[1], f[2], f[3]);
+      }
+    }
+    tmem_st_wait();
+    fence_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (tid == 0) {
+      if (n + 1 < nsl) {
+        issue_tma(n + 1);
+        tma_pending = n + 1;
+      }
+      const uint32_t bsm = smem_u32(Bb);
+      const uint32_t id = idesc_tf32(128, p.dvn);
+#pragma unroll
+      for (int kk = 0; kk < C / 8; ++kk)
+        mma_ts(tmem, tmem + 128 + buf * 64 + kk * 8,
+               sdesc(bsm + (kk >> 2) * (p.dvn * 128) + (kk & 3) * 32), id, (n > 0 || kk > 0) ? 1u : 0u);
+      mma_commit(&bar_mma);
+    }
+  }
+  if (ok) ok = mbar_wait(&bar_mma, (nsl - 1) & 1);
+  const bool fail = __syncthreads_or(!ok);
+  tc_fence_after();
+  if (!fail) {
+    float *dst = states + (bh * p.nseg + seg) * (int64_t)p.dk * p.dv;
+    for (int c0 = 0; c0 < p.dvn; c0 += 32) {
+      float v[32];
+      tmem_ld32(tmem + lb + c0, v);
+      if (tid < p.dk) {
+#pragma unroll
+        for (int jj = 0; jj < 32; ++jj)
+          if (c0 + jj < p.dv) dst[(int64_t)tid * p.dv + c0 + jj] = v[jj];
+      }
+    }
+    if (tid == 0) Aseg[bh * p.nseg + seg] = Af;
+  } else if (tid == 0 && tma_pending >= 0) {
+    mbar_wait(&bar_tma, tma_pending & 1);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tmem, 256);
+}
+
+// ===========================================================================
+// State passing over segments, in place (one thread per state element).
+//   causal:      st[s] <- state entering segment s from the left; the first is
+//                h0 (read transposed when TRANS_H0), or 0
+//   anti-causal: st[s] <- state entering segment s from the right (0 for the
+//                last); the state left of segment 0 goes to fin (if given)
+// grid (B*H, ceil(dk*dv / 128))
+template <bool REV, bool TRANS_H0>
+__global__ void __launch_bounds__(NTH) k_seg_scan(float *__restrict__ st,
+                                                  const float *__restrict__ Aseg,
+                                                  const float *__restrict__ h0,
+                                                  float *__restrict__ fin, PassGeo p) {
+  const int64_t bh = blockIdx.x;
+  const int64_t e = (int64_t)blockIdx.y * NTH + threadIdx.x;
+  const int64_t sz = (int64_t)p.dk * p.dv;
+  if (e >= sz) return;
+  float *q = st + bh * p.nseg * sz + e;
+  const float *a = Aseg + bh * p.nseg;
+  constexpr int U = 8;  // segments loaded ahead of the dependent chain
+  float run = 0.f;
+  if (!REV) {
+    if (h0) run = TRANS_H0 ? h0[bh * sz + (e % p.dv) * p.dk + e / p.dv] : h0[bh * sz + e];
+    for (int s0 = 0; s0 < p.nseg; s0 += U) {
+      float x[U], d[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u)
+        if (s0 + u < p.nseg) { x[u] = q[(int64_t)(s0 + u) * sz]; d[u] = expf(a[s0 + u]); }
+#pragma unroll
+      for (int u = 0; u < U; ++u)
+        if (s0 + u < p.nseg) { q[(int64_t)(s0 + u) * sz] = run; run = fmaf(d[u], run, x[u]); }
+    }
+  } else {
+    for (int s0 = p.nseg - 1; s0 >= 0; s0 -= U) {
+      float x[U], d[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u)
+        if (s0 - u >= 0) { x[u] = q[(int64_t)(s0 - u) * sz]; d[u] = expf(a[s0 - u]); }
+#pragma unroll
+      for (int u = 0; u < U; ++u)
+        if (s0 - u >= 0) { q[(int64_t)(s0 - u) * sz] = run; run = fmaf(d[u], run, x[u]); }
+    }
+    if (fin) fin[bh * sz + e] = run;
+  }
+}
+
+// ===========================================================================
+// Walk over the chunks of one segment (left to right, or right to left when
+// REV) with the running state resident in tensor memory.  grid (nseg, H, B),
+// 128 threads, two CTAs per SM.
+//
+// Tensor memory (256 columns):
+//   X   [0,64)    S = q' k'^T (M = 64: rows 16w..16w+15 in lanes 32w..), then
+//                 out'^T (lane j = feature, column = token)
+//   VT  [64,128)  v'^T of the chunk (A operand)
+//   HT  [128,256) running state, transposed (A operand): lane j, column i
+// Shared memory: q' tile (scaled in place to the B operand of the inter term),
+// k' tile (then reused for w * k'^T, the B operand of the state update), v'
+// tile (then reused for P).
+template <bool REV, bool ATOMIC>
+__global__ void __launch_bounds__(NTH) k_walk(const __grid_constant__ CUtensorMap tmQ,
+                                              const __grid_constant__ CUtensorMap tmK,
+                                              const __grid_constant__ CUtensorMap tmV,
+                                              const float *__restrict__ la,
+                                              const float *__restrict__ Hseg, OutArgs oa,
+                                              PassGeo p) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  const int ncbk = p.dkp / 32, ncbv = p.dvp / 32;
+  const uint32_t vbytes = (uint32_t)max(ncbv * 8192, 16384);
+  uint8_t *Qb = smem;
+  uint8_t *Kb = Qb + ncbk * 8192;
+  uint8_t *Vb = Kb + ncbk * 8192;
+  float *cs = (float *)(Vb + vbytes);
+  float *ew = cs + C, *ww = ew + C;
+  float *red = ww + C;  // [4][64]
+  __shared__ uint64_t bar_tma, bar_s, bar_i, bar_o, bar_h;
+  __shared__ uint32_t tmem_base;
+  __shared__ float a_chunk;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int64_t seg = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const int64_t bh = b * p.H + h;
+  const int64_t s_begin = seg * (int64_t)p.Ls;
+  const int64_t s_end = imin64(p.L, s_begin + p.Ls);
+  const int nc = (int)cdiv(s_end - s_begin, C);
+  const int kslot = qk_slot(p, h), vslot = v_slot(p, h);
+  const int dk = p.dk, dv = p.dv, dkn = p.dkn;
+  const uint32_t tile_tx = (uint32_t)(2 * ncbk + ncbv) * 8192;
+  const int oslot = oa.out_slots == p.H ? (int)h : (int)(h / p.hpg);
+
+  if (warp == 0) tmem_alloc(&tmem_base, 256);
+  if (tid == 0) {
+    mbar_init(&bar_tma, 1);
+    mbar_init(&bar_s, 1);
+    mbar_init(&bar_i, 1);
+    mbar_init(&bar_o, 1);
+    mbar_init(&bar_h, 1);
+    fence_mbar_init();
+    prefetch_tmap(&tmQ);
+    prefetch_tmap(&tmK);
+    prefetch_tmap(&tmV);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base;
+  const uint32_t lb = (uint32_t)(warp * 32) << 16;
+  int tma_pending = -1;
+  // load chunk c's tiles; `use` counts the barrier's phases (chunks in walk order)
+  auto issue_tma = [&](int c, int use) {
+    const int row = (int)(b * p.L + s_begin + (int64_t)c * C);
+    mbar_expect_tx(&bar_tma, tile_tx);
+    for (int cb = 0; cb < ncbk; ++cb) {
+      tma_load_3d(Qb + cb * 8192, &tmQ, &bar_tma, cb * 32, kslot, row);
+      tma_load_3d(Kb + cb * 8192, &tmK, &bar_tma, cb * 32, kslot, row);
+    }
+    for (int cb = 0; cb < ncbv; ++cb) tma_load_3d(Vb + cb * 8192, &tmV, &bar_tma, cb * 32, vslot, row);
+    tma_pending = use;
+  };
+  if (tid == 0) issue_tma(REV ? nc - 1 : 0, 0);
+
+  {  // running state, transposed: lane j, column i = state[i][j]
+    const float *H0 = Hseg + (bh * p.nseg + seg) * (int64_t)dk * dv;
+    for (int c0 = 0; c0 < rup(dk, 32); c0 += 32) {
+      float hv[32];
+#pragma unroll
+      for (int ii = 0; ii < 32; ++ii) {
+        const int i = c0 + ii;
+        hv[ii] = (tid < dv && i < dk) ? H0[(int64_t)i * dv + tid] : 0.f;
+      }
+      tmem_st32(tmem + lb + 128 + c0, hv);
+    }
+    tmem_st_wait();
+  }
+
+  bool ok = true;
+  for (int ci = 0; ci < nc; ++ci) {
+    const int c = REV ? nc - 1 - ci : ci;
+    const int64_t t0 = s_begin + (int64_t)c * C;
+    const int len = (int)imin64(C, s_end - t0);
+    if (warp == 0) {
+      const double tot = warp_cumsum64(la, (b * p.L + t0) * p.H + h, p.H, len, 0.0, cs);
+      __syncwarp();
+      const float tf = (float)tot;
+      for (int t = lane; t < C; t += 32) {
+        ew[t] = t < len ? expf(cs[t]) : 0.f;
+        ww[t] = t < len ? expf(tf - cs[t]) : 0.f;
+      }
+      if (lane == 0) a_chunk = expf(tf);
+    }
+    ok = mbar_wait(&bar_tma, ci & 1) && ok;
+    if (tid == 0 && ok) tma_pending = -1;
+    tc_fence_before();
+    if (__syncthreads_or(!ok)) break;
+    tc_fence_after();
+    // inter-term factor of a query row, state-update weight of a key column
+    const float *interf = REV ? ww : ew;
+    const float *statew = REV ? ew : ww;
+    {  // round the TMA-fed q' and k' tiles to TF32 (nearest) in place: the
+       // tensor core would otherwise truncate them
+      const int r = tid & 63, half = tid >> 6;
+      const int cols = p.dkp / 2;
+      for (int col = half * cols; col < (half + 1) * cols; col += 4) {
+        float4 *q4 = reinterpret_cast<float4 *>(Qb + sw128_off(r, col, C));
+        float4 *k4 = reinterpret_cast<float4 *>(Kb + sw128_off(r, col, C));
+        float4 a = *q4, bb = *k4;
+        a.x = tf32r(a.x); a.y = tf32r(a.y); a.z = tf32r(a.z); a.w = tf32r(a.w);
+        bb.x = tf32r(bb.x); bb.y = tf32r(bb.y); bb.z = tf32r(bb.z); bb.w = tf32r(bb.w);
+        *q4 = a;
+        *k4 = bb;
+      }
+      fence_async_smem();
+      __syncthreads();
+    }
+    if (tid == 0) {  // S = q' k'^T (M = 64, N = 64, K = dk)
+      const uint32_t qa = smem_u32(Qb), ka = smem_u32(Kb);
+      const uint32_t id = idesc_tf32(64, 64);
+      for (int kk = 0; kk < dk / 8; ++kk) {
+        const uint32_t off = (kk >> 2) * 8192 + (kk & 3) * 32;
+        mma_ss(tmem, sdesc(qa + off), sdesc(ka + off), id, kk > 0 ? 1u : 0u);
+      }
+      mma_commit(&bar_s);
+    }
+    {  // v'^T into tensor memory
+      float v[32];
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+#pragma unroll
+        for (int uu = 0; uu < 32; ++uu) {
+          const int u = half * 32 + uu;
+          v[uu] = (tid < dv && u < len) ? tf32r(*(const float *)(Vb + sw128_off(u, tid, C))) : 0.f;
+        }
+        tmem_st32(tmem + lb + 64 + half * 32, v);
+      }
+    }
+    float kw[C];  // w_u * k'[u][i], i = tid
+#pragma unroll
+    for (int u = 0; u < C; ++u)
+      kw[u] = (tid < dk) ? tf32r(*(const float *)(Kb + sw128_off(u, tid, C)) * statew[u]) : 0.f;
+    ok = mbar_wait(&bar_s, ci & 1) && ok;
+    tc_fence_after();
+    float sr[C];
+    {
+      float t32[32];
+      tmem_ld32(tmem + lb, t32);
+#pragma unroll
+      for (int u = 0; u < 32; ++u) sr[u] = t32[u];
+      tmem_ld32(tmem + lb + 32, t32);
+#pragma unroll
+      for (int u = 0; u < 32; ++u) sr[32 + u] = t32[u];
+    }
+    tc_fence_before();
+    __syncthreads();  // every read of the v' and k' tiles and of S is done
+    if (lane < 16) {  // P into the v' tile's space: rows r = 16w + lane
+      const int r = warp * 16 + lane;
+      const float cr = cs[r < len ? r : 0];
+      uint8_t *P = Vb;
+#pragma unroll
+      for (int u = 0; u < C; u += 4) {
+        float f[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int uu = u + e;
+          const bool valid = r < len && uu < len && (REV ? uu >= r : uu <= r);
+          f[e] = valid ? tf32r(expf(REV ? cs[uu] - cr : cr - cs[uu]) * sr[uu]) : 0.f;
+        }
+        *reinterpret_cast<float4 *>(P + sw128_off(r, u, C)) = make_float4(f[0], f[1], f[2], f[3]);
+      }
+    }
+    if (tid < dkn) {  // w * k'^T into the k' tile's space (B operand, dkn rows)
+#pragma unroll
+      for (int u = 0; u < C; u += 4)
+        *reinterpret_cast<float4 *>(Kb + sw128_off(tid, u, dkn)) =
+            make_float4(kw[u], kw[u + 1], kw[u + 2], kw[u + 3]);
+    }
+    {  // q' rows scaled by the inter-term factor, in place
+      const int r = tid & 63, half = tid >> 6;
+      const float e = interf[r];
+      const int cols = p.dkp / 2;
+      for (int col = half * cols; col < (half + 1) * cols; col += 4) {
+        float4 *q4 = reinterpret_cast<float4 *>(Qb + sw128_off(r, col, C));
+        float4 f = *q4;
+        f.x = tf32r(f.x * e); f.y = tf32r(f.y * e); f.z = tf32r(f.z * e); f.w = tf32r(f.w * e);
+        *q4 = f;
+      }
+    }
+    tmem_st_wait();
+    fence_async_smem();
+    tc_fence_before();
+    if (__syncthreads_or(!ok)) break;
+    tc_fence_after();
+    const bool split = oa.dcs != nullptr;
+    if (tid == 0) {  // out'^T = HT (f q')^T  [+ v'^T P^T]
+      const uint32_t qa = smem_u32(Qb), pa = smem_u32(Vb);
+      const uint32_t id = idesc_tf32(128, 64);
+      for (int kk = 0; kk < dk / 8; ++kk)
+        mma_ts(tmem, tmem + 128 + kk * 8, sdesc(qa + (kk >> 2) * 8192 + (kk & 3) * 32), id,
+               kk > 0 ? 1u : 0u);
+      if (split) mma_commit(&bar_i);
+#pragma unroll
+      for (int kk = 0; kk < C / 8; ++kk)
+        if (!split) mma_ts(tmem, tmem + 64 + kk * 8, sdesc(pa + (kk >> 2) * 8192 + (kk & 3) * 32), id, 1u);
+      if (!split) mma_commit(&bar_o);
+    }
+    if (split) {
+      // r[t] = y_t . (inter-chunk part of out'_t), reduced over the 128 lanes
+      ok = mbar_wait(&bar_i, ci & 1) && ok;
+      tc_fence_after();
+      float o[C];
+      {
+        float t32[32];
+        tmem_ld32(tmem + lb, t32);
+#pragma unroll
+        for (int t = 0; t < 32; ++t) o[t] = t32[t];
+        tmem_ld32(tmem + lb + 32, t32);
+#pragma unroll
+        for (int t = 0; t < 32; ++t) o[32 + t] = t32[t];
+      }
+      const int64_t ldy = (int64_t)(p.H / p.hpg) * dv;
+      const float *ys = oa.y + ((b * p.L + t0) * (p.H / p.hpg) + h / p.hpg) * (int64_t)dv + tid;
+#pragma unroll
+      for (int t = 0; t < C; ++t) o[t] = (tid < dv && t < len) ? o[t] * ys[t * ldy] : 0.f;
+#pragma unroll
+      for (int off = 16, n = C; off >= 1; off >>= 1, n >>= 1) {
+        const bool up = (lane & off) != 0;
+#pragma unroll
+        for (int k2 = 0; k2 < n / 2; ++k2) {
+          const float mine = up ? o[n / 2 + k2] : o[k2];
+          const float send = up ? o[k2] : o[n / 2 + k2];
+          o[k2] = mine + __shfl_xor_sync(0xffffffffu, send, off);
+        }
+      }
+      red[warp * C + 2 * lane] = o[0];
+      red[warp * C + 2 * lane + 1] = o[1];
+      tc_fence_before();
+      __syncthreads();
+      tc_fence_after();
+      if (tid < len)
+        oa.dcs[(b * p.L + t0 + tid) * p.H + h] = red[tid] + red[C + tid] + red[2 * C + tid] + red[3 * C + tid];
+      if (tid == 0) {  // + v'^T P^T
+        const uint32_t pa = smem_u32(Vb);
+        const uint32_t id = idesc_tf32(128, 64);
+#pragma unroll
+        for (int kk = 0; kk < C / 8; ++kk)
+          mma_ts(tmem, tmem + 64 + kk * 8, sdesc(pa + (kk >> 2) * 8192 + (kk & 3) * 32), id, 1u);
+        mma_commit(&bar_o);
+      }
+    }
+    ok = mbar_wait(&bar_o, ci & 1) && ok;
+    tc_fence_after();
+    {
+      float o[C];
+      {
+        float t32[32];
+        tmem_ld32(tmem + lb, t32);
+#pragma unroll
+        for (int t = 0; t < 32; ++t) o[t] = t32[t];
+        tmem_ld32(tmem + lb + 32, t32);
+#pragma unroll
+        for (int t = 0; t < 32; ++t) o[32 + t] = t32[t];
+      }
+      if (tid < dv) {
+        const int64_t ld = (int64_t)oa.out_slots * dv;
+        float *os = oa.out + ((b * p.L + t0) * oa.out_slots + oslot) * (int64_t)dv + tid;
+#pragma unroll
+        for (int t = 0; t < C; ++t) {
+          if (t < len) {
+            if (ATOMIC) atomicAdd(os + t * ld, o[t]);
+            else os[t * ld] = o[t];
+          }
+        }
+      }
+    }
+    {  // HT <- exp(A_c) HT, before the state-update MMA accumulates into it
+      const float a = a_chunk;
+      for (int c0 = 0; c0 < rup(dk, 32); c0 += 32) {
+        float hv[32];
+        tmem_ld32(tmem + lb + 128 + c0, hv);
+#pragma unroll
+        for (int ii = 0; ii < 32; ++ii) hv[ii] *= a;
+        tmem_st32(tmem + lb + 128 + c0, hv);
+      }
+      tmem_st_wait();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (tid == 0) {  // HT += v'^T (w k')   (M = dv lanes, N = dkn, K = 64 tokens)
+      const uint32_t kwa = smem_u32(Kb);
+      const uint32_t id = idesc_tf32(128, dkn);
+#pragma unroll
+      for (int kk = 0; kk < C / 8; ++kk)
+        mma_ts(tmem + 128, tmem + 64 + kk * 8, sdesc(kwa + (kk >> 2) * (dkn * 128) + (kk & 3) * 32),
+               id, 1u);
+      mma_commit(&bar_h);
+    }
+    ok = mbar_wait(&bar_h, ci & 1) && ok;
+    tc_fence_after();
+    if (tid == 0 && ok && ci + 1 < nc) issue_tma(REV ? c - 1 : c + 1, ci + 1);
+    tc_fence_before();
+    if (__syncthreads_or(!ok)) break;  // also orders the dcs reads of red before reuse
+    tc_fence_after();
+  }
+  __syncthreads();
+  if (tid == 0 && tma_pending >= 0) mbar_wait(&bar_tma, tma_pending & 1);
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tmem, 256);
+}
+
+// ===========================================================================
+// Intra-chunk part of dlog_alpha, per (chunk, head):
+//   B_t = sum_{t' >= t, s < t, both in the chunk} exp(cs_t' - cs_s) (q_t'.k_s)(dout_t'.v_s)
+// (the lower-left block of M = D o (q k^T) o (dout v^T) below row t, left of
+// column t).  Two score MMAs (M = 64) share one 2-tile shared-memory buffer.
+// grid (N chunks, H, B), 128 threads.
+__global__ void __launch_bounds__(NTH) k_dla_intra(const __grid_constant__ CUtensorMap tmQ,
+                                                   const __grid_constant__ CUtensorMap tmK,
+                                                   const __grid_constant__ CUtensorMap tmV,
+                                                   const __grid_constant__ CUtensorMap tmD,
+                                                   const float *__restrict__ la,
+                                                   float *__restrict__ Bt, PassGeo p) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  const int dk = p.dk, dv = p.dv;  // here dk = q/k features, dv = v/dout features
+  const int ncbk = p.dkp / 32, ncbv = p.dvp / 32, ncbm = ncbk > ncbv ? ncbk : ncbv;
+  uint8_t *T1 = smem, *T2 = smem + ncbm * 8192;
+  float *R = (float *)(T2 + ncbm * 8192);  // [64][65]
+  float *cs = R + C * (C + 1);
+  __shared__ uint64_t bar_tma, bar_mma;
+  __shared__ uint32_t tmem_base;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int64_t c = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const int64_t t0 = c * C;
+  const int len = (int)imin64(C, p.L - t0);
+  const int grp = (int)(h / p.hpg);
+  const int row = (int)(b * p.L + t0);
+
+  if (warp == 0) tmem_alloc(&tmem_base, 128);
+  if (tid == 0) {
+    mbar_init(&bar_tma, 1);
+    mbar_init(&bar_mma, 1);
+    fence_mbar_init();
+    mbar_expect_tx(&bar_tma, (uint32_t)(2 * ncbk) * 8192);
+    for (int cb = 0; cb < ncbk; ++cb) {
+      tma_load_3d(T1 + cb * 8192, &tmQ, &bar_tma, cb * 32, grp, row);
+      tma_load_3d(T2 + cb * 8192, &tmK, &bar_tma, cb * 32, grp, row);
+    }
+  }
+  if (warp == 0) warp_cumsum64(la, (b * p.L + t0) * p.H + h, p.H, len, 0.0, cs);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base;
+  const uint32_t lb = (uint32_t)(warp * 32) << 16;
+  bool ok = true;
+  for (int phase = 0; phase < 2; ++phase) {
+    const int ncb = phase == 0 ? ncbk : ncbv;
+    const int kdim = phase == 0 ? dk : dv;
+    ok = mbar_wait(&bar_tma, phase) && ok;
+    if (__syncthreads_or(!ok)) break;
+    {  // round both tiles to TF32 (nearest) in place
+      const int r = tid & 63, half = tid >> 6;
+      const int cols = ncb * 16;
+      for (int col = half * cols; col < (half + 1) * cols; col += 4) {
+        float4 *a4 = reinterpret_cast<float4 *>(T1 + sw128_off(r, col, C));
+        float4 *b4 = reinterpret_cast<float4 *>(T2 + sw128_off(r, col, C));
+        float4 x = *a4, y = *b4;
+        x.x = tf32r(x.x); x.y = tf32r(x.y); x.z = tf32r(x.z); x.w = tf32r(x.w);
+        y.x = tf32r(y.x); y.y = tf32r(y.y); y.z = tf32r(y.z); y.w = tf32r(y.w);
+        *a4 = x;
+        *b4 = y;
+      }
+    }
+    fence_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (tid == 0) {  // phase 0: q k^T -> cols [0,64); phase 1: dout v^T -> [64,128)
+      const uint32_t a = smem_u32(T1), bb = smem_u32(T2);
+      const uint32_t id = idesc_tf32(64, 64);
+      for (int kk = 0; kk < kdim / 8; ++kk) {
+        const uint32_t off = (kk >> 2) * 8192 + (kk & 3) * 32;
+        mma_ss(tmem + phase * 64, sdesc(a + off), sdesc(bb + off), id, kk > 0 ? 1u : 0u);
+      }
+      mma_commit(&bar_mma);
+    }
+    ok = mbar_wait(&bar_mma, phase) && ok;
+    tc_fence_after();
+    if (phase == 0 && tid == 0 && ok) {  // the tiles are free: load dout and v
+      mbar_expect_tx(&bar_tma, (uint32_t)(2 * ncbv) * 8192);
+      for (int cb = 0; cb < ncbv; ++cb) {
+        tma_load_3d(T1 + cb * 8192, &tmD, &bar_tma, cb * 32, (int)h, row);
+        tma_load_3d(T2 + cb * 8192, &tmV, &bar_tma, cb * 32, (int)h, row);
+      }
+    }
+  }
+  if (__syncthreads_or(!ok) == 0) {
+    float sq[C], dp[C];
+    {
+      float t32[32];
+      tmem_ld32(tmem + lb, t32);
+#pragma unroll
+      for (int u = 0; u < 32; ++u) sq[u] = t32[u];
+      tmem_ld32(tmem + lb + 32, t32);
+#pragma unroll
+      for (int u = 0; u < 32; ++u) sq[32 + u] = t32[u];
+      tmem_ld32(tmem + lb + 64, t32);
+#pragma unroll
+      for (int u = 0; u < 32; ++u) dp[u] = t32[u];
+      tmem_ld32(tmem + lb + 96, t32);
+#pragma unroll
+      for (int u = 0; u < 32; ++u) dp[32 + u] = t32[u];
+    }
+    if (lane < 16) {  // row r: prefix sums R[r][t] = sum_{u < t} M[r][u]
+      const int r = warp * 16 + lane;
+      const float cr = cs[r < len ? r : 0];
+      float acc = 0.f;
+      R[r * (C + 1)] = 0.f;
+#pragma unroll
+      for (int u = 0; u < C; ++u) {
+        const float m = (r < len && u <= r) ? expf(cr - cs[u]) * sq[u] * dp[u] : 0.f;
+        acc += m;
+        R[r * (C + 1) + u + 1] = acc;
+      }
+    }
+    __syncthreads();
+    if (tid < len) {
+      float bsum = 0.f;
+      for (int r = tid; r < len; ++r) bsum += R[r * (C + 1) + tid];
+      Bt[(b * p.L + t0 + tid) * p.H + h] = bsum;
+    }
+  } else if (tid == 0) {
+    mbar_wait(&bar_tma, 1);  // a load may still be in flight
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tmem, 128);
+}
+
+// ===========================================================================
+// dlog_alpha of one segment:
+//   dla_t = B_t + sum_{t' >= t in the segment} (rq_t' - rk_t') + <G_end, S_end>
+// where B_t is the intra-chunk block sum, rq / rk the inter-chunk terms
+// q_t.dq_inter(t) and k_t.dk_inter(t), G_end the gradient of the state at the
+// segment's end (from its right) and S_end that state (the state entering the
+// next segment, given transposed [dv x dk]).  grid (nseg, H, B).
+constexpr int DT = 256;
+__global__ void __launch_bounds__(DT) k_dla(const float *__restrict__ Bt,
+                                            const float *__restrict__ rq,
+                                            const float *__restrict__ rk,
+                                            const float *__restrict__ Gst,
+                                            const float *__restrict__ StT, float *__restrict__ dla,
+                                            int64_t L, int64_t H, int dk, int dv, int Ls, int nseg) {
+  __shared__ double sh[DT];
+  __shared__ double carry_in;
+  const int tid = threadIdx.x;
+  const int64_t seg = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const int64_t bh = b * H + h;
+  const int64_t sz = (int64_t)dk * dv;
+  double acc = 0.0;
+  if (seg + 1 < nseg) {
+    const float *G = Gst + (bh * nseg + seg) * sz;
+    const float *S = StT + (bh * nseg + seg + 1) * sz;
+    for (int64_t e = tid; e < sz; e += DT) {
+      const int64_t i = e / dv, j = e % dv;
+      acc += (double)G[e] * (double)S[j * dk + i];
+    }
+  }
+  sh[tid] = acc;
+  __syncthreads();
+  for (int o = DT / 2; o > 0; o >>= 1) {
+    if (tid < o) sh[tid] += sh[tid + o];
+    __syncthreads();
+  }
+  if (tid == 0) carry_in = sh[0];
+  __syncthreads();
+  const int64_t s_begin = seg * (int64_t)Ls;
+  const int64_t s_end = imin64(L, s_begin + Ls);
+  for (int64_t hi = s_end; hi > s_begin; hi -= DT) {
+    const int64_t lo = hi - DT > s_begin ? hi - DT : s_begin;
+    const int64_t t = lo + tid;
+    double x = 0.0;
+    if (t < hi) x = (double)rq[(b * L + t) * H + h] - (double)rk[(b * L + t) * H + h];
+    __syncthreads();
+    sh[tid] = x;
+    __syncthreads();
+    for (int o = 1; o < DT; o <<= 1) {  // inclusive suffix sums
+      const double y = (tid + o < DT) ? sh[tid + o] : 0.0;
+      __syncthreads();
+      sh[tid] += y;
+      __syncthreads();
+    }
+    if (t < hi) dla[(b * L + t) * H + h] = (float)((double)Bt[(b * L + t) * H + h] + sh[tid] + carry_in);
+    __syncthreads();
+    if (tid == 0) carry_in += sh[0];
+    __syncthreads();
+  }
+}
+
+// ===========================================================================
+// Host side.
+
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+cudaError_t get_encoder() {
+  std::call_once(g_encode_once, [] {
+    cudaDriverEntryPointQueryResult q;
+    void *fn = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                        cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  return g_encode ? cudaSuccess : cudaErrorNotSupported;
+}
+
+// 3-D view [rows, slots, d] of a row-major fp32 tensor; box = 32 features x
+// 1 slot x 64 rows, 128-byte swizzle, zero fill out of bounds.
+cudaError_t make_map(CUtensorMap *m, const float *base, int64_t rows, int64_t slots, int64_t d) {
+  cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)slots, (cuuint64_t)rows};
+  cuuint64_t strides[2] = {(cuuint64_t)(d * 4), (cuuint64_t)(slots * d * 4)};
+  cuuint32_t box[3] = {32, 1, (cuuint32_t)C};
+  cuuint32_t es[3] = {1, 1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float *>(base), dims,
+                        strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+int num_sms() {
+  static int cache[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) return 148;
+  if (!cache[dev]) {
+    int n = 0;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    cache[dev] = n > 0 ? n : 148;
+  }
+  return cache[dev];
+}
+
+// Segment length: enough segments for about four CTAs per SM in flight.
+void choose_segments(const Geo &g, int *Ls, int *nseg) {
+  const int64_t bh = g.B * g.H;
+  const int64_t want = std::max<int64_t>(1, (4 * (int64_t)num_sms() + bh - 1) / bh);
+  int64_t ls = cdiv(cdiv(g.L, want), C) * C;
+  if (ls < C) ls = C;
+  *Ls = (int)std::min<int64_t>(ls, 1 << 30);
+  *nseg = (int)cdiv(g.L, *Ls);
+}
+
+PassGeo make_pass(const Geo &g, int dk, int dv, bool qk_head, bool v_head) {
+  PassGeo p;
+  p.B = g.B; p.L = g.L; p.H = g.H; p.hpg = g.hpg;
+  p.dk = dk; p.dv = dv;
+  p.dkp = rup(dk, 32); p.dkn = rup(dk, 16);
+  p.dvp = rup(dv, 32); p.dvn = rup(dv, 16);
+  p.qk_per_head = qk_head ? 1 : 0;
+  p.v_per_head = v_head ? 1 : 0;
+  choose_segments(g, &p.Ls, &p.nseg);
+  return p;
+}
+
+size_t state_floats(const PassGeo &p) {
+  return (size_t)(p.B * p.H * p.nseg) * (size_t)p.dk * p.dv;
+}
+
+size_t seg_state_smem(const PassGeo &p) {
+  return (size_t)(p.dkp / 32 + p.dvp / 32) * 8192 + (size_t)p.dvn * 256 + 2 * C * 4 + 1024;
+}
+size_t walk_smem(const PassGeo &p) {
+  return (size_t)(p.dkp / 32) * 2 * 8192 + std::max(p.dvp / 32 * 8192, 16384) + 7 * C * 4 + 1024;
+}
+
+size_t dla_intra_smem(const PassGeo &p) {
+  const int ncbm = std::max(p.dkp, p.dvp) / 32;
+  return (size_t)ncbm * 2 * 8192 + (size_t)(C * (C + 1) + C) * 4 + 1024;
+}
+
+template <typename K>
+cudaError_t set_smem(K kern, size_t bytes) {
+  return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+}
+
+// One scan pass: segment contributions, state passing, then the walk.
+//   q', k' : [B*L, qk_slots, dk]   v' : [B*L, v_slots, dv]
+template <bool REV>
+cudaError_t run_pass(const PassGeo &p, const float *qp, const float *kp, const float *vp,
+                     const float *la, const float *h0, bool trans_h0, float *fin, float *states,
+                     float *Aseg, const OutArgs &oa, bool atomic, cudaStream_t s,
+                     const char *name_state, const char *name_walk) {
+  cudaError_t e;
+  const int64_t rows = p.B * p.L;
+  const int64_t G = p.H / p.hpg;
+  CUtensorMap mq, mk, mv;
+  if ((e = make_map(&mq, qp, rows, p.qk_per_head ? p.H : G, p.dk)) != cudaSuccess) return e;
+  if ((e = make_map(&mk, kp, rows, p.qk_per_head ? p.H : G, p.dk)) != cudaSuccess) return e;
+  if ((e = make_map(&mv, vp, rows, p.v_per_head ? p.H : G, p.dv)) != cudaSuccess) return e;
+  const dim3 grid((unsigned)p.nseg, (unsigned)p.H, (unsigned)p.B);
+  {
+    const size_t sm = seg_state_smem(p);
+    if ((e = set_smem(k_seg_state<REV>, sm)) != cudaSuccess) return e;
+    LaunchTrace lt(name_state, s);
+    k_seg_state<REV><<<grid, NTH, sm, s>>>(mk, mv, la, states, Aseg, p);
+  }
+  {
+    LaunchTrace lt("tc.seg_scan", s);
+    const dim3 sg((unsigned)(p.B * p.H), (unsigned)cdiv((int64_t)p.dk * p.dv, NTH));
+    if (trans_h0) k_seg_scan<REV, true><<<sg, NTH, 0, s>>>(states, Aseg, h0, fin, p);
+    else k_seg_scan<REV, false><<<sg, NTH, 0, s>>>(states, Aseg, h0, fin, p);
+  }
+  {
+    const size_t sm = walk_smem(p);
+    LaunchTrace lt(name_walk, s);
+    if (atomic) {
+      if ((e = set_smem(k_walk<REV, true>, sm)) != cudaSuccess) return e;
+      k_walk<REV, true><<<grid, NTH, sm, s>>>(mq, mk, mv, la, states, oa, p);
+    } else {
+      if ((e = set_smem(k_walk<REV, false>, sm)) != cudaSuccess) return e;
+      k_walk<REV, false><<<grid, NTH, sm, s>>>(mq, mk, mv, la, states, oa, p);
+    }
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace
 
 int check_shape(int64_t dk, int64_t dv, int64_t chunk) {
-  if (chunk != 64) return SSD_ERR_CHUNK;
+  if (chunk != C) return SSD_ERR_CHUNK;
   if (dk % 8 || dv % 8 || dk > 128 || dv > 128) return SSD_ERR_UNSUPPORTED;
   return SSD_OK;
 }
-size_t fwd_workspace_bytes(const Geo &) { return 0; }
-size_t bwd_workspace_bytes(const Geo &) { return 0; }
 
-cudaError_t fwd(const float *, const float *, const float *, const float *, const float *,
-                float *, const Geo &, void *, cudaStream_t) {
-  return cudaErrorNotSupported;
+size_t fwd_workspace_bytes(const Geo &g) {
+  const PassGeo p = make_pass(g, (int)g.dk, (int)g.dv, false, true);
+  return sizeof(float) * (state_floats(p) + (size_t)(g.B * g.H * p.nseg));
 }
-cudaError_t bwd(const float *, const float *, const float *, const float *, const float *,
-                const float *, float *, float *, float *, float *, float *, const Geo &, void *,
-                cudaStream_t) {
-  return cudaErrorNotSupported;
+
+// Three passes' states (two kept for dlog_alpha) + decays + two dcs arrays.
+size_t bwd_workspace_bytes(const Geo &g) {
+  const PassGeo p = make_pass(g, (int)g.dk, (int)g.dv, false, true);
+  const size_t nst = state_floats(p), na = (size_t)(g.B * g.H * p.nseg);
+  return sizeof(float) * (3 * nst + 3 * na + 3 * (size_t)(g.B * g.L * g.H)) + 256;
+}
+
+cudaError_t fwd(const float *q, const float *k, const float *v, const float *la, const float *h0,
+                float *out, const Geo &g, void *ws, cudaStream_t s) {
+  cudaError_t e = get_encoder();
+  if (e != cudaSuccess) return e;
+  if (g.B * g.L >= (int64_t)1 << 31) return cudaErrorNotSupported;
+  const PassGeo p = make_pass(g, (int)g.dk, (int)g.dv, false, true);
+  float *st = static_cast<float *>(ws);
+  float *Aseg = st + state_floats(p);
+  OutArgs oa{out, (int)g.H, nullptr, nullptr};
+  return run_pass<false>(p, q, k, v, la, h0, false, nullptr, st, Aseg, oa, false, s,
+                         "tc.seg_state", "tc.walk_out");
+}
+
+cudaError_t bwd(const float *q, const float *k, const float *v, const float *la, const float *h0,
+                const float *dout, float *dq, float *dk, float *dv, float *dla, float *dh0,
+                const Geo &g, void *ws, cudaStream_t s) {
+  cudaError_t e = get_encoder();
+  if (e != cudaSuccess) return e;
+  if (g.B * g.L >= (int64_t)1 << 31) return cudaErrorNotSupported;
+  const int DK = (int)g.dk, DV = (int)g.dv;
+  // dq_h = scan(q' = dout, k' = v, v' = k; causal; initial state h0^T)
+  const PassGeo pa = make_pass(g, DV, DK, true, false);
+  // dk_h = anti-causal scan(q' = v, k' = dout, v' = q)
+  const PassGeo pb = make_pass(g, DV, DK, true, false);
+  // dv = anti-causal scan(q' = k, k' = q, v' = dout); its leftmost state is dh0
+  const PassGeo pc = make_pass(g, DK, DV, false, true);
+  const size_t nst = state_floats(pa), na = (size_t)(g.B * g.H * pa.nseg);
+  float *stA = static_cast<float *>(ws);
+  float *stB = stA + nst;
+  float *stC = stB + nst;
+  float *aA = stC + nst;
+  float *aB = aA + na;
+  float *aC = aB + na;
+  float *dcsq = aC + na;
+  float *dcsk = dcsq + g.B * g.L * g.H;
+  float *Bt = dcsk + g.B * g.L * g.H;
+  const bool grouped = g.hpg > 1;
+  if (grouped) {
+    if ((e = cudaMemsetAsync(dq, 0, sizeof(float) * g.B * g.L * g.G * g.dk, s)) != cudaSuccess) return e;
+    if ((e = cudaMemsetAsync(dk, 0, sizeof(float) * g.B * g.L * g.G * g.dk, s)) != cudaSuccess) return e;
+  }
+  const int oslots = grouped ? (int)g.G : (int)g.H;
+  OutArgs oq{dq, oslots, q, dcsq};
+  if ((e = run_pass<false>(pa, dout, v, k, la, h0, true, nullptr, stA, aA, oq, grouped, s,
+                           "tc.seg_state_dq", "tc.walk_dq")) != cudaSuccess)
+    return e;
+  OutArgs okk{dk, oslots, k, dcsk};
+  if ((e = run_pass<true>(pb, v, dout, q, la, nullptr, false, nullptr, stB, aB, okk, grouped, s,
+                          "tc.seg_state_dk", "tc.walk_dk")) != cudaSuccess)
+    return e;
+  OutArgs ov{dv, (int)g.H, nullptr, nullptr};
+  if ((e = run_pass<true>(pc, k, q, dout, la, nullptr, false, dh0, stC, aC, ov, false, s,
+                          "tc.seg_state_dv", "tc.walk_dv")) != cudaSuccess)
+    return e;
+  {  // intra-chunk block sums of dlog_alpha
+    const PassGeo pi = make_pass(g, DK, DV, false, true);
+    CUtensorMap mq, mk, mv, md;
+    const int64_t rows = g.B * g.L;
+    if ((e = make_map(&mq, q, rows, g.G, DK)) != cudaSuccess) return e;
+    if ((e = make_map(&mk, k, rows, g.G, DK)) != cudaSuccess) return e;
+    if ((e = make_map(&mv, v, rows, g.H, DV)) != cudaSuccess) return e;
+    if ((e = make_map(&md, dout, rows, g.H, DV)) != cudaSuccess) return e;
+    const size_t sm = dla_intra_smem(pi);
+    if ((e = set_smem(k_dla_intra, sm)) != cudaSuccess) return e;
+    LaunchTrace lt("tc.dla_intra", s);
+    k_dla_intra<<<dim3((unsigned)g.N, (unsigned)g.H, (unsigned)g.B), NTH, sm, s>>>(mq, mk, mv, md,
+                                                                                  la, Bt, pi);
+  }
+  {
+    LaunchTrace lt("tc.dla", s);
+    k_dla<<<dim3((unsigned)pa.nseg, (unsigned)g.H, (unsigned)g.B), DT, 0, s>>>(
+        Bt, dcsq, dcsk, stC, stA, dla, g.L, g.H, DK, DV, pa.Ls, pa.nseg);
+  }
+  return cudaGetLastError();
 }
 
 cudaError_t read_and_clear_error(unsigned int *word) {
