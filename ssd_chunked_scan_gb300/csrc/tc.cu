@@ -44,9 +44,17 @@ namespace tc {
 
 constexpr int C = 64;     // chunk length of the tensor-core path
 constexpr int NTH = 128;  // threads per CTA: one per tensor-memory lane
+constexpr int NT2 = 256;  // two threads per tensor-memory lane (column halves)
 
 __host__ __device__ constexpr int rup(int x, int m) { return (x + m - 1) / m * m; }
 __host__ __device__ inline int64_t imin64(int64_t a, int64_t b) { return a < b ? a : b; }
+
+// 2^x, hardware approximation (relative error ~2^-22)
+__device__ __forceinline__ float ex2f(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
 
 // Inclusive prefix sums of la over n <= 64 tokens starting at `first` (fp64
 // accumulation by warp 0, rounded once to fp32), plus `carry` added before
@@ -106,29 +114,31 @@ __device__ __forceinline__ int v_slot(const PassGeo &p, int64_t h) {
 //   causal      D = sum_u exp(A_seg - cs_u) k'_u v'_u^T   (evaluated at its end)
 //   anti-causal D = sum_u exp(cs_u) k'_u v'_u^T           (evaluated at its start)
 // with cs the in-segment inclusive prefix of la and A_seg its total (also
-// written).  grid (nseg, H, B), 128 threads.
+// written).  grid (nseg, H, B), 256 threads: thread (quarter q, lane l, half f)
+// owns tensor-memory lane 32q + l and token half f of each 64-token slice.
 // Tensor memory (256 columns): D [0,128), A operand k'^T double-buffered at
 // [128,192) / [192,256).  Shared memory: k' and v' tiles (TMA), and the B
 // operand (sc * v')^T [dvn x 64], K-major.
 template <bool REV>
-__global__ void __launch_bounds__(NTH) k_seg_state(const __grid_constant__ CUtensorMap tmK,
+__global__ void __launch_bounds__(NT2, 2) k_seg_state(const __grid_constant__ CUtensorMap tmK,
                                                    const __grid_constant__ CUtensorMap tmV,
                                                    const float *__restrict__ la,
                                                    float *__restrict__ states,
                                                    float *__restrict__ Aseg, PassGeo p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
-  uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  uint8_t *smem = smem_align1024(smem_raw);
   const int ncbk = p.dkp / 32, ncbv = p.dvp / 32;
   uint8_t *Xt = smem;                       // k' tile [64 x dkp]
   uint8_t *Yt = Xt + ncbk * 8192;           // v' tile [64 x dvp]
   uint8_t *Bb = Yt + ncbv * 8192;           // (sc v')^T [dvn x 64]
-  float *cs = (float *)(Bb + p.dvn * 256);  // 64
-  float *sc = cs + C;                       // 64
+  float *cs = (float *)(Bb + p.dvn * 256);  // [64] scratch of warp 0
+  float *scb = cs + C;                      // [2][64] per-token weights, double-buffered
   __shared__ uint64_t bar_tma, bar_mma;
   __shared__ uint32_t tmem_base;
   __shared__ double seg_total;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int qd = warp & 3, hf = warp >> 2, L = qd * 32 + lane;
   const int64_t seg = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int64_t bh = b * p.H + h;
   const int64_t s_begin = seg * (int64_t)p.Ls;
@@ -163,47 +173,52 @@ __global__ void __launch_bounds__(NTH) k_seg_state(const __grid_constant__ CUten
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_base;
-  const uint32_t lb = (uint32_t)(warp * 32) << 16;
+  const uint32_t lb = (uint32_t)(qd * 32) << 16;
   const float Af = (float)seg_total;
   double carry = 0.0;
   bool ok = true;
-  int tma_pending = 0;  // slice whose tiles are in flight (tid 0's view)
+  int tma_pending = 0;  // slice whose tiles are in flight (thread 0's view)
+  // warp 0: weights of slice n into buffer n & 1, continuing the running prefix
+  auto slice_weights = [&](int n) {
+    const int64_t t0 = s_begin + (int64_t)n * C;
+    const int len = (int)imin64(C, s_end - t0);
+    const double part = warp_cumsum64(la, (b * p.L + t0) * p.H + h, p.H, len, carry, cs);
+    __syncwarp();
+    float *sc = scb + (n & 1) * C;
+    for (int u = lane; u < C; u += 32) sc[u] = u < len ? expf(REV ? cs[u] : Af - cs[u]) : 0.f;
+    carry += part;
+    __syncwarp();
+  };
+  if (warp == 0) slice_weights(0);
 
   for (int n = 0; n < nsl; ++n) {
     const int64_t t0 = s_begin + (int64_t)n * C;
     const int len = (int)imin64(C, s_end - t0);
-    if (warp == 0) {
-      const double part = warp_cumsum64(la, (b * p.L + t0) * p.H + h, p.H, len, carry, cs);
-      __syncwarp();
-      for (int u = lane; u < C; u += 32) sc[u] = u < len ? expf(REV ? cs[u] : Af - cs[u]) : 0.f;
-      carry += part;
-    }
+    const float *sc = scb + (n & 1) * C;
     ok = mbar_wait(&bar_tma, n & 1) && ok;
     if (n >= 1) ok = mbar_wait(&bar_mma, (n - 1) & 1) && ok;
     if (tid == 0 && ok) tma_pending = -1;
     if (__syncthreads_or(!ok)) break;
     tc_fence_after();
     const int buf = n & 1;
-    {  // A operand: k'^T, lane i = feature, 64 tokens
+    {  // A operand: k'^T, lane = feature, tokens [32 hf, 32 hf + 32)
       float v[32];
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
-#pragma unroll
-        for (int uu = 0; uu < 32; ++uu) {
-          const int u = half * 32 + uu;
-          v[uu] = (tid < p.dk && u < len) ? tf32r(*(const float *)(Xt + sw128_off(u, tid, C))) : 0.f;
-        }
-        tmem_st32(tmem + lb + 128 + buf * 64 + half * 32, v);
+      for (int uu = 0; uu < 32; ++uu) {
+        const int u = hf * 32 + uu;
+        v[uu] = (L < p.dk && u < len) ? tf32r(*(const float *)(Xt + sw128_off(u, L, C))) : 0.f;
       }
+      tmem_st32(tmem + lb + 128 + buf * 64 + hf * 32, v);
     }
-    if (tid < p.dvn) {  // B operand: (sc v')^T, row j = feature
-#pragma unroll 4
-      for (int u = 0; u < C; u += 4) {
+    if (L < p.dvn) {  // B operand: (sc v')^T, row = feature
+#pragma unroll
+      for (int uu = 0; uu < 32; uu += 4) {
+        const int u = hf * 32 + uu;
         float f[4];
 #pragma unroll
         for (int r = 0; r < 4; ++r)
-          f[r] = tid < p.dv ? tf32r(*(const float *)(Yt + sw128_off(u + r, tid, C)) * sc[u + r]) : 0.f;
-        *reinterpret_cast<float4 *>(Bb + sw128_off(tid, u, p.dvn)) = make_float4(f[0], f[1], f[2], f[3]);
+          f[r] = L < p.dv ? tf32r(*(const float *)(Yt + sw128_off(u + r, L, C)) * sc[u + r]) : 0.f;
+        *reinterpret_cast<float4 *>(Bb + sw128_off(L, u, p.dvn)) = make_float4(f[0], f[1], f[2], f[3]);
       }
     }
     tmem_st_wait();
@@ -224,19 +239,21 @@ __global__ void __launch_bounds__(NTH) k_seg_state(const __grid_constant__ CUten
                sdesc(bsm + (kk >> 2) * (p.dvn * 128) + (kk & 3) * 32), id, (n > 0 || kk > 0) ? 1u : 0u);
       mma_commit(&bar_mma);
     }
+    if (warp == 0 && n + 1 < nsl) slice_weights(n + 1);
   }
   if (ok) ok = mbar_wait(&bar_mma, (nsl - 1) & 1);
   const bool fail = __syncthreads_or(!ok);
   tc_fence_after();
   if (!fail) {
     float *dst = states + (bh * p.nseg + seg) * (int64_t)p.dk * p.dv;
-    for (int c0 = 0; c0 < p.dvn; c0 += 32) {
+    for (int c0 = hf * 64; c0 < hf * 64 + 64; c0 += 32) {
+      if (c0 >= p.dvn) break;  // warp-uniform
       float v[32];
       tmem_ld32(tmem + lb + c0, v);
-      if (tid < p.dk) {
+      if (L < p.dk) {
 #pragma unroll
         for (int jj = 0; jj < 32; ++jj)
-          if (c0 + jj < p.dv) dst[(int64_t)tid * p.dv + c0 + jj] = v[jj];
+          if (c0 + jj < p.dv) dst[(int64_t)L * p.dv + c0 + jj] = v[jj];
       }
     }
     if (tid == 0) Aseg[bh * p.nseg + seg] = Af;
@@ -251,11 +268,12 @@ __global__ void __launch_bounds__(NTH) k_seg_state(const __grid_constant__ CUten
 // ===========================================================================
 // State passing over segments, in place (one thread per state element).
 //   causal:      st[s] <- state entering segment s from the left; the first is
-//                h0 (read transposed when TRANS_H0), or 0
+//                h0 (read transposed when TRANS), or 0
 //   anti-causal: st[s] <- state entering segment s from the right (0 for the
-//                last); the state left of segment 0 goes to fin (if given)
+//                last); the state left of segment 0 goes to fin (if given,
+//                written transposed when TRANS)
 // grid (B*H, ceil(dk*dv / 128))
-template <bool REV, bool TRANS_H0>
+template <bool REV, bool TRANS>
 __global__ void __launch_bounds__(NTH) k_seg_scan(float *__restrict__ st,
                                                   const float *__restrict__ Aseg,
                                                   const float *__restrict__ h0,
@@ -269,7 +287,7 @@ __global__ void __launch_bounds__(NTH) k_seg_scan(float *__restrict__ st,
   constexpr int U = 8;  // segments loaded ahead of the dependent chain
   float run = 0.f;
   if (!REV) {
-    if (h0) run = TRANS_H0 ? h0[bh * sz + (e % p.dv) * p.dk + e / p.dv] : h0[bh * sz + e];
+    if (h0) run = TRANS ? h0[bh * sz + (e % p.dv) * p.dk + e / p.dv] : h0[bh * sz + e];
     for (int s0 = 0; s0 < p.nseg; s0 += U) {
       float x[U], d[U];
 #pragma unroll
@@ -289,45 +307,52 @@ __global__ void __launch_bounds__(NTH) k_seg_scan(float *__restrict__ st,
       for (int u = 0; u < U; ++u)
         if (s0 - u >= 0) { q[(int64_t)(s0 - u) * sz] = run; run = fmaf(d[u], run, x[u]); }
     }
-    if (fin) fin[bh * sz + e] = run;
+    if (fin) fin[bh * sz + (TRANS ? (e % p.dv) * p.dk + e / p.dv : e)] = run;
   }
 }
 
 // ===========================================================================
 // Walk over the chunks of one segment (left to right, or right to left when
 // REV) with the running state resident in tensor memory.  grid (nseg, H, B),
-// 128 threads, two CTAs per SM.
+// 256 threads: thread (quarter q, lane l, half f) owns tensor-memory lane
+// 32q + l and column half f of each 64-column block; two CTAs per SM.
 //
 // Tensor memory (256 columns):
-//   X   [0,64)    S = q' k'^T (M = 64: rows 16w..16w+15 in lanes 32w..), then
+//   X   [0,64)    S = q' k'^T (M = 64: rows 16q..16q+15 in lanes 32q..), then
 //                 out'^T (lane j = feature, column = token)
 //   VT  [64,128)  v'^T of the chunk (A operand)
 //   HT  [128,256) running state, transposed (A operand): lane j, column i
 // Shared memory: q' tile (scaled in place to the B operand of the inter term),
 // k' tile (then reused for w * k'^T, the B operand of the state update), v'
 // tile (then reused for P).
+// The entering state is read from Hseg as [dk x dv] (or [dv x dk] when
+// HT_SRC_T).
 template <bool REV, bool ATOMIC>
-__global__ void __launch_bounds__(NTH) k_walk(const __grid_constant__ CUtensorMap tmQ,
+__global__ void __launch_bounds__(NT2, 2) k_walk(const __grid_constant__ CUtensorMap tmQ,
                                               const __grid_constant__ CUtensorMap tmK,
                                               const __grid_constant__ CUtensorMap tmV,
                                               const float *__restrict__ la,
-                                              const float *__restrict__ Hseg, OutArgs oa,
-                                              PassGeo p) {
+                                              const float *__restrict__ Hseg, int hseg_t,
+                                              OutArgs oa, PassGeo p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
-  uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  uint8_t *smem = smem_align1024(smem_raw);
   const int ncbk = p.dkp / 32, ncbv = p.dvp / 32;
   const uint32_t vbytes = (uint32_t)max(ncbv * 8192, 16384);
   uint8_t *Qb = smem;
   uint8_t *Kb = Qb + ncbk * 8192;
   uint8_t *Vb = Kb + ncbk * 8192;
-  float *cs = (float *)(Vb + vbytes);
-  float *ew = cs + C, *ww = ew + C;
-  float *red = ww + C;  // [4][64]
+  // per-chunk factors, double-buffered: in-chunk prefix of la times log2(e),
+  // exp(cs), exp(A - cs); computed one chunk ahead by warp 0
+  float *cs2b = (float *)(Vb + vbytes);  // [2][64]
+  float *ewb = cs2b + 2 * C, *wwb = ewb + 2 * C;
+  float *red = wwb + 2 * C;  // [4][64]
+  float *scr = red + 4 * C;  // [64] scratch of warp 0
   __shared__ uint64_t bar_tma, bar_s, bar_i, bar_o, bar_h;
   __shared__ uint32_t tmem_base;
-  __shared__ float a_chunk;
+  __shared__ float a_chunk[2];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int qd = warp & 3, hf = warp >> 2, L = qd * 32 + lane;
   const int64_t seg = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int64_t bh = b * p.H + h;
   const int64_t s_begin = seg * (int64_t)p.Ls;
@@ -337,6 +362,7 @@ __global__ void __launch_bounds__(NTH) k_walk(const __grid_constant__ CUtensorMa
   const int dk = p.dk, dv = p.dv, dkn = p.dkn;
   const uint32_t tile_tx = (uint32_t)(2 * ncbk + ncbv) * 8192;
   const int oslot = oa.out_slots == p.H ? (int)h : (int)(h / p.hpg);
+  constexpr float LOG2E = 1.4426950408889634f;
 
   if (warp == 0) tmem_alloc(&tmem_base, 256);
   if (tid == 0) {
@@ -354,29 +380,52 @@ __global__ void __launch_bounds__(NTH) k_walk(const __grid_constant__ CUtensorMa
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_base;
-  const uint32_t lb = (uint32_t)(warp * 32) << 16;
-  int tma_pending = -1;
-  // load chunk c's tiles; `use` counts the barrier's phases (chunks in walk order)
-  auto issue_tma = [&](int c, int use) {
+  const uint32_t lb = (uint32_t)(qd * 32) << 16;
+  int tma_pending = -1;  // barrier phase of loads not yet waited for (thread 0)
+  // chunk c's tiles; `use` counts the barrier's phases (chunks in walk order).
+  // The q'/v' and k' halves may be issued at different times.
+  auto tma_qv = [&](int c, int use) {
     const int row = (int)(b * p.L + s_begin + (int64_t)c * C);
     mbar_expect_tx(&bar_tma, tile_tx);
-    for (int cb = 0; cb < ncbk; ++cb) {
-      tma_load_3d(Qb + cb * 8192, &tmQ, &bar_tma, cb * 32, kslot, row);
-      tma_load_3d(Kb + cb * 8192, &tmK, &bar_tma, cb * 32, kslot, row);
-    }
+    for (int cb = 0; cb < ncbk; ++cb) tma_load_3d(Qb + cb * 8192, &tmQ, &bar_tma, cb * 32, kslot, row);
     for (int cb = 0; cb < ncbv; ++cb) tma_load_3d(Vb + cb * 8192, &tmV, &bar_tma, cb * 32, vslot, row);
     tma_pending = use;
   };
-  if (tid == 0) issue_tma(REV ? nc - 1 : 0, 0);
+  auto tma_k = [&](int c) {
+    const int row = (int)(b * p.L + s_begin + (int64_t)c * C);
+    for (int cb = 0; cb < ncbk; ++cb) tma_load_3d(Kb + cb * 8192, &tmK, &bar_tma, cb * 32, kslot, row);
+  };
+  if (tid == 0) {
+    tma_qv(REV ? nc - 1 : 0, 0);
+    tma_k(REV ? nc - 1 : 0);
+  }
+
+  // warp 0: the factors of chunk c into buffer bf
+  auto chunk_factors = [&](int c, int bf) {
+    const int64_t t0 = s_begin + (int64_t)c * C;
+    const int len = (int)imin64(C, s_end - t0);
+    const double tot = warp_cumsum64(la, (b * p.L + t0) * p.H + h, p.H, len, 0.0, scr);
+    __syncwarp();
+    const float tot2 = (float)tot * LOG2E;
+    for (int t = lane; t < C; t += 32) {
+      const float x = t < len ? scr[t] * LOG2E : 0.f;
+      cs2b[bf * C + t] = x;
+      ewb[bf * C + t] = t < len ? ex2f(x) : 0.f;
+      wwb[bf * C + t] = t < len ? ex2f(tot2 - x) : 0.f;
+    }
+    if (lane == 0) a_chunk[bf] = ex2f(tot2);
+    __syncwarp();
+  };
+  if (warp == 0) chunk_factors(REV ? nc - 1 : 0, 0);
 
   {  // running state, transposed: lane j, column i = state[i][j]
     const float *H0 = Hseg + (bh * p.nseg + seg) * (int64_t)dk * dv;
-    for (int c0 = 0; c0 < rup(dk, 32); c0 += 32) {
+    for (int c0 = hf * 64; c0 < hf * 64 + 64 && c0 < rup(dk, 32); c0 += 32) {
       float hv[32];
 #pragma unroll
       for (int ii = 0; ii < 32; ++ii) {
         const int i = c0 + ii;
-        hv[ii] = (tid < dv && i < dk) ? H0[(int64_t)i * dv + tid] : 0.f;
+        hv[ii] = (L < dv && i < dk) ? (hseg_t ? H0[(int64_t)L * dk + i] : H0[(int64_t)i * dv + L]) : 0.f;
       }
       tmem_st32(tmem + lb + 128 + c0, hv);
     }
@@ -384,20 +433,14 @@ __global__ void __launch_bounds__(NTH) k_walk(const __grid_constant__ CUtensorMa
   }
 
   bool ok = true;
+  const bool split = oa.dcs != nullptr;
   for (int ci = 0; ci < nc; ++ci) {
     const int c = REV ? nc - 1 - ci : ci;
     const int64_t t0 = s_begin + (int64_t)c * C;
     const int len = (int)imin64(C, s_end - t0);
-    if (warp == 0) {
-      const double tot = warp_cumsum64(la, (b * p.L + t0) * p.H + h, p.H, len, 0.0, cs);
-      __syncwarp();
-      const float tf = (float)tot;
-      for (int t = lane; t < C; t += 32) {
-        ew[t] = t < len ? expf(cs[t]) : 0.f;
-        ww[t] = t < len ? expf(tf - cs[t]) : 0.f;
-      }
-      if (lane == 0) a_chunk = expf(tf);
-    }
+    const int cnext = REV ? c - 1 : c + 1;
+    const int fb = ci & 1;
+    const float *cs2 = cs2b + fb * C, *ew = ewb + fb * C, *ww = wwb + fb * C;
     ok = mbar_wait(&bar_tma, ci & 1) && ok;
     if (tid == 0 && ok) tma_pending = -1;
     tc_fence_before();
@@ -406,22 +449,6 @@ __global__ void __launch_bounds__(NTH) k_walk(const __grid_constant__ CUtensorMa
     // inter-term factor of a query row, state-update weight of a key column
     const float *interf = REV ? ww : ew;
     const float *statew = REV ? ew : ww;
-    {  // round the TMA-fed q' and k' tiles to TF32 (nearest) in place: the
-       // tensor core would otherwise truncate them
-      const int r = tid & 63, half = tid >> 6;
-      const int cols = p.dkp / 2;
-      for (int col = half * cols; col < (half + 1) * cols; col += 4) {
-        float4 *q4 = reinterpret_cast<float4 *>(Qb + sw128_off(r, col, C));
-        float4 *k4 = reinterpret_cast<float4 *>(Kb + sw128_off(r, col, C));
-        float4 a = *q4, bb = *k4;
-        a.x = tf32r(a.x); a.y = tf32r(a.y); a.z = tf32r(a.z); a.w = tf32r(a.w);
-        bb.x = tf32r(bb.x); bb.y = tf32r(bb.y); bb.z = tf32r(bb.z); bb.w = tf32r(bb.w);
-        *q4 = a;
-        *k4 = bb;
-      }
-      fence_async_smem();
-      __syncthreads();
-    }
     if (tid == 0) {  // S = q' k'^T (M = 64, N = 64, K = dk)
       const uint32_t qa = smem_u32(Qb), ka = smem_u32(Kb);
       const uint32_t id = idesc_tf32(64, 64);
@@ -431,63 +458,54 @@ __global__ void __launch_bounds__(NTH) k_walk(const __grid_constant__ CUtensorMa
       }
       mma_commit(&bar_s);
     }
-    {  // v'^T into tensor memory
+    {  // v'^T into tensor memory: lane = feature, tokens [32 hf, 32 hf + 32)
       float v[32];
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
-#pragma unroll
-        for (int uu = 0; uu < 32; ++uu) {
-          const int u = half * 32 + uu;
-          v[uu] = (tid < dv && u < len) ? tf32r(*(const float *)(Vb + sw128_off(u, tid, C))) : 0.f;
-        }
-        tmem_st32(tmem + lb + 64 + half * 32, v);
+      for (int uu = 0; uu < 32; ++uu) {
+        const int u = hf * 32 + uu;
+        v[uu] = (L < dv && u < len) ? tf32r(*(const float *)(Vb + sw128_off(u, L, C))) : 0.f;
       }
+      tmem_st32(tmem + lb + 64 + hf * 32, v);
     }
-    float kw[C];  // w_u * k'[u][i], i = tid
+    float kw[32];  // w_u * k'[u][L], tokens [32 hf, 32 hf + 32)
 #pragma unroll
-    for (int u = 0; u < C; ++u)
-      kw[u] = (tid < dk) ? tf32r(*(const float *)(Kb + sw128_off(u, tid, C)) * statew[u]) : 0.f;
+    for (int uu = 0; uu < 32; ++uu) {
+      const int u = hf * 32 + uu;
+      kw[uu] = (L < dk) ? tf32r(*(const float *)(Kb + sw128_off(u, L, C)) * statew[u]) : 0.f;
+    }
     ok = mbar_wait(&bar_s, ci & 1) && ok;
     tc_fence_after();
-    float sr[C];
-    {
-      float t32[32];
-      tmem_ld32(tmem + lb, t32);
-#pragma unroll
-      for (int u = 0; u < 32; ++u) sr[u] = t32[u];
-      tmem_ld32(tmem + lb + 32, t32);
-#pragma unroll
-      for (int u = 0; u < 32; ++u) sr[32 + u] = t32[u];
-    }
+    float sr[32];
+    tmem_ld32(tmem + lb + hf * 32, sr);
     tc_fence_before();
     __syncthreads();  // every read of the v' and k' tiles and of S is done
-    if (lane < 16) {  // P into the v' tile's space: rows r = 16w + lane
-      const int r = warp * 16 + lane;
-      const float cr = cs[r < len ? r : 0];
+    if (lane < 16) {  // P into the v' tile's space: row r, tokens [32 hf, +32)
+      const int r = qd * 16 + lane;
+      const float cr = cs2[r];
       uint8_t *P = Vb;
 #pragma unroll
-      for (int u = 0; u < C; u += 4) {
+      for (int uu = 0; uu < 32; uu += 4) {
         float f[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          const int uu = u + e;
-          const bool valid = r < len && uu < len && (REV ? uu >= r : uu <= r);
-          f[e] = valid ? tf32r(expf(REV ? cs[uu] - cr : cr - cs[uu]) * sr[uu]) : 0.f;
+          const int u = hf * 32 + uu + e;
+          const bool valid = r < len && u < len && (REV ? u >= r : u <= r);
+          f[e] = valid ? tf32r(ex2f(REV ? cs2[u] - cr : cr - cs2[u]) * sr[uu + e]) : 0.f;
         }
-        *reinterpret_cast<float4 *>(P + sw128_off(r, u, C)) = make_float4(f[0], f[1], f[2], f[3]);
+        *reinterpret_cast<float4 *>(P + sw128_off(r, hf * 32 + uu, C)) = make_float4(f[0], f[1], f[2], f[3]);
       }
     }
-    if (tid < dkn) {  // w * k'^T into the k' tile's space (B operand, dkn rows)
+    if (L < dkn) {  // w * k'^T into the k' tile's space (B operand, dkn rows)
 #pragma unroll
-      for (int u = 0; u < C; u += 4)
-        *reinterpret_cast<float4 *>(Kb + sw128_off(tid, u, dkn)) =
-            make_float4(kw[u], kw[u + 1], kw[u + 2], kw[u + 3]);
+      for (int uu = 0; uu < 32; uu += 4)
+        *reinterpret_cast<float4 *>(Kb + sw128_off(L, hf * 32 + uu, dkn)) =
+            make_float4(kw[uu], kw[uu + 1], kw[uu + 2], kw[uu + 3]);
     }
-    {  // q' rows scaled by the inter-term factor, in place
-      const int r = tid & 63, half = tid >> 6;
+    {  // q' rows scaled by the inter-term factor, in place (4 threads per row)
+      const int r = tid & 63, part = tid >> 6;
       const float e = interf[r];
-      const int cols = p.dkp / 2;
-      for (int col = half * cols; col < (half + 1) * cols; col += 4) {
+      const int cols = p.dkp / 4;
+      for (int col = part * cols; col < (part + 1) * cols; col += 4) {
         float4 *q4 = reinterpret_cast<float4 *>(Qb + sw128_off(r, col, C));
         float4 f = *q4;
         f.x = tf32r(f.x * e); f.y = tf32r(f.y * e); f.z = tf32r(f.z * e); f.w = tf32r(f.w * e);
@@ -499,39 +517,37 @@ __global__ void __launch_bounds__(NTH) k_walk(const __grid_constant__ CUtensorMa
     tc_fence_before();
     if (__syncthreads_or(!ok)) break;
     tc_fence_after();
-    const bool split = oa.dcs != nullptr;
     if (tid == 0) {  // out'^T = HT (f q')^T  [+ v'^T P^T]
       const uint32_t qa = smem_u32(Qb), pa = smem_u32(Vb);
       const uint32_t id = idesc_tf32(128, 64);
       for (int kk = 0; kk < dk / 8; ++kk)
         mma_ts(tmem, tmem + 128 + kk * 8, sdesc(qa + (kk >> 2) * 8192 + (kk & 3) * 32), id,
                kk > 0 ? 1u : 0u);
-      if (split) mma_commit(&bar_i);
+      if (split) {
+        mma_commit(&bar_i);
+      } else {
 #pragma unroll
-      for (int kk = 0; kk < C / 8; ++kk)
-        if (!split) mma_ts(tmem, tmem + 64 + kk * 8, sdesc(pa + (kk >> 2) * 8192 + (kk & 3) * 32), id, 1u);
-      if (!split) mma_commit(&bar_o);
+        for (int kk = 0; kk < C / 8; ++kk)
+          mma_ts(tmem, tmem + 64 + kk * 8, sdesc(pa + (kk >> 2) * 8192 + (kk & 3) * 32), id, 1u);
+        mma_commit(&bar_o);
+      }
     }
+    if (warp == 0 && ci + 1 < nc) chunk_factors(cnext, fb ^ 1);
     if (split) {
-      // r[t] = y_t . (inter-chunk part of out'_t), reduced over the 128 lanes
+      // dcs[t] = y_t . (inter-chunk part of out'_t), reduced over the 128 lanes
       ok = mbar_wait(&bar_i, ci & 1) && ok;
       tc_fence_after();
-      float o[C];
-      {
-        float t32[32];
-        tmem_ld32(tmem + lb, t32);
-#pragma unroll
-        for (int t = 0; t < 32; ++t) o[t] = t32[t];
-        tmem_ld32(tmem + lb + 32, t32);
-#pragma unroll
-        for (int t = 0; t < 32; ++t) o[32 + t] = t32[t];
-      }
+      float o[32];
+      tmem_ld32(tmem + lb + hf * 32, o);
       const int64_t ldy = (int64_t)(p.H / p.hpg) * dv;
-      const float *ys = oa.y + ((b * p.L + t0) * (p.H / p.hpg) + h / p.hpg) * (int64_t)dv + tid;
+      const float *ys = oa.y + ((b * p.L + t0) * (p.H / p.hpg) + h / p.hpg) * (int64_t)dv + L;
 #pragma unroll
-      for (int t = 0; t < C; ++t) o[t] = (tid < dv && t < len) ? o[t] * ys[t * ldy] : 0.f;
+      for (int tt = 0; tt < 32; ++tt) {
+        const int t = hf * 32 + tt;
+        o[tt] = (L < dv && t < len) ? o[tt] * ys[t * ldy] : 0.f;
+      }
 #pragma unroll
-      for (int off = 16, n = C; off >= 1; off >>= 1, n >>= 1) {
+      for (int off = 16, n = 32; off >= 1; off >>= 1, n >>= 1) {
         const bool up = (lane & off) != 0;
 #pragma unroll
         for (int k2 = 0; k2 < n / 2; ++k2) {
@@ -540,8 +556,7 @@ __global__ void __launch_bounds__(NTH) k_walk(const __grid_constant__ CUtensorMa
           o[k2] = mine + __shfl_xor_sync(0xffffffffu, send, off);
         }
       }
-      red[warp * C + 2 * lane] = o[0];
-      red[warp * C + 2 * lane + 1] = o[1];
+      red[qd * C + hf * 32 + lane] = o[0];
       tc_fence_before();
       __syncthreads();
       tc_fence_after();
@@ -558,32 +573,27 @@ __global__ void __launch_bounds__(NTH) k_walk(const __grid_constant__ CUtensorMa
     }
     ok = mbar_wait(&bar_o, ci & 1) && ok;
     tc_fence_after();
+    // q' and v' tiles are free now: start the next chunk's loads
+    if (tid == 0 && ok && ci + 1 < nc) tma_qv(cnext, ci + 1);
     {
-      float o[C];
-      {
-        float t32[32];
-        tmem_ld32(tmem + lb, t32);
-#pragma unroll
-        for (int t = 0; t < 32; ++t) o[t] = t32[t];
-        tmem_ld32(tmem + lb + 32, t32);
-#pragma unroll
-        for (int t = 0; t < 32; ++t) o[32 + t] = t32[t];
-      }
-      if (tid < dv) {
+      float o[32];
+      tmem_ld32(tmem + lb + hf * 32, o);
+      if (L < dv) {
         const int64_t ld = (int64_t)oa.out_slots * dv;
-        float *os = oa.out + ((b * p.L + t0) * oa.out_slots + oslot) * (int64_t)dv + tid;
+        float *os = oa.out + ((b * p.L + t0) * oa.out_slots + oslot) * (int64_t)dv + L;
 #pragma unroll
-        for (int t = 0; t < C; ++t) {
+        for (int tt = 0; tt < 32; ++tt) {
+          const int t = hf * 32 + tt;
           if (t < len) {
-            if (ATOMIC) atomicAdd(os + t * ld, o[t]);
-            else os[t * ld] = o[t];
+            if (ATOMIC) atomicAdd(os + t * ld, o[tt]);
+            else os[t * ld] = o[tt];
           }
         }
       }
     }
     {  // HT <- exp(A_c) HT, before the state-update MMA accumulates into it
-      const float a = a_chunk;
-      for (int c0 = 0; c0 < rup(dk, 32); c0 += 32) {
+      const float a = a_chunk[fb];
+      for (int c0 = hf * 64; c0 < hf * 64 + 64 && c0 < rup(dk, 32); c0 += 32) {
         float hv[32];
         tmem_ld32(tmem + lb + 128 + c0, hv);
 #pragma unroll
@@ -606,9 +616,9 @@ __global__ void __launch_bounds__(NTH) k_walk(const __grid_constant__ CUtensorMa
     }
     ok = mbar_wait(&bar_h, ci & 1) && ok;
     tc_fence_after();
-    if (tid == 0 && ok && ci + 1 < nc) issue_tma(REV ? c - 1 : c + 1, ci + 1);
+    if (tid == 0 && ok && ci + 1 < nc) tma_k(cnext);
     tc_fence_before();
-    if (__syncthreads_or(!ok)) break;  // also orders the dcs reads of red before reuse
+    if (__syncthreads_or(!ok)) break;
     tc_fence_after();
   }
   __syncthreads();
@@ -631,7 +641,7 @@ __global__ void __launch_bounds__(NTH) k_dla_intra(const __grid_constant__ CUten
                                                    const float *__restrict__ la,
                                                    float *__restrict__ Bt, PassGeo p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
-  uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  uint8_t *smem = smem_align1024(smem_raw);
   const int dk = p.dk, dv = p.dv;  // here dk = q/k features, dv = v/dout features
   const int ncbk = p.dkp / 32, ncbv = p.dvp / 32, ncbm = ncbk > ncbv ? ncbk : ncbv;
   uint8_t *T1 = smem, *T2 = smem + ncbm * 8192;
@@ -754,28 +764,25 @@ __global__ void __launch_bounds__(NTH) k_dla_intra(const __grid_constant__ CUten
 // where B_t is the intra-chunk block sum, rq / rk the inter-chunk terms
 // q_t.dq_inter(t) and k_t.dk_inter(t), G_end the gradient of the state at the
 // segment's end (from its right) and S_end that state (the state entering the
-// next segment, given transposed [dv x dk]).  grid (nseg, H, B).
+// next segment); both are given in the same layout (each transposed, sz
+// elements).  grid (nseg, H, B).
 constexpr int DT = 256;
 __global__ void __launch_bounds__(DT) k_dla(const float *__restrict__ Bt,
                                             const float *__restrict__ rq,
                                             const float *__restrict__ rk,
                                             const float *__restrict__ Gst,
-                                            const float *__restrict__ StT, float *__restrict__ dla,
-                                            int64_t L, int64_t H, int dk, int dv, int Ls, int nseg) {
+                                            const float *__restrict__ Sst, float *__restrict__ dla,
+                                            int64_t L, int64_t H, int64_t sz, int Ls, int nseg) {
   __shared__ double sh[DT];
   __shared__ double carry_in;
   const int tid = threadIdx.x;
   const int64_t seg = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int64_t bh = b * H + h;
-  const int64_t sz = (int64_t)dk * dv;
   double acc = 0.0;
   if (seg + 1 < nseg) {
     const float *G = Gst + (bh * nseg + seg) * sz;
-    const float *S = StT + (bh * nseg + seg + 1) * sz;
-    for (int64_t e = tid; e < sz; e += DT) {
-      const int64_t i = e / dv, j = e % dv;
-      acc += (double)G[e] * (double)S[j * dk + i];
-    }
+    const float *S = Sst + (bh * nseg + seg + 1) * sz;
+    for (int64_t e = tid; e < sz; e += DT) acc += (double)G[e] * (double)S[e];
   }
   sh[tid] = acc;
   __syncthreads();
@@ -882,10 +889,10 @@ size_t state_floats(const PassGeo &p) {
 }
 
 size_t seg_state_smem(const PassGeo &p) {
-  return (size_t)(p.dkp / 32 + p.dvp / 32) * 8192 + (size_t)p.dvn * 256 + 2 * C * 4 + 1024;
+  return (size_t)(p.dkp / 32 + p.dvp / 32) * 8192 + (size_t)p.dvn * 256 + 3 * C * 4 + 1024;
 }
 size_t walk_smem(const PassGeo &p) {
-  return (size_t)(p.dkp / 32) * 2 * 8192 + std::max(p.dvp / 32 * 8192, 16384) + 7 * C * 4 + 1024;
+  return (size_t)(p.dkp / 32) * 2 * 8192 + std::max(p.dvp / 32 * 8192, 16384) + 11 * C * 4 + 1024;
 }
 
 size_t dla_intra_smem(const PassGeo &p) {
@@ -898,13 +905,42 @@ cudaError_t set_smem(K kern, size_t bytes) {
   return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
 }
 
-// One scan pass: segment contributions, state passing, then the walk.
+// Segment contributions and state passing of one pass: on return `states`
+// holds the state entering every segment (from the left, or from the right
+// when REV).
+//   k' : [B*L, qk_slots, dk]   v' : [B*L, v_slots, dv]
+template <bool REV>
+cudaError_t run_states(const PassGeo &p, const float *kp, const float *vp, const float *la,
+                       const float *h0, bool trans, float *fin, float *states, float *Aseg,
+                       cudaStream_t s, const char *name_state) {
+  cudaError_t e;
+  const int64_t rows = p.B * p.L;
+  const int64_t G = p.H / p.hpg;
+  CUtensorMap mk, mv;
+  if ((e = make_map(&mk, kp, rows, p.qk_per_head ? p.H : G, p.dk)) != cudaSuccess) return e;
+  if ((e = make_map(&mv, vp, rows, p.v_per_head ? p.H : G, p.dv)) != cudaSuccess) return e;
+  const dim3 grid((unsigned)p.nseg, (unsigned)p.H, (unsigned)p.B);
+  {
+    const size_t sm = seg_state_smem(p);
+    if ((e = set_smem(k_seg_state<REV>, sm)) != cudaSuccess) return e;
+    LaunchTrace lt(name_state, s);
+    k_seg_state<REV><<<grid, NT2, sm, s>>>(mk, mv, la, states, Aseg, p);
+  }
+  {
+    LaunchTrace lt("tc.seg_scan", s);
+    const dim3 sg((unsigned)(p.B * p.H), (unsigned)cdiv((int64_t)p.dk * p.dv, NTH));
+    if (trans) k_seg_scan<REV, true><<<sg, NTH, 0, s>>>(states, Aseg, h0, fin, p);
+    else k_seg_scan<REV, false><<<sg, NTH, 0, s>>>(states, Aseg, h0, fin, p);
+  }
+  return cudaGetLastError();
+}
+
+// The walk of one pass over every segment, from the entering states.
 //   q', k' : [B*L, qk_slots, dk]   v' : [B*L, v_slots, dv]
 template <bool REV>
-cudaError_t run_pass(const PassGeo &p, const float *qp, const float *kp, const float *vp,
-                     const float *la, const float *h0, bool trans_h0, float *fin, float *states,
-                     float *Aseg, const OutArgs &oa, bool atomic, cudaStream_t s,
-                     const char *name_state, const char *name_walk) {
+cudaError_t run_walk(const PassGeo &p, const float *qp, const float *kp, const float *vp,
+                     const float *la, const float *states, bool states_t, const OutArgs &oa,
+                     bool atomic, cudaStream_t s, const char *name_walk) {
   cudaError_t e;
   const int64_t rows = p.B * p.L;
   const int64_t G = p.H / p.hpg;
@@ -913,28 +949,14 @@ cudaError_t run_pass(const PassGeo &p, const float *qp, const float *kp, const f
   if ((e = make_map(&mk, kp, rows, p.qk_per_head ? p.H : G, p.dk)) != cudaSuccess) return e;
   if ((e = make_map(&mv, vp, rows, p.v_per_head ? p.H : G, p.dv)) != cudaSuccess) return e;
   const dim3 grid((unsigned)p.nseg, (unsigned)p.H, (unsigned)p.B);
-  {
-    const size_t sm = seg_state_smem(p);
-    if ((e = set_smem(k_seg_state<REV>, sm)) != cudaSuccess) return e;
-    LaunchTrace lt(name_state, s);
-    k_seg_state<REV><<<grid, NTH, sm, s>>>(mk, mv, la, states, Aseg, p);
-  }
-  {
-    LaunchTrace lt("tc.seg_scan", s);
-    const dim3 sg((unsigned)(p.B * p.H), (unsigned)cdiv((int64_t)p.dk * p.dv, NTH));
-    if (trans_h0) k_seg_scan<REV, true><<<sg, NTH, 0, s>>>(states, Aseg, h0, fin, p);
-    else k_seg_scan<REV, false><<<sg, NTH, 0, s>>>(states, Aseg, h0, fin, p);
-  }
-  {
-    const size_t sm = walk_smem(p);
-    LaunchTrace lt(name_walk, s);
-    if (atomic) {
-      if ((e = set_smem(k_walk<REV, true>, sm)) != cudaSuccess) return e;
-      k_walk<REV, true><<<grid, NTH, sm, s>>>(mq, mk, mv, la, states, oa, p);
-    } else {
-      if ((e = set_smem(k_walk<REV, false>, sm)) != cudaSuccess) return e;
-      k_walk<REV, false><<<grid, NTH, sm, s>>>(mq, mk, mv, la, states, oa, p);
-    }
+  const size_t sm = walk_smem(p);
+  LaunchTrace lt(name_walk, s);
+  if (atomic) {
+    if ((e = set_smem(k_walk<REV, true>, sm)) != cudaSuccess) return e;
+    k_walk<REV, true><<<grid, NT2, sm, s>>>(mq, mk, mv, la, states, states_t ? 1 : 0, oa, p);
+  } else {
+    if ((e = set_smem(k_walk<REV, false>, sm)) != cudaSuccess) return e;
+    k_walk<REV, false><<<grid, NT2, sm, s>>>(mq, mk, mv, la, states, states_t ? 1 : 0, oa, p);
   }
   return cudaGetLastError();
 }
@@ -952,11 +974,12 @@ size_t fwd_workspace_bytes(const Geo &g) {
   return sizeof(float) * (state_floats(p) + (size_t)(g.B * g.H * p.nseg));
 }
 
-// Three passes' states (two kept for dlog_alpha) + decays + two dcs arrays.
+// Two passes' states (both kept for dlog_alpha) + their decays + three
+// per-token arrays.
 size_t bwd_workspace_bytes(const Geo &g) {
   const PassGeo p = make_pass(g, (int)g.dk, (int)g.dv, false, true);
   const size_t nst = state_floats(p), na = (size_t)(g.B * g.H * p.nseg);
-  return sizeof(float) * (3 * nst + 3 * na + 3 * (size_t)(g.B * g.L * g.H)) + 256;
+  return sizeof(float) * (2 * nst + 2 * na + 3 * (size_t)(g.B * g.L * g.H)) + 256;
 }
 
 cudaError_t fwd(const float *q, const float *k, const float *v, const float *la, const float *h0,
@@ -967,9 +990,10 @@ cudaError_t fwd(const float *q, const float *k, const float *v, const float *la,
   const PassGeo p = make_pass(g, (int)g.dk, (int)g.dv, false, true);
   float *st = static_cast<float *>(ws);
   float *Aseg = st + state_floats(p);
+  if ((e = run_states<false>(p, k, v, la, h0, false, nullptr, st, Aseg, s, "tc.seg_state")) != cudaSuccess)
+    return e;
   OutArgs oa{out, (int)g.H, nullptr, nullptr};
-  return run_pass<false>(p, q, k, v, la, h0, false, nullptr, st, Aseg, oa, false, s,
-                         "tc.seg_state", "tc.walk_out");
+  return run_walk<false>(p, q, k, v, la, st, false, oa, false, s, "tc.walk_out");
 }
 
 cudaError_t bwd(const float *q, const float *k, const float *v, const float *la, const float *h0,
@@ -983,35 +1007,35 @@ cudaError_t bwd(const float *q, const float *k, const float *v, const float *la,
   const PassGeo pa = make_pass(g, DV, DK, true, false);
   // dk_h = anti-causal scan(q' = v, k' = dout, v' = q)
   const PassGeo pb = make_pass(g, DV, DK, true, false);
-  // dv = anti-causal scan(q' = k, k' = q, v' = dout); its leftmost state is dh0
+  // dv = anti-causal scan(q' = k, k' = q, v' = dout).  Its states are the
+  // transposes of pass B's, and its leftmost state is dh0.
   const PassGeo pc = make_pass(g, DK, DV, false, true);
   const size_t nst = state_floats(pa), na = (size_t)(g.B * g.H * pa.nseg);
   float *stA = static_cast<float *>(ws);
   float *stB = stA + nst;
-  float *stC = stB + nst;
-  float *aA = stC + nst;
+  float *aA = stB + nst;
   float *aB = aA + na;
-  float *aC = aB + na;
-  float *dcsq = aC + na;
-  float *dcsk = dcsq + g.B * g.L * g.H;
-  float *Bt = dcsk + g.B * g.L * g.H;
+  float *rq = aB + na;
+  float *rk = rq + g.B * g.L * g.H;
+  float *Bt = rk + g.B * g.L * g.H;
   const bool grouped = g.hpg > 1;
   if (grouped) {
     if ((e = cudaMemsetAsync(dq, 0, sizeof(float) * g.B * g.L * g.G * g.dk, s)) != cudaSuccess) return e;
     if ((e = cudaMemsetAsync(dk, 0, sizeof(float) * g.B * g.L * g.G * g.dk, s)) != cudaSuccess) return e;
   }
   const int oslots = grouped ? (int)g.G : (int)g.H;
-  OutArgs oq{dq, oslots, q, dcsq};
-  if ((e = run_pass<false>(pa, dout, v, k, la, h0, true, nullptr, stA, aA, oq, grouped, s,
-                           "tc.seg_state_dq", "tc.walk_dq")) != cudaSuccess)
+  if ((e = run_states<false>(pa, v, k, la, h0, true, nullptr, stA, aA, s, "tc.seg_state_dq")) != cudaSuccess)
     return e;
-  OutArgs okk{dk, oslots, k, dcsk};
-  if ((e = run_pass<true>(pb, v, dout, q, la, nullptr, false, nullptr, stB, aB, okk, grouped, s,
-                          "tc.seg_state_dk", "tc.walk_dk")) != cudaSuccess)
+  OutArgs oq{dq, oslots, q, rq};
+  if ((e = run_walk<false>(pa, dout, v, k, la, stA, false, oq, grouped, s, "tc.walk_dq")) != cudaSuccess)
+    return e;
+  if ((e = run_states<true>(pb, dout, q, la, nullptr, true, dh0, stB, aB, s, "tc.seg_state_dk")) != cudaSuccess)
+    return e;
+  OutArgs okk{dk, oslots, k, rk};
+  if ((e = run_walk<true>(pb, v, dout, q, la, stB, false, okk, grouped, s, "tc.walk_dk")) != cudaSuccess)
     return e;
   OutArgs ov{dv, (int)g.H, nullptr, nullptr};
-  if ((e = run_pass<true>(pc, k, q, dout, la, nullptr, false, dh0, stC, aC, ov, false, s,
-                          "tc.seg_state_dv", "tc.walk_dv")) != cudaSuccess)
+  if ((e = run_walk<true>(pc, k, q, dout, la, stB, true, ov, false, s, "tc.walk_dv")) != cudaSuccess)
     return e;
   {  // intra-chunk block sums of dlog_alpha
     const PassGeo pi = make_pass(g, DK, DV, false, true);
@@ -1027,10 +1051,10 @@ cudaError_t bwd(const float *q, const float *k, const float *v, const float *la,
     k_dla_intra<<<dim3((unsigned)g.N, (unsigned)g.H, (unsigned)g.B), NTH, sm, s>>>(mq, mk, mv, md,
                                                                                   la, Bt, pi);
   }
-  {
+  {  // pass A's states are S^T, pass B's are G^T: the carry is their plain dot
     LaunchTrace lt("tc.dla", s);
     k_dla<<<dim3((unsigned)pa.nseg, (unsigned)g.H, (unsigned)g.B), DT, 0, s>>>(
-        Bt, dcsq, dcsk, stC, stA, dla, g.L, g.H, DK, DV, pa.Ls, pa.nseg);
+        Bt, rq, rk, stB, stA, dla, g.L, g.H, DK * DV, pa.Ls, pa.nseg);
   }
   return cudaGetLastError();
 }

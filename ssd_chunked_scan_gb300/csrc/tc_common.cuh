@@ -17,6 +17,15 @@ __device__ __forceinline__ uint32_t smem_u32(const void *p) {
   return (uint32_t)__cvta_generic_to_shared(p);
 }
 
+// The dynamic shared-memory base rounded up to 1024 bytes (the 128-byte
+// swizzle repeats every 1024 bytes).  Derived by pointer arithmetic on the
+// __shared__ array itself so that the compiler keeps the shared address space
+// and emits shared-memory loads and stores for everything based on it.
+__device__ __forceinline__ uint8_t *smem_align1024(uint8_t *base) {
+  const uint32_t a = smem_u32(base);
+  return base + ((1024u - (a & 1023u)) & 1023u);
+}
+
 // ---- mbarrier ---------------------------------------------------------------
 __device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
@@ -169,11 +178,13 @@ __device__ __forceinline__ void tmem_st_wait() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
-// fp32 -> tf32, round to nearest (ties away), kept in an fp32 container.
+// fp32 -> tf32 (10 explicit mantissa bits), rounded to nearest with ties
+// away from zero, kept in an fp32 container: add half of the dropped range
+// (bit 12) to the magnitude bits and clear the 13 dropped bits.  Two integer
+// operations; a carry out of the mantissa correctly bumps the exponent.
+// Finite inputs only.
 __device__ __forceinline__ float tf32r(float x) {
-  uint32_t r;
-  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
-  return __uint_as_float(r);
+  return __uint_as_float((__float_as_uint(x) + 0x1000u) & 0xffffe000u);
 }
 
 // Byte offset of element (row, col) inside a K-major 128B-swizzled operand
