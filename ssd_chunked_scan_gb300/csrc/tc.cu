@@ -115,27 +115,30 @@ __device__ __forceinline__ int v_slot(const PassGeo &p, int64_t h) {
 //   anti-causal D = sum_u exp(cs_u) k'_u v'_u^T           (evaluated at its start)
 // with cs the in-segment inclusive prefix of la and A_seg its total (also
 // written).  grid (nseg, H, B), 256 threads: thread (quarter q, lane l, half f)
-// owns tensor-memory lane 32q + l and token half f of each 64-token slice.
-// Tensor memory (256 columns): D [0,128), A operand k'^T double-buffered at
-// [128,192) / [192,256).  Shared memory: k' and v' tiles (TMA), and the B
-// operand (sc * v')^T [dvn x 64], K-major.
+// owns tensor-memory lane 32q + l and token half f of each 32-token slice.
+// The segment is streamed in 32-token slices through a two-stage TMA ring,
+// loaded two slices ahead.  Tensor memory (256 columns): D [0,128), A operand
+// k'^T double-buffered at [128,160) / [160,192).  Shared memory: two stages of
+// k' and v' tiles, and the B operand (sc * v')^T [dvn x 32], double-buffered.
+constexpr int SL = 32;  // slice length of the segment contraction
 template <bool REV>
 __global__ void __launch_bounds__(NT2, 2) k_seg_state(const __grid_constant__ CUtensorMap tmK,
-                                                   const __grid_constant__ CUtensorMap tmV,
-                                                   const float *__restrict__ la,
-                                                   float *__restrict__ states,
-                                                   float *__restrict__ Aseg, PassGeo p) {
+                                                      const __grid_constant__ CUtensorMap tmV,
+                                                      const float *__restrict__ la,
+                                                      float *__restrict__ states,
+                                                      float *__restrict__ Aseg, PassGeo p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t *smem = smem_align1024(smem_raw);
   const int ncbk = p.dkp / 32, ncbv = p.dvp / 32;
-  uint8_t *Xt = smem;                       // k' tile [64 x dkp]
-  uint8_t *Yt = Xt + ncbk * 8192;           // v' tile [64 x dvp]
-  uint8_t *Bb = Yt + ncbv * 8192;           // (sc v')^T [dvn x 64]
-  float *cs = (float *)(Bb + p.dvn * 256);  // [64] scratch of warp 0
-  float *scb = cs + C;                      // [2][64] per-token weights, double-buffered
-  __shared__ uint64_t bar_tma, bar_mma;
+  const uint32_t xbytes = (uint32_t)ncbk * 4096, ybytes = (uint32_t)ncbv * 4096;
+  const uint32_t stage = xbytes + ybytes;
+  const uint32_t bbytes = (uint32_t)rup(p.dvn * 128, 1024);
+  uint8_t *tiles = smem;                      // [2][k' tile 32 x dkp | v' tile 32 x dvp]
+  uint8_t *Bb = smem + 2 * stage;             // [2][dvn x 32] K-major
+  float *scb = (float *)(Bb + 2 * bbytes);    // [256] per-token weights of 8 slices
+  __shared__ double wtot[8];
+  __shared__ uint64_t bar_tma[2], bar_mma[2];
   __shared__ uint32_t tmem_base;
-  __shared__ double seg_total;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int qd = warp & 3, hf = warp >> 2, L = qd * 32 + lane;
@@ -143,82 +146,110 @@ __global__ void __launch_bounds__(NT2, 2) k_seg_state(const __grid_constant__ CU
   const int64_t bh = b * p.H + h;
   const int64_t s_begin = seg * (int64_t)p.Ls;
   const int64_t s_end = imin64(p.L, s_begin + p.Ls);
-  const int nsl = (int)cdiv(s_end - s_begin, C);
+  const int nsl = (int)cdiv(s_end - s_begin, SL);
   const int kslot = qk_slot(p, h), vslot = v_slot(p, h);
-  const uint32_t tile_tx = (uint32_t)(ncbk + ncbv) * 8192;
 
   if (warp == 0) tmem_alloc(&tmem_base, 256);
   if (tid == 0) {
-    mbar_init(&bar_tma, 1);
-    mbar_init(&bar_mma, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bar_tma[i], 1);
+      mbar_init(&bar_mma[i], 1);
+    }
     fence_mbar_init();
     prefetch_tmap(&tmK);
     prefetch_tmap(&tmV);
   }
   __syncthreads();
+  int pend[2] = {-1, -1};  // slice in flight per stage (thread 0's view)
   auto issue_tma = [&](int n) {
-    const int row = (int)(b * p.L + s_begin + (int64_t)n * C);
-    mbar_expect_tx(&bar_tma, tile_tx);
-    for (int cb = 0; cb < ncbk; ++cb) tma_load_3d(Xt + cb * 8192, &tmK, &bar_tma, cb * 32, kslot, row);
-    for (int cb = 0; cb < ncbv; ++cb) tma_load_3d(Yt + cb * 8192, &tmV, &bar_tma, cb * 32, vslot, row);
+    const int st = n & 1;
+    pend[st] = n;
+    const int row = (int)(b * p.L + s_begin + (int64_t)n * SL);
+    uint8_t *Xt = tiles + st * stage, *Yt = Xt + xbytes;
+    mbar_expect_tx(&bar_tma[st], stage);
+    for (int cb = 0; cb < ncbk; ++cb) tma_load_3d(Xt + cb * 4096, &tmK, &bar_tma[st], cb * 32, kslot, row);
+    for (int cb = 0; cb < ncbv; ++cb) tma_load_3d(Yt + cb * 4096, &tmV, &bar_tma[st], cb * 32, vslot, row);
   };
-  if (tid == 0) issue_tma(0);
-  if (warp == 0) {
-    double tot = 0.0;
-    for (int64_t t = s_begin; t < s_end; t += C)
-      tot += warp_cumsum64(la, (b * p.L + t) * p.H + h, p.H, (int)imin64(C, s_end - t), 0.0, nullptr);
-    if (lane == 0) seg_total = tot;
+  if (tid == 0) {
+    issue_tma(0);
+    if (nsl > 1) issue_tma(1);
+  }
+  // segment total of la: all threads, fp64
+  __shared__ double wsum[8];
+  {
+    double part = 0.0;
+    for (int64_t t = s_begin + tid; t < s_end; t += NT2) part += (double)la[(b * p.L + t) * p.H + h];
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+    if (lane == 0) wsum[warp] = part;
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  double tot = 0.0;
+#pragma unroll
+  for (int w2 = 0; w2 < 8; ++w2) tot += wsum[w2];
+  const float Af = (float)tot;
+  if (tid == 0) Aseg[bh * p.nseg + seg] = Af;
   const uint32_t tmem = tmem_base;
   const uint32_t lb = (uint32_t)(qd * 32) << 16;
-  const float Af = (float)seg_total;
   double carry = 0.0;
   bool ok = true;
-  int tma_pending = 0;  // slice whose tiles are in flight (thread 0's view)
-  // warp 0: weights of slice n into buffer n & 1, continuing the running prefix
-  auto slice_weights = [&](int n) {
-    const int64_t t0 = s_begin + (int64_t)n * C;
-    const int len = (int)imin64(C, s_end - t0);
-    const double part = warp_cumsum64(la, (b * p.L + t0) * p.H + h, p.H, len, carry, cs);
-    __syncwarp();
-    float *sc = scb + (n & 1) * C;
-    for (int u = lane; u < C; u += 32) sc[u] = u < len ? expf(REV ? cs[u] : Af - cs[u]) : 0.f;
-    carry += part;
-    __syncwarp();
+  // all threads: weights of the 256 tokens from slice n on (one per thread),
+  // continuing the running in-segment prefix (fp64 block scan)
+  auto batch_weights = [&](int n) {
+    const int64_t t = s_begin + (int64_t)n * SL + tid;
+    double x = t < s_end ? (double)la[(b * p.L + t) * p.H + h] : 0.0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const double y = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += y;
+    }
+    if (lane == 31) wtot[warp] = x;
+    __syncthreads();
+    double before = carry, all = carry;
+#pragma unroll
+    for (int w2 = 0; w2 < 8; ++w2) {
+      if (w2 < warp) before += wtot[w2];
+      all += wtot[w2];
+    }
+    const float csf = (float)(before + x);
+    scb[tid] = t < s_end ? expf(REV ? csf : Af - csf) : 0.f;
+    carry = all;
+    __syncthreads();
   };
-  if (warp == 0) slice_weights(0);
 
   for (int n = 0; n < nsl; ++n) {
-    const int64_t t0 = s_begin + (int64_t)n * C;
-    const int len = (int)imin64(C, s_end - t0);
-    const float *sc = scb + (n & 1) * C;
-    ok = mbar_wait(&bar_tma, n & 1) && ok;
-    if (n >= 1) ok = mbar_wait(&bar_mma, (n - 1) & 1) && ok;
-    if (tid == 0 && ok) tma_pending = -1;
+    const int st = n & 1;
+    const int64_t t0 = s_begin + (int64_t)n * SL;
+    const int len = (int)imin64(SL, s_end - t0);
+    if ((n & 7) == 0) batch_weights(n);
+    const float *sc = scb + (n & 7) * SL;
+    const uint8_t *Xt = tiles + st * stage, *Yt = Xt + xbytes;
+    uint8_t *Bs = Bb + st * bbytes;
+    ok = mbar_wait(&bar_tma[st], (n >> 1) & 1) && ok;
+    if (tid == 0 && ok) pend[st] = -1;
+    if (n >= 2) ok = mbar_wait(&bar_mma[st], ((n >> 1) - 1) & 1) && ok;  // slice n-2 done
     if (__syncthreads_or(!ok)) break;
     tc_fence_after();
-    const int buf = n & 1;
-    {  // A operand: k'^T, lane = feature, tokens [32 hf, 32 hf + 32)
-      float v[32];
+    {  // A operand: k'^T, lane = feature, tokens [16 hf, 16 hf + 16)
+      float v[16];
 #pragma unroll
-      for (int uu = 0; uu < 32; ++uu) {
-        const int u = hf * 32 + uu;
-        v[uu] = (L < p.dk && u < len) ? tf32r(*(const float *)(Xt + sw128_off(u, L, C))) : 0.f;
+      for (int uu = 0; uu < 16; ++uu) {
+        const int u = hf * 16 + uu;
+        v[uu] = (L < p.dk && u < len) ? tf32r(*(const float *)(Xt + sw128_off(u, L, SL))) : 0.f;
       }
-      tmem_st32(tmem + lb + 128 + buf * 64 + hf * 32, v);
+      tmem_st16(tmem + lb + 128 + st * 32 + hf * 16, v);
     }
     if (L < p.dvn) {  // B operand: (sc v')^T, row = feature
 #pragma unroll
-      for (int uu = 0; uu < 32; uu += 4) {
-        const int u = hf * 32 + uu;
+      for (int uu = 0; uu < 16; uu += 4) {
+        const int u = hf * 16 + uu;
         float f[4];
 #pragma unroll
         for (int r = 0; r < 4; ++r)
-          f[r] = L < p.dv ? tf32r(*(const float *)(Yt + sw128_off(u + r, L, C)) * sc[u + r]) : 0.f;
-        *reinterpret_cast<float4 *>(Bb + sw128_off(L, u, p.dvn)) = make_float4(f[0], f[1], f[2], f[3]);
+          f[r] = L < p.dv ? tf32r(*(const float *)(Yt + sw128_off(u + r, L, SL)) * sc[u + r]) : 0.f;
+        *reinterpret_cast<float4 *>(Bs + sw128_off(L, u, p.dvn)) = make_float4(f[0], f[1], f[2], f[3]);
       }
     }
     tmem_st_wait();
@@ -227,21 +258,18 @@ __global__ void __launch_bounds__(NT2, 2) k_seg_state(const __grid_constant__ CU
     __syncthreads();
     tc_fence_after();
     if (tid == 0) {
-      if (n + 1 < nsl) {
-        issue_tma(n + 1);
-        tma_pending = n + 1;
-      }
-      const uint32_t bsm = smem_u32(Bb);
+      if (n + 2 < nsl) issue_tma(n + 2);  // this stage's tiles are consumed
+      const uint32_t bsm = smem_u32(Bs);
       const uint32_t id = idesc_tf32(128, p.dvn);
 #pragma unroll
-      for (int kk = 0; kk < C / 8; ++kk)
-        mma_ts(tmem, tmem + 128 + buf * 64 + kk * 8,
-               sdesc(bsm + (kk >> 2) * (p.dvn * 128) + (kk & 3) * 32), id, (n > 0 || kk > 0) ? 1u : 0u);
-      mma_commit(&bar_mma);
+      for (int kk = 0; kk < SL / 8; ++kk)
+        mma_ts(tmem, tmem + 128 + st * 32 + kk * 8, sdesc(bsm + kk * 32), id, (n > 0 || kk > 0) ? 1u : 0u);
+      mma_commit(&bar_mma[st]);
     }
-    if (warp == 0 && n + 1 < nsl) slice_weights(n + 1);
   }
-  if (ok) ok = mbar_wait(&bar_mma, (nsl - 1) & 1);
+  if (ok) {
+    for (int n = (nsl >= 2 ? nsl - 2 : 0); n < nsl; ++n) ok = mbar_wait(&bar_mma[n & 1], (n >> 1) & 1) && ok;
+  }
   const bool fail = __syncthreads_or(!ok);
   tc_fence_after();
   if (!fail) {
@@ -256,9 +284,10 @@ __global__ void __launch_bounds__(NT2, 2) k_seg_state(const __grid_constant__ CU
           if (c0 + jj < p.dv) dst[(int64_t)L * p.dv + c0 + jj] = v[jj];
       }
     }
-    if (tid == 0) Aseg[bh * p.nseg + seg] = Af;
-  } else if (tid == 0 && tma_pending >= 0) {
-    mbar_wait(&bar_tma, tma_pending & 1);
+  } else if (tid == 0) {
+    // tiles of up to two slices may still be in flight: wait for them
+    for (int st = 0; st < 2; ++st)
+      if (pend[st] >= 0) mbar_wait(&bar_tma[st], (pend[st] >> 1) & 1);
   }
   tc_fence_before();
   __syncthreads();
@@ -272,22 +301,26 @@ __global__ void __launch_bounds__(NT2, 2) k_seg_state(const __grid_constant__ CU
 //   anti-causal: st[s] <- state entering segment s from the right (0 for the
 //                last); the state left of segment 0 goes to fin (if given,
 //                written transposed when TRANS)
+// When stT is given, every result is also written there transposed.
 // grid (B*H, ceil(dk*dv / 128))
 template <bool REV, bool TRANS>
 __global__ void __launch_bounds__(NTH) k_seg_scan(float *__restrict__ st,
                                                   const float *__restrict__ Aseg,
                                                   const float *__restrict__ h0,
-                                                  float *__restrict__ fin, PassGeo p) {
+                                                  float *__restrict__ fin,
+                                                  float *__restrict__ stT, PassGeo p) {
   const int64_t bh = blockIdx.x;
   const int64_t e = (int64_t)blockIdx.y * NTH + threadIdx.x;
   const int64_t sz = (int64_t)p.dk * p.dv;
   if (e >= sz) return;
+  const int64_t et = (e % p.dv) * p.dk + e / p.dv;  // transposed position
   float *q = st + bh * p.nseg * sz + e;
+  float *qt = stT ? stT + bh * p.nseg * sz + et : nullptr;
   const float *a = Aseg + bh * p.nseg;
   constexpr int U = 8;  // segments loaded ahead of the dependent chain
   float run = 0.f;
   if (!REV) {
-    if (h0) run = TRANS ? h0[bh * sz + (e % p.dv) * p.dk + e / p.dv] : h0[bh * sz + e];
+    if (h0) run = TRANS ? h0[bh * sz + et] : h0[bh * sz + e];
     for (int s0 = 0; s0 < p.nseg; s0 += U) {
       float x[U], d[U];
 #pragma unroll
@@ -295,7 +328,11 @@ __global__ void __launch_bounds__(NTH) k_seg_scan(float *__restrict__ st,
         if (s0 + u < p.nseg) { x[u] = q[(int64_t)(s0 + u) * sz]; d[u] = expf(a[s0 + u]); }
 #pragma unroll
       for (int u = 0; u < U; ++u)
-        if (s0 + u < p.nseg) { q[(int64_t)(s0 + u) * sz] = run; run = fmaf(d[u], run, x[u]); }
+        if (s0 + u < p.nseg) {
+          q[(int64_t)(s0 + u) * sz] = run;
+          if (qt) qt[(int64_t)(s0 + u) * sz] = run;
+          run = fmaf(d[u], run, x[u]);
+        }
     }
   } else {
     for (int s0 = p.nseg - 1; s0 >= 0; s0 -= U) {
@@ -305,9 +342,13 @@ __global__ void __launch_bounds__(NTH) k_seg_scan(float *__restrict__ st,
         if (s0 - u >= 0) { x[u] = q[(int64_t)(s0 - u) * sz]; d[u] = expf(a[s0 - u]); }
 #pragma unroll
       for (int u = 0; u < U; ++u)
-        if (s0 - u >= 0) { q[(int64_t)(s0 - u) * sz] = run; run = fmaf(d[u], run, x[u]); }
+        if (s0 - u >= 0) {
+          q[(int64_t)(s0 - u) * sz] = run;
+          if (qt) qt[(int64_t)(s0 - u) * sz] = run;
+          run = fmaf(d[u], run, x[u]);
+        }
     }
-    if (fin) fin[bh * sz + (TRANS ? (e % p.dv) * p.dk + e / p.dv : e)] = run;
+    if (fin) fin[bh * sz + (TRANS ? et : e)] = run;
   }
 }
 
@@ -535,17 +576,22 @@ __global__ void __launch_bounds__(NT2, 2) k_walk(const __grid_constant__ CUtenso
     if (warp == 0 && ci + 1 < nc) chunk_factors(cnext, fb ^ 1);
     if (split) {
       // dcs[t] = y_t . (inter-chunk part of out'_t), reduced over the 128 lanes
+      float yv[32];
+      {
+        const int64_t ldy = (int64_t)(p.H / p.hpg) * dv;
+        const float *ys = oa.y + ((b * p.L + t0) * (p.H / p.hpg) + h / p.hpg) * (int64_t)dv + L;
+#pragma unroll
+        for (int tt = 0; tt < 32; ++tt) {
+          const int t = hf * 32 + tt;
+          yv[tt] = (L < dv && t < len) ? ys[t * ldy] : 0.f;
+        }
+      }
       ok = mbar_wait(&bar_i, ci & 1) && ok;
       tc_fence_after();
       float o[32];
       tmem_ld32(tmem + lb + hf * 32, o);
-      const int64_t ldy = (int64_t)(p.H / p.hpg) * dv;
-      const float *ys = oa.y + ((b * p.L + t0) * (p.H / p.hpg) + h / p.hpg) * (int64_t)dv + L;
 #pragma unroll
-      for (int tt = 0; tt < 32; ++tt) {
-        const int t = hf * 32 + tt;
-        o[tt] = (L < dv && t < len) ? o[tt] * ys[t * ldy] : 0.f;
-      }
+      for (int tt = 0; tt < 32; ++tt) o[tt] *= yv[tt];
 #pragma unroll
       for (int off = 16, n = 32; off >= 1; off >>= 1, n >>= 1) {
         const bool up = (lane & off) != 0;
@@ -629,11 +675,14 @@ __global__ void __launch_bounds__(NT2, 2) k_walk(const __grid_constant__ CUtenso
 }
 
 // ===========================================================================
-// Intra-chunk part of dlog_alpha, per (chunk, head):
+// Intra-chunk part of dlog_alpha, per (chunk, group), for each head h of the
+// group:
 //   B_t = sum_{t' >= t, s < t, both in the chunk} exp(cs_t' - cs_s) (q_t'.k_s)(dout_t'.v_s)
-// (the lower-left block of M = D o (q k^T) o (dout v^T) below row t, left of
-// column t).  Two score MMAs (M = 64) share one 2-tile shared-memory buffer.
-// grid (N chunks, H, B), 128 threads.
+// (the block of M = D o (q k^T) o (dout v^T) below row t and left of column
+// t).  q k^T is computed once; dout v^T per head.  Both score MMAs have M = 64
+// (rows 16w..16w+15 in lanes 32w..) and share one two-tile shared-memory
+// buffer; the next head's tiles load while the current head's sums run.
+// grid (N chunks, G, B), 128 threads, two CTAs per SM.
 __global__ void __launch_bounds__(NTH) k_dla_intra(const __grid_constant__ CUtensorMap tmQ,
                                                    const __grid_constant__ CUtensorMap tmK,
                                                    const __grid_constant__ CUtensorMap tmV,
@@ -646,16 +695,23 @@ __global__ void __launch_bounds__(NTH) k_dla_intra(const __grid_constant__ CUten
   const int ncbk = p.dkp / 32, ncbv = p.dvp / 32, ncbm = ncbk > ncbv ? ncbk : ncbv;
   uint8_t *T1 = smem, *T2 = smem + ncbm * 8192;
   float *R = (float *)(T2 + ncbm * 8192);  // [64][65]
-  float *cs = R + C * (C + 1);
+  float *cs = R + C * (C + 1);            // [64]
   __shared__ uint64_t bar_tma, bar_mma;
   __shared__ uint32_t tmem_base;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int64_t c = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const int64_t c = blockIdx.x, grp = blockIdx.y, b = blockIdx.z;
   const int64_t t0 = c * C;
   const int len = (int)imin64(C, p.L - t0);
-  const int grp = (int)(h / p.hpg);
   const int row = (int)(b * p.L + t0);
+  const int hpg = p.hpg;
 
+  auto load_dv = [&](int64_t h) {  // dout -> T1, v -> T2
+    mbar_expect_tx(&bar_tma, (uint32_t)(2 * ncbv) * 8192);
+    for (int cb = 0; cb < ncbv; ++cb) {
+      tma_load_3d(T1 + cb * 8192, &tmD, &bar_tma, cb * 32, (int)h, row);
+      tma_load_3d(T2 + cb * 8192, &tmV, &bar_tma, cb * 32, (int)h, row);
+    }
+  };
   if (warp == 0) tmem_alloc(&tmem_base, 128);
   if (tid == 0) {
     mbar_init(&bar_tma, 1);
@@ -663,21 +719,26 @@ __global__ void __launch_bounds__(NTH) k_dla_intra(const __grid_constant__ CUten
     fence_mbar_init();
     mbar_expect_tx(&bar_tma, (uint32_t)(2 * ncbk) * 8192);
     for (int cb = 0; cb < ncbk; ++cb) {
-      tma_load_3d(T1 + cb * 8192, &tmQ, &bar_tma, cb * 32, grp, row);
-      tma_load_3d(T2 + cb * 8192, &tmK, &bar_tma, cb * 32, grp, row);
+      tma_load_3d(T1 + cb * 8192, &tmQ, &bar_tma, cb * 32, (int)grp, row);
+      tma_load_3d(T2 + cb * 8192, &tmK, &bar_tma, cb * 32, (int)grp, row);
     }
   }
-  if (warp == 0) warp_cumsum64(la, (b * p.L + t0) * p.H + h, p.H, len, 0.0, cs);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_base;
   const uint32_t lb = (uint32_t)(warp * 32) << 16;
   bool ok = true;
-  for (int phase = 0; phase < 2; ++phase) {
-    const int ncb = phase == 0 ? ncbk : ncbv;
-    const int kdim = phase == 0 ? dk : dv;
-    ok = mbar_wait(&bar_tma, phase) && ok;
+  int pending = 1;  // loads in flight (thread 0's view)
+  float sq[C];
+  // phase 0: q k^T; phase 1 + hh: dout v^T of head hh
+  for (int ph = 0; ph <= hpg; ++ph) {
+    const int ncb = ph == 0 ? ncbk : ncbv;
+    const int kdim = ph == 0 ? dk : dv;
+    const int64_t h = grp * hpg + (ph == 0 ? 0 : ph - 1);
+    if (ph >= 1 && warp == 0) warp_cumsum64(la, (b * p.L + t0) * p.H + h, p.H, len, 0.0, cs);
+    ok = mbar_wait(&bar_tma, ph & 1) && ok;
+    if (tid == 0 && ok) pending = 0;
     if (__syncthreads_or(!ok)) break;
     {  // round both tiles to TF32 (nearest) in place
       const int r = tid & 63, half = tid >> 6;
@@ -696,28 +757,22 @@ __global__ void __launch_bounds__(NTH) k_dla_intra(const __grid_constant__ CUten
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (tid == 0) {  // phase 0: q k^T -> cols [0,64); phase 1: dout v^T -> [64,128)
+    if (tid == 0) {  // phase 0 -> cols [0,64); later phases -> [64,128)
       const uint32_t a = smem_u32(T1), bb = smem_u32(T2);
       const uint32_t id = idesc_tf32(64, 64);
       for (int kk = 0; kk < kdim / 8; ++kk) {
         const uint32_t off = (kk >> 2) * 8192 + (kk & 3) * 32;
-        mma_ss(tmem + phase * 64, sdesc(a + off), sdesc(bb + off), id, kk > 0 ? 1u : 0u);
+        mma_ss(tmem + (ph == 0 ? 0 : 64), sdesc(a + off), sdesc(bb + off), id, kk > 0 ? 1u : 0u);
       }
       mma_commit(&bar_mma);
     }
-    ok = mbar_wait(&bar_mma, phase) && ok;
+    ok = mbar_wait(&bar_mma, ph & 1) && ok;
     tc_fence_after();
-    if (phase == 0 && tid == 0 && ok) {  // the tiles are free: load dout and v
-      mbar_expect_tx(&bar_tma, (uint32_t)(2 * ncbv) * 8192);
-      for (int cb = 0; cb < ncbv; ++cb) {
-        tma_load_3d(T1 + cb * 8192, &tmD, &bar_tma, cb * 32, (int)h, row);
-        tma_load_3d(T2 + cb * 8192, &tmV, &bar_tma, cb * 32, (int)h, row);
-      }
+    if (tid == 0 && ok && ph < hpg) {  // the tiles are consumed: next head's loads
+      load_dv(grp * hpg + ph);
+      pending = 1;
     }
-  }
-  if (__syncthreads_or(!ok) == 0) {
-    float sq[C], dp[C];
-    {
+    if (ph == 0) {
       float t32[32];
       tmem_ld32(tmem + lb, t32);
 #pragma unroll
@@ -725,6 +780,11 @@ __global__ void __launch_bounds__(NTH) k_dla_intra(const __grid_constant__ CUten
       tmem_ld32(tmem + lb + 32, t32);
 #pragma unroll
       for (int u = 0; u < 32; ++u) sq[32 + u] = t32[u];
+      continue;
+    }
+    float dp[C];
+    {
+      float t32[32];
       tmem_ld32(tmem + lb + 64, t32);
 #pragma unroll
       for (int u = 0; u < 32; ++u) dp[u] = t32[u];
@@ -750,9 +810,9 @@ __global__ void __launch_bounds__(NTH) k_dla_intra(const __grid_constant__ CUten
       for (int r = tid; r < len; ++r) bsum += R[r * (C + 1) + tid];
       Bt[(b * p.L + t0 + tid) * p.H + h] = bsum;
     }
-  } else if (tid == 0) {
-    mbar_wait(&bar_tma, 1);  // a load may still be in flight
+    __syncthreads();  // R and cs are reused by the next head
   }
+  if (tid == 0 && pending) mbar_wait(&bar_tma, 0);  // best effort after a failure
   tc_fence_before();
   __syncthreads();
   if (warp == 0) tmem_dealloc(tmem, 128);
@@ -836,11 +896,12 @@ cudaError_t get_encoder() {
 }
 
 // 3-D view [rows, slots, d] of a row-major fp32 tensor; box = 32 features x
-// 1 slot x 64 rows, 128-byte swizzle, zero fill out of bounds.
-cudaError_t make_map(CUtensorMap *m, const float *base, int64_t rows, int64_t slots, int64_t d) {
+// 1 slot x box_rows rows, 128-byte swizzle, zero fill out of bounds.
+cudaError_t make_map(CUtensorMap *m, const float *base, int64_t rows, int64_t slots, int64_t d,
+                     int box_rows = C) {
   cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)slots, (cuuint64_t)rows};
   cuuint64_t strides[2] = {(cuuint64_t)(d * 4), (cuuint64_t)(slots * d * 4)};
-  cuuint32_t box[3] = {32, 1, (cuuint32_t)C};
+  cuuint32_t box[3] = {32, 1, (cuuint32_t)box_rows};
   cuuint32_t es[3] = {1, 1, 1};
   CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float *>(base), dims,
                         strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -889,7 +950,8 @@ size_t state_floats(const PassGeo &p) {
 }
 
 size_t seg_state_smem(const PassGeo &p) {
-  return (size_t)(p.dkp / 32 + p.dvp / 32) * 8192 + (size_t)p.dvn * 256 + 3 * C * 4 + 1024;
+  return (size_t)(p.dkp / 32 + p.dvp / 32) * 4096 * 2 + (size_t)rup(p.dvn * 128, 1024) * 2 +
+         NT2 * 4 + 1024;
 }
 size_t walk_smem(const PassGeo &p) {
   return (size_t)(p.dkp / 32) * 2 * 8192 + std::max(p.dvp / 32 * 8192, 16384) + 11 * C * 4 + 1024;
@@ -912,13 +974,13 @@ cudaError_t set_smem(K kern, size_t bytes) {
 template <bool REV>
 cudaError_t run_states(const PassGeo &p, const float *kp, const float *vp, const float *la,
                        const float *h0, bool trans, float *fin, float *states, float *Aseg,
-                       cudaStream_t s, const char *name_state) {
+                       float *statesT, cudaStream_t s, const char *name_state) {
   cudaError_t e;
   const int64_t rows = p.B * p.L;
   const int64_t G = p.H / p.hpg;
   CUtensorMap mk, mv;
-  if ((e = make_map(&mk, kp, rows, p.qk_per_head ? p.H : G, p.dk)) != cudaSuccess) return e;
-  if ((e = make_map(&mv, vp, rows, p.v_per_head ? p.H : G, p.dv)) != cudaSuccess) return e;
+  if ((e = make_map(&mk, kp, rows, p.qk_per_head ? p.H : G, p.dk, SL)) != cudaSuccess) return e;
+  if ((e = make_map(&mv, vp, rows, p.v_per_head ? p.H : G, p.dv, SL)) != cudaSuccess) return e;
   const dim3 grid((unsigned)p.nseg, (unsigned)p.H, (unsigned)p.B);
   {
     const size_t sm = seg_state_smem(p);
@@ -929,8 +991,8 @@ cudaError_t run_states(const PassGeo &p, const float *kp, const float *vp, const
   {
     LaunchTrace lt("tc.seg_scan", s);
     const dim3 sg((unsigned)(p.B * p.H), (unsigned)cdiv((int64_t)p.dk * p.dv, NTH));
-    if (trans) k_seg_scan<REV, true><<<sg, NTH, 0, s>>>(states, Aseg, h0, fin, p);
-    else k_seg_scan<REV, false><<<sg, NTH, 0, s>>>(states, Aseg, h0, fin, p);
+    if (trans) k_seg_scan<REV, true><<<sg, NTH, 0, s>>>(states, Aseg, h0, fin, statesT, p);
+    else k_seg_scan<REV, false><<<sg, NTH, 0, s>>>(states, Aseg, h0, fin, statesT, p);
   }
   return cudaGetLastError();
 }
@@ -974,12 +1036,12 @@ size_t fwd_workspace_bytes(const Geo &g) {
   return sizeof(float) * (state_floats(p) + (size_t)(g.B * g.H * p.nseg));
 }
 
-// Two passes' states (both kept for dlog_alpha) + their decays + three
-// per-token arrays.
+// Two passes' states (both kept for dlog_alpha) and a transposed copy of the
+// second, their decays, and three per-token arrays.
 size_t bwd_workspace_bytes(const Geo &g) {
   const PassGeo p = make_pass(g, (int)g.dk, (int)g.dv, false, true);
   const size_t nst = state_floats(p), na = (size_t)(g.B * g.H * p.nseg);
-  return sizeof(float) * (2 * nst + 2 * na + 3 * (size_t)(g.B * g.L * g.H)) + 256;
+  return sizeof(float) * (3 * nst + 2 * na + 3 * (size_t)(g.B * g.L * g.H)) + 256;
 }
 
 cudaError_t fwd(const float *q, const float *k, const float *v, const float *la, const float *h0,
@@ -990,7 +1052,7 @@ cudaError_t fwd(const float *q, const float *k, const float *v, const float *la,
   const PassGeo p = make_pass(g, (int)g.dk, (int)g.dv, false, true);
   float *st = static_cast<float *>(ws);
   float *Aseg = st + state_floats(p);
-  if ((e = run_states<false>(p, k, v, la, h0, false, nullptr, st, Aseg, s, "tc.seg_state")) != cudaSuccess)
+  if ((e = run_states<false>(p, k, v, la, h0, false, nullptr, st, Aseg, nullptr, s, "tc.seg_state")) != cudaSuccess)
     return e;
   OutArgs oa{out, (int)g.H, nullptr, nullptr};
   return run_walk<false>(p, q, k, v, la, st, false, oa, false, s, "tc.walk_out");
@@ -1008,12 +1070,13 @@ cudaError_t bwd(const float *q, const float *k, const float *v, const float *la,
   // dk_h = anti-causal scan(q' = v, k' = dout, v' = q)
   const PassGeo pb = make_pass(g, DV, DK, true, false);
   // dv = anti-causal scan(q' = k, k' = q, v' = dout).  Its states are the
-  // transposes of pass B's, and its leftmost state is dh0.
+  // transposes of pass B's (written by B's scan), and its leftmost state is dh0.
   const PassGeo pc = make_pass(g, DK, DV, false, true);
   const size_t nst = state_floats(pa), na = (size_t)(g.B * g.H * pa.nseg);
   float *stA = static_cast<float *>(ws);
   float *stB = stA + nst;
-  float *aA = stB + nst;
+  float *stC = stB + nst;  // pass B's states, transposed: pass C's states
+  float *aA = stC + nst;
   float *aB = aA + na;
   float *rq = aB + na;
   float *rk = rq + g.B * g.L * g.H;
@@ -1024,18 +1087,18 @@ cudaError_t bwd(const float *q, const float *k, const float *v, const float *la,
     if ((e = cudaMemsetAsync(dk, 0, sizeof(float) * g.B * g.L * g.G * g.dk, s)) != cudaSuccess) return e;
   }
   const int oslots = grouped ? (int)g.G : (int)g.H;
-  if ((e = run_states<false>(pa, v, k, la, h0, true, nullptr, stA, aA, s, "tc.seg_state_dq")) != cudaSuccess)
+  if ((e = run_states<false>(pa, v, k, la, h0, true, nullptr, stA, aA, nullptr, s, "tc.seg_state_dq")) != cudaSuccess)
     return e;
   OutArgs oq{dq, oslots, q, rq};
   if ((e = run_walk<false>(pa, dout, v, k, la, stA, false, oq, grouped, s, "tc.walk_dq")) != cudaSuccess)
     return e;
-  if ((e = run_states<true>(pb, dout, q, la, nullptr, true, dh0, stB, aB, s, "tc.seg_state_dk")) != cudaSuccess)
+  if ((e = run_states<true>(pb, dout, q, la, nullptr, true, dh0, stB, aB, stC, s, "tc.seg_state_dk")) != cudaSuccess)
     return e;
   OutArgs okk{dk, oslots, k, rk};
   if ((e = run_walk<true>(pb, v, dout, q, la, stB, false, okk, grouped, s, "tc.walk_dk")) != cudaSuccess)
     return e;
   OutArgs ov{dv, (int)g.H, nullptr, nullptr};
-  if ((e = run_walk<true>(pc, k, q, dout, la, stB, true, ov, false, s, "tc.walk_dv")) != cudaSuccess)
+  if ((e = run_walk<true>(pc, k, q, dout, la, stC, false, ov, false, s, "tc.walk_dv")) != cudaSuccess)
     return e;
   {  // intra-chunk block sums of dlog_alpha
     const PassGeo pi = make_pass(g, DK, DV, false, true);
@@ -1048,7 +1111,7 @@ cudaError_t bwd(const float *q, const float *k, const float *v, const float *la,
     const size_t sm = dla_intra_smem(pi);
     if ((e = set_smem(k_dla_intra, sm)) != cudaSuccess) return e;
     LaunchTrace lt("tc.dla_intra", s);
-    k_dla_intra<<<dim3((unsigned)g.N, (unsigned)g.H, (unsigned)g.B), NTH, sm, s>>>(mq, mk, mv, md,
+    k_dla_intra<<<dim3((unsigned)g.N, (unsigned)g.G, (unsigned)g.B), NTH, sm, s>>>(mq, mk, mv, md,
                                                                                   la, Bt, pi);
   }
   {  // pass A's states are S^T, pass B's are G^T: the carry is their plain dot
