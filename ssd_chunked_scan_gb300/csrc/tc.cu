@@ -273,16 +273,28 @@ __global__ void __launch_bounds__(NT2, 2) k_seg_state(const __grid_constant__ CU
   const bool fail = __syncthreads_or(!ok);
   tc_fence_after();
   if (!fail) {
-    float *dst = states + (bh * p.nseg + seg) * (int64_t)p.dk * p.dv;
+    // stage D [dk x dv] through the (now idle) tile buffers in the swizzled
+    // column-block layout, then write it out coalesced
+    uint8_t *Ds = tiles;  // needs dk * dvp * 4 <= 2 * stage bytes
+    const int dkr = rup(p.dk, 8);
     for (int c0 = hf * 64; c0 < hf * 64 + 64; c0 += 32) {
       if (c0 >= p.dvn) break;  // warp-uniform
       float v[32];
       tmem_ld32(tmem + lb + c0, v);
       if (L < p.dk) {
 #pragma unroll
-        for (int jj = 0; jj < 32; ++jj)
-          if (c0 + jj < p.dv) dst[(int64_t)L * p.dv + c0 + jj] = v[jj];
+        for (int jj = 0; jj < 32; jj += 4)
+          if (c0 + jj < p.dvp)
+            *reinterpret_cast<float4 *>(Ds + sw128_off(L, c0 + jj, dkr)) =
+                make_float4(v[jj], v[jj + 1], v[jj + 2], v[jj + 3]);
       }
+    }
+    __syncthreads();
+    float *dst = states + (bh * p.nseg + seg) * (int64_t)p.dk * p.dv;
+    const int n4 = p.dk * p.dv / 4;
+    for (int m = tid; m < n4; m += NT2) {
+      const int e = 4 * m, i = e / p.dv, j = e - i * p.dv;
+      *reinterpret_cast<float4 *>(dst + e) = *reinterpret_cast<const float4 *>(Ds + sw128_off(i, j, dkr));
     }
   } else if (tid == 0) {
     // tiles of up to two slices may still be in flight: wait for them
