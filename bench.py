@@ -51,6 +51,11 @@ def load_peaks():
                 "source": "fallback"}
 
 
+# DRAM bytes (read + write) per launch from one ncu capture of the kernel as it
+# stands (profiles/tc_g2h8_d128_L8192_long.md); kernels without a capture of
+# their current version report null
+TRAFFIC = {"tc.walk_dq": 418.697728e6 + 30.914304e6}
+
 # nominal dense tensor rates: tf32 1.1 PF vs bf16 2.25 PF per GPU
 TF32_OVER_BF16 = 1.1 / 2.25
 # FP32 FFMA: 152 SMs x 128 lanes x 2 flop x 2070 MHz (maximum SM clock)
@@ -253,7 +258,7 @@ def run_reference(args, w):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--path", default=os.environ.get("SSD_BENCH_PATH", "tc"), choices=["tc", "simt"])
@@ -419,7 +424,7 @@ def main():
         roof = {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "peak_note": f"{peaks['source']} copy bandwidth"}
     roof["frac"] = roof["achieved"] / roof["peak"]
-    roof["traffic"] = None
+    roof["traffic"] = TRAFFIC.get(top_name) if w.name == WORKLOAD else None
     roof["kernel"] = top_name
     roof["kernel_ms_per_launch"] = per_launch_ms
     roof["alg_bytes_per_launch"] = kb

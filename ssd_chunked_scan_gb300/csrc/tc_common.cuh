@@ -38,18 +38,19 @@ __device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes) {
                "r"(bytes)
                : "memory");
 }
-// Bounded wait for the phase with the given parity to complete.  Gives up
-// after ~2^31 SM clock cycles (about a second), records the failure in the
-// device error word and returns false.
+// Bounded wait for the phase with the given parity to complete.  Each
+// try_wait may park the warp for up to 20 us (suspend-time hint) instead of
+// spinning; the loop gives up after ~2^31 SM clock cycles (about a second),
+// records the failure in the device error word and returns false.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
   uint32_t ok = 0;
   const long long t0 = clock64();
   while (true) {
     asm volatile(
-        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
         " selp.u32 %0, 1, 0, p;\n}\n"
         : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(20000u)
         : "memory");
     if (ok) return true;
     if (clock64() - t0 > (1ll << 31)) {
