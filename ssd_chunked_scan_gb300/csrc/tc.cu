@@ -448,7 +448,7 @@ __global__ void __launch_bounds__(NT2, 2) k_walk(const __grid_constant__ CUtenso
     const int row = (int)(b * p.L + s_begin + (int64_t)c * C);
     for (int cb = 0; cb < ncbk; ++cb) tma_load_3d(Kb + cb * 8192, &tmK, &bar_tma, cb * 32, kslot, row);
   };
-  if (tid == 0) {
+  if (tid == 0 && !hseg_t) {
     tma_qv(REV ? nc - 1 : 0, 0);
     tma_k(REV ? nc - 1 : 0);
   }
@@ -473,14 +473,40 @@ __global__ void __launch_bounds__(NT2, 2) k_walk(const __grid_constant__ CUtenso
 
   {  // running state, transposed: lane j, column i = state[i][j]
     const float *H0 = Hseg + (bh * p.nseg + seg) * (int64_t)dk * dv;
-    for (int c0 = hf * 64; c0 < hf * 64 + 64 && c0 < rup(dk, 32); c0 += 32) {
-      float hv[32];
-#pragma unroll
-      for (int ii = 0; ii < 32; ++ii) {
-        const int i = c0 + ii;
-        hv[ii] = (L < dv && i < dk) ? (hseg_t ? H0[(int64_t)L * dk + i] : H0[(int64_t)i * dv + L]) : 0.f;
+    if (hseg_t) {
+      // the entering state is stored transposed ([dv x dk]): read it coalesced
+      // into the idle tile buffers ([dv rows x (dk + 1)]), then by rows
+      float *Ts = reinterpret_cast<float *>(Qb);
+      const int n = dv * dk;
+      for (int e = tid; e < n; e += NT2) {
+        const int r = e / dk, cc = e - r * dk;
+        Ts[r * (dk + 1) + cc] = H0[e];
       }
-      tmem_st32(tmem + lb + 128 + c0, hv);
+      __syncthreads();
+      for (int c0 = hf * 64; c0 < hf * 64 + 64 && c0 < rup(dk, 32); c0 += 32) {
+        float hv[32];
+#pragma unroll
+        for (int ii = 0; ii < 32; ++ii) {
+          const int i = c0 + ii;
+          hv[ii] = (L < dv && i < dk) ? Ts[L * (dk + 1) + i] : 0.f;
+        }
+        tmem_st32(tmem + lb + 128 + c0, hv);
+      }
+      __syncthreads();  // the tile buffers are about to receive the first loads
+      if (tid == 0) {
+        tma_qv(REV ? nc - 1 : 0, 0);
+        tma_k(REV ? nc - 1 : 0);
+      }
+    } else {
+      for (int c0 = hf * 64; c0 < hf * 64 + 64 && c0 < rup(dk, 32); c0 += 32) {
+        float hv[32];
+#pragma unroll
+        for (int ii = 0; ii < 32; ++ii) {
+          const int i = c0 + ii;
+          hv[ii] = (L < dv && i < dk) ? H0[(int64_t)i * dv + L] : 0.f;
+        }
+        tmem_st32(tmem + lb + 128 + c0, hv);
+      }
     }
     tmem_st_wait();
   }
@@ -845,44 +871,51 @@ __global__ void __launch_bounds__(DT) k_dla(const float *__restrict__ Bt,
                                             const float *__restrict__ Gst,
                                             const float *__restrict__ Sst, float *__restrict__ dla,
                                             int64_t L, int64_t H, int64_t sz, int Ls, int nseg) {
-  __shared__ double sh[DT];
-  __shared__ double carry_in;
-  const int tid = threadIdx.x;
+  __shared__ double wred[DT / 32];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int64_t seg = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int64_t bh = b * H + h;
-  double acc = 0.0;
+  // carry = <G_end, S_end>: float4 loads, fp32 partial sums, fp64 across threads
+  float part = 0.f;
   if (seg + 1 < nseg) {
-    const float *G = Gst + (bh * nseg + seg) * sz;
-    const float *S = Sst + (bh * nseg + seg + 1) * sz;
-    for (int64_t e = tid; e < sz; e += DT) acc += (double)G[e] * (double)S[e];
+    const float4 *G = reinterpret_cast<const float4 *>(Gst + (bh * nseg + seg) * sz);
+    const float4 *S = reinterpret_cast<const float4 *>(Sst + (bh * nseg + seg + 1) * sz);
+    for (int64_t e = tid; e < sz / 4; e += DT) {
+      const float4 g = G[e], x = S[e];
+      part = fmaf(g.x, x.x, fmaf(g.y, x.y, fmaf(g.z, x.z, fmaf(g.w, x.w, part))));
+    }
   }
-  sh[tid] = acc;
+  double dp = part;
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) dp += __shfl_xor_sync(0xffffffffu, dp, o);
+  if (lane == 0) wred[warp] = dp;
   __syncthreads();
-  for (int o = DT / 2; o > 0; o >>= 1) {
-    if (tid < o) sh[tid] += sh[tid + o];
-    __syncthreads();
-  }
-  if (tid == 0) carry_in = sh[0];
+  double carry = 0.0;
+#pragma unroll
+  for (int w2 = 0; w2 < DT / 32; ++w2) carry += wred[w2];
   __syncthreads();
+  // suffix sums of rq - rk over the segment, 256 tokens at a time from its end
   const int64_t s_begin = seg * (int64_t)Ls;
   const int64_t s_end = imin64(L, s_begin + Ls);
   for (int64_t hi = s_end; hi > s_begin; hi -= DT) {
-    const int64_t lo = hi - DT > s_begin ? hi - DT : s_begin;
-    const int64_t t = lo + tid;
-    double x = 0.0;
-    if (t < hi) x = (double)rq[(b * L + t) * H + h] - (double)rk[(b * L + t) * H + h];
-    __syncthreads();
-    sh[tid] = x;
-    __syncthreads();
-    for (int o = 1; o < DT; o <<= 1) {  // inclusive suffix sums
-      const double y = (tid + o < DT) ? sh[tid + o] : 0.0;
-      __syncthreads();
-      sh[tid] += y;
-      __syncthreads();
+    const int64_t t = hi - DT + tid;  // thread tid owns token t (valid if t >= s_begin)
+    const bool ok = t >= s_begin;
+    const int64_t idx = (b * L + t) * H + h;
+    double x = ok ? (double)rq[idx] - (double)rk[idx] : 0.0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {  // inclusive suffix within the warp
+      const double y = __shfl_down_sync(0xffffffffu, x, o);
+      if (lane + o < 32) x += y;
     }
-    if (t < hi) dla[(b * L + t) * H + h] = (float)((double)Bt[(b * L + t) * H + h] + sh[tid] + carry_in);
+    if (lane == 0) wred[warp] = x;  // warp total
     __syncthreads();
-    if (tid == 0) carry_in += sh[0];
+    double after = carry;  // everything right of this warp
+#pragma unroll
+    for (int w2 = 0; w2 < DT / 32; ++w2)
+      if (w2 > warp) after += wred[w2];
+    if (ok) dla[idx] = (float)((double)Bt[idx] + x + after);
+#pragma unroll
+    for (int w2 = 0; w2 < DT / 32; ++w2) carry += wred[w2];
     __syncthreads();
   }
 }
@@ -1048,12 +1081,12 @@ size_t fwd_workspace_bytes(const Geo &g) {
   return sizeof(float) * (state_floats(p) + (size_t)(g.B * g.H * p.nseg));
 }
 
-// Two passes' states (both kept for dlog_alpha) and a transposed copy of the
-// second, their decays, and three per-token arrays.
+// Two passes' states (both kept for dlog_alpha), their decays, and three
+// per-token arrays.
 size_t bwd_workspace_bytes(const Geo &g) {
   const PassGeo p = make_pass(g, (int)g.dk, (int)g.dv, false, true);
   const size_t nst = state_floats(p), na = (size_t)(g.B * g.H * p.nseg);
-  return sizeof(float) * (3 * nst + 2 * na + 3 * (size_t)(g.B * g.L * g.H)) + 256;
+  return sizeof(float) * (2 * nst + 2 * na + 3 * (size_t)(g.B * g.L * g.H)) + 256;
 }
 
 cudaError_t fwd(const float *q, const float *k, const float *v, const float *la, const float *h0,
@@ -1082,13 +1115,13 @@ cudaError_t bwd(const float *q, const float *k, const float *v, const float *la,
   // dk_h = anti-causal scan(q' = v, k' = dout, v' = q)
   const PassGeo pb = make_pass(g, DV, DK, true, false);
   // dv = anti-causal scan(q' = k, k' = q, v' = dout).  Its states are the
-  // transposes of pass B's (written by B's scan), and its leftmost state is dh0.
+  // transposes of pass B's (read transposed by its walk), and its leftmost
+  // state is dh0.
   const PassGeo pc = make_pass(g, DK, DV, false, true);
   const size_t nst = state_floats(pa), na = (size_t)(g.B * g.H * pa.nseg);
   float *stA = static_cast<float *>(ws);
   float *stB = stA + nst;
-  float *stC = stB + nst;  // pass B's states, transposed: pass C's states
-  float *aA = stC + nst;
+  float *aA = stB + nst;
   float *aB = aA + na;
   float *rq = aB + na;
   float *rk = rq + g.B * g.L * g.H;
@@ -1104,13 +1137,13 @@ cudaError_t bwd(const float *q, const float *k, const float *v, const float *la,
   OutArgs oq{dq, oslots, q, rq};
   if ((e = run_walk<false>(pa, dout, v, k, la, stA, false, oq, grouped, s, "tc.walk_dq")) != cudaSuccess)
     return e;
-  if ((e = run_states<true>(pb, dout, q, la, nullptr, true, dh0, stB, aB, stC, s, "tc.seg_state_dk")) != cudaSuccess)
+  if ((e = run_states<true>(pb, dout, q, la, nullptr, true, dh0, stB, aB, nullptr, s, "tc.seg_state_dk")) != cudaSuccess)
     return e;
   OutArgs okk{dk, oslots, k, rk};
   if ((e = run_walk<true>(pb, v, dout, q, la, stB, false, okk, grouped, s, "tc.walk_dk")) != cudaSuccess)
     return e;
   OutArgs ov{dv, (int)g.H, nullptr, nullptr};
-  if ((e = run_walk<true>(pc, k, q, dout, la, stC, false, ov, false, s, "tc.walk_dv")) != cudaSuccess)
+  if ((e = run_walk<true>(pc, k, q, dout, la, stB, true, ov, false, s, "tc.walk_dv")) != cudaSuccess)
     return e;
   {  // intra-chunk block sums of dlog_alpha
     const PassGeo pi = make_pass(g, DK, DV, false, true);
