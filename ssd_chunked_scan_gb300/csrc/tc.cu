@@ -448,6 +448,7 @@ __global__ void __launch_bounds__(NT2, 2) k_walk(const __grid_constant__ CUtenso
     const int row = (int)(b * p.L + s_begin + (int64_t)c * C);
     for (int cb = 0; cb < ncbk; ++cb) tma_load_3d(Kb + cb * 8192, &tmK, &bar_tma, cb * 32, kslot, row);
   };
+
   if (tid == 0 && !hseg_t) {
     tma_qv(REV ? nc - 1 : 0, 0);
     tma_k(REV ? nc - 1 : 0);
@@ -513,6 +514,22 @@ __global__ void __launch_bounds__(NT2, 2) k_walk(const __grid_constant__ CUtenso
 
   bool ok = true;
   const bool split = oa.dcs != nullptr;
+  // The resident state is kept as Hs with the true state = alpha * Hs.  While
+  // alpha stays in [2^-40, 2^40] a chunk's decay is folded into alpha (the
+  // inter term scales q' by alpha, the update scales w k' by 1 / alpha), so
+  // the update MMA issues with the output MMAs and no rescale pass runs;
+  // otherwise the threads rescale Hs explicitly and alpha returns to 1.
+  float alpha = 1.f;
+  int hphase = 0;  // completions of bar_h so far (the explicit path only)
+  // HT += v'^T (w k')   (M = dv lanes, N = dkn, K = 64 tokens); thread 0
+  auto issue_update = [&]() {
+    const uint32_t kwa = smem_u32(Kb);
+    const uint32_t id = idesc_tf32(128, dkn);
+#pragma unroll
+    for (int kk = 0; kk < C / 8; ++kk)
+      mma_ts(tmem + 128, tmem + 64 + kk * 8, sdesc(kwa + (kk >> 2) * (dkn * 128) + (kk & 3) * 32),
+             id, 1u);
+  };
   for (int ci = 0; ci < nc; ++ci) {
     const int c = REV ? nc - 1 - ci : ci;
     const int64_t t0 = s_begin + (int64_t)c * C;
@@ -528,6 +545,9 @@ __global__ void __launch_bounds__(NT2, 2) k_walk(const __grid_constant__ CUtenso
     // inter-term factor of a query row, state-update weight of a key column
     const float *interf = REV ? ww : ew;
     const float *statew = REV ? ew : ww;
+    const float a_c = a_chunk[fb], an = alpha * a_c;
+    const bool lazy = a_c >= 0x1p-30f && an >= 0x1p-40f && an <= 0x1p40f;
+    const float kscale = lazy ? 1.f / an : 1.f;
     if (tid == 0) {  // S = q' k'^T (M = 64, N = 64, K = dk)
       const uint32_t qa = smem_u32(Qb), ka = smem_u32(Kb);
       const uint32_t id = idesc_tf32(64, 64);
@@ -550,7 +570,7 @@ __global__ void __launch_bounds__(NT2, 2) k_walk(const __grid_constant__ CUtenso
 #pragma unroll
     for (int uu = 0; uu < 32; ++uu) {
       const int u = hf * 32 + uu;
-      kw[uu] = (L < dk) ? tf32r(*(const float *)(Kb + sw128_off(u, L, C)) * statew[u]) : 0.f;
+      kw[uu] = (L < dk) ? tf32r(*(const float *)(Kb + sw128_off(u, L, C)) * (statew[u] * kscale)) : 0.f;
     }
     ok = mbar_wait(&bar_s, ci & 1) && ok;
     tc_fence_after();
@@ -582,7 +602,7 @@ __global__ void __launch_bounds__(NT2, 2) k_walk(const __grid_constant__ CUtenso
     }
     {  // q' rows scaled by the inter-term factor, in place (4 threads per row)
       const int r = tid & 63, part = tid >> 6;
-      const float e = interf[r];
+      const float e = interf[r] * alpha;
       const int cols = p.dkp / 4;
       for (int col = part * cols; col < (part + 1) * cols; col += 4) {
         float4 *q4 = reinterpret_cast<float4 *>(Qb + sw128_off(r, col, C));
@@ -608,6 +628,7 @@ __global__ void __launch_bounds__(NT2, 2) k_walk(const __grid_constant__ CUtenso
 #pragma unroll
         for (int kk = 0; kk < C / 8; ++kk)
           mma_ts(tmem, tmem + 64 + kk * 8, sdesc(pa + (kk >> 2) * 8192 + (kk & 3) * 32), id, 1u);
+        if (lazy) issue_update();
         mma_commit(&bar_o);
       }
     }
@@ -628,6 +649,20 @@ __global__ void __launch_bounds__(NT2, 2) k_walk(const __grid_constant__ CUtenso
       tc_fence_after();
       float o[32];
       tmem_ld32(tmem + lb + hf * 32, o);
+      // every thread has its inter part: let the intra MMA accumulate on top
+      // while the dot products are reduced
+      tc_fence_before();
+      __syncthreads();
+      tc_fence_after();
+      if (tid == 0) {  // + v'^T P^T
+        const uint32_t pa = smem_u32(Vb);
+        const uint32_t id = idesc_tf32(128, 64);
+#pragma unroll
+        for (int kk = 0; kk < C / 8; ++kk)
+          mma_ts(tmem, tmem + 64 + kk * 8, sdesc(pa + (kk >> 2) * 8192 + (kk & 3) * 32), id, 1u);
+        if (lazy) issue_update();
+        mma_commit(&bar_o);
+      }
 #pragma unroll
       for (int tt = 0; tt < 32; ++tt) o[tt] *= yv[tt];
 #pragma unroll
@@ -641,24 +676,17 @@ __global__ void __launch_bounds__(NT2, 2) k_walk(const __grid_constant__ CUtenso
         }
       }
       red[qd * C + hf * 32 + lane] = o[0];
-      tc_fence_before();
       __syncthreads();
-      tc_fence_after();
       if (tid < len)
         oa.dcs[(b * p.L + t0 + tid) * p.H + h] = red[tid] + red[C + tid] + red[2 * C + tid] + red[3 * C + tid];
-      if (tid == 0) {  // + v'^T P^T
-        const uint32_t pa = smem_u32(Vb);
-        const uint32_t id = idesc_tf32(128, 64);
-#pragma unroll
-        for (int kk = 0; kk < C / 8; ++kk)
-          mma_ts(tmem, tmem + 64 + kk * 8, sdesc(pa + (kk >> 2) * 8192 + (kk & 3) * 32), id, 1u);
-        mma_commit(&bar_o);
-      }
     }
     ok = mbar_wait(&bar_o, ci & 1) && ok;
     tc_fence_after();
-    // q' and v' tiles are free now: start the next chunk's loads
-    if (tid == 0 && ok && ci + 1 < nc) tma_qv(cnext, ci + 1);
+    // q' and v' tiles are free now (and k' too when the update ran): next loads
+    if (tid == 0 && ok && ci + 1 < nc) {
+      tma_qv(cnext, ci + 1);
+      if (lazy) tma_k(cnext);
+    }
     {
       float o[32];
       tmem_ld32(tmem + lb + hf * 32, o);
@@ -675,32 +703,31 @@ __global__ void __launch_bounds__(NT2, 2) k_walk(const __grid_constant__ CUtenso
         }
       }
     }
-    {  // HT <- exp(A_c) HT, before the state-update MMA accumulates into it
-      const float a = a_chunk[fb];
+    if (lazy) {
+      alpha = an;
+    } else {
+      // Hs <- alpha exp(A_c) Hs (the true state, decayed), then the update
       for (int c0 = hf * 64; c0 < hf * 64 + 64 && c0 < rup(dk, 32); c0 += 32) {
         float hv[32];
         tmem_ld32(tmem + lb + 128 + c0, hv);
 #pragma unroll
-        for (int ii = 0; ii < 32; ++ii) hv[ii] *= a;
+        for (int ii = 0; ii < 32; ++ii) hv[ii] *= an;
         tmem_st32(tmem + lb + 128 + c0, hv);
       }
       tmem_st_wait();
+      tc_fence_before();
+      __syncthreads();
+      tc_fence_after();
+      if (tid == 0) {
+        issue_update();
+        mma_commit(&bar_h);
+      }
+      ok = mbar_wait(&bar_h, hphase & 1) && ok;
+      ++hphase;
+      tc_fence_after();
+      if (tid == 0 && ok && ci + 1 < nc) tma_k(cnext);
+      alpha = 1.f;
     }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    if (tid == 0) {  // HT += v'^T (w k')   (M = dv lanes, N = dkn, K = 64 tokens)
-      const uint32_t kwa = smem_u32(Kb);
-      const uint32_t id = idesc_tf32(128, dkn);
-#pragma unroll
-      for (int kk = 0; kk < C / 8; ++kk)
-        mma_ts(tmem + 128, tmem + 64 + kk * 8, sdesc(kwa + (kk >> 2) * (dkn * 128) + (kk & 3) * 32),
-               id, 1u);
-      mma_commit(&bar_h);
-    }
-    ok = mbar_wait(&bar_h, ci & 1) && ok;
-    tc_fence_after();
-    if (tid == 0 && ok && ci + 1 < nc) tma_k(cnext);
     tc_fence_before();
     if (__syncthreads_or(!ok)) break;
     tc_fence_after();
