@@ -38,3 +38,29 @@ def ssd_fwd_brute(q, k, v, la, h0=None):
                     acc += math.exp(e) * (np.asarray(h0, np.float64)[b, h].T @ q[b, t, g])
                 out[b, t, h] = acc
     return out
+
+
+def ssd_final_state_brute(k, v, la, h0=None):
+    """hT = sum_s exp(sum_{r=s+1..L-1} la_r) k_s v_s^T + exp(sum_{r<=L-1} la_r) h0,
+    per (b, h), each exponent summed directly.  [B,H,dk,dv]"""
+    k, v, la = (np.asarray(x, np.float64) for x in (k, v, la))
+    B, L, G, dk = k.shape
+    H, dv = v.shape[2], v.shape[3]
+    hpg = H // G
+    hT = np.zeros((B, H, dk, dv))
+    for b in range(B):
+        for h in range(H):
+            g = h // hpg
+            acc = np.zeros((dk, dv))
+            for s in range(L):
+                e = 0.0
+                for r in range(s + 1, L):
+                    e += la[b, r, h]
+                acc += math.exp(e) * np.outer(k[b, s, g], v[b, s, h])
+            if h0 is not None:
+                e = 0.0
+                for r in range(L):
+                    e += la[b, r, h]
+                acc += math.exp(e) * np.asarray(h0, np.float64)[b, h]
+            hT[b, h] = acc
+    return hT

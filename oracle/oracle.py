@@ -30,9 +30,9 @@ def _load():
         lib = ctypes.CDLL(path)
         d = ctypes.POINTER(ctypes.c_double)
         i64 = ctypes.c_int64
-        lib.ssd_oracle_fwd.argtypes = [d, d, d, d, d, d] + [i64] * 6
+        lib.ssd_oracle_fwd.argtypes = [d, d, d, d, d, d, d] + [i64] * 6
         lib.ssd_oracle_fwd.restype = ctypes.c_int
-        lib.ssd_oracle_bwd.argtypes = [d] * 13 + [i64] * 6
+        lib.ssd_oracle_bwd.argtypes = [d] * 14 + [i64] * 6
         lib.ssd_oracle_bwd.restype = ctypes.c_int
         lib.ssd_oracle_num_threads.argtypes = []
         lib.ssd_oracle_num_threads.restype = ctypes.c_int
@@ -67,28 +67,34 @@ def _dims(q, v, la):
     return B, L, G, H, dk, dv
 
 
-def ssd_fwd_ref(q, k, v, log_alpha, h0=None):
-    """out [B,L,H,dv] (float64) for q,k [B,L,G,dk], v [B,L,H,dv], log_alpha [B,L,H]."""
+def ssd_fwd_ref(q, k, v, log_alpha, h0=None, return_final_state=False):
+    """out [B,L,H,dv] (float64) for q,k [B,L,G,dk], v [B,L,H,dv], log_alpha [B,L,H].
+
+    With ``return_final_state`` also returns hT = S_{L-1} [B,H,dk,dv]."""
     q, k, v, la, h0 = map(_f64, (q, k, v, log_alpha, h0))
     B, L, G, H, dk, dv = _dims(q, v, la)
     assert k.shape == q.shape
     if h0 is not None:
         assert h0.shape == (B, H, dk, dv)
     out = np.zeros((B, L, H, dv), np.float64)
+    hT = np.zeros((B, H, dk, dv), np.float64) if return_final_state else None
+    if hT is not None and L == 0 and h0 is not None:
+        hT[...] = h0
     rc = _load().ssd_oracle_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(la), _ptr(h0), _ptr(out),
-                                B, L, G, H, dk, dv)
+                                _ptr(hT) if L > 0 else _ptr(None), B, L, G, H, dk, dv)
     if rc:
         raise RuntimeError(f"oracle fwd failed ({rc})")
-    return out
+    return (out, hT) if return_final_state else out
 
 
-def ssd_bwd_ref(q, k, v, log_alpha, h0, dout, per_head=False):
-    """Gradients of <dout, out>: dict with dq, dk, dv, dlog_alpha, dh0 (float64).
+def ssd_bwd_ref(q, k, v, log_alpha, h0, dout, per_head=False, dhT=None):
+    """Gradients of <dout, out> (+ <dhT, hT> when dhT is given): dict with dq,
+    dk, dv, dlog_alpha, dh0 (float64).
 
     With ``per_head=True`` also returns dq_heads / dk_heads [B,L,H,dk], the
     per-head contributions before the sum over the heads of each group.
     """
-    q, k, v, la, h0, dout = map(_f64, (q, k, v, log_alpha, h0, dout))
+    q, k, v, la, h0, dout, dhT = map(_f64, (q, k, v, log_alpha, h0, dout, dhT))
     B, L, G, H, dk, dv = _dims(q, v, la)
     assert k.shape == q.shape and dout.shape == v.shape
     r = {
@@ -98,12 +104,16 @@ def ssd_bwd_ref(q, k, v, log_alpha, h0, dout, per_head=False):
     }
     dqh = np.zeros((B, L, H, dk)) if per_head else None
     dkh = np.zeros((B, L, H, dk)) if per_head else None
+    if dhT is not None:
+        assert dhT.shape == (B, H, dk, dv)
     rc = _load().ssd_oracle_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(la), _ptr(h0), _ptr(dout),
-                                _ptr(r["dq"]), _ptr(r["dk"]), _ptr(r["dv"]),
+                                _ptr(dhT), _ptr(r["dq"]), _ptr(r["dk"]), _ptr(r["dv"]),
                                 _ptr(r["dlog_alpha"]), _ptr(r["dh0"]), _ptr(dqh), _ptr(dkh),
                                 B, L, G, H, dk, dv)
     if rc:
         raise RuntimeError(f"oracle bwd failed ({rc})")
+    if L == 0 and dhT is not None:
+        r["dh0"][...] = dhT
     if per_head:
         r["dq_heads"], r["dk_heads"] = dqh, dkh
     return r

@@ -29,9 +29,14 @@
  * states inside each checkpoint segment (never by dividing out a decay).
  * dla uses the direct adjoint above, not a cumulative-sum identity.
  *
+ * Optionally the forward also returns the final state hT = S_{L-1} and the
+ * backward takes its cotangent dhT (loss <dout, out> + <dhT, hT>): the
+ * adjoint then starts from G_{L-1} = q_{L-1} dout_{L-1}^T + dhT.
+ *
  * Layouts (row-major, the benchmark records' argument sizes):
- *   q, k [B,L,G,dk]   v, out [B,L,H,dv]   la [B,L,H]   h0, dh0 [B,H,dk,dv]
- * h0 may be NULL (zeros); dh0, dq_heads, dk_heads may be NULL (not wanted).
+ *   q, k [B,L,G,dk]   v, out [B,L,H,dv]   la [B,L,H]   h0, dh0, hT, dhT [B,H,dk,dv]
+ * h0 and dhT may be NULL (zeros); dh0, hT, dq_heads, dk_heads may be NULL
+ * (not wanted).
  * dq_heads / dk_heads [B,L,H,dk] receive the per-head, pre-group-sum
  * gradients when given.
  */
@@ -66,7 +71,7 @@ int ssd_oracle_num_threads(void) {
 }
 
 int ssd_oracle_fwd(const double *q, const double *k, const double *v,
-                   const double *la, const double *h0, double *out,
+                   const double *la, const double *h0, double *out, double *hT,
                    int64_t B, int64_t L, int64_t G, int64_t H, int64_t dk,
                    int64_t dv) {
   if (B < 0 || L < 0 || G <= 0 || H <= 0 || dk <= 0 || dv <= 0 || H % G)
@@ -94,6 +99,7 @@ int ssd_oracle_fwd(const double *q, const double *k, const double *v,
         for (int64_t j = 0; j < dv; ++j) ot[j] += qi * row[j];
       }
     }
+    if (hT) memcpy(hT + bh * dk * dv, S, sizeof(double) * dk * dv);
     free(S);
   }
   return err;
@@ -101,6 +107,7 @@ int ssd_oracle_fwd(const double *q, const double *k, const double *v,
 
 int ssd_oracle_bwd(const double *q, const double *k, const double *v,
                    const double *la, const double *h0, const double *dout,
+                   const double *dhT,
                    double *dq, double *dk_out, double *dv_out, double *dla,
                    double *dh0, double *dq_heads, double *dk_heads,
                    int64_t B, int64_t L, int64_t G, int64_t H, int64_t dk,
@@ -123,6 +130,7 @@ int ssd_oracle_bwd(const double *q, const double *k, const double *v,
     double *seg = (double *)malloc(sizeof(double) * sz * (CKPT + 1));
     double *Gs = (double *)calloc((size_t)sz, sizeof(double));
     if (!ck || !seg || !Gs) { err = 2; free(ck); free(seg); free(Gs); continue; }
+    if (dhT) memcpy(Gs, dhT + bh * sz, sizeof(double) * sz);
     double *S = seg; /* scratch for the forward sweep */
     if (h0) memcpy(S, h0 + bh * sz, sizeof(double) * sz);
     else memset(S, 0, sizeof(double) * sz);

@@ -170,3 +170,79 @@ def test_checkpoint_boundaries():
             la[0, t, 0] = old
             fd = (lp - lm) / 2e-6
             assert abs(fd - g["dlog_alpha"][0, t, 0]) <= 1e-6 * max(1.0, abs(fd))
+
+
+# ---- final state hT and its cotangent dhT ---------------------------------
+
+def test_final_state_matches_unrolled_sums():
+    from oracle.brute import ssd_final_state_brute
+    q, k, v, la, h0, _ = _case(2, 23, 2, 4, 5, 3, seed=31)
+    la = la * 0.3
+    _, hT = ssd_fwd_ref(q, k, v, la, h0, return_final_state=True)
+    assert rel_err(hT, ssd_final_state_brute(k, v, la, h0)) < 1e-12
+
+
+def test_sequence_split_carries_the_state():
+    # running [0, L1) then [L1, L) from the first part's final state equals
+    # one run over [0, L)
+    q, k, v, la, h0, _ = _case(2, 150, 2, 4, 6, 5, seed=32)
+    out, hT = ssd_fwd_ref(q, k, v, la, h0, return_final_state=True)
+    L1 = 61
+    o1, h1 = ssd_fwd_ref(q[:, :L1], k[:, :L1], v[:, :L1], la[:, :L1], h0, return_final_state=True)
+    o2, h2 = ssd_fwd_ref(q[:, L1:], k[:, L1:], v[:, L1:], la[:, L1:], h1, return_final_state=True)
+    np.testing.assert_allclose(np.concatenate([o1, o2], 1), out, rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(h2, hT, rtol=1e-12, atol=1e-13)
+
+
+def _loss_T(q, k, v, la, h0, dout, dhT):
+    out, hT = ssd_fwd_ref(q, k, v, la, h0, return_final_state=True)
+    return float(np.sum(out * dout) + np.sum(hT * dhT))
+
+
+def test_grads_with_final_state_cotangent_match_central_differences():
+    B, L, G, H, dk, dv = 2, 9, 2, 4, 4, 3
+    q, k, v, la, h0, dout = (x.astype(np.float64) for x in _case(B, L, G, H, dk, dv, seed=33))
+    dhT = np.random.default_rng(5).standard_normal((B, H, dk, dv))
+    g = ssd_bwd_ref(q, k, v, la, h0, dout, dhT=dhT)
+    eps = 1e-6
+    rng = np.random.default_rng(1)
+    for name, x in {"dq": q, "dk": k, "dv": v, "dlog_alpha": la, "dh0": h0}.items():
+        flat = x.reshape(-1)
+        for i in rng.choice(flat.size, size=min(flat.size, 20), replace=False):
+            old = flat[i]
+            flat[i] = old + eps
+            lp = _loss_T(q, k, v, la, h0, dout, dhT)
+            flat[i] = old - eps
+            lm = _loss_T(q, k, v, la, h0, dout, dhT)
+            flat[i] = old
+            fd = (lp - lm) / (2 * eps)
+            an = g[name].reshape(-1)[i]
+            assert abs(fd - an) <= 1e-7 * max(1.0, abs(an)), (name, i, fd, an)
+
+
+def test_euler_identity_with_final_state():
+    # out and hT are both homogeneous of degree 1 in (v, h0) jointly
+    q, k, v, la, h0, dout = _case(2, 140, 2, 4, 6, 5, seed=34)
+    dhT = np.random.default_rng(6).standard_normal(h0.shape)
+    out, hT = ssd_fwd_ref(q, k, v, la, h0, return_final_state=True)
+    g = ssd_bwd_ref(q, k, v, la, h0, dout, dhT=dhT)
+    f = lambda x: np.asarray(x, np.float64)
+    total = float(np.sum(out * f(dout)) + np.sum(hT * dhT))
+    lhs = float(np.sum(f(v) * g["dv"]) + np.sum(f(h0) * g["dh0"]))
+    assert abs(lhs - total) < 1e-11 * (abs(total) + 1.0)
+    # and the dcs identity picks up the final-state term <dhT, hT>
+    gh = ssd_bwd_ref(q, k, v, la, h0, dout, per_head=True, dhT=dhT)
+    qh = np.repeat(q.astype(np.float64), 2, axis=2)
+    kh = np.repeat(k.astype(np.float64), 2, axis=2)
+    dcs = np.sum(qh * gh["dq_heads"], -1) - np.sum(kh * gh["dk_heads"], -1)
+    carry = np.einsum("bhij,bhij->bh", dhT, hT)
+    dla = np.flip(np.cumsum(np.flip(dcs, 1), 1), 1) + carry[:, None, :]
+    assert rel_err(dla, g["dlog_alpha"]) < 1e-10
+
+
+def test_empty_sequence_final_state():
+    q, k, v, la, h0, dout = _case(2, 0, 1, 2, 4, 3, seed=35)
+    _, hT = ssd_fwd_ref(q, k, v, la, h0, return_final_state=True)
+    np.testing.assert_array_equal(hT, h0.astype(np.float64))
+    dhT = np.ones(h0.shape)
+    assert np.array_equal(ssd_bwd_ref(q, k, v, la, h0, dout, dhT=dhT)["dh0"], dhT)
