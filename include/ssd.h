@@ -124,6 +124,34 @@ SSD_API int ssd_bwd(const float *q, const float *k, const float *v,
             int64_t dv_dim, int64_t chunk, ssd_stream_t stream);
 
 /*
+ * Final state and its cotangent.  A sequence can be processed in pieces:
+ * running [0, L1) and then [L1, L) with the first piece's final state as h0
+ * gives the outputs of one run over [0, L) (up to rounding), and the backward
+ * of the pieces chains through dhT / dh0 the same way.  The benchmark pages
+ * time only out (fwd) and the five argument gradients (fwd_bwd); these entry
+ * points add the final state S_{L-1} of the same recurrence as an output.
+ *
+ * ssd_fwd_ex: as ssd_fwd, and also writes
+ *   hT   [B,H,dk,dv]  the final state S_{L-1} (h0, or zeros, when L == 0),
+ *                     or NULL when not wanted (then identical to ssd_fwd).
+ * ssd_bwd_ex: as ssd_bwd for the scalar <dout, out> + <dhT, hT>:
+ *   dhT  [B,H,dk,dv]  read, or NULL for zeros (then identical to ssd_bwd).
+ *                     When L == 0, dh0 = dhT.
+ * Same checks, errors, alignment, path support and stream behaviour as
+ * ssd_fwd / ssd_bwd; hT must not alias any other argument.
+ */
+SSD_API int ssd_fwd_ex(const float *q, const float *k, const float *v,
+                       const float *log_alpha, const float *h0, float *out, float *hT,
+                       int64_t B, int64_t L, int64_t G, int64_t H, int64_t dk,
+                       int64_t dv, int64_t chunk, ssd_stream_t stream);
+SSD_API int ssd_bwd_ex(const float *q, const float *k, const float *v,
+                       const float *log_alpha, const float *h0, const float *dout,
+                       const float *dhT, float *dq, float *dk, float *dv,
+                       float *dlog_alpha, float *dh0, int64_t B, int64_t L, int64_t G,
+                       int64_t H, int64_t dk_dim, int64_t dv_dim, int64_t chunk,
+                       ssd_stream_t stream);
+
+/*
  * Allocation-free forward.  The benchmark pages have no counterpart: this
  * entry point exists for callers that cannot allocate device memory at call
  * time -- code whose memory is fully reserved up front by a framework's own
@@ -187,7 +215,8 @@ SSD_API int ssd_trace_get(int i, char *name, int name_len, long long *launches,
                           double *total_ms);
 SSD_API int ssd_trace_reset(void);
 
-/* Library version as major*10000 + minor*100 + patch. */
+/* Library version as major*10000 + minor*100 + patch (0.2.0 added the
+ * final-state entry points). */
 SSD_API int ssd_version(void);
 
 #ifdef __cplusplus

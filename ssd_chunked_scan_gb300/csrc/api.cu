@@ -106,7 +106,7 @@ int ws_alloc(void **p, size_t bytes, cudaStream_t s) {
 
 extern "C" {
 
-int ssd_version(void) { return 100; }
+int ssd_version(void) { return 200; }
 
 const char *ssd_strerror(int status) {
   switch (status) {
@@ -132,36 +132,48 @@ int ssd_set_path(int path) {
 
 int ssd_get_path(void) { return current_path(); }
 
-int ssd_fwd(const float *q, const float *k, const float *v, const float *log_alpha,
-            const float *h0, float *out, int64_t B, int64_t L, int64_t G, int64_t H, int64_t dk,
-            int64_t dv, int64_t chunk, ssd_stream_t stream) {
+int ssd_fwd_ex(const float *q, const float *k, const float *v, const float *log_alpha,
+               const float *h0, float *out, float *hT, int64_t B, int64_t L, int64_t G, int64_t H,
+               int64_t dk, int64_t dv, int64_t chunk, ssd_stream_t stream) {
   int rc = check_common(B, L, G, H, dk, dv, chunk);
   if (rc) return rc;
   const int path = current_path();
   rc = check_path_shape(path, L, dk, dv, chunk);
   if (rc) return rc;
-  if (B == 0 || L == 0) return SSD_OK;
-  if (!q || !k || !v || !log_alpha || !out) return SSD_ERR_ARG;
   if (misaligned(q) || misaligned(k) || misaligned(v) || misaligned(log_alpha) ||
-      misaligned(h0) || misaligned(out))
+      misaligned(h0) || misaligned(out) || misaligned(hT))
     return SSD_ERR_ALIGN;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (B == 0 || L == 0) {  // the final state is the initial one
+    if (!hT || B == 0) return SSD_OK;
+    const size_t bytes = sizeof(float) * B * H * dk * dv;
+    return from_cuda(h0 ? cudaMemcpyAsync(hT, h0, bytes, cudaMemcpyDeviceToDevice, s)
+                        : cudaMemsetAsync(hT, 0, bytes, s));
+  }
+  if (!q || !k || !v || !log_alpha || !out) return SSD_ERR_ARG;
   const ssd::Geo g = make_geo(B, L, G, H, dk, dv, chunk);
   const size_t wsb = path == SSD_PATH_SIMT ? ssd::simt::fwd_workspace_bytes(g)
                                            : ssd::tc::fwd_workspace_bytes(g);
   void *ws = nullptr;
   rc = ws_alloc(&ws, wsb, s);
   if (rc) return rc;
-  cudaError_t e = path == SSD_PATH_SIMT ? ssd::simt::fwd(q, k, v, log_alpha, h0, out, g, ws, s)
-                                        : ssd::tc::fwd(q, k, v, log_alpha, h0, out, g, ws, s);
+  cudaError_t e = path == SSD_PATH_SIMT
+                      ? ssd::simt::fwd(q, k, v, log_alpha, h0, out, hT, g, ws, s)
+                      : ssd::tc::fwd(q, k, v, log_alpha, h0, out, hT, g, ws, s);
   if (ws) cudaFreeAsync(ws, s);
   return from_cuda(e);
 }
 
-int ssd_bwd(const float *q, const float *k, const float *v, const float *log_alpha,
-            const float *h0, const float *dout, float *dq, float *dk, float *dv,
-            float *dlog_alpha, float *dh0, int64_t B, int64_t L, int64_t G, int64_t H,
-            int64_t dk_dim, int64_t dv_dim, int64_t chunk, ssd_stream_t stream) {
+int ssd_fwd(const float *q, const float *k, const float *v, const float *log_alpha,
+            const float *h0, float *out, int64_t B, int64_t L, int64_t G, int64_t H, int64_t dk,
+            int64_t dv, int64_t chunk, ssd_stream_t stream) {
+  return ssd_fwd_ex(q, k, v, log_alpha, h0, out, nullptr, B, L, G, H, dk, dv, chunk, stream);
+}
+
+int ssd_bwd_ex(const float *q, const float *k, const float *v, const float *log_alpha,
+               const float *h0, const float *dout, const float *dhT, float *dq, float *dk,
+               float *dv, float *dlog_alpha, float *dh0, int64_t B, int64_t L, int64_t G,
+               int64_t H, int64_t dk_dim, int64_t dv_dim, int64_t chunk, ssd_stream_t stream) {
   int rc = check_common(B, L, G, H, dk_dim, dv_dim, chunk);
   if (rc) return rc;
   const int path = current_path();
@@ -169,13 +181,14 @@ int ssd_bwd(const float *q, const float *k, const float *v, const float *log_alp
   if (rc) return rc;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (misaligned(q) || misaligned(k) || misaligned(v) || misaligned(log_alpha) ||
-      misaligned(h0) || misaligned(dout) || misaligned(dq) || misaligned(dk) ||
-      misaligned(dv) || misaligned(dlog_alpha) || misaligned(dh0))
+      misaligned(h0) || misaligned(dout) || misaligned(dhT) || misaligned(dq) ||
+      misaligned(dk) || misaligned(dv) || misaligned(dlog_alpha) || misaligned(dh0))
     return SSD_ERR_ALIGN;
-  if (B == 0 || L == 0) {
-    if (dh0 && B > 0)
-      return from_cuda(cudaMemsetAsync(dh0, 0, sizeof(float) * B * H * dk_dim * dv_dim, s));
-    return SSD_OK;
+  if (B == 0 || L == 0) {  // dh0 = dhT (or zero)
+    if (!dh0 || B == 0) return SSD_OK;
+    const size_t bytes = sizeof(float) * B * H * dk_dim * dv_dim;
+    return from_cuda(dhT ? cudaMemcpyAsync(dh0, dhT, bytes, cudaMemcpyDeviceToDevice, s)
+                         : cudaMemsetAsync(dh0, 0, bytes, s));
   }
   if (!q || !k || !v || !log_alpha || !dout || !dq || !dk || !dv || !dlog_alpha)
     return SSD_ERR_ARG;
@@ -187,10 +200,20 @@ int ssd_bwd(const float *q, const float *k, const float *v, const float *log_alp
   if (rc) return rc;
   cudaError_t e =
       path == SSD_PATH_SIMT
-          ? ssd::simt::bwd(q, k, v, log_alpha, h0, dout, dq, dk, dv, dlog_alpha, dh0, g, ws, s)
-          : ssd::tc::bwd(q, k, v, log_alpha, h0, dout, dq, dk, dv, dlog_alpha, dh0, g, ws, s);
+          ? ssd::simt::bwd(q, k, v, log_alpha, h0, dout, dhT, dq, dk, dv, dlog_alpha, dh0, g,
+                           ws, s)
+          : ssd::tc::bwd(q, k, v, log_alpha, h0, dout, dhT, dq, dk, dv, dlog_alpha, dh0, g, ws,
+                         s);
   if (ws) cudaFreeAsync(ws, s);
   return from_cuda(e);
+}
+
+int ssd_bwd(const float *q, const float *k, const float *v, const float *log_alpha,
+            const float *h0, const float *dout, float *dq, float *dk, float *dv,
+            float *dlog_alpha, float *dh0, int64_t B, int64_t L, int64_t G, int64_t H,
+            int64_t dk_dim, int64_t dv_dim, int64_t chunk, ssd_stream_t stream) {
+  return ssd_bwd_ex(q, k, v, log_alpha, h0, dout, nullptr, dq, dk, dv, dlog_alpha, dh0, B, L, G,
+                    H, dk_dim, dv_dim, chunk, stream);
 }
 
 int ssd_last_device_error(ssd_stream_t stream) {

@@ -80,7 +80,7 @@ SSD_API int ssd_fwd_noalloc(const float *q, const float *k, const float *v,
     cudaGetLastError();
     return SSD_ERR_CUDA;
   }
-  cudaError_t e = ssd::simt::fwd(q, k, v, log_alpha, h0, out, g, ws,
+  cudaError_t e = ssd::simt::fwd(q, k, v, log_alpha, h0, out, nullptr, g, ws,
                                  reinterpret_cast<cudaStream_t>(stream));
   if (e == cudaSuccess) return SSD_OK;
   return (e == cudaErrorInvalidConfiguration || e == cudaErrorLaunchOutOfResources ||

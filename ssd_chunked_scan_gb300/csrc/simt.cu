@@ -151,12 +151,15 @@ __global__ void __launch_bounds__(NT) k_chunk_state(const float *__restrict__ X,
 
 // ---------------------------------------------------------------------------
 // State passing, in place.  Forward: states[c] <- H_{c-1} (the state entering
-// chunk c), from contributions S_c.  Reverse: states[c] <- dX_c (gradient of
-// the state leaving chunk c), from query contributions; dh0 <- dX_{-1}.
+// chunk c), from contributions S_c; the state after the last chunk goes to fin
+// when given.  Reverse: states[c] <- dX_c (gradient of the state leaving chunk
+// c), from query contributions, starting from dX_{N-1} = dfin (the cotangent
+// of the final state, zero when NULL); dh0 <- dX_{-1}.
 // grid (B*H, ceil(dk*dv / NT))
 __global__ void __launch_bounds__(NT) k_scan_fwd(float *__restrict__ states,
                                                  const float *__restrict__ Adec,
-                                                 const float *__restrict__ h0, Geo g) {
+                                                 const float *__restrict__ h0,
+                                                 float *__restrict__ fin, Geo g) {
   const int64_t bh = blockIdx.x;
   const int64_t e = (int64_t)blockIdx.y * NT + threadIdx.x;
   const int64_t sz = g.dk * g.dv;
@@ -177,16 +180,18 @@ __global__ void __launch_bounds__(NT) k_scan_fwd(float *__restrict__ states,
     p[c * sz] = run;
     run = fmaf(expf(a[c]), run, x);
   }
+  if (fin) fin[bh * sz + e] = run;
 }
 
 __global__ void __launch_bounds__(NT) k_scan_rev(float *__restrict__ states,
                                                  const float *__restrict__ Adec,
+                                                 const float *__restrict__ dfin,
                                                  float *__restrict__ dh0, Geo g) {
   const int64_t bh = blockIdx.x;
   const int64_t e = (int64_t)blockIdx.y * NT + threadIdx.x;
   const int64_t sz = g.dk * g.dv;
   if (e >= sz) return;
-  float run = 0.f;
+  float run = dfin ? dfin[bh * sz + e] : 0.f;
   float *p = states + st_off(g, bh, 0) + e;
   const float *a = Adec + bh * g.N;
   int64_t c = g.N - 1;
@@ -483,14 +488,32 @@ __global__ void __launch_bounds__(NT) k_chunk_grad(
   }
 }
 
-// dla[t] += sum of the totals of all later chunks (fp64 carry).  grid (B*H)
+// dla[t] += sum of the totals of all later chunks (fp64 carry), plus
+// <dhT, hT> when the final state has a cotangent (both given, [dk x dv] per
+// head).  grid (B*H)
 __global__ void __launch_bounds__(NT) k_dla_carry(float *__restrict__ dla,
-                                                  const float *__restrict__ dcs_sum, Geo g) {
+                                                  const float *__restrict__ dcs_sum,
+                                                  const float *__restrict__ dhT,
+                                                  const float *__restrict__ hT, Geo g) {
   __shared__ double sh[NT];
   __shared__ double carry_in;
   const int64_t bh = blockIdx.x, b = bh / g.H, h = bh % g.H;
-  if (threadIdx.x == 0) carry_in = 0.0;
-  __syncthreads();
+  {
+    double part = 0.0;
+    if (dhT) {
+      const int64_t sz = g.dk * g.dv;
+      for (int64_t e = threadIdx.x; e < sz; e += NT)
+        part += (double)dhT[bh * sz + e] * (double)hT[bh * sz + e];
+    }
+    sh[threadIdx.x] = part;
+    __syncthreads();
+    for (int o = NT / 2; o > 0; o >>= 1) {
+      if (threadIdx.x < o) sh[threadIdx.x] += sh[threadIdx.x + o];
+      __syncthreads();
+    }
+    if (threadIdx.x == 0) carry_in = sh[0];
+    __syncthreads();
+  }
   // walk chunk blocks from the end; within a block, an exclusive suffix scan
   for (int64_t hi = g.N; hi > 0; hi -= NT) {
     const int64_t lo = hi - NT > 0 ? hi - NT : 0;
@@ -544,27 +567,30 @@ static void dispatch_state(const float *X, const float *Y, const float *la, floa
   else launch_state<2, 2, QUERY>(X, Y, la, st, Adec, g, s);
 }
 
-static void launch_scan_fwd(float *st, const float *Adec, const float *h0, const Geo &g,
-                            cudaStream_t s) {
+static void launch_scan_fwd(float *st, const float *Adec, const float *h0, float *fin,
+                            const Geo &g, cudaStream_t s) {
   dim3 grid((unsigned)(g.B * g.H), (unsigned)cdiv(g.dk * g.dv, NT));
   LaunchTrace lt("simt.state_scan_fwd", s);
-  k_scan_fwd<<<grid, NT, 0, s>>>(st, Adec, h0, g);
+  k_scan_fwd<<<grid, NT, 0, s>>>(st, Adec, h0, fin, g);
 }
 
 size_t fwd_workspace_bytes(const Geo &g) {
   return sizeof(float) * (size_t)(g.B * g.H * g.N * g.dk * g.dv + g.B * g.H * g.N);
 }
 
+// Two chunk-state arrays, their decays and chunk totals, and room for the
+// final state (used only when it has a cotangent).
 size_t bwd_workspace_bytes(const Geo &g) {
-  return sizeof(float) * (size_t)(2 * g.B * g.H * g.N * g.dk * g.dv + 2 * g.B * g.H * g.N);
+  return sizeof(float) * (size_t)(2 * g.B * g.H * g.N * g.dk * g.dv + 2 * g.B * g.H * g.N +
+                                  g.B * g.H * g.dk * g.dv);
 }
 
 cudaError_t fwd(const float *q, const float *k, const float *v, const float *la, const float *h0,
-                float *out, const Geo &g, void *ws, cudaStream_t s) {
+                float *out, float *hT, const Geo &g, void *ws, cudaStream_t s) {
   float *st = static_cast<float *>(ws);
   float *Adec = st + g.B * g.H * g.N * g.dk * g.dv;
   dispatch_state<false>(k, v, la, st, Adec, g, s);
-  launch_scan_fwd(st, Adec, h0, g, s);
+  launch_scan_fwd(st, Adec, h0, hT, g, s);
   dim3 grid((unsigned)g.N, (unsigned)g.H, (unsigned)g.B);
   LaunchTrace lt("simt.chunk_out", s);
   if (g.dv > 64) k_chunk_out<2><<<grid, NT, 0, s>>>(q, k, v, la, st, out, g);
@@ -589,22 +615,23 @@ static cudaError_t launch_grad(const float *q, const float *k, const float *v, c
 }
 
 cudaError_t bwd(const float *q, const float *k, const float *v, const float *la, const float *h0,
-                const float *dout, float *dq, float *dk, float *dv, float *dla, float *dh0,
-                const Geo &g, void *ws, cudaStream_t s) {
+                const float *dout, const float *dhT, float *dq, float *dk, float *dv, float *dla,
+                float *dh0, const Geo &g, void *ws, cudaStream_t s) {
   const int64_t nst = g.B * g.H * g.N * g.dk * g.dv;
   float *Hst = static_cast<float *>(ws);
   float *dXst = Hst + nst;
   float *Adec = dXst + nst;
   float *dcs_sum = Adec + g.B * g.H * g.N;
+  float *hT = dhT ? dcs_sum + g.B * g.H * g.N : nullptr;
   // forward states entering each chunk (recomputed; nothing is saved by fwd)
   dispatch_state<false>(k, v, la, Hst, Adec, g, s);
-  launch_scan_fwd(Hst, Adec, h0, g, s);
+  launch_scan_fwd(Hst, Adec, h0, hT, g, s);
   // query contributions, then the reverse state-gradient pass
   dispatch_state<true>(q, dout, la, dXst, nullptr, g, s);
   {
     dim3 grid((unsigned)(g.B * g.H), (unsigned)cdiv(g.dk * g.dv, NT));
     LaunchTrace lt("simt.state_scan_rev", s);
-    k_scan_rev<<<grid, NT, 0, s>>>(dXst, Adec, dh0, g);
+    k_scan_rev<<<grid, NT, 0, s>>>(dXst, Adec, dhT, dh0, g);
   }
   cudaError_t err;
   const bool bk = g.dk > 64, bv = g.dv > 64;
@@ -615,7 +642,7 @@ cudaError_t bwd(const float *q, const float *k, const float *v, const float *la,
   if (err != cudaSuccess) return err;
   {
     LaunchTrace lt("simt.dla_carry", s);
-    k_dla_carry<<<(unsigned)(g.B * g.H), NT, 0, s>>>(dla, dcs_sum, g);
+    k_dla_carry<<<(unsigned)(g.B * g.H), NT, 0, s>>>(dla, dcs_sum, dhT, hT, g);
   }
   return cudaGetLastError();
 }

@@ -9,13 +9,14 @@ namespace simt {
 size_t fwd_workspace_bytes(const Geo &g);
 size_t bwd_workspace_bytes(const Geo &g);
 
-// Enqueue the forward / backward on stream s.  ws must hold the bytes above
+// Enqueue the forward / backward on stream s.  hT (final state, written) and
+// dhT (its cotangent, read) may be NULL.  ws must hold the bytes above
 // (256-byte aligned).  Returns the first launch error.
 cudaError_t fwd(const float *q, const float *k, const float *v, const float *la, const float *h0,
-                float *out, const Geo &g, void *ws, cudaStream_t s);
+                float *out, float *hT, const Geo &g, void *ws, cudaStream_t s);
 cudaError_t bwd(const float *q, const float *k, const float *v, const float *la, const float *h0,
-                const float *dout, float *dq, float *dk, float *dv, float *dla, float *dh0,
-                const Geo &g, void *ws, cudaStream_t s);
+                const float *dout, const float *dhT, float *dq, float *dk, float *dv, float *dla,
+                float *dh0, const Geo &g, void *ws, cudaStream_t s);
 
 }  // namespace simt
 }  // namespace ssd

@@ -12,9 +12,11 @@
 // on (q, k, v).  The gradients of <dout, out> are passes too, because the
 // adjoint of a linear scan is a linear scan:
 //   dq_h = causal(q' = dout, k' = v, v' = k, initial state h0^T)
-//   dk_h = anti-causal(q' = v, k' = dout, v' = q)
-//   dv   = anti-causal(q' = k, k' = q, v' = dout), whose leftmost state is dh0
-// and dla_t = sum_{t'>=t} (q_t'.dq_h[t'] - k_t'.dk_h[t']).
+//   dk_h = anti-causal(q' = v, k' = dout, v' = q, initial state dhT^T)
+//   dv   = anti-causal(q' = k, k' = q, v' = dout, initial state dhT), whose
+//          leftmost state is dh0
+// and dla_t = sum_{t'>=t} (q_t'.dq_h[t'] - k_t'.dk_h[t']) + <dhT, hT>, where
+// dhT is the cotangent of the final state hT (zero unless given).
 //
 // A pass cuts every (batch, head) sequence into segments of Ls tokens (a
 // multiple of the 64-token chunk) so that B*H*nseg CTAs work at once:
@@ -309,16 +311,17 @@ __global__ void __launch_bounds__(NT2, 2) k_seg_state(const __grid_constant__ CU
 // ===========================================================================
 // State passing over segments, in place (one thread per state element).
 //   causal:      st[s] <- state entering segment s from the left; the first is
-//                h0 (read transposed when TRANS), or 0
-//   anti-causal: st[s] <- state entering segment s from the right (0 for the
-//                last); the state left of segment 0 goes to fin (if given,
-//                written transposed when TRANS)
-// When stT is given, every result is also written there transposed.
+//                init, or 0; the state right of the last segment goes to fin
+//   anti-causal: st[s] <- state entering segment s from the right; the one
+//                entering the last is init, or 0; the state left of segment 0
+//                goes to fin
+// init is read, and fin (if given) written, transposed when TRANS.  When stT
+// is given, every result is also written there transposed.
 // grid (B*H, ceil(dk*dv / 128))
 template <bool REV, bool TRANS>
 __global__ void __launch_bounds__(NTH) k_seg_scan(float *__restrict__ st,
                                                   const float *__restrict__ Aseg,
-                                                  const float *__restrict__ h0,
+                                                  const float *__restrict__ init,
                                                   float *__restrict__ fin,
                                                   float *__restrict__ stT, PassGeo p) {
   const int64_t bh = blockIdx.x;
@@ -331,8 +334,8 @@ __global__ void __launch_bounds__(NTH) k_seg_scan(float *__restrict__ st,
   const float *a = Aseg + bh * p.nseg;
   constexpr int U = 8;  // segments loaded ahead of the dependent chain
   float run = 0.f;
+  if (init) run = TRANS ? init[bh * sz + et] : init[bh * sz + e];
   if (!REV) {
-    if (h0) run = TRANS ? h0[bh * sz + et] : h0[bh * sz + e];
     for (int s0 = 0; s0 < p.nseg; s0 += U) {
       float x[U], d[U];
 #pragma unroll
@@ -346,6 +349,7 @@ __global__ void __launch_bounds__(NTH) k_seg_scan(float *__restrict__ st,
           run = fmaf(d[u], run, x[u]);
         }
     }
+    if (fin) fin[bh * sz + (TRANS ? et : e)] = run;
   } else {
     for (int s0 = p.nseg - 1; s0 >= 0; s0 -= U) {
       float x[U], d[U];
@@ -890,13 +894,17 @@ __global__ void __launch_bounds__(NTH) k_dla_intra(const __grid_constant__ CUten
 // q_t.dq_inter(t) and k_t.dk_inter(t), G_end the gradient of the state at the
 // segment's end (from its right) and S_end that state (the state entering the
 // next segment); both are given in the same layout (each transposed, sz
-// elements).  grid (nseg, H, B).
+// elements).  For the last segment G_end is the final state's cotangent and
+// S_end the final state: Gfin and Sfin, both [dk x dv] per head, or no term
+// when Gfin is NULL.  grid (nseg, H, B).
 constexpr int DT = 256;
 __global__ void __launch_bounds__(DT) k_dla(const float *__restrict__ Bt,
                                             const float *__restrict__ rq,
                                             const float *__restrict__ rk,
                                             const float *__restrict__ Gst,
-                                            const float *__restrict__ Sst, float *__restrict__ dla,
+                                            const float *__restrict__ Sst,
+                                            const float *__restrict__ Gfin,
+                                            const float *__restrict__ Sfin, float *__restrict__ dla,
                                             int64_t L, int64_t H, int64_t sz, int Ls, int nseg) {
   __shared__ double wred[DT / 32];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -904,9 +912,15 @@ __global__ void __launch_bounds__(DT) k_dla(const float *__restrict__ Bt,
   const int64_t bh = b * H + h;
   // carry = <G_end, S_end>: float4 loads, fp32 partial sums, fp64 across threads
   float part = 0.f;
+  const float4 *G = nullptr, *S = nullptr;
   if (seg + 1 < nseg) {
-    const float4 *G = reinterpret_cast<const float4 *>(Gst + (bh * nseg + seg) * sz);
-    const float4 *S = reinterpret_cast<const float4 *>(Sst + (bh * nseg + seg + 1) * sz);
+    G = reinterpret_cast<const float4 *>(Gst + (bh * nseg + seg) * sz);
+    S = reinterpret_cast<const float4 *>(Sst + (bh * nseg + seg + 1) * sz);
+  } else if (Gfin) {
+    G = reinterpret_cast<const float4 *>(Gfin + bh * sz);
+    S = reinterpret_cast<const float4 *>(Sfin + bh * sz);
+  }
+  if (G) {
     for (int64_t e = tid; e < sz / 4; e += DT) {
       const float4 g = G[e], x = S[e];
       part = fmaf(g.x, x.x, fmaf(g.y, x.y, fmaf(g.z, x.z, fmaf(g.w, x.w, part))));
@@ -1108,31 +1122,32 @@ size_t fwd_workspace_bytes(const Geo &g) {
   return sizeof(float) * (state_floats(p) + (size_t)(g.B * g.H * p.nseg));
 }
 
-// Two passes' states (both kept for dlog_alpha), their decays, and three
-// per-token arrays.
+// Two passes' states (both kept for dlog_alpha), their decays, three
+// per-token arrays, and the final state (used only when it has a cotangent).
 size_t bwd_workspace_bytes(const Geo &g) {
   const PassGeo p = make_pass(g, (int)g.dk, (int)g.dv, false, true);
   const size_t nst = state_floats(p), na = (size_t)(g.B * g.H * p.nseg);
-  return sizeof(float) * (2 * nst + 2 * na + 3 * (size_t)(g.B * g.L * g.H)) + 256;
+  return sizeof(float) * (2 * nst + 2 * na + 3 * (size_t)(g.B * g.L * g.H) +
+                          (size_t)(g.B * g.H * g.dk * g.dv)) + 256;
 }
 
 cudaError_t fwd(const float *q, const float *k, const float *v, const float *la, const float *h0,
-                float *out, const Geo &g, void *ws, cudaStream_t s) {
+                float *out, float *hT, const Geo &g, void *ws, cudaStream_t s) {
   cudaError_t e = get_encoder();
   if (e != cudaSuccess) return e;
   if (g.B * g.L >= (int64_t)1 << 31) return cudaErrorNotSupported;
   const PassGeo p = make_pass(g, (int)g.dk, (int)g.dv, false, true);
   float *st = static_cast<float *>(ws);
   float *Aseg = st + state_floats(p);
-  if ((e = run_states<false>(p, k, v, la, h0, false, nullptr, st, Aseg, nullptr, s, "tc.seg_state")) != cudaSuccess)
+  if ((e = run_states<false>(p, k, v, la, h0, false, hT, st, Aseg, nullptr, s, "tc.seg_state")) != cudaSuccess)
     return e;
   OutArgs oa{out, (int)g.H, nullptr, nullptr};
   return run_walk<false>(p, q, k, v, la, st, false, oa, false, s, "tc.walk_out");
 }
 
 cudaError_t bwd(const float *q, const float *k, const float *v, const float *la, const float *h0,
-                const float *dout, float *dq, float *dk, float *dv, float *dla, float *dh0,
-                const Geo &g, void *ws, cudaStream_t s) {
+                const float *dout, const float *dhT, float *dq, float *dk, float *dv, float *dla,
+                float *dh0, const Geo &g, void *ws, cudaStream_t s) {
   cudaError_t e = get_encoder();
   if (e != cudaSuccess) return e;
   if (g.B * g.L >= (int64_t)1 << 31) return cudaErrorNotSupported;
@@ -1153,18 +1168,25 @@ cudaError_t bwd(const float *q, const float *k, const float *v, const float *la,
   float *rq = aB + na;
   float *rk = rq + g.B * g.L * g.H;
   float *Bt = rk + g.B * g.L * g.H;
+  // the final state, [dk x dv] per head, needed for dlog_alpha only when it
+  // has a cotangent
+  float *hT = nullptr;
+  if (dhT) {  // 16-byte aligned for the float4 reads of k_dla
+    const uintptr_t a = reinterpret_cast<uintptr_t>(Bt + g.B * g.L * g.H);
+    hT = reinterpret_cast<float *>((a + 15) & ~uintptr_t(15));
+  }
   const bool grouped = g.hpg > 1;
   if (grouped) {
     if ((e = cudaMemsetAsync(dq, 0, sizeof(float) * g.B * g.L * g.G * g.dk, s)) != cudaSuccess) return e;
     if ((e = cudaMemsetAsync(dk, 0, sizeof(float) * g.B * g.L * g.G * g.dk, s)) != cudaSuccess) return e;
   }
   const int oslots = grouped ? (int)g.G : (int)g.H;
-  if ((e = run_states<false>(pa, v, k, la, h0, true, nullptr, stA, aA, nullptr, s, "tc.seg_state_dq")) != cudaSuccess)
+  if ((e = run_states<false>(pa, v, k, la, h0, true, hT, stA, aA, nullptr, s, "tc.seg_state_dq")) != cudaSuccess)
     return e;
   OutArgs oq{dq, oslots, q, rq};
   if ((e = run_walk<false>(pa, dout, v, k, la, stA, false, oq, grouped, s, "tc.walk_dq")) != cudaSuccess)
     return e;
-  if ((e = run_states<true>(pb, dout, q, la, nullptr, true, dh0, stB, aB, nullptr, s, "tc.seg_state_dk")) != cudaSuccess)
+  if ((e = run_states<true>(pb, dout, q, la, dhT, true, dh0, stB, aB, nullptr, s, "tc.seg_state_dk")) != cudaSuccess)
     return e;
   OutArgs okk{dk, oslots, k, rk};
   if ((e = run_walk<true>(pb, v, dout, q, la, stB, false, okk, grouped, s, "tc.walk_dk")) != cudaSuccess)
@@ -1189,7 +1211,7 @@ cudaError_t bwd(const float *q, const float *k, const float *v, const float *la,
   {  // pass A's states are S^T, pass B's are G^T: the carry is their plain dot
     LaunchTrace lt("tc.dla", s);
     k_dla<<<dim3((unsigned)pa.nseg, (unsigned)g.H, (unsigned)g.B), DT, 0, s>>>(
-        Bt, rq, rk, stB, stA, dla, g.L, g.H, DK * DV, pa.Ls, pa.nseg);
+        Bt, rq, rk, stB, stA, dhT, hT, dla, g.L, g.H, DK * DV, pa.Ls, pa.nseg);
   }
   return cudaGetLastError();
 }

@@ -11,11 +11,12 @@ int check_shape(int64_t dk, int64_t dv, int64_t chunk);
 size_t fwd_workspace_bytes(const Geo &g);
 size_t bwd_workspace_bytes(const Geo &g);
 
+// hT (final state, written) and dhT (its cotangent, read) may be NULL.
 cudaError_t fwd(const float *q, const float *k, const float *v, const float *la, const float *h0,
-                float *out, const Geo &g, void *ws, cudaStream_t s);
+                float *out, float *hT, const Geo &g, void *ws, cudaStream_t s);
 cudaError_t bwd(const float *q, const float *k, const float *v, const float *la, const float *h0,
-                const float *dout, float *dq, float *dk, float *dv, float *dla, float *dh0,
-                const Geo &g, void *ws, cudaStream_t s);
+                const float *dout, const float *dhT, float *dq, float *dk, float *dv, float *dla,
+                float *dh0, const Geo &g, void *ws, cudaStream_t s);
 
 // Reads and clears the device error word of the current device (set by a
 // bounded wait that gave up).

@@ -64,3 +64,10 @@ def make_inputs(B, L, G, H, dk, dv, seed, la_mu=0.0, with_h0=True, with_dout=Tru
 
 def workload_inputs(w: Workload, with_h0=True, with_dout=True):
     return make_inputs(w.B, w.L, w.G, w.H, w.dk, w.dv, w.seed, w.la_mu, with_h0, with_dout)
+
+
+def make_state_cotangent(B, H, dk, dv, seed):
+    """float32 cotangent dhT [B,H,dk,dv] of the final state: standard normal
+    scaled by 1/sqrt(dk), the size of one q_t dout_t^T term."""
+    rng = np.random.default_rng(seed + 7919)
+    return (rng.standard_normal((B, H, dk, dv)) / np.sqrt(dk)).astype(np.float32)

@@ -46,6 +46,10 @@ def _load():
     lib.ssd_fwd.argtypes = [p] * 6 + [i64] * 7 + [p]
     lib.ssd_fwd.restype = ctypes.c_int
     lib.ssd_bwd.argtypes = [p] * 11 + [i64] * 7 + [p]
+    lib.ssd_fwd_ex.argtypes = [p] * 7 + [i64] * 7 + [p]
+    lib.ssd_fwd_ex.restype = ctypes.c_int
+    lib.ssd_bwd_ex.argtypes = [p] * 12 + [i64] * 7 + [p]
+    lib.ssd_bwd_ex.restype = ctypes.c_int
     lib.ssd_bwd.restype = ctypes.c_int
     lib.ssd_set_path.argtypes = [ctypes.c_int]
     lib.ssd_set_path.restype = ctypes.c_int
@@ -173,6 +177,20 @@ def ssd_fwd(q, k, v, log_alpha, h0=None, chunk=64, out=None, stream=None):
     return out
 
 
+def _grad_buffers(B, L, G, H, dk, dv, dev, want_dh0, grads):
+    shapes = {"dq": (B, L, G, dk), "dk": (B, L, G, dk), "dv": (B, L, H, dv),
+              "dlog_alpha": (B, L, H), "dh0": (B, H, dk, dv)}
+    g = dict(grads or {})
+    for n, s in shapes.items():
+        if n == "dh0" and not want_dh0:
+            g[n] = None
+            continue
+        if g.get(n) is None:
+            g[n] = torch.empty(s, dtype=torch.float32, device=dev)
+        _check(n, g[n], s, dev)
+    return g
+
+
 def ssd_bwd(q, k, v, log_alpha, h0, dout, chunk=64, want_dh0=True, grads=None, stream=None):
     """Gradients of <dout, out>: dict dq, dk, dv, dlog_alpha, dh0 (dh0 None if not wanted).
 
@@ -184,21 +202,51 @@ def ssd_bwd(q, k, v, log_alpha, h0, dout, chunk=64, want_dh0=True, grads=None, s
                     ("log_alpha", log_alpha, (B, L, H)), ("h0", h0, (B, H, dk, dv)),
                     ("dout", dout, (B, L, H, dv))):
         _check(n, t, s, dev)
-    shapes = {"dq": (B, L, G, dk), "dk": (B, L, G, dk), "dv": (B, L, H, dv),
-              "dlog_alpha": (B, L, H), "dh0": (B, H, dk, dv)}
-    g = dict(grads or {})
-    for n, s in shapes.items():
-        if n == "dh0" and not want_dh0:
-            g[n] = None
-            continue
-        if g.get(n) is None:
-            g[n] = torch.empty(s, dtype=torch.float32, device=dev)
-        _check(n, g[n], s, dev)
+    g = _grad_buffers(B, L, G, H, dk, dv, dev, want_dh0, grads)
     rc = LIB.ssd_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(h0), _ptr(dout),
                      _ptr(g["dq"]), _ptr(g["dk"]), _ptr(g["dv"]), _ptr(g["dlog_alpha"]),
                      _ptr(g["dh0"]), B, L, G, H, dk, dv, int(chunk), _stream(stream))
     if rc:
         raise SSDError(rc, "ssd_bwd")
+    return g
+
+
+def ssd_fwd_ex(q, k, v, log_alpha, h0=None, chunk=64, out=None, hT=None, stream=None):
+    """(out, hT): the forward plus the final state hT [B,H,dk,dv] = S_{L-1}."""
+    B, L, G, H, dk, dv = _dims(q, v)
+    dev = q.device
+    for n, t, s in (("q", q, (B, L, G, dk)), ("k", k, (B, L, G, dk)), ("v", v, (B, L, H, dv)),
+                    ("log_alpha", log_alpha, (B, L, H)), ("h0", h0, (B, H, dk, dv))):
+        _check(n, t, s, dev)
+    if out is None:
+        out = torch.empty((B, L, H, dv), dtype=torch.float32, device=dev)
+    if hT is None:
+        hT = torch.empty((B, H, dk, dv), dtype=torch.float32, device=dev)
+    _check("out", out, (B, L, H, dv), dev)
+    _check("hT", hT, (B, H, dk, dv), dev)
+    rc = LIB.ssd_fwd_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(h0), _ptr(out),
+                        _ptr(hT), B, L, G, H, dk, dv, int(chunk), _stream(stream))
+    if rc:
+        raise SSDError(rc, "ssd_fwd_ex")
+    return out, hT
+
+
+def ssd_bwd_ex(q, k, v, log_alpha, h0, dout, dhT, chunk=64, want_dh0=True, grads=None,
+               stream=None):
+    """Gradients of <dout, out> + <dhT, hT> (dhT None means zero), as ssd_bwd."""
+    B, L, G, H, dk, dv = _dims(q, v)
+    dev = q.device
+    for n, t, s in (("q", q, (B, L, G, dk)), ("k", k, (B, L, G, dk)), ("v", v, (B, L, H, dv)),
+                    ("log_alpha", log_alpha, (B, L, H)), ("h0", h0, (B, H, dk, dv)),
+                    ("dout", dout, (B, L, H, dv)), ("dhT", dhT, (B, H, dk, dv))):
+        _check(n, t, s, dev)
+    g = _grad_buffers(B, L, G, H, dk, dv, dev, want_dh0, grads)
+    rc = LIB.ssd_bwd_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(h0), _ptr(dout),
+                        _ptr(dhT), _ptr(g["dq"]), _ptr(g["dk"]), _ptr(g["dv"]),
+                        _ptr(g["dlog_alpha"]), _ptr(g["dh0"]), B, L, G, H, dk, dv, int(chunk),
+                        _stream(stream))
+    if rc:
+        raise SSDError(rc, "ssd_bwd_ex")
     return g
 
 

@@ -29,13 +29,16 @@ def lib():
     p, i64 = ctypes.c_void_p, ctypes.c_int64
     l.ssd_fwd.argtypes = [p] * 6 + [i64] * 7 + [p]
     l.ssd_bwd.argtypes = [p] * 11 + [i64] * 7 + [p]
+    l.ssd_fwd_ex.argtypes = [p] * 7 + [i64] * 7 + [p]
+    l.ssd_bwd_ex.argtypes = [p] * 12 + [i64] * 7 + [p]
     l.ssd_strerror.restype = ctypes.c_char_p
     return l
 
 
 def test_exports_every_declared_symbol(lib):
     names = _declared()
-    assert {"ssd_fwd", "ssd_bwd", "ssd_set_path", "ssd_strerror"} <= names
+    assert {"ssd_fwd", "ssd_bwd", "ssd_fwd_ex", "ssd_bwd_ex", "ssd_set_path",
+            "ssd_strerror"} <= names
     for n in names:
         assert hasattr(lib, n), n
 
@@ -52,6 +55,25 @@ def _fwd(lib, ptrs=(0x1000,) * 6, B=1, L=8, G=1, H=1, dk=8, dv=8, chunk=64):
 
 def _bwd(lib, ptrs=(0x1000,) * 11, B=1, L=8, G=1, H=1, dk=8, dv=8, chunk=64):
     return lib.ssd_bwd(*[ctypes.c_void_p(x) for x in ptrs], B, L, G, H, dk, dv, chunk, None)
+
+
+def _fwd_ex(lib, ptrs=(0x1000,) * 7, B=1, L=8, G=1, H=1, dk=8, dv=8, chunk=64):
+    return lib.ssd_fwd_ex(*[ctypes.c_void_p(x) for x in ptrs], B, L, G, H, dk, dv, chunk, None)
+
+
+def _bwd_ex(lib, ptrs=(0x1000,) * 12, B=1, L=8, G=1, H=1, dk=8, dv=8, chunk=64):
+    return lib.ssd_bwd_ex(*[ctypes.c_void_p(x) for x in ptrs], B, L, G, H, dk, dv, chunk, None)
+
+
+@pytest.mark.parametrize("path", [0, 1])
+def test_host_argument_checks_final_state(lib, path):
+    assert lib.ssd_set_path(path) == 0
+    assert _fwd_ex(lib, ptrs=(0x1000,) * 6 + (0x1004,)) == 2     # hT misaligned
+    assert _bwd_ex(lib, ptrs=(0x1000,) * 6 + (0x100c,) + (0x1000,) * 5) == 2  # dhT
+    assert _fwd_ex(lib, G=2, H=3) == 1
+    assert _bwd_ex(lib, dv=0) == 1
+    assert _fwd_ex(lib, L=0, ptrs=(0,) * 7) == 0    # empty, hT not wanted
+    assert _bwd_ex(lib, L=0, ptrs=(0,) * 12) == 0   # empty, dh0 not wanted
 
 
 @pytest.mark.parametrize("path", [0, 1])
@@ -87,3 +109,5 @@ def test_injected_workspace_failure_is_reported_before_launch(lib, monkeypatch):
     assert lib.ssd_set_path(1) == 0
     assert _fwd(lib) == 5
     assert _bwd(lib) == 5
+    assert _fwd_ex(lib) == 5
+    assert _bwd_ex(lib) == 5
