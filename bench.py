@@ -189,44 +189,60 @@ class ClockSampler:
                 "power_w_max": max(pw) if pw else None, "samples": len(inwin), "window": window}
 
 
-def cpu_oracle_sample(w, min_seconds=10.0, max_reps=4):
-    """Time the float64 oracle (fwd + bwd) on one batch entry of the workload,
-    repeated until min_seconds have passed; returns tokens/s and details."""
+def oracle_sample(w, threads):
+    """The oracle's bounded sample of workload w: the first nb batch entries
+    (every group and head, full sequence), nb the fewest whose nb*H
+    independent (batch, head) sequences keep `threads` threads busy.
+    Returns (arrays, nb, threads actually used)."""
     import numpy as np
-    from oracle import oracle_threads, ssd_bwd_ref, ssd_fwd_ref
     from ssd_chunked_scan_gb300.inputs import workload_inputs
-    q, k, v, la, h0, dout = workload_inputs(w)
-    sl = lambda x: np.ascontiguousarray(x[:1])
-    q, k, v, la, h0, dout = map(sl, (q, k, v, la, h0, dout))
+    nb = max(1, min(w.B, -(-threads // w.H)))
+    arrs = tuple(np.ascontiguousarray(x[:nb]) for x in workload_inputs(w))
+    return arrs, nb, min(threads, nb * w.H)
+
+
+def cpu_oracle_sample(w, min_seconds=10.0, max_reps=60):
+    """Time the float64 oracle (fwd + bwd) on a sample of the workload,
+    repeated until min_seconds have passed; returns tokens/s and details."""
+    from oracle import oracle_threads, ssd_bwd_ref, ssd_fwd_ref
+    (q, k, v, la, h0, dout), nb, used = oracle_sample(w, oracle_threads())
     toks, t0, reps = 0, time.perf_counter(), 0
     while True:
         ssd_fwd_ref(q, k, v, la, h0)
         ssd_bwd_ref(q, k, v, la, h0, dout)
         reps += 1
-        toks += w.L * w.H
+        toks += nb * w.L * w.H
         el = time.perf_counter() - t0
         if el >= min_seconds or reps >= max_reps:
             break
-    return {"value": toks / el, "unit": "tokens/s", "cores": oracle_threads(), "kind": "oracle",
-            "sample": f"batch entry 0 of {w.name} (1 x {w.L} x {w.H} heads, all groups), "
-                      f"float64 fwd+bwd, {reps} rep(s), {el:.1f} s"}
+    return {"value": toks / el, "unit": "tokens/s", "cores": used, "kind": "oracle",
+            "sample": f"batch entries 0..{nb - 1} of {w.name} ({nb} x {w.L} x {w.H} heads, "
+                      f"all groups), float64 fwd+bwd, {reps} rep(s), {el:.1f} s"}
+
+
+def max_over_ranks(x, device=None):
+    """The largest x over all ranks (x itself when not distributed)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tokens_per_s(tokens_per_rank, world, ms):
+    """Whole-job throughput of `world` replicas that each processed
+    tokens_per_rank tokens, over the slowest rank's ms."""
+    return tokens_per_rank * world / (ms / 1e3)
 
 
 def run_reference(args, w):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return 0
-    import numpy as np
     from oracle import oracle_threads, ssd_bwd_ref, ssd_fwd_ref
-    from ssd_chunked_scan_gb300.inputs import workload_inputs
-    q, k, v, la, h0, dout = workload_inputs(w)
-    # bounded sample: batch entry 0, group 0 and its heads, full sequence
-    hpg = w.H // w.G
-    sq = lambda x: np.ascontiguousarray(x[:1, :, :1])
-    sv = lambda x: np.ascontiguousarray(x[:1, :, :hpg])
-    q, k = sq(q), sq(k)
-    v, la, dout = sv(v), sv(la), sv(dout)
-    h0 = np.ascontiguousarray(h0[:1, :hpg])
+    (q, k, v, la, h0, dout), nb, used = oracle_sample(w, oracle_threads())
 
     def step():
         ssd_fwd_ref(q, k, v, la, h0)
@@ -237,9 +253,10 @@ def run_reference(args, w):
     for _ in range(args.steps):
         step()
     el = time.perf_counter() - t0
-    toks = w.L * hpg
+    toks = nb * w.L * w.H
     val = toks * args.steps / el
-    sample = f"batch entry 0, group 0 ({hpg} heads) of {w.name}, full L={w.L}, float64 fwd+bwd per step"
+    sample = (f"batch entries 0..{nb - 1} ({nb * w.H} heads, all groups) of {w.name}, "
+              f"full L={w.L}, float64 fwd+bwd per step")
     line = {"impl": "reference", "metric": METRIC, "value": val, "unit": "tokens/s",
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": el / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
@@ -247,7 +264,7 @@ def run_reference(args, w):
             "config": {"workload": w.name, "mode": "fwd_bwd", "B": w.B, "G": w.G, "H": w.H,
                        "L": w.L, "dk": w.dk, "dv": w.dv, "chunk": w.chunk,
                        "sample_tokens_per_step": toks},
-            "cpu_baseline": {"value": val, "unit": "tokens/s", "cores": oracle_threads(),
+            "cpu_baseline": {"value": val, "unit": "tokens/s", "cores": used,
                              "kind": "oracle", "sample": sample},
             "e2e": {"value": val, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
@@ -327,11 +344,7 @@ def main():
     th1 = time.time()
     barrier()
     launches = ssd.ssd_launch_count() - n0
-    ms = e0.elapsed_time(e1) / args.steps
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, dev)
     if ssd.ssd_last_device_error() != 0:
         raise RuntimeError("device error word set during the timed region")
 
@@ -387,14 +400,10 @@ def main():
         g1.record(stream)
         torch.cuda.synchronize(dev)
         barrier()
-        e2e_ms = g0.elapsed_time(g1) / args.steps
-        if world > 1:
-            t = torch.tensor([e2e_ms], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e2e_ms = float(t.item())
+        e2e_ms = max_over_ranks(g0.elapsed_time(g1) / args.steps, dev)
         h2d = sum(x.numel() * x.element_size() for x in (host if fb else host[:5]))
         d2h = h_out.numel() * 4 + (sum(x.numel() * x.element_size() for x in h_grads.values()) if fb else 0)
-        e2e = {"value": w.tokens * world / (e2e_ms / 1e3), "unit": "tokens/s",
+        e2e = {"value": job_tokens_per_s(w.tokens, world, e2e_ms), "unit": "tokens/s",
                "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
 
     if rank != 0:
@@ -434,7 +443,7 @@ def main():
     t_hbm = bytes_fb / (peaks["hbm_gbs"] * 1e9)
     t_tc = fl_fb / (peaks["bf16_tflops"] * TF32_OVER_BF16 * 1e12)
     step_roof_s = max(t_hbm, t_tc)
-    value = w.tokens * world / (ms / 1e3)
+    value = job_tokens_per_s(w.tokens, world, ms)
     page_ms = PAGE_FWD_BWD_MS.get(w.name)
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
