@@ -37,6 +37,11 @@ PAGE_FWD_BWD_MS = {"g2h8_d128_L8192_long": 11.883, "g2h8_d128_L2048": 3.210,
 PAGE_FWD_MS = {"g2h8_d128_L8192_long": 4.182, "g2h8_d128_L2048": 1.170,
                "g1h24_dk128_dv64_L8192": 3.461, "g1h1_d128_L512": 0.08903,
                "g2h4_dk48_dv40_L2048": 0.3709}
+# the same page's memory records for impl "chunked", g2h8_d128 (RTX 3090, 24 GB):
+# peak MB of fwd / fwd_bwd at seq 8192, and the largest seq (doubling) that ran
+PAGE_PEAK_MB = {"fwd": 1128.0, "fwd_bwd": 1323.007568359375}
+PAGE_MAX_LEN = 65536
+MiB = 1 << 20
 
 
 def load_peaks():
@@ -272,6 +277,100 @@ def run_reference(args, w):
     return 0
 
 
+def resident_bytes(B, L, G, H, dk, dv, mode):
+    """Bytes of the caller's tensors one step touches: the five arguments and
+    out, plus dout and the five gradients for fwd_bwd."""
+    args = 4 * (2 * B * L * G * dk + B * L * H * dv + B * L * H + B * H * dk * dv)
+    out = 4 * B * L * H * dv
+    if mode == "fwd":
+        return args + out
+    return 2 * args + out + 4 * B * L * H * dv
+
+
+def measure_peak(ssd, torch, dev, fn, resident):
+    """Peak device bytes of one call of fn: the caller's resident tensors plus
+    the high-water mark of the library's workspace pool during the call."""
+    torch.cuda.synchronize(dev)
+    ssd.ssd_pool_high_water(reset=True)
+    fn()
+    torch.cuda.synchronize(dev)
+    return resident + ssd.ssd_pool_high_water()
+
+
+def run_max_len(args, w):
+    """Largest sequence length (doubling from the workload's L) whose fwd_bwd
+    runs on one GPU, with the peak memory of each length that ran.  The next
+    length is not attempted once its predicted footprint (caller tensors plus
+    the reported workspace) exceeds 90% of the free device memory."""
+    import torch
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    from ssd_chunked_scan_gb300 import ssd
+    from ssd_chunked_scan_gb300.inputs import make_inputs_on_device
+    ssd.ssd_set_path(ssd.SSD_PATH_TC if args.path == "tc" else ssd.SSD_PATH_SIMT)
+    B, G, H, dk, dv, C = w.B, w.G, w.H, w.dk, w.dv, w.chunk
+
+    def need(L):
+        ws = max(ssd.ssd_fwd_workspace_bytes(B, L, G, H, dk, dv, C),
+                 ssd.ssd_bwd_workspace_bytes(B, L, G, H, dk, dv, C))
+        return resident_bytes(B, L, G, H, dk, dv, "fwd_bwd") + ws
+
+    runs, L, stop = [], w.L, None
+    P = 512  # prefix / suffix tokens compared with separate short runs
+    while True:
+        free, total = torch.cuda.mem_get_info(dev)
+        try:
+            ok_shape = need(L)
+        except ssd.SSDError as e:  # beyond what the path's index types take
+            stop = {"seq": L, "reason": str(e)}
+            break
+        if ok_shape > 0.9 * free:
+            stop = {"seq": L, "needed_mb": ok_shape / MiB, "free_mb": free / MiB,
+                    "reason": "predicted footprint above 90% of free device memory"}
+            break
+        q, k, v, la, h0, dout = make_inputs_on_device(dev, B, L, G, H, dk, dv, w.seed, w.la_mu)
+        out = torch.empty((B, L, H, dv), device=dev)
+        grads = {"dq": torch.empty_like(q), "dk": torch.empty_like(k), "dv": torch.empty_like(v),
+                 "dlog_alpha": torch.empty_like(la), "dh0": torch.empty_like(h0)}
+
+        def step():
+            ssd.ssd_fwd(q, k, v, la, h0, chunk=C, out=out)
+            ssd.ssd_bwd(q, k, v, la, h0, dout, chunk=C, grads=grads)
+        t0 = time.perf_counter()
+        peak = measure_peak(ssd, torch, dev, step, resident_bytes(B, L, G, H, dk, dv, "fwd_bwd"))
+        sec = time.perf_counter() - t0
+        if ssd.ssd_last_device_error() != 0:
+            raise RuntimeError(f"device error word set at L={L}")
+        finite = all(bool(torch.isfinite(t).all()) for t in [out] + list(grads.values()))
+        # self-consistency: the first P outputs depend only on the first P
+        # inputs; dk, dv of the last P tokens only on the last P inputs
+        pre = [x[:, :P].contiguous() for x in (q, k, v, la, dout)]
+        suf = [x[:, L - P:].contiguous() for x in (q, k, v, la, dout)]
+        o_pre = ssd.ssd_fwd(pre[0], pre[1], pre[2], pre[3], h0, chunk=C)
+        g_suf = ssd.ssd_bwd(suf[0], suf[1], suf[2], suf[3], None, suf[4], chunk=C)
+        torch.cuda.synchronize(dev)
+        rel = lambda a, b: float((a - b).abs().max() / b.abs().max().clamp_min(1e-30))
+        cons = {"out_prefix": rel(out[:, :P], o_pre), "dk_suffix": rel(grads["dk"][:, L - P:], g_suf["dk"]),
+                "dv_suffix": rel(grads["dv"][:, L - P:], g_suf["dv"])}
+        runs.append({"seq": L, "peak_mb": peak / MiB, "predicted_mb": ok_shape / MiB,
+                     "fwd_bwd_s": sec, "finite": finite, "consistency_rel_err": cons})
+        del q, k, v, la, h0, dout, out, grads, pre, suf, o_pre, g_suf
+        torch.cuda.empty_cache()
+        L *= 2
+    best = runs[-1] if runs else None
+    line = {"metric": "largest sequence length for fwd_bwd on one GPU (doubling)",
+            "value": best["seq"] if best else 0, "unit": "tokens", "n_gpus": 1,
+            "higher_is_better": True, "dtype": "tf32" if args.path == "tc" else "f32",
+            "data": "synthetic (seeded, generated on the device)",
+            "config": {"workload": w.name, "path": args.path, "B": B, "G": G, "H": H,
+                       "dk": dk, "dv": dv, "chunk": C, "start_seq": w.L},
+            "largest_ok": best, "runs": runs, "first_not_run": stop,
+            "device_total_mb": torch.cuda.mem_get_info(dev)[1] / MiB,
+            "page_context": {"rtx3090_24gb_chunked_largest_seq": PAGE_MAX_LEN}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -282,8 +381,9 @@ def main():
     ap.add_argument("--workload", default=WORKLOAD)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--mode", default="fwd_bwd", choices=["fwd_bwd", "fwd"],
-                    help="fwd times ssd_fwd alone (a step is then one forward pass)")
+    ap.add_argument("--mode", default="fwd_bwd", choices=["fwd_bwd", "fwd", "max_len"],
+                    help="fwd times ssd_fwd alone (a step is then one forward pass); "
+                         "max_len finds the largest sequence length fwd_bwd runs at")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -291,6 +391,8 @@ def main():
     w = BY_NAME[args.workload]
     if args.impl == "reference":
         return run_reference(args, w)
+    if args.mode == "max_len":
+        return run_max_len(args, w)
 
     import torch
     import torch.distributed as dist
@@ -369,6 +471,21 @@ def main():
     f1.record(stream)
     torch.cuda.synchronize(dev)
     fwd_ms = f0.elapsed_time(f1) / args.steps
+
+    # peak device memory of one step (caller tensors + workspace high-water)
+    dims = (w.B, w.L, w.G, w.H, w.dk, w.dv)
+    memory = {
+        "peak_mb_fwd": measure_peak(ssd, torch, dev,
+                                    lambda: ssd.ssd_fwd(q, k, v, la, h0, chunk=w.chunk, out=out),
+                                    resident_bytes(*dims, "fwd")) / MiB,
+        "peak_mb_fwd_bwd": measure_peak(ssd, torch, dev, step,
+                                        resident_bytes(*dims, args.mode)) / MiB,
+        "resident_mb_fwd_bwd": resident_bytes(*dims, "fwd_bwd") / MiB,
+        "workspace_mb_fwd": ssd.ssd_fwd_workspace_bytes(*dims, w.chunk) / MiB,
+        "workspace_mb_bwd": ssd.ssd_bwd_workspace_bytes(*dims, w.chunk) / MiB,
+        "definition": "caller tensors the call touches + high-water of the library's "
+                      "workspace pool during the call",
+    }
 
     # end to end through the public API: pinned host inputs -> device, fwd+bwd,
     # out and every gradient -> pinned host, every step
@@ -467,7 +584,9 @@ def main():
         "gpu_launches": launches,
         "clocks": clk,
         "e2e": e2e,
-        "page_context": {"rtx3090_fwd_bwd_ms": page_ms, "rtx3090_fwd_ms": PAGE_FWD_MS.get(w.name)},
+        "memory": memory,
+        "page_context": {"rtx3090_fwd_bwd_ms": page_ms, "rtx3090_fwd_ms": PAGE_FWD_MS.get(w.name),
+                         "rtx3090_chunked_peak_mb": PAGE_PEAK_MB if w.name == WORKLOAD else None},
     }
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_oracle_sample(w)

@@ -53,7 +53,11 @@
  *                 formed with fp32 atomic adds when H > G, so their last
  *                 bits may differ from run to run.
  *   SSD_PATH_SIMT all-fp32 CUDA-core path.  Supports chunk in {16, 32, 64},
- *                 1 <= dk, dv <= 128.
+ *                 1 <= dk, dv <= 128.  Its workspace holds every chunk's
+ *                 state (B*H*ceil(L/chunk)*dk*dv floats per pass), where
+ *                 the tensor-core path keeps one state per segment (about
+ *                 four segments per SM in all, whatever L); see
+ *                 ssd_fwd_workspace_bytes.
  */
 #ifndef SSD_H_
 #define SSD_H_
@@ -180,6 +184,29 @@ SSD_API int ssd_fwd_noalloc(const float *q, const float *k, const float *v,
                             int64_t B, int64_t L, int64_t G, int64_t H, int64_t dk,
                             int64_t dv, int64_t chunk, ssd_stream_t stream);
 SSD_API size_t ssd_fwd_noalloc_scratch_bytes(void);
+
+/*
+ * Memory.  The op keeps nothing between calls: besides the caller's tensors a
+ * call needs only its temporary workspace, which these report for the active
+ * path and the current device (the tensor-core path sizes its segment states
+ * by the device's SM count; without a device a count of 148 is assumed).
+ *   ssd_fwd_workspace_bytes  bytes ssd_fwd / ssd_fwd_ex take for this problem
+ *   ssd_bwd_workspace_bytes  bytes ssd_bwd / ssd_bwd_ex take for this problem
+ * Each returns the status the call itself would return from its shape checks
+ * (pointers are not involved) and writes 0 for an empty problem.  `bytes`
+ * must not be NULL.
+ *
+ * ssd_pool_high_water: the high-water mark, in bytes, of the current device's
+ * default stream-ordered memory pool (the pool the workspace comes from; it
+ * also counts anything else the process took from that pool with
+ * cudaMallocAsync).  bytes may be NULL; reset != 0 then lowers the mark to the
+ * memory in use now.  Returns SSD_ERR_CUDA without a usable device.
+ */
+SSD_API int ssd_fwd_workspace_bytes(int64_t B, int64_t L, int64_t G, int64_t H, int64_t dk,
+                                    int64_t dv, int64_t chunk, size_t *bytes);
+SSD_API int ssd_bwd_workspace_bytes(int64_t B, int64_t L, int64_t G, int64_t H, int64_t dk,
+                                    int64_t dv, int64_t chunk, size_t *bytes);
+SSD_API int ssd_pool_high_water(int reset, size_t *bytes);
 
 /* Select the arithmetic path for later calls in this process (all threads).
  * Returns SSD_ERR_ARG for an unknown value.  The initial path is SSD_PATH_TC,

@@ -43,13 +43,14 @@ int check_common(int64_t B, int64_t L, int64_t G, int64_t H, int64_t dk, int64_t
   return SSD_OK;
 }
 
-int check_path_shape(int path, int64_t L, int64_t dk, int64_t dv, int64_t chunk) {
+int check_path_shape(int path, int64_t B, int64_t L, int64_t dk, int64_t dv, int64_t chunk) {
   if (path == SSD_PATH_SIMT) {
     if (chunk != 16 && chunk != 32 && chunk != 64) return SSD_ERR_CHUNK;
     if (dk > 128 || dv > 128) return SSD_ERR_UNSUPPORTED;
   } else {
     int rc = ssd::tc::check_shape(dk, dv, chunk);
     if (rc) return rc;
+    if (B * L >= ((int64_t)1 << 31)) return SSD_ERR_UNSUPPORTED;  // 32-bit TMA row index
   }
   if (ssd::cdiv(L, chunk) > 0x7fffffffLL) return SSD_ERR_UNSUPPORTED;
   return SSD_OK;
@@ -138,7 +139,7 @@ int ssd_fwd_ex(const float *q, const float *k, const float *v, const float *log_
   int rc = check_common(B, L, G, H, dk, dv, chunk);
   if (rc) return rc;
   const int path = current_path();
-  rc = check_path_shape(path, L, dk, dv, chunk);
+  rc = check_path_shape(path, B, L, dk, dv, chunk);
   if (rc) return rc;
   if (misaligned(q) || misaligned(k) || misaligned(v) || misaligned(log_alpha) ||
       misaligned(h0) || misaligned(out) || misaligned(hT))
@@ -177,7 +178,7 @@ int ssd_bwd_ex(const float *q, const float *k, const float *v, const float *log_
   int rc = check_common(B, L, G, H, dk_dim, dv_dim, chunk);
   if (rc) return rc;
   const int path = current_path();
-  rc = check_path_shape(path, L, dk_dim, dv_dim, chunk);
+  rc = check_path_shape(path, B, L, dk_dim, dv_dim, chunk);
   if (rc) return rc;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (misaligned(q) || misaligned(k) || misaligned(v) || misaligned(log_alpha) ||
@@ -214,6 +215,62 @@ int ssd_bwd(const float *q, const float *k, const float *v, const float *log_alp
             int64_t dk_dim, int64_t dv_dim, int64_t chunk, ssd_stream_t stream) {
   return ssd_bwd_ex(q, k, v, log_alpha, h0, dout, nullptr, dq, dk, dv, dlog_alpha, dh0, B, L, G,
                     H, dk_dim, dv_dim, chunk, stream);
+}
+
+int ssd_fwd_workspace_bytes(int64_t B, int64_t L, int64_t G, int64_t H, int64_t dk, int64_t dv,
+                            int64_t chunk, size_t *bytes) {
+  if (!bytes) return SSD_ERR_ARG;
+  *bytes = 0;
+  int rc = check_common(B, L, G, H, dk, dv, chunk);
+  if (rc) return rc;
+  const int path = current_path();
+  rc = check_path_shape(path, B, L, dk, dv, chunk);
+  if (rc) return rc;
+  if (B == 0 || L == 0) return SSD_OK;
+  const ssd::Geo g = make_geo(B, L, G, H, dk, dv, chunk);
+  *bytes = path == SSD_PATH_SIMT ? ssd::simt::fwd_workspace_bytes(g)
+                                 : ssd::tc::fwd_workspace_bytes(g);
+  return SSD_OK;
+}
+
+int ssd_bwd_workspace_bytes(int64_t B, int64_t L, int64_t G, int64_t H, int64_t dk, int64_t dv,
+                            int64_t chunk, size_t *bytes) {
+  if (!bytes) return SSD_ERR_ARG;
+  *bytes = 0;
+  int rc = check_common(B, L, G, H, dk, dv, chunk);
+  if (rc) return rc;
+  const int path = current_path();
+  rc = check_path_shape(path, B, L, dk, dv, chunk);
+  if (rc) return rc;
+  if (B == 0 || L == 0) return SSD_OK;
+  const ssd::Geo g = make_geo(B, L, G, H, dk, dv, chunk);
+  *bytes = path == SSD_PATH_SIMT ? ssd::simt::bwd_workspace_bytes(g)
+                                 : ssd::tc::bwd_workspace_bytes(g);
+  return SSD_OK;
+}
+
+int ssd_pool_high_water(int reset, size_t *bytes) {
+  if (bytes) *bytes = 0;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) { cudaGetLastError(); return SSD_ERR_CUDA; }
+  cudaMemPool_t pool;
+  if (cudaDeviceGetDefaultMemPool(&pool, dev) != cudaSuccess) { cudaGetLastError(); return SSD_ERR_CUDA; }
+  if (bytes) {
+    uint64_t v = 0;
+    if (cudaMemPoolGetAttribute(pool, cudaMemPoolAttrUsedMemHigh, &v) != cudaSuccess) {
+      cudaGetLastError();
+      return SSD_ERR_CUDA;
+    }
+    *bytes = (size_t)v;
+  }
+  if (reset) {
+    uint64_t zero = 0;  // resets the mark to the memory in use now
+    if (cudaMemPoolSetAttribute(pool, cudaMemPoolAttrUsedMemHigh, &zero) != cudaSuccess) {
+      cudaGetLastError();
+      return SSD_ERR_CUDA;
+    }
+  }
+  return SSD_OK;
 }
 
 int ssd_last_device_error(ssd_stream_t stream) {

@@ -71,3 +71,21 @@ def make_state_cotangent(B, H, dk, dv, seed):
     scaled by 1/sqrt(dk), the size of one q_t dout_t^T term."""
     rng = np.random.default_rng(seed + 7919)
     return (rng.standard_normal((B, H, dk, dv)) / np.sqrt(dk)).astype(np.float32)
+
+
+def make_inputs_on_device(device, B, L, G, H, dk, dv, seed, la_mu=0.0):
+    """Seeded inputs generated on a CUDA device (for sizes too large to make
+    on the host), with make_inputs' distributions but not its values:
+    q, k ~ N(0,1)/sqrt(dk), v, dout ~ N(0,1), log_alpha = -softplus(N(la_mu,1)),
+    h0 ~ 0.1 N(0,1), all float32 and contiguous."""
+    import torch
+    gen = torch.Generator(device=device)
+    gen.manual_seed(seed)
+    r = lambda *sh: torch.randn(sh, generator=gen, device=device)
+    q = r(B, L, G, dk) / dk ** 0.5
+    k = r(B, L, G, dk) / dk ** 0.5
+    v = r(B, L, H, dv)
+    la = -torch.nn.functional.softplus(r(B, L, H) + la_mu)
+    h0 = 0.1 * r(B, H, dk, dv)
+    dout = r(B, L, H, dv)
+    return q, k, v, la, h0, dout

@@ -68,6 +68,12 @@ def _load():
     lib.ssd_trace_get.argtypes = [ctypes.c_int, ctypes.c_char_p, ctypes.c_int,
                                   ctypes.POINTER(ctypes.c_longlong), ctypes.POINTER(ctypes.c_double)]
     lib.ssd_trace_reset.argtypes = []
+    lib.ssd_fwd_workspace_bytes.argtypes = [i64] * 7 + [ctypes.POINTER(ctypes.c_size_t)]
+    lib.ssd_fwd_workspace_bytes.restype = ctypes.c_int
+    lib.ssd_bwd_workspace_bytes.argtypes = [i64] * 7 + [ctypes.POINTER(ctypes.c_size_t)]
+    lib.ssd_bwd_workspace_bytes.restype = ctypes.c_int
+    lib.ssd_pool_high_water.argtypes = [ctypes.c_int, ctypes.POINTER(ctypes.c_size_t)]
+    lib.ssd_pool_high_water.restype = ctypes.c_int
     lib.ssd_fwd_noalloc.argtypes = [p] * 6 + [i64] * 7 + [p]
     lib.ssd_fwd_noalloc.restype = ctypes.c_int
     lib.ssd_fwd_noalloc_scratch_bytes.argtypes = []
@@ -123,6 +129,34 @@ def ssd_trace_collect() -> dict:
             raise SSDError(rc, "ssd_trace_get")
         res[buf.value.decode()] = (int(cnt.value), float(ms.value))
     return res
+
+
+def ssd_fwd_workspace_bytes(B, L, G, H, dk, dv, chunk=64) -> int:
+    """Device workspace bytes ssd_fwd takes for this problem on the active path."""
+    n = ctypes.c_size_t(0)
+    rc = LIB.ssd_fwd_workspace_bytes(B, L, G, H, dk, dv, chunk, ctypes.byref(n))
+    if rc:
+        raise SSDError(rc, "ssd_fwd_workspace_bytes")
+    return int(n.value)
+
+
+def ssd_bwd_workspace_bytes(B, L, G, H, dk, dv, chunk=64) -> int:
+    """Device workspace bytes ssd_bwd takes for this problem on the active path."""
+    n = ctypes.c_size_t(0)
+    rc = LIB.ssd_bwd_workspace_bytes(B, L, G, H, dk, dv, chunk, ctypes.byref(n))
+    if rc:
+        raise SSDError(rc, "ssd_bwd_workspace_bytes")
+    return int(n.value)
+
+
+def ssd_pool_high_water(reset=False) -> int:
+    """High-water bytes of the current device's default stream-ordered pool
+    (read before an optional reset to the memory in use now)."""
+    n = ctypes.c_size_t(0)
+    rc = LIB.ssd_pool_high_water(1 if reset else 0, ctypes.byref(n))
+    if rc:
+        raise SSDError(rc, "ssd_pool_high_water")
+    return int(n.value)
 
 
 def _stream(stream):

@@ -32,6 +32,9 @@ def lib():
     l.ssd_fwd_ex.argtypes = [p] * 7 + [i64] * 7 + [p]
     l.ssd_bwd_ex.argtypes = [p] * 12 + [i64] * 7 + [p]
     l.ssd_strerror.restype = ctypes.c_char_p
+    sz = ctypes.POINTER(ctypes.c_size_t)
+    l.ssd_fwd_workspace_bytes.argtypes = [i64] * 7 + [sz]
+    l.ssd_bwd_workspace_bytes.argtypes = [i64] * 7 + [sz]
     return l
 
 
@@ -111,3 +114,31 @@ def test_injected_workspace_failure_is_reported_before_launch(lib, monkeypatch):
     assert _bwd(lib) == 5
     assert _fwd_ex(lib) == 5
     assert _bwd_ex(lib) == 5
+
+
+def _ws(lib, fn, *dims):
+    n = ctypes.c_size_t(123)
+    rc = getattr(lib, fn)(*dims, ctypes.byref(n))
+    return rc, n.value
+
+
+def test_workspace_queries(lib):
+    # all-fp32 path: one state per chunk and pass, plus per-chunk decays
+    assert lib.ssd_set_path(1) == 0
+    B, L, G, H, dk, dv, C = 2, 1000, 2, 4, 48, 40, 64
+    N = -(-L // C)
+    assert _ws(lib, "ssd_fwd_workspace_bytes", B, L, G, H, dk, dv, C) == (
+        0, 4 * (B * H * N * dk * dv + B * H * N))
+    assert _ws(lib, "ssd_bwd_workspace_bytes", B, L, G, H, dk, dv, C) == (
+        0, 4 * (2 * B * H * N * dk * dv + 2 * B * H * N + B * H * dk * dv))
+    assert _ws(lib, "ssd_fwd_workspace_bytes", B, L, G, H, dk, dv, 48)[0] == 3
+    assert _ws(lib, "ssd_fwd_workspace_bytes", B, 0, G, H, dk, dv, C) == (0, 0)
+    assert lib.ssd_fwd_workspace_bytes(B, L, G, H, dk, dv, C, None) == 1
+    # tensor-core path: the segment states do not grow with L
+    assert lib.ssd_set_path(0) == 0
+    rc1, a = _ws(lib, "ssd_bwd_workspace_bytes", 4, 8192, 2, 8, 128, 128, 64)
+    rc2, b = _ws(lib, "ssd_bwd_workspace_bytes", 4, 8 * 8192, 2, 8, 128, 128, 64)
+    assert rc1 == rc2 == 0 and 0 < a < b < 8 * a
+    assert b - a == pytest.approx(4 * 3 * 4 * 7 * 8192 * 8, rel=0.05)  # per-token arrays only
+    assert _ws(lib, "ssd_fwd_workspace_bytes", 1 << 16, 1 << 15, 1, 1, 8, 8, 64)[0] == 4  # B*L >= 2^31
+    assert _ws(lib, "ssd_fwd_workspace_bytes", 1, 100, 1, 1, 12, 8, 64)[0] == 4          # dk % 8
