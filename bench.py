@@ -107,6 +107,14 @@ def kernel_costs(w, sms=152):
         c[n] = (3 * qk + 2 * vv + 2 * la + sst, fw + BL * H * dk * 2, "hbm")
     c["tc.dla_intra"] = (2 * qk + 2 * vv + 2 * la, BL * (G * C * dk + H * C * dv + H * C), "hbm")
     c["tc.dla"] = (4 * la + 2 * sst, BL * H * 4 + 2 * B * H * nseg * dk * dv, "hbm")
+    # sequential kernels (chunk = 1): fp32 state updates and reductions, one
+    # token at a time; E arrays hold one float per token, head and column block
+    nblk = -(-dv // 32)
+    e = B * L * H * nblk * f
+    c["seq.sweep_out"] = (2 * qk + 2 * vv + la + 2 * h0, BL * H * 4 * dk * dv, "alu")
+    c["seq.sweep_dq"] = (3 * qk + 2 * vv + la + h0 + e, BL * H * 6 * dk * dv, "alu")
+    c["seq.sweep_dkdv"] = (3 * qk + 3 * vv + la + 2 * h0 + e, BL * H * 6 * dk * dv, "alu")
+    c["seq.dla"] = (2 * e + la, BL * H * 2 * nblk, "hbm")
     return c
 
 
@@ -379,6 +387,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--path", default=os.environ.get("SSD_BENCH_PATH", "tc"), choices=["tc", "simt"])
     ap.add_argument("--workload", default=WORKLOAD)
+    ap.add_argument("--chunk", type=int, default=None,
+                    help="override the workload's chunk length (1: the sequential kernels)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--mode", default="fwd_bwd", choices=["fwd_bwd", "fwd", "max_len"],
@@ -389,6 +399,9 @@ def main():
 
     from ssd_chunked_scan_gb300.inputs import BY_NAME
     w = BY_NAME[args.workload]
+    if args.chunk:
+        import dataclasses
+        w = dataclasses.replace(w, chunk=args.chunk)
     if args.impl == "reference":
         return run_reference(args, w)
     if args.mode == "max_len":
@@ -567,7 +580,7 @@ def main():
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
         "higher_is_better": True, "scaling": "weak",
         "vs_baseline": (value / (w.tokens / (page_ms / 1e3))) if page_ms else None,
-        "dtype": "tf32" if args.path == "tc" else "f32", "data": "synthetic",
+        "dtype": "tf32" if (args.path == "tc" and w.chunk != 1) else "f32", "data": "synthetic",
         "config": {"workload": w.name, "mode": args.mode, "path": args.path, "B": w.B, "G": w.G,
                    "H": w.H, "L": w.L, "dk": w.dk, "dv": w.dv, "chunk": w.chunk,
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",

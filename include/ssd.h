@@ -44,7 +44,8 @@
  *     stream.  Calls on different streams may run concurrently.
  *   - No function throws or aborts; each returns an ssd_status code.
  *
- * Two arithmetic paths implement the same op (ssd_set_path):
+ * Two arithmetic paths implement the chunked evaluation (ssd_set_path), and
+ * chunk == 1 selects a third, sequential one:
  *   SSD_PATH_TC   tensor-core path: tcgen05.mma (kind::tf32) with the
  *                 accumulators in tensor memory; operands rounded to TF32
  *                 (to nearest), accumulation and state passing in fp32.
@@ -58,6 +59,11 @@
  *                 the tensor-core path keeps one state per segment (about
  *                 four segments per SM in all, whatever L); see
  *                 ssd_fwd_workspace_bytes.
+ *   chunk == 1    (either path) the sequential evaluation: the recurrence one
+ *                 token at a time, the state in registers, all fp32, no
+ *                 workspace in the forward (suits decoding a few tokens with
+ *                 h0 / hT).  1 <= dk, dv <= 128.  Its backward forms dq and
+ *                 dk with fp32 atomic adds (last bits may vary run to run).
  */
 #ifndef SSD_H_
 #define SSD_H_
@@ -103,8 +109,8 @@ typedef enum ssd_path { SSD_PATH_TC = 0, SSD_PATH_SIMT = 1 } ssd_path;
  *   log_alpha  [B,L,H]      read (finite)
  *   h0         [B,H,dk,dv]  read, or NULL for zeros
  *   out        [B,L,H,dv]   written
- *   chunk      the chunk length of the chunked evaluation; results do not
- *              depend on it beyond rounding.
+ *   chunk      the chunk length of the chunked evaluation (1: sequential);
+ *              results do not depend on it beyond rounding.
  */
 SSD_API int ssd_fwd(const float *q, const float *k, const float *v,
             const float *log_alpha, const float *h0, float *out,

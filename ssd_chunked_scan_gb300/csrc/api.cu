@@ -6,6 +6,7 @@
 
 #include "../../include/ssd.h"
 #include "common.cuh"
+#include "seq.h"
 #include "simt.h"
 #include "tc.h"
 
@@ -43,8 +44,18 @@ int check_common(int64_t B, int64_t L, int64_t G, int64_t H, int64_t dk, int64_t
   return SSD_OK;
 }
 
+// Which kernels serve a call: chunk == 1 is the sequential evaluation on every
+// path; otherwise the selected path's chunked kernels.
+enum class Impl { TC, SIMT, SEQ };
+Impl impl_of(int path, int64_t chunk) {
+  if (chunk == 1) return Impl::SEQ;
+  return path == SSD_PATH_SIMT ? Impl::SIMT : Impl::TC;
+}
+
 int check_path_shape(int path, int64_t B, int64_t L, int64_t dk, int64_t dv, int64_t chunk) {
-  if (path == SSD_PATH_SIMT) {
+  if (chunk == 1) {
+    if (dk > 128 || dv > 128) return SSD_ERR_UNSUPPORTED;
+  } else if (path == SSD_PATH_SIMT) {
     if (chunk != 16 && chunk != 32 && chunk != 64) return SSD_ERR_CHUNK;
     if (dk > 128 || dv > 128) return SSD_ERR_UNSUPPORTED;
   } else {
@@ -153,14 +164,15 @@ int ssd_fwd_ex(const float *q, const float *k, const float *v, const float *log_
   }
   if (!q || !k || !v || !log_alpha || !out) return SSD_ERR_ARG;
   const ssd::Geo g = make_geo(B, L, G, H, dk, dv, chunk);
-  const size_t wsb = path == SSD_PATH_SIMT ? ssd::simt::fwd_workspace_bytes(g)
-                                           : ssd::tc::fwd_workspace_bytes(g);
+  const Impl im = impl_of(path, chunk);
+  if (im == Impl::SEQ) return from_cuda(ssd::seq::fwd(q, k, v, log_alpha, h0, out, hT, g, s));
+  const size_t wsb = im == Impl::SIMT ? ssd::simt::fwd_workspace_bytes(g)
+                                      : ssd::tc::fwd_workspace_bytes(g);
   void *ws = nullptr;
   rc = ws_alloc(&ws, wsb, s);
   if (rc) return rc;
-  cudaError_t e = path == SSD_PATH_SIMT
-                      ? ssd::simt::fwd(q, k, v, log_alpha, h0, out, hT, g, ws, s)
-                      : ssd::tc::fwd(q, k, v, log_alpha, h0, out, hT, g, ws, s);
+  cudaError_t e = im == Impl::SIMT ? ssd::simt::fwd(q, k, v, log_alpha, h0, out, hT, g, ws, s)
+                                   : ssd::tc::fwd(q, k, v, log_alpha, h0, out, hT, g, ws, s);
   if (ws) cudaFreeAsync(ws, s);
   return from_cuda(e);
 }
@@ -194,17 +206,20 @@ int ssd_bwd_ex(const float *q, const float *k, const float *v, const float *log_
   if (!q || !k || !v || !log_alpha || !dout || !dq || !dk || !dv || !dlog_alpha)
     return SSD_ERR_ARG;
   const ssd::Geo g = make_geo(B, L, G, H, dk_dim, dv_dim, chunk);
-  const size_t wsb = path == SSD_PATH_SIMT ? ssd::simt::bwd_workspace_bytes(g)
-                                           : ssd::tc::bwd_workspace_bytes(g);
+  const Impl im = impl_of(path, chunk);
+  const size_t wsb = im == Impl::SEQ    ? ssd::seq::bwd_workspace_bytes(g)
+                     : im == Impl::SIMT ? ssd::simt::bwd_workspace_bytes(g)
+                                        : ssd::tc::bwd_workspace_bytes(g);
   void *ws = nullptr;
   rc = ws_alloc(&ws, wsb, s);
   if (rc) return rc;
-  cudaError_t e =
-      path == SSD_PATH_SIMT
-          ? ssd::simt::bwd(q, k, v, log_alpha, h0, dout, dhT, dq, dk, dv, dlog_alpha, dh0, g,
-                           ws, s)
-          : ssd::tc::bwd(q, k, v, log_alpha, h0, dout, dhT, dq, dk, dv, dlog_alpha, dh0, g, ws,
-                         s);
+  cudaError_t e;
+  if (im == Impl::SEQ)
+    e = ssd::seq::bwd(q, k, v, log_alpha, h0, dout, dhT, dq, dk, dv, dlog_alpha, dh0, g, ws, s);
+  else if (im == Impl::SIMT)
+    e = ssd::simt::bwd(q, k, v, log_alpha, h0, dout, dhT, dq, dk, dv, dlog_alpha, dh0, g, ws, s);
+  else
+    e = ssd::tc::bwd(q, k, v, log_alpha, h0, dout, dhT, dq, dk, dv, dlog_alpha, dh0, g, ws, s);
   if (ws) cudaFreeAsync(ws, s);
   return from_cuda(e);
 }
@@ -228,8 +243,10 @@ int ssd_fwd_workspace_bytes(int64_t B, int64_t L, int64_t G, int64_t H, int64_t 
   if (rc) return rc;
   if (B == 0 || L == 0) return SSD_OK;
   const ssd::Geo g = make_geo(B, L, G, H, dk, dv, chunk);
-  *bytes = path == SSD_PATH_SIMT ? ssd::simt::fwd_workspace_bytes(g)
-                                 : ssd::tc::fwd_workspace_bytes(g);
+  const Impl im = impl_of(path, chunk);
+  *bytes = im == Impl::SEQ    ? ssd::seq::fwd_workspace_bytes(g)
+           : im == Impl::SIMT ? ssd::simt::fwd_workspace_bytes(g)
+                              : ssd::tc::fwd_workspace_bytes(g);
   return SSD_OK;
 }
 
@@ -244,8 +261,10 @@ int ssd_bwd_workspace_bytes(int64_t B, int64_t L, int64_t G, int64_t H, int64_t 
   if (rc) return rc;
   if (B == 0 || L == 0) return SSD_OK;
   const ssd::Geo g = make_geo(B, L, G, H, dk, dv, chunk);
-  *bytes = path == SSD_PATH_SIMT ? ssd::simt::bwd_workspace_bytes(g)
-                                 : ssd::tc::bwd_workspace_bytes(g);
+  const Impl im = impl_of(path, chunk);
+  *bytes = im == Impl::SEQ    ? ssd::seq::bwd_workspace_bytes(g)
+           : im == Impl::SIMT ? ssd::simt::bwd_workspace_bytes(g)
+                              : ssd::tc::bwd_workspace_bytes(g);
   return SSD_OK;
 }
 

@@ -142,3 +142,15 @@ def test_workspace_queries(lib):
     assert b - a == pytest.approx(4 * 3 * 4 * 7 * 8192 * 8, rel=0.05)  # per-token arrays only
     assert _ws(lib, "ssd_fwd_workspace_bytes", 1 << 16, 1 << 15, 1, 1, 8, 8, 64)[0] == 4  # B*L >= 2^31
     assert _ws(lib, "ssd_fwd_workspace_bytes", 1, 100, 1, 1, 12, 8, 64)[0] == 4          # dk % 8
+
+
+@pytest.mark.parametrize("path", [0, 1])
+def test_chunk_one_is_sequential_on_every_path(lib, path):
+    assert lib.ssd_set_path(path) == 0
+    assert _ws(lib, "ssd_fwd_workspace_bytes", 2, 100, 1, 2, 5, 3, 1) == (0, 0)
+    B, L, H, dk, dv = 2, 100, 2, 5, 70
+    nblk = -(-dv // 32)
+    assert _ws(lib, "ssd_bwd_workspace_bytes", B, L, 1, H, dk, dv, 1) == (
+        0, 4 * (2 * nblk * B * L * H + B * H * dk * dv))
+    assert _ws(lib, "ssd_fwd_workspace_bytes", 2, 100, 1, 2, 129, 3, 1)[0] == 4
+    assert _fwd(lib, dk=5, dv=3, chunk=1, ptrs=(0x1000, 0x1004) + (0x1000,) * 4) == 2
