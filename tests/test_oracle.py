@@ -246,3 +246,17 @@ def test_empty_sequence_final_state():
     np.testing.assert_array_equal(hT, h0.astype(np.float64))
     dhT = np.ones(h0.shape)
     assert np.array_equal(ssd_bwd_ref(q, k, v, la, h0, dout, dhT=dhT)["dh0"], dhT)
+
+
+def test_dla_from_output_and_value_gradients():
+    # per head, q.dq_h - k.dk_h = out.dout - v.dv (both are <S_t, q dout^T> -
+    # <G_t, k v^T>), so dla is also the reverse cumulative sum of
+    # out.dout - v.dv plus <dhT, hT>
+    q, k, v, la, h0, dout = _case(2, 90, 2, 4, 6, 5, seed=36)
+    dhT = np.random.default_rng(7).standard_normal(h0.shape)
+    out, hT = ssd_fwd_ref(q, k, v, la, h0, return_final_state=True)
+    g = ssd_bwd_ref(q, k, v, la, h0, dout, dhT=dhT)
+    e = np.sum(out * dout.astype(np.float64), -1) - np.sum(v.astype(np.float64) * g["dv"], -1)
+    carry = np.einsum("bhij,bhij->bh", dhT, hT)
+    dla = np.flip(np.cumsum(np.flip(e, 1), 1), 1) + carry[:, None, :]
+    assert rel_err(dla, g["dlog_alpha"]) < 1e-10
