@@ -1,4 +1,5 @@
-"""Compile the float64 C oracle into ``oracle/libssd_oracle.so``.
+"""Compile the float64 C oracles (SSD scan, Mamba selective scan) into
+``oracle/libssd_oracle.so``.
 
 Test infrastructure: the oracle is what the CUDA library is checked against;
 nothing in the product library uses it.  Portable C, no ISA flags, so the same
@@ -10,16 +11,16 @@ import subprocess
 import sys
 
 HERE = os.path.dirname(os.path.abspath(__file__))
-SRC = os.path.join(HERE, "ssd_oracle.c")
+SRCS = [os.path.join(HERE, "ssd_oracle.c"), os.path.join(HERE, "mamba_oracle.c")]
 LIB = os.path.join(HERE, "libssd_oracle.so")
 
 
 def build_oracle(force: bool = False) -> str:
     if (not force and os.path.exists(LIB)
-            and os.path.getmtime(LIB) >= os.path.getmtime(SRC)):
+            and os.path.getmtime(LIB) >= max(os.path.getmtime(s) for s in SRCS)):
         return LIB
     cc = os.environ.get("CC", "gcc")
-    base = [cc, "-O2", "-fPIC", "-shared", "-std=c11", "-fno-fast-math", SRC, "-o", LIB, "-lm"]
+    base = [cc, "-O2", "-fPIC", "-shared", "-std=c11", "-fno-fast-math"] + SRCS + ["-o", LIB, "-lm"]
     try:
         subprocess.run(base[:1] + ["-fopenmp"] + base[1:], check=True,
                        stdout=subprocess.PIPE, stderr=subprocess.PIPE)

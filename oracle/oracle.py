@@ -117,3 +117,51 @@ def ssd_bwd_ref(q, k, v, log_alpha, h0, dout, per_head=False, dhT=None):
     if per_head:
         r["dq_heads"], r["dk_heads"] = dqh, dkh
     return r
+
+
+# ---- Mamba-1 selective scan ("kernel_mamba_cpu.json" records) --------------
+
+def _load_mamba():
+    lib = _load()
+    if not getattr(lib, "_mamba_ready", False):
+        d = ctypes.POINTER(ctypes.c_double)
+        i64 = ctypes.c_int64
+        lib.mamba_oracle_fwd.argtypes = [d] * 7 + [i64] * 4
+        lib.mamba_oracle_fwd.restype = ctypes.c_int
+        lib.mamba_oracle_bwd.argtypes = [d] * 13 + [i64] * 4
+        lib.mamba_oracle_bwd.restype = ctypes.c_int
+        lib._mamba_ready = True
+    return lib
+
+
+def mamba_fwd_ref(x, delta, A, Bm, Cm, Dk=None):
+    """float64 y [B,L,D] of the selective scan
+    h_t[n] = exp(delta_t A[d,n]) h_{t-1}[n] + delta_t B_t[n] x_t,
+    y_t = sum_n C_t[n] h_t[n] + D[d] x_t (h_{-1} = 0)."""
+    x, delta, A, Bm, Cm, Dk = map(_f64, (x, delta, A, Bm, Cm, Dk))
+    B, L, D = x.shape
+    N = A.shape[1]
+    y = np.empty((B, L, D))
+    rc = _load_mamba().mamba_oracle_fwd(_ptr(x), _ptr(delta), _ptr(A), _ptr(Bm), _ptr(Cm),
+                                        _ptr(Dk), _ptr(y), B, L, D, N)
+    if rc:
+        raise RuntimeError(f"mamba_oracle_fwd failed ({rc})")
+    return y
+
+
+def mamba_bwd_ref(x, delta, A, Bm, Cm, Dk, dy):
+    """float64 gradients of <dy, y>: dict dx, ddelta, dA, dB, dC, dD (dD None
+    when Dk is None)."""
+    x, delta, A, Bm, Cm, Dk, dy = map(_f64, (x, delta, A, Bm, Cm, Dk, dy))
+    B, L, D = x.shape
+    N = A.shape[1]
+    g = {"dx": np.empty((B, L, D)), "ddelta": np.empty((B, L, D)), "dA": np.empty((D, N)),
+         "dB": np.empty((B, L, N)), "dC": np.empty((B, L, N)),
+         "dD": np.empty((D,)) if Dk is not None else None}
+    rc = _load_mamba().mamba_oracle_bwd(
+        _ptr(x), _ptr(delta), _ptr(A), _ptr(Bm), _ptr(Cm), _ptr(Dk), _ptr(dy), _ptr(g["dx"]),
+        _ptr(g["ddelta"]), _ptr(g["dA"]), _ptr(g["dB"]), _ptr(g["dC"]), _ptr(g["dD"]),
+        B, L, D, N)
+    if rc:
+        raise RuntimeError(f"mamba_oracle_bwd failed ({rc})")
+    return g

@@ -89,3 +89,54 @@ def make_inputs_on_device(device, B, L, G, H, dk, dv, seed, la_mu=0.0):
     h0 = 0.1 * r(B, H, dk, dv)
     dout = r(B, L, H, dv)
     return q, k, v, la, h0, dout
+
+
+# ---- Mamba-1 selective scan ("kernel_mamba_cpu.json" records) --------------
+#
+# Shapes: batch 4, state 16, dim in {256, 512, 1024}, seq in {512, 2048, 8192}
+# (the records' ``shape`` blocks).  Distributions (not on the pages): x, B, C,
+# D, dy ~ N(0,1); delta log-uniform on [1e-3, 1e-1] (the range Mamba draws its
+# step sizes from); A[d,n] = -(n+1) exp(0.5 N(0,1)) (the S4D-real
+# initialisation -(n+1), perturbed per channel).  Draw order x, delta, A, B,
+# C, D, dy from one PCG64 stream per workload.
+
+@dataclass(frozen=True)
+class MambaWorkload:
+    name: str
+    B: int
+    L: int
+    D: int
+    N: int = 16
+    seed: int = 0
+
+    @property
+    def tokens(self) -> int:
+        """Channel-tokens per call: B * L * D."""
+        return self.B * self.L * self.D
+
+
+# index i gets seed 2000 + i
+MAMBA_WORKLOADS = [
+    MambaWorkload(f"mamba_d{d}_L{l}", 4, l, d, 16, seed=2000 + i)
+    for i, (l, d) in enumerate([(512, 256), (2048, 256), (512, 512), (2048, 512), (512, 1024),
+                                (2048, 1024), (8192, 256), (8192, 512), (8192, 1024)])
+]
+MAMBA_BY_NAME = {w.name: w for w in MAMBA_WORKLOADS}
+
+
+def make_mamba_inputs(B, L, D, N, seed, with_D=True, with_dy=True):
+    """float32 numpy arrays x, delta, A, Bm, Cm, Dk, dy (Dk / dy None if not asked)."""
+    rng = np.random.default_rng(seed)
+    f32 = np.float32
+    x = rng.standard_normal((B, L, D)).astype(f32)
+    delta = np.exp(rng.uniform(np.log(1e-3), np.log(1e-1), (B, L, D))).astype(f32)
+    A = (-(np.arange(1, N + 1)[None, :]) * np.exp(0.5 * rng.standard_normal((D, N)))).astype(f32)
+    Bm = rng.standard_normal((B, L, N)).astype(f32)
+    Cm = rng.standard_normal((B, L, N)).astype(f32)
+    Dk = rng.standard_normal((D,)).astype(f32) if with_D else None
+    dy = rng.standard_normal((B, L, D)).astype(f32) if with_dy else None
+    return x, delta, A, Bm, Cm, Dk, dy
+
+
+def mamba_workload_inputs(w: MambaWorkload, with_D=True, with_dy=True):
+    return make_mamba_inputs(w.B, w.L, w.D, w.N, w.seed, with_D, with_dy)
