@@ -5,7 +5,9 @@
 #include <cstring>
 
 #include "../../include/ssd.h"
+#include "../../include/ssd_mamba.h"
 #include "common.cuh"
+#include "mamba.h"
 #include "seq.h"
 #include "simt.h"
 #include "tc.h"
@@ -290,6 +292,74 @@ int ssd_pool_high_water(int reset, size_t *bytes) {
     }
   }
   return SSD_OK;
+}
+
+static int mamba_check(int64_t B, int64_t L, int64_t D, int64_t N) {
+  if (B < 0 || L < 0 || D < 1 || N < 1) return SSD_ERR_ARG;
+  if (N > 16) return SSD_ERR_UNSUPPORTED;
+  // grid limits: batch on grid z, segments (at most 1024 tokens each) on grid y
+  if (B > 65535 || (D + 15) / 16 > 0x7fffffffLL || L > (int64_t)65535 * 1024)
+    return SSD_ERR_UNSUPPORTED;
+  return SSD_OK;
+}
+
+int ssd_mamba_workspace_bytes(int bwd, int64_t B, int64_t L, int64_t D, int64_t N,
+                              size_t *bytes) {
+  if (!bytes) return SSD_ERR_ARG;
+  *bytes = 0;
+  int rc = mamba_check(B, L, D, N);
+  if (rc) return rc;
+  if (B == 0 || L == 0) return SSD_OK;
+  *bytes = bwd ? ssd::mamba::bwd_workspace_bytes(B, L, D, N)
+               : ssd::mamba::fwd_workspace_bytes(B, L, D, N);
+  return SSD_OK;
+}
+
+int ssd_mamba_fwd(const float *x, const float *delta, const float *A, const float *Bm,
+                  const float *Cm, const float *Dk, float *y, int64_t B, int64_t L, int64_t D,
+                  int64_t N, ssd_stream_t stream) {
+  int rc = mamba_check(B, L, D, N);
+  if (rc) return rc;
+  if (misaligned(x) || misaligned(delta) || misaligned(A) || misaligned(Bm) || misaligned(Cm) ||
+      misaligned(Dk) || misaligned(y))
+    return SSD_ERR_ALIGN;
+  if (B == 0 || L == 0) return SSD_OK;
+  if (!x || !delta || !A || !Bm || !Cm || !y) return SSD_ERR_ARG;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  void *ws = nullptr;
+  rc = ws_alloc(&ws, ssd::mamba::fwd_workspace_bytes(B, L, D, N), s);
+  if (rc) return rc;
+  cudaError_t e = ssd::mamba::fwd(x, delta, A, Bm, Cm, Dk, y, B, L, D, N, ws, s);
+  if (ws) cudaFreeAsync(ws, s);
+  return from_cuda(e);
+}
+
+int ssd_mamba_bwd(const float *x, const float *delta, const float *A, const float *Bm,
+                  const float *Cm, const float *Dk, const float *dy, float *dx, float *ddelta,
+                  float *dA, float *dB, float *dC, float *dD, int64_t B, int64_t L, int64_t D,
+                  int64_t N, ssd_stream_t stream) {
+  int rc = mamba_check(B, L, D, N);
+  if (rc) return rc;
+  if (misaligned(x) || misaligned(delta) || misaligned(A) || misaligned(Bm) || misaligned(Cm) ||
+      misaligned(Dk) || misaligned(dy) || misaligned(dx) || misaligned(ddelta) ||
+      misaligned(dA) || misaligned(dB) || misaligned(dC) || misaligned(dD))
+    return SSD_ERR_ALIGN;
+  if (!dA || (Dk && !dD)) return SSD_ERR_ARG;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (B == 0 || L == 0) {
+    cudaError_t e = cudaMemsetAsync(dA, 0, sizeof(float) * D * N, s);
+    if (e == cudaSuccess && dD) e = cudaMemsetAsync(dD, 0, sizeof(float) * D, s);
+    return from_cuda(e);
+  }
+  if (!x || !delta || !A || !Bm || !Cm || !dy || !dx || !ddelta || !dB || !dC)
+    return SSD_ERR_ARG;
+  void *ws = nullptr;
+  rc = ws_alloc(&ws, ssd::mamba::bwd_workspace_bytes(B, L, D, N), s);
+  if (rc) return rc;
+  cudaError_t e = ssd::mamba::bwd(x, delta, A, Bm, Cm, Dk, dy, dx, ddelta, dA, dB, dC,
+                                  Dk ? dD : nullptr, B, L, D, N, ws, s);
+  if (ws) cudaFreeAsync(ws, s);
+  return from_cuda(e);
 }
 
 int ssd_last_device_error(ssd_stream_t stream) {

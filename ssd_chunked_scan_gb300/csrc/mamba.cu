@@ -1,0 +1,446 @@
+// Mamba-1 selective scan (state N <= 16), forward and backward, all fp32 on
+// the CUDA cores.  The op of the "kernel_mamba_cpu.json" benchmark records:
+//
+//   h_t[d,n] = exp(delta_t[d] A[d,n]) h_{t-1}[d,n] + delta_t[d] B_t[n] x_t[d],  h_{-1} = 0
+//   y_t[d]   = sum_n C_t[n] h_t[d,n] + D[d] x_t[d]
+//
+// There is no dense contraction here (each state element has its own decay),
+// so the work is elementwise recurrences and short reductions; it is bound by
+// the exponentials (one per (token, channel, state)) and by HBM traffic.
+//
+// Layout of the work: one thread per (batch, channel d, state n); the 16
+// lanes of a half-warp hold the states of one channel, so the reduction over
+// n is four shuffles, and a CTA of 256 threads covers 16 consecutive
+// channels.  Each (batch, channel) sequence is cut into nseg segments so that
+// enough CTAs run at once:
+//
+//   k_mb_local<false>  each segment's final state from a zero state, and its
+//                      delta sum (fp64), from which the segment's decay
+//                      exp(A * sum delta) follows
+//   k_mb_scan<false>   state entering every segment (sequential over segments)
+//   k_mb_out           each segment again from its entering state, emitting y
+//
+// The backward uses u_t = exp(delta_t A) g_t, g_t = dL/dh_t, which satisfies
+// g_t = C_t dy_t + u_{t+1} (u_L = 0):
+//
+//   k_mb_local<true>   each segment's u at its left end from u = 0 at its right
+//   k_mb_scan<true>    u entering every segment from the right
+//   k_mb_bwd           per segment: a forward pass that checkpoints h every 32
+//                      tokens (shared memory), then the 32-token blocks right
+//                      to left: recompute h_t and the decays into registers,
+//                      walk them backwards accumulating
+//                        dx_t = sum_n g delta B + D dy     dA += g delta a h_{t-1}
+//                        ddelta_t = sum_n g (A a h_{t-1} + B x)
+//                        dB_t[n] += g delta x,  dC_t[n] += dy h_t   (over d)
+//                      dB / dC / dA / dD are summed across CTAs with fp32
+//                      atomic adds (caller buffers zero-filled first).
+#include "common.cuh"
+#include "mamba.h"
+
+namespace ssd {
+namespace mamba {
+
+constexpr int NL = 16;           // lanes per channel (N <= 16)
+constexpr int CH = 16;           // channels per CTA
+constexpr int NT = CH * NL;      // 256 threads
+constexpr int TB = 32;           // tokens per staged block
+constexpr float LOG2E = 1.4426950408889634f;
+
+struct MGeo {
+  int64_t B, L, D, N;
+  int64_t Ls;    // segment length (multiple of TB)
+  int64_t nseg;
+};
+
+__device__ inline float half_sum(float v) {  // sum over the 16 lanes of a half-warp
+#pragma unroll
+  for (int o = 8; o >= 1; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// Token staging of one block: per-channel series ([TB][CH]) and per-token
+// state-indexed rows ([TB][NL]).
+struct Stage {
+  float *xs, *ds, *ys;  // x, delta, dy    [TB][CH]
+  float *bs, *cs;       // B, C            [TB][NL]
+};
+
+__device__ inline void stage_block(const Stage &st, const float *x, const float *dt,
+                                   const float *dy, const float *Bm, const float *Cm,
+                                   const MGeo &g, int64_t b, int64_t d0, int64_t t0, int len) {
+  for (int idx = threadIdx.x; idx < TB * CH; idx += NT) {
+    const int tt = idx / CH, c = idx - tt * CH;
+    const bool ok = tt < len && d0 + c < g.D;
+    const int64_t o = (b * g.L + t0 + tt) * g.D + d0 + c;
+    st.xs[idx] = ok ? x[o] : 0.f;
+    st.ds[idx] = ok ? dt[o] : 0.f;
+    if (dy) st.ys[idx] = ok ? dy[o] : 0.f;
+  }
+  for (int idx = threadIdx.x; idx < TB * NL; idx += NT) {
+    const int tt = idx / NL, n = idx - tt * NL;
+    const bool ok = tt < len && n < g.N;
+    const int64_t o = (b * g.L + t0 + tt) * g.N + n;
+    if (Bm) st.bs[idx] = ok ? Bm[o] : 0.f;
+    if (Cm) st.cs[idx] = ok ? Cm[o] : 0.f;
+  }
+}
+
+// Segment-local pass.  Forward: state after the segment from h = 0, and the
+// fp64 delta sum.  Reverse: u at the segment's left end from u = 0 at its
+// right end.  grid (ceil(D/CH), nseg, B)
+template <bool REV>
+__global__ void __launch_bounds__(NT) k_mb_local(const float *__restrict__ x,
+                                                 const float *__restrict__ dt,
+                                                 const float *__restrict__ A,
+                                                 const float *__restrict__ Bm,
+                                                 const float *__restrict__ Cm,
+                                                 const float *__restrict__ dy,
+                                                 float *__restrict__ states,
+                                                 float *__restrict__ dsum, MGeo g) {
+  __shared__ float xs[TB * CH], ds[TB * CH], ys[TB * CH], bs[TB * NL], cs[TB * NL];
+  const Stage st{xs, ds, ys, bs, cs};
+  const int tid = threadIdx.x, c = tid / NL, n = tid % NL;
+  const int64_t d0 = (int64_t)blockIdx.x * CH, seg = blockIdx.y, b = blockIdx.z;
+  const int64_t d = d0 + c;
+  const bool ok = d < g.D && n < g.N;
+  const float A2 = ok ? A[d * g.N + n] * LOG2E : 0.f;
+  const int64_t s0 = seg * g.Ls, s1 = s0 + g.Ls < g.L ? s0 + g.Ls : g.L;
+  const int64_t nb = (s1 - s0 + TB - 1) / TB;
+  float h = 0.f;
+  double dsacc = 0.0;
+  for (int64_t k = 0; k < nb; ++k) {
+    const int64_t kb = REV ? nb - 1 - k : k;
+    const int64_t t0 = s0 + kb * TB;
+    const int len = (int)(s1 - t0 < TB ? s1 - t0 : TB);
+    stage_block(st, x, dt, REV ? dy : nullptr, REV ? nullptr : Bm, REV ? Cm : nullptr, g, b, d0,
+                t0, len);
+    __syncthreads();
+    if (!REV) {
+      for (int i = 0; i < len; ++i) {
+        const float de = ds[i * CH + c];
+        const float a = exp2f(de * A2);
+        h = fmaf(a, h, de * xs[i * CH + c] * bs[i * NL + n]);
+        dsacc += (double)de;
+      }
+    } else {
+      for (int i = len - 1; i >= 0; --i) {
+        const float de = ds[i * CH + c];
+        const float a = exp2f(de * A2);
+        h = a * fmaf(cs[i * NL + n], ys[i * CH + c], h);
+      }
+    }
+    __syncthreads();
+  }
+  if (ok) states[((b * g.nseg + seg) * g.D + d) * g.N + n] = h;
+  if (!REV && n == 0 && d < g.D) dsum[(b * g.nseg + seg) * g.D + d] = (float)dsacc;
+}
+
+// Across segments, in place: states[s] <- the state entering segment s from
+// the left (forward) or the u entering it from the right (reverse).
+// grid (ceil(B*D*N / 256))
+template <bool REV>
+__global__ void __launch_bounds__(256) k_mb_scan(float *__restrict__ states,
+                                                 const float *__restrict__ dsum,
+                                                 const float *__restrict__ A, MGeo g) {
+  const int64_t e = (int64_t)blockIdx.x * 256 + threadIdx.x;
+  if (e >= g.B * g.D * g.N) return;
+  const int64_t b = e / (g.D * g.N), dn = e - b * g.D * g.N, d = dn / g.N;
+  const float A2 = A[dn] * LOG2E;
+  float run = 0.f;
+  for (int64_t k = 0; k < g.nseg; ++k) {
+    const int64_t s = REV ? g.nseg - 1 - k : k;
+    float *p = states + (b * g.nseg + s) * g.D * g.N + dn;
+    const float xv = *p;
+    *p = run;
+    run = fmaf(exp2f(A2 * dsum[(b * g.nseg + s) * g.D + d]), run, xv);
+  }
+}
+
+// y of every segment from its entering state.  grid (ceil(D/CH), nseg, B)
+__global__ void __launch_bounds__(NT) k_mb_out(const float *__restrict__ x,
+                                               const float *__restrict__ dt,
+                                               const float *__restrict__ A,
+                                               const float *__restrict__ Bm,
+                                               const float *__restrict__ Cm,
+                                               const float *__restrict__ Dk,
+                                               const float *__restrict__ hin,
+                                               float *__restrict__ y, MGeo g) {
+  __shared__ float xs[TB * CH], ds[TB * CH], yo[TB * CH], bs[TB * NL], cs[TB * NL];
+  const Stage st{xs, ds, nullptr, bs, cs};
+  const int tid = threadIdx.x, c = tid / NL, n = tid % NL;
+  const int64_t d0 = (int64_t)blockIdx.x * CH, seg = blockIdx.y, b = blockIdx.z;
+  const int64_t d = d0 + c;
+  const bool ok = d < g.D && n < g.N;
+  const float A2 = ok ? A[d * g.N + n] * LOG2E : 0.f;
+  const float Dd = (Dk && d < g.D) ? Dk[d] : 0.f;
+  const int64_t s0 = seg * g.Ls, s1 = s0 + g.Ls < g.L ? s0 + g.Ls : g.L;
+  float h = ok ? hin[((b * g.nseg + seg) * g.D + d) * g.N + n] : 0.f;
+  for (int64_t t0 = s0; t0 < s1; t0 += TB) {
+    const int len = (int)(s1 - t0 < TB ? s1 - t0 : TB);
+    stage_block(st, x, dt, nullptr, Bm, Cm, g, b, d0, t0, len);
+    __syncthreads();
+    for (int i = 0; i < len; ++i) {
+      const float de = ds[i * CH + c], xv = xs[i * CH + c];
+      const float a = exp2f(de * A2);
+      h = fmaf(a, h, de * xv * bs[i * NL + n]);
+      const float yv = half_sum(cs[i * NL + n] * h);
+      if (n == 0) yo[i * CH + c] = fmaf(Dd, xv, yv);
+    }
+    __syncthreads();
+    for (int idx = tid; idx < len * CH; idx += NT) {
+      const int tt = idx / CH, cc = idx - tt * CH;
+      if (d0 + cc < g.D) y[(b * g.L + t0 + tt) * g.D + d0 + cc] = yo[idx];
+    }
+  }
+}
+
+// Backward of every segment.  Dynamic shared memory: the h checkpoints
+// [Ls/TB][NT], then the staging and reduction buffers.  grid (ceil(D/CH), nseg, B)
+__global__ void __launch_bounds__(NT, 2) k_mb_bwd(
+    const float *__restrict__ x, const float *__restrict__ dt, const float *__restrict__ A,
+    const float *__restrict__ Bm, const float *__restrict__ Cm, const float *__restrict__ Dk,
+    const float *__restrict__ dy, const float *__restrict__ hin, const float *__restrict__ uin,
+    float *__restrict__ dx, float *__restrict__ ddt, float *__restrict__ dA,
+    float *__restrict__ dB, float *__restrict__ dC, float *__restrict__ dD, MGeo g) {
+  extern __shared__ float4 smem4[];
+  float *sm = reinterpret_cast<float *>(smem4);
+  const int nck = (int)(g.Ls / TB);
+  float *ck = sm;                        // [nck][NT]
+  float *xs = ck + nck * NT;             // [TB][CH]
+  float *ds = xs + TB * CH;
+  float *ys = ds + TB * CH;
+  float *bs = ys + TB * CH;              // [TB][NL]
+  float *cs = bs + TB * NL;
+  float *rdx = cs + TB * NL;             // [TB][CH]
+  float *rdt = rdx + TB * CH;
+  float *rB = rdt + TB * CH;             // [TB][NT/32][NL]
+  float *rC = rB + TB * (NT / 32) * NL;
+  const Stage st{xs, ds, ys, bs, cs};
+  const int tid = threadIdx.x, c = tid / NL, n = tid % NL, warp = tid >> 5;
+  const int64_t d0 = (int64_t)blockIdx.x * CH, seg = blockIdx.y, b = blockIdx.z;
+  const int64_t d = d0 + c;
+  const bool ok = d < g.D && n < g.N;
+  const float Av = ok ? A[d * g.N + n] : 0.f;
+  const float A2 = Av * LOG2E;
+  const float Dd = (Dk && d < g.D) ? Dk[d] : 0.f;
+  const int64_t s0 = seg * g.Ls, s1 = s0 + g.Ls < g.L ? s0 + g.Ls : g.L;
+  const int nb = (int)((s1 - s0 + TB - 1) / TB);
+
+  // forward over the segment: checkpoint h before every block
+  float h = ok ? hin[((b * g.nseg + seg) * g.D + d) * g.N + n] : 0.f;
+  for (int k = 0; k < nb; ++k) {
+    const int64_t t0 = s0 + (int64_t)k * TB;
+    const int len = (int)(s1 - t0 < TB ? s1 - t0 : TB);
+    ck[k * NT + tid] = h;
+    stage_block(st, x, dt, nullptr, Bm, nullptr, g, b, d0, t0, len);
+    __syncthreads();
+    for (int i = 0; i < len; ++i) {
+      const float de = ds[i * CH + c];
+      h = fmaf(exp2f(de * A2), h, de * xs[i * CH + c] * bs[i * NL + n]);
+    }
+    __syncthreads();
+  }
+
+  // blocks right to left
+  float u = ok ? uin[((b * g.nseg + seg) * g.D + d) * g.N + n] : 0.f;
+  float dA_acc = 0.f, dD_acc = 0.f;
+  for (int k = nb - 1; k >= 0; --k) {
+    const int64_t t0 = s0 + (int64_t)k * TB;
+    const int len = (int)(s1 - t0 < TB ? s1 - t0 : TB);
+    stage_block(st, x, dt, dy, Bm, Cm, g, b, d0, t0, len);
+    __syncthreads();
+    const float hstart = ck[k * NT + tid];
+    float hs[TB], as[TB];
+    {
+      float hh = hstart;
+#pragma unroll
+      for (int i = 0; i < TB; ++i) {
+        if (i < len) {
+          const float de = ds[i * CH + c];
+          as[i] = exp2f(de * A2);
+          hh = fmaf(as[i], hh, de * xs[i * CH + c] * bs[i * NL + n]);
+        } else {
+          as[i] = 1.f;
+        }
+        hs[i] = hh;
+      }
+    }
+#pragma unroll
+    for (int i = TB - 1; i >= 0; --i) {
+      if (i < len) {
+        const float de = ds[i * CH + c], xv = xs[i * CH + c], dyv = ys[i * CH + c];
+        const float Bn = bs[i * NL + n];
+        const float gg = ok ? fmaf(cs[i * NL + n], dyv, u) : 0.f;
+        const float hp = i > 0 ? hs[i - 1] : hstart;
+        const float ahp = as[i] * hp;
+        dA_acc = fmaf(gg * de, ahp, dA_acc);
+        const float pdt = half_sum(gg * fmaf(Av, ahp, Bn * xv));
+        const float pdx = half_sum(gg * de * Bn);
+        float pB = gg * de * xv;
+        float pC = ok ? dyv * hs[i] : 0.f;
+        pB += __shfl_xor_sync(0xffffffffu, pB, 16);  // the warp's two channels
+        pC += __shfl_xor_sync(0xffffffffu, pC, 16);
+        if ((tid & 31) < NL) {
+          rB[(i * (NT / 32) + warp) * NL + n] = pB;
+          rC[(i * (NT / 32) + warp) * NL + n] = pC;
+        }
+        if (n == 0) {
+          rdx[i * CH + c] = fmaf(Dd, dyv, pdx);
+          rdt[i * CH + c] = pdt;
+          dD_acc = fmaf(dyv, xv, dD_acc);
+        }
+        u = as[i] * gg;
+      }
+    }
+    __syncthreads();
+    for (int idx = tid; idx < len * CH; idx += NT) {
+      const int tt = idx / CH, cc = idx - tt * CH;
+      if (d0 + cc < g.D) {
+        const int64_t o = (b * g.L + t0 + tt) * g.D + d0 + cc;
+        dx[o] = rdx[idx];
+        ddt[o] = rdt[idx];
+      }
+    }
+    for (int idx = tid; idx < len * NL; idx += NT) {
+      const int tt = idx / NL, nn = idx - tt * NL;
+      if (nn < g.N) {
+        float sb = 0.f, sc = 0.f;
+#pragma unroll
+        for (int w2 = 0; w2 < NT / 32; ++w2) {
+          sb += rB[(tt * (NT / 32) + w2) * NL + nn];
+          sc += rC[(tt * (NT / 32) + w2) * NL + nn];
+        }
+        const int64_t o = (b * g.L + t0 + tt) * g.N + nn;
+        atomicAdd(dB + o, sb);
+        atomicAdd(dC + o, sc);
+      }
+    }
+    __syncthreads();
+  }
+  if (ok) atomicAdd(dA + d * g.N + n, dA_acc);
+  if (dD && n == 0 && d < g.D) atomicAdd(dD + d, dD_acc);
+}
+
+// ---------------------------------------------------------------------------
+
+namespace {
+
+int num_sms() {
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) { cudaGetLastError(); dev = 0; }
+  if (dev < 0 || dev >= 64) return 148;
+  if (!cache[dev]) {
+    int v = 0;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+      cudaGetLastError();
+      v = 0;
+    }
+    cache[dev] = v > 0 ? v : 148;
+  }
+  return cache[dev];
+}
+
+// Segments: about eight 256-thread CTAs per SM in all, each segment a
+// multiple of TB tokens and at most MAX_LS (the backward's checkpoints live in
+// shared memory).
+constexpr int64_t MAX_LS = 1024;
+
+MGeo make_geo(int64_t B, int64_t L, int64_t D, int64_t N) {
+  MGeo g;
+  g.B = B; g.L = L; g.D = D; g.N = N;
+  const int64_t base = B * ((D + CH - 1) / CH);
+  const int64_t want = (8 * (int64_t)num_sms() + base - 1) / base;
+  int64_t ls = (L + want - 1) / want;
+  ls = (ls + TB - 1) / TB * TB;
+  if (ls > MAX_LS) ls = MAX_LS;
+  if (ls < TB) ls = TB;
+  g.Ls = ls;
+  g.nseg = (L + ls - 1) / ls;
+  return g;
+}
+
+size_t bwd_smem(const MGeo &g) {
+  return sizeof(float) * ((size_t)(g.Ls / TB) * NT + 5 * TB * CH + 2 * TB * NL +
+                          2 * (size_t)TB * (NT / 32) * NL);
+}
+
+}  // namespace
+
+size_t fwd_workspace_bytes(int64_t B, int64_t L, int64_t D, int64_t N) {
+  const MGeo g = make_geo(B, L, D, N);
+  return sizeof(float) * (size_t)(g.B * g.nseg * g.D * (g.N + 1));
+}
+
+size_t bwd_workspace_bytes(int64_t B, int64_t L, int64_t D, int64_t N) {
+  const MGeo g = make_geo(B, L, D, N);
+  return sizeof(float) * (size_t)(g.B * g.nseg * g.D * (2 * g.N + 1));
+}
+
+cudaError_t fwd(const float *x, const float *dt, const float *A, const float *Bm, const float *Cm,
+                const float *Dk, float *y, int64_t B, int64_t L, int64_t D, int64_t N, void *ws,
+                cudaStream_t s) {
+  const MGeo g = make_geo(B, L, D, N);
+  float *hst = static_cast<float *>(ws);
+  float *dsum = hst + g.B * g.nseg * g.D * g.N;
+  const dim3 grid((unsigned)((D + CH - 1) / CH), (unsigned)g.nseg, (unsigned)B);
+  {
+    LaunchTrace lt("mamba.seg_state", s);
+    k_mb_local<false><<<grid, NT, 0, s>>>(x, dt, A, Bm, Cm, nullptr, hst, dsum, g);
+  }
+  {
+    LaunchTrace lt("mamba.seg_scan", s);
+    k_mb_scan<false><<<(unsigned)cdiv(B * D * N, 256), 256, 0, s>>>(hst, dsum, A, g);
+  }
+  {
+    LaunchTrace lt("mamba.out", s);
+    k_mb_out<<<grid, NT, 0, s>>>(x, dt, A, Bm, Cm, Dk, hst, y, g);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t bwd(const float *x, const float *dt, const float *A, const float *Bm, const float *Cm,
+                const float *Dk, const float *dy, float *dx, float *ddt, float *dA, float *dB,
+                float *dC, float *dD, int64_t B, int64_t L, int64_t D, int64_t N, void *ws,
+                cudaStream_t s) {
+  const MGeo g = make_geo(B, L, D, N);
+  const int64_t nst = g.B * g.nseg * g.D * g.N;
+  float *hst = static_cast<float *>(ws);
+  float *ust = hst + nst;
+  float *dsum = ust + nst;
+  cudaError_t e;
+  if ((e = cudaMemsetAsync(dA, 0, sizeof(float) * D * N, s)) != cudaSuccess) return e;
+  if ((e = cudaMemsetAsync(dB, 0, sizeof(float) * B * L * N, s)) != cudaSuccess) return e;
+  if ((e = cudaMemsetAsync(dC, 0, sizeof(float) * B * L * N, s)) != cudaSuccess) return e;
+  if (dD && (e = cudaMemsetAsync(dD, 0, sizeof(float) * D, s)) != cudaSuccess) return e;
+  const dim3 grid((unsigned)((D + CH - 1) / CH), (unsigned)g.nseg, (unsigned)B);
+  const unsigned sgrid = (unsigned)cdiv(B * D * N, 256);
+  {
+    LaunchTrace lt("mamba.seg_state", s);
+    k_mb_local<false><<<grid, NT, 0, s>>>(x, dt, A, Bm, Cm, nullptr, hst, dsum, g);
+  }
+  {
+    LaunchTrace lt("mamba.seg_scan", s);
+    k_mb_scan<false><<<sgrid, 256, 0, s>>>(hst, dsum, A, g);
+  }
+  {
+    LaunchTrace lt("mamba.seg_grad_state", s);
+    k_mb_local<true><<<grid, NT, 0, s>>>(x, dt, A, Bm, Cm, dy, ust, nullptr, g);
+  }
+  {
+    LaunchTrace lt("mamba.seg_scan", s);
+    k_mb_scan<true><<<sgrid, 256, 0, s>>>(ust, dsum, A, g);
+  }
+  const size_t sm = bwd_smem(g);
+  if ((e = cudaFuncSetAttribute(k_mb_bwd, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm)) !=
+      cudaSuccess)
+    return e;
+  {
+    LaunchTrace lt("mamba.bwd", s);
+    k_mb_bwd<<<grid, NT, sm, s>>>(x, dt, A, Bm, Cm, Dk, dy, hst, ust, dx, ddt, dA, dB, dC, dD, g);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace mamba
+}  // namespace ssd

@@ -74,6 +74,12 @@ def _load():
     lib.ssd_bwd_workspace_bytes.restype = ctypes.c_int
     lib.ssd_pool_high_water.argtypes = [ctypes.c_int, ctypes.POINTER(ctypes.c_size_t)]
     lib.ssd_pool_high_water.restype = ctypes.c_int
+    lib.ssd_mamba_fwd.argtypes = [p] * 7 + [i64] * 4 + [p]
+    lib.ssd_mamba_fwd.restype = ctypes.c_int
+    lib.ssd_mamba_bwd.argtypes = [p] * 13 + [i64] * 4 + [p]
+    lib.ssd_mamba_bwd.restype = ctypes.c_int
+    lib.ssd_mamba_workspace_bytes.argtypes = [ctypes.c_int] + [i64] * 4 + [ctypes.POINTER(ctypes.c_size_t)]
+    lib.ssd_mamba_workspace_bytes.restype = ctypes.c_int
     lib.ssd_fwd_noalloc.argtypes = [p] * 6 + [i64] * 7 + [p]
     lib.ssd_fwd_noalloc.restype = ctypes.c_int
     lib.ssd_fwd_noalloc_scratch_bytes.argtypes = []
@@ -306,3 +312,64 @@ def ssd_fwd_noalloc(q, k, v, log_alpha, h0, out, chunk=64, stream=None):
     if rc:
         raise SSDError(rc, "ssd_fwd_noalloc")
     return out
+
+
+# ---- Mamba-1 selective scan (include/ssd_mamba.h) --------------------------
+
+def _mamba_dims(x, A):
+    if x.dim() != 3 or A.dim() != 2:
+        raise ValueError("x must be [B,L,D] and A [D,N]")
+    B, L, D = x.shape
+    return B, L, D, A.shape[1]
+
+
+def _mamba_check_args(x, delta, A, Bm, Cm, Dk):
+    B, L, D, N = _mamba_dims(x, A)
+    dev = x.device
+    for n, t, sh in (("x", x, (B, L, D)), ("delta", delta, (B, L, D)), ("A", A, (D, N)),
+                     ("Bm", Bm, (B, L, N)), ("Cm", Cm, (B, L, N)), ("Dk", Dk, (D,))):
+        _check(n, t, sh, dev)
+    return B, L, D, N, dev
+
+
+def ssd_mamba_fwd(x, delta, A, Bm, Cm, Dk=None, y=None, stream=None):
+    """y [B,L,D] of the selective scan for x, delta [B,L,D], A [D,N], Bm, Cm [B,L,N], Dk [D]."""
+    B, L, D, N, dev = _mamba_check_args(x, delta, A, Bm, Cm, Dk)
+    if y is None:
+        y = torch.empty((B, L, D), dtype=torch.float32, device=dev)
+    _check("y", y, (B, L, D), dev)
+    rc = LIB.ssd_mamba_fwd(_ptr(x), _ptr(delta), _ptr(A), _ptr(Bm), _ptr(Cm), _ptr(Dk), _ptr(y),
+                           B, L, D, N, _stream(stream))
+    if rc:
+        raise SSDError(rc, "ssd_mamba_fwd")
+    return y
+
+
+def ssd_mamba_bwd(x, delta, A, Bm, Cm, Dk, dy, grads=None, stream=None):
+    """Gradients of <dy, y>: dict dx, ddelta, dA, dB, dC, dD (dD None when Dk is None)."""
+    B, L, D, N, dev = _mamba_check_args(x, delta, A, Bm, Cm, Dk)
+    _check("dy", dy, (B, L, D), dev)
+    shapes = {"dx": (B, L, D), "ddelta": (B, L, D), "dA": (D, N), "dB": (B, L, N),
+              "dC": (B, L, N), "dD": (D,)}
+    g = dict(grads or {})
+    for n, sh in shapes.items():
+        if n == "dD" and Dk is None:
+            g[n] = None
+            continue
+        if g.get(n) is None:
+            g[n] = torch.empty(sh, dtype=torch.float32, device=dev)
+        _check(n, g[n], sh, dev)
+    rc = LIB.ssd_mamba_bwd(_ptr(x), _ptr(delta), _ptr(A), _ptr(Bm), _ptr(Cm), _ptr(Dk), _ptr(dy),
+                           _ptr(g["dx"]), _ptr(g["ddelta"]), _ptr(g["dA"]), _ptr(g["dB"]),
+                           _ptr(g["dC"]), _ptr(g["dD"]), B, L, D, N, _stream(stream))
+    if rc:
+        raise SSDError(rc, "ssd_mamba_bwd")
+    return g
+
+
+def ssd_mamba_workspace_bytes(bwd, B, L, D, N) -> int:
+    n = ctypes.c_size_t(0)
+    rc = LIB.ssd_mamba_workspace_bytes(1 if bwd else 0, B, L, D, N, ctypes.byref(n))
+    if rc:
+        raise SSDError(rc, "ssd_mamba_workspace_bytes")
+    return int(n.value)

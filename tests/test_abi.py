@@ -154,3 +154,24 @@ def test_chunk_one_is_sequential_on_every_path(lib, path):
         0, 4 * (2 * nblk * B * L * H + B * H * dk * dv))
     assert _ws(lib, "ssd_fwd_workspace_bytes", 2, 100, 1, 2, 129, 3, 1)[0] == 4
     assert _fwd(lib, dk=5, dv=3, chunk=1, ptrs=(0x1000, 0x1004) + (0x1000,) * 4) == 2
+
+
+def test_mamba_host_checks(lib):
+    p = ctypes.c_void_p
+    i64 = ctypes.c_int64
+    lib.ssd_mamba_fwd.argtypes = [p] * 7 + [i64] * 4 + [p]
+    lib.ssd_mamba_bwd.argtypes = [p] * 13 + [i64] * 4 + [p]
+    lib.ssd_mamba_workspace_bytes.argtypes = [ctypes.c_int] + [i64] * 4 + [ctypes.POINTER(ctypes.c_size_t)]
+    ok = [p(0x1000)] * 7
+    assert lib.ssd_mamba_fwd(*ok, 1, 8, 4, 17, None) == 4      # N > 16
+    assert lib.ssd_mamba_fwd(*ok, 1, 8, 0, 4, None) == 1       # D = 0
+    assert lib.ssd_mamba_fwd(*([p(0x1000)] * 6 + [p(0x1008)]), 1, 8, 4, 4, None) == 2
+    assert lib.ssd_mamba_fwd(*([p(0x1000)] * 2 + [p(0)] + [p(0x1000)] * 4), 1, 8, 4, 4, None) == 1
+    assert lib.ssd_mamba_fwd(*ok, 1, 0, 4, 4, None) == 0       # empty
+    n = ctypes.c_size_t(7)
+    assert lib.ssd_mamba_workspace_bytes(0, 2, 0, 4, 4, ctypes.byref(n)) == 0 and n.value == 0
+    assert lib.ssd_mamba_workspace_bytes(1, 4, 8192, 1024, 16, ctypes.byref(n)) == 0
+    fwd_n = ctypes.c_size_t(0)
+    assert lib.ssd_mamba_workspace_bytes(0, 4, 8192, 1024, 16, ctypes.byref(fwd_n)) == 0
+    # forward: states + delta sums per segment; backward adds the u states
+    assert 0 < fwd_n.value < n.value < 2 * fwd_n.value
