@@ -379,6 +379,223 @@ def run_max_len(args, w):
     return 0
 
 
+# ---- Mamba-1 selective scan (--op mamba) -----------------------------------
+
+MAMBA_WORKLOAD = "mamba_d1024_L8192"
+MAMBA_METRIC = "Mamba-1 selective scan fwd / fwd_bwd channel-tokens/s (B·L·D) at 1 GB300"
+# "kernel_mamba_cpu.json" records, impl chunked (CPU backend): ms per call
+PAGE_MAMBA_CPU_MS = {"mamba_d1024_L8192": {"fwd": 298.87558800692204, "fwd_bwd": 1867.5783030048478},
+                     "mamba_d256_L8192": {"fwd": 107.37162199802697, "fwd_bwd": 644.8948080069385},
+                     "mamba_d512_L8192": {"fwd": 205.45388301252387, "fwd_bwd": 1037.0018319954397}}
+# MUFU (ex2) rate: 16 results per clock per SM x 152 SMs x 2070 MHz
+MUFU_GEXP = 152 * 16 * 2.070
+
+
+def mamba_nseg(w, sms=152):
+    """Segments per sequence chosen by the Mamba kernels (same rule as mamba.cu)."""
+    base = w.B * w.D
+    want = -(-1024 * sms // base)
+    ls = -(-w.L // want)
+    ls = min(max(-(-ls // 32) * 32, 32), 1024)
+    return -(-w.L // ls)
+
+
+def mamba_costs(w, sms=152):
+    """Algorithmic bytes and exponentials per launch of each Mamba kernel."""
+    f = 4
+    BLD, BLN = w.B * w.L * w.D * f, w.B * w.L * w.N * f
+    nseg = mamba_nseg(w, sms)
+    st = w.B * nseg * w.D * w.N * f
+    ds = w.B * nseg * w.D * f
+    ex = w.B * w.L * w.D * w.N
+    return {
+        "mamba.seg_state": (2 * BLD + BLN + st + ds, ex),
+        "mamba.seg_scan": (2 * st + ds, w.B * nseg * w.D * w.N),
+        "mamba.out": (3 * BLD + 2 * BLN + st + ds, ex),
+        "mamba.seg_grad_state": (2 * BLD + BLN + st + ds, ex),
+        "mamba.bwd": (5 * BLD + 4 * BLN + 2 * st, 2 * ex),
+    }
+
+
+def run_mamba(args):
+    """One JSON line for the Mamba selective scan: fwd + bwd per step."""
+    import torch
+    from ssd_chunked_scan_gb300 import ssd
+    from ssd_chunked_scan_gb300.inputs import MAMBA_BY_NAME, mamba_workload_inputs
+    name = args.workload if args.workload in MAMBA_BY_NAME else MAMBA_WORKLOAD
+    w = MAMBA_BY_NAME[name]
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    host = [torch.from_numpy(x).pin_memory() for x in mamba_workload_inputs(w)]
+    x, dt, A, Bm, Cm, Dk, dy = [t.to(dev) for t in host]
+    y = torch.empty_like(x)
+    grads = {"dx": torch.empty_like(x), "ddelta": torch.empty_like(x), "dA": torch.empty_like(A),
+             "dB": torch.empty_like(Bm), "dC": torch.empty_like(Cm), "dD": torch.empty_like(Dk)}
+    stream = torch.cuda.current_stream(dev)
+    fb = args.mode != "fwd"
+
+    def step():
+        ssd.ssd_mamba_fwd(x, dt, A, Bm, Cm, Dk, y=y)
+        if fb:
+            ssd.ssd_mamba_bwd(x, dt, A, Bm, Cm, Dk, dy, grads=grads)
+
+    def timed(fn, n):
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(n):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        return e0.elapsed_time(e1) / n
+
+    clocks = ClockSampler(0)
+    clocks.start()
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    n0 = ssd.ssd_launch_count()
+    th0 = time.time()
+    ms = timed(step, args.steps)
+    th1 = time.time()
+    launches = ssd.ssd_launch_count() - n0
+    ssd.ssd_trace_reset()
+    ssd.ssd_trace_enable(True)
+    for _ in range(args.steps):
+        step()
+    torch.cuda.synchronize(dev)
+    ssd.ssd_trace_enable(False)
+    trace = ssd.ssd_trace_collect()
+    ssd.ssd_trace_reset()
+    clocks.stop()
+    fwd_ms = timed(lambda: ssd.ssd_mamba_fwd(x, dt, A, Bm, Cm, Dk, y=y), args.steps)
+
+    e2e = None
+    if not args.no_e2e:
+        dbuf = [torch.empty_like(t) for t in (x, dt, A, Bm, Cm, Dk, dy)]
+        h_y = torch.empty(y.shape, pin_memory=True)
+        h_g = {n: torch.empty(t.shape, pin_memory=True) for n, t in grads.items()}
+
+        def e2e_step():
+            for d, hsrc in zip(dbuf, host):
+                d.copy_(hsrc, non_blocking=True)
+            ssd.ssd_mamba_fwd(*dbuf[:6], y=y)
+            h_y.copy_(y, non_blocking=True)
+            if fb:
+                ssd.ssd_mamba_bwd(*dbuf, grads=grads)
+                for n in h_g:
+                    h_g[n].copy_(grads[n], non_blocking=True)
+        e2e_step()
+        e2e_ms = timed(e2e_step, args.steps)
+        h2d = sum(t.numel() * 4 for t in (host if fb else host[:6]))
+        d2h = y.numel() * 4 + (sum(t.numel() * 4 for t in grads.values()) if fb else 0)
+        e2e = {"value": w.tokens / (e2e_ms / 1e3), "unit": "channel-tokens/s", "ms_per_step": e2e_ms,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+    peaks = load_peaks()
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    costs = mamba_costs(w, sms)
+    top_name, (top_n, top_ms) = max(trace.items(), key=lambda kv: kv[1][1])
+    per = top_ms / top_n
+    kb, kx = costs[top_name]
+    t_hbm = kb / (peaks["hbm_gbs"] * 1e9)
+    t_mufu = kx / (MUFU_GEXP * 1e9)
+    if t_mufu >= t_hbm:
+        roof = {"bound": "alu", "achieved": kx / (per / 1e3) / 1e9, "peak": MUFU_GEXP,
+                "unit": "Gexp/s", "peak_note": "MUFU ex2: 152 SMs x 16 per clock x 2070 MHz"}
+    else:
+        roof = {"bound": "hbm", "achieved": kb / (per / 1e3) / 1e9, "peak": peaks["hbm_gbs"],
+                "unit": "GB/s", "peak_note": f"{peaks['source']} copy bandwidth"}
+    roof.update({"frac": roof["achieved"] / roof["peak"], "traffic": None, "kernel": top_name,
+                 "kernel_ms_per_launch": per, "alg_bytes_per_launch": kb,
+                 "alg_exp_per_launch": kx})
+    page = PAGE_MAMBA_CPU_MS.get(w.name, {})
+    line = {
+        "metric": MAMBA_METRIC, "value": w.tokens / (ms / 1e3), "unit": "channel-tokens/s",
+        "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": w.name, "op": "mamba", "mode": "fwd_bwd" if fb else "fwd",
+                   "B": w.B, "L": w.L, "D": w.D, "N": w.N, "segments": mamba_nseg(w, sms),
+                   "l2": "no flush: each step's inputs and outputs exceed L2"},
+        "roofline": roof,
+        "fwd": {"ms": fwd_ms, "tokens_per_s": w.tokens / (fwd_ms / 1e3)},
+        "kernels": {n: {"launches": c, "ms_total": t, "share": t / sum(v[1] for v in trace.values())}
+                    for n, (c, t) in sorted(trace.items(), key=lambda kv: -kv[1][1])},
+        "gpu_launches": launches, "clocks": clocks.summary(th0, th1), "e2e": e2e,
+        "page_context": {"cpu_chunked_ms": page or None},
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = mamba_cpu_sample(w, fb)
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_mamba_reference(args):
+    """The float64 Mamba oracle as the reference arm: one fwd + bwd of batch
+    entry 0 of the workload per step, on the host cores (rank 0 only)."""
+    if int(os.environ.get("RANK", "0")) != 0:
+        return 0
+    import numpy as np
+    from oracle import mamba_bwd_ref, mamba_fwd_ref, oracle_threads
+    from ssd_chunked_scan_gb300.inputs import MAMBA_BY_NAME, mamba_workload_inputs
+    w = MAMBA_BY_NAME.get(args.workload, MAMBA_BY_NAME[MAMBA_WORKLOAD])
+    x, dt, A, Bm, Cm, Dk, dy = mamba_workload_inputs(w)
+    sl = lambda a: np.ascontiguousarray(a[:1])
+    x, dt, Bm, Cm, dy = map(sl, (x, dt, Bm, Cm, dy))
+    fb = args.mode != "fwd"
+
+    def step():
+        mamba_fwd_ref(x, dt, A, Bm, Cm, Dk)
+        if fb:
+            mamba_bwd_ref(x, dt, A, Bm, Cm, Dk, dy)
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    el = time.perf_counter() - t0
+    val = w.L * w.D * args.steps / el
+    sample = f"batch entry 0 of {w.name} ({w.L} x {w.D} channels), float64 {'fwd+bwd' if fb else 'fwd'} per step"
+    cores = min(oracle_threads(), w.D)
+    print(json.dumps({
+        "impl": "reference", "metric": MAMBA_METRIC, "value": val, "unit": "channel-tokens/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": el / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "op": "mamba", "mode": "fwd_bwd" if fb else "fwd",
+                   "B": w.B, "L": w.L, "D": w.D, "N": w.N, "sample_tokens_per_step": w.L * w.D},
+        "cpu_baseline": {"value": val, "unit": "channel-tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": val, "unit": "channel-tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0}}), flush=True)
+    return 0
+
+
+def mamba_cpu_sample(w, fb, min_seconds=10.0, max_reps=30):
+    """The float64 Mamba oracle on batch entry 0 of the workload, repeated for
+    about min_seconds."""
+    import numpy as np
+    from oracle import mamba_bwd_ref, mamba_fwd_ref, oracle_threads
+    from ssd_chunked_scan_gb300.inputs import mamba_workload_inputs
+    x, dt, A, Bm, Cm, Dk, dy = mamba_workload_inputs(w)
+    sl = lambda a: np.ascontiguousarray(a[:1])
+    x, dt, Bm, Cm, dy = map(sl, (x, dt, Bm, Cm, dy))
+    toks, reps, t0 = 0, 0, time.perf_counter()
+    while True:
+        mamba_fwd_ref(x, dt, A, Bm, Cm, Dk)
+        if fb:
+            mamba_bwd_ref(x, dt, A, Bm, Cm, Dk, dy)
+        reps += 1
+        toks += w.L * w.D
+        el = time.perf_counter() - t0
+        if el >= min_seconds or reps >= max_reps:
+            break
+    return {"value": toks / el, "unit": "channel-tokens/s", "cores": min(oracle_threads(), w.D),
+            "kind": "oracle", "sample": f"batch entry 0 of {w.name} (1 x {w.L} x {w.D} channels), "
+                                        f"float64 {'fwd+bwd' if fb else 'fwd'}, {reps} rep(s), {el:.1f} s"}
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -387,6 +604,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--path", default=os.environ.get("SSD_BENCH_PATH", "tc"), choices=["tc", "simt"])
     ap.add_argument("--workload", default=WORKLOAD)
+    ap.add_argument("--op", default="ssd", choices=["ssd", "mamba"],
+                    help="mamba times the Mamba-1 selective scan instead (its own JSON line)")
     ap.add_argument("--chunk", type=int, default=None,
                     help="override the workload's chunk length (1: the sequential kernels)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -397,6 +616,10 @@ def main():
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
+    if args.op == "mamba":
+        if args.impl == "reference":
+            return run_mamba_reference(args)
+        return run_mamba(args)
     from ssd_chunked_scan_gb300.inputs import BY_NAME
     w = BY_NAME[args.workload]
     if args.chunk:

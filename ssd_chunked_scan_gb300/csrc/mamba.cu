@@ -8,14 +8,16 @@
 // so the work is elementwise recurrences and short reductions; it is bound by
 // the exponentials (one per (token, channel, state)) and by HBM traffic.
 //
-// Layout of the work: one thread per (batch, channel d, state n); the 16
-// lanes of a half-warp hold the states of one channel, so the reduction over
-// n is four shuffles, and a CTA of 256 threads covers 16 consecutive
-// channels.  Each (batch, channel) sequence is cut into nseg segments so that
-// enough CTAs run at once:
+// Each (batch, channel) sequence is cut into nseg segments so that enough
+// threads run at once.  The forward-type passes give one thread a whole
+// channel segment with the channel's 16 states in registers (B_t and C_t
+// rows are shared-memory broadcasts); the backward's main kernel gives one
+// thread one state of a channel (the 16 lanes of a half-warp hold a channel,
+// the reduction over n is four shuffles) so that 32 tokens of recomputed
+// states fit in its registers.
 //
 //   k_mb_local<false>  each segment's final state from a zero state, and its
-//                      delta sum (fp64), from which the segment's decay
+//                      delta sum, from which the segment's decay
 //                      exp(A * sum delta) follows
 //   k_mb_scan<false>   state entering every segment (sequential over segments)
 //   k_mb_out           each segment again from its entering state, emitting y
@@ -85,54 +87,100 @@ __device__ inline void stage_block(const Stage &st, const float *x, const float 
   }
 }
 
-// Segment-local pass.  Forward: state after the segment from h = 0, and the
-// fp64 delta sum.  Reverse: u at the segment's left end from u = 0 at its
-// right end.  grid (ceil(D/CH), nseg, B)
+// The channel kernels: one thread per (batch, channel, segment) holding the
+// channel's NL states in registers; a CTA covers CCH consecutive channels.
+constexpr int CCH = 128;
+
+// Per-block staging of the channel kernels: per-channel series [TB][CCH] and
+// the per-token rows of B and C [TB][NL] (read as float4 broadcasts).
+__device__ inline void stage_channels(float *xs, float *ds, float *ys, float *bs, float *cs,
+                                      const float *x, const float *dt, const float *dy,
+                                      const float *Bm, const float *Cm, const MGeo &g, int64_t b,
+                                      int64_t d0, int64_t t0, int len) {
+  for (int idx = threadIdx.x; idx < TB * CCH; idx += CCH) {
+    const int tt = idx / CCH, c = idx - tt * CCH;
+    const bool ok = tt < len && d0 + c < g.D;
+    const int64_t o = (b * g.L + t0 + tt) * g.D + d0 + c;
+    if (xs) xs[idx] = ok ? x[o] : 0.f;
+    ds[idx] = ok ? dt[o] : 0.f;
+    if (ys) ys[idx] = ok ? dy[o] : 0.f;
+  }
+  for (int idx = threadIdx.x; idx < TB * NL; idx += CCH) {
+    const int tt = idx / NL, n = idx - tt * NL;
+    const bool ok = tt < len && n < g.N;
+    const int64_t o = (b * g.L + t0 + tt) * g.N + n;
+    if (bs) bs[idx] = ok ? Bm[o] : 0.f;
+    if (cs) cs[idx] = ok ? Cm[o] : 0.f;
+  }
+}
+
+// Segment-local pass.  Forward: the state after the segment from h = 0, and
+// the segment's delta sum (fp32 per 32-token block, fp64 across blocks).
+// Reverse: u at the segment's left end from u = 0 at its right end.
+// grid (ceil(D/CCH), nseg, B), CCH threads
 template <bool REV>
-__global__ void __launch_bounds__(NT) k_mb_local(const float *__restrict__ x,
-                                                 const float *__restrict__ dt,
-                                                 const float *__restrict__ A,
-                                                 const float *__restrict__ Bm,
-                                                 const float *__restrict__ Cm,
-                                                 const float *__restrict__ dy,
-                                                 float *__restrict__ states,
-                                                 float *__restrict__ dsum, MGeo g) {
-  __shared__ float xs[TB * CH], ds[TB * CH], ys[TB * CH], bs[TB * NL], cs[TB * NL];
-  const Stage st{xs, ds, ys, bs, cs};
-  const int tid = threadIdx.x, c = tid / NL, n = tid % NL;
-  const int64_t d0 = (int64_t)blockIdx.x * CH, seg = blockIdx.y, b = blockIdx.z;
+__global__ void __launch_bounds__(CCH) k_mb_local(const float *__restrict__ x,
+                                                  const float *__restrict__ dt,
+                                                  const float *__restrict__ A,
+                                                  const float *__restrict__ Bm,
+                                                  const float *__restrict__ Cm,
+                                                  const float *__restrict__ dy,
+                                                  float *__restrict__ states,
+                                                  float *__restrict__ dsum, MGeo g) {
+  __shared__ float xs[TB * CCH], ds[TB * CCH];
+  __shared__ __align__(16) float rs[TB * NL];  // B rows (forward) or C rows (reverse)
+  const int c = threadIdx.x;
+  const int64_t d0 = (int64_t)blockIdx.x * CCH, seg = blockIdx.y, b = blockIdx.z;
   const int64_t d = d0 + c;
-  const bool ok = d < g.D && n < g.N;
-  const float A2 = ok ? A[d * g.N + n] * LOG2E : 0.f;
+  const bool ok = d < g.D;
+  float A2[NL], h[NL];
+#pragma unroll
+  for (int n = 0; n < NL; ++n) {
+    A2[n] = (ok && n < g.N) ? A[d * g.N + n] * LOG2E : 0.f;
+    h[n] = 0.f;
+  }
   const int64_t s0 = seg * g.Ls, s1 = s0 + g.Ls < g.L ? s0 + g.Ls : g.L;
   const int64_t nb = (s1 - s0 + TB - 1) / TB;
-  float h = 0.f;
   double dsacc = 0.0;
   for (int64_t k = 0; k < nb; ++k) {
     const int64_t kb = REV ? nb - 1 - k : k;
     const int64_t t0 = s0 + kb * TB;
     const int len = (int)(s1 - t0 < TB ? s1 - t0 : TB);
-    stage_block(st, x, dt, REV ? dy : nullptr, REV ? nullptr : Bm, REV ? Cm : nullptr, g, b, d0,
-                t0, len);
+    // reverse: xs holds dy
+    stage_channels(REV ? nullptr : xs, ds, REV ? xs : nullptr, REV ? nullptr : rs,
+                   REV ? rs : nullptr, x, dt, dy, Bm, Cm, g, b, d0, t0, len);
     __syncthreads();
-    if (!REV) {
-      for (int i = 0; i < len; ++i) {
-        const float de = ds[i * CH + c];
-        const float a = exp2f(de * A2);
-        h = fmaf(a, h, de * xs[i * CH + c] * bs[i * NL + n]);
-        dsacc += (double)de;
+    float bsum = 0.f;
+    for (int j = 0; j < len; ++j) {
+      const int i = REV ? len - 1 - j : j;
+      const float de = ds[i * CCH + c], sv = xs[i * CCH + c];
+      const float4 *r4 = reinterpret_cast<const float4 *>(rs + i * NL);
+      float r[NL];
+#pragma unroll
+      for (int q = 0; q < NL / 4; ++q) {
+        const float4 v = r4[q];
+        r[4 * q] = v.x; r[4 * q + 1] = v.y; r[4 * q + 2] = v.z; r[4 * q + 3] = v.w;
       }
-    } else {
-      for (int i = len - 1; i >= 0; --i) {
-        const float de = ds[i * CH + c];
-        const float a = exp2f(de * A2);
-        h = a * fmaf(cs[i * NL + n], ys[i * CH + c], h);
+      if (!REV) {
+        const float dx_ = de * sv;
+#pragma unroll
+        for (int n = 0; n < NL; ++n) h[n] = fmaf(exp2f(de * A2[n]), h[n], dx_ * r[n]);
+        bsum += de;
+      } else {
+#pragma unroll
+        for (int n = 0; n < NL; ++n) h[n] = exp2f(de * A2[n]) * fmaf(r[n], sv, h[n]);
       }
     }
+    dsacc += (double)bsum;
     __syncthreads();
   }
-  if (ok) states[((b * g.nseg + seg) * g.D + d) * g.N + n] = h;
-  if (!REV && n == 0 && d < g.D) dsum[(b * g.nseg + seg) * g.D + d] = (float)dsacc;
+  if (ok) {
+    float *dst = states + ((b * g.nseg + seg) * g.D + d) * g.N;
+#pragma unroll
+    for (int n = 0; n < NL; ++n)
+      if (n < g.N) dst[n] = h[n];
+    if (!REV) dsum[(b * g.nseg + seg) * g.D + d] = (float)dsacc;
+  }
 }
 
 // Across segments, in place: states[s] <- the state entering segment s from
@@ -156,41 +204,62 @@ __global__ void __launch_bounds__(256) k_mb_scan(float *__restrict__ states,
   }
 }
 
-// y of every segment from its entering state.  grid (ceil(D/CH), nseg, B)
-__global__ void __launch_bounds__(NT) k_mb_out(const float *__restrict__ x,
-                                               const float *__restrict__ dt,
-                                               const float *__restrict__ A,
-                                               const float *__restrict__ Bm,
-                                               const float *__restrict__ Cm,
-                                               const float *__restrict__ Dk,
-                                               const float *__restrict__ hin,
-                                               float *__restrict__ y, MGeo g) {
-  __shared__ float xs[TB * CH], ds[TB * CH], yo[TB * CH], bs[TB * NL], cs[TB * NL];
-  const Stage st{xs, ds, nullptr, bs, cs};
-  const int tid = threadIdx.x, c = tid / NL, n = tid % NL;
-  const int64_t d0 = (int64_t)blockIdx.x * CH, seg = blockIdx.y, b = blockIdx.z;
+// y of every segment from its entering state.  grid (ceil(D/CCH), nseg, B),
+// CCH threads
+__global__ void __launch_bounds__(CCH) k_mb_out(const float *__restrict__ x,
+                                                const float *__restrict__ dt,
+                                                const float *__restrict__ A,
+                                                const float *__restrict__ Bm,
+                                                const float *__restrict__ Cm,
+                                                const float *__restrict__ Dk,
+                                                const float *__restrict__ hin,
+                                                float *__restrict__ y, MGeo g) {
+  __shared__ float xs[TB * CCH], ds[TB * CCH];
+  __shared__ __align__(16) float bs[TB * NL], cs[TB * NL];
+  const int c = threadIdx.x;
+  const int64_t d0 = (int64_t)blockIdx.x * CCH, seg = blockIdx.y, b = blockIdx.z;
   const int64_t d = d0 + c;
-  const bool ok = d < g.D && n < g.N;
-  const float A2 = ok ? A[d * g.N + n] * LOG2E : 0.f;
-  const float Dd = (Dk && d < g.D) ? Dk[d] : 0.f;
+  const bool ok = d < g.D;
+  float A2[NL], h[NL];
+  const float *hsrc = hin + ((b * g.nseg + seg) * g.D + d) * g.N;
+#pragma unroll
+  for (int n = 0; n < NL; ++n) {
+    const bool on = ok && n < g.N;
+    A2[n] = on ? A[d * g.N + n] * LOG2E : 0.f;
+    h[n] = on ? hsrc[n] : 0.f;
+  }
+  const float Dd = (Dk && ok) ? Dk[d] : 0.f;
   const int64_t s0 = seg * g.Ls, s1 = s0 + g.Ls < g.L ? s0 + g.Ls : g.L;
-  float h = ok ? hin[((b * g.nseg + seg) * g.D + d) * g.N + n] : 0.f;
   for (int64_t t0 = s0; t0 < s1; t0 += TB) {
     const int len = (int)(s1 - t0 < TB ? s1 - t0 : TB);
-    stage_block(st, x, dt, nullptr, Bm, Cm, g, b, d0, t0, len);
+    stage_channels(xs, ds, nullptr, bs, cs, x, dt, nullptr, Bm, Cm, g, b, d0, t0, len);
     __syncthreads();
     for (int i = 0; i < len; ++i) {
-      const float de = ds[i * CH + c], xv = xs[i * CH + c];
-      const float a = exp2f(de * A2);
-      h = fmaf(a, h, de * xv * bs[i * NL + n]);
-      const float yv = half_sum(cs[i * NL + n] * h);
-      if (n == 0) yo[i * CH + c] = fmaf(Dd, xv, yv);
+      const float de = ds[i * CCH + c], xv = xs[i * CCH + c];
+      const float4 *b4 = reinterpret_cast<const float4 *>(bs + i * NL);
+      const float4 *c4 = reinterpret_cast<const float4 *>(cs + i * NL);
+      const float dx_ = de * xv;
+      float y0 = 0.f, y1 = 0.f;
+#pragma unroll
+      for (int q = 0; q < NL / 4; ++q) {
+        const float4 bv = b4[q], cv = c4[q];
+        h[4 * q + 0] = fmaf(exp2f(de * A2[4 * q + 0]), h[4 * q + 0], dx_ * bv.x);
+        h[4 * q + 1] = fmaf(exp2f(de * A2[4 * q + 1]), h[4 * q + 1], dx_ * bv.y);
+        h[4 * q + 2] = fmaf(exp2f(de * A2[4 * q + 2]), h[4 * q + 2], dx_ * bv.z);
+        h[4 * q + 3] = fmaf(exp2f(de * A2[4 * q + 3]), h[4 * q + 3], dx_ * bv.w);
+        y0 = fmaf(cv.x, h[4 * q + 0], y0);
+        y1 = fmaf(cv.y, h[4 * q + 1], y1);
+        y0 = fmaf(cv.z, h[4 * q + 2], y0);
+        y1 = fmaf(cv.w, h[4 * q + 3], y1);
+      }
+      xs[i * CCH + c] = fmaf(Dd, xv, y0 + y1);  // y replaces x in place
     }
     __syncthreads();
-    for (int idx = tid; idx < len * CH; idx += NT) {
-      const int tt = idx / CH, cc = idx - tt * CH;
-      if (d0 + cc < g.D) y[(b * g.L + t0 + tt) * g.D + d0 + cc] = yo[idx];
+    for (int idx = c; idx < len * CCH; idx += CCH) {
+      const int tt = idx / CCH, cc = idx - tt * CCH;
+      if (d0 + cc < g.D) y[(b * g.L + t0 + tt) * g.D + d0 + cc] = xs[idx];
     }
+    __syncthreads();
   }
 }
 
@@ -341,16 +410,16 @@ int num_sms() {
   return cache[dev];
 }
 
-// Segments: about eight 256-thread CTAs per SM in all, each segment a
-// multiple of TB tokens and at most MAX_LS (the backward's checkpoints live in
-// shared memory).
+// Segments: about 1024 channel threads per SM in all, each segment a multiple
+// of TB tokens and at most MAX_LS (the backward's checkpoints live in shared
+// memory).
 constexpr int64_t MAX_LS = 1024;
 
 MGeo make_geo(int64_t B, int64_t L, int64_t D, int64_t N) {
   MGeo g;
   g.B = B; g.L = L; g.D = D; g.N = N;
-  const int64_t base = B * ((D + CH - 1) / CH);
-  const int64_t want = (8 * (int64_t)num_sms() + base - 1) / base;
+  const int64_t base = B * D;
+  const int64_t want = (1024 * (int64_t)num_sms() + base - 1) / base;
   int64_t ls = (L + want - 1) / want;
   ls = (ls + TB - 1) / TB * TB;
   if (ls > MAX_LS) ls = MAX_LS;
@@ -383,10 +452,10 @@ cudaError_t fwd(const float *x, const float *dt, const float *A, const float *Bm
   const MGeo g = make_geo(B, L, D, N);
   float *hst = static_cast<float *>(ws);
   float *dsum = hst + g.B * g.nseg * g.D * g.N;
-  const dim3 grid((unsigned)((D + CH - 1) / CH), (unsigned)g.nseg, (unsigned)B);
+  const dim3 cgrid((unsigned)((D + CCH - 1) / CCH), (unsigned)g.nseg, (unsigned)B);
   {
     LaunchTrace lt("mamba.seg_state", s);
-    k_mb_local<false><<<grid, NT, 0, s>>>(x, dt, A, Bm, Cm, nullptr, hst, dsum, g);
+    k_mb_local<false><<<cgrid, CCH, 0, s>>>(x, dt, A, Bm, Cm, nullptr, hst, dsum, g);
   }
   {
     LaunchTrace lt("mamba.seg_scan", s);
@@ -394,7 +463,7 @@ cudaError_t fwd(const float *x, const float *dt, const float *A, const float *Bm
   }
   {
     LaunchTrace lt("mamba.out", s);
-    k_mb_out<<<grid, NT, 0, s>>>(x, dt, A, Bm, Cm, Dk, hst, y, g);
+    k_mb_out<<<cgrid, CCH, 0, s>>>(x, dt, A, Bm, Cm, Dk, hst, y, g);
   }
   return cudaGetLastError();
 }
@@ -414,10 +483,11 @@ cudaError_t bwd(const float *x, const float *dt, const float *A, const float *Bm
   if ((e = cudaMemsetAsync(dC, 0, sizeof(float) * B * L * N, s)) != cudaSuccess) return e;
   if (dD && (e = cudaMemsetAsync(dD, 0, sizeof(float) * D, s)) != cudaSuccess) return e;
   const dim3 grid((unsigned)((D + CH - 1) / CH), (unsigned)g.nseg, (unsigned)B);
+  const dim3 cgrid((unsigned)((D + CCH - 1) / CCH), (unsigned)g.nseg, (unsigned)B);
   const unsigned sgrid = (unsigned)cdiv(B * D * N, 256);
   {
     LaunchTrace lt("mamba.seg_state", s);
-    k_mb_local<false><<<grid, NT, 0, s>>>(x, dt, A, Bm, Cm, nullptr, hst, dsum, g);
+    k_mb_local<false><<<cgrid, CCH, 0, s>>>(x, dt, A, Bm, Cm, nullptr, hst, dsum, g);
   }
   {
     LaunchTrace lt("mamba.seg_scan", s);
@@ -425,7 +495,7 @@ cudaError_t bwd(const float *x, const float *dt, const float *A, const float *Bm
   }
   {
     LaunchTrace lt("mamba.seg_grad_state", s);
-    k_mb_local<true><<<grid, NT, 0, s>>>(x, dt, A, Bm, Cm, dy, ust, nullptr, g);
+    k_mb_local<true><<<cgrid, CCH, 0, s>>>(x, dt, A, Bm, Cm, dy, ust, nullptr, g);
   }
   {
     LaunchTrace lt("mamba.seg_scan", s);
