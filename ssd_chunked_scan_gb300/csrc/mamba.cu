@@ -27,8 +27,8 @@
 //
 //   k_mb_local<true>   each segment's u at its left end from u = 0 at its right
 //   k_mb_scan<true>    u entering every segment from the right
-//   k_mb_bwd           per segment: a forward pass that checkpoints h every 32
-//                      tokens (shared memory), then the 32-token blocks right
+//   k_mb_bwd           per segment: a forward pass that checkpoints h every 16
+//                      tokens (shared memory), then the 16-token windows right
 //                      to left: recompute h_t and the decays into registers,
 //                      walk them backwards accumulating
 //                        dx_t = sum_n g delta B + D dy     dA += g delta a h_{t-1}
@@ -263,8 +263,13 @@ __global__ void __launch_bounds__(CCH) k_mb_out(const float *__restrict__ x,
   }
 }
 
-// Backward of every segment.  Dynamic shared memory: the h checkpoints
-// [Ls/TB][NT], then the staging and reduction buffers.  grid (ceil(D/CH), nseg, B)
+// Backward of every segment, in windows of WB tokens.  Dynamic shared memory:
+// the h checkpoints [Ls/WB][NT], then the staging and reduction buffers.
+// The per-token sums over n (dx, ddelta) are collected for a whole window in
+// registers and reduce-scattered over the half-warp at its end (15 shuffles
+// per window instead of 4 per token), lane n ending with token n's sums.
+// grid (ceil(D/CH), nseg, B)
+constexpr int WB = 16;
 __global__ void __launch_bounds__(NT, 2) k_mb_bwd(
     const float *__restrict__ x, const float *__restrict__ dt, const float *__restrict__ A,
     const float *__restrict__ Bm, const float *__restrict__ Cm, const float *__restrict__ Dk,
@@ -273,16 +278,16 @@ __global__ void __launch_bounds__(NT, 2) k_mb_bwd(
     float *__restrict__ dB, float *__restrict__ dC, float *__restrict__ dD, MGeo g) {
   extern __shared__ float4 smem4[];
   float *sm = reinterpret_cast<float *>(smem4);
-  const int nck = (int)(g.Ls / TB);
+  const int nck = (int)(g.Ls / WB);
   float *ck = sm;                        // [nck][NT]
   float *xs = ck + nck * NT;             // [TB][CH]
   float *ds = xs + TB * CH;
   float *ys = ds + TB * CH;
   float *bs = ys + TB * CH;              // [TB][NL]
   float *cs = bs + TB * NL;
-  float *rdx = cs + TB * NL;             // [TB][CH]
+  float *rdx = cs + TB * NL;             // [WB][CH]
   float *rdt = rdx + TB * CH;
-  float *rB = rdt + TB * CH;             // [TB][NT/32][NL]
+  float *rB = rdt + TB * CH;             // [WB][NT/32][NL]
   float *rC = rB + TB * (NT / 32) * NL;
   const Stage st{xs, ds, ys, bs, cs};
   const int tid = threadIdx.x, c = tid / NL, n = tid % NL, warp = tid >> 5;
@@ -293,13 +298,13 @@ __global__ void __launch_bounds__(NT, 2) k_mb_bwd(
   const float A2 = Av * LOG2E;
   const float Dd = (Dk && d < g.D) ? Dk[d] : 0.f;
   const int64_t s0 = seg * g.Ls, s1 = s0 + g.Ls < g.L ? s0 + g.Ls : g.L;
-  const int nb = (int)((s1 - s0 + TB - 1) / TB);
+  const int nb = (int)((s1 - s0 + WB - 1) / WB);
 
-  // forward over the segment: checkpoint h before every block
+  // forward over the segment: checkpoint h before every window
   float h = ok ? hin[((b * g.nseg + seg) * g.D + d) * g.N + n] : 0.f;
   for (int k = 0; k < nb; ++k) {
-    const int64_t t0 = s0 + (int64_t)k * TB;
-    const int len = (int)(s1 - t0 < TB ? s1 - t0 : TB);
+    const int64_t t0 = s0 + (int64_t)k * WB;
+    const int len = (int)(s1 - t0 < WB ? s1 - t0 : WB);
     ck[k * NT + tid] = h;
     stage_block(st, x, dt, nullptr, Bm, nullptr, g, b, d0, t0, len);
     __syncthreads();
@@ -310,20 +315,20 @@ __global__ void __launch_bounds__(NT, 2) k_mb_bwd(
     __syncthreads();
   }
 
-  // blocks right to left
+  // windows right to left
   float u = ok ? uin[((b * g.nseg + seg) * g.D + d) * g.N + n] : 0.f;
   float dA_acc = 0.f, dD_acc = 0.f;
   for (int k = nb - 1; k >= 0; --k) {
-    const int64_t t0 = s0 + (int64_t)k * TB;
-    const int len = (int)(s1 - t0 < TB ? s1 - t0 : TB);
+    const int64_t t0 = s0 + (int64_t)k * WB;
+    const int len = (int)(s1 - t0 < WB ? s1 - t0 : WB);
     stage_block(st, x, dt, dy, Bm, Cm, g, b, d0, t0, len);
     __syncthreads();
     const float hstart = ck[k * NT + tid];
-    float hs[TB], as[TB];
+    float hs[WB], as[WB];
     {
       float hh = hstart;
 #pragma unroll
-      for (int i = 0; i < TB; ++i) {
+      for (int i = 0; i < WB; ++i) {
         if (i < len) {
           const float de = ds[i * CH + c];
           as[i] = exp2f(de * A2);
@@ -334,18 +339,22 @@ __global__ void __launch_bounds__(NT, 2) k_mb_bwd(
         hs[i] = hh;
       }
     }
+    float vdt[WB], vdx[WB];
 #pragma unroll
-    for (int i = TB - 1; i >= 0; --i) {
+    for (int i = WB - 1; i >= 0; --i) {
+      vdt[i] = 0.f;
+      vdx[i] = 0.f;
       if (i < len) {
         const float de = ds[i * CH + c], xv = xs[i * CH + c], dyv = ys[i * CH + c];
         const float Bn = bs[i * NL + n];
         const float gg = ok ? fmaf(cs[i * NL + n], dyv, u) : 0.f;
         const float hp = i > 0 ? hs[i - 1] : hstart;
         const float ahp = as[i] * hp;
-        dA_acc = fmaf(gg * de, ahp, dA_acc);
-        const float pdt = half_sum(gg * fmaf(Av, ahp, Bn * xv));
-        const float pdx = half_sum(gg * de * Bn);
-        float pB = gg * de * xv;
+        const float gde = gg * de;
+        dA_acc = fmaf(gde, ahp, dA_acc);
+        vdt[i] = gg * fmaf(Av, ahp, Bn * xv);
+        vdx[i] = gde * Bn;
+        float pB = gde * xv;
         float pC = ok ? dyv * hs[i] : 0.f;
         pB += __shfl_xor_sync(0xffffffffu, pB, 16);  // the warp's two channels
         pC += __shfl_xor_sync(0xffffffffu, pC, 16);
@@ -353,13 +362,26 @@ __global__ void __launch_bounds__(NT, 2) k_mb_bwd(
           rB[(i * (NT / 32) + warp) * NL + n] = pB;
           rC[(i * (NT / 32) + warp) * NL + n] = pC;
         }
-        if (n == 0) {
-          rdx[i * CH + c] = fmaf(Dd, dyv, pdx);
-          rdt[i * CH + c] = pdt;
-          dD_acc = fmaf(dyv, xv, dD_acc);
-        }
         u = as[i] * gg;
       }
+    }
+    // reduce-scatter over the half-warp: lane n ends with token n's sums
+#pragma unroll
+    for (int o = WB / 2; o >= 1; o >>= 1) {
+      const bool up = (n & o) != 0;
+#pragma unroll
+      for (int j = 0; j < o; ++j) {
+        const float sdt = up ? vdt[j] : vdt[j + o], kdt = up ? vdt[j + o] : vdt[j];
+        const float sdx = up ? vdx[j] : vdx[j + o], kdx = up ? vdx[j + o] : vdx[j];
+        vdt[j] = kdt + __shfl_xor_sync(0xffffffffu, sdt, o);
+        vdx[j] = kdx + __shfl_xor_sync(0xffffffffu, sdx, o);
+      }
+    }
+    if (n < len) {
+      const float dyn = ys[n * CH + c];
+      rdx[n * CH + c] = fmaf(Dd, dyn, vdx[0]);
+      rdt[n * CH + c] = vdt[0];
+      dD_acc = fmaf(dyn, xs[n * CH + c], dD_acc);
     }
     __syncthreads();
     for (int idx = tid; idx < len * CH; idx += NT) {
@@ -387,6 +409,7 @@ __global__ void __launch_bounds__(NT, 2) k_mb_bwd(
     __syncthreads();
   }
   if (ok) atomicAdd(dA + d * g.N + n, dA_acc);
+  dD_acc = half_sum(dD_acc);
   if (dD && n == 0 && d < g.D) atomicAdd(dD + d, dD_acc);
 }
 
@@ -430,7 +453,7 @@ MGeo make_geo(int64_t B, int64_t L, int64_t D, int64_t N) {
 }
 
 size_t bwd_smem(const MGeo &g) {
-  return sizeof(float) * ((size_t)(g.Ls / TB) * NT + 5 * TB * CH + 2 * TB * NL +
+  return sizeof(float) * ((size_t)(g.Ls / WB) * NT + 5 * TB * CH + 2 * TB * NL +
                           2 * (size_t)TB * (NT / 32) * NL);
 }
 
