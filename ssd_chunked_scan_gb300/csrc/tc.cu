@@ -309,7 +309,9 @@ __global__ void __launch_bounds__(NT2, 2) k_seg_state(const __grid_constant__ CU
 }
 
 // ===========================================================================
-// State passing over segments, in place (one thread per state element).
+// State passing over segments, in place (each thread owns 4 consecutive state
+// elements and loads up to SU segments of them at once, so a pass costs about
+// one memory round trip per SU segments).
 //   causal:      st[s] <- state entering segment s from the left; the first is
 //                init, or 0; the state right of the last segment goes to fin
 //   anti-causal: st[s] <- state entering segment s from the right; the one
@@ -317,7 +319,8 @@ __global__ void __launch_bounds__(NT2, 2) k_seg_state(const __grid_constant__ CU
 //                goes to fin
 // init is read, and fin (if given) written, transposed when TRANS.  When stT
 // is given, every result is also written there transposed.
-// grid (B*H, ceil(dk*dv / 128))
+// grid (B*H, ceil(dk*dv / (4*128))), dk*dv a multiple of 4
+constexpr int SU = 10;
 template <bool REV, bool TRANS>
 __global__ void __launch_bounds__(NTH) k_seg_scan(float *__restrict__ st,
                                                   const float *__restrict__ Aseg,
@@ -325,46 +328,50 @@ __global__ void __launch_bounds__(NTH) k_seg_scan(float *__restrict__ st,
                                                   float *__restrict__ fin,
                                                   float *__restrict__ stT, PassGeo p) {
   const int64_t bh = blockIdx.x;
-  const int64_t e = (int64_t)blockIdx.y * NTH + threadIdx.x;
+  const int64_t e0 = 4 * ((int64_t)blockIdx.y * NTH + threadIdx.x);
   const int64_t sz = (int64_t)p.dk * p.dv;
-  if (e >= sz) return;
-  const int64_t et = (e % p.dv) * p.dk + e / p.dv;  // transposed position
-  float *q = st + bh * p.nseg * sz + e;
-  float *qt = stT ? stT + bh * p.nseg * sz + et : nullptr;
+  if (e0 >= sz) return;
+  auto tpos = [&](int64_t e) { return (e % p.dv) * p.dk + e / p.dv; };  // transposed position
+  float4 *q = reinterpret_cast<float4 *>(st + bh * p.nseg * sz + e0);
+  const int64_t sz4 = sz / 4;
   const float *a = Aseg + bh * p.nseg;
-  constexpr int U = 8;  // segments loaded ahead of the dependent chain
-  float run = 0.f;
-  if (init) run = TRANS ? init[bh * sz + et] : init[bh * sz + e];
-  if (!REV) {
-    for (int s0 = 0; s0 < p.nseg; s0 += U) {
-      float x[U], d[U];
+  float run[4] = {0.f, 0.f, 0.f, 0.f};
+  if (init) {
 #pragma unroll
-      for (int u = 0; u < U; ++u)
-        if (s0 + u < p.nseg) { x[u] = q[(int64_t)(s0 + u) * sz]; d[u] = expf(a[s0 + u]); }
+    for (int j = 0; j < 4; ++j) run[j] = init[bh * sz + (TRANS ? tpos(e0 + j) : e0 + j)];
+  }
+  for (int k0 = 0; k0 < p.nseg; k0 += SU) {
+    float4 x[SU];
+    float d[SU];
 #pragma unroll
-      for (int u = 0; u < U; ++u)
-        if (s0 + u < p.nseg) {
-          q[(int64_t)(s0 + u) * sz] = run;
-          if (qt) qt[(int64_t)(s0 + u) * sz] = run;
-          run = fmaf(d[u], run, x[u]);
-        }
+    for (int u = 0; u < SU; ++u) {
+      const int k = k0 + u;
+      if (k < p.nseg) {
+        const int s = REV ? p.nseg - 1 - k : k;
+        x[u] = q[(int64_t)s * sz4];
+        d[u] = expf(a[s]);
+      }
     }
-    if (fin) fin[bh * sz + (TRANS ? et : e)] = run;
-  } else {
-    for (int s0 = p.nseg - 1; s0 >= 0; s0 -= U) {
-      float x[U], d[U];
 #pragma unroll
-      for (int u = 0; u < U; ++u)
-        if (s0 - u >= 0) { x[u] = q[(int64_t)(s0 - u) * sz]; d[u] = expf(a[s0 - u]); }
+    for (int u = 0; u < SU; ++u) {
+      const int k = k0 + u;
+      if (k < p.nseg) {
+        const int s = REV ? p.nseg - 1 - k : k;
+        q[(int64_t)s * sz4] = make_float4(run[0], run[1], run[2], run[3]);
+        if (stT) {
 #pragma unroll
-      for (int u = 0; u < U; ++u)
-        if (s0 - u >= 0) {
-          q[(int64_t)(s0 - u) * sz] = run;
-          if (qt) qt[(int64_t)(s0 - u) * sz] = run;
-          run = fmaf(d[u], run, x[u]);
+          for (int j = 0; j < 4; ++j) stT[bh * p.nseg * sz + (int64_t)s * sz + tpos(e0 + j)] = run[j];
         }
+        run[0] = fmaf(d[u], run[0], x[u].x);
+        run[1] = fmaf(d[u], run[1], x[u].y);
+        run[2] = fmaf(d[u], run[2], x[u].z);
+        run[3] = fmaf(d[u], run[3], x[u].w);
+      }
     }
-    if (fin) fin[bh * sz + (TRANS ? et : e)] = run;
+  }
+  if (fin) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) fin[bh * sz + (TRANS ? tpos(e0 + j) : e0 + j)] = run[j];
   }
 }
 
@@ -748,7 +755,8 @@ __global__ void __launch_bounds__(NT2, 2) k_walk(const __grid_constant__ CUtenso
 // group:
 //   B_t = sum_{t' >= t, s < t, both in the chunk} exp(cs_t' - cs_s) (q_t'.k_s)(dout_t'.v_s)
 // (the block of M = D o (q k^T) o (dout v^T) below row t and left of column
-// t).  q k^T is computed once; dout v^T per head.  Both score MMAs have M = 64
+// t), from the row and column sums of M's strictly lower triangle.  q k^T is
+// computed once; dout v^T per head.  Both score MMAs have M = 64
 // (rows 16w..16w+15 in lanes 32w..) and share one two-tile shared-memory
 // buffer; the next head's tiles load while the current head's sums run.
 // grid (N chunks, G, B), 128 threads, two CTAs per SM.
@@ -763,7 +771,7 @@ __global__ void __launch_bounds__(NTH) k_dla_intra(const __grid_constant__ CUten
   const int dk = p.dk, dv = p.dv;  // here dk = q/k features, dv = v/dout features
   const int ncbk = p.dkp / 32, ncbv = p.dvp / 32, ncbm = ncbk > ncbv ? ncbk : ncbv;
   uint8_t *T1 = smem, *T2 = smem + ncbm * 8192;
-  float *R = (float *)(T2 + ncbm * 8192);  // [64][65]
+  float *R = (float *)(T2 + ncbm * 8192);  // [4][64] column partials, [64] row sums
   float *cs = R + C * (C + 1);            // [64]
   __shared__ uint64_t bar_tma, bar_mma;
   __shared__ uint32_t tmem_base;
@@ -805,7 +813,11 @@ __global__ void __launch_bounds__(NTH) k_dla_intra(const __grid_constant__ CUten
     const int ncb = ph == 0 ? ncbk : ncbv;
     const int kdim = ph == 0 ? dk : dv;
     const int64_t h = grp * hpg + (ph == 0 ? 0 : ph - 1);
-    if (ph >= 1 && warp == 0) warp_cumsum64(la, (b * p.L + t0) * p.H + h, p.H, len, 0.0, cs);
+    if (ph >= 1 && warp == 0) {  // in-chunk prefix of la, times log2(e)
+      warp_cumsum64(la, (b * p.L + t0) * p.H + h, p.H, len, 0.0, cs);
+      __syncwarp();
+      for (int t = lane; t < C; t += 32) cs[t] = t < len ? cs[t] * 1.4426950408889634f : 0.f;
+    }
     ok = mbar_wait(&bar_tma, ph & 1) && ok;
     if (tid == 0 && ok) pending = 0;
     if (__syncthreads_or(!ok)) break;
@@ -861,23 +873,56 @@ __global__ void __launch_bounds__(NTH) k_dla_intra(const __grid_constant__ CUten
 #pragma unroll
       for (int u = 0; u < 32; ++u) dp[32 + u] = t32[u];
     }
-    if (lane < 16) {  // row r: prefix sums R[r][t] = sum_{u < t} M[r][u]
-      const int r = warp * 16 + lane;
-      const float cr = cs[r < len ? r : 0];
-      float acc = 0.f;
-      R[r * (C + 1)] = 0.f;
+    // B_t = B_{t+1} + rowpre_t - colsuf_t with rowpre_t = sum_{u<t} M[t][u]
+    // (a row of the strictly lower triangle) and colsuf_t = sum_{r>t} M[r][t]
+    // (a column of it).  Row r lives in lane r % 16 of warp r / 16; the column
+    // sums are reduce-scattered over the warp (lane l ends with columns 2l,
+    // 2l+1), then added over the four warps in shared memory.
+    {
+      const int r = warp * 16 + (lane & 15);
+      const bool rowok = lane < 16 && r < len;
+      const float cr = cs[rowok ? r : 0];
+      float *m = dp;  // M's row, in place of dout v^T's
+      float rp0 = 0.f, rp1 = 0.f;
 #pragma unroll
       for (int u = 0; u < C; ++u) {
-        const float m = (r < len && u <= r) ? expf(cr - cs[u]) * sq[u] * dp[u] : 0.f;
-        acc += m;
-        R[r * (C + 1) + u + 1] = acc;
+        m[u] = (rowok && u < r) ? ex2f(cr - cs[u]) * sq[u] * dp[u] : 0.f;
+        if (u & 1) rp1 += m[u];
+        else rp0 += m[u];
       }
+#pragma unroll
+      for (int off = 16, n = C; off >= 1; off >>= 1, n >>= 1) {
+        const bool up = (lane & off) != 0;
+#pragma unroll
+        for (int k2 = 0; k2 < n / 2; ++k2) {
+          const float mine = up ? m[n / 2 + k2] : m[k2];
+          const float send = up ? m[k2] : m[n / 2 + k2];
+          m[k2] = mine + __shfl_xor_sync(0xffffffffu, send, off);
+        }
+      }
+      R[warp * C + 2 * lane] = m[0];
+      R[warp * C + 2 * lane + 1] = m[1];
+      if (rowok) R[4 * C + r] = rp0 + rp1;
     }
     __syncthreads();
-    if (tid < len) {
-      float bsum = 0.f;
-      for (int r = tid; r < len; ++r) bsum += R[r * (C + 1) + tid];
-      Bt[(b * p.L + t0 + tid) * p.H + h] = bsum;
+    if (warp == 0) {  // suffix sums of rowpre - colsuf; lane l owns t = 2l, 2l + 1
+      float dd[2];
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const int t = 2 * lane + j;
+        dd[j] = t < len ? R[4 * C + t] - (R[t] + R[C + t] + R[2 * C + t] + R[3 * C + t]) : 0.f;
+      }
+      float x = dd[0] + dd[1];  // inclusive suffix over lanes of the pair sums
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const float y = __shfl_down_sync(0xffffffffu, x, o);
+        if (lane + o < 32) x += y;
+      }
+      const float b1 = x - dd[0];  // B_{2l+1} = suffix from 2l+1
+      const float b0 = x;          // B_{2l}
+      float *bt = Bt + (b * p.L + t0) * p.H + h;
+      if (2 * lane < len) bt[(int64_t)(2 * lane) * p.H] = b0;
+      if (2 * lane + 1 < len) bt[(int64_t)(2 * lane + 1) * p.H] = b1;
     }
     __syncthreads();  // R and cs are reused by the next head
   }
@@ -1076,7 +1121,7 @@ cudaError_t run_states(const PassGeo &p, const float *kp, const float *vp, const
   }
   {
     LaunchTrace lt("tc.seg_scan", s);
-    const dim3 sg((unsigned)(p.B * p.H), (unsigned)cdiv((int64_t)p.dk * p.dv, NTH));
+    const dim3 sg((unsigned)(p.B * p.H), (unsigned)cdiv((int64_t)p.dk * p.dv, 4 * NTH));
     if (trans) k_seg_scan<REV, true><<<sg, NTH, 0, s>>>(states, Aseg, h0, fin, statesT, p);
     else k_seg_scan<REV, false><<<sg, NTH, 0, s>>>(states, Aseg, h0, fin, statesT, p);
   }
