@@ -578,10 +578,18 @@ __global__ void __launch_bounds__(NT2, 2) k_walk(const __grid_constant__ CUtenso
       tmem_st32(tmem + lb + 64 + hf * 32, v);
     }
     float kw[32];  // w_u * k'[u][L], tokens [32 hf, 32 hf + 32)
+    {
+      const float4 *sw4 = reinterpret_cast<const float4 *>(statew + hf * 32);
 #pragma unroll
-    for (int uu = 0; uu < 32; ++uu) {
-      const int u = hf * 32 + uu;
-      kw[uu] = (L < dk) ? tf32r(*(const float *)(Kb + sw128_off(u, L, C)) * (statew[u] * kscale)) : 0.f;
+      for (int u4 = 0; u4 < 8; ++u4) {
+        const float4 wv = sw4[u4];
+        const float wq[4] = {wv.x, wv.y, wv.z, wv.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int uu = 4 * u4 + e, u = hf * 32 + uu;
+          kw[uu] = (L < dk) ? tf32r(*(const float *)(Kb + sw128_off(u, L, C)) * (wq[e] * kscale)) : 0.f;
+        }
+      }
     }
     ok = mbar_wait(&bar_s, ci & 1) && ok;
     tc_fence_after();
@@ -596,11 +604,13 @@ __global__ void __launch_bounds__(NT2, 2) k_walk(const __grid_constant__ CUtenso
 #pragma unroll
       for (int uu = 0; uu < 32; uu += 4) {
         float f[4];
+        const float4 c4 = *reinterpret_cast<const float4 *>(cs2 + hf * 32 + uu);
+        const float cu[4] = {c4.x, c4.y, c4.z, c4.w};
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const int u = hf * 32 + uu + e;
           const bool valid = r < len && u < len && (REV ? u >= r : u <= r);
-          f[e] = valid ? tf32r(ex2f(REV ? cs2[u] - cr : cr - cs2[u]) * sr[uu + e]) : 0.f;
+          f[e] = valid ? tf32r(ex2f(REV ? cu[e] - cr : cr - cu[e]) * sr[uu + e]) : 0.f;
         }
         *reinterpret_cast<float4 *>(P + sw128_off(r, hf * 32 + uu, C)) = make_float4(f[0], f[1], f[2], f[3]);
       }
