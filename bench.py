@@ -56,10 +56,21 @@ def load_peaks():
                 "source": "fallback"}
 
 
-# DRAM bytes (read + write) per launch from one ncu capture of the kernel as it
-# stands (profiles/tc_g2h8_d128_L8192_long.md); kernels without a capture of
-# their current version report null
-TRAFFIC = {"tc.walk_dq": 418.697728e6 + 30.914304e6}
+# DRAM bytes (read + write) per launch of each tensor-core kernel from one ncu
+# capture of the kernels as they stand (profiles/tc_g2h8_d128_L8192_long.md,
+# g2h8_d128 L=8192 long-memory workload); a kernel without an entry reports
+# null.  Every change to a kernel must refresh or drop its entry.
+TRAFFIC = {
+    "tc.seg_state": 169031424 + 22852608,
+    "tc.seg_state_dq": 168997632 + 20012544,
+    "tc.seg_state_dk": 169008384 + 19907328,
+    "tc.walk_out": 249233664 + 95364608,
+    "tc.walk_dq": 418997248 + 27221504,
+    "tc.walk_dk": 418941184 + 26888448,
+    "tc.walk_dv": 248437504 + 95309312,
+    "tc.dla_intra": 336851200 + 608768,
+    "tc.dla": 78656256 + 32000,
+}
 
 # nominal dense tensor rates: tf32 1.1 PF vs bf16 2.25 PF per GPU
 TF32_OVER_BF16 = 1.1 / 2.25
@@ -163,6 +174,13 @@ class ClockSampler:
             return
         self.t = threading.Thread(target=self._read, daemon=True)
         self.t.start()
+
+    def wait_first(self, timeout=5.0):
+        """Block until the sampler has produced a sample (nvidia-smi's start-up
+        stalls the GPU briefly; it must not fall inside a timed region)."""
+        t0 = time.time()
+        while self.proc is not None and not self.samples and time.time() - t0 < timeout:
+            time.sleep(0.02)
 
     def _read(self):
         for line in self.proc.stdout:
@@ -451,6 +469,7 @@ def run_mamba(args):
 
     clocks = ClockSampler(0)
     clocks.start()
+    clocks.wait_first()
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize(dev)
@@ -662,6 +681,7 @@ def main():
 
     clocks = ClockSampler(local)
     clocks.start()
+    clocks.wait_first()
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize(dev)

@@ -184,8 +184,10 @@ __global__ void __launch_bounds__(CCH) k_mb_local(const float *__restrict__ x,
 }
 
 // Across segments, in place: states[s] <- the state entering segment s from
-// the left (forward) or the u entering it from the right (reverse).
+// the left (forward) or the u entering it from the right (reverse).  The
+// segments' values are loaded MS at a time ahead of the dependent chain.
 // grid (ceil(B*D*N / 256))
+constexpr int MS = 12;
 template <bool REV>
 __global__ void __launch_bounds__(256) k_mb_scan(float *__restrict__ states,
                                                  const float *__restrict__ dsum,
@@ -195,12 +197,26 @@ __global__ void __launch_bounds__(256) k_mb_scan(float *__restrict__ states,
   const int64_t b = e / (g.D * g.N), dn = e - b * g.D * g.N, d = dn / g.N;
   const float A2 = A[dn] * LOG2E;
   float run = 0.f;
-  for (int64_t k = 0; k < g.nseg; ++k) {
-    const int64_t s = REV ? g.nseg - 1 - k : k;
-    float *p = states + (b * g.nseg + s) * g.D * g.N + dn;
-    const float xv = *p;
-    *p = run;
-    run = fmaf(exp2f(A2 * dsum[(b * g.nseg + s) * g.D + d]), run, xv);
+  for (int64_t k0 = 0; k0 < g.nseg; k0 += MS) {
+    float xv[MS], dec[MS];
+#pragma unroll
+    for (int u = 0; u < MS; ++u) {
+      const int64_t k = k0 + u;
+      if (k < g.nseg) {
+        const int64_t s = REV ? g.nseg - 1 - k : k;
+        xv[u] = states[(b * g.nseg + s) * g.D * g.N + dn];
+        dec[u] = exp2f(A2 * dsum[(b * g.nseg + s) * g.D + d]);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < MS; ++u) {
+      const int64_t k = k0 + u;
+      if (k < g.nseg) {
+        const int64_t s = REV ? g.nseg - 1 - k : k;
+        states[(b * g.nseg + s) * g.D * g.N + dn] = run;
+        run = fmaf(dec[u], run, xv[u]);
+      }
+    }
   }
 }
 
