@@ -406,11 +406,11 @@ __global__ void __launch_bounds__(NT2, 2) k_walk(const __grid_constant__ CUtenso
   uint8_t *Kb = Qb + ncbk * 8192;
   uint8_t *Vb = Kb + ncbk * 8192;
   // per-chunk factors, double-buffered: in-chunk prefix of la times log2(e),
-  // exp(cs), exp(A - cs); computed one chunk ahead by warp 0
+  // exp(cs), exp(A - cs); computed one chunk ahead by warp 4
   float *cs2b = (float *)(Vb + vbytes);  // [2][64]
   float *ewb = cs2b + 2 * C, *wwb = ewb + 2 * C;
   float *red = wwb + 2 * C;  // [4][64]
-  float *scr = red + 4 * C;  // [64] scratch of warp 0
+  float *scr = red + 4 * C;  // [64] scratch of warp 4
   __shared__ uint64_t bar_tma, bar_s, bar_i, bar_o, bar_h;
   __shared__ uint32_t tmem_base;
   __shared__ float a_chunk[2];
@@ -424,13 +424,16 @@ __global__ void __launch_bounds__(NT2, 2) k_walk(const __grid_constant__ CUtenso
   const int nc = (int)cdiv(s_end - s_begin, C);
   const int kslot = qk_slot(p, h), vslot = v_slot(p, h);
   const int dk = p.dk, dv = p.dv, dkn = p.dkn;
-  const uint32_t tile_tx = (uint32_t)(2 * ncbk + ncbv) * 8192;
   const int oslot = oa.out_slots == p.H ? (int)h : (int)(h / p.hpg);
   constexpr float LOG2E = 1.4426950408889634f;
 
+  // Serial issue work is spread over warps: thread 0 issues the MMAs, lane 0
+  // of warps 1, 2, 3 the q', v' and k' tile loads (three arrivals complete a
+  // load phase), warp 4 computes the next chunk's decay factors.
+  const bool ldq = tid == 32, ldv = tid == 64, ldk = tid == 96;
   if (warp == 0) tmem_alloc(&tmem_base, 256);
   if (tid == 0) {
-    mbar_init(&bar_tma, 1);
+    mbar_init(&bar_tma, 3);
     mbar_init(&bar_s, 1);
     mbar_init(&bar_i, 1);
     mbar_init(&bar_o, 1);
@@ -445,27 +448,38 @@ __global__ void __launch_bounds__(NT2, 2) k_walk(const __grid_constant__ CUtenso
   tc_fence_after();
   const uint32_t tmem = tmem_base;
   const uint32_t lb = (uint32_t)(qd * 32) << 16;
-  int tma_pending = -1;  // barrier phase of loads not yet waited for (thread 0)
+  int tma_pending = -1;  // barrier phase of this loader's loads not yet waited for
   // chunk c's tiles; `use` counts the barrier's phases (chunks in walk order).
-  // The q'/v' and k' halves may be issued at different times.
-  auto tma_qv = [&](int c, int use) {
+  // Each loader thread arrives once per phase with its own byte count; the
+  // k' tile may be issued later than the q' and v' tiles.
+  auto tma_q = [&](int c, int use) {
     const int row = (int)(b * p.L + s_begin + (int64_t)c * C);
-    mbar_expect_tx(&bar_tma, tile_tx);
+    mbar_expect_tx(&bar_tma, (uint32_t)ncbk * 8192);
     for (int cb = 0; cb < ncbk; ++cb) tma_load_3d(Qb + cb * 8192, &tmQ, &bar_tma, cb * 32, kslot, row);
+    tma_pending = use;
+  };
+  auto tma_v = [&](int c, int use) {
+    const int row = (int)(b * p.L + s_begin + (int64_t)c * C);
+    mbar_expect_tx(&bar_tma, (uint32_t)ncbv * 8192);
     for (int cb = 0; cb < ncbv; ++cb) tma_load_3d(Vb + cb * 8192, &tmV, &bar_tma, cb * 32, vslot, row);
     tma_pending = use;
   };
-  auto tma_k = [&](int c) {
+  auto tma_k = [&](int c, int use) {
     const int row = (int)(b * p.L + s_begin + (int64_t)c * C);
+    mbar_expect_tx(&bar_tma, (uint32_t)ncbk * 8192);
     for (int cb = 0; cb < ncbk; ++cb) tma_load_3d(Kb + cb * 8192, &tmK, &bar_tma, cb * 32, kslot, row);
+    tma_pending = use;
+  };
+  auto issue_first_loads = [&]() {
+    const int c0 = REV ? nc - 1 : 0;
+    if (ldq) tma_q(c0, 0);
+    if (ldv) tma_v(c0, 0);
+    if (ldk) tma_k(c0, 0);
   };
 
-  if (tid == 0 && !hseg_t) {
-    tma_qv(REV ? nc - 1 : 0, 0);
-    tma_k(REV ? nc - 1 : 0);
-  }
+  if (!hseg_t) issue_first_loads();
 
-  // warp 0: the factors of chunk c into buffer bf
+  // warp 4: the factors of chunk c into buffer bf
   auto chunk_factors = [&](int c, int bf) {
     const int64_t t0 = s_begin + (int64_t)c * C;
     const int len = (int)imin64(C, s_end - t0);
@@ -481,7 +495,7 @@ __global__ void __launch_bounds__(NT2, 2) k_walk(const __grid_constant__ CUtenso
     if (lane == 0) a_chunk[bf] = ex2f(tot2);
     __syncwarp();
   };
-  if (warp == 0) chunk_factors(REV ? nc - 1 : 0, 0);
+  if (warp == 4) chunk_factors(REV ? nc - 1 : 0, 0);
 
   {  // running state, transposed: lane j, column i = state[i][j]
     const float *H0 = Hseg + (bh * p.nseg + seg) * (int64_t)dk * dv;
@@ -505,10 +519,7 @@ __global__ void __launch_bounds__(NT2, 2) k_walk(const __grid_constant__ CUtenso
         tmem_st32(tmem + lb + 128 + c0, hv);
       }
       __syncthreads();  // the tile buffers are about to receive the first loads
-      if (tid == 0) {
-        tma_qv(REV ? nc - 1 : 0, 0);
-        tma_k(REV ? nc - 1 : 0);
-      }
+      issue_first_loads();
     } else {
       for (int c0 = hf * 64; c0 < hf * 64 + 64 && c0 < rup(dk, 32); c0 += 32) {
         float hv[32];
@@ -549,7 +560,7 @@ __global__ void __launch_bounds__(NT2, 2) k_walk(const __grid_constant__ CUtenso
     const int fb = ci & 1;
     const float *cs2 = cs2b + fb * C, *ew = ewb + fb * C, *ww = wwb + fb * C;
     ok = mbar_wait(&bar_tma, ci & 1) && ok;
-    if (tid == 0 && ok) tma_pending = -1;
+    if (ok) tma_pending = -1;
     tc_fence_before();
     if (__syncthreads_or(!ok)) break;
     tc_fence_after();
@@ -653,7 +664,7 @@ __global__ void __launch_bounds__(NT2, 2) k_walk(const __grid_constant__ CUtenso
         mma_commit(&bar_o);
       }
     }
-    if (warp == 0 && ci + 1 < nc) chunk_factors(cnext, fb ^ 1);
+    if (warp == 4 && ci + 1 < nc) chunk_factors(cnext, fb ^ 1);
     if (split) {
       // dcs[t] = y_t . (inter-chunk part of out'_t), reduced over the 128 lanes
       float yv[32];
@@ -704,9 +715,10 @@ __global__ void __launch_bounds__(NT2, 2) k_walk(const __grid_constant__ CUtenso
     ok = mbar_wait(&bar_o, ci & 1) && ok;
     tc_fence_after();
     // q' and v' tiles are free now (and k' too when the update ran): next loads
-    if (tid == 0 && ok && ci + 1 < nc) {
-      tma_qv(cnext, ci + 1);
-      if (lazy) tma_k(cnext);
+    if (ok && ci + 1 < nc) {
+      if (ldq) tma_q(cnext, ci + 1);
+      if (ldv) tma_v(cnext, ci + 1);
+      if (ldk && lazy) tma_k(cnext, ci + 1);
     }
     {
       float o[32];
@@ -746,7 +758,7 @@ __global__ void __launch_bounds__(NT2, 2) k_walk(const __grid_constant__ CUtenso
       ok = mbar_wait(&bar_h, hphase & 1) && ok;
       ++hphase;
       tc_fence_after();
-      if (tid == 0 && ok && ci + 1 < nc) tma_k(cnext);
+      if (ldk && ok && ci + 1 < nc) tma_k(cnext, ci + 1);
       alpha = 1.f;
     }
     tc_fence_before();
@@ -754,7 +766,7 @@ __global__ void __launch_bounds__(NT2, 2) k_walk(const __grid_constant__ CUtenso
     tc_fence_after();
   }
   __syncthreads();
-  if (tid == 0 && tma_pending >= 0) mbar_wait(&bar_tma, tma_pending & 1);
+  if ((ldq || ldv || ldk) && tma_pending >= 0) mbar_wait(&bar_tma, tma_pending & 1);
   tc_fence_before();
   __syncthreads();
   if (warp == 0) tmem_dealloc(tmem, 256);
