@@ -151,10 +151,13 @@ __global__ void __launch_bounds__(NT2, 2) k_seg_state(const __grid_constant__ CU
   const int nsl = (int)cdiv(s_end - s_begin, SL);
   const int kslot = qk_slot(p, h), vslot = v_slot(p, h);
 
+  // thread 0 issues the MMAs; lane 0 of warp 1 / warp 2 loads the k' / v'
+  // slices (two arrivals complete a stage's load phase)
+  const bool ldk = tid == 32, ldv = tid == 64;
   if (warp == 0) tmem_alloc(&tmem_base, 256);
   if (tid == 0) {
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&bar_tma[i], 1);
+      mbar_init(&bar_tma[i], 2);
       mbar_init(&bar_mma[i], 1);
     }
     fence_mbar_init();
@@ -162,17 +165,21 @@ __global__ void __launch_bounds__(NT2, 2) k_seg_state(const __grid_constant__ CU
     prefetch_tmap(&tmV);
   }
   __syncthreads();
-  int pend[2] = {-1, -1};  // slice in flight per stage (thread 0's view)
-  auto issue_tma = [&](int n) {
+  int pend[2] = {-1, -1};  // slice in flight per stage (each loader's view)
+  auto issue_tma = [&](int n) {  // the calling loader's half of slice n
     const int st = n & 1;
     pend[st] = n;
     const int row = (int)(b * p.L + s_begin + (int64_t)n * SL);
     uint8_t *Xt = tiles + st * stage, *Yt = Xt + xbytes;
-    mbar_expect_tx(&bar_tma[st], stage);
-    for (int cb = 0; cb < ncbk; ++cb) tma_load_3d(Xt + cb * 4096, &tmK, &bar_tma[st], cb * 32, kslot, row);
-    for (int cb = 0; cb < ncbv; ++cb) tma_load_3d(Yt + cb * 4096, &tmV, &bar_tma[st], cb * 32, vslot, row);
+    if (ldk) {
+      mbar_expect_tx(&bar_tma[st], xbytes);
+      for (int cb = 0; cb < ncbk; ++cb) tma_load_3d(Xt + cb * 4096, &tmK, &bar_tma[st], cb * 32, kslot, row);
+    } else {
+      mbar_expect_tx(&bar_tma[st], ybytes);
+      for (int cb = 0; cb < ncbv; ++cb) tma_load_3d(Yt + cb * 4096, &tmV, &bar_tma[st], cb * 32, vslot, row);
+    }
   };
-  if (tid == 0) {
+  if (ldk || ldv) {
     issue_tma(0);
     if (nsl > 1) issue_tma(1);
   }
@@ -230,7 +237,7 @@ __global__ void __launch_bounds__(NT2, 2) k_seg_state(const __grid_constant__ CU
     const uint8_t *Xt = tiles + st * stage, *Yt = Xt + xbytes;
     uint8_t *Bs = Bb + st * bbytes;
     ok = mbar_wait(&bar_tma[st], (n >> 1) & 1) && ok;
-    if (tid == 0 && ok) pend[st] = -1;
+    if (ok) pend[st] = -1;
     if (n >= 2) ok = mbar_wait(&bar_mma[st], ((n >> 1) - 1) & 1) && ok;  // slice n-2 done
     if (__syncthreads_or(!ok)) break;
     tc_fence_after();
@@ -259,8 +266,8 @@ __global__ void __launch_bounds__(NT2, 2) k_seg_state(const __grid_constant__ CU
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    if ((ldk || ldv) && n + 2 < nsl) issue_tma(n + 2);  // this stage's tiles are consumed
     if (tid == 0) {
-      if (n + 2 < nsl) issue_tma(n + 2);  // this stage's tiles are consumed
       const uint32_t bsm = smem_u32(Bs);
       const uint32_t id = idesc_tf32(128, p.dvn);
 #pragma unroll
@@ -298,7 +305,7 @@ __global__ void __launch_bounds__(NT2, 2) k_seg_state(const __grid_constant__ CU
       const int e = 4 * m, i = e / p.dv, j = e - i * p.dv;
       *reinterpret_cast<float4 *>(dst + e) = *reinterpret_cast<const float4 *>(Ds + sw128_off(i, j, dkr));
     }
-  } else if (tid == 0) {
+  } else if (ldk || ldv) {
     // tiles of up to two slices may still be in flight: wait for them
     for (int st = 0; st < 2; ++st)
       if (pend[st] >= 0) mbar_wait(&bar_tma[st], (pend[st] >> 1) & 1);
