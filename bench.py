@@ -61,15 +61,23 @@ def load_peaks():
 # g2h8_d128 L=8192 long-memory workload); a kernel without an entry reports
 # null.  Every change to a kernel must refresh or drop its entry.
 TRAFFIC = {
-    "tc.seg_state": 169031424 + 22852608,
-    "tc.seg_state_dq": 168997632 + 20012544,
-    "tc.seg_state_dk": 169008384 + 19907328,
-    "tc.walk_out": 249233664 + 95364608,
-    "tc.walk_dq": 418997248 + 27221504,
-    "tc.walk_dk": 418941184 + 26888448,
-    "tc.walk_dv": 248437504 + 95309312,
-    "tc.dla_intra": 336851200 + 608768,
-    "tc.dla": 78656256 + 32000,
+    "tc.seg_state": 168923136 + 22324480,
+    "tc.seg_state_dq": 168907520 + 19192320,
+    "tc.seg_state_dk": 168946688 + 19278592,
+    "tc.walk_out": 249328384 + 94038272,
+    "tc.walk_dq": 419541504 + 27310592,
+    "tc.walk_dk": 419954688 + 27263232,
+    "tc.walk_dv": 248214272 + 93885696,
+    "tc.dla_intra": 336926720 + 662016,
+    "tc.dla": 78654976 + 85248,
+}
+# the same for the Mamba kernels at d1024 L8192 (profiles/mamba_d1024_L8192.md)
+MAMBA_TRAFFIC = {
+    "mamba.seg_state": 270665216 + 4625920,
+    "mamba.seg_scan": 10388736,
+    "mamba.out": 282570240 + 100506880,
+    "mamba.seg_grad_state": 270926080 + 769024,
+    "mamba.bwd": 430734592 + 242471936,
 }
 
 # nominal dense tensor rates: tf32 1.1 PF vs bf16 2.25 PF per GPU
@@ -525,7 +533,9 @@ def run_mamba(args):
     else:
         roof = {"bound": "hbm", "achieved": kb / (per / 1e3) / 1e9, "peak": peaks["hbm_gbs"],
                 "unit": "GB/s", "peak_note": f"{peaks['source']} copy bandwidth"}
-    roof.update({"frac": roof["achieved"] / roof["peak"], "traffic": None, "kernel": top_name,
+    roof.update({"frac": roof["achieved"] / roof["peak"],
+                 "traffic": MAMBA_TRAFFIC.get(top_name) if w.name == MAMBA_WORKLOAD else None,
+                 "kernel": top_name,
                  "kernel_ms_per_launch": per, "alg_bytes_per_launch": kb,
                  "alg_exp_per_launch": kx})
     page = PAGE_MAMBA_CPU_MS.get(w.name, {})
@@ -591,7 +601,7 @@ def run_mamba_reference(args):
     return 0
 
 
-def mamba_cpu_sample(w, fb, min_seconds=10.0, max_reps=30):
+def mamba_cpu_sample(w, fb, min_seconds=10.0, max_reps=80):
     """The float64 Mamba oracle on batch entry 0 of the workload, repeated for
     about min_seconds."""
     import numpy as np
