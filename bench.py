@@ -64,10 +64,6 @@ TRAFFIC = {
     "tc.seg_state": 168923136 + 22324480,
     "tc.seg_state_dq": 168907520 + 19192320,
     "tc.seg_state_dk": 168946688 + 19278592,
-    "tc.walk_out": 249328384 + 94038272,
-    "tc.walk_dq": 419541504 + 27310592,
-    "tc.walk_dk": 419954688 + 27263232,
-    "tc.walk_dv": 248214272 + 93885696,
     "tc.dla_intra": 336926720 + 662016,
     "tc.dla": 78654976 + 85248,
 }

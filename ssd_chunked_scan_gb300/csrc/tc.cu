@@ -402,6 +402,7 @@ template <bool REV, bool ATOMIC>
 __global__ void __launch_bounds__(NT2, 2) k_walk(const __grid_constant__ CUtensorMap tmQ,
                                               const __grid_constant__ CUtensorMap tmK,
                                               const __grid_constant__ CUtensorMap tmV,
+                                              const __grid_constant__ CUtensorMap tmO,
                                               const float *__restrict__ la,
                                               const float *__restrict__ Hseg, int hseg_t,
                                               OutArgs oa, PassGeo p) {
@@ -721,16 +722,25 @@ __global__ void __launch_bounds__(NT2, 2) k_walk(const __grid_constant__ CUtenso
     }
     ok = mbar_wait(&bar_o, ci & 1) && ok;
     tc_fence_after();
-    // q' and v' tiles are free now (and k' too when the update ran): next loads
+    // q' and v' tiles are free now (and k' too when the update ran): next loads.
+    // A full chunk's output is staged in the v' tile and stored by TMA first,
+    // so its next v' tile is loaded after that store has read the buffer.
+    const bool staged = len == C;
     if (ok && ci + 1 < nc) {
       if (ldq) tma_q(cnext, ci + 1);
-      if (ldv) tma_v(cnext, ci + 1);
+      if (ldv && !staged) tma_v(cnext, ci + 1);
       if (ldk && lazy) tma_k(cnext, ci + 1);
     }
     {
       float o[32];
       tmem_ld32(tmem + lb + hf * 32, o);
-      if (L < dv) {
+      if (staged) {  // out'[t][L] into the v' tile, in the layout a load of tmO gives
+        if (L < p.dvp) {
+#pragma unroll
+          for (int tt = 0; tt < 32; ++tt)
+            *reinterpret_cast<float *>(Vb + sw128_off(hf * 32 + tt, L, C)) = o[tt];
+        }
+      } else if (L < dv) {
         const int64_t ld = (int64_t)oa.out_slots * dv;
         float *os = oa.out + ((b * p.L + t0) * oa.out_slots + oslot) * (int64_t)dv + L;
 #pragma unroll
@@ -741,6 +751,20 @@ __global__ void __launch_bounds__(NT2, 2) k_walk(const __grid_constant__ CUtenso
             else os[t * ld] = o[tt];
           }
         }
+      }
+    }
+    if (staged) {
+      fence_async_smem();
+      __syncthreads();
+      if (ldv) {  // store (or add, for a group's heads) the chunk's output rows
+        const int row = (int)(b * p.L + t0);
+        for (int cb = 0; cb < ncbv; ++cb) {
+          if (ATOMIC) tma_reduce_add_3d(&tmO, Vb + cb * 8192, cb * 32, oslot, row);
+          else tma_store_3d(&tmO, Vb + cb * 8192, cb * 32, oslot, row);
+        }
+        bulk_commit_group();
+        bulk_wait_read_all();
+        if (ok && ci + 1 < nc) tma_v(cnext, ci + 1);
       }
     }
     if (lazy) {
@@ -774,6 +798,7 @@ __global__ void __launch_bounds__(NT2, 2) k_walk(const __grid_constant__ CUtenso
   }
   __syncthreads();
   if ((ldq || ldv || ldk) && tma_pending >= 0) mbar_wait(&bar_tma, tma_pending & 1);
+  if (ldv) bulk_wait_all();  // the output stores have landed
   tc_fence_before();
   __syncthreads();
   if (warp == 0) tmem_dealloc(tmem, 256);
@@ -1166,19 +1191,20 @@ cudaError_t run_walk(const PassGeo &p, const float *qp, const float *kp, const f
   cudaError_t e;
   const int64_t rows = p.B * p.L;
   const int64_t G = p.H / p.hpg;
-  CUtensorMap mq, mk, mv;
+  CUtensorMap mq, mk, mv, mo;
   if ((e = make_map(&mq, qp, rows, p.qk_per_head ? p.H : G, p.dk)) != cudaSuccess) return e;
   if ((e = make_map(&mk, kp, rows, p.qk_per_head ? p.H : G, p.dk)) != cudaSuccess) return e;
   if ((e = make_map(&mv, vp, rows, p.v_per_head ? p.H : G, p.dv)) != cudaSuccess) return e;
+  if ((e = make_map(&mo, oa.out, rows, oa.out_slots, p.dv)) != cudaSuccess) return e;
   const dim3 grid((unsigned)p.nseg, (unsigned)p.H, (unsigned)p.B);
   const size_t sm = walk_smem(p);
   LaunchTrace lt(name_walk, s);
   if (atomic) {
     if ((e = set_smem(k_walk<REV, true>, sm)) != cudaSuccess) return e;
-    k_walk<REV, true><<<grid, NT2, sm, s>>>(mq, mk, mv, la, states, states_t ? 1 : 0, oa, p);
+    k_walk<REV, true><<<grid, NT2, sm, s>>>(mq, mk, mv, mo, la, states, states_t ? 1 : 0, oa, p);
   } else {
     if ((e = set_smem(k_walk<REV, false>, sm)) != cudaSuccess) return e;
-    k_walk<REV, false><<<grid, NT2, sm, s>>>(mq, mk, mv, la, states, states_t ? 1 : 0, oa, p);
+    k_walk<REV, false><<<grid, NT2, sm, s>>>(mq, mk, mv, mo, la, states, states_t ? 1 : 0, oa, p);
   }
   return cudaGetLastError();
 }
