@@ -569,6 +569,20 @@ __global__ void __launch_bounds__(NT2, 2) k_walk(const __grid_constant__ CUtenso
     const float *cs2 = cs2b + fb * C, *ew = ewb + fb * C, *ww = wwb + fb * C;
     ok = mbar_wait(&bar_tma, ci & 1) && ok;
     if (ok) tma_pending = -1;
+    // S = q' k'^T (M = 64, N = 64, K = dk), issued as soon as the tiles are
+    // in, before the CTA barrier: the issuing warp then starts its passes
+    // with the others instead of 16 MMA issues behind them.  (The previous
+    // chunk's output was read from these columns before its final barrier.)
+    if (tid == 0 && ok) {
+      tc_fence_after();
+      const uint32_t qa = smem_u32(Qb), ka = smem_u32(Kb);
+      const uint32_t id = idesc_tf32(64, 64);
+      for (int kk = 0; kk < dk / 8; ++kk) {
+        const uint32_t off = (kk >> 2) * 8192 + (kk & 3) * 32;
+        mma_ss(tmem, sdesc(qa + off), sdesc(ka + off), id, kk > 0 ? 1u : 0u);
+      }
+      mma_commit(&bar_s);
+    }
     tc_fence_before();
     if (__syncthreads_or(!ok)) break;
     tc_fence_after();
@@ -578,15 +592,6 @@ __global__ void __launch_bounds__(NT2, 2) k_walk(const __grid_constant__ CUtenso
     const float a_c = a_chunk[fb], an = alpha * a_c;
     const bool lazy = a_c >= 0x1p-30f && an >= 0x1p-40f && an <= 0x1p40f;
     const float kscale = lazy ? 1.f / an : 1.f;
-    if (tid == 0) {  // S = q' k'^T (M = 64, N = 64, K = dk)
-      const uint32_t qa = smem_u32(Qb), ka = smem_u32(Kb);
-      const uint32_t id = idesc_tf32(64, 64);
-      for (int kk = 0; kk < dk / 8; ++kk) {
-        const uint32_t off = (kk >> 2) * 8192 + (kk & 3) * 32;
-        mma_ss(tmem, sdesc(qa + off), sdesc(ka + off), id, kk > 0 ? 1u : 0u);
-      }
-      mma_commit(&bar_s);
-    }
     {  // v'^T into tensor memory: lane = feature, tokens [32 hf, 32 hf + 32)
       float v[32];
 #pragma unroll
