@@ -621,22 +621,30 @@ __global__ void __launch_bounds__(NT2, 2) k_walk(const __grid_constant__ CUtenso
     tmem_ld32(tmem + lb + hf * 32, sr);
     tc_fence_before();
     __syncthreads();  // every read of the v' and k' tiles and of S is done
-    if (lane < 16) {  // P into the v' tile's space: row r, tokens [32 hf, +32)
-      const int r = qd * 16 + lane;
+    {  // P into the v' tile's space.  S row r sits in lane r % 16 (M = 64); the
+       // lane 16 above it takes the upper 16 of the warp's 32 tokens
+      const int r = qd * 16 + (lane & 15), up = lane >> 4;
+      const int ub = hf * 32 + 16 * up;  // first token of this lane's 16
+      float s16[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const float hi = __shfl_sync(0xffffffffu, sr[16 + i], lane & 15);
+        s16[i] = up ? hi : sr[i];
+      }
       const float cr = cs2[r];
       uint8_t *P = Vb;
 #pragma unroll
-      for (int uu = 0; uu < 32; uu += 4) {
+      for (int uu = 0; uu < 16; uu += 4) {
         float f[4];
-        const float4 c4 = *reinterpret_cast<const float4 *>(cs2 + hf * 32 + uu);
+        const float4 c4 = *reinterpret_cast<const float4 *>(cs2 + ub + uu);
         const float cu[4] = {c4.x, c4.y, c4.z, c4.w};
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          const int u = hf * 32 + uu + e;
+          const int u = ub + uu + e;
           const bool valid = r < len && u < len && (REV ? u >= r : u <= r);
-          f[e] = valid ? tf32r(ex2f(REV ? cu[e] - cr : cr - cu[e]) * sr[uu + e]) : 0.f;
+          f[e] = valid ? tf32r(ex2f(REV ? cu[e] - cr : cr - cu[e]) * s16[uu + e]) : 0.f;
         }
-        *reinterpret_cast<float4 *>(P + sw128_off(r, hf * 32 + uu, C)) = make_float4(f[0], f[1], f[2], f[3]);
+        *reinterpret_cast<float4 *>(P + sw128_off(r, ub + uu, C)) = make_float4(f[0], f[1], f[2], f[3]);
       }
     }
     if (L < dkn) {  // w * k'^T into the k' tile's space (B operand, dkn rows)
