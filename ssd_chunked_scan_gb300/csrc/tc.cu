@@ -874,7 +874,11 @@ __global__ void __launch_bounds__(NTH) k_dla_intra(const __grid_constant__ CUten
   const uint32_t lb = (uint32_t)(warp * 32) << 16;
   bool ok = true;
   int pending = 1;  // loads in flight (thread 0's view)
-  float sq[C];
+  // Score rows live in lanes 0-15 of each warp (M = 64); the lane 16 above a
+  // row works on its upper 32 columns, so every lane holds 32 columns:
+  // u = 32 * up + i.
+  const int up = lane >> 4;
+  float sq[32];  // q k^T, this lane's half row
   // phase 0: q k^T; phase 1 + hh: dout v^T of head hh
   for (int ph = 0; ph <= hpg; ++ph) {
     const int ncb = ph == 0 ? ncbk : ncbv;
@@ -921,55 +925,62 @@ __global__ void __launch_bounds__(NTH) k_dla_intra(const __grid_constant__ CUten
       pending = 1;
     }
     if (ph == 0) {
-      float t32[32];
-      tmem_ld32(tmem + lb, t32);
+      float lo[32], hi[32];
+      tmem_ld32(tmem + lb, lo);
+      tmem_ld32(tmem + lb + 32, hi);
 #pragma unroll
-      for (int u = 0; u < 32; ++u) sq[u] = t32[u];
-      tmem_ld32(tmem + lb + 32, t32);
-#pragma unroll
-      for (int u = 0; u < 32; ++u) sq[32 + u] = t32[u];
+      for (int i = 0; i < 32; ++i) {
+        const float x = __shfl_sync(0xffffffffu, hi[i], lane & 15);
+        sq[i] = up ? x : lo[i];
+      }
       continue;
     }
-    float dp[C];
+    float dp[32];  // dout v^T of this head, this lane's half row
     {
-      float t32[32];
-      tmem_ld32(tmem + lb + 64, t32);
+      float lo[32], hi[32];
+      tmem_ld32(tmem + lb + 64, lo);
+      tmem_ld32(tmem + lb + 96, hi);
 #pragma unroll
-      for (int u = 0; u < 32; ++u) dp[u] = t32[u];
-      tmem_ld32(tmem + lb + 96, t32);
-#pragma unroll
-      for (int u = 0; u < 32; ++u) dp[32 + u] = t32[u];
+      for (int i = 0; i < 32; ++i) {
+        const float x = __shfl_sync(0xffffffffu, hi[i], lane & 15);
+        dp[i] = up ? x : lo[i];
+      }
     }
     // B_t = B_{t+1} + rowpre_t - colsuf_t with rowpre_t = sum_{u<t} M[t][u]
     // (a row of the strictly lower triangle) and colsuf_t = sum_{r>t} M[r][t]
-    // (a column of it).  Row r lives in lane r % 16 of warp r / 16; the column
-    // sums are reduce-scattered over the warp (lane l ends with columns 2l,
-    // 2l+1), then added over the four warps in shared memory.
+    // (a column of it).  Row r's two halves live in lanes r % 16 and
+    // r % 16 + 16 of warp r / 16; the column sums are reduce-scattered over
+    // each half-warp (lane l ends with columns 32 up + 2 (l % 16) + {0, 1}),
+    // then added over the four warps in shared memory.
     {
       const int r = warp * 16 + (lane & 15);
-      const bool rowok = lane < 16 && r < len;
+      const bool rowok = r < len;
       const float cr = cs[rowok ? r : 0];
-      float *m = dp;  // M's row, in place of dout v^T's
+      float *m = dp;  // M's half row, in place of dout v^T's
       float rp0 = 0.f, rp1 = 0.f;
 #pragma unroll
-      for (int u = 0; u < C; ++u) {
-        m[u] = (rowok && u < r) ? ex2f(cr - cs[u]) * sq[u] * dp[u] : 0.f;
-        if (u & 1) rp1 += m[u];
-        else rp0 += m[u];
+      for (int i = 0; i < 32; ++i) {
+        const int u = 32 * up + i;
+        m[i] = (rowok && u < r) ? ex2f(cr - cs[u]) * sq[i] * dp[i] : 0.f;
+        if (i & 1) rp1 += m[i];
+        else rp0 += m[i];
       }
+      float rp = rp0 + rp1;
+      rp += __shfl_xor_sync(0xffffffffu, rp, 16);  // both halves of the row
 #pragma unroll
-      for (int off = 16, n = C; off >= 1; off >>= 1, n >>= 1) {
-        const bool up = (lane & off) != 0;
+      for (int off = 8, n = 32; off >= 1; off >>= 1, n >>= 1) {
+        const bool hiL = (lane & off) != 0;
 #pragma unroll
         for (int k2 = 0; k2 < n / 2; ++k2) {
-          const float mine = up ? m[n / 2 + k2] : m[k2];
-          const float send = up ? m[k2] : m[n / 2 + k2];
+          const float mine = hiL ? m[n / 2 + k2] : m[k2];
+          const float send = hiL ? m[k2] : m[n / 2 + k2];
           m[k2] = mine + __shfl_xor_sync(0xffffffffu, send, off);
         }
       }
-      R[warp * C + 2 * lane] = m[0];
-      R[warp * C + 2 * lane + 1] = m[1];
-      if (rowok) R[4 * C + r] = rp0 + rp1;
+      const int u0 = 32 * up + 2 * (lane & 15);
+      R[warp * C + u0] = m[0];
+      R[warp * C + u0 + 1] = m[1];
+      if (rowok && up == 0) R[4 * C + r] = rp;
     }
     __syncthreads();
     if (warp == 0) {  // suffix sums of rowpre - colsuf; lane l owns t = 2l, 2l + 1
