@@ -61,11 +61,15 @@ def load_peaks():
 # g2h8_d128 L=8192 long-memory workload); a kernel without an entry reports
 # null.  Every change to a kernel must refresh or drop its entry.
 TRAFFIC = {
-    "tc.seg_state": 168923136 + 22324480,
-    "tc.seg_state_dq": 168907520 + 19192320,
-    "tc.seg_state_dk": 168946688 + 19278592,
-    "tc.dla_intra": 336926720 + 662016,
-    "tc.dla": 78654976 + 85248,
+    "tc.seg_state": 168930816 + 22046720,
+    "tc.seg_state_dq": 168900096 + 19518720,
+    "tc.seg_state_dk": 168965120 + 19146240,
+    "tc.walk_out": 249322496 + 95026688,
+    "tc.walk_dq": 420793344 + 27806208,
+    "tc.walk_dk": 420911104 + 27909632,
+    "tc.walk_dv": 248137984 + 94992128,
+    "tc.dla_intra": 336876288 + 664832,
+    "tc.dla": 78654720 + 26112,
 }
 # the same for the Mamba kernels at d1024 L8192 (profiles/mamba_d1024_L8192.md)
 MAMBA_TRAFFIC = {
