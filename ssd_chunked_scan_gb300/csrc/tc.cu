@@ -826,7 +826,7 @@ __global__ void __launch_bounds__(NT2, 2) k_walk(const __grid_constant__ CUtenso
 // computed once; dout v^T per head.  Both score MMAs have M = 64
 // (rows 16w..16w+15 in lanes 32w..) and share one two-tile shared-memory
 // buffer; the next head's tiles load while the current head's sums run.
-// grid (N chunks, G, B), 128 threads, two CTAs per SM.
+// grid (N chunks, G, B), 128 threads, three CTAs per SM.
 __global__ void __launch_bounds__(NTH) k_dla_intra(const __grid_constant__ CUtensorMap tmQ,
                                                    const __grid_constant__ CUtensorMap tmK,
                                                    const __grid_constant__ CUtensorMap tmV,
@@ -839,7 +839,7 @@ __global__ void __launch_bounds__(NTH) k_dla_intra(const __grid_constant__ CUten
   const int ncbk = p.dkp / 32, ncbv = p.dvp / 32, ncbm = ncbk > ncbv ? ncbk : ncbv;
   uint8_t *T1 = smem, *T2 = smem + ncbm * 8192;
   float *R = (float *)(T2 + ncbm * 8192);  // [4][64] column partials, [64] row sums
-  float *cs = R + C * (C + 1);            // [64]
+  float *cs = R + 5 * C;                  // [64]
   __shared__ uint64_t bar_tma, bar_mma;
   __shared__ uint32_t tmem_base;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -1171,7 +1171,7 @@ size_t walk_smem(const PassGeo &p) {
 
 size_t dla_intra_smem(const PassGeo &p) {
   const int ncbm = std::max(p.dkp, p.dvp) / 32;
-  return (size_t)ncbm * 2 * 8192 + (size_t)(C * (C + 1) + C) * 4 + 1024;
+  return (size_t)ncbm * 2 * 8192 + (size_t)(6 * C) * 4 + 1024;  // three CTAs per SM fit
 }
 
 template <typename K>
