@@ -420,7 +420,7 @@ MUFU_GEXP = 152 * 16 * 2.070
 def mamba_nseg(w, sms=152):
     """Segments per sequence chosen by the Mamba kernels (same rule as mamba.cu)."""
     base = w.B * w.D
-    want = -(-1024 * sms // base)
+    want = max(1, (640 * sms) // base)
     ls = -(-w.L // want)
     ls = min(max(-(-ls // 32) * 32, 32), 1024)
     return -(-w.L // ls)
