@@ -147,6 +147,43 @@ def tc_nseg(w, sms=152):
     return -(-w.L // Ls)
 
 
+def kernel_roofline(trace, costs, peaks, traffic_ok):
+    """Roofline entry of the kernel with the most device time in `trace`
+    ({name: (launches, total ms)}): algorithmic bytes (or flops) per launch
+    over its mean launch time, against the measured peak."""
+    top_name, (top_n, top_ms) = max(trace.items(), key=lambda kv: kv[1][1])
+    per_launch_ms = top_ms / top_n
+    if top_name not in costs:
+        raise KeyError(f"no algorithmic cost entry for kernel {top_name}")
+    kb, kf, kbound = costs[top_name]
+    if kbound == "tensor":
+        peak = peaks["bf16_tflops"] * TF32_OVER_BF16
+        ach = kf / (per_launch_ms / 1e3) / 1e12
+        roof = {"bound": "tensor", "achieved": ach, "peak": peak, "unit": "TFLOP/s",
+                "peak_note": f"tf32 = {peaks['source']} bf16 burst x nominal tf32/bf16 ratio"}
+    elif kbound == "alu":
+        ach = kf / (per_launch_ms / 1e3) / 1e12
+        roof = {"bound": "alu", "achieved": ach, "peak": FP32_TFLOPS, "unit": "TFLOP/s",
+                "peak_note": "fp32 FFMA: 152 SMs x 128 lanes x 2 flop x 2070 MHz"}
+    else:
+        ach = kb / (per_launch_ms / 1e3) / 1e9
+        roof = {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "peak_note": f"{peaks['source']} copy bandwidth"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["traffic"] = TRAFFIC.get(top_name) if traffic_ok else None
+    roof["kernel"] = top_name
+    roof["kernel_ms_per_launch"] = per_launch_ms
+    roof["alg_bytes_per_launch"] = kb
+    roof["alg_flops_per_launch"] = kf
+    return roof
+
+
+def kernel_table(trace):
+    tot = sum(x[1] for x in trace.values())
+    return {n: {"launches": c, "ms_total": t, "share": t / tot}
+            for n, (c, t) in sorted(trace.items(), key=lambda kv: -kv[1][1])}
+
+
 def step_totals(w):
     """Minimal bytes and flops of one fwd + bwd step (two calls)."""
     B, L, G, H, dk, dv, C = w.B, w.L, w.G, w.H, w.dk, w.dv, w.chunk
@@ -725,6 +762,21 @@ def main():
     ssd.ssd_trace_enable(False)
     trace = ssd.ssd_trace_collect()
     ssd.ssd_trace_reset()
+    # and once more with the backward's passes serialised, so that each
+    # kernel's time is its own (the ncu launch list is serialised too)
+    overlap_on = (ssd.ssd_get_overlap() and args.path == "tc" and args.mode == "fwd_bwd"
+                  and w.chunk != 1)
+    trace_iso = None
+    if overlap_on:
+        prev = ssd.ssd_set_overlap(False)
+        ssd.ssd_trace_enable(True)
+        for _ in range(args.steps):
+            step()
+        torch.cuda.synchronize(dev)
+        ssd.ssd_trace_enable(False)
+        ssd.ssd_set_overlap(prev)
+        trace_iso = ssd.ssd_trace_collect()
+        ssd.ssd_trace_reset()
     clocks.stop()
     clk = clocks.summary(th0, th1)
 
@@ -796,31 +848,14 @@ def main():
 
     peaks = load_peaks()
     costs = kernel_costs(w, torch.cuda.get_device_properties(dev).multi_processor_count)
-    top = max(trace.items(), key=lambda kv: kv[1][1])
-    top_name, (top_n, top_ms) = top
-    per_launch_ms = top_ms / top_n
-    if top_name not in costs:
-        raise KeyError(f"no algorithmic cost entry for kernel {top_name}")
-    kb, kf, kbound = costs[top_name]
-    if kbound == "tensor":
-        peak = peaks["bf16_tflops"] * TF32_OVER_BF16
-        ach = kf / (per_launch_ms / 1e3) / 1e12
-        roof = {"bound": "tensor", "achieved": ach, "peak": peak, "unit": "TFLOP/s",
-                "peak_note": f"tf32 = {peaks['source']} bf16 burst x nominal tf32/bf16 ratio"}
-    elif kbound == "alu":
-        ach = kf / (per_launch_ms / 1e3) / 1e12
-        roof = {"bound": "alu", "achieved": ach, "peak": FP32_TFLOPS, "unit": "TFLOP/s",
-                "peak_note": "fp32 FFMA: 152 SMs x 128 lanes x 2 flop x 2070 MHz"}
-    else:
-        ach = kb / (per_launch_ms / 1e3) / 1e9
-        roof = {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                "peak_note": f"{peaks['source']} copy bandwidth"}
-    roof["frac"] = roof["achieved"] / roof["peak"]
-    roof["traffic"] = TRAFFIC.get(top_name) if w.name == WORKLOAD else None
-    roof["kernel"] = top_name
-    roof["kernel_ms_per_launch"] = per_launch_ms
-    roof["alg_bytes_per_launch"] = kb
-    roof["alg_flops_per_launch"] = kf
+    roof = kernel_roofline(trace, costs, peaks, w.name == WORKLOAD)
+    roof["timing"] = ("live, in the timed configuration" + (
+        ": the backward runs its dk / dv passes on a second stream beside the dq pass, so a "
+        "kernel's time includes the periods it shares the GPU with the other pass's kernels"
+        if overlap_on else ""))
+    roof_iso = kernel_roofline(trace_iso, costs, peaks, w.name == WORKLOAD) if trace_iso else None
+    if roof_iso is not None:
+        roof_iso["timing"] = "the same steps with the backward's passes serialised (one kernel at a time)"
 
     bytes_fb, fl_fb, bytes_f, fl_f = step_totals(w)
     t_hbm = bytes_fb / (peaks["hbm_gbs"] * 1e9)
@@ -845,8 +880,9 @@ def main():
         "fwd": {"ms": fwd_ms, "tokens_per_s": w.tokens / (fwd_ms / 1e3),
                 "frac_of_roofline": max(bytes_f / (peaks["hbm_gbs"] * 1e9),
                                         fl_f / (peaks["bf16_tflops"] * TF32_OVER_BF16 * 1e12)) / (fwd_ms / 1e3)},
-        "kernels": {n: {"launches": c, "ms_total": t, "share": t / sum(x[1] for x in trace.values())}
-                    for n, (c, t) in sorted(trace.items(), key=lambda kv: -kv[1][1])},
+        "kernels": kernel_table(trace),
+        "roofline_isolated": roof_iso,
+        "kernels_isolated": kernel_table(trace_iso) if trace_iso else None,
         "gpu_launches": launches,
         "clocks": clk,
         "e2e": e2e,

@@ -221,6 +221,19 @@ SSD_API int ssd_pool_high_water(int reset, size_t *bytes);
 SSD_API int ssd_set_path(int path);
 SSD_API int ssd_get_path(void);
 
+/* Overlap of the tensor-core backward's independent passes (process-wide,
+ * all threads; on by default).  When on, ssd_bwd / ssd_bwd_ex run the dk and
+ * dv passes on a stream of the library's own (one per device, created at the
+ * first backward), forked from and joined back into the caller's stream
+ * inside the call, so the call stays ordered on `stream` like any other; the
+ * causal dq pass and the intra-chunk dlog_alpha sums run on `stream`
+ * meanwhile.  Off runs every kernel on `stream` in turn (the same results up
+ * to the order of the float atomic adds that sum a group's heads; for
+ * profiling one kernel at a time).  The SIMT and sequential paths are not
+ * affected.  ssd_set_overlap returns the previous setting. */
+SSD_API int ssd_set_overlap(int on);
+SSD_API int ssd_get_overlap(void);
+
 /* Static description of a status code; never NULL. */
 SSD_API const char *ssd_strerror(int status);
 

@@ -9,6 +9,7 @@ generators work on machines without the built library.
 
 def __getattr__(name):
     if name in ("ssd_fwd", "ssd_bwd", "ssd_fwd_ex", "ssd_bwd_ex", "ssd_set_path", "ssd_get_path", "ssd_strerror",
+                "ssd_set_overlap", "ssd_get_overlap",
                 "ssd_last_device_error", "SSDError", "SSD_PATH_TC", "SSD_PATH_SIMT"):
         from . import ssd
         return getattr(ssd, name)

@@ -146,6 +146,10 @@ int ssd_set_path(int path) {
 
 int ssd_get_path(void) { return current_path(); }
 
+int ssd_set_overlap(int on) { return ssd::tc::set_overlap(on != 0) ? 1 : 0; }
+
+int ssd_get_overlap(void) { return ssd::tc::get_overlap() ? 1 : 0; }
+
 int ssd_fwd_ex(const float *q, const float *k, const float *v, const float *log_alpha,
                const float *h0, float *out, float *hT, int64_t B, int64_t L, int64_t G, int64_t H,
                int64_t dk, int64_t dv, int64_t chunk, ssd_stream_t stream) {

@@ -31,6 +31,7 @@
 // 128-byte-swizzled layout (w * k'^T, P).  Operands written by threads are
 // rounded to TF32 to nearest; TMA-fed ones are truncated by the tensor core.
 #include <algorithm>
+#include <atomic>
 #include <cstring>
 #include <mutex>
 
@@ -1236,7 +1237,39 @@ cudaError_t run_walk(const PassGeo &p, const float *qp, const float *kp, const f
   return cudaGetLastError();
 }
 
+// A second stream of the library's own per device, on which the backward runs
+// its anti-causal passes (dk, dv) while the caller's stream runs the causal one
+// (dq) and the intra-chunk dlog_alpha sums: each kernel fills one wave, and the
+// other pass's kernels take the SM slots its tail leaves and overlap its short
+// scans.  Fork and join are events; the lock makes the enqueue of one backward
+// atomic with respect to others on other host threads (the events are reused).
+struct Side {
+  cudaStream_t s2 = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+};
+std::mutex g_side_mu;
+Side g_side[64];
+std::atomic<bool> g_overlap{true};
+
+cudaError_t get_side(Side **out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  Side &sd = g_side[dev];
+  if (!sd.s2) {
+    if ((e = cudaStreamCreateWithFlags(&sd.s2, cudaStreamNonBlocking)) != cudaSuccess) return e;
+    if ((e = cudaEventCreateWithFlags(&sd.fork, cudaEventDisableTiming)) != cudaSuccess) return e;
+    if ((e = cudaEventCreateWithFlags(&sd.join, cudaEventDisableTiming)) != cudaSuccess) return e;
+  }
+  *out = &sd;
+  return cudaSuccess;
+}
+
 }  // namespace
+
+bool set_overlap(bool on) { return g_overlap.exchange(on); }
+bool get_overlap() { return g_overlap.load(); }
 
 int check_shape(int64_t dk, int64_t dv, int64_t chunk) {
   if (chunk != C) return SSD_ERR_CHUNK;
@@ -1308,33 +1341,68 @@ cudaError_t bwd(const float *q, const float *k, const float *v, const float *la,
     if ((e = cudaMemsetAsync(dk, 0, sizeof(float) * g.B * g.L * g.G * g.dk, s)) != cudaSuccess) return e;
   }
   const int oslots = grouped ? (int)g.G : (int)g.H;
-  if ((e = run_states<false>(pa, v, k, la, h0, true, hT, stA, aA, nullptr, s, "tc.seg_state_dq")) != cudaSuccess)
-    return e;
-  OutArgs oq{dq, oslots, q, rq};
-  if ((e = run_walk<false>(pa, dout, v, k, la, stA, false, oq, grouped, s, "tc.walk_dq")) != cudaSuccess)
-    return e;
-  if ((e = run_states<true>(pb, dout, q, la, dhT, true, dh0, stB, aB, nullptr, s, "tc.seg_state_dk")) != cudaSuccess)
-    return e;
+  // The dk / dv passes (pass B's states, both anti-causal walks) run on the
+  // side stream, forked from s after the memsets and joined before k_dla
+  // (or on s itself when overlap is off).
+  const bool overlap = g_overlap.load();
+  std::unique_lock<std::mutex> lock(g_side_mu, std::defer_lock);
+  Side *sd = nullptr;
+  if (overlap) {
+    lock.lock();
+    if ((e = get_side(&sd)) != cudaSuccess) return e;
+    if ((e = cudaEventRecord(sd->fork, s)) == cudaErrorInvalidResourceHandle ||
+        e == cudaErrorContextIsDestroyed) {
+      // the cached handles died with a device reset: make new ones once
+      cudaGetLastError();
+      *sd = Side{};
+      if ((e = get_side(&sd)) != cudaSuccess) return e;
+      e = cudaEventRecord(sd->fork, s);
+    }
+    if (e != cudaSuccess) return e;
+    if ((e = cudaStreamWaitEvent(sd->s2, sd->fork, 0)) != cudaSuccess) return e;
+  }
+  cudaStream_t s2 = overlap ? sd->s2 : s;
+  cudaError_t eb = run_states<true>(pb, dout, q, la, dhT, true, dh0, stB, aB, nullptr, s2, "tc.seg_state_dk");
   OutArgs okk{dk, oslots, k, rk};
-  if ((e = run_walk<true>(pb, v, dout, q, la, stB, false, okk, grouped, s, "tc.walk_dk")) != cudaSuccess)
-    return e;
+  if (eb == cudaSuccess) eb = run_walk<true>(pb, v, dout, q, la, stB, false, okk, grouped, s2, "tc.walk_dk");
   OutArgs ov{dv, (int)g.H, nullptr, nullptr};
-  if ((e = run_walk<true>(pc, k, q, dout, la, stB, true, ov, false, s, "tc.walk_dv")) != cudaSuccess)
-    return e;
-  {  // intra-chunk block sums of dlog_alpha
+  if (eb == cudaSuccess) eb = run_walk<true>(pc, k, q, dout, la, stB, true, ov, false, s2, "tc.walk_dv");
+  // whatever was enqueued on s2 is joined back into s before this returns,
+  // even after an error (the caller frees the workspace on s)
+  cudaError_t ej = overlap ? cudaEventRecord(sd->join, s2) : cudaSuccess;
+  auto join = [&]() -> cudaError_t {
+    if (!overlap || ej != cudaSuccess) return ej;
+    return cudaStreamWaitEvent(s, sd->join, 0);
+  };
+  if (eb != cudaSuccess) {
+    join();
+    return eb;
+  }
+  // pass A and the intra-chunk sums on s, meanwhile
+  auto on_s = [&]() -> cudaError_t {
+    cudaError_t ea = run_states<false>(pa, v, k, la, h0, true, hT, stA, aA, nullptr, s, "tc.seg_state_dq");
+    if (ea != cudaSuccess) return ea;
+    OutArgs oq{dq, oslots, q, rq};
+    if ((ea = run_walk<false>(pa, dout, v, k, la, stA, false, oq, grouped, s, "tc.walk_dq")) != cudaSuccess)
+      return ea;
+    // intra-chunk block sums of dlog_alpha
     const PassGeo pi = make_pass(g, DK, DV, false, true);
     CUtensorMap mq, mk, mv, md;
     const int64_t rows = g.B * g.L;
-    if ((e = make_map(&mq, q, rows, g.G, DK)) != cudaSuccess) return e;
-    if ((e = make_map(&mk, k, rows, g.G, DK)) != cudaSuccess) return e;
-    if ((e = make_map(&mv, v, rows, g.H, DV)) != cudaSuccess) return e;
-    if ((e = make_map(&md, dout, rows, g.H, DV)) != cudaSuccess) return e;
+    if ((ea = make_map(&mq, q, rows, g.G, DK)) != cudaSuccess) return ea;
+    if ((ea = make_map(&mk, k, rows, g.G, DK)) != cudaSuccess) return ea;
+    if ((ea = make_map(&mv, v, rows, g.H, DV)) != cudaSuccess) return ea;
+    if ((ea = make_map(&md, dout, rows, g.H, DV)) != cudaSuccess) return ea;
     const size_t sm = dla_intra_smem(pi);
-    if ((e = set_smem(k_dla_intra, sm)) != cudaSuccess) return e;
+    if ((ea = set_smem(k_dla_intra, sm)) != cudaSuccess) return ea;
     LaunchTrace lt("tc.dla_intra", s);
     k_dla_intra<<<dim3((unsigned)g.N, (unsigned)g.G, (unsigned)g.B), NTH, sm, s>>>(mq, mk, mv, md,
                                                                                   la, Bt, pi);
-  }
+    return cudaGetLastError();
+  };
+  const cudaError_t ea = on_s();
+  if ((e = join()) != cudaSuccess) return e;
+  if (ea != cudaSuccess) return ea;
   {  // pass A's states are S^T, pass B's are G^T: the carry is their plain dot
     LaunchTrace lt("tc.dla", s);
     k_dla<<<dim3((unsigned)pa.nseg, (unsigned)g.H, (unsigned)g.B), DT, 0, s>>>(

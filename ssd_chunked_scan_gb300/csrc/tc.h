@@ -18,6 +18,11 @@ cudaError_t bwd(const float *q, const float *k, const float *v, const float *la,
                 const float *dout, const float *dhT, float *dq, float *dk, float *dv, float *dla,
                 float *dh0, const Geo &g, void *ws, cudaStream_t s);
 
+// Whether bwd runs its dk / dv passes on a side stream (see ssd_set_overlap);
+// set_overlap returns the previous setting.
+bool set_overlap(bool on);
+bool get_overlap();
+
 // Reads and clears the device error word of the current device (set by a
 // bounded wait that gave up).
 cudaError_t read_and_clear_error(unsigned int *word);

@@ -26,7 +26,8 @@ SSD_ERR_SCRATCH = 9
 SSD_PATH_TC = 0
 SSD_PATH_SIMT = 1
 
-EXPORTED = ("ssd_fwd", "ssd_bwd", "ssd_set_path", "ssd_get_path", "ssd_strerror",
+EXPORTED = ("ssd_fwd", "ssd_bwd", "ssd_set_path", "ssd_get_path", "ssd_set_overlap",
+            "ssd_get_overlap", "ssd_strerror",
             "ssd_last_device_error", "ssd_version", "ssd_launch_count", "ssd_trace_enable",
             "ssd_trace_collect", "ssd_trace_get", "ssd_trace_reset", "ssd_fwd_noalloc",
             "ssd_fwd_noalloc_scratch_bytes")
@@ -55,6 +56,10 @@ def _load():
     lib.ssd_set_path.restype = ctypes.c_int
     lib.ssd_get_path.argtypes = []
     lib.ssd_get_path.restype = ctypes.c_int
+    lib.ssd_set_overlap.argtypes = [ctypes.c_int]
+    lib.ssd_set_overlap.restype = ctypes.c_int
+    lib.ssd_get_overlap.argtypes = []
+    lib.ssd_get_overlap.restype = ctypes.c_int
     lib.ssd_strerror.argtypes = [ctypes.c_int]
     lib.ssd_strerror.restype = ctypes.c_char_p
     lib.ssd_last_device_error.argtypes = [p]
@@ -102,6 +107,17 @@ def ssd_set_path(path: int) -> None:
 
 def ssd_get_path() -> int:
     return int(LIB.ssd_get_path())
+
+
+def ssd_set_overlap(on: bool) -> bool:
+    """Run the tensor-core backward's dk / dv passes on the library's side
+    stream (True, the default) or every kernel on the caller's stream in turn;
+    returns the previous setting."""
+    return bool(LIB.ssd_set_overlap(1 if on else 0))
+
+
+def ssd_get_overlap() -> bool:
+    return bool(LIB.ssd_get_overlap())
 
 
 def ssd_last_device_error(stream=None) -> int:

@@ -105,6 +105,16 @@ def test_set_path(lib):
     assert lib.ssd_set_path(0) == 0 and lib.ssd_get_path() == 0
 
 
+def test_set_overlap(lib):
+    first = lib.ssd_set_overlap(0)
+    try:
+        assert first == 1  # on by default
+        assert lib.ssd_get_overlap() == 0
+        assert lib.ssd_set_overlap(5) == 0 and lib.ssd_get_overlap() == 1
+    finally:
+        lib.ssd_set_overlap(first)
+
+
 def test_injected_workspace_failure_is_reported_before_launch(lib, monkeypatch):
     # SSD_FAULT_ALLOC=1 makes the workspace request fail on the host; the
     # call must return SSD_ERR_ALLOC without enqueueing anything
