@@ -59,14 +59,12 @@ __device__ __forceinline__ float ex2f(float x) {
   return y;
 }
 
-// Inclusive prefix sums of la over n <= 64 tokens starting at `first` (fp64
-// accumulation by warp 0, rounded once to fp32), plus `carry` added before
-// rounding.  Returns (in warp 0) the sum of the n values.
-__device__ inline double warp_cumsum64(const float *__restrict__ la, int64_t first,
-                                       int64_t stride, int n, double carry, float *cs) {
+// Inclusive prefix sums over n <= 64 tokens of la, given as the two values
+// each lane holds (lane l: tokens 2l and 2l + 1, zero past n), accumulated in
+// fp64 by one warp and rounded once to fp32 into cs, plus `carry` added before
+// rounding.  Returns the sum of the n values.
+__device__ inline double warp_cumsum64_regs(double x0, double x1, int n, double carry, float *cs) {
   const int l = threadIdx.x & 31;
-  double x0 = (2 * l < n) ? (double)la[first + (int64_t)(2 * l) * stride] : 0.0;
-  double x1 = (2 * l + 1 < n) ? (double)la[first + (int64_t)(2 * l + 1) * stride] : 0.0;
   double pair = x0 + x1, incl = pair;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -79,6 +77,15 @@ __device__ inline double warp_cumsum64(const float *__restrict__ la, int64_t fir
     if (2 * l + 1 < n) cs[2 * l + 1] = (float)(carry + incl);
   }
   return __shfl_sync(0xffffffffu, incl, 31);
+}
+
+// The same, loading la[first + t * stride] for t < n itself.
+__device__ inline double warp_cumsum64(const float *__restrict__ la, int64_t first,
+                                       int64_t stride, int n, double carry, float *cs) {
+  const int l = threadIdx.x & 31;
+  const double x0 = (2 * l < n) ? (double)la[first + (int64_t)(2 * l) * stride] : 0.0;
+  const double x1 = (2 * l + 1 < n) ? (double)la[first + (int64_t)(2 * l + 1) * stride] : 0.0;
+  return warp_cumsum64_regs(x0, x1, n, carry, cs);
 }
 
 // ===========================================================================
@@ -206,10 +213,14 @@ __global__ void __launch_bounds__(NT2, 2) k_seg_state(const __grid_constant__ CU
   double carry = 0.0;
   bool ok = true;
   // all threads: weights of the 256 tokens from slice n on (one per thread),
-  // continuing the running in-segment prefix (fp64 block scan)
+  // continuing the running in-segment prefix (fp64 block scan); each thread's
+  // la value of the next batch is loaded one batch ahead
+  auto la_at = [&](int64_t t) { return t < s_end ? (double)la[(b * p.L + t) * p.H + h] : 0.0; };
+  double la_next = la_at(s_begin + tid);
   auto batch_weights = [&](int n) {
     const int64_t t = s_begin + (int64_t)n * SL + tid;
-    double x = t < s_end ? (double)la[(b * p.L + t) * p.H + h] : 0.0;
+    double x = la_next;
+    la_next = la_at(t + 8 * SL);
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const double y = __shfl_up_sync(0xffffffffu, x, o);
@@ -488,11 +499,20 @@ __global__ void __launch_bounds__(NT2, 2) k_walk(const __grid_constant__ CUtenso
 
   if (!hseg_t) issue_first_loads();
 
-  // warp 4: the factors of chunk c into buffer bf
+  // warp 4: the factors of chunk c into buffer bf, from la values loaded one
+  // chunk ahead (la_x0, la_x1: this lane's two tokens of chunk c)
+  double la_x0 = 0.0, la_x1 = 0.0;
+  auto la_prefetch = [&](int c) {
+    const int64_t t0 = s_begin + (int64_t)c * C;
+    const int len = (int)imin64(C, s_end - t0);
+    const float *lp = la + (b * p.L + t0) * p.H + h;
+    la_x0 = (2 * lane < len) ? (double)lp[(int64_t)(2 * lane) * p.H] : 0.0;
+    la_x1 = (2 * lane + 1 < len) ? (double)lp[(int64_t)(2 * lane + 1) * p.H] : 0.0;
+  };
   auto chunk_factors = [&](int c, int bf) {
     const int64_t t0 = s_begin + (int64_t)c * C;
     const int len = (int)imin64(C, s_end - t0);
-    const double tot = warp_cumsum64(la, (b * p.L + t0) * p.H + h, p.H, len, 0.0, scr);
+    const double tot = warp_cumsum64_regs(la_x0, la_x1, len, 0.0, scr);
     __syncwarp();
     const float tot2 = (float)tot * LOG2E;
     for (int t = lane; t < C; t += 32) {
@@ -504,7 +524,10 @@ __global__ void __launch_bounds__(NT2, 2) k_walk(const __grid_constant__ CUtenso
     if (lane == 0) a_chunk[bf] = ex2f(tot2);
     __syncwarp();
   };
-  if (warp == 4) chunk_factors(REV ? nc - 1 : 0, 0);
+  if (warp == 4) {
+    la_prefetch(REV ? nc - 1 : 0);
+    chunk_factors(REV ? nc - 1 : 0, 0);
+  }
 
   {  // running state, transposed: lane j, column i = state[i][j]
     const float *H0 = Hseg + (bh * p.nseg + seg) * (int64_t)dk * dv;
@@ -568,6 +591,7 @@ __global__ void __launch_bounds__(NT2, 2) k_walk(const __grid_constant__ CUtenso
     const int cnext = REV ? c - 1 : c + 1;
     const int fb = ci & 1;
     const float *cs2 = cs2b + fb * C, *ew = ewb + fb * C, *ww = wwb + fb * C;
+    if (warp == 4 && ci + 1 < nc) la_prefetch(cnext);  // used by chunk_factors below
     ok = mbar_wait(&bar_tma, ci & 1) && ok;
     if (ok) tma_pending = -1;
     // S = q' k'^T (M = 64, N = 64, K = dk), issued as soon as the tiles are
