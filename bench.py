@@ -61,23 +61,25 @@ def load_peaks():
 # g2h8_d128 L=8192 long-memory workload); a kernel without an entry reports
 # null.  Every change to a kernel must refresh or drop its entry.
 TRAFFIC = {
-    "tc.seg_state": 168930816 + 22046720,
-    "tc.seg_state_dq": 168900096 + 19518720,
-    "tc.seg_state_dk": 168965120 + 19146240,
-    "tc.walk_out": 249322496 + 95026688,
-    "tc.walk_dq": 420793344 + 27806208,
-    "tc.walk_dk": 420911104 + 27909632,
-    "tc.walk_dv": 248137984 + 94992128,
-    "tc.dla_intra": 336876288 + 664832,
-    "tc.dla": 78654720 + 26112,
+    "tc.seg_state": 169083648 + 4021248,
+    "tc.seg_state_dq": 169071616 + 1070848,
+    "tc.seg_state_dk": 169008128 + 995328,
+    "tc.seg_scan": (21019136 + 18931712 + 21022464) // 3,  # mean of the three passes' scans
+    "tc.walk_out": 221381632 + 93543424,
+    "tc.walk_dq": 389164288 + 24201216,
+    "tc.walk_dk": 389141504 + 24491008,
+    "tc.walk_dv": 221358592 + 94183936,
+    "tc.dla_intra": 336926464 + 483072,
+    "tc.dla": 36711936,
 }
-# the same for the Mamba kernels at d1024 L8192 (profiles/mamba_d1024_L8192.md)
+# the same for the Mamba kernels at d1024 L8192 (profiles/mamba_d1024_L8192.md);
+# seg_state and seg_scan run more than once per step: the mean of their launches
 MAMBA_TRAFFIC = {
-    "mamba.seg_state": 270665216 + 4625920,
-    "mamba.seg_scan": 10388736,
-    "mamba.out": 282570240 + 100506880,
-    "mamba.seg_grad_state": 270926080 + 769024,
-    "mamba.bwd": 430734592 + 242471936,
+    "mamba.seg_state": (270620672 + 3479808 + 270631680 + 651776) // 2,
+    "mamba.seg_scan": (6209792 + 6209024 + 6208768) // 3,
+    "mamba.out": 278497280 + 98762240,
+    "mamba.seg_grad_state": 270618624 + 310016,
+    "mamba.bwd": 426092288 + 241760768,
 }
 
 # nominal dense tensor rates: tf32 1.1 PF vs bf16 2.25 PF per GPU
