@@ -281,21 +281,37 @@ def oracle_sample(w, threads):
 
 def cpu_oracle_sample(w, min_seconds=10.0, max_reps=60):
     """Time the float64 oracle (fwd + bwd) on a sample of the workload,
-    repeated until min_seconds have passed; returns tokens/s and details."""
+    repeated until min_seconds have passed; returns tokens/s and details,
+    with the fwd and fwd+bwd time of one rep and a single-thread figure (the
+    oracle on one (batch, head) sequence, which one thread runs)."""
+    import numpy as np
     from oracle import oracle_threads, ssd_bwd_ref, ssd_fwd_ref
     (q, k, v, la, h0, dout), nb, used = oracle_sample(w, oracle_threads())
-    toks, t0, reps = 0, time.perf_counter(), 0
+    toks, t0, reps, t_fwd = 0, time.perf_counter(), 0, 0.0
     while True:
+        ta = time.perf_counter()
         ssd_fwd_ref(q, k, v, la, h0)
+        t_fwd += time.perf_counter() - ta
         ssd_bwd_ref(q, k, v, la, h0, dout)
         reps += 1
         toks += nb * w.L * w.H
         el = time.perf_counter() - t0
         if el >= min_seconds or reps >= max_reps:
             break
+    one = (q[:1, :, :1], k[:1, :, :1], v[:1, :, :1], la[:1, :, :1], h0[:1, :1], dout[:1, :, :1])
+    one = tuple(np.ascontiguousarray(x) for x in one)
+    ta = time.perf_counter()
+    ssd_fwd_ref(*one[:5])
+    tb = time.perf_counter()
+    ssd_bwd_ref(*one)
+    tc_ = time.perf_counter()
     return {"value": toks / el, "unit": "tokens/s", "cores": used, "kind": "oracle",
             "sample": f"batch entries 0..{nb - 1} of {w.name} ({nb} x {w.L} x {w.H} heads, "
-                      f"all groups), float64 fwd+bwd, {reps} rep(s), {el:.1f} s"}
+                      f"all groups), float64 fwd+bwd, {reps} rep(s), {el:.1f} s",
+            "fwd_ms_per_rep": t_fwd / reps * 1e3, "fwd_bwd_ms_per_rep": el / reps * 1e3,
+            "single_thread": {"sample": f"one (batch, head) sequence of {w.name}, {w.L} tokens",
+                              "fwd_ms": (tb - ta) * 1e3, "fwd_bwd_ms": (tc_ - ta) * 1e3,
+                              "tokens_per_s": w.L / (tc_ - ta)}}
 
 
 def max_over_ranks(x, device=None):
@@ -742,16 +758,30 @@ def main():
     torch.cuda.synchronize(dev)
     n0 = ssd.ssd_launch_count()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    # events at the ends of up to five equal runs of steps inside the region:
+    # the per-run ms per step give the median and quartiles
+    nrep = min(5, args.steps)
+    ends = {round(args.steps * (j + 1) / nrep) - 1: torch.cuda.Event(enable_timing=True)
+            for j in range(nrep)}
     th0 = time.time()
     e0.record(stream)
-    for _ in range(args.steps):
+    for i in range(args.steps):
         step()
+        if i in ends:
+            ends[i].record(stream)
     e1.record(stream)
     torch.cuda.synchronize(dev)
     th1 = time.time()
     barrier()
     launches = ssd.ssd_launch_count() - n0
     ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, dev)
+    runs, prev_ev, prev_i = [], e0, -1
+    for i in sorted(ends):
+        runs.append(prev_ev.elapsed_time(ends[i]) / (i - prev_i))
+        prev_ev, prev_i = ends[i], i
+    qs = statistics.quantiles(runs, n=4, method="inclusive") if len(runs) > 1 else runs * 3
+    repeats = {"runs": len(runs), "ms_per_step_median": statistics.median(runs),
+               "ms_per_step_q1": qs[0], "ms_per_step_q3": qs[2]}
     if ssd.ssd_last_device_error() != 0:
         raise RuntimeError("device error word set during the timed region")
 
@@ -882,6 +912,7 @@ def main():
         "fwd": {"ms": fwd_ms, "tokens_per_s": w.tokens / (fwd_ms / 1e3),
                 "frac_of_roofline": max(bytes_f / (peaks["hbm_gbs"] * 1e9),
                                         fl_f / (peaks["bf16_tflops"] * TF32_OVER_BF16 * 1e12)) / (fwd_ms / 1e3)},
+        "repeats": repeats,
         "kernels": kernel_table(trace),
         "roofline_isolated": roof_iso,
         "kernels_isolated": kernel_table(trace_iso) if trace_iso else None,
