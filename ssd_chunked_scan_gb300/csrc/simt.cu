@@ -155,59 +155,81 @@ __global__ void __launch_bounds__(NT) k_chunk_state(const float *__restrict__ X,
 // when given.  Reverse: states[c] <- dX_c (gradient of the state leaving chunk
 // c), from query contributions, starting from dX_{N-1} = dfin (the cotangent
 // of the final state, zero when NULL); dh0 <- dX_{-1}.
-// grid (B*H, ceil(dk*dv / NT))
-__global__ void __launch_bounds__(NT) k_scan_fwd(float *__restrict__ states,
-                                                 const float *__restrict__ Adec,
-                                                 const float *__restrict__ h0,
-                                                 float *__restrict__ fin, Geo g) {
-  const int64_t bh = blockIdx.x;
-  const int64_t e = (int64_t)blockIdx.y * NT + threadIdx.x;
-  const int64_t sz = g.dk * g.dv;
-  if (e >= sz) return;
-  float run = h0 ? h0[bh * sz + e] : 0.f;
-  float *p = states + st_off(g, bh, 0) + e;
-  const float *a = Adec + bh * g.N;
-  int64_t c = 0;
-  for (; c + 4 <= g.N; c += 4) {
-    float x0 = p[(c + 0) * sz], x1 = p[(c + 1) * sz], x2 = p[(c + 2) * sz], x3 = p[(c + 3) * sz];
-    p[(c + 0) * sz] = run; run = fmaf(expf(a[c + 0]), run, x0);
-    p[(c + 1) * sz] = run; run = fmaf(expf(a[c + 1]), run, x1);
-    p[(c + 2) * sz] = run; run = fmaf(expf(a[c + 2]), run, x2);
-    p[(c + 3) * sz] = run; run = fmaf(expf(a[c + 3]), run, x3);
+// Each thread owns V consecutive state elements (V = 4: one float4, when
+// dk*dv is a multiple of 4) and loads SCU chunks' values ahead of the
+// dependent chain, so a pass costs about one memory round trip per SCU chunks.
+// grid (B*H, ceil(dk*dv / (V*NT)))
+constexpr int SCU = 8;
+
+template <int V>
+__device__ inline void ld_v(float (&x)[V], const float *p) {
+  if constexpr (V == 4) {
+    const float4 f = *reinterpret_cast<const float4 *>(p);
+    x[0] = f.x; x[1] = f.y; x[2] = f.z; x[3] = f.w;
+  } else {
+    x[0] = *p;
   }
-  for (; c < g.N; ++c) {
-    float x = p[c * sz];
-    p[c * sz] = run;
-    run = fmaf(expf(a[c]), run, x);
-  }
-  if (fin) fin[bh * sz + e] = run;
+}
+template <int V>
+__device__ inline void st_v(float *p, const float (&x)[V]) {
+  if constexpr (V == 4) *reinterpret_cast<float4 *>(p) = make_float4(x[0], x[1], x[2], x[3]);
+  else *p = x[0];
 }
 
-__global__ void __launch_bounds__(NT) k_scan_rev(float *__restrict__ states,
-                                                 const float *__restrict__ Adec,
-                                                 const float *__restrict__ dfin,
-                                                 float *__restrict__ dh0, Geo g) {
+template <int V, bool REV>
+__global__ void __launch_bounds__(NT) k_scan(float *__restrict__ states,
+                                             const float *__restrict__ Adec,
+                                             const float *__restrict__ init,
+                                             float *__restrict__ fin, Geo g) {
   const int64_t bh = blockIdx.x;
-  const int64_t e = (int64_t)blockIdx.y * NT + threadIdx.x;
+  const int64_t e0 = (int64_t)V * ((int64_t)blockIdx.y * NT + threadIdx.x);
   const int64_t sz = g.dk * g.dv;
-  if (e >= sz) return;
-  float run = dfin ? dfin[bh * sz + e] : 0.f;
-  float *p = states + st_off(g, bh, 0) + e;
+  if (e0 >= sz) return;
+  float run[V];
+#pragma unroll
+  for (int j = 0; j < V; ++j) run[j] = init ? init[bh * sz + e0 + j] : 0.f;
+  float *p = states + st_off(g, bh, 0) + e0;
   const float *a = Adec + bh * g.N;
-  int64_t c = g.N - 1;
-  for (; c - 3 >= 0; c -= 4) {
-    float x0 = p[(c - 0) * sz], x1 = p[(c - 1) * sz], x2 = p[(c - 2) * sz], x3 = p[(c - 3) * sz];
-    p[(c - 0) * sz] = run; run = fmaf(expf(a[c - 0]), run, x0);
-    p[(c - 1) * sz] = run; run = fmaf(expf(a[c - 1]), run, x1);
-    p[(c - 2) * sz] = run; run = fmaf(expf(a[c - 2]), run, x2);
-    p[(c - 3) * sz] = run; run = fmaf(expf(a[c - 3]), run, x3);
+  for (int64_t k0 = 0; k0 < g.N; k0 += SCU) {
+    float x[SCU][V], d[SCU];
+#pragma unroll
+    for (int u = 0; u < SCU; ++u) {
+      const int64_t k = k0 + u;
+      if (k < g.N) {
+        const int64_t c = REV ? g.N - 1 - k : k;
+        ld_v<V>(x[u], p + c * sz);
+        d[u] = expf(a[c]);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < SCU; ++u) {
+      const int64_t k = k0 + u;
+      if (k < g.N) {
+        const int64_t c = REV ? g.N - 1 - k : k;
+        st_v<V>(p + c * sz, run);
+#pragma unroll
+        for (int j = 0; j < V; ++j) run[j] = fmaf(d[u], run[j], x[u][j]);
+      }
+    }
   }
-  for (; c >= 0; --c) {
-    float x = p[c * sz];
-    p[c * sz] = run;
-    run = fmaf(expf(a[c]), run, x);
+  if (fin) {
+#pragma unroll
+    for (int j = 0; j < V; ++j) fin[bh * sz + e0 + j] = run[j];
   }
-  if (dh0) dh0[bh * sz + e] = run;
+}
+
+template <bool REV>
+static void launch_scan(float *st, const float *Adec, const float *init, float *fin,
+                        const Geo &g, cudaStream_t s, const char *name) {
+  const int64_t sz = g.dk * g.dv;
+  LaunchTrace lt(name, s);
+  if (sz % 4 == 0) {
+    const dim3 grid((unsigned)(g.B * g.H), (unsigned)cdiv(sz, 4 * NT));
+    k_scan<4, REV><<<grid, NT, 0, s>>>(st, Adec, init, fin, g);
+  } else {
+    const dim3 grid((unsigned)(g.B * g.H), (unsigned)cdiv(sz, NT));
+    k_scan<1, REV><<<grid, NT, 0, s>>>(st, Adec, init, fin, g);
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -336,7 +358,7 @@ __device__ inline void store_or_add(const float (&acc)[4][4 * NB], float *dst, i
 // accumulated over the group's heads in a fixed order.  dla receives the
 // in-chunk reverse cumulative sums; dcs_sum[bh*N + c] the chunk totals.
 template <int NBK, int NBV>
-__global__ void __launch_bounds__(NT) k_chunk_grad(
+__global__ void __launch_bounds__(NT, 2) k_chunk_grad(
     const float *__restrict__ q, const float *__restrict__ k, const float *__restrict__ v,
     const float *__restrict__ la, const float *__restrict__ dout, const float *__restrict__ Hst,
     const float *__restrict__ dXst, float *__restrict__ dq, float *__restrict__ dk,
@@ -569,9 +591,7 @@ static void dispatch_state(const float *X, const float *Y, const float *la, floa
 
 static void launch_scan_fwd(float *st, const float *Adec, const float *h0, float *fin,
                             const Geo &g, cudaStream_t s) {
-  dim3 grid((unsigned)(g.B * g.H), (unsigned)cdiv(g.dk * g.dv, NT));
-  LaunchTrace lt("simt.state_scan_fwd", s);
-  k_scan_fwd<<<grid, NT, 0, s>>>(st, Adec, h0, fin, g);
+  launch_scan<false>(st, Adec, h0, fin, g, s, "simt.state_scan_fwd");
 }
 
 size_t fwd_workspace_bytes(const Geo &g) {
@@ -628,11 +648,7 @@ cudaError_t bwd(const float *q, const float *k, const float *v, const float *la,
   launch_scan_fwd(Hst, Adec, h0, hT, g, s);
   // query contributions, then the reverse state-gradient pass
   dispatch_state<true>(q, dout, la, dXst, nullptr, g, s);
-  {
-    dim3 grid((unsigned)(g.B * g.H), (unsigned)cdiv(g.dk * g.dv, NT));
-    LaunchTrace lt("simt.state_scan_rev", s);
-    k_scan_rev<<<grid, NT, 0, s>>>(dXst, Adec, dhT, dh0, g);
-  }
+  launch_scan<true>(dXst, Adec, dhT, dh0, g, s, "simt.state_scan_rev");
   cudaError_t err;
   const bool bk = g.dk > 64, bv = g.dv > 64;
   if (bk && bv) err = launch_grad<2, 2>(q, k, v, la, dout, Hst, dXst, dq, dk, dv, dla, dcs_sum, g, s);
