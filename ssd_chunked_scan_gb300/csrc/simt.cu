@@ -45,23 +45,38 @@ __host__ __device__ constexpr int ldn(int nb) { return 64 * nb + 4; }
 // kk < KS, m < ld, zero outside kk < kmax - k0, m < mmax.  src(k, m) =
 // src[k * sk + m * sm].  MCONTIG selects which index consecutive threads walk
 // (the one that is contiguous in global memory).
+// Each thread issues the global loads of SU_ST elements before it stores any
+// of them, so a stage costs about one memory round trip per SU_ST elements.
+constexpr int SU_ST = 4;
 template <bool MCONTIG>
 __device__ inline void stage(float *__restrict__ dst, int ld, const float *__restrict__ src,
                              int64_t sk, int64_t sm, int k0, int kmax, int mmax,
                              const float *kscale, const float *mscale) {
   const int total = KS * ld;
-  for (int idx = threadIdx.x; idx < total; idx += NT) {
-    int kk, m;
-    if (MCONTIG) { kk = idx / ld; m = idx - kk * ld; }
-    else { m = idx / KS; kk = idx - m * KS; }
-    const int kg = k0 + kk;
-    float x = 0.f;
-    if (kg < kmax && m < mmax) {
-      x = src[(int64_t)kg * sk + (int64_t)m * sm];
-      if (kscale) x *= kscale[kg];
-      if (mscale) x *= mscale[m];
+  for (int base = threadIdx.x; base < total; base += SU_ST * NT) {
+    float x[SU_ST];
+    int kk[SU_ST], m[SU_ST];
+#pragma unroll
+    for (int u = 0; u < SU_ST; ++u) {
+      const int idx = base + u * NT;
+      if (MCONTIG) { kk[u] = idx / ld; m[u] = idx - kk[u] * ld; }
+      else { m[u] = idx / KS; kk[u] = idx - m[u] * KS; }
+      const int kg = k0 + kk[u];
+      x[u] = (idx < total && kg < kmax && m[u] < mmax) ? src[(int64_t)kg * sk + (int64_t)m[u] * sm] : 0.f;
     }
-    dst[kk * ld + m] = x;
+#pragma unroll
+    for (int u = 0; u < SU_ST; ++u) {
+      const int idx = base + u * NT;
+      if (idx < total) {
+        const int kg = k0 + kk[u];
+        float v = x[u];
+        if (kg < kmax && m[u] < mmax) {
+          if (kscale) v *= kscale[kg];
+          if (mscale) v *= mscale[m[u]];
+        }
+        dst[kk[u] * ld + m[u]] = v;
+      }
+    }
   }
 }
 
