@@ -47,7 +47,7 @@ __host__ __device__ constexpr int ldn(int nb) { return 64 * nb + 4; }
 // (the one that is contiguous in global memory).
 // Each thread issues the global loads of SU_ST elements before it stores any
 // of them, so a stage costs about one memory round trip per SU_ST elements.
-constexpr int SU_ST = 4;
+constexpr int SU_ST = 8;
 template <bool MCONTIG>
 __device__ inline void stage(float *__restrict__ dst, int ld, const float *__restrict__ src,
                              int64_t sk, int64_t sm, int k0, int kmax, int mmax,
