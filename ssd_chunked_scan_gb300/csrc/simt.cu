@@ -45,19 +45,20 @@ __host__ __device__ constexpr int ldn(int nb) { return 64 * nb + 4; }
 // kk < KS, m < ld, zero outside kk < kmax - k0, m < mmax.  src(k, m) =
 // src[k * sk + m * sm].  MCONTIG selects which index consecutive threads walk
 // (the one that is contiguous in global memory).
-// Each thread issues the global loads of SU_ST elements before it stores any
-// of them, so a stage costs about one memory round trip per SU_ST elements.
-constexpr int SU_ST = 8;
-template <bool MCONTIG>
+// Each thread issues the global loads of U elements before it stores any of
+// them, so a stage costs about one memory round trip per U elements (16 by
+// default; 8 in the output kernel, which then keeps three CTAs per SM).
+constexpr int SU_ST = 16;
+template <bool MCONTIG, int U = SU_ST>
 __device__ inline void stage(float *__restrict__ dst, int ld, const float *__restrict__ src,
                              int64_t sk, int64_t sm, int k0, int kmax, int mmax,
                              const float *kscale, const float *mscale) {
   const int total = KS * ld;
-  for (int base = threadIdx.x; base < total; base += SU_ST * NT) {
-    float x[SU_ST];
-    int kk[SU_ST], m[SU_ST];
+  for (int base = threadIdx.x; base < total; base += U * NT) {
+    float x[U];
+    int kk[U], m[U];
 #pragma unroll
-    for (int u = 0; u < SU_ST; ++u) {
+    for (int u = 0; u < U; ++u) {
       const int idx = base + u * NT;
       if (MCONTIG) { kk[u] = idx / ld; m[u] = idx - kk[u] * ld; }
       else { m[u] = idx / KS; kk[u] = idx - m[u] * KS; }
@@ -65,7 +66,7 @@ __device__ inline void stage(float *__restrict__ dst, int ld, const float *__res
       x[u] = (idx < total && kg < kmax && m[u] < mmax) ? src[(int64_t)kg * sk + (int64_t)m[u] * sm] : 0.f;
     }
 #pragma unroll
-    for (int u = 0; u < SU_ST; ++u) {
+    for (int u = 0; u < U; ++u) {
       const int idx = base + u * NT;
       if (idx < total) {
         const int kg = k0 + kk[u];
@@ -249,12 +250,13 @@ static void launch_scan(float *st, const float *Adec, const float *init, float *
 
 // ---------------------------------------------------------------------------
 // Raw q.k scores of one chunk into registers: acc[t][s] (rows t, cols s).
+template <int U = SU_ST>
 __device__ inline void chunk_scores(float (&acc)[4][4], const float *qs, const float *ks,
                                     float *As, float *Bs, const Geo &g, int len) {
   zero_acc<1, 1>(acc);
   for (int i0 = 0; i0 < g.dk; i0 += KS) {
-    stage<false>(As, LDT, qs + i0, 1, g.G * g.dk, 0, (int)g.dk - i0, len, nullptr, nullptr);
-    stage<false>(Bs, LDT, ks + i0, 1, g.G * g.dk, 0, (int)g.dk - i0, len, nullptr, nullptr);
+    stage<false, U>(As, LDT, qs + i0, 1, g.G * g.dk, 0, (int)g.dk - i0, len, nullptr, nullptr);
+    stage<false, U>(Bs, LDT, ks + i0, 1, g.G * g.dk, 0, (int)g.dk - i0, len, nullptr, nullptr);
     __syncthreads();
     mma_slice<1, 1>(acc, As, LDT, Bs, LDT, min(KS, (int)g.dk - i0));
     __syncthreads();
@@ -283,7 +285,7 @@ __global__ void __launch_bounds__(NT) k_chunk_out(const float *__restrict__ q,
   const float *ks = k + qk_off(g, b, t0, grp);
 
   float sc[4][4];
-  chunk_scores(sc, qs, ks, As, Bs, g, len);
+  chunk_scores<8>(sc, qs, ks, As, Bs, g, len);
 #pragma unroll
   for (int r = 0; r < 4; ++r) {
     const int t = row_of(r);
@@ -301,15 +303,15 @@ __global__ void __launch_bounds__(NT) k_chunk_out(const float *__restrict__ q,
   zero_acc<1, NB>(acc);
   const float *vs = v + v_off(g, b, t0, h);
   for (int s0 = 0; s0 < len; s0 += KS) {
-    stage<true>(Bs, ldn(NB), vs, g.H * g.dv, 1, s0, len, (int)g.dv, nullptr, nullptr);
+    stage<true, 8>(Bs, ldn(NB), vs, g.H * g.dv, 1, s0, len, (int)g.dv, nullptr, nullptr);
     __syncthreads();
     mma_slice<1, NB>(acc, Pt + s0 * LDT, LDT, Bs, ldn(NB), min(KS, len - s0));
     __syncthreads();
   }
   const float *Hs = states + st_off(g, bh, c);
   for (int i0 = 0; i0 < g.dk; i0 += KS) {
-    stage<false>(As, LDT, qs + i0, 1, g.G * g.dk, 0, (int)g.dk - i0, len, nullptr, ecs);
-    stage<true>(Bs, ldn(NB), Hs + (int64_t)i0 * g.dv, g.dv, 1, 0, (int)g.dk - i0, (int)g.dv, nullptr, nullptr);
+    stage<false, 8>(As, LDT, qs + i0, 1, g.G * g.dk, 0, (int)g.dk - i0, len, nullptr, ecs);
+    stage<true, 8>(Bs, ldn(NB), Hs + (int64_t)i0 * g.dv, g.dv, 1, 0, (int)g.dk - i0, (int)g.dv, nullptr, nullptr);
     __syncthreads();
     mma_slice<1, NB>(acc, As, LDT, Bs, ldn(NB), min(KS, (int)g.dk - i0));
     __syncthreads();
@@ -532,7 +534,7 @@ __global__ void __launch_bounds__(NT) k_dla_carry(float *__restrict__ dla,
                                                   const float *__restrict__ dcs_sum,
                                                   const float *__restrict__ dhT,
                                                   const float *__restrict__ hT, Geo g) {
-  __shared__ double sh[NT];
+  __shared__ double sh[NT], ex[NT];
   __shared__ double carry_in;
   const int64_t bh = blockIdx.x, b = bh / g.H, h = bh % g.H;
   {
@@ -565,12 +567,25 @@ __global__ void __launch_bounds__(NT) k_dla_carry(float *__restrict__ dla,
       sh[threadIdx.x] += y;
       __syncthreads();
     }
-    const double excl = sh[threadIdx.x] - x + carry_in;
-    if (c < hi) {
-      const int64_t t0 = c * g.C;
-      const int len = (int)(g.L - t0 < g.C ? g.L - t0 : g.C);
-      float *dl = dla + la_off(g, b, t0, h);
-      for (int t = 0; t < len; ++t) dl[(int64_t)t * g.H] = (float)((double)dl[(int64_t)t * g.H] + excl);
+    ex[threadIdx.x] = sh[threadIdx.x] - x + carry_in;  // carry into chunk c
+    __syncthreads();
+    // every token of chunks lo..hi-1 gets its chunk's carry, all threads, the
+    // loads of 8 tokens per thread in flight before their stores
+    const int64_t ntok = (hi - lo) * g.C;
+    for (int64_t i0 = threadIdx.x; i0 < ntok; i0 += 8 * NT) {
+      float cur[8];
+      int64_t off[8];
+      bool in[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int64_t i = i0 + (int64_t)u * NT, t = lo * g.C + i;
+        in[u] = i < ntok && t < g.L;
+        off[u] = in[u] ? la_off(g, b, t, h) : 0;
+        cur[u] = in[u] ? dla[off[u]] : 0.f;
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+        if (in[u]) dla[off[u]] = (float)((double)cur[u] + ex[(i0 + (int64_t)u * NT) / g.C]);
     }
     __syncthreads();
     if (threadIdx.x == 0) carry_in += sh[0];
