@@ -56,7 +56,7 @@ def load_peaks():
                 "source": "fallback"}
 
 
-# DRAM bytes (read + write) per launch of each tensor-core kernel from one ncu
+# DRAM bytes (read + write) per launch of each kernel from one ncu
 # capture of the kernels as they stand (profiles/tc_g2h8_d128_L8192_long.md,
 # g2h8_d128 L=8192 long-memory workload); a kernel without an entry reports
 # null.  Every change to a kernel must refresh or drop its entry.
@@ -71,6 +71,15 @@ TRAFFIC = {
     "tc.walk_dv": 221358592 + 94183936,
     "tc.dla_intra": 336926464 + 483072,
     "tc.dla": 36711936,
+    # the CUDA-core path's kernels (profiles/simt_g2h8_d128_L8192_long.md); kernels
+    # that run twice per step: the mean of their launches
+    "simt.chunk_state": (168927744 + 213100544 + 168965120 + 209852160) // 2,
+    "simt.state_scan_fwd": (270607872 + 204486912 + 270578176 + 204050688) // 2,
+    "simt.chunk_out": 471726848 + 110684672,
+    "simt.query_state": 168932864 + 209318400,
+    "simt.state_scan_rev": 268482048 + 206218496,
+    "simt.chunk_grad": 1171999232 + 349719040,
+    "simt.dla_carry": 1090304,
 }
 # the same for the Mamba kernels at d1024 L8192 (profiles/mamba_d1024_L8192.md);
 # seg_state and seg_scan run more than once per step: the mean of their launches
