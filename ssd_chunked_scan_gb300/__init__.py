@@ -8,6 +8,9 @@ generators work on machines without the built library.
 
 
 def __getattr__(name):
+    if name == "ssd_scan":
+        from .autograd import ssd_scan
+        return ssd_scan
     if name in ("ssd_fwd", "ssd_bwd", "ssd_fwd_ex", "ssd_bwd_ex", "ssd_set_path", "ssd_get_path", "ssd_strerror",
                 "ssd_set_overlap", "ssd_get_overlap",
                 "ssd_last_device_error", "SSDError", "SSD_PATH_TC", "SSD_PATH_SIMT"):

@@ -198,6 +198,8 @@ def _check(name, t, shape, device):
         return
     if not isinstance(t, torch.Tensor) or t.dtype != torch.float32:
         raise TypeError(f"{name} must be a float32 torch tensor")
+    if t.device.type != "cuda":  # the library takes device pointers only
+        raise ValueError(f"{name} must be a CUDA tensor, got {t.device}")
     if t.device != device:
         raise ValueError(f"{name} must be on {device}, got {t.device}")
     if not t.is_contiguous():
