@@ -57,8 +57,11 @@
  *                 1 <= dk, dv <= 128.  Its workspace holds every chunk's
  *                 state (B*H*ceil(L/chunk)*dk*dv floats per pass), where
  *                 the tensor-core path keeps one state per segment (about
- *                 four segments per SM in all, whatever L); see
- *                 ssd_fwd_workspace_bytes.
+ *                 two segments per SM in all, whatever L); see
+ *                 ssd_fwd_workspace_bytes.  The tensor-core backward runs
+ *                 part of its work on a stream of the library's own, forked
+ *                 from and joined back into `stream` within the call (see
+ *                 ssd_set_overlap).
  *   chunk == 1    (either path) the sequential evaluation: the recurrence one
  *                 token at a time, the state in registers, all fp32, no
  *                 workspace in the forward (suits decoding a few tokens with
