@@ -265,7 +265,7 @@ SSD_API int ssd_trace_get(int i, char *name, int name_len, long long *launches,
 SSD_API int ssd_trace_reset(void);
 
 /* Library version as major*10000 + minor*100 + patch (0.2.0 added the
- * final-state entry points). */
+ * final-state entry points, 0.3.0 ssd_set_overlap / ssd_get_overlap). */
 SSD_API int ssd_version(void);
 
 #ifdef __cplusplus

@@ -120,7 +120,7 @@ int ws_alloc(void **p, size_t bytes, cudaStream_t s) {
 
 extern "C" {
 
-int ssd_version(void) { return 200; }
+int ssd_version(void) { return 300; }
 
 const char *ssd_strerror(int status) {
   switch (status) {

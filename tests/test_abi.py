@@ -105,6 +105,10 @@ def test_set_path(lib):
     assert lib.ssd_set_path(0) == 0 and lib.ssd_get_path() == 0
 
 
+def test_version(lib):
+    assert lib.ssd_version() == 300
+
+
 def test_set_overlap(lib):
     first = lib.ssd_set_overlap(0)
     try:
