@@ -67,23 +67,46 @@ struct Stage {
   float *bs, *cs;       // B, C            [TB][NL]
 };
 
+// Each thread loads all of its elements of the block (two of each series at
+// 256 threads) before it stores any, so staging costs one memory round trip.
 __device__ inline void stage_block(const Stage &st, const float *x, const float *dt,
                                    const float *dy, const float *Bm, const float *Cm,
                                    const MGeo &g, int64_t b, int64_t d0, int64_t t0, int len) {
-  for (int idx = threadIdx.x; idx < TB * CH; idx += NT) {
-    const int tt = idx / CH, c = idx - tt * CH;
-    const bool ok = tt < len && d0 + c < g.D;
+  constexpr int PC = (TB * CH + NT - 1) / NT, PN = (TB * NL + NT - 1) / NT;
+  float vx[PC], vd[PC], vy[PC], vb[PN], vc[PN];
+#pragma unroll
+  for (int u = 0; u < PC; ++u) {
+    const int idx = threadIdx.x + u * NT, tt = idx / CH, c = idx - tt * CH;
+    const bool ok = idx < TB * CH && tt < len && d0 + c < g.D;
     const int64_t o = (b * g.L + t0 + tt) * g.D + d0 + c;
-    st.xs[idx] = ok ? x[o] : 0.f;
-    st.ds[idx] = ok ? dt[o] : 0.f;
-    if (dy) st.ys[idx] = ok ? dy[o] : 0.f;
+    vx[u] = ok ? x[o] : 0.f;
+    vd[u] = ok ? dt[o] : 0.f;
+    vy[u] = (dy && ok) ? dy[o] : 0.f;
   }
-  for (int idx = threadIdx.x; idx < TB * NL; idx += NT) {
-    const int tt = idx / NL, n = idx - tt * NL;
-    const bool ok = tt < len && n < g.N;
+#pragma unroll
+  for (int u = 0; u < PN; ++u) {
+    const int idx = threadIdx.x + u * NT, tt = idx / NL, n = idx - tt * NL;
+    const bool ok = idx < TB * NL && tt < len && n < g.N;
     const int64_t o = (b * g.L + t0 + tt) * g.N + n;
-    if (Bm) st.bs[idx] = ok ? Bm[o] : 0.f;
-    if (Cm) st.cs[idx] = ok ? Cm[o] : 0.f;
+    vb[u] = (Bm && ok) ? Bm[o] : 0.f;
+    vc[u] = (Cm && ok) ? Cm[o] : 0.f;
+  }
+#pragma unroll
+  for (int u = 0; u < PC; ++u) {
+    const int idx = threadIdx.x + u * NT;
+    if (idx < TB * CH) {
+      st.xs[idx] = vx[u];
+      st.ds[idx] = vd[u];
+      if (dy) st.ys[idx] = vy[u];
+    }
+  }
+#pragma unroll
+  for (int u = 0; u < PN; ++u) {
+    const int idx = threadIdx.x + u * NT;
+    if (idx < TB * NL) {
+      if (Bm) st.bs[idx] = vb[u];
+      if (Cm) st.cs[idx] = vc[u];
+    }
   }
 }
 
@@ -93,24 +116,51 @@ constexpr int CCH = 128;
 
 // Per-block staging of the channel kernels: per-channel series [TB][CCH] and
 // the per-token rows of B and C [TB][NL] (read as float4 broadcasts).
+// The channel kernels' staging issues the loads of SB rows of the block per
+// thread before storing them, so a block costs TB / SB memory round trips.
+constexpr int SB = 4;
 __device__ inline void stage_channels(float *xs, float *ds, float *ys, float *bs, float *cs,
                                       const float *x, const float *dt, const float *dy,
                                       const float *Bm, const float *Cm, const MGeo &g, int64_t b,
                                       int64_t d0, int64_t t0, int len) {
-  for (int idx = threadIdx.x; idx < TB * CCH; idx += CCH) {
-    const int tt = idx / CCH, c = idx - tt * CCH;
-    const bool ok = tt < len && d0 + c < g.D;
-    const int64_t o = (b * g.L + t0 + tt) * g.D + d0 + c;
-    if (xs) xs[idx] = ok ? x[o] : 0.f;
-    ds[idx] = ok ? dt[o] : 0.f;
-    if (ys) ys[idx] = ok ? dy[o] : 0.f;
+  const int c = threadIdx.x;  // idx = tt * CCH + c: thread c stages channel c of every row
+  const bool cok = d0 + c < g.D;
+  for (int t0b = 0; t0b < TB; t0b += SB) {
+    float vx[SB], vd[SB], vy[SB];
+#pragma unroll
+    for (int u = 0; u < SB; ++u) {
+      const int tt = t0b + u;
+      const bool ok = tt < len && cok;
+      const int64_t o = (b * g.L + t0 + tt) * g.D + d0 + c;
+      vx[u] = (xs && ok) ? x[o] : 0.f;
+      vd[u] = ok ? dt[o] : 0.f;
+      vy[u] = (ys && ok) ? dy[o] : 0.f;
+    }
+#pragma unroll
+    for (int u = 0; u < SB; ++u) {
+      const int idx = (t0b + u) * CCH + c;
+      if (xs) xs[idx] = vx[u];
+      ds[idx] = vd[u];
+      if (ys) ys[idx] = vy[u];
+    }
   }
-  for (int idx = threadIdx.x; idx < TB * NL; idx += CCH) {
-    const int tt = idx / NL, n = idx - tt * NL;
-    const bool ok = tt < len && n < g.N;
+  constexpr int PN = (TB * NL + CCH - 1) / CCH;
+  float vb[PN], vc[PN];
+#pragma unroll
+  for (int u = 0; u < PN; ++u) {
+    const int idx = threadIdx.x + u * CCH, tt = idx / NL, n = idx - tt * NL;
+    const bool ok = idx < TB * NL && tt < len && n < g.N;
     const int64_t o = (b * g.L + t0 + tt) * g.N + n;
-    if (bs) bs[idx] = ok ? Bm[o] : 0.f;
-    if (cs) cs[idx] = ok ? Cm[o] : 0.f;
+    vb[u] = (bs && ok) ? Bm[o] : 0.f;
+    vc[u] = (cs && ok) ? Cm[o] : 0.f;
+  }
+#pragma unroll
+  for (int u = 0; u < PN; ++u) {
+    const int idx = threadIdx.x + u * CCH;
+    if (idx < TB * NL) {
+      if (bs) bs[idx] = vb[u];
+      if (cs) cs[idx] = vc[u];
+    }
   }
 }
 
@@ -286,7 +336,7 @@ __global__ void __launch_bounds__(CCH) k_mb_out(const float *__restrict__ x,
 // per window instead of 4 per token), lane n ending with token n's sums.
 // grid (ceil(D/CH), nseg, B)
 constexpr int WB = 16;
-__global__ void __launch_bounds__(NT, 2) k_mb_bwd(
+__global__ void __launch_bounds__(NT, 3) k_mb_bwd(
     const float *__restrict__ x, const float *__restrict__ dt, const float *__restrict__ A,
     const float *__restrict__ Bm, const float *__restrict__ Cm, const float *__restrict__ Dk,
     const float *__restrict__ dy, const float *__restrict__ hin, const float *__restrict__ uin,
