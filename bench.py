@@ -84,11 +84,11 @@ TRAFFIC = {
 # the same for the Mamba kernels at d1024 L8192 (profiles/mamba_d1024_L8192.md);
 # seg_state and seg_scan run more than once per step: the mean of their launches
 MAMBA_TRAFFIC = {
-    "mamba.seg_state": (270620672 + 3479808 + 270631680 + 651776) // 2,
-    "mamba.seg_scan": (6209792 + 6209024 + 6208768) // 3,
-    "mamba.out": 278497280 + 98762240,
-    "mamba.seg_grad_state": 270618624 + 310016,
-    "mamba.bwd": 426092288 + 241760768,
+    "mamba.seg_state": (270622976 + 3436800 + 270637056 + 328448) // 2,
+    "mamba.seg_scan": (6209280 + 6209024 + 6209024) // 3,
+    "mamba.out": 278507776 + 99099904,
+    "mamba.seg_grad_state": 270713856 + 371456,
+    "mamba.bwd": 427659520 + 242076672,
 }
 
 # nominal dense tensor rates: tf32 1.1 PF vs bf16 2.25 PF per GPU
