@@ -689,6 +689,76 @@ def mamba_cpu_sample(w, fb, min_seconds=10.0, max_reps=80):
                                         f"float64 {'fwd+bwd' if fb else 'fwd'}, {reps} rep(s), {el:.1f} s"}
 
 
+def sweep_records(workloads, paths=("tc", "simt"), modes=("fwd", "fwd_bwd")):
+    """The records of a sweep: every (workload, path, mode) a path supports,
+    as the key dicts that identify a record."""
+    recs = []
+    for w in workloads:
+        for path in paths:
+            if path == "tc" and (w.dk % 8 or w.dv % 8 or w.dk > 128 or w.dv > 128 or w.chunk != 64):
+                continue
+            for mode in modes:
+                recs.append({"workload": w.name, "path": path, "mode": mode, "chunk": w.chunk})
+    return recs
+
+
+def sweep_key(rec):
+    return (rec["workload"], rec["path"], rec["mode"], rec["chunk"])
+
+
+def sweep_todo(out_path, records):
+    """Records not yet in the JSON-lines file out_path (a line counts once it
+    holds a record key, whether it measured a value or recorded an error), so
+    an interrupted sweep resumes where it stopped."""
+    done = set()
+    if os.path.exists(out_path):
+        with open(out_path) as f:
+            for line in f:
+                line = line.strip()
+                if not line:
+                    continue
+                try:
+                    r = json.loads(line)
+                except ValueError:
+                    continue  # a line cut short by an interruption
+                if isinstance(r, dict) and isinstance(r.get("record"), dict):
+                    done.add(sweep_key(r["record"]))
+    return [r for r in records if sweep_key(r) not in done]
+
+
+def run_sweep(args):
+    """Measure every record of the sweep not yet in args.sweep, one bench
+    process per record, appending one JSON line each: the record's bench line,
+    or the error that stopped it (the sweep goes on)."""
+    from ssd_chunked_scan_gb300.inputs import WORKLOADS
+    todo = sweep_todo(args.sweep, sweep_records(WORKLOADS))
+    if os.path.exists(args.sweep) and os.path.getsize(args.sweep) > 0:
+        with open(args.sweep, "rb") as f:
+            f.seek(-1, os.SEEK_END)
+            cut = f.read(1) != b"\n"
+        if cut:  # close a line an interruption left unfinished
+            with open(args.sweep, "a") as f:
+                f.write("\n")
+    for rec in todo:
+        cmd = [sys.executable, os.path.abspath(__file__), "--workload", rec["workload"],
+               "--path", rec["path"], "--mode", rec["mode"], "--steps", str(args.steps),
+               "--warmup", str(args.warmup), "--no-cpu-baseline", "--no-e2e"]
+        try:
+            r = subprocess.run(cmd, capture_output=True, text=True, timeout=600)
+            lines = [l for l in r.stdout.splitlines() if l.startswith("{")]
+            if r.returncode == 0 and lines:
+                out = {"record": rec, "result": json.loads(lines[-1])}
+            else:
+                tail = (r.stderr or r.stdout).strip().splitlines()[-1:] or ["no output"]
+                out = {"record": rec, "error": f"exit {r.returncode}: {tail[0][:300]}"}
+        except subprocess.TimeoutExpired:
+            out = {"record": rec, "error": "timed out after 600 s"}
+        with open(args.sweep, "a") as f:
+            f.write(json.dumps(out) + "\n")
+        print(json.dumps({"record": rec, "ok": "result" in out}), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -706,8 +776,15 @@ def main():
     ap.add_argument("--mode", default="fwd_bwd", choices=["fwd_bwd", "fwd", "max_len"],
                     help="fwd times ssd_fwd alone (a step is then one forward pass); "
                          "max_len finds the largest sequence length fwd_bwd runs at")
+    ap.add_argument("--sweep", default=None, metavar="OUT.jsonl",
+                    help="measure every (workload, path, mode) record not yet in OUT.jsonl "
+                         "(fwd and fwd_bwd, both paths), appending one line per record")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
+    if args.sweep:
+        if args.steps == 200:
+            args.steps = 20  # a record is a short measurement
+        return run_sweep(args)
 
     if args.op == "mamba":
         if args.impl == "reference":

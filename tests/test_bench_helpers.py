@@ -76,3 +76,20 @@ def test_step_totals_match_the_workload_sizes():
     assert bytes_f / mib == pytest.approx(323, abs=1)
     assert bytes_fb / mib == pytest.approx(841, abs=1)
     assert fl_fb > fl_f > 0
+
+
+def test_sweep_resumes_after_recorded_lines(tmp_path):
+    from ssd_chunked_scan_gb300.inputs import WORKLOADS
+    recs = bench.sweep_records(WORKLOADS)
+    # five page workloads x two paths x two modes, each path taking all five
+    assert len(recs) == 20 and len({bench.sweep_key(r) for r in recs}) == 20
+    out = tmp_path / "sweep.jsonl"
+    assert bench.sweep_todo(str(out), recs) == recs  # nothing recorded yet
+    import json
+    with open(out, "w") as f:
+        f.write(json.dumps({"record": recs[0], "result": {"value": 1.0}}) + "\n")
+        f.write(json.dumps({"record": recs[3], "error": "exit 1: boom"}) + "\n")
+        f.write('{"record": {"workload": "g1h1')  # cut short by an interruption
+    todo = bench.sweep_todo(str(out), recs)
+    assert recs[0] not in todo and recs[3] not in todo
+    assert len(todo) == 18 and todo[0] == recs[1]
