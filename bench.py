@@ -976,11 +976,13 @@ def main():
         roof_iso["timing"] = "the same steps with the backward's passes serialised (one kernel at a time)"
 
     bytes_fb, fl_fb, bytes_f, fl_f = step_totals(w)
-    t_hbm = bytes_fb / (peaks["hbm_gbs"] * 1e9)
-    t_tc = fl_fb / (peaks["bf16_tflops"] * TF32_OVER_BF16 * 1e12)
+    # the step's own algorithmic totals: a forward alone with --mode fwd
+    step_bytes, step_flops = (bytes_f, fl_f) if args.mode == "fwd" else (bytes_fb, fl_fb)
+    t_hbm = step_bytes / (peaks["hbm_gbs"] * 1e9)
+    t_tc = step_flops / (peaks["bf16_tflops"] * TF32_OVER_BF16 * 1e12)
     step_roof_s = max(t_hbm, t_tc)
     value = job_tokens_per_s(w.tokens, world, ms)
-    page_ms = PAGE_FWD_BWD_MS.get(w.name)
+    page_ms = (PAGE_FWD_MS if args.mode == "fwd" else PAGE_FWD_BWD_MS).get(w.name)
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
@@ -993,7 +995,7 @@ def main():
                    "l2": "no flush: each step's inputs and outputs (967 MiB) exceed L2"},
         "roofline": roof,
         "step_roofline": {"bound": "hbm" if t_hbm >= t_tc else "tensor",
-                          "alg_bytes": bytes_fb, "alg_flops": fl_fb,
+                          "alg_bytes": step_bytes, "alg_flops": step_flops,
                           "roofline_ms": step_roof_s * 1e3, "frac": step_roof_s * 1e3 / ms},
         "fwd": {"ms": fwd_ms, "tokens_per_s": w.tokens / (fwd_ms / 1e3),
                 "frac_of_roofline": max(bytes_f / (peaks["hbm_gbs"] * 1e9),
@@ -1006,7 +1008,8 @@ def main():
         "clocks": clk,
         "e2e": e2e,
         "memory": memory,
-        "page_context": {"rtx3090_fwd_bwd_ms": page_ms, "rtx3090_fwd_ms": PAGE_FWD_MS.get(w.name),
+        "page_context": {"rtx3090_fwd_bwd_ms": PAGE_FWD_BWD_MS.get(w.name),
+                         "rtx3090_fwd_ms": PAGE_FWD_MS.get(w.name),
                          "rtx3090_chunked_peak_mb": PAGE_PEAK_MB if w.name == WORKLOAD else None},
     }
     if world == 1 and not args.no_cpu_baseline:
