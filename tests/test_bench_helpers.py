@@ -93,3 +93,12 @@ def test_sweep_resumes_after_recorded_lines(tmp_path):
     todo = bench.sweep_todo(str(out), recs)
     assert recs[0] not in todo and recs[3] not in todo
     assert len(todo) == 18 and todo[0] == recs[1]
+
+
+def test_l2_note_says_whether_a_step_fits_in_l2():
+    w = BY_NAME[bench.WORKLOAD]
+    big = bench.resident_bytes(w.B, w.L, w.G, w.H, w.dk, w.dv, "fwd_bwd")
+    assert big > bench.L2_BYTES and "exceed L2" in bench.l2_note(big)
+    small = BY_NAME["g1h1_d128_L512"]
+    b = bench.resident_bytes(small.B, small.L, small.G, small.H, small.dk, small.dv, "fwd")
+    assert b < bench.L2_BYTES and "fit in L2" in bench.l2_note(b)
