@@ -150,9 +150,9 @@ def kernel_costs(w, sms=152):
 
 def tc_nseg(w, sms=152):
     """Segments per sequence chosen by the tensor-core path (same rule as tc.cu:
-    one wave of two CTAs per SM)."""
+    one wave of walk CTAs at one CTA per SM)."""
     bh = w.B * w.H
-    want = max(1, (2 * sms) // bh)
+    want = max(1, sms // bh)
     Ls = -(-(-(-w.L // want)) // 64) * 64
     Ls = max(Ls, 64)
     return -(-w.L // Ls)

@@ -19,21 +19,25 @@
 // dhT is the cotangent of the final state hT (zero unless given).
 //
 // A pass cuts every (batch, head) sequence into segments of Ls tokens (a
-// multiple of the 64-token chunk) so that B*H*nseg CTAs work at once:
+// multiple of the 64-token chunk), about one segment per SM in all:
 //   k_seg_state  each segment's zero-initial-state contribution (one contraction)
 //   k_seg_scan   the states entering every segment (sequential over segments)
 //   k_walk       each segment's chunks in order, the running state resident in
 //                tensor memory
 //
-// Operands the tensor cores must see transposed (anything contracted over
-// tokens) are made by the threads from the TMA-loaded tiles: into tensor
-// memory as the A operand (k'^T, v'^T) or into shared memory in the K-major
-// 128-byte-swizzled layout (w * k'^T, P).  Operands written by threads are
-// rounded to TF32 to nearest; TMA-fed ones are truncated by the tensor core.
+// Operand layouts.  A product that contracts over features (q' k'^T, the
+// state times q') takes K-major operands: TMA tiles in the 128-byte swizzle.
+// A product that contracts over tokens (P v', the state update v'^T (w k'))
+// takes MN-major operands: TMA tiles in the 128-byte swizzle with 32-byte
+// atoms, the only layout in which the tensor cores read fp32 operands
+// transposed.  So no operand is ever transposed by the threads; they only
+// scale (w k') and mask (P).  TMA-fed operands are truncated to TF32 by the
+// tensor core; operands written by threads are rounded to nearest.
 #include <algorithm>
 #include <atomic>
 #include <cstring>
 #include <mutex>
+#include <utility>
 
 #include <cudaTypedefs.h>
 
@@ -46,8 +50,9 @@ namespace ssd {
 namespace tc {
 
 constexpr int C = 64;     // chunk length of the tensor-core path
-constexpr int NTH = 128;  // threads per CTA: one per tensor-memory lane
-constexpr int NT2 = 256;  // two threads per tensor-memory lane (column halves)
+constexpr int NTH = 128;  // threads per CTA of the small kernels
+constexpr float LOG2E = 1.4426950408889634f;
+constexpr double LOG2E_D = 1.4426950408889634;
 
 __host__ __device__ constexpr int rup(int x, int m) { return (x + m - 1) / m * m; }
 __host__ __device__ inline int64_t imin64(int64_t a, int64_t b) { return a < b ? a : b; }
@@ -101,17 +106,6 @@ struct PassGeo {
   int Ls, nseg;        // segment length (multiple of C) and segments per sequence
 };
 
-// Output of a walk: out'[b, t, slot, 0:dv] with slot = h (out_slots == H) or
-// h / hpg (out_slots == G, summed over the group's heads by atomic adds);
-// optionally dcs[b, t, h] = y[b, t, h / hpg, :] . (the inter-chunk part of
-// out'_t, the term carried by the state entering the chunk).
-struct OutArgs {
-  float *out;
-  int out_slots;
-  const float *y;
-  float *dcs;
-};
-
 __device__ __forceinline__ int qk_slot(const PassGeo &p, int64_t h) {
   return (int)(p.qk_per_head ? h : h / p.hpg);
 }
@@ -120,38 +114,47 @@ __device__ __forceinline__ int v_slot(const PassGeo &p, int64_t h) {
 }
 
 // ===========================================================================
-// Segment contraction, the zero-initial-state contribution of one segment:
+// Segment contraction, the zero-initial-state contribution of one segment,
+// stored as the pass's state [dk' x dv'] (row-major):
 //   causal      D = sum_u exp(A_seg - cs_u) k'_u v'_u^T   (evaluated at its end)
 //   anti-causal D = sum_u exp(cs_u) k'_u v'_u^T           (evaluated at its start)
 // with cs the in-segment inclusive prefix of la and A_seg its total (also
-// written).  grid (nseg, H, B), 256 threads: thread (quarter q, lane l, half f)
-// owns tensor-memory lane 32q + l and token half f of each 32-token slice.
-// The segment is streamed in 32-token slices through a two-stage TMA ring,
-// loaded two slices ahead.  Tensor memory (256 columns): D [0,128), A operand
-// k'^T double-buffered at [128,160) / [160,192).  Shared memory: two stages of
-// k' and v' tiles, and the B operand (sc * v')^T [dvn x 32], double-buffered.
-constexpr int SL = 32;  // slice length of the segment contraction
+// written).  grid (nseg, H, B), one CTA per SM, 192 threads.  Per 64-token
+// slice, both products on the tensor cores, operands straight from TMA:
+//   T^T  = v'^T W           (W = diag(w) of the slice, K-major in shared memory)
+//   D^T += T^T k'           (T^T from tensor memory, k' MN-major)
+// so that no thread pass touches the k' / v' tiles (thread reads of shared
+// memory are slow while the tensor cores stream from it).  Warp 0 issues the
+// TMA loads (three-stage ring, L2 prefetches after it), warp 1 the MMAs,
+// warps 2-5 compute the weights into W (double-buffered; only its diagonal is
+// rewritten) and finally write D out.  Tensor memory: D^T [0,128) (lane = v'
+// feature, column = k' feature), T^T [128,256) (two buffers).
+constexpr int SL = 64;          // slice length
+constexpr int SS_STAGES = 3;    // slices in flight
+constexpr int SS_PREFETCH = 2;  // slices past the ring, prefetched into L2
+constexpr int SS_THREADS = 192;
 template <bool REV>
-__global__ void __launch_bounds__(NT2, 2) k_seg_state(const __grid_constant__ CUtensorMap tmK,
-                                                      const __grid_constant__ CUtensorMap tmV,
-                                                      const float *__restrict__ la,
-                                                      float *__restrict__ states,
-                                                      float *__restrict__ Aseg, PassGeo p) {
+__global__ void __launch_bounds__(SS_THREADS, 1) k_seg_state(const __grid_constant__ CUtensorMap tmK,
+                                                             const __grid_constant__ CUtensorMap tmV,
+                                                             const float *__restrict__ la,
+                                                             float *__restrict__ states,
+                                                             float *__restrict__ Aseg, PassGeo p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t *smem = smem_align1024(smem_raw);
   const int ncbk = p.dkp / 32, ncbv = p.dvp / 32;
-  const uint32_t xbytes = (uint32_t)ncbk * 4096, ybytes = (uint32_t)ncbv * 4096;
-  const uint32_t stage = xbytes + ybytes;
-  const uint32_t bbytes = (uint32_t)rup(p.dvn * 128, 1024);
-  uint8_t *tiles = smem;                      // [2][k' tile 32 x dkp | v' tile 32 x dvp]
-  uint8_t *Bb = smem + 2 * stage;             // [2][dvn x 32] K-major
-  float *scb = (float *)(Bb + 2 * bbytes);    // [256] per-token weights of 8 slices
-  __shared__ double wtot[8];
-  __shared__ uint64_t bar_tma[2], bar_mma[2];
+  constexpr uint32_t BLK = SL * 128;           // one 32-feature block of a slice
+  const uint32_t kbytes = (uint32_t)ncbk * BLK;
+  const uint32_t stage = kbytes + 4 * BLK;     // k' blocks, then all four v' blocks
+  auto Kt = [&](int st) { return smem + st * stage; };
+  auto Vt = [&](int st) { return smem + st * stage + kbytes; };
+  uint8_t *Wb = smem + SS_STAGES * stage;      // [2][SL x SL] K-major, 2 column blocks each
+  __shared__ uint64_t full[SS_STAGES], empty[SS_STAGES], w_full[2], w_free[2], done;
   __shared__ uint32_t tmem_base;
+  __shared__ double wred[4];
+  __shared__ int abort_flag;
+  volatile int *ab = &abort_flag;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int qd = warp & 3, hf = warp >> 2, L = qd * 32 + lane;
   const int64_t seg = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int64_t bh = b * p.H + h;
   const int64_t s_begin = seg * (int64_t)p.Ls;
@@ -159,172 +162,157 @@ __global__ void __launch_bounds__(NT2, 2) k_seg_state(const __grid_constant__ CU
   const int nsl = (int)cdiv(s_end - s_begin, SL);
   const int kslot = qk_slot(p, h), vslot = v_slot(p, h);
 
-  // thread 0 issues the MMAs; lane 0 of warp 1 / warp 2 loads the k' / v'
-  // slices (two arrivals complete a stage's load phase)
-  const bool ldk = tid == 32, ldv = tid == 64;
-  if (warp == 0) tmem_alloc(&tmem_base, 256);
+  if (warp == 1) tmem_alloc(&tmem_base, 256);
   if (tid == 0) {
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&bar_tma[i], 2);
-      mbar_init(&bar_mma[i], 1);
+    for (int i = 0; i < SS_STAGES; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 1);
     }
+    for (int i = 0; i < 2; ++i) {  // (W buffers)
+      mbar_init(&w_full[i], 32);
+      mbar_init(&w_free[i], 1);
+    }
+    mbar_init(&done, 1);
+    abort_flag = 0;
     fence_mbar_init();
     prefetch_tmap(&tmK);
     prefetch_tmap(&tmV);
   }
+  // v' blocks past dv' are read by the M = 128 MMAs: keep them zero; W is
+  // zero off its diagonal
+  for (int st = 0; st < SS_STAGES; ++st)
+    for (int e = ncbv * (int)BLK / 16 + tid; e < 4 * (int)BLK / 16; e += SS_THREADS)
+      reinterpret_cast<float4 *>(Vt(st))[e] = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int e = tid; e < 2 * 2 * (int)BLK / 16; e += SS_THREADS)
+    reinterpret_cast<float4 *>(Wb)[e] = make_float4(0.f, 0.f, 0.f, 0.f);
+  fence_async_smem();
+  tc_fence_before();
   __syncthreads();
-  int pend[2] = {-1, -1};  // slice in flight per stage (each loader's view)
-  auto issue_tma = [&](int n) {  // the calling loader's half of slice n
-    const int st = n & 1;
-    pend[st] = n;
-    const int row = (int)(b * p.L + s_begin + (int64_t)n * SL);
-    uint8_t *Xt = tiles + st * stage, *Yt = Xt + xbytes;
-    if (ldk) {
-      mbar_expect_tx(&bar_tma[st], xbytes);
-      for (int cb = 0; cb < ncbk; ++cb) tma_load_3d(Xt + cb * 4096, &tmK, &bar_tma[st], cb * 32, kslot, row);
-    } else {
-      mbar_expect_tx(&bar_tma[st], ybytes);
-      for (int cb = 0; cb < ncbv; ++cb) tma_load_3d(Yt + cb * 4096, &tmV, &bar_tma[st], cb * 32, vslot, row);
+  tc_fence_after();
+  const uint32_t tmem = tmem_base;
+  const uint32_t T_D = tmem, T_T = tmem + 128;
+
+  if (warp == 0) {
+    if (lane == 0) {  // producer
+      int last[SS_STAGES];
+      for (int i = 0; i < SS_STAGES; ++i) last[i] = -1;
+      for (int n = 0; n < nsl; ++n) {
+        const int st = n % SS_STAGES, use = n / SS_STAGES;
+        if (use > 0 && !mbar_wait(&empty[st], (use - 1) & 1, ab)) break;
+        const int row = (int)(b * p.L + s_begin + (int64_t)n * SL);
+        mbar_expect_tx(&full[st], kbytes + (uint32_t)ncbv * BLK);
+        for (int cb = 0; cb < ncbk; ++cb) tma_load_3d(Kt(st) + cb * BLK, &tmK, &full[st], cb * 32, kslot, row);
+        for (int cb = 0; cb < ncbv; ++cb) tma_load_3d(Vt(st) + cb * BLK, &tmV, &full[st], cb * 32, vslot, row);
+        last[st] = n;
+        for (int pf = (n == 0 ? SS_STAGES : SS_STAGES + SS_PREFETCH - 1); pf < SS_STAGES + SS_PREFETCH; ++pf) {
+          if (n + pf >= nsl) break;
+          const int prow = (int)(b * p.L + s_begin + (int64_t)(n + pf) * SL);
+          for (int cb = 0; cb < ncbk; ++cb) tma_prefetch_3d(&tmK, cb * 32, kslot, prow);
+          for (int cb = 0; cb < ncbv; ++cb) tma_prefetch_3d(&tmV, cb * 32, vslot, prow);
+        }
+      }
+      // loads still in flight must land before the CTA exits
+      for (int st = 0; st < SS_STAGES; ++st)
+        if (last[st] >= 0) mbar_wait(&full[st], (last[st] / SS_STAGES) & 1);
     }
-  };
-  if (ldk || ldv) {
-    issue_tma(0);
-    if (nsl > 1) issue_tma(1);
-  }
-  // segment total of la: all threads, fp64
-  __shared__ double wsum[8];
-  {
+  } else if (warp == 1) {
+    if (lane == 0) {  // MMA issuer
+      const uint32_t id_t = idesc_tf32(128, SL, 1, 0);       // T^T = v'^T W
+      const uint32_t id_d = idesc_tf32(128, p.dkp, 0, 1);    // D^T += T^T k'
+      // T^T of slice n goes to buffer n & 1, and the D MMAs of slice n - 1 are
+      // issued after the T MMAs of slice n: consecutive MMA groups never wait
+      // for each other's results in tensor memory
+      auto issue_d = [&](int n) {
+        const int st = n % SS_STAGES;
+        const uint64_t dk_ = sdesc_mn(smem_u32(Kt(st)), BLK);
+#pragma unroll
+        for (int kk = 0; kk < SL / 8; ++kk)
+          mma_ts(T_D, T_T + (n & 1) * SL + kk * 8, dk_ + (uint64_t)(kk * 64), id_d, (n > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(&empty[st]);
+      };
+      bool ok = true;
+      for (int n = 0; n < nsl; ++n) {
+        const int st = n % SS_STAGES, use = n / SS_STAGES, wb = n & 1;
+        if (!mbar_wait(&full[st], use & 1, ab)) { ok = false; break; }
+        if (!mbar_wait(&w_full[wb], (n >> 1) & 1, ab)) { ok = false; break; }
+        tc_fence_after();
+        const uint64_t dv_ = sdesc_mn(smem_u32(Vt(st)), BLK);
+        const uint64_t dw = sdesc(smem_u32(Wb + wb * 2 * BLK));
+#pragma unroll
+        for (int kk = 0; kk < SL / 8; ++kk)
+          mma_ss(T_T + wb * SL, dv_ + (uint64_t)(kk * 64), dw + (uint64_t)((kk >> 2) * (BLK >> 4) + (kk & 3) * 2),
+                 id_t, kk > 0 ? 1u : 0u);
+        mma_commit(&w_free[wb]);
+        if (n > 0) issue_d(n - 1);
+      }
+      if (ok && nsl > 0) issue_d(nsl - 1);
+      mma_commit(&done);  // every MMA issued above has completed when this arrives
+      mbar_wait(&done, 0);
+    }
+  } else {  // warps 2-5: weights into W, then the result
+    const int wt = tid - 64, wq = warp & 3;
     double part = 0.0;
-    for (int64_t t = s_begin + tid; t < s_end; t += NT2) part += (double)la[(b * p.L + t) * p.H + h];
+#pragma unroll 8
+    for (int64_t t = s_begin + wt; t < s_end; t += 128) part += (double)la[(b * p.L + t) * p.H + h];
 #pragma unroll
     for (int o = 16; o >= 1; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
-    if (lane == 0) wsum[warp] = part;
+    if (lane == 0) wred[warp - 2] = part;
+    named_sync(1, 128);
+    const double tot = wred[0] + wred[1] + wred[2] + wred[3];
+    if (wt == 0) Aseg[bh * p.nseg + seg] = (float)tot;
+    bool ok = true;
+    if (warp == 2) {  // one warp writes the diagonal: lane l owns tokens 2l, 2l + 1
+      static_assert(SL == 64, "two tokens per lane");
+      double carry = 0.0;
+      auto la_of = [&](int n, int u) {
+        const int64_t t = s_begin + (int64_t)n * SL + u;
+        return (n < nsl && t < s_end) ? (double)la[(b * p.L + t) * p.H + h] : 0.0;
+      };
+      double x0n = la_of(0, 2 * lane), x1n = la_of(0, 2 * lane + 1);  // one slice ahead
+      for (int n = 0; n < nsl; ++n) {
+        const int wb = n & 1;
+        const int64_t t0 = s_begin + (int64_t)n * SL;
+        const int len = (int)imin64(SL, s_end - t0);
+        const double x0 = x0n, x1 = x1n;
+        x0n = la_of(n + 1, 2 * lane);
+        x1n = la_of(n + 1, 2 * lane + 1);
+        double incl = x0 + x1;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const double y = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += y;
+        }
+        const double cs1 = carry + incl, cs0 = cs1 - x1;
+        carry += __shfl_sync(0xffffffffu, incl, 31);
+        const float w0 = 2 * lane < len ? exp2f((float)((REV ? cs0 : tot - cs0) * LOG2E_D)) : 0.f;
+        const float w1 = 2 * lane + 1 < len ? exp2f((float)((REV ? cs1 : tot - cs1) * LOG2E_D)) : 0.f;
+        if (n >= 2 && !mbar_wait(&w_free[wb], ((n >> 1) - 1) & 1, ab)) { ok = false; break; }
+        uint8_t *W = Wb + wb * 2 * BLK;
+        *reinterpret_cast<float *>(W + sw128_off(2 * lane, 2 * lane, SL)) = tf32r(w0);
+        *reinterpret_cast<float *>(W + sw128_off(2 * lane + 1, 2 * lane + 1, SL)) = tf32r(w1);
+        fence_async_smem();
+        mbar_arrive(&w_full[wb]);
+      }
+    }
+    if (ok && mbar_wait(&done, 0, ab)) {
+      tc_fence_after();
+      // D^T in tensor memory: lane j (v' feature), column i (k' feature)
+      const int j = 32 * wq + lane;
+      float *dst = states + (bh * p.nseg + seg) * (int64_t)p.dk * p.dv;
+      for (int c0 = 0; c0 < p.dkp; c0 += 32) {
+        float v[32];
+        tmem_ld32(T_D + ((uint32_t)(32 * wq) << 16) + c0, v);
+        if (j < p.dv) {
+#pragma unroll
+          for (int ii = 0; ii < 32; ++ii)
+            if (c0 + ii < p.dk) dst[(int64_t)(c0 + ii) * p.dv + j] = v[ii];
+        }
+      }
+    }
   }
   tc_fence_before();
   __syncthreads();
-  tc_fence_after();
-  double tot = 0.0;
-#pragma unroll
-  for (int w2 = 0; w2 < 8; ++w2) tot += wsum[w2];
-  const float Af = (float)tot;
-  if (tid == 0) Aseg[bh * p.nseg + seg] = Af;
-  const uint32_t tmem = tmem_base;
-  const uint32_t lb = (uint32_t)(qd * 32) << 16;
-  double carry = 0.0;
-  bool ok = true;
-  // all threads: weights of the 256 tokens from slice n on (one per thread),
-  // continuing the running in-segment prefix (fp64 block scan); each thread's
-  // la value of the next batch is loaded one batch ahead
-  auto la_at = [&](int64_t t) { return t < s_end ? (double)la[(b * p.L + t) * p.H + h] : 0.0; };
-  double la_next = la_at(s_begin + tid);
-  auto batch_weights = [&](int n) {
-    const int64_t t = s_begin + (int64_t)n * SL + tid;
-    double x = la_next;
-    la_next = la_at(t + 8 * SL);
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const double y = __shfl_up_sync(0xffffffffu, x, o);
-      if (lane >= o) x += y;
-    }
-    if (lane == 31) wtot[warp] = x;
-    __syncthreads();
-    double before = carry, all = carry;
-#pragma unroll
-    for (int w2 = 0; w2 < 8; ++w2) {
-      if (w2 < warp) before += wtot[w2];
-      all += wtot[w2];
-    }
-    const float csf = (float)(before + x);
-    scb[tid] = t < s_end ? expf(REV ? csf : Af - csf) : 0.f;
-    carry = all;
-    __syncthreads();
-  };
-
-  for (int n = 0; n < nsl; ++n) {
-    const int st = n & 1;
-    const int64_t t0 = s_begin + (int64_t)n * SL;
-    const int len = (int)imin64(SL, s_end - t0);
-    if ((n & 7) == 0) batch_weights(n);
-    const float *sc = scb + (n & 7) * SL;
-    const uint8_t *Xt = tiles + st * stage, *Yt = Xt + xbytes;
-    uint8_t *Bs = Bb + st * bbytes;
-    ok = mbar_wait(&bar_tma[st], (n >> 1) & 1) && ok;
-    if (ok) pend[st] = -1;
-    if (n >= 2) ok = mbar_wait(&bar_mma[st], ((n >> 1) - 1) & 1) && ok;  // slice n-2 done
-    if (__syncthreads_or(!ok)) break;
-    tc_fence_after();
-    {  // A operand: k'^T, lane = feature, tokens [16 hf, 16 hf + 16)
-      float v[16];
-#pragma unroll
-      for (int uu = 0; uu < 16; ++uu) {
-        const int u = hf * 16 + uu;
-        v[uu] = (L < p.dk && u < len) ? tf32r(*(const float *)(Xt + sw128_off(u, L, SL))) : 0.f;
-      }
-      tmem_st16(tmem + lb + 128 + st * 32 + hf * 16, v);
-    }
-    if (L < p.dvn) {  // B operand: (sc v')^T, row = feature
-#pragma unroll
-      for (int uu = 0; uu < 16; uu += 4) {
-        const int u = hf * 16 + uu;
-        float f[4];
-#pragma unroll
-        for (int r = 0; r < 4; ++r)
-          f[r] = L < p.dv ? tf32r(*(const float *)(Yt + sw128_off(u + r, L, SL)) * sc[u + r]) : 0.f;
-        *reinterpret_cast<float4 *>(Bs + sw128_off(L, u, p.dvn)) = make_float4(f[0], f[1], f[2], f[3]);
-      }
-    }
-    tmem_st_wait();
-    fence_async_smem();
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    if ((ldk || ldv) && n + 2 < nsl) issue_tma(n + 2);  // this stage's tiles are consumed
-    if (tid == 0) {
-      const uint32_t bsm = smem_u32(Bs);
-      const uint32_t id = idesc_tf32(128, p.dvn);
-#pragma unroll
-      for (int kk = 0; kk < SL / 8; ++kk)
-        mma_ts(tmem, tmem + 128 + st * 32 + kk * 8, sdesc(bsm + kk * 32), id, (n > 0 || kk > 0) ? 1u : 0u);
-      mma_commit(&bar_mma[st]);
-    }
-  }
-  if (ok) {
-    for (int n = (nsl >= 2 ? nsl - 2 : 0); n < nsl; ++n) ok = mbar_wait(&bar_mma[n & 1], (n >> 1) & 1) && ok;
-  }
-  const bool fail = __syncthreads_or(!ok);
-  tc_fence_after();
-  if (!fail) {
-    // stage D [dk x dv] through the (now idle) tile buffers in the swizzled
-    // column-block layout, then write it out coalesced
-    uint8_t *Ds = tiles;  // needs dk * dvp * 4 <= 2 * stage bytes
-    const int dkr = rup(p.dk, 8);
-    for (int c0 = hf * 64; c0 < hf * 64 + 64; c0 += 32) {
-      if (c0 >= p.dvn) break;  // warp-uniform
-      float v[32];
-      tmem_ld32(tmem + lb + c0, v);
-      if (L < p.dk) {
-#pragma unroll
-        for (int jj = 0; jj < 32; jj += 4)
-          if (c0 + jj < p.dvp)
-            *reinterpret_cast<float4 *>(Ds + sw128_off(L, c0 + jj, dkr)) =
-                make_float4(v[jj], v[jj + 1], v[jj + 2], v[jj + 3]);
-      }
-    }
-    __syncthreads();
-    float *dst = states + (bh * p.nseg + seg) * (int64_t)p.dk * p.dv;
-    const int n4 = p.dk * p.dv / 4;
-    for (int m = tid; m < n4; m += NT2) {
-      const int e = 4 * m, i = e / p.dv, j = e - i * p.dv;
-      *reinterpret_cast<float4 *>(dst + e) = *reinterpret_cast<const float4 *>(Ds + sw128_off(i, j, dkr));
-    }
-  } else if (ldk || ldv) {
-    // tiles of up to two slices may still be in flight: wait for them
-    for (int st = 0; st < 2; ++st)
-      if (pend[st] >= 0) mbar_wait(&bar_tma[st], (pend[st] >> 1) & 1);
-  }
-  tc_fence_before();
-  __syncthreads();
-  if (warp == 0) tmem_dealloc(tmem, 256);
+  if (warp == 1) tmem_dealloc(tmem, 256);
 }
 
 // ===========================================================================
@@ -397,449 +385,489 @@ __global__ void __launch_bounds__(NTH) k_seg_scan(float *__restrict__ st,
 // ===========================================================================
 // Walk over the chunks of one segment (left to right, or right to left when
 // REV) with the running state resident in tensor memory.  grid (nseg, H, B),
-// 256 threads: thread (quarter q, lane l, half f) owns tensor-memory lane
-// 32q + l and column half f of each 64-column block; two CTAs per SM.
+// one CTA per SM, 384 threads in warp-specialised roles:
+//   warp 0      TMA producer: q', k' (K-major) and v' (MN-major) tiles of each
+//               chunk into a two-stage ring
+//   warp 1      state-chain MMAs of chunk c:  X = S^T q'^T (inter term),
+//               Y = v'^T P^T (intra term), S^T += v'^T (w k') (update)
+//   warp 2      score MMAs  Sc = q' k'^T  of the next chunk
+//   warp 3      decay factors of each chunk (fp64 in-chunk prefix of la, the
+//               lazy state scale) into a four-slot ring
+//   warps 4-7   mask: P = D o Sc into shared memory (K-major), and k' turned
+//               in place into w k' (MN-major, scaled by the state weights)
+//   warps 8-11  epilogue: out'_t = f_t X_t + Y_t to global memory (atomic
+//               add over a group's heads when ATOMIC), dcs_t = y_t . f_t X_t
+//               when SPLIT, and the occasional explicit state rescale
+// so the next chunk's scores and mask overlap the current chunk's products.
 //
-// Tensor memory (256 columns):
-//   X   [0,64)    S = q' k'^T (M = 64: rows 16q..16q+15 in lanes 32q..), then
-//                 out'^T (lane j = feature, column = token)
-//   VT  [64,128)  v'^T of the chunk (A operand)
-//   HT  [128,256) running state, transposed (A operand): lane j, column i
-// Shared memory: q' tile (scaled in place to the B operand of the inter term),
-// k' tile (then reused for w * k'^T, the B operand of the state update), v'
-// tile (then reused for P).
-// The entering state is read from Hseg as [dk x dv] (or [dv x dk] when
-// HT_SRC_T).
-template <bool REV, bool ATOMIC>
-__global__ void __launch_bounds__(NT2, 2) k_walk(const __grid_constant__ CUtensorMap tmQ,
+// Tensor memory (512 columns): S^T [0,128) (lane j = v' feature, column i =
+// k' feature), Sc [128,256) two 64-column buffers (M = 64: row r in lane
+// 32(r/16) + r%16), X [256,384) and Y [384,512) two buffers each (lane j,
+// column = token).  Shared memory per stage: q' tile (128-byte swizzle,
+// K-major), k' tile (the same, later w k' in the 32-byte-atom layout),
+// v' tile (32-byte-atom layout, all four 32-feature blocks so that the M = 128
+// MMAs read zeros past dv'); one P tile [64 x 64].
+//
+// The stored state is kept as Hs with the true state = alpha * Hs.  While
+// alpha stays in [2^-40, 2^40] a chunk's decay is folded into alpha (the
+// inter term takes f_t * alpha, the update w / alpha'), so no pass over the
+// state runs; otherwise the epilogue warps rescale Hs to the true decayed state
+// between the chunk's inter product and its update, and alpha returns to 1.
+//
+// The entering state is read from Hseg as [dk' x dv'] (or [dv' x dk'] when
+// hseg_t).
+constexpr int WT = 384;
+constexpr int kPrefetch = 3;  // chunks ahead of the one being loaded, prefetched into L2
+struct Fac {     // decay factors of one chunk, walk order
+  float cs2[C];  // in-chunk inclusive prefix of la, times log2(e) (0 past the end)
+  float qf[C];   // inter-term factor of query row t times the state scale
+  float kw[C];   // state-update weight of key row s over the new state scale
+  float an;      // the rescale factor (state scale times the chunk's decay)
+  int rescale;   // 1: rescale the stored state before this chunk's update
+};
+struct WalkOut {
+  float *out;       // out'[b, t, slot, 0:dv']
+  int out_slots;    // H (slot = head) or G (slot = group, summed by atomic adds)
+  const float *y;   // SPLIT: y[b, t, h / hpg, 0:dv']
+  float *dcs;       // SPLIT: dcs[b, t, h] = y_t . (inter-chunk part of out'_t)
+};
+
+template <bool REV, bool ATOMIC, bool SPLIT>
+__global__ void __launch_bounds__(WT, 1) k_walk(const __grid_constant__ CUtensorMap tmQ,
                                               const __grid_constant__ CUtensorMap tmK,
                                               const __grid_constant__ CUtensorMap tmV,
-                                              const __grid_constant__ CUtensorMap tmO,
                                               const float *__restrict__ la,
                                               const float *__restrict__ Hseg, int hseg_t,
-                                              OutArgs oa, PassGeo p) {
+                                              WalkOut oa, PassGeo p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t *smem = smem_align1024(smem_raw);
   const int ncbk = p.dkp / 32, ncbv = p.dvp / 32;
-  const uint32_t vbytes = (uint32_t)max(ncbv * 8192, 16384);
-  uint8_t *Qb = smem;
-  uint8_t *Kb = Qb + ncbk * 8192;
-  uint8_t *Vb = Kb + ncbk * 8192;
-  // per-chunk factors, double-buffered: in-chunk prefix of la times log2(e),
-  // exp(cs), exp(A - cs); computed one chunk ahead by warp 4
-  float *cs2b = (float *)(Vb + vbytes);  // [2][64]
-  float *ewb = cs2b + 2 * C, *wwb = ewb + 2 * C;
-  float *red = wwb + 2 * C;  // [4][64]
-  float *scr = red + 4 * C;  // [64] scratch of warp 4
-  __shared__ uint64_t bar_tma, bar_s, bar_i, bar_o, bar_h;
+  constexpr uint32_t BLK = C * 128;  // one 32-feature block of a 64-row tile
+  const uint32_t qkbytes = (uint32_t)ncbk * BLK;
+  const uint32_t stage = 2 * qkbytes + 4 * BLK;
+  auto Qs = [&](int st) { return smem + st * stage; };
+  auto Ks = [&](int st) { return smem + st * stage + qkbytes; };
+  auto Vs = [&](int st) { return smem + st * stage + 2 * qkbytes; };
+  uint8_t *P = smem + 2 * stage;
+  Fac *fac = reinterpret_cast<Fac *>(P + 2 * BLK);
+  float *red = reinterpret_cast<float *>(fac + 4);  // [4][64]
+
+  __shared__ uint64_t full[2], empty[2], s_full[2], s_empty[2], xy_full[2], x_empty[2];
+  // The mask signals P (p_full) before it turns k' into w k' (wk_full, one
+  // barrier per stage), so that the intra-term MMAs issue during the turn
+  __shared__ uint64_t p_full, p_empty, rescaled, st_init, drain_s, drain_m, wk_full[2];
+  __shared__ uint64_t fac_full[4], fac_empty[4];
   __shared__ uint32_t tmem_base;
-  __shared__ float a_chunk[2];
+  __shared__ int abort_flag;
+  volatile int *ab = &abort_flag;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int qd = warp & 3, hf = warp >> 2, L = qd * 32 + lane;
   const int64_t seg = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int64_t bh = b * p.H + h;
   const int64_t s_begin = seg * (int64_t)p.Ls;
   const int64_t s_end = imin64(p.L, s_begin + p.Ls);
   const int nc = (int)cdiv(s_end - s_begin, C);
   const int kslot = qk_slot(p, h), vslot = v_slot(p, h);
-  const int dk = p.dk, dv = p.dv, dkn = p.dkn;
-  const int oslot = oa.out_slots == p.H ? (int)h : (int)(h / p.hpg);
-  constexpr float LOG2E = 1.4426950408889634f;
+  const int dk = p.dk, dv = p.dv;
+  auto chunk_of = [&](int ci) { return REV ? nc - 1 - ci : ci; };
 
-  // Serial issue work is spread over warps: thread 0 issues the MMAs, lane 0
-  // of warps 1, 2, 3 the q', v' and k' tile loads (three arrivals complete a
-  // load phase), warp 4 computes the next chunk's decay factors.
-  const bool ldq = tid == 32, ldv = tid == 64, ldk = tid == 96;
-  if (warp == 0) tmem_alloc(&tmem_base, 256);
+  if (warp == 1) tmem_alloc(&tmem_base, 512);
   if (tid == 0) {
-    mbar_init(&bar_tma, 3);
-    mbar_init(&bar_s, 1);
-    mbar_init(&bar_i, 1);
-    mbar_init(&bar_o, 1);
-    mbar_init(&bar_h, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 1);
+      mbar_init(&s_full[i], 1);
+      mbar_init(&s_empty[i], 128);
+      mbar_init(&xy_full[i], 1);
+      mbar_init(&x_empty[i], 128);
+      mbar_init(&wk_full[i], 128);
+    }
+    mbar_init(&p_full, 128);
+    mbar_init(&p_empty, 1);
+    mbar_init(&rescaled, 128);
+    mbar_init(&st_init, 128);
+    mbar_init(&drain_s, 1);
+    mbar_init(&drain_m, 1);
+    for (int i = 0; i < 4; ++i) {
+      mbar_init(&fac_full[i], 32);
+      mbar_init(&fac_empty[i], 257);
+    }
+    abort_flag = 0;
     fence_mbar_init();
     prefetch_tmap(&tmQ);
     prefetch_tmap(&tmK);
     prefetch_tmap(&tmV);
   }
+  // v' blocks past dv' are read by the M = 128 MMAs: keep them zero
+  for (int st = 0; st < 2; ++st)
+    for (int e = ncbv * (int)BLK / 16 + tid; e < 4 * (int)BLK / 16; e += WT)
+      reinterpret_cast<float4 *>(Vs(st))[e] = make_float4(0.f, 0.f, 0.f, 0.f);
+  fence_async_smem();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_base;
-  const uint32_t lb = (uint32_t)(qd * 32) << 16;
-  int tma_pending = -1;  // barrier phase of this loader's loads not yet waited for
-  // chunk c's tiles; `use` counts the barrier's phases (chunks in walk order).
-  // Each loader thread arrives once per phase with its own byte count; the
-  // k' tile may be issued later than the q' and v' tiles.
-  auto tma_q = [&](int c, int use) {
-    const int row = (int)(b * p.L + s_begin + (int64_t)c * C);
-    mbar_expect_tx(&bar_tma, (uint32_t)ncbk * 8192);
-    for (int cb = 0; cb < ncbk; ++cb) tma_load_3d(Qb + cb * 8192, &tmQ, &bar_tma, cb * 32, kslot, row);
-    tma_pending = use;
-  };
-  auto tma_v = [&](int c, int use) {
-    const int row = (int)(b * p.L + s_begin + (int64_t)c * C);
-    mbar_expect_tx(&bar_tma, (uint32_t)ncbv * 8192);
-    for (int cb = 0; cb < ncbv; ++cb) tma_load_3d(Vb + cb * 8192, &tmV, &bar_tma, cb * 32, vslot, row);
-    tma_pending = use;
-  };
-  auto tma_k = [&](int c, int use) {
-    const int row = (int)(b * p.L + s_begin + (int64_t)c * C);
-    mbar_expect_tx(&bar_tma, (uint32_t)ncbk * 8192);
-    for (int cb = 0; cb < ncbk; ++cb) tma_load_3d(Kb + cb * 8192, &tmK, &bar_tma, cb * 32, kslot, row);
-    tma_pending = use;
-  };
-  auto issue_first_loads = [&]() {
-    const int c0 = REV ? nc - 1 : 0;
-    if (ldq) tma_q(c0, 0);
-    if (ldv) tma_v(c0, 0);
-    if (ldk) tma_k(c0, 0);
-  };
+  const uint32_t T_ST = tmem, T_SC = tmem + 128, T_X = tmem + 256, T_Y = tmem + 384;
 
-  if (!hseg_t) issue_first_loads();
-
-  // warp 4: the factors of chunk c into buffer bf, from la values loaded one
-  // chunk ahead (la_x0, la_x1: this lane's two tokens of chunk c)
-  double la_x0 = 0.0, la_x1 = 0.0;
-  auto la_prefetch = [&](int c) {
-    const int64_t t0 = s_begin + (int64_t)c * C;
-    const int len = (int)imin64(C, s_end - t0);
-    const float *lp = la + (b * p.L + t0) * p.H + h;
-    la_x0 = (2 * lane < len) ? (double)lp[(int64_t)(2 * lane) * p.H] : 0.0;
-    la_x1 = (2 * lane + 1 < len) ? (double)lp[(int64_t)(2 * lane + 1) * p.H] : 0.0;
-  };
-  auto chunk_factors = [&](int c, int bf) {
-    const int64_t t0 = s_begin + (int64_t)c * C;
-    const int len = (int)imin64(C, s_end - t0);
-    const double tot = warp_cumsum64_regs(la_x0, la_x1, len, 0.0, scr);
-    __syncwarp();
-    const float tot2 = (float)tot * LOG2E;
-    for (int t = lane; t < C; t += 32) {
-      const float x = t < len ? scr[t] * LOG2E : 0.f;
-      cs2b[bf * C + t] = x;
-      ewb[bf * C + t] = t < len ? ex2f(x) : 0.f;
-      wwb[bf * C + t] = t < len ? ex2f(tot2 - x) : 0.f;
-    }
-    if (lane == 0) a_chunk[bf] = ex2f(tot2);
-    __syncwarp();
-  };
-  if (warp == 4) {
-    la_prefetch(REV ? nc - 1 : 0);
-    chunk_factors(REV ? nc - 1 : 0, 0);
-  }
-
-  {  // running state, transposed: lane j, column i = state[i][j]
-    const float *H0 = Hseg + (bh * p.nseg + seg) * (int64_t)dk * dv;
-    if (hseg_t) {
-      // the entering state is stored transposed ([dv x dk]): read it coalesced
-      // into the idle tile buffers ([dv rows x (dk + 1)]), then by rows
-      float *Ts = reinterpret_cast<float *>(Qb);
-      const int n = dv * dk;
-      for (int e = tid; e < n; e += NT2) {
-        const int r = e / dk, cc = e - r * dk;
-        Ts[r * (dk + 1) + cc] = H0[e];
-      }
-      __syncthreads();
-      for (int c0 = hf * 64; c0 < hf * 64 + 64 && c0 < rup(dk, 32); c0 += 32) {
-        float hv[32];
-#pragma unroll
-        for (int ii = 0; ii < 32; ++ii) {
-          const int i = c0 + ii;
-          hv[ii] = (L < dv && i < dk) ? Ts[L * (dk + 1) + i] : 0.f;
+  if (warp == 0) {
+    // ---- TMA producer ------------------------------------------------------
+    if (lane == 0) {
+      int last[2] = {-1, -1};
+      for (int ci = 0; ci < nc; ++ci) {
+        const int st = ci & 1;
+        if (ci >= 2 && !mbar_wait(&empty[st], ((ci >> 1) - 1) & 1, ab)) break;
+        const int row = (int)(b * p.L + s_begin + (int64_t)chunk_of(ci) * C);
+        mbar_expect_tx(&full[st], 2 * qkbytes + (uint32_t)ncbv * BLK);
+        for (int cb = 0; cb < ncbk; ++cb) {
+          tma_load_3d(Qs(st) + cb * BLK, &tmQ, &full[st], cb * 32, kslot, row);
+          tma_load_3d(Ks(st) + cb * BLK, &tmK, &full[st], cb * 32, kslot, row);
         }
-        tmem_st32(tmem + lb + 128 + c0, hv);
-      }
-      __syncthreads();  // the tile buffers are about to receive the first loads
-      issue_first_loads();
-    } else {
-      for (int c0 = hf * 64; c0 < hf * 64 + 64 && c0 < rup(dk, 32); c0 += 32) {
-        float hv[32];
-#pragma unroll
-        for (int ii = 0; ii < 32; ++ii) {
-          const int i = c0 + ii;
-          hv[ii] = (L < dv && i < dk) ? H0[(int64_t)i * dv + L] : 0.f;
-        }
-        tmem_st32(tmem + lb + 128 + c0, hv);
-      }
-    }
-    tmem_st_wait();
-  }
-
-  bool ok = true;
-  const bool split = oa.dcs != nullptr;
-  // The resident state is kept as Hs with the true state = alpha * Hs.  While
-  // alpha stays in [2^-40, 2^40] a chunk's decay is folded into alpha (the
-  // inter term scales q' by alpha, the update scales w k' by 1 / alpha), so
-  // the update MMA issues with the output MMAs and no rescale pass runs;
-  // otherwise the threads rescale Hs explicitly and alpha returns to 1.
-  float alpha = 1.f;
-  int hphase = 0;  // completions of bar_h so far (the explicit path only)
-  // HT += v'^T (w k')   (M = dv lanes, N = dkn, K = 64 tokens); thread 0
-  auto issue_update = [&]() {
-    const uint32_t kwa = smem_u32(Kb);
-    const uint32_t id = idesc_tf32(128, dkn);
-#pragma unroll
-    for (int kk = 0; kk < C / 8; ++kk)
-      mma_ts(tmem + 128, tmem + 64 + kk * 8, sdesc(kwa + (kk >> 2) * (dkn * 128) + (kk & 3) * 32),
-             id, 1u);
-  };
-  for (int ci = 0; ci < nc; ++ci) {
-    const int c = REV ? nc - 1 - ci : ci;
-    const int64_t t0 = s_begin + (int64_t)c * C;
-    const int len = (int)imin64(C, s_end - t0);
-    const int cnext = REV ? c - 1 : c + 1;
-    const int fb = ci & 1;
-    const float *cs2 = cs2b + fb * C, *ew = ewb + fb * C, *ww = wwb + fb * C;
-    if (warp == 4 && ci + 1 < nc) la_prefetch(cnext);  // used by chunk_factors below
-    ok = mbar_wait(&bar_tma, ci & 1) && ok;
-    if (ok) tma_pending = -1;
-    // S = q' k'^T (M = 64, N = 64, K = dk), issued as soon as the tiles are
-    // in, before the CTA barrier: the issuing warp then starts its passes
-    // with the others instead of 16 MMA issues behind them.  (The previous
-    // chunk's output was read from these columns before its final barrier.)
-    if (tid == 0 && ok) {
-      tc_fence_after();
-      const uint32_t qa = smem_u32(Qb), ka = smem_u32(Kb);
-      const uint32_t id = idesc_tf32(64, 64);
-      for (int kk = 0; kk < dk / 8; ++kk) {
-        const uint32_t off = (kk >> 2) * 8192 + (kk & 3) * 32;
-        mma_ss(tmem, sdesc(qa + off), sdesc(ka + off), id, kk > 0 ? 1u : 0u);
-      }
-      mma_commit(&bar_s);
-    }
-    tc_fence_before();
-    if (__syncthreads_or(!ok)) break;
-    tc_fence_after();
-    // inter-term factor of a query row, state-update weight of a key column
-    const float *interf = REV ? ww : ew;
-    const float *statew = REV ? ew : ww;
-    const float a_c = a_chunk[fb], an = alpha * a_c;
-    const bool lazy = a_c >= 0x1p-30f && an >= 0x1p-40f && an <= 0x1p40f;
-    const float kscale = lazy ? 1.f / an : 1.f;
-    {  // v'^T into tensor memory: lane = feature, tokens [32 hf, 32 hf + 32)
-      float v[32];
-#pragma unroll
-      for (int uu = 0; uu < 32; ++uu) {
-        const int u = hf * 32 + uu;
-        v[uu] = (L < dv && u < len) ? tf32r(*(const float *)(Vb + sw128_off(u, L, C))) : 0.f;
-      }
-      tmem_st32(tmem + lb + 64 + hf * 32, v);
-    }
-    float kw[32];  // w_u * k'[u][L], tokens [32 hf, 32 hf + 32)
-    {
-      const float4 *sw4 = reinterpret_cast<const float4 *>(statew + hf * 32);
-#pragma unroll
-      for (int u4 = 0; u4 < 8; ++u4) {
-        const float4 wv = sw4[u4];
-        const float wq[4] = {wv.x, wv.y, wv.z, wv.w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int uu = 4 * u4 + e, u = hf * 32 + uu;
-          kw[uu] = (L < dk) ? tf32r(*(const float *)(Kb + sw128_off(u, L, C)) * (wq[e] * kscale)) : 0.f;
-        }
-      }
-    }
-    ok = mbar_wait(&bar_s, ci & 1) && ok;
-    tc_fence_after();
-    float sr[32];
-    tmem_ld32(tmem + lb + hf * 32, sr);
-    tc_fence_before();
-    __syncthreads();  // every read of the v' and k' tiles and of S is done
-    {  // P into the v' tile's space.  S row r sits in lane r % 16 (M = 64); the
-       // lane 16 above it takes the upper 16 of the warp's 32 tokens
-      const int r = qd * 16 + (lane & 15), up = lane >> 4;
-      const int ub = hf * 32 + 16 * up;  // first token of this lane's 16
-      float s16[16];
-#pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const float hi = __shfl_sync(0xffffffffu, sr[16 + i], lane & 15);
-        s16[i] = up ? hi : sr[i];
-      }
-      const float cr = cs2[r];
-      uint8_t *P = Vb;
-#pragma unroll
-      for (int uu = 0; uu < 16; uu += 4) {
-        float f[4];
-        const float4 c4 = *reinterpret_cast<const float4 *>(cs2 + ub + uu);
-        const float cu[4] = {c4.x, c4.y, c4.z, c4.w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int u = ub + uu + e;
-          const bool valid = r < len && u < len && (REV ? u >= r : u <= r);
-          f[e] = valid ? tf32r(ex2f(REV ? cu[e] - cr : cr - cu[e]) * s16[uu + e]) : 0.f;
-        }
-        *reinterpret_cast<float4 *>(P + sw128_off(r, ub + uu, C)) = make_float4(f[0], f[1], f[2], f[3]);
-      }
-    }
-    if (L < dkn) {  // w * k'^T into the k' tile's space (B operand, dkn rows)
-#pragma unroll
-      for (int uu = 0; uu < 32; uu += 4)
-        *reinterpret_cast<float4 *>(Kb + sw128_off(L, hf * 32 + uu, dkn)) =
-            make_float4(kw[uu], kw[uu + 1], kw[uu + 2], kw[uu + 3]);
-    }
-    {  // q' rows scaled by the inter-term factor, in place (4 threads per row)
-      const int r = tid & 63, part = tid >> 6;
-      const float e = interf[r] * alpha;
-      const int cols = p.dkp / 4;
-      for (int col = part * cols; col < (part + 1) * cols; col += 4) {
-        float4 *q4 = reinterpret_cast<float4 *>(Qb + sw128_off(r, col, C));
-        float4 f = *q4;
-        f.x = tf32r(f.x * e); f.y = tf32r(f.y * e); f.z = tf32r(f.z * e); f.w = tf32r(f.w * e);
-        *q4 = f;
-      }
-    }
-    tmem_st_wait();
-    fence_async_smem();
-    tc_fence_before();
-    if (__syncthreads_or(!ok)) break;
-    tc_fence_after();
-    if (tid == 0) {  // out'^T = HT (f q')^T  [+ v'^T P^T]
-      const uint32_t qa = smem_u32(Qb), pa = smem_u32(Vb);
-      const uint32_t id = idesc_tf32(128, 64);
-      for (int kk = 0; kk < dk / 8; ++kk)
-        mma_ts(tmem, tmem + 128 + kk * 8, sdesc(qa + (kk >> 2) * 8192 + (kk & 3) * 32), id,
-               kk > 0 ? 1u : 0u);
-      if (split) {
-        mma_commit(&bar_i);
-      } else {
-#pragma unroll
-        for (int kk = 0; kk < C / 8; ++kk)
-          mma_ts(tmem, tmem + 64 + kk * 8, sdesc(pa + (kk >> 2) * 8192 + (kk & 3) * 32), id, 1u);
-        if (lazy) issue_update();
-        mma_commit(&bar_o);
-      }
-    }
-    if (warp == 4 && ci + 1 < nc) chunk_factors(cnext, fb ^ 1);
-    if (split) {
-      // dcs[t] = y_t . (inter-chunk part of out'_t), reduced over the 128 lanes
-      float yv[32];
-      {
-        const int64_t ldy = (int64_t)(p.H / p.hpg) * dv;
-        const float *ys = oa.y + ((b * p.L + t0) * (p.H / p.hpg) + h / p.hpg) * (int64_t)dv + L;
-#pragma unroll
-        for (int tt = 0; tt < 32; ++tt) {
-          const int t = hf * 32 + tt;
-          yv[tt] = (L < dv && t < len) ? ys[t * ldy] : 0.f;
-        }
-      }
-      ok = mbar_wait(&bar_i, ci & 1) && ok;
-      tc_fence_after();
-      float o[32];
-      tmem_ld32(tmem + lb + hf * 32, o);
-      // every thread has its inter part: let the intra MMA accumulate on top
-      // while the dot products are reduced
-      tc_fence_before();
-      __syncthreads();
-      tc_fence_after();
-      if (tid == 0) {  // + v'^T P^T
-        const uint32_t pa = smem_u32(Vb);
-        const uint32_t id = idesc_tf32(128, 64);
-#pragma unroll
-        for (int kk = 0; kk < C / 8; ++kk)
-          mma_ts(tmem, tmem + 64 + kk * 8, sdesc(pa + (kk >> 2) * 8192 + (kk & 3) * 32), id, 1u);
-        if (lazy) issue_update();
-        mma_commit(&bar_o);
-      }
-#pragma unroll
-      for (int tt = 0; tt < 32; ++tt) o[tt] *= yv[tt];
-#pragma unroll
-      for (int off = 16, n = 32; off >= 1; off >>= 1, n >>= 1) {
-        const bool up = (lane & off) != 0;
-#pragma unroll
-        for (int k2 = 0; k2 < n / 2; ++k2) {
-          const float mine = up ? o[n / 2 + k2] : o[k2];
-          const float send = up ? o[k2] : o[n / 2 + k2];
-          o[k2] = mine + __shfl_xor_sync(0xffffffffu, send, off);
-        }
-      }
-      red[qd * C + hf * 32 + lane] = o[0];
-      __syncthreads();
-      if (tid < len)
-        oa.dcs[(b * p.L + t0 + tid) * p.H + h] = red[tid] + red[C + tid] + red[2 * C + tid] + red[3 * C + tid];
-    }
-    ok = mbar_wait(&bar_o, ci & 1) && ok;
-    tc_fence_after();
-    // q' and v' tiles are free now (and k' too when the update ran): next loads.
-    // A full chunk's output is staged in the v' tile and stored by TMA first,
-    // so its next v' tile is loaded after that store has read the buffer.
-    const bool staged = len == C;
-    if (ok && ci + 1 < nc) {
-      if (ldq) tma_q(cnext, ci + 1);
-      if (ldv && !staged) tma_v(cnext, ci + 1);
-      if (ldk && lazy) tma_k(cnext, ci + 1);
-    }
-    {
-      float o[32];
-      tmem_ld32(tmem + lb + hf * 32, o);
-      if (staged) {  // out'[t][L] into the v' tile, in the layout a load of tmO gives
-        if (L < p.dvp) {
-#pragma unroll
-          for (int tt = 0; tt < 32; ++tt)
-            *reinterpret_cast<float *>(Vb + sw128_off(hf * 32 + tt, L, C)) = o[tt];
-        }
-      } else if (L < dv) {
-        const int64_t ld = (int64_t)oa.out_slots * dv;
-        float *os = oa.out + ((b * p.L + t0) * oa.out_slots + oslot) * (int64_t)dv + L;
-#pragma unroll
-        for (int tt = 0; tt < 32; ++tt) {
-          const int t = hf * 32 + tt;
-          if (t < len) {
-            if (ATOMIC) atomicAdd(os + t * ld, o[tt]);
-            else os[t * ld] = o[tt];
+        for (int cb = 0; cb < ncbv; ++cb) tma_load_3d(Vs(st) + cb * BLK, &tmV, &full[st], cb * 32, vslot, row);
+        last[st] = ci;
+        // Only two stages fit in shared memory, so the tiles of chunk ci + 2
+        // are requested when chunk ci is done with its stage; prefetching the
+        // chunks after that into L2 keeps more bytes in flight than the smem
+        // ring holds and turns those loads into L2 hits.
+        for (int pf = (ci == 0 ? 1 : kPrefetch); pf <= kPrefetch; ++pf) {
+          if (ci + pf >= nc) break;
+          const int prow = (int)(b * p.L + s_begin + (int64_t)chunk_of(ci + pf) * C);
+          for (int cb = 0; cb < ncbk; ++cb) {
+            tma_prefetch_3d(&tmQ, cb * 32, kslot, prow);
+            tma_prefetch_3d(&tmK, cb * 32, kslot, prow);
           }
+          for (int cb = 0; cb < ncbv; ++cb) tma_prefetch_3d(&tmV, cb * 32, vslot, prow);
         }
       }
+      for (int st = 0; st < 2; ++st)  // loads in flight must land before the CTA exits
+        if (last[st] >= 0) mbar_wait(&full[st], (last[st] >> 1) & 1);
     }
-    if (staged) {
-      fence_async_smem();
-      __syncthreads();
-      if (ldv) {  // store (or add, for a group's heads) the chunk's output rows
-        const int row = (int)(b * p.L + t0);
-        for (int cb = 0; cb < ncbv; ++cb) {
-          if (ATOMIC) tma_reduce_add_3d(&tmO, Vb + cb * 8192, cb * 32, oslot, row);
-          else tma_store_3d(&tmO, Vb + cb * 8192, cb * 32, oslot, row);
-        }
-        bulk_commit_group();
-        bulk_wait_read_all();
-        if (ok && ci + 1 < nc) tma_v(cnext, ci + 1);
-      }
-    }
-    if (lazy) {
-      alpha = an;
-    } else {
-      // Hs <- alpha exp(A_c) Hs (the true state, decayed), then the update
-      for (int c0 = hf * 64; c0 < hf * 64 + 64 && c0 < rup(dk, 32); c0 += 32) {
-        float hv[32];
-        tmem_ld32(tmem + lb + 128 + c0, hv);
+  } else if (warp == 1) {
+    // ---- state-chain MMAs ----------------------------------------------------
+    if (lane == 0) {
+      const uint32_t id_x = idesc_tf32(128, 64), id_y = idesc_tf32(128, 64, 1, 0);
+      const uint32_t id_u = idesc_tf32(128, p.dkp, 1, 1);  // N a whole number of 32-wide atoms
+      const uint64_t dp = sdesc(smem_u32(P));
+      int nres = 0;
+      if (mbar_wait(&st_init, 0, ab)) {
+        for (int ci = 0; ci < nc; ++ci) {
+          const int st = ci & 1, xb = ci & 1, slot = ci & 3;
+          if (!mbar_wait(&full[st], (ci >> 1) & 1, ab)) break;
+          if (ci >= 2 && !mbar_wait(&x_empty[xb], ((ci >> 1) - 1) & 1, ab)) break;
+          tc_fence_after();
+          // descriptors advance by adds in 16-byte units: K-major K steps are
+          // 32 B inside a 128-byte row and BLK between column blocks, MN-major
+          // K steps are 8 rows (1024 B)
+          const uint64_t dq = sdesc(smem_u32(Qs(st))), dkm = sdesc_mn(smem_u32(Ks(st)), BLK);
+          const uint64_t dvm = sdesc_mn(smem_u32(Vs(st)), BLK);
 #pragma unroll
-        for (int ii = 0; ii < 32; ++ii) hv[ii] *= an;
-        tmem_st32(tmem + lb + 128 + c0, hv);
+          for (int kk = 0; kk < 16; ++kk)  // X = S^T q'^T
+            if (kk < dk / 8)
+              mma_ts(T_X + xb * 64, T_ST + kk * 8, dq + (uint64_t)((kk >> 2) * (BLK >> 4) + (kk & 3) * 2),
+                     id_x, kk > 0 ? 1u : 0u);
+          if (!mbar_wait(&p_full, ci & 1, ab)) break;  // P is in place
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < C / 8; ++kk)  // Y = v'^T P^T
+            mma_ss(T_Y + xb * 64, dvm + (uint64_t)(kk * 64), dp + (uint64_t)((kk >> 2) * (BLK >> 4) + (kk & 3) * 2),
+                   id_y, kk > 0 ? 1u : 0u);
+          mma_commit(&xy_full[xb]);
+          mma_commit(&p_empty);
+          if (!mbar_wait(&fac_full[slot], (ci >> 2) & 1, ab)) break;
+          const int resc = fac[slot].rescale;
+          mbar_arrive(&fac_empty[slot]);
+          if (!mbar_wait(&wk_full[st], (ci >> 1) & 1, ab)) break;  // w k' is in place
+          if (resc) {
+            if (!mbar_wait(&rescaled, nres & 1, ab)) break;
+            ++nres;
+          }
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < C / 8; ++kk)  // S^T += v'^T (w k')
+            mma_ss(T_ST, dvm + (uint64_t)(kk * 64), dkm + (uint64_t)(kk * 64), id_u, 1u);
+          mma_commit(&empty[st]);
+        }
+      }
+      mma_commit(&drain_m);  // arrives once every MMA issued above has completed
+      mbar_wait(&drain_m, 0);
+    }
+  } else if (warp == 2) {
+    // ---- score MMAs ----------------------------------------------------------
+    if (lane == 0) {
+      const uint32_t id_s = idesc_tf32(64, 64);
+      for (int ci = 0; ci < nc; ++ci) {
+        const int st = ci & 1, sb = ci & 1;
+        if (!mbar_wait(&full[st], (ci >> 1) & 1, ab)) break;
+        if (ci >= 2 && !mbar_wait(&s_empty[sb], ((ci >> 1) - 1) & 1, ab)) break;
+        tc_fence_after();
+        const uint64_t dq = sdesc(smem_u32(Qs(st))), dkk = sdesc(smem_u32(Ks(st)));
+#pragma unroll
+        for (int kk = 0; kk < 16; ++kk)
+          if (kk < dk / 8) {
+            const uint64_t off = (uint64_t)((kk >> 2) * (BLK >> 4) + (kk & 3) * 2);
+            mma_ss(T_SC + sb * 64, dq + off, dkk + off, id_s, kk > 0 ? 1u : 0u);
+          }
+        mma_commit(&s_full[sb]);
+      }
+      mma_commit(&drain_s);
+      mbar_wait(&drain_s, 0);
+    }
+  } else if (warp == 3) {
+    // ---- decay factors ---------------------------------------------------------
+    double x0 = 0.0, x1 = 0.0;
+    auto la_load = [&](int ci) {
+      const int64_t t0 = s_begin + (int64_t)chunk_of(ci) * C;
+      const int len = (int)imin64(C, s_end - t0);
+      const float *lp = la + (b * p.L + t0) * p.H + h;
+      x0 = (2 * lane < len) ? (double)lp[(int64_t)(2 * lane) * p.H] : 0.0;
+      x1 = (2 * lane + 1 < len) ? (double)lp[(int64_t)(2 * lane + 1) * p.H] : 0.0;
+    };
+    la_load(0);
+    float alpha = 1.f;
+    for (int ci = 0; ci < nc; ++ci) {
+      const int slot = ci & 3;
+      const int64_t t0 = s_begin + (int64_t)chunk_of(ci) * C;
+      const int len = (int)imin64(C, s_end - t0);
+      const double cx0 = x0, cx1 = x1;
+      if (ci + 1 < nc) la_load(ci + 1);
+      if (ci >= 4 && !mbar_wait(&fac_empty[slot], ((ci >> 2) - 1) & 1, ab)) break;
+      Fac &F = fac[slot];
+      const double tot = warp_cumsum64_regs(cx0, cx1, len, 0.0, F.cs2);
+      __syncwarp();
+      const float tot2 = (float)(tot * LOG2E_D);
+      const float a_c = ex2f(tot2), an = alpha * a_c;
+      const bool lazy = a_c >= 0x1p-30f && an >= 0x1p-40f && an <= 0x1p40f;
+      const float kscale = lazy ? 1.f / an : 1.f;
+      for (int t = lane; t < C; t += 32) {
+        const bool in = t < len;
+        const float x = in ? F.cs2[t] * LOG2E : 0.f;
+        const float e = in ? ex2f(x) : 0.f;             // exp(cs_t)
+        const float wgt = in ? ex2f(tot2 - x) : 0.f;    // exp(A_c - cs_t)
+        F.cs2[t] = x;
+        F.qf[t] = (REV ? wgt : e) * alpha;
+        F.kw[t] = (REV ? e : wgt) * kscale;
+      }
+      if (lane == 0) {
+        F.an = an;
+        F.rescale = lazy ? 0 : 1;
+      }
+      alpha = lazy ? an : 1.f;
+      __syncwarp();
+      mbar_arrive(&fac_full[slot]);
+    }
+  } else if (warp < 8) {
+    // ---- mask: P and w k' ------------------------------------------------------
+    // The loops below run 8 columns per step: the roles' hot loops together
+    // must fit the instruction cache, so nothing long is unrolled.
+    const int wt = tid - 128, wq = warp & 3;
+    const uint32_t lb = (uint32_t)(32 * wq) << 16;
+    for (int ci = 0; ci < nc; ++ci) {
+      const int slot = ci & 3, sb = ci & 1, st = ci & 1;
+      const int64_t t0 = s_begin + (int64_t)chunk_of(ci) * C;
+      const int len = (int)imin64(C, s_end - t0);
+      if (!mbar_wait(&fac_full[slot], (ci >> 2) & 1, ab)) break;
+      // The chunk's factors, two per lane (tokens lane and lane + 32), handed
+      // around with shuffles: thread reads of shared memory are slow while
+      // the tensor cores stream their operands from it.
+      const Fac &F = fac[slot];
+      const float csA = F.cs2[lane], csB = F.cs2[lane + 32];
+      const float kwA = F.kw[lane], kwB = F.kw[lane + 32];
+      if (!mbar_wait(&s_full[sb], (ci >> 1) & 1, ab)) break;
+      if (ci >= 1 && !mbar_wait(&p_empty, (ci - 1) & 1, ab)) break;
+      tc_fence_after();
+      // score row r = 16 wq + lane % 16 sits in lane lane % 16 (M = 64); the
+      // lane 16 above it takes the row's upper 32 columns
+      const int r = 16 * wq + (lane & 15), up = lane >> 4, ub = 32 * up;
+      const float cr = __shfl_sync(0xffffffffu, wq < 2 ? csA : csB, r & 31);
+#pragma unroll 1
+      for (int g = 0; g < 2; ++g) {  // 16 of this lane's 32 columns per step
+        float lo[16], hi[16];
+        tmem_ld16x2(T_SC + sb * 64 + 16 * g + lb, T_SC + sb * 64 + 32 + 16 * g + lb, lo, hi);
+        if (g == 1) {
+          tc_fence_before();
+          mbar_arrive(&s_empty[sb]);
+        }
+        float f[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const float hv = __shfl_sync(0xffffffffu, hi[i], lane & 15);
+          const float s_ = up ? hv : lo[i];
+          const float a = __shfl_sync(0xffffffffu, csA, 16 * g + i), bb = __shfl_sync(0xffffffffu, csB, 16 * g + i);
+          const float cu = up ? bb : a;
+          const int u = ub + 16 * g + i;
+          const bool valid = r < len && u < len && (REV ? u >= r : u <= r);
+          f[i] = valid ? tf32r(ex2f(REV ? cu - cr : cr - cu) * s_) : 0.f;
+        }
+#pragma unroll
+        for (int i = 0; i < 16; i += 4)
+          *reinterpret_cast<float4 *>(P + sw128_off(r, ub + 16 * g + i, C)) = make_float4(f[i], f[i + 1], f[i + 2], f[i + 3]);
+      }
+      fence_async_smem();
+      mbar_arrive(&p_full);
+      // k' (K-major, 128-byte swizzle) -> w k' (MN-major, 32-byte atoms), in
+      // place: both layouts keep row s in the same 128 bytes of its block, so
+      // each row is permuted within itself (8 threads per row, one 16-byte
+      // chunk each; a warp holds 4 whole rows)
+      // (one column block per iteration: its four 16-row passes load first)
+      uint8_t *K = Ks(st);
+      const int ch = wt & 7;
+      float wr4[4];
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4)
+        wr4[q4] = __shfl_sync(0xffffffffu, q4 < 2 ? kwA : kwB, (q4 * 16 + (wt >> 3)) & 31);
+#pragma unroll 1
+      for (int blk = 0; blk < ncbk; ++blk) {
+        float4 v[4];
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+          const int row = q4 * 16 + (wt >> 3);
+          v[q4] = *reinterpret_cast<const float4 *>(K + blk * BLK + row * 128 + ((ch ^ (row & 7)) << 4));
+        }
+        __syncwarp();
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+          const int row = q4 * 16 + (wt >> 3);
+          const float wr = wr4[q4];
+          float4 x = v[q4];
+          x.x = tf32r(x.x * wr); x.y = tf32r(x.y * wr); x.z = tf32r(x.z * wr); x.w = tf32r(x.w * wr);
+          *reinterpret_cast<float4 *>(K + blk * BLK + row * 128 + ((((ch >> 1) ^ (row & 3)) << 5) | ((ch & 1) << 4))) = x;
+        }
+      }
+      fence_async_smem();
+      mbar_arrive(&wk_full[st]);
+      mbar_arrive(&fac_empty[slot]);
+    }
+  } else {
+    // ---- epilogue --------------------------------------------------------------
+    const int et = tid - 256, wq = warp & 3;
+    const int j = 32 * wq + lane;  // v' feature of this lane
+    const uint32_t lb = (uint32_t)(32 * wq) << 16;
+    {  // entering state into tensor memory: lane j, column i = state[i][j]
+      const float *H0 = Hseg + (bh * p.nseg + seg) * (int64_t)dk * dv;
+      for (int c0 = 0; c0 < p.dkp; c0 += 32) {
+        float hv[32];
+#pragma unroll
+        for (int ii = 0; ii < 32; ++ii) {
+          const int i = c0 + ii;
+          hv[ii] = (j < dv && i < dk) ? (hseg_t ? H0[(int64_t)j * dk + i] : H0[(int64_t)i * dv + j]) : 0.f;
+        }
+        tmem_st32(T_ST + lb + c0, hv);
       }
       tmem_st_wait();
       tc_fence_before();
-      __syncthreads();
-      tc_fence_after();
-      if (tid == 0) {
-        issue_update();
-        mma_commit(&bar_h);
-      }
-      ok = mbar_wait(&bar_h, hphase & 1) && ok;
-      ++hphase;
-      tc_fence_after();
-      if (ldk && ok && ci + 1 < nc) tma_k(cnext, ci + 1);
-      alpha = 1.f;
+      mbar_arrive(&st_init);
     }
-    tc_fence_before();
-    if (__syncthreads_or(!ok)) break;
-    tc_fence_after();
+    const int oslot = oa.out_slots == p.H ? (int)h : (int)(h / p.hpg);
+    const int64_t ld = (int64_t)oa.out_slots * dv;
+    const int64_t ldy = (int64_t)(p.H / p.hpg) * dv;
+    // SPLIT: the y values of 16-token step (chunk cy, step g), loaded two steps
+    // before they are used (yr0: this step, yr1: the next; the ring runs
+    // across chunks), so the loads' latency hides behind the steps between
+    float yr0[SPLIT ? 16 : 1], yr1[SPLIT ? 16 : 1];
+    auto load_y = [&](float (&dst)[SPLIT ? 16 : 1], int cy, int g) {
+      if constexpr (SPLIT) {
+        const int64_t ty = s_begin + (int64_t)chunk_of(cy < nc ? cy : 0) * C;
+        const int leny = cy < nc ? (int)imin64(C, s_end - ty) : 0;
+        const float *yp = oa.y + ((b * p.L + ty) * (p.H / p.hpg) + h / p.hpg) * (int64_t)dv + j;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) dst[i] = (j < dv && 16 * g + i < leny) ? yp[(16 * g + i) * ldy] : 0.f;
+      }
+    };
+    load_y(yr0, 0, 0);
+    load_y(yr1, 0, 1);
+    for (int ci = 0; ci < nc; ++ci) {
+      const int slot = ci & 3, xb = ci & 1;
+      const int64_t t0 = s_begin + (int64_t)chunk_of(ci) * C;
+      const int len = (int)imin64(C, s_end - t0);
+      if (!mbar_wait(&fac_full[slot], (ci >> 2) & 1, ab)) break;
+      if (!mbar_wait(&xy_full[xb], (ci >> 1) & 1, ab)) break;
+      tc_fence_after();
+      const Fac &F = fac[slot];
+      if (F.rescale) {  // Hs <- alpha exp(A_c) Hs before the update is issued
+        const float an = F.an;
+        for (int c0 = 0; c0 < p.dkp; c0 += 32) {
+          float hv[32];
+          tmem_ld32(T_ST + lb + c0, hv);
+#pragma unroll
+          for (int ii = 0; ii < 32; ++ii) hv[ii] *= an;
+          tmem_st32(T_ST + lb + c0, hv);
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(&rescaled);
+      }
+      const float qfA = F.qf[lane], qfB = F.qf[lane + 32];  // shuffled below (see the mask)
+      float *os = oa.out + ((b * p.L + t0) * oa.out_slots + oslot) * (int64_t)dv + j;
+      auto step = [&](const int g) {  // tokens 16 g .. 16 g + 15
+        float xa[16], ya[16];
+        tmem_ld16x2(T_X + xb * 64 + 16 * g + lb, T_Y + xb * 64 + 16 * g + lb, xa, ya);
+        if (g == 3) {
+          tc_fence_before();
+          mbar_arrive(&x_empty[xb]);
+        }
+        // all sixteen values first: a shuffle cannot move past a branch, so
+        // interleaving them with the (conditional) stores would serialise the
+        // shuffle latencies
+        const float qsrc = g < 2 ? qfA : qfB;
+        float o[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const float xi = __shfl_sync(0xffffffffu, qsrc, (16 * g + i) & 31) * xa[i];
+          o[i] = xi + ya[i];
+          if constexpr (SPLIT) xa[i] = xi * yr0[i];
+        }
+        if constexpr (SPLIT) {  // shift the ring and load two steps ahead
+#pragma unroll
+          for (int i = 0; i < 16; ++i) yr0[i] = yr1[i];
+          load_y(yr1, g + 2 < 4 ? ci : ci + 1, (g + 2) & 3);
+        }
+        if (j < dv) {
+          float *o16 = os + (int64_t)(16 * g) * ld;
+          if (16 * g + 16 <= len) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              if (ATOMIC) atomicAdd(o16 + i * ld, o[i]);
+              else o16[i * ld] = o[i];
+            }
+          } else {
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              if (16 * g + i < len) {
+                if (ATOMIC) atomicAdd(o16 + i * ld, o[i]);
+                else o16[i * ld] = o[i];
+              }
+          }
+        }
+        if constexpr (SPLIT) {
+          // sum the 16 products over the warp's 32 lanes: four halving
+          // exchanges leave each lane one value (index (lane >> 1) & 15)
+          // summed over 16 lanes, one butterfly finishes the sum
+#pragma unroll
+          for (int off = 16, n = 16; off >= 2; off >>= 1, n >>= 1) {
+            const bool upper = (lane & off) != 0;
+#pragma unroll
+            for (int k2 = 0; k2 < n / 2; ++k2) {
+              const float mine = upper ? xa[n / 2 + k2] : xa[k2];
+              const float send = upper ? xa[k2] : xa[n / 2 + k2];
+              xa[k2] = mine + __shfl_xor_sync(0xffffffffu, send, off);
+            }
+          }
+          xa[0] += __shfl_xor_sync(0xffffffffu, xa[0], 1);
+          if ((lane & 1) == 0) red[wq * C + 16 * g + (lane >> 1)] = xa[0];
+        }
+      };
+#pragma unroll 1
+      for (int g = 0; g < 4; ++g) step(g);
+      if constexpr (SPLIT) {
+        named_sync(2, 128);
+        if (et < len) oa.dcs[(b * p.L + t0 + et) * p.H + h] = red[et] + red[C + et] + red[2 * C + et] + red[3 * C + et];
+        named_sync(2, 128);
+      }
+      mbar_arrive(&fac_empty[slot]);
+    }
   }
-  __syncthreads();
-  if ((ldq || ldv || ldk) && tma_pending >= 0) mbar_wait(&bar_tma, tma_pending & 1);
-  if (ldv) bulk_wait_all();  // the output stores have landed
   tc_fence_before();
   __syncthreads();
-  if (warp == 0) tmem_dealloc(tmem, 256);
+  if (warp == 1) tmem_dealloc(tmem, 512);
 }
 
 // ===========================================================================
@@ -1130,17 +1158,19 @@ cudaError_t get_encoder() {
 }
 
 // 3-D view [rows, slots, d] of a row-major fp32 tensor; box = 32 features x
-// 1 slot x box_rows rows, 128-byte swizzle, zero fill out of bounds.
+// 1 slot x box_rows rows, zero fill out of bounds.  K-major operands use the
+// plain 128-byte swizzle, MN-major ones the 128-byte swizzle with 32-byte
+// atoms (sdesc / sdesc_mn).
 cudaError_t make_map(CUtensorMap *m, const float *base, int64_t rows, int64_t slots, int64_t d,
-                     int box_rows = C) {
+                     int box_rows, bool mn_major) {
   cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)slots, (cuuint64_t)rows};
   cuuint64_t strides[2] = {(cuuint64_t)(d * 4), (cuuint64_t)(slots * d * 4)};
   cuuint32_t box[3] = {32, 1, (cuuint32_t)box_rows};
   cuuint32_t es[3] = {1, 1, 1};
   CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float *>(base), dims,
                         strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                        mn_major ? CU_TENSOR_MAP_SWIZZLE_128B_ATOM_32B : CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
@@ -1157,13 +1187,11 @@ int num_sms() {
   return cache[dev];
 }
 
-// Segment length: as many segments as fit one wave of the segment kernels
-// (two CTAs per SM), so no partial second wave trails behind; measured
-// faster than two full waves (1.032 -> 0.996 ms per fwd+bwd step at
-// B=4, H=8, L=8192) and than 1.6 waves (1.195 ms).
+// Segment length: the walk runs one CTA per SM, so as many segments per
+// sequence as keep every (batch, head, segment) walk in one wave.
 void choose_segments(const Geo &g, int *Ls, int *nseg) {
   const int64_t bh = g.B * g.H;
-  const int64_t want = std::max<int64_t>(1, (2 * (int64_t)num_sms()) / bh);
+  const int64_t want = std::max<int64_t>(1, (int64_t)num_sms() / bh);
   int64_t ls = cdiv(cdiv(g.L, want), C) * C;
   if (ls < C) ls = C;
   *Ls = (int)std::min<int64_t>(ls, 1 << 30);
@@ -1187,16 +1215,33 @@ size_t state_floats(const PassGeo &p) {
 }
 
 size_t seg_state_smem(const PassGeo &p) {
-  return (size_t)(p.dkp / 32 + p.dvp / 32) * 4096 * 2 + (size_t)rup(p.dvn * 128, 1024) * 2 +
-         NT2 * 4 + 1024;
+  return (size_t)SS_STAGES * ((size_t)(p.dkp / 32) * SL * 128 + 4 * SL * 128) + 2 * 2 * SL * 128 + 1024;
 }
+// At least 120 KB, so that a walk CTA (which takes all 512 tensor-memory
+// columns) never shares its SM with a second one.
 size_t walk_smem(const PassGeo &p) {
-  return (size_t)(p.dkp / 32) * 2 * 8192 + std::max(p.dvp / 32 * 8192, 16384) + 11 * C * 4 + 1024;
+  const size_t stage = (size_t)(p.dkp / 32) * 2 * C * 128 + 4 * C * 128;
+  const size_t need = 2 * stage + 2 * C * 128 + 4 * sizeof(Fac) + 4 * C * 4 + 1024;
+  return std::max<size_t>(need, 120 * 1024);
 }
 
 size_t dla_intra_smem(const PassGeo &p) {
   const int ncbm = std::max(p.dkp, p.dvp) / 32;
   return (size_t)ncbm * 2 * 8192 + (size_t)(6 * C) * 4 + 1024;  // three CTAs per SM fit
+}
+
+// Launch helper (grid, block, dynamic shared memory, stream, kernel arguments).
+template <typename... KArgs, typename... Args>
+cudaError_t launch(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                   Args &&...args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cfg.attrs = nullptr;
+  cfg.numAttrs = 0;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
 }
 
 template <typename K>
@@ -1216,48 +1261,62 @@ cudaError_t run_states(const PassGeo &p, const float *kp, const float *vp, const
   const int64_t rows = p.B * p.L;
   const int64_t G = p.H / p.hpg;
   CUtensorMap mk, mv;
-  if ((e = make_map(&mk, kp, rows, p.qk_per_head ? p.H : G, p.dk, SL)) != cudaSuccess) return e;
-  if ((e = make_map(&mv, vp, rows, p.v_per_head ? p.H : G, p.dv, SL)) != cudaSuccess) return e;
+  if ((e = make_map(&mk, kp, rows, p.qk_per_head ? p.H : G, p.dk, SL, true)) != cudaSuccess) return e;
+  if ((e = make_map(&mv, vp, rows, p.v_per_head ? p.H : G, p.dv, SL, true)) != cudaSuccess) return e;
   const dim3 grid((unsigned)p.nseg, (unsigned)p.H, (unsigned)p.B);
   {
     const size_t sm = seg_state_smem(p);
     if ((e = set_smem(k_seg_state<REV>, sm)) != cudaSuccess) return e;
     LaunchTrace lt(name_state, s);
-    k_seg_state<REV><<<grid, NT2, sm, s>>>(mk, mv, la, states, Aseg, p);
+    if ((e = launch(k_seg_state<REV>, grid, dim3(SS_THREADS), sm, s, mk, mv, la, states, Aseg, p)) != cudaSuccess)
+      return e;
   }
   {
     LaunchTrace lt("tc.seg_scan", s);
     const dim3 sg((unsigned)(p.B * p.H), (unsigned)cdiv((int64_t)p.dk * p.dv, 4 * NTH));
-    if (trans) k_seg_scan<REV, true><<<sg, NTH, 0, s>>>(states, Aseg, h0, fin, statesT, p);
-    else k_seg_scan<REV, false><<<sg, NTH, 0, s>>>(states, Aseg, h0, fin, statesT, p);
+    e = trans ? launch(k_seg_scan<REV, true>, sg, dim3(NTH), 0, s, states, Aseg, h0, fin, statesT, p)
+              : launch(k_seg_scan<REV, false>, sg, dim3(NTH), 0, s, states, Aseg, h0, fin, statesT, p);
+    if (e != cudaSuccess) return e;
   }
   return cudaGetLastError();
 }
 
+template <bool REV, bool ATOMIC, bool SPLIT>
+cudaError_t launch_walk(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
+                        const PassGeo &p, const float *la, const float *states, bool states_t,
+                        const WalkOut &oa, cudaStream_t s) {
+  cudaError_t e;
+  const size_t sm = walk_smem(p);
+  if ((e = set_smem(k_walk<REV, ATOMIC, SPLIT>, sm)) != cudaSuccess) return e;
+  const dim3 grid((unsigned)p.nseg, (unsigned)p.H, (unsigned)p.B);
+  return launch(k_walk<REV, ATOMIC, SPLIT>, grid, dim3(WT), sm, s, mq, mk, mv, la, states, states_t ? 1 : 0, oa, p);
+}
+
 // The walk of one pass over every segment, from the entering states.
 //   q', k' : [B*L, qk_slots, dk]   v' : [B*L, v_slots, dv]
+// atomic: out' is summed over the heads of a group; oa.dcs given: the per-token
+// inter-term dots are written too.
 template <bool REV>
 cudaError_t run_walk(const PassGeo &p, const float *qp, const float *kp, const float *vp,
-                     const float *la, const float *states, bool states_t, const OutArgs &oa,
+                     const float *la, const float *states, bool states_t, const WalkOut &oa,
                      bool atomic, cudaStream_t s, const char *name_walk) {
   cudaError_t e;
   const int64_t rows = p.B * p.L;
   const int64_t G = p.H / p.hpg;
-  CUtensorMap mq, mk, mv, mo;
-  if ((e = make_map(&mq, qp, rows, p.qk_per_head ? p.H : G, p.dk)) != cudaSuccess) return e;
-  if ((e = make_map(&mk, kp, rows, p.qk_per_head ? p.H : G, p.dk)) != cudaSuccess) return e;
-  if ((e = make_map(&mv, vp, rows, p.v_per_head ? p.H : G, p.dv)) != cudaSuccess) return e;
-  if ((e = make_map(&mo, oa.out, rows, oa.out_slots, p.dv)) != cudaSuccess) return e;
-  const dim3 grid((unsigned)p.nseg, (unsigned)p.H, (unsigned)p.B);
-  const size_t sm = walk_smem(p);
+  CUtensorMap mq, mk, mv;
+  if ((e = make_map(&mq, qp, rows, p.qk_per_head ? p.H : G, p.dk, C, false)) != cudaSuccess) return e;
+  if ((e = make_map(&mk, kp, rows, p.qk_per_head ? p.H : G, p.dk, C, false)) != cudaSuccess) return e;
+  if ((e = make_map(&mv, vp, rows, p.v_per_head ? p.H : G, p.dv, C, true)) != cudaSuccess) return e;
   LaunchTrace lt(name_walk, s);
+  const bool split = oa.dcs != nullptr;
   if (atomic) {
-    if ((e = set_smem(k_walk<REV, true>, sm)) != cudaSuccess) return e;
-    k_walk<REV, true><<<grid, NT2, sm, s>>>(mq, mk, mv, mo, la, states, states_t ? 1 : 0, oa, p);
+    e = split ? launch_walk<REV, true, true>(mq, mk, mv, p, la, states, states_t, oa, s)
+              : launch_walk<REV, true, false>(mq, mk, mv, p, la, states, states_t, oa, s);
   } else {
-    if ((e = set_smem(k_walk<REV, false>, sm)) != cudaSuccess) return e;
-    k_walk<REV, false><<<grid, NT2, sm, s>>>(mq, mk, mv, mo, la, states, states_t ? 1 : 0, oa, p);
+    e = split ? launch_walk<REV, false, true>(mq, mk, mv, p, la, states, states_t, oa, s)
+              : launch_walk<REV, false, false>(mq, mk, mv, p, la, states, states_t, oa, s);
   }
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
@@ -1268,8 +1327,8 @@ cudaError_t run_walk(const PassGeo &p, const float *qp, const float *kp, const f
 // scans.  Fork and join are events; the lock makes the enqueue of one backward
 // atomic with respect to others on other host threads (the events are reused).
 struct Side {
-  cudaStream_t s2 = nullptr;
-  cudaEvent_t fork = nullptr, join = nullptr;
+  cudaStream_t s2 = nullptr, s3 = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr, join3 = nullptr;
 };
 std::mutex g_side_mu;
 Side g_side[64];
@@ -1283,8 +1342,10 @@ cudaError_t get_side(Side **out) {
   Side &sd = g_side[dev];
   if (!sd.s2) {
     if ((e = cudaStreamCreateWithFlags(&sd.s2, cudaStreamNonBlocking)) != cudaSuccess) return e;
+    if ((e = cudaStreamCreateWithFlags(&sd.s3, cudaStreamNonBlocking)) != cudaSuccess) return e;
     if ((e = cudaEventCreateWithFlags(&sd.fork, cudaEventDisableTiming)) != cudaSuccess) return e;
     if ((e = cudaEventCreateWithFlags(&sd.join, cudaEventDisableTiming)) != cudaSuccess) return e;
+    if ((e = cudaEventCreateWithFlags(&sd.join3, cudaEventDisableTiming)) != cudaSuccess) return e;
   }
   *out = &sd;
   return cudaSuccess;
@@ -1325,7 +1386,7 @@ cudaError_t fwd(const float *q, const float *k, const float *v, const float *la,
   float *Aseg = st + state_floats(p);
   if ((e = run_states<false>(p, k, v, la, h0, false, hT, st, Aseg, nullptr, s, "tc.seg_state")) != cudaSuccess)
     return e;
-  OutArgs oa{out, (int)g.H, nullptr, nullptr};
+  WalkOut oa{out, (int)g.H, nullptr, nullptr};
   return run_walk<false>(p, q, k, v, la, st, false, oa, false, s, "tc.walk_out");
 }
 
@@ -1365,9 +1426,11 @@ cudaError_t bwd(const float *q, const float *k, const float *v, const float *la,
     if ((e = cudaMemsetAsync(dk, 0, sizeof(float) * g.B * g.L * g.G * g.dk, s)) != cudaSuccess) return e;
   }
   const int oslots = grouped ? (int)g.G : (int)g.H;
-  // The dk / dv passes (pass B's states, both anti-causal walks) run on the
-  // side stream, forked from s after the memsets and joined before k_dla
-  // (or on s itself when overlap is off).
+  // The dk / dv passes (pass B's states, both anti-causal walks) run on one
+  // side stream and the intra-chunk dlog_alpha sums (inputs only) on another,
+  // both forked from s after the memsets and joined before k_dla (or all on s
+  // when overlap is off).  The walks take one CTA per SM and leave the rest
+  // of the SMs to the other streams' kernels.
   const bool overlap = g_overlap.load();
   std::unique_lock<std::mutex> lock(g_side_mu, std::defer_lock);
   Side *sd = nullptr;
@@ -1384,53 +1447,63 @@ cudaError_t bwd(const float *q, const float *k, const float *v, const float *la,
     }
     if (e != cudaSuccess) return e;
     if ((e = cudaStreamWaitEvent(sd->s2, sd->fork, 0)) != cudaSuccess) return e;
+    if ((e = cudaStreamWaitEvent(sd->s3, sd->fork, 0)) != cudaSuccess) return e;
   }
-  cudaStream_t s2 = overlap ? sd->s2 : s;
+  cudaStream_t s2 = overlap ? sd->s2 : s, s3 = overlap ? sd->s3 : s;
+  // intra-chunk block sums of dlog_alpha, on s3
+  cudaError_t ei = cudaSuccess;
+  {
+    const PassGeo pi = make_pass(g, DK, DV, false, true);
+    CUtensorMap mq, mk, mv, md;
+    const int64_t rows = g.B * g.L;
+    if (ei == cudaSuccess) ei = make_map(&mq, q, rows, g.G, DK, C, false);
+    if (ei == cudaSuccess) ei = make_map(&mk, k, rows, g.G, DK, C, false);
+    if (ei == cudaSuccess) ei = make_map(&mv, v, rows, g.H, DV, C, false);
+    if (ei == cudaSuccess) ei = make_map(&md, dout, rows, g.H, DV, C, false);
+    const size_t sm = dla_intra_smem(pi);
+    if (ei == cudaSuccess) ei = set_smem(k_dla_intra, sm);
+    if (ei == cudaSuccess) {
+      LaunchTrace lt("tc.dla_intra", s3);
+      ei = launch(k_dla_intra, dim3((unsigned)g.N, (unsigned)g.G, (unsigned)g.B), dim3(NTH), sm, s3, mq, mk, mv, md,
+                  la, Bt, pi);
+    }
+  }
+  const cudaError_t ej3 = overlap ? cudaEventRecord(sd->join3, s3) : cudaSuccess;
   cudaError_t eb = run_states<true>(pb, dout, q, la, dhT, true, dh0, stB, aB, nullptr, s2, "tc.seg_state_dk");
-  OutArgs okk{dk, oslots, k, rk};
+  WalkOut okk{dk, oslots, k, rk};
   if (eb == cudaSuccess) eb = run_walk<true>(pb, v, dout, q, la, stB, false, okk, grouped, s2, "tc.walk_dk");
-  OutArgs ov{dv, (int)g.H, nullptr, nullptr};
+  WalkOut ov{dv, (int)g.H, nullptr, nullptr};
   if (eb == cudaSuccess) eb = run_walk<true>(pc, k, q, dout, la, stB, true, ov, false, s2, "tc.walk_dv");
   // whatever was enqueued on s2 is joined back into s before this returns,
   // even after an error (the caller frees the workspace on s)
   cudaError_t ej = overlap ? cudaEventRecord(sd->join, s2) : cudaSuccess;
   auto join = [&]() -> cudaError_t {
-    if (!overlap || ej != cudaSuccess) return ej;
-    return cudaStreamWaitEvent(s, sd->join, 0);
+    if (!overlap) return cudaSuccess;
+    if (ej != cudaSuccess) return ej;
+    if (ej3 != cudaSuccess) return ej3;
+    cudaError_t e1 = cudaStreamWaitEvent(s, sd->join, 0);
+    cudaError_t e2 = cudaStreamWaitEvent(s, sd->join3, 0);
+    return e1 != cudaSuccess ? e1 : e2;
   };
-  if (eb != cudaSuccess) {
+  if (eb != cudaSuccess || ei != cudaSuccess) {
     join();
-    return eb;
+    return eb != cudaSuccess ? eb : ei;
   }
-  // pass A and the intra-chunk sums on s, meanwhile
+  // pass A on s, meanwhile
   auto on_s = [&]() -> cudaError_t {
     cudaError_t ea = run_states<false>(pa, v, k, la, h0, true, hT, stA, aA, nullptr, s, "tc.seg_state_dq");
     if (ea != cudaSuccess) return ea;
-    OutArgs oq{dq, oslots, q, rq};
-    if ((ea = run_walk<false>(pa, dout, v, k, la, stA, false, oq, grouped, s, "tc.walk_dq")) != cudaSuccess)
-      return ea;
-    // intra-chunk block sums of dlog_alpha
-    const PassGeo pi = make_pass(g, DK, DV, false, true);
-    CUtensorMap mq, mk, mv, md;
-    const int64_t rows = g.B * g.L;
-    if ((ea = make_map(&mq, q, rows, g.G, DK)) != cudaSuccess) return ea;
-    if ((ea = make_map(&mk, k, rows, g.G, DK)) != cudaSuccess) return ea;
-    if ((ea = make_map(&mv, v, rows, g.H, DV)) != cudaSuccess) return ea;
-    if ((ea = make_map(&md, dout, rows, g.H, DV)) != cudaSuccess) return ea;
-    const size_t sm = dla_intra_smem(pi);
-    if ((ea = set_smem(k_dla_intra, sm)) != cudaSuccess) return ea;
-    LaunchTrace lt("tc.dla_intra", s);
-    k_dla_intra<<<dim3((unsigned)g.N, (unsigned)g.G, (unsigned)g.B), NTH, sm, s>>>(mq, mk, mv, md,
-                                                                                  la, Bt, pi);
-    return cudaGetLastError();
+    WalkOut oq{dq, oslots, q, rq};
+    return run_walk<false>(pa, dout, v, k, la, stA, false, oq, grouped, s, "tc.walk_dq");
   };
   const cudaError_t ea = on_s();
   if ((e = join()) != cudaSuccess) return e;
   if (ea != cudaSuccess) return ea;
   {  // pass A's states are S^T, pass B's are G^T: the carry is their plain dot
     LaunchTrace lt("tc.dla", s);
-    k_dla<<<dim3((unsigned)pa.nseg, (unsigned)g.H, (unsigned)g.B), DT, 0, s>>>(
-        Bt, rq, rk, stB, stA, dhT, hT, dla, g.L, g.H, DK * DV, pa.Ls, pa.nseg);
+    if ((e = launch(k_dla, dim3((unsigned)pa.nseg, (unsigned)g.H, (unsigned)g.B), dim3(DT), 0, s, Bt, rq, rk, stB, stA,
+                    dhT, hT, dla, g.L, g.H, (int64_t)(DK * DV), pa.Ls, pa.nseg)) != cudaSuccess)
+      return e;
   }
   return cudaGetLastError();
 }

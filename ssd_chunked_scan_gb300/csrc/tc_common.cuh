@@ -38,11 +38,30 @@ __device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes) {
                "r"(bytes)
                : "memory");
 }
-// Bounded wait for the phase with the given parity to complete.  Each
-// try_wait may park the warp for up to 20 us (suspend-time hint) instead of
-// spinning; the loop gives up after ~2^31 SM clock cycles (about a second),
-// records the failure in the device error word and returns false.
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
+// Spin limit of the bounded waits, in SM clock cycles (about a second).
+constexpr long long kWaitLimit = 1ll << 31;
+
+// One test of the phase with the given parity; true once it has completed.
+__device__ __forceinline__ bool mbar_test(uint64_t *bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// The waiting loop of mbar_wait, out of line: the warp-specialised kernels
+// call it from many places, and their hot code must fit the instruction
+// cache together.  Each try_wait may park the warp for up to 20 us
+// (suspend-time hint) instead of spinning; the loop gives up after
+// kWaitLimit cycles, records the failure in the device error word and
+// returns false.  When `abort` is given, it also gives up as soon as another
+// thread of the CTA has set *abort (it sets *abort itself when it times out),
+// so that every role of a warp-specialised kernel leaves its loop once one of
+// them has failed.
+__device__ __noinline__ bool mbar_wait_slow(uint64_t *bar, uint32_t parity, volatile int *abort) {
   uint32_t ok = 0;
   const long long t0 = clock64();
   while (true) {
@@ -53,11 +72,28 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
         : "r"(smem_u32(bar)), "r"(parity), "r"(20000u)
         : "memory");
     if (ok) return true;
-    if (clock64() - t0 > (1ll << 31)) {
+    if (abort && *abort) return false;
+    if (clock64() - t0 > kWaitLimit) {
       atomicOr(&g_error_word, 1u);
+      if (abort) *abort = 1;
       return false;
     }
   }
+}
+// Bounded wait for the phase with the given parity to complete (see
+// mbar_wait_slow): one inline test, the loop out of line.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity,
+                                          volatile int *abort = nullptr) {
+  if (mbar_test(bar, parity)) return true;
+  return mbar_wait_slow(bar, parity, abort);
+}
+// Plain arrive (release semantics at CTA scope).
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+// Barrier among the `nthreads` threads (whole warps) that use named barrier `id`.
+__device__ __forceinline__ void named_sync(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
 // ---- TMA --------------------------------------------------------------------
@@ -133,9 +169,10 @@ __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
                : "memory");
 }
 
-// ---- descriptors ------------------------------------------------------------
-// Shared-memory matrix descriptor: K-major, 128-byte swizzle, rows of 128 B,
-// 8-row groups 1024 B apart.
+// ---- descriptors ----------------------------------------------------------
+// Shared-memory matrix descriptor of a K-major operand in the 128-byte
+// swizzle (16-byte chunks XORed with the row within each 8-row group, the
+// layout TMA's SWIZZLE_128B writes): rows of 128 B, 8-row groups 1024 B apart.
 __device__ __forceinline__ uint64_t sdesc(uint32_t saddr) {
   uint64_t d = 0;
   d |= (uint64_t)((saddr >> 4) & 0x3FFF);
@@ -145,9 +182,29 @@ __device__ __forceinline__ uint64_t sdesc(uint32_t saddr) {
   d |= (uint64_t)2 << 61;            // 128-byte swizzle
   return d;
 }
-// Instruction descriptor, kind::tf32, fp32 accumulate, both operands K-major.
-__host__ __device__ constexpr uint32_t idesc_tf32(uint32_t M, uint32_t N) {
-  return (1u << 4) | (2u << 7) | (2u << 10) | ((N >> 3) << 17) | ((M >> 4) << 24);
+// Descriptor of an MN-major (transposed) fp32 operand: the layout TMA's
+// SWIZZLE_128B_ATOM_32B writes (32-byte granules of each 128-byte row XORed
+// with the row within each 4-row group).  The tile is stored as blocks of 32
+// MN-elements x `rows` K-rows; blocks are rows * 128 B apart (leading byte
+// offset), 4-row groups 512 B apart (stride byte offset).  Layout type 1 is
+// the 128-byte swizzle with 32-byte atoms; the tensor cores accept fp32
+// (tf32) operands in MN-major order only in this layout, and K-major
+// operands only in the plain 128-byte swizzle (measured on GB300).
+__device__ __forceinline__ uint64_t sdesc_mn(uint32_t saddr, uint32_t block_bytes) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr >> 4) & 0x3FFF);
+  d |= (uint64_t)((block_bytes >> 4) & 0x3FFF) << 16;
+  d |= (uint64_t)(512 >> 4) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)1 << 61;
+  return d;
+}
+// Instruction descriptor, kind::tf32, fp32 accumulate; a_mn / b_mn mark an
+// MN-major A / B operand.
+__host__ __device__ constexpr uint32_t idesc_tf32(uint32_t M, uint32_t N, uint32_t a_mn = 0,
+                                                  uint32_t b_mn = 0) {
+  return (1u << 4) | (2u << 7) | (2u << 10) | (a_mn << 15) | (b_mn << 16) | ((N >> 3) << 17) |
+         ((M >> 4) << 24);
 }
 
 // ---- MMA ----------------------------------------------------------------------
@@ -192,6 +249,37 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+// Two loads of 32 lanes x 16 columns, then one wait.
+__device__ __forceinline__ void tmem_ld16x2(uint32_t ta, uint32_t tb, float (&a)[16], float (&b)[16]) {
+  uint32_t r[16], q[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(ta));
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(q[0]), "=r"(q[1]), "=r"(q[2]), "=r"(q[3]), "=r"(q[4]), "=r"(q[5]), "=r"(q[6]), "=r"(q[7]),
+        "=r"(q[8]), "=r"(q[9]), "=r"(q[10]), "=r"(q[11]), "=r"(q[12]), "=r"(q[13]), "=r"(q[14]), "=r"(q[15])
+      : "r"(tb));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    a[i] = __uint_as_float(r[i]);
+    b[i] = __uint_as_float(q[i]);
+  }
+}
+// 32 lanes x 8 columns per warp.
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, float (&v)[8]) {
+  uint32_t r[8];
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
+                 "=r"(r[6]), "=r"(r[7])
+               : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
 }
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) {
   asm volatile(
@@ -242,6 +330,12 @@ __device__ __forceinline__ float tf32r(float x) {
 __device__ __forceinline__ uint32_t sw128_off(int row, int col, int rows) {
   const int blk = col >> 5, c = (col & 31) >> 2, w = col & 3;
   return (uint32_t)(blk * rows * 128 + row * 128 + ((c ^ (row & 7)) << 4) + (w << 2));
+}
+// The same for the MN-major layout with 32-byte atoms (sdesc_mn): within a
+// 128-byte row, 32-byte granule (col % 32) / 8 is XORed with (row % 4).
+__device__ __forceinline__ uint32_t atom32_off(int row, int col, int rows) {
+  const int blk = col >> 5, g = (col & 31) >> 3, w = col & 7;
+  return (uint32_t)(blk * rows * 128 + row * 128 + ((g ^ (row & 3)) << 5) + (w << 2));
 }
 
 }  // namespace tc
