@@ -56,23 +56,23 @@ def load_peaks():
                 "source": "fallback"}
 
 
-# DRAM bytes (read + write) per launch of each kernel from one ncu
-# capture of the kernels as they stand (profiles/tc_g2h8_d128_L8192_long.md,
-# g2h8_d128 L=8192 long-memory workload); a kernel without an entry reports
-# null.  Every change to a kernel must refresh or drop its entry.
-TRAFFIC = {
-    "tc.seg_state": 169083648 + 4021248,
-    "tc.seg_state_dq": 169071616 + 1070848,
-    "tc.seg_state_dk": 169008128 + 995328,
-    "tc.seg_scan": (21019136 + 18931712 + 21022464) // 3,  # mean of the three passes' scans
-    "tc.walk_out": 221381632 + 93543424,
-    "tc.walk_dq": 389164288 + 24201216,
-    "tc.walk_dk": 389141504 + 24491008,
-    "tc.walk_dv": 221358592 + 94183936,
-    "tc.dla_intra": 336926464 + 483072,
-    "tc.dla": 36711936,
-    # the CUDA-core path's kernels (profiles/simt_g2h8_d128_L8192_long.md); kernels
-    # that run twice per step: the mean of their launches
+# DRAM bytes (read + write) per launch of each kernel at the g2h8_d128 L=8192
+# long-memory workload, from one ncu capture of the launch list
+# (gpu__time_duration.sum, dram__bytes_read.sum, dram__bytes_write.sum) of the
+# kernels as they stood then.  Each group names the commit of the capture and
+# the SHA-256 (first 16 hex digits) of the kernel source it measured: when the
+# file in the tree no longer hashes to that, the group's figures no longer
+# describe the kernels and the bench line reports traffic null, saying why.
+TRAFFIC_GROUPS = {
+    "tc.": {"source": "ssd_chunked_scan_gb300/csrc/tc.cu", "sha16": None, "commit": None,
+            "bytes": {}},
+    "simt.": {"source": "ssd_chunked_scan_gb300/csrc/simt.cu", "sha16": None, "commit": "f753b28",
+              "bytes": {}},
+    "mamba.": {"source": "ssd_chunked_scan_gb300/csrc/mamba.cu", "sha16": "46a5b2d4c8f2dcb9", "commit": "c617278",
+               "bytes": {}},
+}
+_SIMT_TRAFFIC = {
+    # kernels that run twice per step: the mean of their launches
     "simt.chunk_state": (168927744 + 213100544 + 168965120 + 209852160) // 2,
     "simt.state_scan_fwd": (270607872 + 204486912 + 270578176 + 204050688) // 2,
     "simt.chunk_out": 471726848 + 110684672,
@@ -81,15 +81,41 @@ TRAFFIC = {
     "simt.chunk_grad": 1171999232 + 349719040,
     "simt.dla_carry": 1090304,
 }
-# the same for the Mamba kernels at d1024 L8192 (profiles/mamba_d1024_L8192.md);
-# seg_state and seg_scan run more than once per step: the mean of their launches
-MAMBA_TRAFFIC = {
+# the same for the Mamba kernels at d1024 L8192; seg_state and seg_scan run more
+# than once per step: the mean of their launches
+_MAMBA_TRAFFIC = {
     "mamba.seg_state": (270622976 + 3436800 + 270637056 + 328448) // 2,
     "mamba.seg_scan": (6209280 + 6209024 + 6209024) // 3,
     "mamba.out": 278507776 + 99099904,
     "mamba.seg_grad_state": 270713856 + 371456,
     "mamba.bwd": 427659520 + 242076672,
 }
+TRAFFIC_GROUPS["simt."]["bytes"] = _SIMT_TRAFFIC
+TRAFFIC_GROUPS["mamba."]["bytes"] = _MAMBA_TRAFFIC
+
+
+def _sha16(rel):
+    import hashlib
+    try:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            return hashlib.sha256(f.read()).hexdigest()[:16]
+    except OSError:
+        return None
+
+
+def traffic_of(kernel):
+    """(DRAM bytes per launch or None, a note on where the figure comes from)."""
+    for prefix, grp in TRAFFIC_GROUPS.items():
+        if not kernel.startswith(prefix):
+            continue
+        if kernel not in grp["bytes"] or grp["sha16"] is None:
+            return None, f"no ncu capture of {kernel} in its current form"
+        if _sha16(grp["source"]) != grp["sha16"]:
+            return None, (f"{grp['source']} changed since the ncu capture at commit {grp['commit']}; "
+                          "its figure no longer applies")
+        return grp["bytes"][kernel], (f"ncu capture at commit {grp['commit']}, "
+                                      f"{grp['source']} unchanged since (sha256 {grp['sha16']}...)")
+    return None, f"no ncu capture of {kernel}"
 
 # nominal dense tensor rates: tf32 1.1 PF vs bf16 2.25 PF per GPU
 TF32_OVER_BF16 = 1.1 / 2.25
@@ -181,7 +207,10 @@ def kernel_roofline(trace, costs, peaks, traffic_ok):
         roof = {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "peak_note": f"{peaks['source']} copy bandwidth"}
     roof["frac"] = roof["achieved"] / roof["peak"]
-    roof["traffic"] = TRAFFIC.get(top_name) if traffic_ok else None
+    if traffic_ok:
+        roof["traffic"], roof["traffic_source"] = traffic_of(top_name)
+    else:
+        roof["traffic"], roof["traffic_source"] = None, "captured at the default workload only"
     roof["kernel"] = top_name
     roof["kernel_ms_per_launch"] = per_launch_ms
     roof["alg_bytes_per_launch"] = kb
@@ -208,72 +237,138 @@ def step_totals(w):
 
 
 class ClockSampler:
-    """nvidia-smi clocks / throttle reasons sampled every 100 ms in the background."""
+    """SM clock, power and clock-event (throttle) reasons of one GPU, sampled in
+    the background every 5 ms through NVML's read-only queries (ctypes on
+    libnvidia-ml), so that even a timed region of a few tens of milliseconds
+    holds samples; `nvidia-smi -lms 100` when NVML cannot be loaded.  The GPU
+    is found by the CUDA device's UUID."""
 
+    PERIOD_S = 0.005
+    # clock-event reason bits (nvml.h) reported by name
+    BITS = {"sw_power_cap": 0x4, "hw_slowdown": 0x8 | 0x80, "sw_thermal_slowdown": 0x20,
+            "hw_thermal_slowdown": 0x40}
     Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
     def __init__(self, index):
-        self.samples = []
-        self.proc = None
+        self.samples = []  # (time, sm_mhz, max_mhz, power_w, [reason names])
         self.index = index
+        self.proc = None
+        self.source = None
+        self._stop = threading.Event()
+        self.t = None
+
+    def _uuid(self):
+        try:
+            import torch
+            u = str(torch.cuda.get_device_properties(self.index).uuid)
+            return u if u.startswith("GPU-") else "GPU-" + u
+        except Exception:
+            return None
+
+    def _nvml(self):
+        import ctypes
+        lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if lib.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit failed")
+        h = ctypes.c_void_p()
+        uuid = self._uuid()
+        if uuid is None or lib.nvmlDeviceGetHandleByUUID(uuid.encode(), ctypes.byref(h)) != 0:
+            n = ctypes.c_uint(0)
+            if lib.nvmlDeviceGetCount_v2(ctypes.byref(n)) != 0 or n.value != 1:
+                raise OSError("cannot tell which NVML device is this CUDA device")
+            if lib.nvmlDeviceGetHandleByIndex_v2(0, ctypes.byref(h)) != 0:
+                raise OSError("nvmlDeviceGetHandleByIndex failed")
+        reasons_fn = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        return lib, h, reasons_fn
 
     def start(self):
         try:
+            lib, h, reasons_fn = self._nvml()
+        except Exception:
+            return self._start_smi()
+        import ctypes
+        self.source = "nvml, 5 ms"
+
+        def run():
+            sm, mx, pw, rs = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong()
+            while not self._stop.is_set():
+                t = time.time()
+                ok = (lib.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(sm)) == 0 and
+                      lib.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0 and
+                      reasons_fn(h, ctypes.byref(rs)) == 0)
+                p = float(pw.value) / 1e3 if lib.nvmlDeviceGetPowerUsage(h, ctypes.byref(pw)) == 0 else None
+                if ok:
+                    names = sorted(n for n, b in self.BITS.items() if rs.value & b)
+                    self.samples.append((t, float(sm.value), float(mx.value), p, names))
+                self._stop.wait(self.PERIOD_S)
+        self.t = threading.Thread(target=run, daemon=True)
+        self.t.start()
+
+    def _start_smi(self):
+        dev = self._uuid() or str(self.index)
+        try:
             self.proc = subprocess.Popen(
-                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                ["nvidia-smi", "-i", dev, f"--query-gpu={self.Q}",
                  "--format=csv,noheader,nounits", "-lms", "100"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except Exception:
             self.proc = None
             return
-        self.t = threading.Thread(target=self._read, daemon=True)
+        self.source = "nvidia-smi, 100 ms"
+        self.t = threading.Thread(target=self._read_smi, daemon=True)
         self.t.start()
+
+    def _read_smi(self):
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 8 and num(parts[0]) is not None:
+                rs = sorted(names[i] for i in range(4) if parts[4 + i].lower() == "active")
+                self.samples.append((time.time(), num(parts[0]), num(parts[1]), num(parts[2]), rs))
 
     def wait_first(self, timeout=5.0):
         """Block until the sampler has produced a sample (nvidia-smi's start-up
         stalls the GPU briefly; it must not fall inside a timed region)."""
         t0 = time.time()
-        while self.proc is not None and not self.samples and time.time() - t0 < timeout:
-            time.sleep(0.02)
-
-    def _read(self):
-        for line in self.proc.stdout:
-            parts = [p.strip() for p in line.split(",")]
-            if len(parts) >= 8:
-                self.samples.append((time.time(), parts))
+        while self.t is not None and not self.samples and time.time() - t0 < timeout:
+            time.sleep(0.01)
 
     def stop(self):
+        self._stop.set()
         if self.proc is not None:
             self.proc.terminate()
             try:
                 self.proc.wait(timeout=5)
             except Exception:
                 self.proc.kill()
+        if self.t is not None:
+            self.t.join(timeout=5)
 
     def summary(self, t0, t1):
-        inwin = [p for (t, p) in self.samples if t0 <= t <= t1]
+        inwin = [x for x in self.samples if t0 <= x[0] <= t1]
         window = "timed"
         if not inwin:
-            inwin = [p for (t, p) in self.samples]
-            window = "whole run (timed region shorter than the sampling period)"
+            inwin = list(self.samples)
+            window = "whole run (no sample fell inside the timed region)"
         if not inwin:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
-
-        def num(x):
-            try:
-                return float(x)
-            except ValueError:
-                return None
-        sm = [num(p[0]) for p in inwin if num(p[0]) is not None]
-        mx = [num(p[1]) for p in inwin if num(p[1]) is not None]
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for p in inwin for i in range(4) if p[4 + i].lower() == "active"})
-        pw = [num(p[2]) for p in inwin if num(p[2]) is not None]
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0,
+                    "source": self.source}
+        sm = [x[1] for x in inwin if x[1] is not None]
+        mx = [x[2] for x in inwin if x[2] is not None]
+        pw = [x[3] for x in inwin if x[3] is not None]
+        reasons = sorted({r for x in inwin for r in x[4]})
         return {"sm_mhz": statistics.median(sm) if sm else None,
                 "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
-                "power_w_max": max(pw) if pw else None, "samples": len(inwin), "window": window}
+                "power_w_max": max(pw) if pw else None, "samples": len(inwin), "window": window,
+                "source": self.source}
 
 
 def oracle_sample(w, threads):
@@ -297,11 +392,14 @@ def cpu_oracle_sample(w, min_seconds=10.0, max_reps=60):
     from oracle import oracle_threads, ssd_bwd_ref, ssd_fwd_ref
     (q, k, v, la, h0, dout), nb, used = oracle_sample(w, oracle_threads())
     toks, t0, reps, t_fwd = 0, time.perf_counter(), 0, 0.0
+    first = None
     while True:
         ta = time.perf_counter()
-        ssd_fwd_ref(q, k, v, la, h0)
+        r_out = ssd_fwd_ref(q, k, v, la, h0)
         t_fwd += time.perf_counter() - ta
-        ssd_bwd_ref(q, k, v, la, h0, dout)
+        r_g = ssd_bwd_ref(q, k, v, la, h0, dout)
+        if first is None:
+            first = (r_out, r_g)
         reps += 1
         toks += nb * w.L * w.H
         el = time.perf_counter() - t0
@@ -320,7 +418,62 @@ def cpu_oracle_sample(w, min_seconds=10.0, max_reps=60):
             "fwd_ms_per_rep": t_fwd / reps * 1e3, "fwd_bwd_ms_per_rep": el / reps * 1e3,
             "single_thread": {"sample": f"one (batch, head) sequence of {w.name}, {w.L} tokens",
                               "fwd_ms": (tb - ta) * 1e3, "fwd_bwd_ms": (tc_ - ta) * 1e3,
-                              "tokens_per_s": w.L / (tc_ - ta)}}
+                              "tokens_per_s": w.L / (tc_ - ta)},
+            "_ref": first, "_nb": nb}
+
+
+GRAD_KEYS = {"q": "dq", "k": "dk", "v": "dv", "log_alpha": "dlog_alpha", "h0": "dh0"}
+
+
+def _rel(x, ref):
+    import numpy as np
+    x = np.asarray(x, np.float64)
+    ref = np.asarray(ref, np.float64)
+    den = float(np.max(np.abs(ref))) if ref.size else 0.0
+    num = float(np.max(np.abs(x - ref))) if ref.size else 0.0
+    return num / den if den > 0 else num
+
+
+def oracle_accuracy(w, out, grads, ref=None, nb=None):
+    """The accuracy fields of a bench record, as the benchmark pages keep them
+    beside each timing: rel_err = max|x - ref| / max|ref| of the output and of
+    each gradient against the float64 oracle, on a sample of the workload,
+    computed outside the timed region; residual_mb = 0 (nothing is kept
+    between the forward and the backward: the backward recomputes its
+    states).  out / grads: the GPU results for the whole workload (host numpy
+    arrays; grads None for a forward alone).  ref: the oracle's (out, grads)
+    on batch entries 0..nb-1, when the CPU baseline has computed them; else
+    the oracle runs here on one (batch 0, group 0) unit."""
+    import numpy as np
+    from oracle import ssd_bwd_ref, ssd_fwd_ref
+    from ssd_chunked_scan_gb300.inputs import workload_inputs
+    hpg = w.H // w.G
+    if ref is not None:
+        sel = lambda x, kind: x[:nb]
+        sample = f"batch entries 0..{nb - 1} of {w.name}, every head"
+        r_out, r_g = ref
+    else:
+        gs, hs = slice(0, 1), slice(0, hpg)
+
+        def sel(x, kind):
+            if kind == "qk":
+                return np.ascontiguousarray(x[:1, :, gs])
+            if kind == "h":
+                return np.ascontiguousarray(x[:1, hs])
+            return np.ascontiguousarray(x[:1, :, hs])
+        q, k, v, la, h0, dout = workload_inputs(w)
+        uq, uk, uv, ula, uh0, udo = (sel(q, "qk"), sel(k, "qk"), sel(v, "v"), sel(la, "v"),
+                                     sel(h0, "h"), sel(dout, "v"))
+        r_out = ssd_fwd_ref(uq, uk, uv, ula, uh0)
+        r_g = ssd_bwd_ref(uq, uk, uv, ula, uh0, udo) if grads is not None else None
+        sample = f"batch entry 0, group 0 of {w.name} ({hpg} heads x {w.L} tokens)"
+    kinds = {"dq": "qk", "dk": "qk", "dv": "v", "dlog_alpha": "v", "dh0": "h"}
+    acc = {"rel_err": _rel(sel(out, "v"), r_out),
+           "rel_err_grads": None if grads is None else
+           {a: _rel(sel(grads[g], kinds[g]), r_g[g]) for a, g in GRAD_KEYS.items()},
+           "residual_mb": 0.0,
+           "accuracy_sample": sample + ", float64 oracle, max|x - ref| / max|ref| per tensor"}
+    return acc
 
 
 def max_over_ranks(x, device=None):
@@ -609,8 +762,10 @@ def run_mamba(args):
     else:
         roof = {"bound": "hbm", "achieved": kb / (per / 1e3) / 1e9, "peak": peaks["hbm_gbs"],
                 "unit": "GB/s", "peak_note": f"{peaks['source']} copy bandwidth"}
+    traffic, traffic_src = (traffic_of(top_name) if w.name == MAMBA_WORKLOAD
+                            else (None, "captured at the default workload only"))
     roof.update({"frac": roof["achieved"] / roof["peak"],
-                 "traffic": MAMBA_TRAFFIC.get(top_name) if w.name == MAMBA_WORKLOAD else None,
+                 "traffic": traffic, "traffic_source": traffic_src,
                  "kernel": top_name,
                  "kernel_ms_per_launch": per, "alg_bytes_per_launch": kb,
                  "alg_exp_per_launch": kx})
@@ -785,6 +940,8 @@ def main():
                     help="override the workload's chunk length (1: the sequential kernels)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-accuracy", action="store_true",
+                    help="skip the rel_err fields (the float64 oracle on a sample of the workload)")
     ap.add_argument("--mode", default="fwd_bwd", choices=["fwd_bwd", "fwd", "max_len"],
                     help="fwd times ssd_fwd alone (a step is then one forward pass); "
                          "max_len finds the largest sequence length fwd_bwd runs at")
@@ -909,6 +1066,12 @@ def main():
         ssd.ssd_trace_reset()
     clocks.stop()
     clk = clocks.summary(th0, th1)
+    # the results of these steps, for the accuracy fields (compared with the
+    # oracle after everything timed has run)
+    want_acc = rank == 0 and not args.no_accuracy
+    res_out = out.cpu().numpy() if want_acc else None
+    res_grads = ({n: t.cpu().numpy() for n, t in grads.items()}
+                 if want_acc and args.mode == "fwd_bwd" else None)
 
     # fwd alone (context line)
     torch.cuda.synchronize(dev)
@@ -935,33 +1098,59 @@ def main():
                       "workspace pool during the call",
     }
 
-    # end to end through the public API: pinned host inputs -> device, fwd+bwd,
-    # out and every gradient -> pinned host, every step
+    # end to end through the public API: every step copies its inputs from
+    # pinned host memory to the device and its output and every gradient back
+    # to pinned host memory.  Two sets of device buffers alternate between
+    # steps, and the copies run on two copy streams (one per direction), so
+    # that step i + 1's inputs arrive and step i - 1's results leave while
+    # step i computes; events order each buffer's reuse.
     e2e = None
     if not args.no_e2e:
+        fb = args.mode == "fwd_bwd"
         h_out = torch.empty(out.shape, pin_memory=True)
         h_grads = {n: torch.empty(t.shape, pin_memory=True) for n, t in grads.items()}
-        dq_, dk_, dv_, dla_, dh0_ = (torch.empty_like(t) for t in (q, k, v, la, h0))
-        dbufs = [torch.empty_like(t) for t in (q, k, v, la, h0, dout)]
+        ins = [[torch.empty_like(t) for t in (q, k, v, la, h0, dout)] for _ in range(2)]
+        outs = [torch.empty_like(out) for _ in range(2)]
+        gsets = [{n: torch.empty_like(t) for n, t in grads.items()} for _ in range(2)]
+        s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+        ev = lambda: torch.cuda.Event()
+        in_ready, in_free = [ev(), ev()], [ev(), ev()]      # inputs landed / consumed
+        res_ready, res_free = [ev(), ev()], [ev(), ev()]    # results written / copied out
+        for e_ in in_free + res_free:
+            e_.record(stream)
 
-        def e2e_step():
-            for d, hsrc in zip(dbufs, host):
-                d.copy_(hsrc, non_blocking=True)
-            o = ssd.ssd_fwd(*dbufs[:5], chunk=w.chunk, out=out)
-            h_out.copy_(o, non_blocking=True)
-            if args.mode == "fwd_bwd":
-                g = ssd.ssd_bwd(*dbufs, chunk=w.chunk, grads=grads)
-                for n in h_grads:
-                    h_grads[n].copy_(g[n], non_blocking=True)
-        fb = args.mode == "fwd_bwd"
-        for _ in range(2):
-            e2e_step()
+        def e2e_step(i):
+            b = i & 1
+            with torch.cuda.stream(s_in):
+                s_in.wait_event(in_free[b])
+                for d, hsrc in zip(ins[b], host if fb else host[:5]):
+                    d.copy_(hsrc, non_blocking=True)
+                in_ready[b].record(s_in)
+            stream.wait_event(in_ready[b])
+            stream.wait_event(res_free[b])
+            ssd.ssd_fwd(*ins[b][:5], chunk=w.chunk, out=outs[b])
+            if fb:
+                ssd.ssd_bwd(*ins[b], chunk=w.chunk, grads=gsets[b])
+            in_free[b].record(stream)
+            res_ready[b].record(stream)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(res_ready[b])
+                h_out.copy_(outs[b], non_blocking=True)
+                if fb:
+                    for n in h_grads:
+                        h_grads[n].copy_(gsets[b][n], non_blocking=True)
+                res_free[b].record(s_out)
+
+        for i in range(2):
+            e2e_step(i)
         torch.cuda.synchronize(dev)
         barrier()
         g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         g0.record(stream)
-        for _ in range(args.steps):
-            e2e_step()
+        s_in.wait_stream(stream)
+        for i in range(args.steps):
+            e2e_step(i)
+        stream.wait_stream(s_out)
         g1.record(stream)
         torch.cuda.synchronize(dev)
         barrier()
@@ -969,7 +1158,9 @@ def main():
         h2d = sum(x.numel() * x.element_size() for x in (host if fb else host[:5]))
         d2h = h_out.numel() * 4 + (sum(x.numel() * x.element_size() for x in h_grads.values()) if fb else 0)
         e2e = {"value": job_tokens_per_s(w.tokens, world, e2e_ms), "unit": "tokens/s",
-               "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+               "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "staging": "two device buffer sets; host-to-device and device-to-host copies "
+                          "on their own streams, overlapping the neighbouring steps' compute"}
 
     if rank != 0:
         if world > 1:
@@ -1024,8 +1215,18 @@ def main():
                          "rtx3090_fwd_ms": PAGE_FWD_MS.get(w.name),
                          "rtx3090_chunked_peak_mb": PAGE_PEAK_MB if w.name == WORKLOAD else None},
     }
+    ref = None
     if world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_oracle_sample(w)
+        cb = cpu_oracle_sample(w)
+        ref, ref_nb = cb.pop("_ref"), cb.pop("_nb")
+        line["cpu_baseline"] = cb
+    if want_acc:
+        if ref is not None:
+            acc = oracle_accuracy(w, res_out, res_grads, ref=(ref[0], ref[1] if res_grads else None),
+                                  nb=ref_nb)
+        else:
+            acc = oracle_accuracy(w, res_out, res_grads)
+        line.update(acc)
     print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()

@@ -99,8 +99,11 @@ typedef enum ssd_status {
   SSD_ERR_TIMEOUT = 7,      /* a device-side bounded wait gave up (see
                                ssd_last_device_error) */
   SSD_ERR_CUDA = 8,         /* another CUDA runtime error (no device, ...) */
-  SSD_ERR_SCRATCH = 9       /* the problem needs more scratch than
+  SSD_ERR_SCRATCH = 9,      /* the problem needs more scratch than
                                ssd_fwd_noalloc's fixed buffer holds */
+  SSD_ERR_CHECK = 10        /* a device-side index check failed (libraries
+                               built with SSD_CHECK only; see
+                               ssd_last_device_error) */
 } ssd_status;
 
 typedef enum ssd_path { SSD_PATH_TC = 0, SSD_PATH_SIMT = 1 } ssd_path;
@@ -180,7 +183,11 @@ SSD_API int ssd_bwd_ex(const float *q, const float *k, const float *v,
  * The problem must fit: B*H*ceil(L/chunk)*(dk*dv + 1)*4 bytes at most
  * (for example B*H*L <= 32768 at dk = dv = 128, chunk 64); larger problems
  * return SSD_ERR_SCRATCH before anything is enqueued.
- *   - It never calls cudaMalloc, cudaFree or any allocating routine.
+ *   - It never calls cudaMalloc, cudaFree or any allocating routine.  Its
+ *     launches are counted by ssd_launch_count but never traced: it records
+ *     no events even while ssd_trace_enable(1) is in force.
+ *   - Its argument checks are ssd_fwd's (the same code, in the same order),
+ *     with chunk == 1 (the sequential kernels) refused as SSD_ERR_CHUNK.
  *   - The first call on a device looks up the array's device address on that
  *     device; make that first call before any stream capture.
  *   - Every call on a device shares the one array: calls that overlap on the
@@ -241,11 +248,25 @@ SSD_API int ssd_get_overlap(void);
 SSD_API const char *ssd_strerror(int status);
 
 /* Synchronises `stream`, then reads and clears the library's device error
- * word on the current device.  Returns SSD_ERR_TIMEOUT when a bounded
+ * words on the current device.  Returns SSD_ERR_TIMEOUT when a bounded
  * device-side wait gave up since the last check (the affected outputs are
- * then unspecified), SSD_ERR_CUDA when the synchronisation itself failed,
- * SSD_OK otherwise. */
+ * then unspecified), SSD_ERR_CHECK when (in a library built with -DSSD_CHECK,
+ * whose kernels test every global index against its buffer's size) an index
+ * check failed and its access was skipped, SSD_ERR_CUDA when the
+ * synchronisation itself failed, SSD_OK otherwise. */
 SSD_API int ssd_last_device_error(ssd_stream_t stream);
+
+/* Test switch for the failure path of the tensor-core kernels' bounded waits
+ * (not needed for the op).  While `on` is nonzero, the epilogue of every
+ * tensor-core walk CTA waits, at its second chunk, on a barrier that nothing
+ * completes.  That wait gives up after its limit (about 2^31 SM cycles, about
+ * a second), every role of the CTA leaves its loop, the tile loads and MMAs
+ * still in flight are drained, tensor memory is freed and the kernel returns;
+ * ssd_last_device_error then reports SSD_ERR_TIMEOUT and the outputs of the
+ * calls made meanwhile are unspecified.  It writes a device variable of the
+ * current device with a synchronous copy, so it applies to calls enqueued
+ * after it returns.  Returns SSD_ERR_CUDA when that copy fails. */
+SSD_API int ssd_test_stall_walks(int on);
 
 /* Launch accounting and tracing (for profiling; not needed for the op).
  * ssd_launch_count: kernels launched by this library in this process so far.

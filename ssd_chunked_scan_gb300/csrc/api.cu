@@ -9,10 +9,17 @@
 #include "common.cuh"
 #include "mamba.h"
 #include "seq.h"
+#include "api_checks.h"
 #include "simt.h"
 #include "tc.h"
 
 namespace {
+
+using ssd::abi::check_common;
+using ssd::abi::check_path_shape;
+using ssd::abi::from_cuda;
+using ssd::abi::make_geo;
+using ssd::abi::misaligned;
 
 std::atomic<int> g_path{-1};
 
@@ -28,8 +35,6 @@ int current_path() {
   return p;
 }
 
-bool misaligned(const void *p) { return p && (reinterpret_cast<uintptr_t>(p) & 15u); }
-
 // Host-side fault injection for tests of the error path: with
 // SSD_FAULT_ALLOC=1 in the environment every workspace request fails before
 // anything is enqueued.
@@ -38,55 +43,12 @@ bool alloc_fault_injected() {
   return e && e[0] == '1';
 }
 
-int check_common(int64_t B, int64_t L, int64_t G, int64_t H, int64_t dk, int64_t dv,
-                 int64_t chunk) {
-  if (B < 0 || L < 0 || G < 1 || H < 1 || dk < 1 || dv < 1 || chunk < 1) return SSD_ERR_ARG;
-  if (H % G != 0) return SSD_ERR_ARG;
-  if (B > 65535 || H > 65535 || G > 65535) return SSD_ERR_UNSUPPORTED;
-  return SSD_OK;
-}
-
 // Which kernels serve a call: chunk == 1 is the sequential evaluation on every
 // path; otherwise the selected path's chunked kernels.
 enum class Impl { TC, SIMT, SEQ };
 Impl impl_of(int path, int64_t chunk) {
   if (chunk == 1) return Impl::SEQ;
   return path == SSD_PATH_SIMT ? Impl::SIMT : Impl::TC;
-}
-
-int check_path_shape(int path, int64_t B, int64_t L, int64_t dk, int64_t dv, int64_t chunk) {
-  if (chunk == 1) {
-    if (dk > 128 || dv > 128) return SSD_ERR_UNSUPPORTED;
-  } else if (path == SSD_PATH_SIMT) {
-    if (chunk != 16 && chunk != 32 && chunk != 64) return SSD_ERR_CHUNK;
-    if (dk > 128 || dv > 128) return SSD_ERR_UNSUPPORTED;
-  } else {
-    int rc = ssd::tc::check_shape(dk, dv, chunk);
-    if (rc) return rc;
-    if (B * L >= ((int64_t)1 << 31)) return SSD_ERR_UNSUPPORTED;  // 32-bit TMA row index
-  }
-  if (ssd::cdiv(L, chunk) > 0x7fffffffLL) return SSD_ERR_UNSUPPORTED;
-  return SSD_OK;
-}
-
-ssd::Geo make_geo(int64_t B, int64_t L, int64_t G, int64_t H, int64_t dk, int64_t dv,
-                  int64_t chunk) {
-  ssd::Geo g;
-  g.B = B; g.L = L; g.G = G; g.H = H; g.dk = dk; g.dv = dv;
-  g.C = (int)chunk;
-  g.N = ssd::cdiv(L, chunk);
-  g.hpg = (int)(H / G);
-  return g;
-}
-
-int from_cuda(cudaError_t e) {
-  if (e == cudaSuccess) return SSD_OK;
-  if (e == cudaErrorMemoryAllocation) return SSD_ERR_ALLOC;
-  if (e == cudaErrorLaunchFailure || e == cudaErrorInvalidConfiguration ||
-      e == cudaErrorLaunchOutOfResources || e == cudaErrorInvalidDeviceFunction ||
-      e == cudaErrorNoKernelImageForDevice || e == cudaErrorInvalidValue)
-    return SSD_ERR_LAUNCH;
-  return SSD_ERR_CUDA;
 }
 
 // Stream-ordered workspace.  The first use on a device raises that device's
@@ -134,6 +96,7 @@ const char *ssd_strerror(int status) {
     case SSD_ERR_TIMEOUT: return "a device-side bounded wait timed out";
     case SSD_ERR_CUDA: return "CUDA runtime error";
     case SSD_ERR_SCRATCH: return "problem too large for the fixed scratch of ssd_fwd_noalloc";
+    case SSD_ERR_CHECK: return "a device-side index check failed (debug build)";
     default: return "unknown status";
   }
 }
@@ -369,9 +332,16 @@ int ssd_mamba_bwd(const float *x, const float *delta, const float *A, const floa
 int ssd_last_device_error(ssd_stream_t stream) {
   cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return SSD_ERR_CUDA;
-  unsigned int word = 0;
+  unsigned int word = 0, sw = 0;
   if (ssd::tc::read_and_clear_error(&word) != cudaSuccess) return SSD_ERR_CUDA;
-  return word ? SSD_ERR_TIMEOUT : SSD_OK;
+  if (ssd::simt::read_and_clear_error(&sw) != cudaSuccess) return SSD_ERR_CUDA;
+  word |= sw;
+  if (word & 1u) return SSD_ERR_TIMEOUT;
+  return word ? SSD_ERR_CHECK : SSD_OK;
+}
+
+int ssd_test_stall_walks(int on) {
+  return ssd::tc::set_test_stall(on) == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
 }
 
 }  // extern "C"

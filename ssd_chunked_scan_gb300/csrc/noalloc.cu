@@ -8,6 +8,7 @@
 #include <mutex>
 
 #include "../../include/ssd.h"
+#include "api_checks.h"
 #include "common.cuh"
 #include "simt.h"
 
@@ -44,8 +45,6 @@ cudaError_t scratch_address(void **out) {
   return cudaSuccess;
 }
 
-bool misaligned(const void *p) { return p && (reinterpret_cast<uintptr_t>(p) & 15u); }
-
 }  // namespace
 
 extern "C" {
@@ -56,21 +55,19 @@ SSD_API int ssd_fwd_noalloc(const float *q, const float *k, const float *v,
                             const float *log_alpha, const float *h0, float *out, int64_t B,
                             int64_t L, int64_t G, int64_t H, int64_t dk, int64_t dv,
                             int64_t chunk, ssd_stream_t stream) {
-  if (B < 0 || L < 0 || G < 1 || H < 1 || dk < 1 || dv < 1 || chunk < 1 || H % G != 0)
-    return SSD_ERR_ARG;
-  if (B > 65535 || H > 65535) return SSD_ERR_UNSUPPORTED;
-  if (chunk != 16 && chunk != 32 && chunk != 64) return SSD_ERR_CHUNK;
-  if (dk > 128 || dv > 128) return SSD_ERR_UNSUPPORTED;
-  if (B == 0 || L == 0) return SSD_OK;
-  if (!q || !k || !v || !log_alpha || !out) return SSD_ERR_ARG;
+  using namespace ssd::abi;
+  // the same checks, in the same order, as ssd_fwd on the all-fp32 path
+  int rc = check_common(B, L, G, H, dk, dv, chunk);
+  if (rc) return rc;
+  if (chunk == 1) return SSD_ERR_CHUNK;  // (ssd_fwd's sequential kernels are not served here)
+  rc = check_path_shape(SSD_PATH_SIMT, B, L, dk, dv, chunk);
+  if (rc) return rc;
   if (misaligned(q) || misaligned(k) || misaligned(v) || misaligned(log_alpha) ||
       misaligned(h0) || misaligned(out))
     return SSD_ERR_ALIGN;
-  ssd::Geo g;
-  g.B = B; g.L = L; g.G = G; g.H = H; g.dk = dk; g.dv = dv;
-  g.C = (int)chunk;
-  g.N = ssd::cdiv(L, chunk);
-  g.hpg = (int)(H / G);
+  if (B == 0 || L == 0) return SSD_OK;
+  if (!q || !k || !v || !log_alpha || !out) return SSD_ERR_ARG;
+  const ssd::Geo g = make_geo(B, L, G, H, dk, dv, chunk);
   // B*H*N*(dk*dv + 1) floats, checked without overflow
   const long double need = (long double)B * H * g.N * ((long double)dk * dv + 1) * 4;
   if (need > (long double)kScratchBytes || ssd::simt::fwd_workspace_bytes(g) > kScratchBytes)
@@ -80,13 +77,10 @@ SSD_API int ssd_fwd_noalloc(const float *q, const float *k, const float *v,
     cudaGetLastError();
     return SSD_ERR_CUDA;
   }
-  cudaError_t e = ssd::simt::fwd(q, k, v, log_alpha, h0, out, nullptr, g, ws,
-                                 reinterpret_cast<cudaStream_t>(stream));
-  if (e == cudaSuccess) return SSD_OK;
-  return (e == cudaErrorInvalidConfiguration || e == cudaErrorLaunchOutOfResources ||
-          e == cudaErrorInvalidDeviceFunction || e == cudaErrorNoKernelImageForDevice)
-             ? SSD_ERR_LAUNCH
-             : SSD_ERR_CUDA;
+  // no trace events here, even with tracing on: recording them allocates
+  ssd::LaunchTrace::Quiet quiet;
+  return from_cuda(ssd::simt::fwd(q, k, v, log_alpha, h0, out, nullptr, g, ws,
+                                  reinterpret_cast<cudaStream_t>(stream)));
 }
 
 }  // extern "C"

@@ -43,7 +43,8 @@ __host__ __device__ constexpr int ldn(int nb) { return 64 * nb + 4; }
 
 // Stage dst[kk * ld + m] = src(k0 + kk, m) * kscale[kk] * mscale[m] for
 // kk < KS, m < ld, zero outside kk < kmax - k0, m < mmax.  src(k, m) =
-// src[k * sk + m * sm].  MCONTIG selects which index consecutive threads walk
+// src[k * sk + m * sm]; avail: elements from src to the end of its buffer
+// (debug-build index checks).  MCONTIG selects which index consecutive threads walk
 // (the one that is contiguous in global memory).
 // Each thread issues the global loads of U elements before it stores any of
 // them, so a stage costs about one memory round trip per U elements (16 by
@@ -51,7 +52,7 @@ __host__ __device__ constexpr int ldn(int nb) { return 64 * nb + 4; }
 constexpr int SU_ST = 16;
 template <bool MCONTIG, int U = SU_ST>
 __device__ inline void stage(float *__restrict__ dst, int ld, const float *__restrict__ src,
-                             int64_t sk, int64_t sm, int k0, int kmax, int mmax,
+                             int64_t avail, int64_t sk, int64_t sm, int k0, int kmax, int mmax,
                              const float *kscale, const float *mscale) {
   const int total = KS * ld;
   for (int base = threadIdx.x; base < total; base += U * NT) {
@@ -63,7 +64,7 @@ __device__ inline void stage(float *__restrict__ dst, int ld, const float *__res
       if (MCONTIG) { kk[u] = idx / ld; m[u] = idx - kk[u] * ld; }
       else { m[u] = idx / KS; kk[u] = idx - m[u] * KS; }
       const int kg = k0 + kk[u];
-      x[u] = (idx < total && kg < kmax && m[u] < mmax) ? src[(int64_t)kg * sk + (int64_t)m[u] * sm] : 0.f;
+      x[u] = (idx < total && kg < kmax && m[u] < mmax) ? LDC(src, (int64_t)kg * sk + (int64_t)m[u] * sm, avail) : 0.f;
     }
 #pragma unroll
     for (int u = 0; u < U; ++u) {
@@ -135,24 +136,25 @@ __global__ void __launch_bounds__(NT) k_chunk_state(const float *__restrict__ X,
   const int64_t grp = h / g.hpg, bh = b * g.H + h;
   const int64_t t0 = c * g.C;
   const int len = (int)(g.L - t0 < g.C ? g.L - t0 : g.C);
-  chunk_cumsum64(la, la_off(g, b, t0, h), g.H, len, cs);
+  chunk_cumsum64(la, n_la(g), la_off(g, b, t0, h), g.H, len, cs);
   const float A = cs[len - 1];
   if (threadIdx.x < len) sc[threadIdx.x] = QUERY ? expf(cs[threadIdx.x]) : expf(A - cs[threadIdx.x]);
-  if (!QUERY && threadIdx.x == 0) Adec[bh * g.N + c] = A;
+  if (!QUERY && threadIdx.x == 0) STC(Adec, bh * g.N + c, g.B * g.H * g.N, A);
   __syncthreads();
 
   float acc[4 * MA][4 * NB];
   zero_acc<MA, NB>(acc);
   const float *xs = X + qk_off(g, b, t0, grp);
   const float *ys = Y + v_off(g, b, t0, h);
+  const int64_t ax = n_qk(g) - qk_off(g, b, t0, grp), ay = n_v(g) - v_off(g, b, t0, h);
   for (int k0 = 0; k0 < len; k0 += KS) {
-    stage<true>(As, ldn(MA), xs, g.G * g.dk, 1, k0, len, (int)g.dk, nullptr, nullptr);
-    stage<true>(Bs, ldn(NB), ys, g.H * g.dv, 1, k0, len, (int)g.dv, sc, nullptr);
+    stage<true>(As, ldn(MA), xs, ax, g.G * g.dk, 1, k0, len, (int)g.dk, nullptr, nullptr);
+    stage<true>(Bs, ldn(NB), ys, ay, g.H * g.dv, 1, k0, len, (int)g.dv, sc, nullptr);
     __syncthreads();
     mma_slice<MA, NB>(acc, As, ldn(MA), Bs, ldn(NB), min(KS, len - k0));
     __syncthreads();
   }
-  float *dst = states + st_off(g, bh, c);
+  const int64_t dst = st_off(g, bh, c), nst = n_st(g);
 #pragma unroll
   for (int r = 0; r < 4 * MA; ++r) {
     const int i = row_of(r);
@@ -160,7 +162,7 @@ __global__ void __launch_bounds__(NT) k_chunk_state(const float *__restrict__ X,
 #pragma unroll
     for (int cc = 0; cc < 4 * NB; ++cc) {
       const int j = col_of(cc);
-      if (j < g.dv) dst[(int64_t)i * g.dv + j] = acc[r][cc];
+      if (j < g.dv) STC(states, dst + (int64_t)i * g.dv + j, nst, acc[r][cc]);
     }
   }
 }
@@ -177,19 +179,20 @@ __global__ void __launch_bounds__(NT) k_chunk_state(const float *__restrict__ X,
 // grid (B*H, ceil(dk*dv / (V*NT)))
 constexpr int SCU = 8;
 
+// (a: element offset into p's buffer of n elements, a multiple of V)
 template <int V>
-__device__ inline void ld_v(float (&x)[V], const float *p) {
+__device__ inline void ld_v(float (&x)[V], const float *p, int64_t a, int64_t n) {
   if constexpr (V == 4) {
-    const float4 f = *reinterpret_cast<const float4 *>(p);
+    const float4 f = LDC(reinterpret_cast<const float4 *>(p), a / 4, n / 4);
     x[0] = f.x; x[1] = f.y; x[2] = f.z; x[3] = f.w;
   } else {
-    x[0] = *p;
+    x[0] = LDC(p, a, n);
   }
 }
 template <int V>
-__device__ inline void st_v(float *p, const float (&x)[V]) {
-  if constexpr (V == 4) *reinterpret_cast<float4 *>(p) = make_float4(x[0], x[1], x[2], x[3]);
-  else *p = x[0];
+__device__ inline void st_v(float *p, int64_t a, int64_t n, const float (&x)[V]) {
+  if constexpr (V == 4) STC(reinterpret_cast<float4 *>(p), a / 4, n / 4, make_float4(x[0], x[1], x[2], x[3]));
+  else STC(p, a, n, x[0]);
 }
 
 template <int V, bool REV>
@@ -203,8 +206,8 @@ __global__ void __launch_bounds__(NT) k_scan(float *__restrict__ states,
   if (e0 >= sz) return;
   float run[V];
 #pragma unroll
-  for (int j = 0; j < V; ++j) run[j] = init ? init[bh * sz + e0 + j] : 0.f;
-  float *p = states + st_off(g, bh, 0) + e0;
+  for (int j = 0; j < V; ++j) run[j] = init ? LDC(init, bh * sz + e0 + j, n_h(g)) : 0.f;
+  const int64_t p0 = st_off(g, bh, 0) + e0, nst = n_st(g);
   const float *a = Adec + bh * g.N;
   for (int64_t k0 = 0; k0 < g.N; k0 += SCU) {
     float x[SCU][V], d[SCU];
@@ -213,8 +216,8 @@ __global__ void __launch_bounds__(NT) k_scan(float *__restrict__ states,
       const int64_t k = k0 + u;
       if (k < g.N) {
         const int64_t c = REV ? g.N - 1 - k : k;
-        ld_v<V>(x[u], p + c * sz);
-        d[u] = expf(a[c]);
+        ld_v<V>(x[u], states, p0 + c * sz, nst);
+        d[u] = expf(LDC(a, c, g.N));
       }
     }
 #pragma unroll
@@ -222,7 +225,7 @@ __global__ void __launch_bounds__(NT) k_scan(float *__restrict__ states,
       const int64_t k = k0 + u;
       if (k < g.N) {
         const int64_t c = REV ? g.N - 1 - k : k;
-        st_v<V>(p + c * sz, run);
+        st_v<V>(states, p0 + c * sz, nst, run);
 #pragma unroll
         for (int j = 0; j < V; ++j) run[j] = fmaf(d[u], run[j], x[u][j]);
       }
@@ -230,7 +233,7 @@ __global__ void __launch_bounds__(NT) k_scan(float *__restrict__ states,
   }
   if (fin) {
 #pragma unroll
-    for (int j = 0; j < V; ++j) fin[bh * sz + e0 + j] = run[j];
+    for (int j = 0; j < V; ++j) STC(fin, bh * sz + e0 + j, n_h(g), run[j]);
   }
 }
 
@@ -251,12 +254,13 @@ static void launch_scan(float *st, const float *Adec, const float *init, float *
 // ---------------------------------------------------------------------------
 // Raw q.k scores of one chunk into registers: acc[t][s] (rows t, cols s).
 template <int U = SU_ST>
-__device__ inline void chunk_scores(float (&acc)[4][4], const float *qs, const float *ks,
+// (aqk: elements from qs, and from ks, to the ends of their buffers)
+__device__ inline void chunk_scores(float (&acc)[4][4], const float *qs, const float *ks, int64_t aqk,
                                     float *As, float *Bs, const Geo &g, int len) {
   zero_acc<1, 1>(acc);
   for (int i0 = 0; i0 < g.dk; i0 += KS) {
-    stage<false, U>(As, LDT, qs + i0, 1, g.G * g.dk, 0, (int)g.dk - i0, len, nullptr, nullptr);
-    stage<false, U>(Bs, LDT, ks + i0, 1, g.G * g.dk, 0, (int)g.dk - i0, len, nullptr, nullptr);
+    stage<false, U>(As, LDT, qs + i0, aqk - i0, 1, g.G * g.dk, 0, (int)g.dk - i0, len, nullptr, nullptr);
+    stage<false, U>(Bs, LDT, ks + i0, aqk - i0, 1, g.G * g.dk, 0, (int)g.dk - i0, len, nullptr, nullptr);
     __syncthreads();
     mma_slice<1, 1>(acc, As, LDT, Bs, LDT, min(KS, (int)g.dk - i0));
     __syncthreads();
@@ -279,13 +283,15 @@ __global__ void __launch_bounds__(NT) k_chunk_out(const float *__restrict__ q,
   const int64_t grp = h / g.hpg, bh = b * g.H + h;
   const int64_t t0 = c * g.C;
   const int len = (int)(g.L - t0 < g.C ? g.L - t0 : g.C);
-  chunk_cumsum64(la, la_off(g, b, t0, h), g.H, len, cs);
+  chunk_cumsum64(la, n_la(g), la_off(g, b, t0, h), g.H, len, cs);
   if (threadIdx.x < len) ecs[threadIdx.x] = expf(cs[threadIdx.x]);
   const float *qs = q + qk_off(g, b, t0, grp);
   const float *ks = k + qk_off(g, b, t0, grp);
+  const int64_t aqk = n_qk(g) - qk_off(g, b, t0, grp), av = n_v(g) - v_off(g, b, t0, h);
+  const int64_t ast = n_st(g) - st_off(g, bh, c);
 
   float sc[4][4];
-  chunk_scores<8>(sc, qs, ks, As, Bs, g, len);
+  chunk_scores<8>(sc, qs, ks, aqk, As, Bs, g, len);
 #pragma unroll
   for (int r = 0; r < 4; ++r) {
     const int t = row_of(r);
@@ -303,20 +309,21 @@ __global__ void __launch_bounds__(NT) k_chunk_out(const float *__restrict__ q,
   zero_acc<1, NB>(acc);
   const float *vs = v + v_off(g, b, t0, h);
   for (int s0 = 0; s0 < len; s0 += KS) {
-    stage<true, 8>(Bs, ldn(NB), vs, g.H * g.dv, 1, s0, len, (int)g.dv, nullptr, nullptr);
+    stage<true, 8>(Bs, ldn(NB), vs, av, g.H * g.dv, 1, s0, len, (int)g.dv, nullptr, nullptr);
     __syncthreads();
     mma_slice<1, NB>(acc, Pt + s0 * LDT, LDT, Bs, ldn(NB), min(KS, len - s0));
     __syncthreads();
   }
   const float *Hs = states + st_off(g, bh, c);
   for (int i0 = 0; i0 < g.dk; i0 += KS) {
-    stage<false, 8>(As, LDT, qs + i0, 1, g.G * g.dk, 0, (int)g.dk - i0, len, nullptr, ecs);
-    stage<true, 8>(Bs, ldn(NB), Hs + (int64_t)i0 * g.dv, g.dv, 1, 0, (int)g.dk - i0, (int)g.dv, nullptr, nullptr);
+    stage<false, 8>(As, LDT, qs + i0, aqk - i0, 1, g.G * g.dk, 0, (int)g.dk - i0, len, nullptr, ecs);
+    stage<true, 8>(Bs, ldn(NB), Hs + (int64_t)i0 * g.dv, ast - (int64_t)i0 * g.dv, g.dv, 1, 0, (int)g.dk - i0,
+                   (int)g.dv, nullptr, nullptr);
     __syncthreads();
     mma_slice<1, NB>(acc, As, LDT, Bs, ldn(NB), min(KS, (int)g.dk - i0));
     __syncthreads();
   }
-  float *os = out + v_off(g, b, t0, h);
+  const int64_t os = v_off(g, b, t0, h), nv = n_v(g);
 #pragma unroll
   for (int r = 0; r < 4; ++r) {
     const int t = row_of(r);
@@ -324,15 +331,16 @@ __global__ void __launch_bounds__(NT) k_chunk_out(const float *__restrict__ q,
 #pragma unroll
     for (int cc = 0; cc < 4 * NB; ++cc) {
       const int j = col_of(cc);
-      if (j < g.dv) os[(int64_t)t * g.H * g.dv + j] = acc[r][cc];
+      if (j < g.dv) STC(out, os + (int64_t)t * g.H * g.dv + j, nv, acc[r][cc]);
     }
   }
 }
 
-// Row dot products of a register tile with a global [row][col] matrix,
-// reduced over the 16 threads that share the rows; written to dst[row].
+// Row dot products of a register tile with a global [row][col] matrix (ax
+// elements from x to the end of its buffer), reduced over the 16 threads that
+// share the rows; written to dst[row].
 template <int NB>
-__device__ inline void row_dots(const float (&acc)[4][4 * NB], const float *x, int64_t ldx,
+__device__ inline void row_dots(const float (&acc)[4][4 * NB], const float *x, int64_t ax, int64_t ldx,
                                 int len, int ncols, float *dst) {
 #pragma unroll
   for (int r = 0; r < 4; ++r) {
@@ -342,7 +350,7 @@ __device__ inline void row_dots(const float (&acc)[4][4 * NB], const float *x, i
 #pragma unroll
       for (int cc = 0; cc < 4 * NB; ++cc) {
         const int i = col_of(cc);
-        if (i < ncols) s = fmaf(x[(int64_t)t * ldx + i], acc[r][cc], s);
+        if (i < ncols) s = fmaf(LDC(x, (int64_t)t * ldx + i, ax), acc[r][cc], s);
       }
     }
 #pragma unroll
@@ -351,9 +359,10 @@ __device__ inline void row_dots(const float (&acc)[4][4 * NB], const float *x, i
   }
 }
 
-// Store (first head of the group) or add (later heads) a register tile.
+// Store (first head of the group) or add (later heads) a register tile (ad
+// elements from dst to the end of its buffer).
 template <int NB>
-__device__ inline void store_or_add(const float (&acc)[4][4 * NB], float *dst, int64_t ldd,
+__device__ inline void store_or_add(const float (&acc)[4][4 * NB], float *dst, int64_t ad, int64_t ldd,
                                     int len, int ncols, bool add) {
 #pragma unroll
   for (int r = 0; r < 4; ++r) {
@@ -363,8 +372,8 @@ __device__ inline void store_or_add(const float (&acc)[4][4 * NB], float *dst, i
     for (int cc = 0; cc < 4 * NB; ++cc) {
       const int i = col_of(cc);
       if (i < ncols) {
-        float *p = dst + (int64_t)t * ldd + i;
-        *p = add ? *p + acc[r][cc] : acc[r][cc];
+        const int64_t o = (int64_t)t * ldd + i;
+        STC(dst, o, ad, add ? LDC(dst, o, ad) + acc[r][cc] : acc[r][cc]);
       }
     }
   }
@@ -398,13 +407,14 @@ __global__ void __launch_bounds__(NT, 2) k_chunk_grad(
   const float *ks = k + qk_off(g, b, t0, grp);
   float *dqs = dq + qk_off(g, b, t0, grp);
   float *dks = dk + qk_off(g, b, t0, grp);
+  const int64_t aqk = n_qk(g) - qk_off(g, b, t0, grp);
 
   float sraw[4][4];
-  chunk_scores(sraw, qs, ks, As, Bs, g, len);
+  chunk_scores(sraw, qs, ks, aqk, As, Bs, g, len);
 
   for (int hh = 0; hh < g.hpg; ++hh) {
     const int64_t h = grp * g.hpg + hh, bh = b * g.H + h;
-    chunk_cumsum64(la, la_off(g, b, t0, h), g.H, len, cs);
+    chunk_cumsum64(la, n_la(g), la_off(g, b, t0, h), g.H, len, cs);
     const float A = cs[len - 1];
     if (threadIdx.x < len) {
       w[threadIdx.x] = expf(A - cs[threadIdx.x]);
@@ -414,14 +424,15 @@ __global__ void __launch_bounds__(NT, 2) k_chunk_grad(
     const float *dos = dout + v_off(g, b, t0, h);
     const float *Hc = Hst + st_off(g, bh, c);
     const float *dXc = dXst + st_off(g, bh, c);
+    const int64_t av = n_v(g) - v_off(g, b, t0, h), ast = n_st(g) - st_off(g, bh, c);
 
     // dP[t][s] = dout_t . v_s, then the decayed, causally masked tiles
     {
       float dp[4][4];
       zero_acc<1, 1>(dp);
       for (int j0 = 0; j0 < g.dv; j0 += KS) {
-        stage<false>(As, LDT, dos + j0, 1, ldv, 0, (int)g.dv - j0, len, nullptr, nullptr);
-        stage<false>(Bs, LDT, vs + j0, 1, ldv, 0, (int)g.dv - j0, len, nullptr, nullptr);
+        stage<false>(As, LDT, dos + j0, av - j0, 1, ldv, 0, (int)g.dv - j0, len, nullptr, nullptr);
+        stage<false>(Bs, LDT, vs + j0, av - j0, 1, ldv, 0, (int)g.dv - j0, len, nullptr, nullptr);
         __syncthreads();
         mma_slice<1, 1>(dp, As, LDT, Bs, LDT, min(KS, (int)g.dv - j0));
         __syncthreads();
@@ -447,20 +458,20 @@ __global__ void __launch_bounds__(NT, 2) k_chunk_grad(
       float acc[4][4 * NBK];
       zero_acc<1, NBK>(acc);
       for (int s0 = 0; s0 < len; s0 += KS) {
-        stage<true>(Bs, ldn(NBK), ks, ldqk, 1, s0, len, (int)g.dk, nullptr, nullptr);
+        stage<true>(Bs, ldn(NBK), ks, aqk, ldqk, 1, s0, len, (int)g.dk, nullptr, nullptr);
         __syncthreads();
         mma_slice<1, NBK>(acc, dPmT + s0 * LDT, LDT, Bs, ldn(NBK), min(KS, len - s0));
         __syncthreads();
       }
       for (int j0 = 0; j0 < g.dv; j0 += KS) {
-        stage<false>(As, LDT, dos + j0, 1, ldv, 0, (int)g.dv - j0, len, nullptr, e);
-        stage<false>(Bs, ldn(NBK), Hc + j0, 1, g.dv, 0, (int)g.dv - j0, (int)g.dk, nullptr, nullptr);
+        stage<false>(As, LDT, dos + j0, av - j0, 1, ldv, 0, (int)g.dv - j0, len, nullptr, e);
+        stage<false>(Bs, ldn(NBK), Hc + j0, ast - j0, 1, g.dv, 0, (int)g.dv - j0, (int)g.dk, nullptr, nullptr);
         __syncthreads();
         mma_slice<1, NBK>(acc, As, LDT, Bs, ldn(NBK), min(KS, (int)g.dv - j0));
         __syncthreads();
       }
-      row_dots<NBK>(acc, qs, ldqk, len, (int)g.dk, dcq);
-      store_or_add<NBK>(acc, dqs, ldqk, len, (int)g.dk, hh > 0);
+      row_dots<NBK>(acc, qs, aqk, ldqk, len, (int)g.dk, dcq);
+      store_or_add<NBK>(acc, dqs, aqk, ldqk, len, (int)g.dk, hh > 0);
     }
 
     // dk_h[s][i] = sum_t dPm[t][s] q_t[i] + w_s sum_j v_s[j] dX[i][j]
@@ -468,20 +479,20 @@ __global__ void __launch_bounds__(NT, 2) k_chunk_grad(
       float acc[4][4 * NBK];
       zero_acc<1, NBK>(acc);
       for (int r0 = 0; r0 < len; r0 += KS) {
-        stage<true>(Bs, ldn(NBK), qs, ldqk, 1, r0, len, (int)g.dk, nullptr, nullptr);
+        stage<true>(Bs, ldn(NBK), qs, aqk, ldqk, 1, r0, len, (int)g.dk, nullptr, nullptr);
         __syncthreads();
         mma_slice<1, NBK>(acc, dPm + r0 * LDT, LDT, Bs, ldn(NBK), min(KS, len - r0));
         __syncthreads();
       }
       for (int j0 = 0; j0 < g.dv; j0 += KS) {
-        stage<false>(As, LDT, vs + j0, 1, ldv, 0, (int)g.dv - j0, len, nullptr, w);
-        stage<false>(Bs, ldn(NBK), dXc + j0, 1, g.dv, 0, (int)g.dv - j0, (int)g.dk, nullptr, nullptr);
+        stage<false>(As, LDT, vs + j0, av - j0, 1, ldv, 0, (int)g.dv - j0, len, nullptr, w);
+        stage<false>(Bs, ldn(NBK), dXc + j0, ast - j0, 1, g.dv, 0, (int)g.dv - j0, (int)g.dk, nullptr, nullptr);
         __syncthreads();
         mma_slice<1, NBK>(acc, As, LDT, Bs, ldn(NBK), min(KS, (int)g.dv - j0));
         __syncthreads();
       }
-      row_dots<NBK>(acc, ks, ldqk, len, (int)g.dk, dck);
-      store_or_add<NBK>(acc, dks, ldqk, len, (int)g.dk, hh > 0);
+      row_dots<NBK>(acc, ks, aqk, ldqk, len, (int)g.dk, dck);
+      store_or_add<NBK>(acc, dks, aqk, ldqk, len, (int)g.dk, hh > 0);
     }
 
     // dv[s][j] = sum_t Pm[t][s] dout_t[j] + w_s sum_i k_s[i] dX[i][j]
@@ -489,19 +500,20 @@ __global__ void __launch_bounds__(NT, 2) k_chunk_grad(
       float acc[4][4 * NBV];
       zero_acc<1, NBV>(acc);
       for (int r0 = 0; r0 < len; r0 += KS) {
-        stage<true>(Bs, ldn(NBV), dos, ldv, 1, r0, len, (int)g.dv, nullptr, nullptr);
+        stage<true>(Bs, ldn(NBV), dos, av, ldv, 1, r0, len, (int)g.dv, nullptr, nullptr);
         __syncthreads();
         mma_slice<1, NBV>(acc, Pm + r0 * LDT, LDT, Bs, ldn(NBV), min(KS, len - r0));
         __syncthreads();
       }
       for (int i0 = 0; i0 < g.dk; i0 += KS) {
-        stage<false>(As, LDT, ks + i0, 1, ldqk, 0, (int)g.dk - i0, len, nullptr, w);
-        stage<true>(Bs, ldn(NBV), dXc + (int64_t)i0 * g.dv, g.dv, 1, 0, (int)g.dk - i0, (int)g.dv, nullptr, nullptr);
+        stage<false>(As, LDT, ks + i0, aqk - i0, 1, ldqk, 0, (int)g.dk - i0, len, nullptr, w);
+        stage<true>(Bs, ldn(NBV), dXc + (int64_t)i0 * g.dv, ast - (int64_t)i0 * g.dv, g.dv, 1, 0, (int)g.dk - i0,
+                    (int)g.dv, nullptr, nullptr);
         __syncthreads();
         mma_slice<1, NBV>(acc, As, LDT, Bs, ldn(NBV), min(KS, (int)g.dk - i0));
         __syncthreads();
       }
-      store_or_add<NBV>(acc, dv + v_off(g, b, t0, h), ldv, len, (int)g.dv, false);
+      store_or_add<NBV>(acc, dv + v_off(g, b, t0, h), av, ldv, len, (int)g.dv, false);
     }
     __syncthreads();
 
@@ -518,10 +530,10 @@ __global__ void __launch_bounds__(NT, 2) k_chunk_grad(
         if (l + o < 32) incl += y;
       }
       double after = incl - pair;  // sum over steps > 2l+1
-      float *dl = dla + la_off(g, b, t0, h);
-      if (2 * l < len) dl[(int64_t)(2 * l) * g.H] = (float)(after + pair);
-      if (2 * l + 1 < len) dl[(int64_t)(2 * l + 1) * g.H] = (float)(after + x1);
-      if (l == 0) dcs_sum[bh * g.N + c] = (float)incl;
+      const int64_t dl = la_off(g, b, t0, h), nla = n_la(g);
+      if (2 * l < len) STC(dla, dl + (int64_t)(2 * l) * g.H, nla, (float)(after + pair));
+      if (2 * l + 1 < len) STC(dla, dl + (int64_t)(2 * l + 1) * g.H, nla, (float)(after + x1));
+      if (l == 0) STC(dcs_sum, bh * g.N + c, g.B * g.H * g.N, (float)incl);
     }
     __syncthreads();
   }
@@ -542,7 +554,7 @@ __global__ void __launch_bounds__(NT) k_dla_carry(float *__restrict__ dla,
     if (dhT) {
       const int64_t sz = g.dk * g.dv;
       for (int64_t e = threadIdx.x; e < sz; e += NT)
-        part += (double)dhT[bh * sz + e] * (double)hT[bh * sz + e];
+        part += (double)LDC(dhT, bh * sz + e, n_h(g)) * (double)LDC(hT, bh * sz + e, n_h(g));
     }
     sh[threadIdx.x] = part;
     __syncthreads();
@@ -557,7 +569,7 @@ __global__ void __launch_bounds__(NT) k_dla_carry(float *__restrict__ dla,
   for (int64_t hi = g.N; hi > 0; hi -= NT) {
     const int64_t lo = hi - NT > 0 ? hi - NT : 0;
     const int64_t c = lo + threadIdx.x;
-    double x = (c < hi) ? (double)dcs_sum[bh * g.N + c] : 0.0;
+    double x = (c < hi) ? (double)LDC(dcs_sum, bh * g.N + c, g.B * g.H * g.N) : 0.0;
     sh[threadIdx.x] = x;
     __syncthreads();
     // inclusive suffix scan (Hillis-Steele) over the block
@@ -581,11 +593,11 @@ __global__ void __launch_bounds__(NT) k_dla_carry(float *__restrict__ dla,
         const int64_t i = i0 + (int64_t)u * NT, t = lo * g.C + i;
         in[u] = i < ntok && t < g.L;
         off[u] = in[u] ? la_off(g, b, t, h) : 0;
-        cur[u] = in[u] ? dla[off[u]] : 0.f;
+        cur[u] = in[u] ? LDC(dla, off[u], n_la(g)) : 0.f;
       }
 #pragma unroll
       for (int u = 0; u < 8; ++u)
-        if (in[u]) dla[off[u]] = (float)((double)cur[u] + ex[(i0 + (int64_t)u * NT) / g.C]);
+        if (in[u]) STC(dla, off[u], n_la(g), (float)((double)cur[u] + ex[(i0 + (int64_t)u * NT) / g.C]));
     }
     __syncthreads();
     if (threadIdx.x == 0) carry_in += sh[0];
@@ -691,6 +703,18 @@ cudaError_t bwd(const float *q, const float *k, const float *v, const float *la,
     k_dla_carry<<<(unsigned)(g.B * g.H), NT, 0, s>>>(dla, dcs_sum, dhT, hT, g);
   }
   return cudaGetLastError();
+}
+
+cudaError_t read_and_clear_error(unsigned int *word) {
+  *word = 0;
+#ifdef SSD_CHECK
+  unsigned int zero = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(word, g_check_word, sizeof(unsigned int));
+  if (e != cudaSuccess) return e;
+  return cudaMemcpyToSymbol(g_check_word, &zero, sizeof(unsigned int));
+#else
+  return cudaSuccess;
+#endif
 }
 
 }  // namespace simt

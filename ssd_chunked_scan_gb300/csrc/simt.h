@@ -18,5 +18,9 @@ cudaError_t bwd(const float *q, const float *k, const float *v, const float *la,
                 const float *dout, const float *dhT, float *dq, float *dk, float *dv, float *dla,
                 float *dh0, const Geo &g, void *ws, cudaStream_t s);
 
+// Reads and clears this path's check word (bit 1: a failed index check; only
+// debug builds set it, otherwise the word reads 0).
+cudaError_t read_and_clear_error(unsigned int *word);
+
 }  // namespace simt
 }  // namespace ssd

@@ -85,11 +85,12 @@ __device__ inline double warp_cumsum64_regs(double x0, double x1, int n, double 
 }
 
 // The same, loading la[first + t * stride] for t < n itself.
-__device__ inline double warp_cumsum64(const float *__restrict__ la, int64_t first,
+// (n_la: elements of la, for the debug build's index checks)
+__device__ inline double warp_cumsum64(const float *__restrict__ la, int64_t n_la, int64_t first,
                                        int64_t stride, int n, double carry, float *cs) {
   const int l = threadIdx.x & 31;
-  const double x0 = (2 * l < n) ? (double)la[first + (int64_t)(2 * l) * stride] : 0.0;
-  const double x1 = (2 * l + 1 < n) ? (double)la[first + (int64_t)(2 * l + 1) * stride] : 0.0;
+  const double x0 = (2 * l < n) ? (double)LDC(la, first + (int64_t)(2 * l) * stride, n_la) : 0.0;
+  const double x1 = (2 * l + 1 < n) ? (double)LDC(la, first + (int64_t)(2 * l + 1) * stride, n_la) : 0.0;
   return warp_cumsum64_regs(x0, x1, n, carry, cs);
 }
 
@@ -161,6 +162,7 @@ __global__ void __launch_bounds__(SS_THREADS, 1) k_seg_state(const __grid_consta
   const int64_t s_end = imin64(p.L, s_begin + p.Ls);
   const int nsl = (int)cdiv(s_end - s_begin, SL);
   const int kslot = qk_slot(p, h), vslot = v_slot(p, h);
+  const int64_t n_la = p.B * p.L * p.H, n_seg = p.B * p.H * p.nseg;
 
   if (warp == 1) tmem_alloc(&tmem_base, 256);
   if (tid == 0) {
@@ -253,20 +255,20 @@ __global__ void __launch_bounds__(SS_THREADS, 1) k_seg_state(const __grid_consta
     const int wt = tid - 64, wq = warp & 3;
     double part = 0.0;
 #pragma unroll 8
-    for (int64_t t = s_begin + wt; t < s_end; t += 128) part += (double)la[(b * p.L + t) * p.H + h];
+    for (int64_t t = s_begin + wt; t < s_end; t += 128) part += (double)LDC(la, (b * p.L + t) * p.H + h, n_la);
 #pragma unroll
     for (int o = 16; o >= 1; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
     if (lane == 0) wred[warp - 2] = part;
     named_sync(1, 128);
     const double tot = wred[0] + wred[1] + wred[2] + wred[3];
-    if (wt == 0) Aseg[bh * p.nseg + seg] = (float)tot;
+    if (wt == 0) STC(Aseg, bh * p.nseg + seg, n_seg, (float)tot);
     bool ok = true;
     if (warp == 2) {  // one warp writes the diagonal: lane l owns tokens 2l, 2l + 1
       static_assert(SL == 64, "two tokens per lane");
       double carry = 0.0;
       auto la_of = [&](int n, int u) {
         const int64_t t = s_begin + (int64_t)n * SL + u;
-        return (n < nsl && t < s_end) ? (double)la[(b * p.L + t) * p.H + h] : 0.0;
+        return (n < nsl && t < s_end) ? (double)LDC(la, (b * p.L + t) * p.H + h, n_la) : 0.0;
       };
       double x0n = la_of(0, 2 * lane), x1n = la_of(0, 2 * lane + 1);  // one slice ahead
       for (int n = 0; n < nsl; ++n) {
@@ -286,26 +288,26 @@ __global__ void __launch_bounds__(SS_THREADS, 1) k_seg_state(const __grid_consta
         carry += __shfl_sync(0xffffffffu, incl, 31);
         const float w0 = 2 * lane < len ? exp2f((float)((REV ? cs0 : tot - cs0) * LOG2E_D)) : 0.f;
         const float w1 = 2 * lane + 1 < len ? exp2f((float)((REV ? cs1 : tot - cs1) * LOG2E_D)) : 0.f;
-        if (n >= 2 && !mbar_wait(&w_free[wb], ((n >> 1) - 1) & 1, ab)) { ok = false; break; }
-        uint8_t *W = Wb + wb * 2 * BLK;
-        *reinterpret_cast<float *>(W + sw128_off(2 * lane, 2 * lane, SL)) = tf32r(w0);
-        *reinterpret_cast<float *>(W + sw128_off(2 * lane + 1, 2 * lane + 1, SL)) = tf32r(w1);
+        if (n >= 2 && !mbar_wait_all(&w_free[wb], ((n >> 1) - 1) & 1, ab)) { ok = false; break; }
+        float *W = reinterpret_cast<float *>(Wb + wb * 2 * BLK);
+        STC(W, sw128_off(2 * lane, 2 * lane, SL) / 4, 2 * BLK / 4, tf32r(w0));
+        STC(W, sw128_off(2 * lane + 1, 2 * lane + 1, SL) / 4, 2 * BLK / 4, tf32r(w1));
         fence_async_smem();
         mbar_arrive(&w_full[wb]);
       }
     }
-    if (ok && mbar_wait(&done, 0, ab)) {
+    if (ok && mbar_wait_all(&done, 0, ab)) {  // (ok is uniform over each warp)
       tc_fence_after();
       // D^T in tensor memory: lane j (v' feature), column i (k' feature)
       const int j = 32 * wq + lane;
-      float *dst = states + (bh * p.nseg + seg) * (int64_t)p.dk * p.dv;
+      const int64_t sz = (int64_t)p.dk * p.dv, dst = (bh * p.nseg + seg) * sz;
       for (int c0 = 0; c0 < p.dkp; c0 += 32) {
         float v[32];
         tmem_ld32(T_D + ((uint32_t)(32 * wq) << 16) + c0, v);
         if (j < p.dv) {
 #pragma unroll
           for (int ii = 0; ii < 32; ++ii)
-            if (c0 + ii < p.dk) dst[(int64_t)(c0 + ii) * p.dv + j] = v[ii];
+            if (c0 + ii < p.dk) STC(states, dst + (int64_t)(c0 + ii) * p.dv + j, n_seg * sz, v[ii]);
         }
       }
     }
@@ -339,13 +341,13 @@ __global__ void __launch_bounds__(NTH) k_seg_scan(float *__restrict__ st,
   const int64_t sz = (int64_t)p.dk * p.dv;
   if (e0 >= sz) return;
   auto tpos = [&](int64_t e) { return (e % p.dv) * p.dk + e / p.dv; };  // transposed position
-  float4 *q = reinterpret_cast<float4 *>(st + bh * p.nseg * sz + e0);
-  const int64_t sz4 = sz / 4;
-  const float *a = Aseg + bh * p.nseg;
+  float4 *q = reinterpret_cast<float4 *>(st);
+  const int64_t sz4 = sz / 4, qb = (bh * p.nseg * sz + e0) / 4;  // (sz and e0 multiples of 4)
+  const int64_t n_st = p.B * p.H * p.nseg * sz, n_a = p.B * p.H * p.nseg, n_h = p.B * p.H * sz;
   float run[4] = {0.f, 0.f, 0.f, 0.f};
   if (init) {
 #pragma unroll
-    for (int j = 0; j < 4; ++j) run[j] = init[bh * sz + (TRANS ? tpos(e0 + j) : e0 + j)];
+    for (int j = 0; j < 4; ++j) run[j] = LDC(init, bh * sz + (TRANS ? tpos(e0 + j) : e0 + j), n_h);
   }
   for (int k0 = 0; k0 < p.nseg; k0 += SU) {
     float4 x[SU];
@@ -355,8 +357,8 @@ __global__ void __launch_bounds__(NTH) k_seg_scan(float *__restrict__ st,
       const int k = k0 + u;
       if (k < p.nseg) {
         const int s = REV ? p.nseg - 1 - k : k;
-        x[u] = q[(int64_t)s * sz4];
-        d[u] = expf(a[s]);
+        x[u] = LDC(q, qb + (int64_t)s * sz4, n_st / 4);
+        d[u] = expf(LDC(Aseg, bh * p.nseg + s, n_a));
       }
     }
 #pragma unroll
@@ -364,10 +366,10 @@ __global__ void __launch_bounds__(NTH) k_seg_scan(float *__restrict__ st,
       const int k = k0 + u;
       if (k < p.nseg) {
         const int s = REV ? p.nseg - 1 - k : k;
-        q[(int64_t)s * sz4] = make_float4(run[0], run[1], run[2], run[3]);
+        STC(q, qb + (int64_t)s * sz4, n_st / 4, make_float4(run[0], run[1], run[2], run[3]));
         if (stT) {
 #pragma unroll
-          for (int j = 0; j < 4; ++j) stT[bh * p.nseg * sz + (int64_t)s * sz + tpos(e0 + j)] = run[j];
+          for (int j = 0; j < 4; ++j) STC(stT, bh * p.nseg * sz + (int64_t)s * sz + tpos(e0 + j), n_st, run[j]);
         }
         run[0] = fmaf(d[u], run[0], x[u].x);
         run[1] = fmaf(d[u], run[1], x[u].y);
@@ -378,7 +380,7 @@ __global__ void __launch_bounds__(NTH) k_seg_scan(float *__restrict__ st,
   }
   if (fin) {
 #pragma unroll
-    for (int j = 0; j < 4; ++j) fin[bh * sz + (TRANS ? tpos(e0 + j) : e0 + j)] = run[j];
+    for (int j = 0; j < 4; ++j) STC(fin, bh * sz + (TRANS ? tpos(e0 + j) : e0 + j), n_h, run[j]);
   }
 }
 
@@ -457,6 +459,8 @@ __global__ void __launch_bounds__(WT, 1) k_walk(const __grid_constant__ CUtensor
   // barrier per stage), so that the intra-term MMAs issue during the turn
   __shared__ uint64_t p_full, p_empty, rescaled, st_init, drain_s, drain_m, wk_full[2];
   __shared__ uint64_t fac_full[4], fac_empty[4];
+  // never: a barrier nothing arrives on (the failure-path test waits on it)
+  __shared__ uint64_t never;
   __shared__ uint32_t tmem_base;
   __shared__ int abort_flag;
   volatile int *ab = &abort_flag;
@@ -470,6 +474,7 @@ __global__ void __launch_bounds__(WT, 1) k_walk(const __grid_constant__ CUtensor
   const int kslot = qk_slot(p, h), vslot = v_slot(p, h);
   const int dk = p.dk, dv = p.dv;
   auto chunk_of = [&](int ci) { return REV ? nc - 1 - ci : ci; };
+  const int64_t n_la = p.B * p.L * p.H;  // element counts (debug-build index checks)
 
   if (warp == 1) tmem_alloc(&tmem_base, 512);
   if (tid == 0) {
@@ -488,6 +493,7 @@ __global__ void __launch_bounds__(WT, 1) k_walk(const __grid_constant__ CUtensor
     mbar_init(&st_init, 128);
     mbar_init(&drain_s, 1);
     mbar_init(&drain_m, 1);
+    mbar_init(&never, 1);
     for (int i = 0; i < 4; ++i) {
       mbar_init(&fac_full[i], 32);
       mbar_init(&fac_empty[i], 257);
@@ -617,9 +623,9 @@ __global__ void __launch_bounds__(WT, 1) k_walk(const __grid_constant__ CUtensor
     auto la_load = [&](int ci) {
       const int64_t t0 = s_begin + (int64_t)chunk_of(ci) * C;
       const int len = (int)imin64(C, s_end - t0);
-      const float *lp = la + (b * p.L + t0) * p.H + h;
-      x0 = (2 * lane < len) ? (double)lp[(int64_t)(2 * lane) * p.H] : 0.0;
-      x1 = (2 * lane + 1 < len) ? (double)lp[(int64_t)(2 * lane + 1) * p.H] : 0.0;
+      const int64_t l0 = (b * p.L + t0) * p.H + h;
+      x0 = (2 * lane < len) ? (double)LDC(la, l0 + (int64_t)(2 * lane) * p.H, n_la) : 0.0;
+      x1 = (2 * lane + 1 < len) ? (double)LDC(la, l0 + (int64_t)(2 * lane + 1) * p.H, n_la) : 0.0;
     };
     la_load(0);
     float alpha = 1.f;
@@ -629,7 +635,7 @@ __global__ void __launch_bounds__(WT, 1) k_walk(const __grid_constant__ CUtensor
       const int len = (int)imin64(C, s_end - t0);
       const double cx0 = x0, cx1 = x1;
       if (ci + 1 < nc) la_load(ci + 1);
-      if (ci >= 4 && !mbar_wait(&fac_empty[slot], ((ci >> 2) - 1) & 1, ab)) break;
+      if (ci >= 4 && !mbar_wait_all(&fac_empty[slot], ((ci >> 2) - 1) & 1, ab)) break;
       Fac &F = fac[slot];
       const double tot = warp_cumsum64_regs(cx0, cx1, len, 0.0, F.cs2);
       __syncwarp();
@@ -664,15 +670,15 @@ __global__ void __launch_bounds__(WT, 1) k_walk(const __grid_constant__ CUtensor
       const int slot = ci & 3, sb = ci & 1, st = ci & 1;
       const int64_t t0 = s_begin + (int64_t)chunk_of(ci) * C;
       const int len = (int)imin64(C, s_end - t0);
-      if (!mbar_wait(&fac_full[slot], (ci >> 2) & 1, ab)) break;
+      if (!mbar_wait_all(&fac_full[slot], (ci >> 2) & 1, ab)) break;
       // The chunk's factors, two per lane (tokens lane and lane + 32), handed
       // around with shuffles: thread reads of shared memory are slow while
       // the tensor cores stream their operands from it.
       const Fac &F = fac[slot];
       const float csA = F.cs2[lane], csB = F.cs2[lane + 32];
       const float kwA = F.kw[lane], kwB = F.kw[lane + 32];
-      if (!mbar_wait(&s_full[sb], (ci >> 1) & 1, ab)) break;
-      if (ci >= 1 && !mbar_wait(&p_empty, (ci - 1) & 1, ab)) break;
+      if (!mbar_wait_all(&s_full[sb], (ci >> 1) & 1, ab)) break;
+      if (ci >= 1 && !mbar_wait_all(&p_empty, (ci - 1) & 1, ab)) break;
       tc_fence_after();
       // score row r = 16 wq + lane % 16 sits in lane lane % 16 (M = 64); the
       // lane 16 above it takes the row's upper 32 columns
@@ -699,7 +705,8 @@ __global__ void __launch_bounds__(WT, 1) k_walk(const __grid_constant__ CUtensor
         }
 #pragma unroll
         for (int i = 0; i < 16; i += 4)
-          *reinterpret_cast<float4 *>(P + sw128_off(r, ub + 16 * g + i, C)) = make_float4(f[i], f[i + 1], f[i + 2], f[i + 3]);
+          STC(reinterpret_cast<float4 *>(P), sw128_off(r, ub + 16 * g + i, C) / 16, 2 * BLK / 16,
+              make_float4(f[i], f[i + 1], f[i + 2], f[i + 3]));
       }
       fence_async_smem();
       mbar_arrive(&p_full);
@@ -708,7 +715,8 @@ __global__ void __launch_bounds__(WT, 1) k_walk(const __grid_constant__ CUtensor
       // each row is permuted within itself (8 threads per row, one 16-byte
       // chunk each; a warp holds 4 whole rows)
       // (one column block per iteration: its four 16-row passes load first)
-      uint8_t *K = Ks(st);
+      float4 *K4 = reinterpret_cast<float4 *>(Ks(st));
+      const int n_k4 = (int)(qkbytes / 16);
       const int ch = wt & 7;
       float wr4[4];
 #pragma unroll
@@ -720,7 +728,7 @@ __global__ void __launch_bounds__(WT, 1) k_walk(const __grid_constant__ CUtensor
 #pragma unroll
         for (int q4 = 0; q4 < 4; ++q4) {
           const int row = q4 * 16 + (wt >> 3);
-          v[q4] = *reinterpret_cast<const float4 *>(K + blk * BLK + row * 128 + ((ch ^ (row & 7)) << 4));
+          v[q4] = LDC(K4, (blk * BLK + row * 128 + ((ch ^ (row & 7)) << 4)) / 16, n_k4);
         }
         __syncwarp();
 #pragma unroll
@@ -729,7 +737,7 @@ __global__ void __launch_bounds__(WT, 1) k_walk(const __grid_constant__ CUtensor
           const float wr = wr4[q4];
           float4 x = v[q4];
           x.x = tf32r(x.x * wr); x.y = tf32r(x.y * wr); x.z = tf32r(x.z * wr); x.w = tf32r(x.w * wr);
-          *reinterpret_cast<float4 *>(K + blk * BLK + row * 128 + ((((ch >> 1) ^ (row & 3)) << 5) | ((ch & 1) << 4))) = x;
+          STC(K4, (blk * BLK + row * 128 + ((((ch >> 1) ^ (row & 3)) << 5) | ((ch & 1) << 4))) / 16, n_k4, x);
         }
       }
       fence_async_smem();
@@ -742,13 +750,13 @@ __global__ void __launch_bounds__(WT, 1) k_walk(const __grid_constant__ CUtensor
     const int j = 32 * wq + lane;  // v' feature of this lane
     const uint32_t lb = (uint32_t)(32 * wq) << 16;
     {  // entering state into tensor memory: lane j, column i = state[i][j]
-      const float *H0 = Hseg + (bh * p.nseg + seg) * (int64_t)dk * dv;
+      const int64_t sz = (int64_t)dk * dv, h0 = (bh * p.nseg + seg) * sz, n_h = p.B * p.H * p.nseg * sz;
       for (int c0 = 0; c0 < p.dkp; c0 += 32) {
         float hv[32];
 #pragma unroll
         for (int ii = 0; ii < 32; ++ii) {
           const int i = c0 + ii;
-          hv[ii] = (j < dv && i < dk) ? (hseg_t ? H0[(int64_t)j * dk + i] : H0[(int64_t)i * dv + j]) : 0.f;
+          hv[ii] = (j < dv && i < dk) ? LDC(Hseg, h0 + (hseg_t ? (int64_t)j * dk + i : (int64_t)i * dv + j), n_h) : 0.f;
         }
         tmem_st32(T_ST + lb + c0, hv);
       }
@@ -759,6 +767,7 @@ __global__ void __launch_bounds__(WT, 1) k_walk(const __grid_constant__ CUtensor
     const int oslot = oa.out_slots == p.H ? (int)h : (int)(h / p.hpg);
     const int64_t ld = (int64_t)oa.out_slots * dv;
     const int64_t ldy = (int64_t)(p.H / p.hpg) * dv;
+    const int64_t n_out = p.B * p.L * ld, n_y = p.B * p.L * ldy;
     // SPLIT: the y values of 16-token step (chunk cy, step g), loaded two steps
     // before they are used (yr0: this step, yr1: the next; the ring runs
     // across chunks), so the loads' latency hides behind the steps between
@@ -767,19 +776,35 @@ __global__ void __launch_bounds__(WT, 1) k_walk(const __grid_constant__ CUtensor
       if constexpr (SPLIT) {
         const int64_t ty = s_begin + (int64_t)chunk_of(cy < nc ? cy : 0) * C;
         const int leny = cy < nc ? (int)imin64(C, s_end - ty) : 0;
-        const float *yp = oa.y + ((b * p.L + ty) * (p.H / p.hpg) + h / p.hpg) * (int64_t)dv + j;
+        const int64_t y0 = ((b * p.L + ty) * (p.H / p.hpg) + h / p.hpg) * (int64_t)dv + j;
 #pragma unroll
-        for (int i = 0; i < 16; ++i) dst[i] = (j < dv && 16 * g + i < leny) ? yp[(16 * g + i) * ldy] : 0.f;
+        for (int i = 0; i < 16; ++i) dst[i] = (j < dv && 16 * g + i < leny) ? LDC(oa.y, y0 + (16 * g + i) * ldy, n_y) : 0.f;
       }
     };
     load_y(yr0, 0, 0);
     load_y(yr1, 0, 1);
+    const int stall_at = g_test_stall ? (nc > 1 ? 1 : 0) : -1;
     for (int ci = 0; ci < nc; ++ci) {
       const int slot = ci & 3, xb = ci & 1;
       const int64_t t0 = s_begin + (int64_t)chunk_of(ci) * C;
       const int len = (int)imin64(C, s_end - t0);
-      if (!mbar_wait(&fac_full[slot], (ci >> 2) & 1, ab)) break;
-      if (!mbar_wait(&xy_full[xb], (ci >> 1) & 1, ab)) break;
+      if constexpr (SPLIT) {
+        // the four epilogue warps meet at named barrier 2 for the token sums
+        // below, so they take the give-up decision together (a barrier that
+        // ORs the threads' failures), never one warp alone; this barrier also
+        // keeps red from being rewritten before the last chunk's sums are read
+        bool ok = mbar_wait(&fac_full[slot], (ci >> 2) & 1, ab);
+        if (ok && ci == stall_at) ok = mbar_wait(&never, 0, ab);
+        if (ok) ok = mbar_wait(&xy_full[xb], (ci >> 1) & 1, ab);
+        if (named_sync_or(2, 128, !ok)) break;
+        __syncwarp();
+      } else {
+        if (!mbar_wait_all(&fac_full[slot], (ci >> 2) & 1, ab)) break;
+        if (ci == stall_at) {
+          if (!mbar_wait_all(&never, 0, ab)) break;
+        }
+        if (!mbar_wait_all(&xy_full[xb], (ci >> 1) & 1, ab)) break;
+      }
       tc_fence_after();
       const Fac &F = fac[slot];
       if (F.rescale) {  // Hs <- alpha exp(A_c) Hs before the update is issued
@@ -796,7 +821,7 @@ __global__ void __launch_bounds__(WT, 1) k_walk(const __grid_constant__ CUtensor
         mbar_arrive(&rescaled);
       }
       const float qfA = F.qf[lane], qfB = F.qf[lane + 32];  // shuffled below (see the mask)
-      float *os = oa.out + ((b * p.L + t0) * oa.out_slots + oslot) * (int64_t)dv + j;
+      const int64_t o0 = ((b * p.L + t0) * oa.out_slots + oslot) * (int64_t)dv + j;
       auto step = [&](const int g) {  // tokens 16 g .. 16 g + 15
         float xa[16], ya[16];
         tmem_ld16x2(T_X + xb * 64 + 16 * g + lb, T_Y + xb * 64 + 16 * g + lb, xa, ya);
@@ -821,19 +846,19 @@ __global__ void __launch_bounds__(WT, 1) k_walk(const __grid_constant__ CUtensor
           load_y(yr1, g + 2 < 4 ? ci : ci + 1, (g + 2) & 3);
         }
         if (j < dv) {
-          float *o16 = os + (int64_t)(16 * g) * ld;
+          const int64_t o16 = o0 + (int64_t)(16 * g) * ld;
           if (16 * g + 16 <= len) {
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
-              if (ATOMIC) atomicAdd(o16 + i * ld, o[i]);
-              else o16[i * ld] = o[i];
+              if (ATOMIC) ADDC(oa.out, o16 + i * ld, n_out, o[i]);
+              else STC(oa.out, o16 + i * ld, n_out, o[i]);
             }
           } else {
 #pragma unroll
             for (int i = 0; i < 16; ++i)
               if (16 * g + i < len) {
-                if (ATOMIC) atomicAdd(o16 + i * ld, o[i]);
-                else o16[i * ld] = o[i];
+                if (ATOMIC) ADDC(oa.out, o16 + i * ld, n_out, o[i]);
+                else STC(oa.out, o16 + i * ld, n_out, o[i]);
               }
           }
         }
@@ -859,8 +884,7 @@ __global__ void __launch_bounds__(WT, 1) k_walk(const __grid_constant__ CUtensor
       for (int g = 0; g < 4; ++g) step(g);
       if constexpr (SPLIT) {
         named_sync(2, 128);
-        if (et < len) oa.dcs[(b * p.L + t0 + et) * p.H + h] = red[et] + red[C + et] + red[2 * C + et] + red[3 * C + et];
-        named_sync(2, 128);
+        if (et < len) STC(oa.dcs, (b * p.L + t0 + et) * p.H + h, n_la, red[et] + red[C + et] + red[2 * C + et] + red[3 * C + et]);
       }
       mbar_arrive(&fac_empty[slot]);
     }
@@ -926,7 +950,10 @@ __global__ void __launch_bounds__(NTH) k_dla_intra(const __grid_constant__ CUten
   const uint32_t tmem = tmem_base;
   const uint32_t lb = (uint32_t)(warp * 32) << 16;
   bool ok = true;
-  int pending = 1;  // loads in flight (thread 0's view)
+  // thread 0's view of what is in flight: the phase whose tile loads, and
+  // the phase whose MMAs, have not been seen to complete (-1: none); both are
+  // drained before the tensor memory is freed, also after a failure
+  int tma_ph = 0, mma_ph = -1;
   // Score rows live in lanes 0-15 of each warp (M = 64); the lane 16 above a
   // row works on its upper 32 columns, so every lane holds 32 columns:
   // u = 32 * up + i.
@@ -938,24 +965,25 @@ __global__ void __launch_bounds__(NTH) k_dla_intra(const __grid_constant__ CUten
     const int kdim = ph == 0 ? dk : dv;
     const int64_t h = grp * hpg + (ph == 0 ? 0 : ph - 1);
     if (ph >= 1 && warp == 0) {  // in-chunk prefix of la, times log2(e)
-      warp_cumsum64(la, (b * p.L + t0) * p.H + h, p.H, len, 0.0, cs);
+      warp_cumsum64(la, p.B * p.L * p.H, (b * p.L + t0) * p.H + h, p.H, len, 0.0, cs);
       __syncwarp();
       for (int t = lane; t < C; t += 32) cs[t] = t < len ? cs[t] * 1.4426950408889634f : 0.f;
     }
     ok = mbar_wait(&bar_tma, ph & 1) && ok;
-    if (tid == 0 && ok) pending = 0;
+    if (tid == 0 && ok) tma_ph = -1;
     if (__syncthreads_or(!ok)) break;
     {  // round both tiles to TF32 (nearest) in place
       const int r = tid & 63, half = tid >> 6;
       const int cols = ncb * 16;
+      float4 *a4 = reinterpret_cast<float4 *>(T1), *b4 = reinterpret_cast<float4 *>(T2);
+      const int n4 = ncbm * 8192 / 16;
       for (int col = half * cols; col < (half + 1) * cols; col += 4) {
-        float4 *a4 = reinterpret_cast<float4 *>(T1 + sw128_off(r, col, C));
-        float4 *b4 = reinterpret_cast<float4 *>(T2 + sw128_off(r, col, C));
-        float4 x = *a4, y = *b4;
+        const int i4 = sw128_off(r, col, C) / 16;
+        float4 x = LDC(a4, i4, n4), y = LDC(b4, i4, n4);
         x.x = tf32r(x.x); x.y = tf32r(x.y); x.z = tf32r(x.z); x.w = tf32r(x.w);
         y.x = tf32r(y.x); y.y = tf32r(y.y); y.z = tf32r(y.z); y.w = tf32r(y.w);
-        *a4 = x;
-        *b4 = y;
+        STC(a4, i4, n4, x);
+        STC(b4, i4, n4, y);
       }
     }
     fence_async_smem();
@@ -970,12 +998,14 @@ __global__ void __launch_bounds__(NTH) k_dla_intra(const __grid_constant__ CUten
         mma_ss(tmem + (ph == 0 ? 0 : 64), sdesc(a + off), sdesc(bb + off), id, kk > 0 ? 1u : 0u);
       }
       mma_commit(&bar_mma);
+      mma_ph = ph;
     }
     ok = mbar_wait(&bar_mma, ph & 1) && ok;
+    if (tid == 0 && ok) mma_ph = -1;
     tc_fence_after();
     if (tid == 0 && ok && ph < hpg) {  // the tiles are consumed: next head's loads
       load_dv(grp * hpg + ph);
-      pending = 1;
+      tma_ph = ph + 1;
     }
     if (ph == 0) {
       float lo[32], hi[32];
@@ -1051,13 +1081,16 @@ __global__ void __launch_bounds__(NTH) k_dla_intra(const __grid_constant__ CUten
       }
       const float b1 = x - dd[0];  // B_{2l+1} = suffix from 2l+1
       const float b0 = x;          // B_{2l}
-      float *bt = Bt + (b * p.L + t0) * p.H + h;
-      if (2 * lane < len) bt[(int64_t)(2 * lane) * p.H] = b0;
-      if (2 * lane + 1 < len) bt[(int64_t)(2 * lane + 1) * p.H] = b1;
+      const int64_t bt = (b * p.L + t0) * p.H + h, n_bt = p.B * p.L * p.H;
+      if (2 * lane < len) STC(Bt, bt + (int64_t)(2 * lane) * p.H, n_bt, b0);
+      if (2 * lane + 1 < len) STC(Bt, bt + (int64_t)(2 * lane + 1) * p.H, n_bt, b1);
     }
     __syncthreads();  // R and cs are reused by the next head
   }
-  if (tid == 0 && pending) mbar_wait(&bar_tma, 0);  // best effort after a failure
+  if (tid == 0) {
+    if (mma_ph >= 0) mbar_wait(&bar_mma, mma_ph & 1);
+    if (tma_ph >= 0) mbar_wait(&bar_tma, tma_ph & 1);
+  }
   tc_fence_before();
   __syncthreads();
   if (warp == 0) tmem_dealloc(tmem, 128);
@@ -1086,19 +1119,27 @@ __global__ void __launch_bounds__(DT) k_dla(const float *__restrict__ Bt,
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int64_t seg = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int64_t bh = b * H + h;
+  const int64_t n_tok = (int64_t)gridDim.z * L * H;  // element counts (debug-build index checks)
   // carry = <G_end, S_end>: float4 loads, fp32 partial sums, fp64 across threads
   float part = 0.f;
   const float4 *G = nullptr, *S = nullptr;
+  int64_t g0 = 0, s0 = 0;        // float4 offsets of G and S
+  [[maybe_unused]] int64_t n4 = 0;  // float4 count of their buffers (index checks)
   if (seg + 1 < nseg) {
-    G = reinterpret_cast<const float4 *>(Gst + (bh * nseg + seg) * sz);
-    S = reinterpret_cast<const float4 *>(Sst + (bh * nseg + seg + 1) * sz);
+    G = reinterpret_cast<const float4 *>(Gst);
+    S = reinterpret_cast<const float4 *>(Sst);
+    g0 = (bh * nseg + seg) * sz / 4;
+    s0 = (bh * nseg + seg + 1) * sz / 4;
+    n4 = (int64_t)gridDim.z * H * nseg * sz / 4;
   } else if (Gfin) {
-    G = reinterpret_cast<const float4 *>(Gfin + bh * sz);
-    S = reinterpret_cast<const float4 *>(Sfin + bh * sz);
+    G = reinterpret_cast<const float4 *>(Gfin);
+    S = reinterpret_cast<const float4 *>(Sfin);
+    g0 = s0 = bh * sz / 4;
+    n4 = (int64_t)gridDim.z * H * sz / 4;
   }
   if (G) {
     for (int64_t e = tid; e < sz / 4; e += DT) {
-      const float4 g = G[e], x = S[e];
+      const float4 g = LDC(G, g0 + e, n4), x = LDC(S, s0 + e, n4);
       part = fmaf(g.x, x.x, fmaf(g.y, x.y, fmaf(g.z, x.z, fmaf(g.w, x.w, part))));
     }
   }
@@ -1118,7 +1159,7 @@ __global__ void __launch_bounds__(DT) k_dla(const float *__restrict__ Bt,
     const int64_t t = hi - DT + tid;  // thread tid owns token t (valid if t >= s_begin)
     const bool ok = t >= s_begin;
     const int64_t idx = (b * L + t) * H + h;
-    double x = ok ? (double)rq[idx] - (double)rk[idx] : 0.0;
+    double x = ok ? (double)LDC(rq, idx, n_tok) - (double)LDC(rk, idx, n_tok) : 0.0;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {  // inclusive suffix within the warp
       const double y = __shfl_down_sync(0xffffffffu, x, o);
@@ -1130,7 +1171,7 @@ __global__ void __launch_bounds__(DT) k_dla(const float *__restrict__ Bt,
 #pragma unroll
     for (int w2 = 0; w2 < DT / 32; ++w2)
       if (w2 > warp) after += wred[w2];
-    if (ok) dla[idx] = (float)((double)Bt[idx] + x + after);
+    if (ok) STC(dla, idx, n_tok, (float)((double)LDC(Bt, idx, n_tok) + x + after));
 #pragma unroll
     for (int w2 = 0; w2 < DT / 32; ++w2) carry += wred[w2];
     __syncthreads();
@@ -1512,7 +1553,19 @@ cudaError_t read_and_clear_error(unsigned int *word) {
   unsigned int zero = 0;
   cudaError_t e = cudaMemcpyFromSymbol(word, g_error_word, sizeof(unsigned int));
   if (e != cudaSuccess) return e;
-  return cudaMemcpyToSymbol(g_error_word, &zero, sizeof(unsigned int));
+  if ((e = cudaMemcpyToSymbol(g_error_word, &zero, sizeof(unsigned int))) != cudaSuccess) return e;
+#ifdef SSD_CHECK
+  unsigned int cw = 0;
+  if ((e = cudaMemcpyFromSymbol(&cw, g_check_word, sizeof(unsigned int))) != cudaSuccess) return e;
+  *word |= cw;
+  if ((e = cudaMemcpyToSymbol(g_check_word, &zero, sizeof(unsigned int))) != cudaSuccess) return e;
+#endif
+  return cudaSuccess;
+}
+
+cudaError_t set_test_stall(int on) {
+  const int v = on ? 1 : 0;
+  return cudaMemcpyToSymbol(g_test_stall, &v, sizeof(int));
 }
 
 }  // namespace tc

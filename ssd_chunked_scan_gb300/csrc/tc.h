@@ -23,9 +23,13 @@ cudaError_t bwd(const float *q, const float *k, const float *v, const float *la,
 bool set_overlap(bool on);
 bool get_overlap();
 
-// Reads and clears the device error word of the current device (set by a
-// bounded wait that gave up).
+// Reads and clears the device error word of the current device: bit 0 is set
+// by a bounded wait that gave up, bit 1 by a failed index check (debug
+// builds).
 cudaError_t read_and_clear_error(unsigned int *word);
+
+// Failure-path test switch (see ssd_test_stall_walks).
+cudaError_t set_test_stall(int on);
 
 }  // namespace tc
 }  // namespace ssd

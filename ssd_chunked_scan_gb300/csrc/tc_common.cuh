@@ -12,6 +12,10 @@ namespace tc {
 // Device error word of the translation unit that includes this header
 // (include it from one .cu only): bit 0 = a bounded mbarrier wait gave up.
 __device__ unsigned int g_error_word;
+// Test switch (0 = off): when set, the epilogue of every walk CTA waits, at
+// its second chunk, on a barrier that nothing ever completes, so that the
+// bounded wait runs out and the failure exit path runs.
+__device__ int g_test_stall;
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
   return (uint32_t)__cvta_generic_to_shared(p);
@@ -87,6 +91,14 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity,
   if (mbar_test(bar, parity)) return true;
   return mbar_wait_slow(bar, parity, abort);
 }
+// mbar_wait for all 32 lanes of a warp: true only when every lane saw the
+// phase complete.  Roles that run as whole warps (shuffles, warp-collective
+// tensor-memory loads) take their give-up decision through this, so that the
+// lanes of a warp never split between leaving and staying in a loop.
+__device__ __forceinline__ bool mbar_wait_all(uint64_t *bar, uint32_t parity,
+                                              volatile int *abort = nullptr) {
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort));
+}
 // Plain arrive (release semantics at CTA scope).
 __device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
@@ -94,6 +106,17 @@ __device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
 // Barrier among the `nthreads` threads (whole warps) that use named barrier `id`.
 __device__ __forceinline__ void named_sync(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+// The same barrier, returning whether `pred` held on any of those threads.
+__device__ __forceinline__ bool named_sync_or(int id, int nthreads, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.or.pred q, %2, %3, p;\n"
+      " selp.u32 %0, 1, 0, q;\n}\n"
+      : "=r"(r)
+      : "r"((uint32_t)pred), "r"(id), "r"(nthreads)
+      : "memory");
+  return r != 0;
 }
 
 // ---- TMA --------------------------------------------------------------------

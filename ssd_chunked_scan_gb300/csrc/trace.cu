@@ -23,6 +23,7 @@ struct Rec {
 
 std::atomic<long long> g_launches{0};
 std::atomic<int> g_enabled{0};
+thread_local bool t_quiet = false;
 std::mutex g_mu;
 std::vector<Rec> g_recs;
 std::vector<cudaEvent_t> g_free;
@@ -47,8 +48,11 @@ std::vector<Agg> g_agg;
 
 }  // namespace
 
+LaunchTrace::Quiet::Quiet() : prev_(t_quiet) { t_quiet = true; }
+LaunchTrace::Quiet::~Quiet() { t_quiet = prev_; }
+
 LaunchTrace::LaunchTrace(const char *name, cudaStream_t s) : name_(name), s_(s), a_(nullptr) {
-  if (g_enabled.load(std::memory_order_relaxed)) {
+  if (!t_quiet && g_enabled.load(std::memory_order_relaxed)) {
     std::lock_guard<std::mutex> lk(g_mu);
     a_ = get_event();
     if (a_) cudaEventRecord(static_cast<cudaEvent_t>(a_), s_);

@@ -11,7 +11,9 @@ import os
 
 import torch
 
-_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_lib", "libssd.so")
+# SSD_LIB_VARIANT=check selects the debug build (index checks, see build.py)
+_LIB_NAME = "libssd_check.so" if os.environ.get("SSD_LIB_VARIANT", "") == "check" else "libssd.so"
+_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_lib", _LIB_NAME)
 
 SSD_OK = 0
 SSD_ERR_ARG = 1
@@ -23,6 +25,7 @@ SSD_ERR_LAUNCH = 6
 SSD_ERR_TIMEOUT = 7
 SSD_ERR_CUDA = 8
 SSD_ERR_SCRATCH = 9
+SSD_ERR_CHECK = 10
 SSD_PATH_TC = 0
 SSD_PATH_SIMT = 1
 
@@ -30,7 +33,7 @@ EXPORTED = ("ssd_fwd", "ssd_bwd", "ssd_set_path", "ssd_get_path", "ssd_set_overl
             "ssd_get_overlap", "ssd_strerror",
             "ssd_last_device_error", "ssd_version", "ssd_launch_count", "ssd_trace_enable",
             "ssd_trace_collect", "ssd_trace_get", "ssd_trace_reset", "ssd_fwd_noalloc",
-            "ssd_fwd_noalloc_scratch_bytes")
+            "ssd_fwd_noalloc_scratch_bytes", "ssd_test_stall_walks")
 
 
 class SSDError(RuntimeError):
@@ -41,7 +44,8 @@ class SSDError(RuntimeError):
 
 def _load():
     if not os.path.exists(_LIB_PATH):
-        raise ImportError(f"libssd.so not built at {_LIB_PATH}; run __graft_entry__.build()")
+        raise ImportError(f"{_LIB_NAME} not built at {_LIB_PATH}; run __graft_entry__.build()"
+                          + (" / build_lib(check=True)" if _LIB_NAME != "libssd.so" else ""))
     lib = ctypes.CDLL(_LIB_PATH)
     p, i64 = ctypes.c_void_p, ctypes.c_int64
     lib.ssd_fwd.argtypes = [p] * 6 + [i64] * 7 + [p]
@@ -89,6 +93,8 @@ def _load():
     lib.ssd_fwd_noalloc.restype = ctypes.c_int
     lib.ssd_fwd_noalloc_scratch_bytes.argtypes = []
     lib.ssd_fwd_noalloc_scratch_bytes.restype = ctypes.c_size_t
+    lib.ssd_test_stall_walks.argtypes = [ctypes.c_int]
+    lib.ssd_test_stall_walks.restype = ctypes.c_int
     return lib
 
 
@@ -122,6 +128,15 @@ def ssd_get_overlap() -> bool:
 
 def ssd_last_device_error(stream=None) -> int:
     return int(LIB.ssd_last_device_error(_stream(stream)))
+
+
+def ssd_test_stall_walks(on: bool) -> None:
+    """Failure-path test switch (include/ssd.h): while on, every tensor-core
+    walk CTA stalls on a barrier nothing completes until its bounded wait gives
+    up, and ssd_last_device_error then reports SSD_ERR_TIMEOUT."""
+    rc = LIB.ssd_test_stall_walks(1 if on else 0)
+    if rc:
+        raise SSDError(rc, "ssd_test_stall_walks")
 
 
 def ssd_launch_count() -> int:

@@ -47,7 +47,7 @@ def test_kernel_table_shares_sum_to_one():
     assert tab["a"]["launches"] == 2
 
 
-def test_every_traced_kernel_has_a_cost_and_traffic_on_the_workload():
+def test_every_traced_kernel_has_a_cost_and_a_traffic_figure_or_a_reason():
     w = BY_NAME[bench.WORKLOAD]
     costs = bench.kernel_costs(w, 152)
     names = ["tc.seg_state", "tc.seg_state_dq", "tc.seg_state_dk", "tc.seg_scan", "tc.walk_out",
@@ -56,12 +56,27 @@ def test_every_traced_kernel_has_a_cost_and_traffic_on_the_workload():
              "simt.state_scan_rev", "simt.chunk_out", "simt.chunk_grad", "simt.dla_carry"]
     for n in names:
         assert n in costs, n
-        assert n in bench.TRAFFIC, n
         kb, kf, bound = costs[n]
         assert kb > 0 and bound in ("hbm", "tensor", "alu")
-        # a capture that moved far fewer bytes than the algorithmic count would
-        # mean the cost model counts something the kernel never touches
-        assert bench.TRAFFIC[n] >= 0.5 * kb or n in ("tc.seg_scan", "tc.dla"), n
+        t, why = bench.traffic_of(n)
+        assert why, n
+        if t is not None:
+            # a capture that moved far fewer bytes than the algorithmic count
+            # would mean the cost model counts something the kernel never touches
+            assert t >= 0.5 * kb or n in ("tc.seg_scan", "tc.dla"), n
+
+
+def test_traffic_is_dropped_once_the_kernel_source_changes(monkeypatch):
+    grp = dict(bench.TRAFFIC_GROUPS["tc."], sha16="0" * 16, commit="abc1234",
+               bytes={"tc.walk_dq": 123})
+    monkeypatch.setitem(bench.TRAFFIC_GROUPS, "tc.", grp)
+    t, why = bench.traffic_of("tc.walk_dq")
+    assert t is None and "changed" in why and "abc1234" in why
+    monkeypatch.setitem(bench.TRAFFIC_GROUPS, "tc.", dict(grp, sha16=bench._sha16(grp["source"])))
+    t, why = bench.traffic_of("tc.walk_dq")
+    assert t == 123 and "unchanged" in why
+    assert bench.traffic_of("tc.walk_dk")[0] is None
+    assert bench.traffic_of("nothing.like.this")[0] is None
 
 
 def test_step_totals_match_the_workload_sizes():

@@ -108,7 +108,8 @@ def test_workload_parity(path, w):
     q, k, v, la, h0, dout = workload_inputs(w)
     out, g = run_gpu(path, q, k, v, la, h0, dout, w.chunk)
     hpg = w.H // w.G
-    units = sorted({(0, 0), (w.B - 1, w.G - 1)})
+    # the first, a middle and the last (batch, group) unit
+    units = sorted({(0, 0), (w.B // 2, w.G // 2), (w.B - 1, w.G - 1)})
     for b, gi in units:
         gs, hs = slice(gi, gi + 1), slice(gi * hpg, (gi + 1) * hpg)
         uq, uk = _unit(q, b, gs), _unit(k, b, gs)
