@@ -163,6 +163,8 @@ def kernel_costs(w, sms=152):
         c[n] = (3 * qk + 2 * vv + 2 * la + sst, fw + BL * H * dk * 2, "hbm")
     c["tc.dla_intra"] = (2 * qk + 2 * vv + 2 * la, BL * (G * C * dk + H * C * dv + H * C), "hbm")
     c["tc.dla"] = (4 * la + 2 * sst, BL * H * 4 + 2 * B * H * nseg * dk * dv, "hbm")
+    # deterministic group sums (opt-in): read every head's share, write the group's
+    c["tc.group_sum"] = (BL * H * dk * f + qk, BL * H * dk, "hbm")
     # sequential kernels (chunk = 1): fp32 state updates and reductions, one
     # token at a time; E arrays hold one float per token, head and column block
     nblk = -(-dv // 32)
@@ -940,6 +942,8 @@ def main():
                     help="override the workload's chunk length (1: the sequential kernels)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--deterministic", action="store_true",
+                    help="tensor-core backward with deterministic group sums (ssd_set_deterministic)")
     ap.add_argument("--no-accuracy", action="store_true",
                     help="skip the rel_err fields (the float64 oracle on a sample of the workload)")
     ap.add_argument("--mode", default="fwd_bwd", choices=["fwd_bwd", "fwd", "max_len"],
@@ -981,6 +985,7 @@ def main():
 
     from ssd_chunked_scan_gb300 import ssd
     from ssd_chunked_scan_gb300.inputs import workload_inputs
+    ssd.ssd_set_deterministic(bool(args.deterministic))
     ssd.ssd_set_path(ssd.SSD_PATH_TC if args.path == "tc" else ssd.SSD_PATH_SIMT)
 
     host = [torch.from_numpy(x).pin_memory() for x in workload_inputs(w)]
@@ -1195,6 +1200,7 @@ def main():
         "config": {"workload": w.name, "mode": args.mode, "path": args.path, "B": w.B, "G": w.G,
                    "H": w.H, "L": w.L, "dk": w.dk, "dv": w.dv, "chunk": w.chunk,
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "deterministic_group_sums": bool(args.deterministic),
                    "l2": l2_note(resident_bytes(w.B, w.L, w.G, w.H, w.dk, w.dv, args.mode))},
         "roofline": roof,
         "step_roofline": {"bound": "hbm" if t_hbm >= t_tc else "tensor",

@@ -57,9 +57,9 @@
  *                 1 <= dk, dv <= 128.  Its workspace holds every chunk's
  *                 state (B*H*ceil(L/chunk)*dk*dv floats per pass), where
  *                 the tensor-core path keeps one state per segment (about
- *                 two segments per SM in all, whatever L); see
+ *                 one segment per SM in all, whatever L); see
  *                 ssd_fwd_workspace_bytes.  The tensor-core backward runs
- *                 part of its work on a stream of the library's own, forked
+ *                 part of its work on streams of the library's own, forked
  *                 from and joined back into `stream` within the call (see
  *                 ssd_set_overlap).
  *   chunk == 1    (either path) the sequential evaluation: the recurrence one
@@ -236,13 +236,27 @@ SSD_API int ssd_get_path(void);
  * dv passes on a stream of the library's own (one per device, created at the
  * first backward), forked from and joined back into the caller's stream
  * inside the call, so the call stays ordered on `stream` like any other; the
- * causal dq pass and the intra-chunk dlog_alpha sums run on `stream`
- * meanwhile.  Off runs every kernel on `stream` in turn (the same results up
+ * intra-chunk dlog_alpha sums run on a second stream of the library's, and
+ * the causal dq pass on `stream`, meanwhile.  Off runs every kernel on `stream` in turn (the same results up
  * to the order of the float atomic adds that sum a group's heads; for
  * profiling one kernel at a time).  The SIMT and sequential paths are not
  * affected.  ssd_set_overlap returns the previous setting. */
 SSD_API int ssd_set_overlap(int on);
 SSD_API int ssd_get_overlap(void);
+
+/* Deterministic group sums in the tensor-core backward (process-wide, off
+ * by default).  When H > G, dq and dk are sums over the heads of a group.
+ * Off, every head's walk adds its share into dq / dk with fp32 atomic adds,
+ * whose order (and so the last bits of the sums) may differ from run to run.
+ * On, every head's share is written to the workspace and one more kernel
+ * adds them in head order, so that the same inputs give bitwise the same dq
+ * and dk on every run; the workspace grows by 2*B*L*H*dk floats and the step
+ * by that kernel.  ssd_bwd_workspace_bytes reports the size for the current
+ * setting (change it only between calls).  The SIMT path always sums heads
+ * in order; the sequential kernels (chunk == 1) use atomic adds either way.
+ * Returns the previous setting. */
+SSD_API int ssd_set_deterministic(int on);
+SSD_API int ssd_get_deterministic(void);
 
 /* Static description of a status code; never NULL. */
 SSD_API const char *ssd_strerror(int status);
@@ -286,7 +300,9 @@ SSD_API int ssd_trace_get(int i, char *name, int name_len, long long *launches,
 SSD_API int ssd_trace_reset(void);
 
 /* Library version as major*10000 + minor*100 + patch (0.2.0 added the
- * final-state entry points, 0.3.0 ssd_set_overlap / ssd_get_overlap). */
+ * final-state entry points, 0.3.0 ssd_set_overlap / ssd_get_overlap, 0.4.0
+ * ssd_set_deterministic / ssd_get_deterministic, ssd_test_stall_walks and
+ * SSD_ERR_CHECK). */
 SSD_API int ssd_version(void);
 
 #ifdef __cplusplus

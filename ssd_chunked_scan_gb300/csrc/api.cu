@@ -82,7 +82,7 @@ int ws_alloc(void **p, size_t bytes, cudaStream_t s) {
 
 extern "C" {
 
-int ssd_version(void) { return 300; }
+int ssd_version(void) { return 400; }
 
 const char *ssd_strerror(int status) {
   switch (status) {
@@ -112,6 +112,10 @@ int ssd_get_path(void) { return current_path(); }
 int ssd_set_overlap(int on) { return ssd::tc::set_overlap(on != 0) ? 1 : 0; }
 
 int ssd_get_overlap(void) { return ssd::tc::get_overlap() ? 1 : 0; }
+
+int ssd_set_deterministic(int on) { return ssd::tc::set_deterministic(on != 0) ? 1 : 0; }
+
+int ssd_get_deterministic(void) { return ssd::tc::get_deterministic() ? 1 : 0; }
 
 int ssd_fwd_ex(const float *q, const float *k, const float *v, const float *log_alpha,
                const float *h0, float *out, float *hT, int64_t B, int64_t L, int64_t G, int64_t H,
@@ -176,9 +180,10 @@ int ssd_bwd_ex(const float *q, const float *k, const float *v, const float *log_
     return SSD_ERR_ARG;
   const ssd::Geo g = make_geo(B, L, G, H, dk_dim, dv_dim, chunk);
   const Impl im = impl_of(path, chunk);
+  const bool det = ssd::tc::get_deterministic();  // read once: sizes the workspace and steers the call
   const size_t wsb = im == Impl::SEQ    ? ssd::seq::bwd_workspace_bytes(g)
                      : im == Impl::SIMT ? ssd::simt::bwd_workspace_bytes(g)
-                                        : ssd::tc::bwd_workspace_bytes(g);
+                                        : ssd::tc::bwd_workspace_bytes(g, det);
   void *ws = nullptr;
   rc = ws_alloc(&ws, wsb, s);
   if (rc) return rc;
@@ -188,7 +193,7 @@ int ssd_bwd_ex(const float *q, const float *k, const float *v, const float *log_
   else if (im == Impl::SIMT)
     e = ssd::simt::bwd(q, k, v, log_alpha, h0, dout, dhT, dq, dk, dv, dlog_alpha, dh0, g, ws, s);
   else
-    e = ssd::tc::bwd(q, k, v, log_alpha, h0, dout, dhT, dq, dk, dv, dlog_alpha, dh0, g, ws, s);
+    e = ssd::tc::bwd(q, k, v, log_alpha, h0, dout, dhT, dq, dk, dv, dlog_alpha, dh0, g, det, ws, s);
   if (ws) cudaFreeAsync(ws, s);
   return from_cuda(e);
 }
@@ -233,7 +238,7 @@ int ssd_bwd_workspace_bytes(int64_t B, int64_t L, int64_t G, int64_t H, int64_t 
   const Impl im = impl_of(path, chunk);
   *bytes = im == Impl::SEQ    ? ssd::seq::bwd_workspace_bytes(g)
            : im == Impl::SIMT ? ssd::simt::bwd_workspace_bytes(g)
-                              : ssd::tc::bwd_workspace_bytes(g);
+                              : ssd::tc::bwd_workspace_bytes(g, ssd::tc::get_deterministic());
   return SSD_OK;
 }
 

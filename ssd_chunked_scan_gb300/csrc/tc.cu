@@ -1179,6 +1179,29 @@ __global__ void __launch_bounds__(DT) k_dla(const float *__restrict__ Bt,
 }
 
 // ===========================================================================
+// Deterministic group sums: out[r, :] = sum over hh = 0 .. hpg - 1, in that
+// order, of in[r hpg + hh, :] for every (batch, token, group) row r of
+// d4 float4s (in: [B, L, H, dk], out: [B, L, G, dk], H = G hpg).
+__global__ void __launch_bounds__(NTH) k_group_sum(const float *__restrict__ in, float *__restrict__ out,
+                                                   int64_t rows, int hpg, int d4) {
+  const float4 *i4 = reinterpret_cast<const float4 *>(in);
+  float4 *o4 = reinterpret_cast<float4 *>(out);
+  const int64_t n = rows * d4, n_in = n * hpg;
+  for (int64_t e = (int64_t)blockIdx.x * NTH + threadIdx.x; e < n; e += (int64_t)gridDim.x * NTH) {
+    const int64_t r = e / d4, c = e - r * d4;
+    float4 acc = LDC(i4, (r * hpg) * d4 + c, n_in);
+    for (int hh = 1; hh < hpg; ++hh) {
+      const float4 x = LDC(i4, (r * hpg + hh) * d4 + c, n_in);
+      acc.x += x.x;
+      acc.y += x.y;
+      acc.z += x.z;
+      acc.w += x.w;
+    }
+    STC(o4, e, n, acc);
+  }
+}
+
+// ===========================================================================
 // Host side.
 
 namespace {
@@ -1374,6 +1397,7 @@ struct Side {
 std::mutex g_side_mu;
 Side g_side[64];
 std::atomic<bool> g_overlap{true};
+std::atomic<bool> g_det{false};
 
 cudaError_t get_side(Side **out) {
   int dev = 0;
@@ -1396,6 +1420,8 @@ cudaError_t get_side(Side **out) {
 
 bool set_overlap(bool on) { return g_overlap.exchange(on); }
 bool get_overlap() { return g_overlap.load(); }
+bool set_deterministic(bool on) { return g_det.exchange(on); }
+bool get_deterministic() { return g_det.load(); }
 
 int check_shape(int64_t dk, int64_t dv, int64_t chunk) {
   if (chunk != C) return SSD_ERR_CHUNK;
@@ -1410,11 +1436,13 @@ size_t fwd_workspace_bytes(const Geo &g) {
 
 // Two passes' states (both kept for dlog_alpha), their decays, three
 // per-token arrays, and the final state (used only when it has a cotangent).
-size_t bwd_workspace_bytes(const Geo &g) {
+size_t bwd_workspace_bytes(const Geo &g, bool det) {
   const PassGeo p = make_pass(g, (int)g.dk, (int)g.dv, false, true);
   const size_t nst = state_floats(p), na = (size_t)(g.B * g.H * p.nseg);
+  // deterministic group sums: per-head dq_h and dk_h, [B, L, H, dk] each
+  const size_t per_head = (det && g.hpg > 1) ? 2 * (size_t)(g.B * g.L * g.H * g.dk) + 4 : 0;
   return sizeof(float) * (2 * nst + 2 * na + 3 * (size_t)(g.B * g.L * g.H) +
-                          (size_t)(g.B * g.H * g.dk * g.dv)) + 256;
+                          (size_t)(g.B * g.H * g.dk * g.dv) + per_head) + 256;
 }
 
 cudaError_t fwd(const float *q, const float *k, const float *v, const float *la, const float *h0,
@@ -1433,7 +1461,7 @@ cudaError_t fwd(const float *q, const float *k, const float *v, const float *la,
 
 cudaError_t bwd(const float *q, const float *k, const float *v, const float *la, const float *h0,
                 const float *dout, const float *dhT, float *dq, float *dk, float *dv, float *dla,
-                float *dh0, const Geo &g, void *ws, cudaStream_t s) {
+                float *dh0, const Geo &g, bool det, void *ws, cudaStream_t s) {
   cudaError_t e = get_encoder();
   if (e != cudaSuccess) return e;
   if (g.B * g.L >= (int64_t)1 << 31) return cudaErrorNotSupported;
@@ -1462,11 +1490,20 @@ cudaError_t bwd(const float *q, const float *k, const float *v, const float *la,
     hT = reinterpret_cast<float *>((a + 15) & ~uintptr_t(15));
   }
   const bool grouped = g.hpg > 1;
-  if (grouped) {
+  // A group's per-head dq / dk: summed by atomic adds into dq / dk, or (det)
+  // written per head into the workspace and summed in head order afterwards
+  const bool atomic = grouped && !det;
+  float *dqh = nullptr, *dkh = nullptr;
+  if (grouped && det) {  // after hT's slot, 16-byte aligned for the float4 sums
+    const uintptr_t a = reinterpret_cast<uintptr_t>(Bt + g.B * g.L * g.H + g.B * g.H * g.dk * g.dv);
+    dqh = reinterpret_cast<float *>((a + 15) & ~uintptr_t(15));
+    dkh = dqh + g.B * g.L * g.H * g.dk;
+  }
+  if (atomic) {
     if ((e = cudaMemsetAsync(dq, 0, sizeof(float) * g.B * g.L * g.G * g.dk, s)) != cudaSuccess) return e;
     if ((e = cudaMemsetAsync(dk, 0, sizeof(float) * g.B * g.L * g.G * g.dk, s)) != cudaSuccess) return e;
   }
-  const int oslots = grouped ? (int)g.G : (int)g.H;
+  const int oslots = atomic ? (int)g.G : (int)g.H;
   // The dk / dv passes (pass B's states, both anti-causal walks) run on one
   // side stream and the intra-chunk dlog_alpha sums (inputs only) on another,
   // both forked from s after the memsets and joined before k_dla (or all on s
@@ -1511,8 +1548,8 @@ cudaError_t bwd(const float *q, const float *k, const float *v, const float *la,
   }
   const cudaError_t ej3 = overlap ? cudaEventRecord(sd->join3, s3) : cudaSuccess;
   cudaError_t eb = run_states<true>(pb, dout, q, la, dhT, true, dh0, stB, aB, nullptr, s2, "tc.seg_state_dk");
-  WalkOut okk{dk, oslots, k, rk};
-  if (eb == cudaSuccess) eb = run_walk<true>(pb, v, dout, q, la, stB, false, okk, grouped, s2, "tc.walk_dk");
+  WalkOut okk{dkh ? dkh : dk, oslots, k, rk};
+  if (eb == cudaSuccess) eb = run_walk<true>(pb, v, dout, q, la, stB, false, okk, atomic, s2, "tc.walk_dk");
   WalkOut ov{dv, (int)g.H, nullptr, nullptr};
   if (eb == cudaSuccess) eb = run_walk<true>(pc, k, q, dout, la, stB, true, ov, false, s2, "tc.walk_dv");
   // whatever was enqueued on s2 is joined back into s before this returns,
@@ -1534,12 +1571,22 @@ cudaError_t bwd(const float *q, const float *k, const float *v, const float *la,
   auto on_s = [&]() -> cudaError_t {
     cudaError_t ea = run_states<false>(pa, v, k, la, h0, true, hT, stA, aA, nullptr, s, "tc.seg_state_dq");
     if (ea != cudaSuccess) return ea;
-    WalkOut oq{dq, oslots, q, rq};
-    return run_walk<false>(pa, dout, v, k, la, stA, false, oq, grouped, s, "tc.walk_dq");
+    WalkOut oq{dqh ? dqh : dq, oslots, q, rq};
+    return run_walk<false>(pa, dout, v, k, la, stA, false, oq, atomic, s, "tc.walk_dq");
   };
   const cudaError_t ea = on_s();
   if ((e = join()) != cudaSuccess) return e;
   if (ea != cudaSuccess) return ea;
+  if (dqh) {  // the group sums, heads in order
+    const int64_t n4 = g.B * g.L * g.G * g.dk / 4;
+    const dim3 grid((unsigned)std::min<int64_t>(cdiv(n4, NTH), 65535 * 8));
+    for (int i = 0; i < 2; ++i) {
+      LaunchTrace lt("tc.group_sum", s);
+      if ((e = launch(k_group_sum, grid, dim3(NTH), 0, s, i == 0 ? dqh : dkh, i == 0 ? dq : dk, g.B * g.L * g.G,
+                      (int)g.hpg, (int)(g.dk / 4))) != cudaSuccess)
+        return e;
+    }
+  }
   {  // pass A's states are S^T, pass B's are G^T: the carry is their plain dot
     LaunchTrace lt("tc.dla", s);
     if ((e = launch(k_dla, dim3((unsigned)pa.nseg, (unsigned)g.H, (unsigned)g.B), dim3(DT), 0, s, Bt, rq, rk, stB, stA,

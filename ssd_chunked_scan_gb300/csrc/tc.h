@@ -9,19 +9,28 @@ namespace tc {
 int check_shape(int64_t dk, int64_t dv, int64_t chunk);
 
 size_t fwd_workspace_bytes(const Geo &g);
-size_t bwd_workspace_bytes(const Geo &g);
+// det: the deterministic group sums (see set_deterministic); the same value
+// must be given to bwd.
+size_t bwd_workspace_bytes(const Geo &g, bool det);
 
 // hT (final state, written) and dhT (its cotangent, read) may be NULL.
 cudaError_t fwd(const float *q, const float *k, const float *v, const float *la, const float *h0,
                 float *out, float *hT, const Geo &g, void *ws, cudaStream_t s);
 cudaError_t bwd(const float *q, const float *k, const float *v, const float *la, const float *h0,
                 const float *dout, const float *dhT, float *dq, float *dk, float *dv, float *dla,
-                float *dh0, const Geo &g, void *ws, cudaStream_t s);
+                float *dh0, const Geo &g, bool det, void *ws, cudaStream_t s);
 
 // Whether bwd runs its dk / dv passes on a side stream (see ssd_set_overlap);
 // set_overlap returns the previous setting.
 bool set_overlap(bool on);
 bool get_overlap();
+
+// Whether bwd sums a group's per-head dq / dk in a fixed order (per-head
+// results in the workspace, then one summing kernel) instead of by atomic
+// adds (see ssd_set_deterministic); set_deterministic returns the previous
+// setting.
+bool set_deterministic(bool on);
+bool get_deterministic();
 
 // Reads and clears the device error word of the current device: bit 0 is set
 // by a bounded wait that gave up, bit 1 by a failed index check (debug

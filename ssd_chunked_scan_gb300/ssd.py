@@ -33,7 +33,8 @@ EXPORTED = ("ssd_fwd", "ssd_bwd", "ssd_set_path", "ssd_get_path", "ssd_set_overl
             "ssd_get_overlap", "ssd_strerror",
             "ssd_last_device_error", "ssd_version", "ssd_launch_count", "ssd_trace_enable",
             "ssd_trace_collect", "ssd_trace_get", "ssd_trace_reset", "ssd_fwd_noalloc",
-            "ssd_fwd_noalloc_scratch_bytes", "ssd_test_stall_walks")
+            "ssd_fwd_noalloc_scratch_bytes", "ssd_test_stall_walks", "ssd_set_deterministic",
+            "ssd_get_deterministic")
 
 
 class SSDError(RuntimeError):
@@ -93,6 +94,10 @@ def _load():
     lib.ssd_fwd_noalloc.restype = ctypes.c_int
     lib.ssd_fwd_noalloc_scratch_bytes.argtypes = []
     lib.ssd_fwd_noalloc_scratch_bytes.restype = ctypes.c_size_t
+    lib.ssd_set_deterministic.argtypes = [ctypes.c_int]
+    lib.ssd_set_deterministic.restype = ctypes.c_int
+    lib.ssd_get_deterministic.argtypes = []
+    lib.ssd_get_deterministic.restype = ctypes.c_int
     lib.ssd_test_stall_walks.argtypes = [ctypes.c_int]
     lib.ssd_test_stall_walks.restype = ctypes.c_int
     return lib
@@ -124,6 +129,17 @@ def ssd_set_overlap(on: bool) -> bool:
 
 def ssd_get_overlap() -> bool:
     return bool(LIB.ssd_get_overlap())
+
+
+def ssd_set_deterministic(on: bool) -> bool:
+    """Sum a group's per-head dq / dk in head order (True) instead of with
+    atomic adds (False, the default) in the tensor-core backward, so that the
+    sums are bitwise reproducible; returns the previous setting."""
+    return bool(LIB.ssd_set_deterministic(1 if on else 0))
+
+
+def ssd_get_deterministic() -> bool:
+    return bool(LIB.ssd_get_deterministic())
 
 
 def ssd_last_device_error(stream=None) -> int:

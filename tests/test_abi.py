@@ -106,7 +106,7 @@ def test_set_path(lib):
 
 
 def test_version(lib):
-    assert lib.ssd_version() == 300
+    assert lib.ssd_version() == 400
 
 
 def test_set_overlap(lib):
@@ -117,6 +117,36 @@ def test_set_overlap(lib):
         assert lib.ssd_set_overlap(5) == 0 and lib.ssd_get_overlap() == 1
     finally:
         lib.ssd_set_overlap(first)
+
+
+def test_set_deterministic(lib):
+    first = lib.ssd_set_deterministic(1)
+    try:
+        assert first == 0  # off by default
+        assert lib.ssd_get_deterministic() == 1
+        assert lib.ssd_set_deterministic(0) == 1 and lib.ssd_get_deterministic() == 0
+    finally:
+        lib.ssd_set_deterministic(first)
+
+
+def test_deterministic_sums_grow_the_workspace_by_the_per_head_gradients(lib):
+    # tensor-core path, grouped heads: 2 * B * L * H * dk more floats (plus
+    # alignment slack); ungrouped problems need no per-head buffers
+    sz = lambda *a: (lambda n: (lib.ssd_bwd_workspace_bytes(*a, ctypes.byref(n)), n.value))(ctypes.c_size_t(0))
+    assert lib.ssd_set_path(0) == 0
+    first = lib.ssd_get_deterministic()
+    try:
+        lib.ssd_set_deterministic(0)
+        rc0, off = sz(2, 300, 2, 8, 64, 64, 64)
+        rc0b, off1 = sz(2, 300, 8, 8, 64, 64, 64)
+        lib.ssd_set_deterministic(1)
+        rc1, on = sz(2, 300, 2, 8, 64, 64, 64)
+        rc1b, on1 = sz(2, 300, 8, 8, 64, 64, 64)
+    finally:
+        lib.ssd_set_deterministic(first)
+    assert rc0 == rc1 == rc0b == rc1b == 0
+    assert on - off == 4 * (2 * 2 * 300 * 8 * 64 + 4)
+    assert on1 == off1
 
 
 def test_injected_workspace_failure_is_reported_before_launch(lib, monkeypatch):
