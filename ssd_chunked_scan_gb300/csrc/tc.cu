@@ -395,8 +395,9 @@ __global__ void __launch_bounds__(NTH) k_seg_scan(float *__restrict__ st,
 //   warp 2      score MMAs  Sc = q' k'^T  of the next chunk
 //   warp 3      decay factors of each chunk (fp64 in-chunk prefix of la, the
 //               lazy state scale) into a four-slot ring
-//   warps 4-7   mask: P = D o Sc into shared memory (K-major), and k' turned
-//               in place into w k' (MN-major, scaled by the state weights)
+//   warps 4-7   mask: v' rounded to TF32 in place, P = D o Sc into shared
+//               memory (K-major), and k' turned in place into w k'
+//               (MN-major, scaled by the state weights, rounded to TF32)
 //   warps 8-11  epilogue: out'_t = f_t X_t + Y_t to global memory (atomic
 //               add over a group's heads when ATOMIC), dcs_t = y_t . f_t X_t
 //               when SPLIT, and the occasional explicit state rescale
@@ -677,6 +678,26 @@ __global__ void __launch_bounds__(WT, 1) k_walk(const __grid_constant__ CUtensor
       const Fac &F = fac[slot];
       const float csA = F.cs2[lane], csB = F.cs2[lane + 32];
       const float kwA = F.kw[lane], kwB = F.kw[lane + 32];
+      // Round the chunk's v' tile to TF32 in place while its score MMAs run:
+      // the tensor core truncates what it reads, and v' feeds the state
+      // update of every chunk, whose bias would accumulate along the walk
+      // (Y and the update read v' only after p_full, below)
+      if (!mbar_wait_all(&full[st], (ci >> 1) & 1, ab)) break;
+      {
+        float4 *V4 = reinterpret_cast<float4 *>(Vs(st));
+        const int n4 = ncbv * (int)BLK / 16;  // a multiple of 4 * 128
+#pragma unroll 1
+        for (int e0 = wt; e0 < n4; e0 += 4 * 128) {
+          float4 x[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) x[u] = LDC(V4, e0 + u * 128, n4);
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            x[u].x = tf32r(x[u].x); x[u].y = tf32r(x[u].y); x[u].z = tf32r(x[u].z); x[u].w = tf32r(x[u].w);
+            STC(V4, e0 + u * 128, n4, x[u]);
+          }
+        }
+      }
       if (!mbar_wait_all(&s_full[sb], (ci >> 1) & 1, ab)) break;
       if (ci >= 1 && !mbar_wait_all(&p_empty, (ci - 1) & 1, ab)) break;
       tc_fence_after();
