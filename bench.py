@@ -64,22 +64,33 @@ def load_peaks():
 # file in the tree no longer hashes to that, the group's figures no longer
 # describe the kernels and the bench line reports traffic null, saying why.
 TRAFFIC_GROUPS = {
-    "tc.": {"source": "ssd_chunked_scan_gb300/csrc/tc.cu", "sha16": None, "commit": None,
-            "bytes": {}},
-    "simt.": {"source": "ssd_chunked_scan_gb300/csrc/simt.cu", "sha16": None, "commit": "f753b28",
+    "tc.": {"source": "ssd_chunked_scan_gb300/csrc/tc.cu", "sha16": "d9cc4fcb928fc674", "commit": "1d35a6f",
+            "bytes": {
+                "tc.seg_state": 172559872,
+                "tc.seg_state_dq": 169523712,
+                "tc.seg_state_dk": 169795584,
+                "tc.seg_scan": (10533120 + 8445184 + 10536448) // 3,  # mean of the three passes' scans
+                "tc.walk_out": 303783424,
+                "tc.walk_dq": 406783232,
+                "tc.walk_dk": 405994496,
+                "tc.walk_dv": 305571072,
+                "tc.dla_intra": 337483008,
+                "tc.dla": 15740416,
+            }},
+    "simt.": {"source": "ssd_chunked_scan_gb300/csrc/simt.cu", "sha16": "5682068978fc8373", "commit": "02155b1",
               "bytes": {}},
     "mamba.": {"source": "ssd_chunked_scan_gb300/csrc/mamba.cu", "sha16": "46a5b2d4c8f2dcb9", "commit": "c617278",
                "bytes": {}},
 }
 _SIMT_TRAFFIC = {
     # kernels that run twice per step: the mean of their launches
-    "simt.chunk_state": (168927744 + 213100544 + 168965120 + 209852160) // 2,
-    "simt.state_scan_fwd": (270607872 + 204486912 + 270578176 + 204050688) // 2,
-    "simt.chunk_out": 471726848 + 110684672,
-    "simt.query_state": 168932864 + 209318400,
-    "simt.state_scan_rev": 268482048 + 206218496,
-    "simt.chunk_grad": 1171999232 + 349719040,
-    "simt.dla_carry": 1090304,
+    "simt.chunk_state": (381861888 + 379118080) // 2,
+    "simt.state_scan_fwd": (475357696 + 475306752) // 2,
+    "simt.chunk_out": 582941184,
+    "simt.query_state": 377939968,
+    "simt.state_scan_rev": 475440384,
+    "simt.chunk_grad": 1518565888,
+    "simt.dla_carry": 1090048,
 }
 # the same for the Mamba kernels at d1024 L8192; seg_state and seg_scan run more
 # than once per step: the mean of their launches
