@@ -270,30 +270,51 @@ __global__ void __launch_bounds__(SS_THREADS, 1) k_seg_state(const __grid_consta
         const int64_t t = s_begin + (int64_t)n * SL + u;
         return (n < nsl && t < s_end) ? (double)LDC(la, (b * p.L + t) * p.H + h, n_la) : 0.0;
       };
-      double x0n = la_of(0, 2 * lane), x1n = la_of(0, 2 * lane + 1);  // one slice ahead
-      for (int n = 0; n < nsl; ++n) {
-        const int wb = n & 1;
-        const int64_t t0 = s_begin + (int64_t)n * SL;
-        const int len = (int)imin64(SL, s_end - t0);
-        const double x0 = x0n, x1 = x1n;
-        x0n = la_of(n + 1, 2 * lane);
-        x1n = la_of(n + 1, 2 * lane + 1);
-        double incl = x0 + x1;
+      // la of the next WLA slices is in flight while the current WLA slices'
+      // weights are made: an L2 round trip takes longer than a slice's MMAs
+      constexpr int WLA = 4;
+      double xc0[WLA], xc1[WLA], xn0[WLA], xn1[WLA];
 #pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const double y = __shfl_up_sync(0xffffffffu, incl, o);
-          if (lane >= o) incl += y;
+      for (int u = 0; u < WLA; ++u) {
+        xc0[u] = la_of(u, 2 * lane);
+        xc1[u] = la_of(u, 2 * lane + 1);
+      }
+      for (int n0 = 0; ok && n0 < nsl; n0 += WLA) {
+#pragma unroll
+        for (int u = 0; u < WLA; ++u) {
+          xn0[u] = la_of(n0 + WLA + u, 2 * lane);
+          xn1[u] = la_of(n0 + WLA + u, 2 * lane + 1);
         }
-        const double cs1 = carry + incl, cs0 = cs1 - x1;
-        carry += __shfl_sync(0xffffffffu, incl, 31);
-        const float w0 = 2 * lane < len ? exp2f((float)((REV ? cs0 : tot - cs0) * LOG2E_D)) : 0.f;
-        const float w1 = 2 * lane + 1 < len ? exp2f((float)((REV ? cs1 : tot - cs1) * LOG2E_D)) : 0.f;
-        if (n >= 2 && !mbar_wait_all(&w_free[wb], ((n >> 1) - 1) & 1, ab)) { ok = false; break; }
-        float *W = reinterpret_cast<float *>(Wb + wb * 2 * BLK);
-        STC(W, sw128_off(2 * lane, 2 * lane, SL) / 4, 2 * BLK / 4, tf32r(w0));
-        STC(W, sw128_off(2 * lane + 1, 2 * lane + 1, SL) / 4, 2 * BLK / 4, tf32r(w1));
-        fence_async_smem();
-        mbar_arrive(&w_full[wb]);
+#pragma unroll
+        for (int u = 0; u < WLA; ++u) {
+          const int n = n0 + u;
+          if (n >= nsl) break;
+          const int wb = n & 1;
+          const int64_t t0 = s_begin + (int64_t)n * SL;
+          const int len = (int)imin64(SL, s_end - t0);
+          const double x0 = xc0[u], x1 = xc1[u];
+          double incl = x0 + x1;
+#pragma unroll
+          for (int o = 1; o < 32; o <<= 1) {
+            const double y = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += y;
+          }
+          const double cs1 = carry + incl, cs0 = cs1 - x1;
+          carry += __shfl_sync(0xffffffffu, incl, 31);
+          const float w0 = 2 * lane < len ? exp2f((float)((REV ? cs0 : tot - cs0) * LOG2E_D)) : 0.f;
+          const float w1 = 2 * lane + 1 < len ? exp2f((float)((REV ? cs1 : tot - cs1) * LOG2E_D)) : 0.f;
+          if (n >= 2 && !mbar_wait_all(&w_free[wb], ((n >> 1) - 1) & 1, ab)) { ok = false; break; }
+          float *W = reinterpret_cast<float *>(Wb + wb * 2 * BLK);
+          STC(W, sw128_off(2 * lane, 2 * lane, SL) / 4, 2 * BLK / 4, tf32r(w0));
+          STC(W, sw128_off(2 * lane + 1, 2 * lane + 1, SL) / 4, 2 * BLK / 4, tf32r(w1));
+          fence_async_smem();
+          mbar_arrive(&w_full[wb]);
+        }
+#pragma unroll
+        for (int u = 0; u < WLA; ++u) {
+          xc0[u] = xn0[u];
+          xc1[u] = xn1[u];
+        }
       }
     }
     if (ok && mbar_wait_all(&done, 0, ab)) {  // (ok is uniform over each warp)
@@ -774,10 +795,24 @@ __global__ void __launch_bounds__(WT, 1) k_walk(const __grid_constant__ CUtensor
       const int64_t sz = (int64_t)dk * dv, h0 = (bh * p.nseg + seg) * sz, n_h = p.B * p.H * p.nseg * sz;
       for (int c0 = 0; c0 < p.dkp; c0 += 32) {
         float hv[32];
+        if (!SPLIT && hseg_t) {  // lane j reads its row as float4s (h0, j dk, c0 multiples of 4; dk of 8)
+          const float4 *H4 = reinterpret_cast<const float4 *>(Hseg);
 #pragma unroll
-        for (int ii = 0; ii < 32; ++ii) {
-          const int i = c0 + ii;
-          hv[ii] = (j < dv && i < dk) ? LDC(Hseg, h0 + (hseg_t ? (int64_t)j * dk + i : (int64_t)i * dv + j), n_h) : 0.f;
+          for (int i4 = 0; i4 < 8; ++i4) {
+            const int i = c0 + 4 * i4;
+            const float4 x = (j < dv && i < dk) ? LDC(H4, (h0 + (int64_t)j * dk + i) / 4, n_h / 4)
+                                                : make_float4(0.f, 0.f, 0.f, 0.f);
+            hv[4 * i4] = x.x;
+            hv[4 * i4 + 1] = x.y;
+            hv[4 * i4 + 2] = x.z;
+            hv[4 * i4 + 3] = x.w;
+          }
+        } else {
+#pragma unroll
+          for (int ii = 0; ii < 32; ++ii) {
+            const int i = c0 + ii;
+            hv[ii] = (j < dv && i < dk) ? LDC(Hseg, h0 + (hseg_t ? (int64_t)j * dk + i : (int64_t)i * dv + j), n_h) : 0.f;
+          }
         }
         tmem_st32(T_ST + lb + c0, hv);
       }
@@ -1127,7 +1162,12 @@ __global__ void __launch_bounds__(NTH) k_dla_intra(const __grid_constant__ CUten
 // elements).  For the last segment G_end is the final state's cotangent and
 // S_end the final state: Gfin and Sfin, both [dk x dv] per head, or no term
 // when Gfin is NULL.  grid (nseg, H, B).
+// The segment is taken in tiles of DT * DTPT tokens from its end; thread tid
+// owns DTPT consecutive tokens of a tile, and all of a tile's loads are issued
+// together (the first tile's before the carry's dot product), so a tile costs
+// one memory round trip; the suffix sums run in fp64.
 constexpr int DT = 256;
+constexpr int DTPT = 8;
 __global__ void __launch_bounds__(DT) k_dla(const float *__restrict__ Bt,
                                             const float *__restrict__ rq,
                                             const float *__restrict__ rk,
@@ -1136,11 +1176,27 @@ __global__ void __launch_bounds__(DT) k_dla(const float *__restrict__ Bt,
                                             const float *__restrict__ Gfin,
                                             const float *__restrict__ Sfin, float *__restrict__ dla,
                                             int64_t L, int64_t H, int64_t sz, int Ls, int nseg) {
+  constexpr int TILE = DT * DTPT;
   __shared__ double wred[DT / 32];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int64_t seg = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int64_t bh = b * H + h;
   const int64_t n_tok = (int64_t)gridDim.z * L * H;  // element counts (debug-build index checks)
+  const int64_t s_begin = seg * (int64_t)Ls;
+  const int64_t s_end = imin64(L, s_begin + Ls);
+  float xq[DTPT], xk[DTPT], xb[DTPT];
+  auto load_tile = [&](int64_t hi) {  // tokens hi - TILE + tid DTPT + u (those >= s_begin)
+    const int64_t t0 = hi - TILE + (int64_t)tid * DTPT;
+#pragma unroll
+    for (int u = 0; u < DTPT; ++u) {
+      const bool ok = t0 + u >= s_begin;
+      const int64_t idx = (b * L + t0 + u) * H + h;
+      xq[u] = ok ? LDC(rq, idx, n_tok) : 0.f;
+      xk[u] = ok ? LDC(rk, idx, n_tok) : 0.f;
+      xb[u] = ok ? LDC(Bt, idx, n_tok) : 0.f;
+    }
+  };
+  load_tile(s_end);
   // carry = <G_end, S_end>: float4 loads, fp32 partial sums, fp64 across threads
   float part = 0.f;
   const float4 *G = nullptr, *S = nullptr;
@@ -1159,6 +1215,7 @@ __global__ void __launch_bounds__(DT) k_dla(const float *__restrict__ Bt,
     n4 = (int64_t)gridDim.z * H * sz / 4;
   }
   if (G) {
+#pragma unroll 4
     for (int64_t e = tid; e < sz / 4; e += DT) {
       const float4 g = LDC(G, g0 + e, n4), x = LDC(S, s0 + e, n4);
       part = fmaf(g.x, x.x, fmaf(g.y, x.y, fmaf(g.z, x.z, fmaf(g.w, x.w, part))));
@@ -1173,26 +1230,31 @@ __global__ void __launch_bounds__(DT) k_dla(const float *__restrict__ Bt,
 #pragma unroll
   for (int w2 = 0; w2 < DT / 32; ++w2) carry += wred[w2];
   __syncthreads();
-  // suffix sums of rq - rk over the segment, 256 tokens at a time from its end
-  const int64_t s_begin = seg * (int64_t)Ls;
-  const int64_t s_end = imin64(L, s_begin + Ls);
-  for (int64_t hi = s_end; hi > s_begin; hi -= DT) {
-    const int64_t t = hi - DT + tid;  // thread tid owns token t (valid if t >= s_begin)
-    const bool ok = t >= s_begin;
-    const int64_t idx = (b * L + t) * H + h;
-    double x = ok ? (double)LDC(rq, idx, n_tok) - (double)LDC(rk, idx, n_tok) : 0.0;
+  for (int64_t hi = s_end; hi > s_begin; hi -= TILE) {
+    if (hi != s_end) load_tile(hi);
+    double suf[DTPT], tot = 0.0;  // suffix sums over this thread's tokens
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {  // inclusive suffix within the warp
+    for (int u = DTPT - 1; u >= 0; --u) {
+      tot += (double)xq[u] - (double)xk[u];
+      suf[u] = tot;
+    }
+    double x = tot;  // inclusive suffix of the thread totals within the warp
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
       const double y = __shfl_down_sync(0xffffffffu, x, o);
       if (lane + o < 32) x += y;
     }
     if (lane == 0) wred[warp] = x;  // warp total
     __syncthreads();
-    double after = carry;  // everything right of this warp
+    double after = carry + (x - tot);  // everything right of this thread's tokens
 #pragma unroll
     for (int w2 = 0; w2 < DT / 32; ++w2)
       if (w2 > warp) after += wred[w2];
-    if (ok) STC(dla, idx, n_tok, (float)((double)LDC(Bt, idx, n_tok) + x + after));
+    const int64_t t0 = hi - TILE + (int64_t)tid * DTPT;
+#pragma unroll
+    for (int u = 0; u < DTPT; ++u)
+      if (t0 + u >= s_begin)
+        STC(dla, (b * L + t0 + u) * H + h, n_tok, (float)((double)xb[u] + suf[u] + after));
 #pragma unroll
     for (int w2 = 0; w2 < DT / 32; ++w2) carry += wred[w2];
     __syncthreads();
