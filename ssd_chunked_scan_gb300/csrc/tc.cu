@@ -959,197 +959,231 @@ __global__ void __launch_bounds__(WT, 1) k_walk(const __grid_constant__ CUtensor
 // computed once; dout v^T per head.  Both score MMAs have M = 64
 // (rows 16w..16w+15 in lanes 32w..) and share one two-tile shared-memory
 // buffer; the next head's tiles load while the current head's sums run.
-// grid (N chunks, G, B), 128 threads, three CTAs per SM.
-__global__ void __launch_bounds__(NTH) k_dla_intra(const __grid_constant__ CUtensorMap tmQ,
-                                                   const __grid_constant__ CUtensorMap tmK,
-                                                   const __grid_constant__ CUtensorMap tmV,
-                                                   const __grid_constant__ CUtensorMap tmD,
-                                                   const float *__restrict__ la,
-                                                   float *__restrict__ Bt, PassGeo p) {
+//
+// Persistent: each CTA holds DI_WG independent workers of 128 threads (one
+// warpgroup each: its own tiles, barriers, named barrier and 128 tensor-memory
+// columns), and worker w of CTA c takes the (chunk, group, batch) items
+// w + DI_WG c, w + DI_WG (c + grid), ...  Beside the backward's walks the grid
+// is the SMs the walks leave idle, and a CTA fills its SM (shared memory),
+// so that no walk or contraction CTA lands beside it; otherwise the grid
+// covers the GPU.
+constexpr int DI_WG = 3;
+__global__ void __launch_bounds__(DI_WG * NTH, 1) k_dla_intra(const __grid_constant__ CUtensorMap tmQ,
+                                                             const __grid_constant__ CUtensorMap tmK,
+                                                             const __grid_constant__ CUtensorMap tmV,
+                                                             const __grid_constant__ CUtensorMap tmD,
+                                                             const float *__restrict__ la,
+                                                             float *__restrict__ Bt, PassGeo p, int64_t N,
+                                                             int64_t G, uint32_t wbytes) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
-  uint8_t *smem = smem_align1024(smem_raw);
   const int dk = p.dk, dv = p.dv;  // here dk = q/k features, dv = v/dout features
   const int ncbk = p.dkp / 32, ncbv = p.dvp / 32, ncbm = ncbk > ncbv ? ncbk : ncbv;
+  __shared__ uint64_t bars[2 * DI_WG];
+  __shared__ uint32_t tmem_base;
+  const int wg = threadIdx.x / NTH;  // this worker
+  const int tid = threadIdx.x % NTH, warp = tid >> 5, lane = tid & 31;
+  const int bid = 1 + wg;            // its named barrier
+  uint8_t *smem = smem_align1024(smem_raw) + (size_t)wg * wbytes;
   uint8_t *T1 = smem, *T2 = smem + ncbm * 8192;
   float *R = (float *)(T2 + ncbm * 8192);  // [4][64] column partials, [64] row sums
   float *cs = R + 5 * C;                  // [64]
-  __shared__ uint64_t bar_tma, bar_mma;
-  __shared__ uint32_t tmem_base;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int64_t c = blockIdx.x, grp = blockIdx.y, b = blockIdx.z;
-  const int64_t t0 = c * C;
-  const int len = (int)imin64(C, p.L - t0);
-  const int row = (int)(b * p.L + t0);
+  uint64_t *bar_tma = &bars[2 * wg], *bar_mma = &bars[2 * wg + 1];
   const int hpg = p.hpg;
+  const int64_t n_items = N * G * p.B;
 
-  auto load_dv = [&](int64_t h) {  // dout -> T1, v -> T2
-    mbar_expect_tx(&bar_tma, (uint32_t)(2 * ncbv) * 8192);
-    for (int cb = 0; cb < ncbv; ++cb) {
-      tma_load_3d(T1 + cb * 8192, &tmD, &bar_tma, cb * 32, (int)h, row);
-      tma_load_3d(T2 + cb * 8192, &tmV, &bar_tma, cb * 32, (int)h, row);
-    }
-  };
-  if (warp == 0) tmem_alloc(&tmem_base, 128);
-  if (tid == 0) {
-    mbar_init(&bar_tma, 1);
-    mbar_init(&bar_mma, 1);
+  if (threadIdx.x < 32) tmem_alloc(&tmem_base, 512);
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < 2 * DI_WG; ++i) mbar_init(&bars[i], 1);
     fence_mbar_init();
-    mbar_expect_tx(&bar_tma, (uint32_t)(2 * ncbk) * 8192);
-    for (int cb = 0; cb < ncbk; ++cb) {
-      tma_load_3d(T1 + cb * 8192, &tmQ, &bar_tma, cb * 32, (int)grp, row);
-      tma_load_3d(T2 + cb * 8192, &tmK, &bar_tma, cb * 32, (int)grp, row);
-    }
+    prefetch_tmap(&tmQ);
+    prefetch_tmap(&tmK);
+    prefetch_tmap(&tmV);
+    prefetch_tmap(&tmD);
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = tmem_base;
-  const uint32_t lb = (uint32_t)(warp * 32) << 16;
+  const uint32_t tmem = tmem_base + (uint32_t)(128 * wg);
+  const uint32_t lb = (uint32_t)(warp * 32) << 16;  // (warp w of a warpgroup reaches lanes 32w..)
+  // thread 0's view of what is in flight: whether a tile load, and an MMA
+  // group, have been issued and not yet seen to complete (and the parity of
+  // the phase each completes); both are drained before the tensor memory is
+  // freed, also after a failure.  kt / km count the phases of the two
+  // barriers waited for so far.
+  bool tma_out = false, mma_out = false;
+  uint32_t kt = 0, km = 0, tma_par = 0, mma_par = 0;
   bool ok = true;
-  // thread 0's view of what is in flight: the phase whose tile loads, and
-  // the phase whose MMAs, have not been seen to complete (-1: none); both are
-  // drained before the tensor memory is freed, also after a failure
-  int tma_ph = 0, mma_ph = -1;
   // Score rows live in lanes 0-15 of each warp (M = 64); the lane 16 above a
   // row works on its upper 32 columns, so every lane holds 32 columns:
   // u = 32 * up + i.
   const int up = lane >> 4;
-  float sq[32];  // q k^T, this lane's half row
-  // phase 0: q k^T; phase 1 + hh: dout v^T of head hh
-  for (int ph = 0; ph <= hpg; ++ph) {
-    const int ncb = ph == 0 ? ncbk : ncbv;
-    const int kdim = ph == 0 ? dk : dv;
-    const int64_t h = grp * hpg + (ph == 0 ? 0 : ph - 1);
-    if (ph >= 1 && warp == 0) {  // in-chunk prefix of la, times log2(e)
-      warp_cumsum64(la, p.B * p.L * p.H, (b * p.L + t0) * p.H + h, p.H, len, 0.0, cs);
-      __syncwarp();
-      for (int t = lane; t < C; t += 32) cs[t] = t < len ? cs[t] * 1.4426950408889634f : 0.f;
-    }
-    ok = mbar_wait(&bar_tma, ph & 1) && ok;
-    if (tid == 0 && ok) tma_ph = -1;
-    if (__syncthreads_or(!ok)) break;
-    {  // round both tiles to TF32 (nearest) in place
-      const int r = tid & 63, half = tid >> 6;
-      const int cols = ncb * 16;
-      float4 *a4 = reinterpret_cast<float4 *>(T1), *b4 = reinterpret_cast<float4 *>(T2);
-      const int n4 = ncbm * 8192 / 16;
-      for (int col = half * cols; col < (half + 1) * cols; col += 4) {
-        const int i4 = sw128_off(r, col, C) / 16;
-        float4 x = LDC(a4, i4, n4), y = LDC(b4, i4, n4);
-        x.x = tf32r(x.x); x.y = tf32r(x.y); x.z = tf32r(x.z); x.w = tf32r(x.w);
-        y.x = tf32r(y.x); y.y = tf32r(y.y); y.z = tf32r(y.z); y.w = tf32r(y.w);
-        STC(a4, i4, n4, x);
-        STC(b4, i4, n4, y);
+  for (int64_t item = wg + (int64_t)DI_WG * blockIdx.x; ok && item < n_items;
+       item += (int64_t)DI_WG * gridDim.x) {
+    const int64_t c = item % N, grp = (item / N) % G, b = item / (N * G);
+    const int64_t t0 = c * C;
+    const int len = (int)imin64(C, p.L - t0);
+    const int row = (int)(b * p.L + t0);
+    if (tid == 0) {  // q -> T1, k -> T2
+      mbar_expect_tx(bar_tma, (uint32_t)(2 * ncbk) * 8192);
+      for (int cb = 0; cb < ncbk; ++cb) {
+        tma_load_3d(T1 + cb * 8192, &tmQ, bar_tma, cb * 32, (int)grp, row);
+        tma_load_3d(T2 + cb * 8192, &tmK, bar_tma, cb * 32, (int)grp, row);
       }
+      tma_out = true;
+      tma_par = kt & 1;
     }
-    fence_async_smem();
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    if (tid == 0) {  // phase 0 -> cols [0,64); later phases -> [64,128)
-      const uint32_t a = smem_u32(T1), bb = smem_u32(T2);
-      const uint32_t id = idesc_tf32(64, 64);
-      for (int kk = 0; kk < kdim / 8; ++kk) {
-        const uint32_t off = (kk >> 2) * 8192 + (kk & 3) * 32;
-        mma_ss(tmem + (ph == 0 ? 0 : 64), sdesc(a + off), sdesc(bb + off), id, kk > 0 ? 1u : 0u);
+    float sq[32];  // q k^T, this lane's half row
+    // phase 0: q k^T; phase 1 + hh: dout v^T of head hh
+    for (int ph = 0; ph <= hpg; ++ph) {
+      const int ncb = ph == 0 ? ncbk : ncbv;
+      const int kdim = ph == 0 ? dk : dv;
+      const int64_t h = grp * hpg + (ph == 0 ? 0 : ph - 1);
+      if (ph >= 1 && warp == 0) {  // in-chunk prefix of la, times log2(e)
+        warp_cumsum64(la, p.B * p.L * p.H, (b * p.L + t0) * p.H + h, p.H, len, 0.0, cs);
+        __syncwarp();
+        for (int t = lane; t < C; t += 32) cs[t] = t < len ? cs[t] * 1.4426950408889634f : 0.f;
       }
-      mma_commit(&bar_mma);
-      mma_ph = ph;
-    }
-    ok = mbar_wait(&bar_mma, ph & 1) && ok;
-    if (tid == 0 && ok) mma_ph = -1;
-    tc_fence_after();
-    if (tid == 0 && ok && ph < hpg) {  // the tiles are consumed: next head's loads
-      load_dv(grp * hpg + ph);
-      tma_ph = ph + 1;
-    }
-    if (ph == 0) {
-      float lo[32], hi[32];
-      tmem_ld32(tmem + lb, lo);
-      tmem_ld32(tmem + lb + 32, hi);
-#pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        const float x = __shfl_sync(0xffffffffu, hi[i], lane & 15);
-        sq[i] = up ? x : lo[i];
+      ok = mbar_wait(bar_tma, kt & 1) && ok;
+      if (tid == 0 && ok) tma_out = false;
+      ++kt;
+      if (named_sync_or(bid, NTH, !ok)) {
+        ok = false;
+        break;
       }
-      continue;
-    }
-    float dp[32];  // dout v^T of this head, this lane's half row
-    {
-      float lo[32], hi[32];
-      tmem_ld32(tmem + lb + 64, lo);
-      tmem_ld32(tmem + lb + 96, hi);
-#pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        const float x = __shfl_sync(0xffffffffu, hi[i], lane & 15);
-        dp[i] = up ? x : lo[i];
-      }
-    }
-    // B_t = B_{t+1} + rowpre_t - colsuf_t with rowpre_t = sum_{u<t} M[t][u]
-    // (a row of the strictly lower triangle) and colsuf_t = sum_{r>t} M[r][t]
-    // (a column of it).  Row r's two halves live in lanes r % 16 and
-    // r % 16 + 16 of warp r / 16; the column sums are reduce-scattered over
-    // each half-warp (lane l ends with columns 32 up + 2 (l % 16) + {0, 1}),
-    // then added over the four warps in shared memory.
-    {
-      const int r = warp * 16 + (lane & 15);
-      const bool rowok = r < len;
-      const float cr = cs[rowok ? r : 0];
-      float *m = dp;  // M's half row, in place of dout v^T's
-      float rp0 = 0.f, rp1 = 0.f;
-#pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        const int u = 32 * up + i;
-        m[i] = (rowok && u < r) ? ex2f(cr - cs[u]) * sq[i] * dp[i] : 0.f;
-        if (i & 1) rp1 += m[i];
-        else rp0 += m[i];
-      }
-      float rp = rp0 + rp1;
-      rp += __shfl_xor_sync(0xffffffffu, rp, 16);  // both halves of the row
-#pragma unroll
-      for (int off = 8, n = 32; off >= 1; off >>= 1, n >>= 1) {
-        const bool hiL = (lane & off) != 0;
-#pragma unroll
-        for (int k2 = 0; k2 < n / 2; ++k2) {
-          const float mine = hiL ? m[n / 2 + k2] : m[k2];
-          const float send = hiL ? m[k2] : m[n / 2 + k2];
-          m[k2] = mine + __shfl_xor_sync(0xffffffffu, send, off);
+      {  // round both tiles to TF32 (nearest) in place
+        const int r = tid & 63, half = tid >> 6;
+        const int cols = ncb * 16;
+        float4 *a4 = reinterpret_cast<float4 *>(T1), *b4 = reinterpret_cast<float4 *>(T2);
+        const int n4 = ncbm * 8192 / 16;
+        for (int col = half * cols; col < (half + 1) * cols; col += 4) {
+          const int i4 = sw128_off(r, col, C) / 16;
+          float4 x = LDC(a4, i4, n4), y = LDC(b4, i4, n4);
+          x.x = tf32r(x.x); x.y = tf32r(x.y); x.z = tf32r(x.z); x.w = tf32r(x.w);
+          y.x = tf32r(y.x); y.y = tf32r(y.y); y.z = tf32r(y.z); y.w = tf32r(y.w);
+          STC(a4, i4, n4, x);
+          STC(b4, i4, n4, y);
         }
       }
-      const int u0 = 32 * up + 2 * (lane & 15);
-      R[warp * C + u0] = m[0];
-      R[warp * C + u0 + 1] = m[1];
-      if (rowok && up == 0) R[4 * C + r] = rp;
-    }
-    __syncthreads();
-    if (warp == 0) {  // suffix sums of rowpre - colsuf; lane l owns t = 2l, 2l + 1
-      float dd[2];
-#pragma unroll
-      for (int j = 0; j < 2; ++j) {
-        const int t = 2 * lane + j;
-        dd[j] = t < len ? R[4 * C + t] - (R[t] + R[C + t] + R[2 * C + t] + R[3 * C + t]) : 0.f;
+      fence_async_smem();
+      tc_fence_before();
+      named_sync(bid, NTH);
+      tc_fence_after();
+      if (tid == 0) {  // phase 0 -> cols [0,64); later phases -> [64,128)
+        const uint32_t a = smem_u32(T1), bb = smem_u32(T2);
+        const uint32_t id = idesc_tf32(64, 64);
+        for (int kk = 0; kk < kdim / 8; ++kk) {
+          const uint32_t off = (kk >> 2) * 8192 + (kk & 3) * 32;
+          mma_ss(tmem + (ph == 0 ? 0 : 64), sdesc(a + off), sdesc(bb + off), id, kk > 0 ? 1u : 0u);
+        }
+        mma_commit(bar_mma);
+        mma_out = true;
+        mma_par = km & 1;
       }
-      float x = dd[0] + dd[1];  // inclusive suffix over lanes of the pair sums
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const float y = __shfl_down_sync(0xffffffffu, x, o);
-        if (lane + o < 32) x += y;
+      ok = mbar_wait(bar_mma, km & 1) && ok;
+      if (tid == 0 && ok) mma_out = false;
+      ++km;
+      tc_fence_after();
+      if (tid == 0 && ok && ph < hpg) {  // the tiles are consumed: next head's loads
+        const int64_t hn = grp * hpg + ph;
+        mbar_expect_tx(bar_tma, (uint32_t)(2 * ncbv) * 8192);
+        for (int cb = 0; cb < ncbv; ++cb) {  // dout -> T1, v -> T2
+          tma_load_3d(T1 + cb * 8192, &tmD, bar_tma, cb * 32, (int)hn, row);
+          tma_load_3d(T2 + cb * 8192, &tmV, bar_tma, cb * 32, (int)hn, row);
+        }
+        tma_out = true;
+        tma_par = kt & 1;
       }
-      const float b1 = x - dd[0];  // B_{2l+1} = suffix from 2l+1
-      const float b0 = x;          // B_{2l}
-      const int64_t bt = (b * p.L + t0) * p.H + h, n_bt = p.B * p.L * p.H;
-      if (2 * lane < len) STC(Bt, bt + (int64_t)(2 * lane) * p.H, n_bt, b0);
-      if (2 * lane + 1 < len) STC(Bt, bt + (int64_t)(2 * lane + 1) * p.H, n_bt, b1);
+      if (ph == 0) {
+        float lo[32], hi[32];
+        tmem_ld32(tmem + lb, lo);
+        tmem_ld32(tmem + lb + 32, hi);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const float x = __shfl_sync(0xffffffffu, hi[i], lane & 15);
+          sq[i] = up ? x : lo[i];
+        }
+        continue;
+      }
+      float dp[32];  // dout v^T of this head, this lane's half row
+      {
+        float lo[32], hi[32];
+        tmem_ld32(tmem + lb + 64, lo);
+        tmem_ld32(tmem + lb + 96, hi);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const float x = __shfl_sync(0xffffffffu, hi[i], lane & 15);
+          dp[i] = up ? x : lo[i];
+        }
+      }
+      // B_t = B_{t+1} + rowpre_t - colsuf_t with rowpre_t = sum_{u<t} M[t][u]
+      // (a row of the strictly lower triangle) and colsuf_t = sum_{r>t} M[r][t]
+      // (a column of it).  Row r's two halves live in lanes r % 16 and
+      // r % 16 + 16 of warp r / 16; the column sums are reduce-scattered over
+      // each half-warp (lane l ends with columns 32 up + 2 (l % 16) + {0, 1}),
+      // then added over the four warps in shared memory.
+      {
+        const int r = warp * 16 + (lane & 15);
+        const bool rowok = r < len;
+        const float cr = cs[rowok ? r : 0];
+        float *m = dp;  // M's half row, in place of dout v^T's
+        float rp0 = 0.f, rp1 = 0.f;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const int u = 32 * up + i;
+          m[i] = (rowok && u < r) ? ex2f(cr - cs[u]) * sq[i] * dp[i] : 0.f;
+          if (i & 1) rp1 += m[i];
+          else rp0 += m[i];
+        }
+        float rp = rp0 + rp1;
+        rp += __shfl_xor_sync(0xffffffffu, rp, 16);  // both halves of the row
+#pragma unroll
+        for (int off = 8, n = 32; off >= 1; off >>= 1, n >>= 1) {
+          const bool hiL = (lane & off) != 0;
+#pragma unroll
+          for (int k2 = 0; k2 < n / 2; ++k2) {
+            const float mine = hiL ? m[n / 2 + k2] : m[k2];
+            const float send = hiL ? m[k2] : m[n / 2 + k2];
+            m[k2] = mine + __shfl_xor_sync(0xffffffffu, send, off);
+          }
+        }
+        const int u0 = 32 * up + 2 * (lane & 15);
+        R[warp * C + u0] = m[0];
+        R[warp * C + u0 + 1] = m[1];
+        if (rowok && up == 0) R[4 * C + r] = rp;
+      }
+      named_sync(bid, NTH);
+      if (warp == 0) {  // suffix sums of rowpre - colsuf; lane l owns t = 2l, 2l + 1
+        float dd[2];
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          const int t = 2 * lane + j;
+          dd[j] = t < len ? R[4 * C + t] - (R[t] + R[C + t] + R[2 * C + t] + R[3 * C + t]) : 0.f;
+        }
+        float x = dd[0] + dd[1];  // inclusive suffix over lanes of the pair sums
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const float y = __shfl_down_sync(0xffffffffu, x, o);
+          if (lane + o < 32) x += y;
+        }
+        const float b1 = x - dd[0];  // B_{2l+1} = suffix from 2l+1
+        const float b0 = x;          // B_{2l}
+        const int64_t bt = (b * p.L + t0) * p.H + h, n_bt = p.B * p.L * p.H;
+        if (2 * lane < len) STC(Bt, bt + (int64_t)(2 * lane) * p.H, n_bt, b0);
+        if (2 * lane + 1 < len) STC(Bt, bt + (int64_t)(2 * lane + 1) * p.H, n_bt, b1);
+      }
+      named_sync(bid, NTH);  // R and cs are reused by the next head
     }
-    __syncthreads();  // R and cs are reused by the next head
+    // the MMA waits above may have given up on some threads only: the
+    // worker leaves (or goes on) as a whole
+    if (named_sync_or(bid, NTH, !ok)) ok = false;
   }
   if (tid == 0) {
-    if (mma_ph >= 0) mbar_wait(&bar_mma, mma_ph & 1);
-    if (tma_ph >= 0) mbar_wait(&bar_tma, tma_ph & 1);
+    if (mma_out) mbar_wait(bar_mma, mma_par);
+    if (tma_out) mbar_wait(bar_tma, tma_par);
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 0) tmem_dealloc(tmem, 128);
+  if (threadIdx.x < 32) tmem_dealloc(tmem_base, 512);
 }
 
 // ===========================================================================
@@ -1372,9 +1406,16 @@ size_t walk_smem(const PassGeo &p) {
   return std::max<size_t>(need, 120 * 1024);
 }
 
-size_t dla_intra_smem(const PassGeo &p) {
+// Shared memory of one k_dla_intra worker (two tiles, the partial sums and
+// the prefix of la; a multiple of 1024 B for the 128-byte swizzle), and of a
+// CTA: at least 112 KB, so that no walk (at least 120 KB) or contraction CTA
+// ever shares an SM with it (they need all of an SM's tensor memory).
+uint32_t dla_intra_worker_bytes(const PassGeo &p) {
   const int ncbm = std::max(p.dkp, p.dvp) / 32;
-  return (size_t)ncbm * 2 * 8192 + (size_t)(6 * C) * 4 + 1024;  // three CTAs per SM fit
+  return (uint32_t)rup(ncbm * 2 * 8192 + 6 * C * 4, 1024);
+}
+size_t dla_intra_smem(const PassGeo &p) {
+  return std::max<size_t>((size_t)DI_WG * dla_intra_worker_bytes(p) + 1024, 112 * 1024);
 }
 
 // Launch helper (grid, block, dynamic shared memory, stream, kernel arguments).
@@ -1622,11 +1663,21 @@ cudaError_t bwd(const float *q, const float *k, const float *v, const float *la,
     if (ei == cudaSuccess) ei = make_map(&mv, v, rows, g.H, DV, C, false);
     if (ei == cudaSuccess) ei = make_map(&md, dout, rows, g.H, DV, C, false);
     const size_t sm = dla_intra_smem(pi);
+    // Beside the walks (overlap on), the kernel takes the SMs that the walks
+    // (one CTA per SM) leave idle, if its work fits in the time of the
+    // backward's three walks there: about one (chunk, head) phase per worker
+    // per walk chunk.  Otherwise it takes the whole GPU.
+    const int64_t sms = num_sms(), items = g.N * g.G * g.B;
+    const int64_t spare = sms - g.B * g.H * pa.nseg;
+    const int64_t per_worker = cdiv(items * (g.hpg + 1), std::max<int64_t>(1, spare) * DI_WG);
+    const int64_t grid = (overlap && spare >= 8 && per_worker <= 3 * cdiv(pa.Ls, C))
+                             ? spare
+                             : std::min<int64_t>(sms, cdiv(items, DI_WG));
     if (ei == cudaSuccess) ei = set_smem(k_dla_intra, sm);
     if (ei == cudaSuccess) {
       LaunchTrace lt("tc.dla_intra", s3);
-      ei = launch(k_dla_intra, dim3((unsigned)g.N, (unsigned)g.G, (unsigned)g.B), dim3(NTH), sm, s3, mq, mk, mv, md,
-                  la, Bt, pi);
+      ei = launch(k_dla_intra, dim3((unsigned)grid), dim3(DI_WG * NTH), sm, s3, mq, mk, mv, md, la, Bt, pi,
+                  (int64_t)g.N, (int64_t)g.G, dla_intra_worker_bytes(pi));
     }
   }
   const cudaError_t ej3 = overlap ? cudaEventRecord(sd->join3, s3) : cudaSuccess;
