@@ -105,7 +105,21 @@ struct PassGeo {
   int qk_per_head;     // q', k' indexed by head (1) or by group (0)
   int v_per_head;      // v' indexed by head (1) or by group (0)
   int Ls, nseg;        // segment length (multiple of C) and segments per sequence
+  int wide_k, wide_v;  // the q'/k' (v') maps load all feature blocks of a row in one box
 };
+
+// The feature blocks [0, nblk) of a 64-row tile, 8 KB apart in shared memory
+// (the layout of one 32-feature box per block): one 4-D box when the map is
+// wide, else one 3-D box per block.  Fewer, larger boxes: the load unit's
+// issue rate, not DRAM, bounds the walks' tile loads.
+__device__ __forceinline__ void load_tile(uint8_t *dst, const CUtensorMap *map, uint64_t *bar, int nblk,
+                                          int slot, int row, int wide) {
+  if (wide) {
+    tma_load_4d(dst, map, bar, 0, row, 0, slot);
+  } else {
+    for (int cb = 0; cb < nblk; ++cb) tma_load_3d(dst + cb * 8192, map, bar, cb * 32, slot, row);
+  }
+}
 
 __device__ __forceinline__ int qk_slot(const PassGeo &p, int64_t h) {
   return (int)(p.qk_per_head ? h : h / p.hpg);
@@ -126,13 +140,13 @@ __device__ __forceinline__ int v_slot(const PassGeo &p, int64_t h) {
 //   D^T += T^T k'           (T^T from tensor memory, k' MN-major)
 // so that no thread pass touches the k' / v' tiles (thread reads of shared
 // memory are slow while the tensor cores stream from it).  Warp 0 issues the
-// TMA loads (three-stage ring, L2 prefetches after it), warp 1 the MMAs,
+// TMA loads (three-stage ring; no L2 prefetches: the load unit issues their
+// boxes at the rate of loads, and the ring alone was faster), warp 1 the MMAs,
 // warps 2-5 compute the weights into W (double-buffered; only its diagonal is
-// rewritten) and finally write D out.  Tensor memory: D^T [0,128) (lane = v'
+// rewritten) and finally stage D in shared memory for one bulk store.  Tensor memory: D^T [0,128) (lane = v'
 // feature, column = k' feature), T^T [128,256) (two buffers).
 constexpr int SL = 64;          // slice length
 constexpr int SS_STAGES = 3;    // slices in flight
-constexpr int SS_PREFETCH = 2;  // slices past the ring, prefetched into L2
 constexpr int SS_THREADS = 192;
 template <bool REV>
 __global__ void __launch_bounds__(SS_THREADS, 1) k_seg_state(const __grid_constant__ CUtensorMap tmK,
@@ -203,15 +217,9 @@ __global__ void __launch_bounds__(SS_THREADS, 1) k_seg_state(const __grid_consta
         if (use > 0 && !mbar_wait(&empty[st], (use - 1) & 1, ab)) break;
         const int row = (int)(b * p.L + s_begin + (int64_t)n * SL);
         mbar_expect_tx(&full[st], kbytes + (uint32_t)ncbv * BLK);
-        for (int cb = 0; cb < ncbk; ++cb) tma_load_3d(Kt(st) + cb * BLK, &tmK, &full[st], cb * 32, kslot, row);
-        for (int cb = 0; cb < ncbv; ++cb) tma_load_3d(Vt(st) + cb * BLK, &tmV, &full[st], cb * 32, vslot, row);
+        load_tile(Kt(st), &tmK, &full[st], ncbk, kslot, row, p.wide_k);
+        load_tile(Vt(st), &tmV, &full[st], ncbv, vslot, row, p.wide_v);
         last[st] = n;
-        for (int pf = (n == 0 ? SS_STAGES : SS_STAGES + SS_PREFETCH - 1); pf < SS_STAGES + SS_PREFETCH; ++pf) {
-          if (n + pf >= nsl) break;
-          const int prow = (int)(b * p.L + s_begin + (int64_t)(n + pf) * SL);
-          for (int cb = 0; cb < ncbk; ++cb) tma_prefetch_3d(&tmK, cb * 32, kslot, prow);
-          for (int cb = 0; cb < ncbv; ++cb) tma_prefetch_3d(&tmV, cb * 32, vslot, prow);
-        }
       }
       // loads still in flight must land before the CTA exits
       for (int st = 0; st < SS_STAGES; ++st)
@@ -253,32 +261,43 @@ __global__ void __launch_bounds__(SS_THREADS, 1) k_seg_state(const __grid_consta
     }
   } else {  // warps 2-5: weights into W, then the result
     const int wt = tid - 64, wq = warp & 3;
-    double part = 0.0;
-#pragma unroll 8
-    for (int64_t t = s_begin + wt; t < s_end; t += 128) part += (double)LDC(la, (b * p.L + t) * p.H + h, n_la);
-#pragma unroll
-    for (int o = 16; o >= 1; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
-    if (lane == 0) wred[warp - 2] = part;
-    named_sync(1, 128);
-    const double tot = wred[0] + wred[1] + wred[2] + wred[3];
-    if (wt == 0) STC(Aseg, bh * p.nseg + seg, n_seg, (float)tot);
-    bool ok = true;
-    if (warp == 2) {  // one warp writes the diagonal: lane l owns tokens 2l, 2l + 1
-      static_assert(SL == 64, "two tokens per lane");
-      double carry = 0.0;
-      auto la_of = [&](int n, int u) {
-        const int64_t t = s_begin + (int64_t)n * SL + u;
-        return (n < nsl && t < s_end) ? (double)LDC(la, (b * p.L + t) * p.H + h, n_la) : 0.0;
-      };
-      // la of the next WLA slices is in flight while the current WLA slices'
-      // weights are made: an L2 round trip takes longer than a slice's MMAs
-      constexpr int WLA = 4;
-      double xc0[WLA], xc1[WLA], xn0[WLA], xn1[WLA];
+    static_assert(SL == 64, "two tokens per lane");
+    // (warp 2, lane l: tokens 2l and 2l + 1 of slice n)
+    auto la_of = [&](int n, int u) {
+      const int64_t t = s_begin + (int64_t)n * SL + u;
+      return (n < nsl && t < s_end) ? (double)LDC(la, (b * p.L + t) * p.H + h, n_la) : 0.0;
+    };
+    // la of the next WLA slices is in flight while the current WLA slices'
+    // weights are made: an L2 round trip takes longer than a slice's MMAs.
+    // The first ones are requested before the segment sum below.
+    constexpr int WLA = 4;
+    double xc0[WLA], xc1[WLA];
+    if (warp == 2) {
 #pragma unroll
       for (int u = 0; u < WLA; ++u) {
         xc0[u] = la_of(u, 2 * lane);
         xc1[u] = la_of(u, 2 * lane + 1);
       }
+    }
+    // The causal weights exp(A_seg - cs_u) need the segment's total first
+    // (all four warps, one batch of loads per thread); the anti-causal ones
+    // do not, and their total is the weights warp's running sum at the end.
+    double tot = 0.0;
+    if (!REV) {
+      double part = 0.0;
+#pragma unroll 16
+      for (int64_t t = s_begin + wt; t < s_end; t += 128) part += (double)LDC(la, (b * p.L + t) * p.H + h, n_la);
+#pragma unroll
+      for (int o = 16; o >= 1; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+      if (lane == 0) wred[warp - 2] = part;
+      named_sync(1, 128);
+      tot = wred[0] + wred[1] + wred[2] + wred[3];
+      if (wt == 0) STC(Aseg, bh * p.nseg + seg, n_seg, (float)tot);
+    }
+    bool ok = true;
+    if (warp == 2) {  // one warp writes the diagonal: lane l owns tokens 2l, 2l + 1
+      double carry = 0.0;
+      double xn0[WLA], xn1[WLA];
       for (int n0 = 0; ok && n0 < nsl; n0 += WLA) {
 #pragma unroll
         for (int u = 0; u < WLA; ++u) {
@@ -316,20 +335,35 @@ __global__ void __launch_bounds__(SS_THREADS, 1) k_seg_state(const __grid_consta
           xc1[u] = xn1[u];
         }
       }
+      if (REV && ok && lane == 0) STC(Aseg, bh * p.nseg + seg, n_seg, (float)carry);
     }
-    if (ok && mbar_wait_all(&done, 0, ab)) {  // (ok is uniform over each warp)
+    // warps 2-5 take the decision together (a barrier that ORs their
+    // failures), since the store below meets at a named barrier: a give-up of
+    // the weights warp, or a wait that ran out, leaves all four out of it
+    const bool fin = ok && mbar_wait_all(&done, 0, ab);  // (ok is uniform over each warp)
+    if (!named_sync_or(1, 128, !fin)) {
       tc_fence_after();
-      // D^T in tensor memory: lane j (v' feature), column i (k' feature)
+      // D^T in tensor memory (lane j = v' feature, column i = k' feature) ->
+      // the state [dk' x dv'] in the free stage-0 buffer (every slice's MMAs
+      // have completed), then one bulk copy to global memory
       const int j = 32 * wq + lane;
       const int64_t sz = (int64_t)p.dk * p.dv, dst = (bh * p.nseg + seg) * sz;
+      float *Dst = reinterpret_cast<float *>(Kt(0));  // sz <= dkp * 128 floats fit a stage
       for (int c0 = 0; c0 < p.dkp; c0 += 32) {
         float v[32];
         tmem_ld32(T_D + ((uint32_t)(32 * wq) << 16) + c0, v);
         if (j < p.dv) {
 #pragma unroll
           for (int ii = 0; ii < 32; ++ii)
-            if (c0 + ii < p.dk) STC(states, dst + (int64_t)(c0 + ii) * p.dv + j, n_seg * sz, v[ii]);
+            if (c0 + ii < p.dk) STC(Dst, (int64_t)(c0 + ii) * p.dv + j, sz, v[ii]);
         }
+      }
+      fence_async_smem();
+      named_sync(1, 128);
+      if (wt == 0) {  // (dst and sz are multiples of 64 floats: 16-byte aligned)
+        bulk_store(states + dst, Dst, (uint32_t)(sz * 4));
+        bulk_commit_group();
+        bulk_wait_all();
       }
     }
   }
@@ -441,7 +475,6 @@ __global__ void __launch_bounds__(NTH) k_seg_scan(float *__restrict__ st,
 // The entering state is read from Hseg as [dk' x dv'] (or [dv' x dk'] when
 // hseg_t).
 constexpr int WT = 384;
-constexpr int kPrefetch = 3;  // chunks ahead of the one being loaded, prefetched into L2
 struct Fac {     // decay factors of one chunk, walk order
   float cs2[C];  // in-chunk inclusive prefix of la, times log2(e) (0 past the end)
   float qf[C];   // inter-term factor of query row t times the state scale
@@ -546,25 +579,14 @@ __global__ void __launch_bounds__(WT, 1) k_walk(const __grid_constant__ CUtensor
         if (ci >= 2 && !mbar_wait(&empty[st], ((ci >> 1) - 1) & 1, ab)) break;
         const int row = (int)(b * p.L + s_begin + (int64_t)chunk_of(ci) * C);
         mbar_expect_tx(&full[st], 2 * qkbytes + (uint32_t)ncbv * BLK);
-        for (int cb = 0; cb < ncbk; ++cb) {
-          tma_load_3d(Qs(st) + cb * BLK, &tmQ, &full[st], cb * 32, kslot, row);
-          tma_load_3d(Ks(st) + cb * BLK, &tmK, &full[st], cb * 32, kslot, row);
-        }
-        for (int cb = 0; cb < ncbv; ++cb) tma_load_3d(Vs(st) + cb * BLK, &tmV, &full[st], cb * 32, vslot, row);
+        load_tile(Qs(st), &tmQ, &full[st], ncbk, kslot, row, p.wide_k);
+        load_tile(Ks(st), &tmK, &full[st], ncbk, kslot, row, p.wide_k);
+        load_tile(Vs(st), &tmV, &full[st], ncbv, vslot, row, p.wide_v);
         last[st] = ci;
-        // Only two stages fit in shared memory, so the tiles of chunk ci + 2
-        // are requested when chunk ci is done with its stage; prefetching the
-        // chunks after that into L2 keeps more bytes in flight than the smem
-        // ring holds and turns those loads into L2 hits.
-        for (int pf = (ci == 0 ? 1 : kPrefetch); pf <= kPrefetch; ++pf) {
-          if (ci + pf >= nc) break;
-          const int prow = (int)(b * p.L + s_begin + (int64_t)chunk_of(ci + pf) * C);
-          for (int cb = 0; cb < ncbk; ++cb) {
-            tma_prefetch_3d(&tmQ, cb * 32, kslot, prow);
-            tma_prefetch_3d(&tmK, cb * 32, kslot, prow);
-          }
-          for (int cb = 0; cb < ncbv; ++cb) tma_prefetch_3d(&tmV, cb * 32, vslot, prow);
-        }
+        // (No L2 prefetch of later chunks: the tensor-memory-access unit
+        // issues prefetch boxes at the same rate as loads, and the walks ran
+        // 15 % faster without them; a chunk's loads are requested one chunk
+        // ahead, which covers their latency.)
       }
       for (int st = 0; st < 2; ++st)  // loads in flight must land before the CTA exits
         if (last[st] >= 0) mbar_wait(&full[st], (last[st] >> 1) & 1);
@@ -1025,10 +1047,8 @@ __global__ void __launch_bounds__(DI_WG * NTH, 1) k_dla_intra(const __grid_const
     const int row = (int)(b * p.L + t0);
     if (tid == 0) {  // q -> T1, k -> T2
       mbar_expect_tx(bar_tma, (uint32_t)(2 * ncbk) * 8192);
-      for (int cb = 0; cb < ncbk; ++cb) {
-        tma_load_3d(T1 + cb * 8192, &tmQ, bar_tma, cb * 32, (int)grp, row);
-        tma_load_3d(T2 + cb * 8192, &tmK, bar_tma, cb * 32, (int)grp, row);
-      }
+      load_tile(T1, &tmQ, bar_tma, ncbk, (int)grp, row, p.wide_k);
+      load_tile(T2, &tmK, bar_tma, ncbk, (int)grp, row, p.wide_k);
       tma_out = true;
       tma_par = kt & 1;
     }
@@ -1086,10 +1106,8 @@ __global__ void __launch_bounds__(DI_WG * NTH, 1) k_dla_intra(const __grid_const
       if (tid == 0 && ok && ph < hpg) {  // the tiles are consumed: next head's loads
         const int64_t hn = grp * hpg + ph;
         mbar_expect_tx(bar_tma, (uint32_t)(2 * ncbv) * 8192);
-        for (int cb = 0; cb < ncbv; ++cb) {  // dout -> T1, v -> T2
-          tma_load_3d(T1 + cb * 8192, &tmD, bar_tma, cb * 32, (int)hn, row);
-          tma_load_3d(T2 + cb * 8192, &tmV, bar_tma, cb * 32, (int)hn, row);
-        }
+        load_tile(T1, &tmD, bar_tma, ncbv, (int)hn, row, p.wide_v);  // dout -> T1, v -> T2
+        load_tile(T2, &tmV, bar_tma, ncbv, (int)hn, row, p.wide_v);
         tma_out = true;
         tma_par = kt & 1;
       }
@@ -1342,16 +1360,33 @@ cudaError_t get_encoder() {
 // 1 slot x box_rows rows, zero fill out of bounds.  K-major operands use the
 // plain 128-byte swizzle, MN-major ones the 128-byte swizzle with 32-byte
 // atoms (sdesc / sdesc_mn).
+// A tensor [rows][slots][d] (fp32, row-major) as 64-row tiles of 32-feature
+// blocks.  Narrow: dims (d, slots, rows), box (32, 1, box_rows), one load per
+// block.  Wide (d a multiple of 32): dims (32, rows, d / 32, slots) with the
+// block as its own dimension (stride 128 B), box (32, box_rows, d / 32, 1):
+// one load brings every block, each landing where its own narrow box would.
 cudaError_t make_map(CUtensorMap *m, const float *base, int64_t rows, int64_t slots, int64_t d,
-                     int box_rows, bool mn_major) {
-  cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)slots, (cuuint64_t)rows};
-  cuuint64_t strides[2] = {(cuuint64_t)(d * 4), (cuuint64_t)(slots * d * 4)};
-  cuuint32_t box[3] = {32, 1, (cuuint32_t)box_rows};
-  cuuint32_t es[3] = {1, 1, 1};
-  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float *>(base), dims,
-                        strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                        mn_major ? CU_TENSOR_MAP_SWIZZLE_128B_ATOM_32B : CU_TENSOR_MAP_SWIZZLE_128B,
-                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                     int box_rows, bool mn_major, bool wide) {
+  const CUtensorMapSwizzle sw = mn_major ? CU_TENSOR_MAP_SWIZZLE_128B_ATOM_32B : CU_TENSOR_MAP_SWIZZLE_128B;
+  CUresult r;
+  if (wide) {
+    if (d % 32) return cudaErrorInvalidValue;
+    cuuint64_t dims[4] = {32, (cuuint64_t)rows, (cuuint64_t)(d / 32), (cuuint64_t)slots};
+    cuuint64_t strides[3] = {(cuuint64_t)(slots * d * 4), 128, (cuuint64_t)(d * 4)};
+    cuuint32_t box[4] = {32, (cuuint32_t)box_rows, (cuuint32_t)(d / 32), 1};
+    cuuint32_t es[4] = {1, 1, 1, 1};
+    r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, const_cast<float *>(base), dims, strides, box, es,
+                 CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  } else {
+    cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)slots, (cuuint64_t)rows};
+    cuuint64_t strides[2] = {(cuuint64_t)(d * 4), (cuuint64_t)(slots * d * 4)};
+    cuuint32_t box[3] = {32, 1, (cuuint32_t)box_rows};
+    cuuint32_t es[3] = {1, 1, 1};
+    r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float *>(base), dims, strides, box, es,
+                 CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  }
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
@@ -1388,6 +1423,8 @@ PassGeo make_pass(const Geo &g, int dk, int dv, bool qk_head, bool v_head) {
   p.qk_per_head = qk_head ? 1 : 0;
   p.v_per_head = v_head ? 1 : 0;
   choose_segments(g, &p.Ls, &p.nseg);
+  p.wide_k = dk % 32 == 0;
+  p.wide_v = dv % 32 == 0;
   return p;
 }
 
@@ -1449,8 +1486,8 @@ cudaError_t run_states(const PassGeo &p, const float *kp, const float *vp, const
   const int64_t rows = p.B * p.L;
   const int64_t G = p.H / p.hpg;
   CUtensorMap mk, mv;
-  if ((e = make_map(&mk, kp, rows, p.qk_per_head ? p.H : G, p.dk, SL, true)) != cudaSuccess) return e;
-  if ((e = make_map(&mv, vp, rows, p.v_per_head ? p.H : G, p.dv, SL, true)) != cudaSuccess) return e;
+  if ((e = make_map(&mk, kp, rows, p.qk_per_head ? p.H : G, p.dk, SL, true, p.wide_k)) != cudaSuccess) return e;
+  if ((e = make_map(&mv, vp, rows, p.v_per_head ? p.H : G, p.dv, SL, true, p.wide_v)) != cudaSuccess) return e;
   const dim3 grid((unsigned)p.nseg, (unsigned)p.H, (unsigned)p.B);
   {
     const size_t sm = seg_state_smem(p);
@@ -1492,9 +1529,9 @@ cudaError_t run_walk(const PassGeo &p, const float *qp, const float *kp, const f
   const int64_t rows = p.B * p.L;
   const int64_t G = p.H / p.hpg;
   CUtensorMap mq, mk, mv;
-  if ((e = make_map(&mq, qp, rows, p.qk_per_head ? p.H : G, p.dk, C, false)) != cudaSuccess) return e;
-  if ((e = make_map(&mk, kp, rows, p.qk_per_head ? p.H : G, p.dk, C, false)) != cudaSuccess) return e;
-  if ((e = make_map(&mv, vp, rows, p.v_per_head ? p.H : G, p.dv, C, true)) != cudaSuccess) return e;
+  if ((e = make_map(&mq, qp, rows, p.qk_per_head ? p.H : G, p.dk, C, false, p.wide_k)) != cudaSuccess) return e;
+  if ((e = make_map(&mk, kp, rows, p.qk_per_head ? p.H : G, p.dk, C, false, p.wide_k)) != cudaSuccess) return e;
+  if ((e = make_map(&mv, vp, rows, p.v_per_head ? p.H : G, p.dv, C, true, p.wide_v)) != cudaSuccess) return e;
   LaunchTrace lt(name_walk, s);
   const bool split = oa.dcs != nullptr;
   if (atomic) {
@@ -1658,10 +1695,10 @@ cudaError_t bwd(const float *q, const float *k, const float *v, const float *la,
     const PassGeo pi = make_pass(g, DK, DV, false, true);
     CUtensorMap mq, mk, mv, md;
     const int64_t rows = g.B * g.L;
-    if (ei == cudaSuccess) ei = make_map(&mq, q, rows, g.G, DK, C, false);
-    if (ei == cudaSuccess) ei = make_map(&mk, k, rows, g.G, DK, C, false);
-    if (ei == cudaSuccess) ei = make_map(&mv, v, rows, g.H, DV, C, false);
-    if (ei == cudaSuccess) ei = make_map(&md, dout, rows, g.H, DV, C, false);
+    if (ei == cudaSuccess) ei = make_map(&mq, q, rows, g.G, DK, C, false, pi.wide_k);
+    if (ei == cudaSuccess) ei = make_map(&mk, k, rows, g.G, DK, C, false, pi.wide_k);
+    if (ei == cudaSuccess) ei = make_map(&mv, v, rows, g.H, DV, C, false, pi.wide_v);
+    if (ei == cudaSuccess) ei = make_map(&md, dout, rows, g.H, DV, C, false, pi.wide_v);
     const size_t sm = dla_intra_smem(pi);
     // Beside the walks (overlap on), the kernel takes the SMs that the walks
     // (one CTA per SM) leave idle, if its work fits in the time of the

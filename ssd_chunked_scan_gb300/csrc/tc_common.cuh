@@ -128,6 +128,14 @@ __device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, u
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
       : "memory");
 }
+__device__ __forceinline__ void tma_load_4d(void *dst, const CUtensorMap *map, uint64_t *bar,
+                                            int x, int y, int z, int w) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(w), "r"(smem_u32(bar))
+      : "memory");
+}
 // Store / add-reduce one box from shared memory to global memory (bulk async
 // group of the issuing thread); the box layout in shared memory is the one a
 // load of the same map produces.
@@ -145,6 +153,14 @@ __device__ __forceinline__ void tma_reduce_add_3d(const CUtensorMap *map, const 
           reinterpret_cast<uint64_t>(map)),
       "r"(x), "r"(y), "r"(z), "r"(smem_u32(src))
       : "memory");
+}
+// Copy `bytes` (a multiple of 16) from shared to global memory (both 16-byte
+// aligned), in the issuing thread's bulk async group.
+__device__ __forceinline__ void bulk_store(void *gdst, const void *ssrc, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(
+                   reinterpret_cast<uint64_t>(gdst)),
+               "r"(smem_u32(ssrc)), "r"(bytes)
+               : "memory");
 }
 __device__ __forceinline__ void bulk_commit_group() {
   asm volatile("cp.async.bulk.commit_group;" ::: "memory");
