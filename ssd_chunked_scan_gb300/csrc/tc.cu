@@ -1216,8 +1216,9 @@ __global__ void __launch_bounds__(DI_WG * NTH, 1) k_dla_intra(const __grid_const
 // when Gfin is NULL.  grid (nseg, H, B).
 // The segment is taken in tiles of DT * DTPT tokens from its end; thread tid
 // owns DTPT consecutive tokens of a tile, and all of a tile's loads are issued
-// together (the first tile's before the carry's dot product), so a tile costs
-// one memory round trip; the suffix sums run in fp64.
+// together (the first tile's before the carry's dot product, whose loads are
+// all in flight at once too), so a tile costs one memory round trip; the
+// suffix sums run in fp64.
 constexpr int DT = 256;
 constexpr int DTPT = 8;
 __global__ void __launch_bounds__(DT) k_dla(const float *__restrict__ Bt,
@@ -1267,10 +1268,18 @@ __global__ void __launch_bounds__(DT) k_dla(const float *__restrict__ Bt,
     n4 = (int64_t)gridDim.z * H * sz / 4;
   }
   if (G) {
-#pragma unroll 4
-    for (int64_t e = tid; e < sz / 4; e += DT) {
-      const float4 g = LDC(G, g0 + e, n4), x = LDC(S, s0 + e, n4);
-      part = fmaf(g.x, x.x, fmaf(g.y, x.y, fmaf(g.z, x.z, fmaf(g.w, x.w, part))));
+    constexpr int U = 8;  // float4 pairs in flight per thread
+    for (int64_t e0 = tid; e0 < sz / 4; e0 += (int64_t)U * DT) {
+      float4 g[U], x[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int64_t e = e0 + (int64_t)u * DT;
+        g[u] = e < sz / 4 ? LDC(G, g0 + e, n4) : make_float4(0.f, 0.f, 0.f, 0.f);
+        x[u] = e < sz / 4 ? LDC(S, s0 + e, n4) : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u)
+        part = fmaf(g[u].x, x[u].x, fmaf(g[u].y, x[u].y, fmaf(g[u].z, x[u].z, fmaf(g[u].w, x[u].w, part))));
     }
   }
   double dp = part;
@@ -1660,10 +1669,6 @@ cudaError_t bwd(const float *q, const float *k, const float *v, const float *la,
     dqh = reinterpret_cast<float *>((a + 15) & ~uintptr_t(15));
     dkh = dqh + g.B * g.L * g.H * g.dk;
   }
-  if (atomic) {
-    if ((e = cudaMemsetAsync(dq, 0, sizeof(float) * g.B * g.L * g.G * g.dk, s)) != cudaSuccess) return e;
-    if ((e = cudaMemsetAsync(dk, 0, sizeof(float) * g.B * g.L * g.G * g.dk, s)) != cudaSuccess) return e;
-  }
   const int oslots = atomic ? (int)g.G : (int)g.H;
   // The dk / dv passes (pass B's states, both anti-causal walks) run on one
   // side stream and the intra-chunk dlog_alpha sums (inputs only) on another,
@@ -1718,7 +1723,11 @@ cudaError_t bwd(const float *q, const float *k, const float *v, const float *la,
     }
   }
   const cudaError_t ej3 = overlap ? cudaEventRecord(sd->join3, s3) : cudaSuccess;
-  cudaError_t eb = run_states<true>(pb, dout, q, la, dhT, true, dh0, stB, aB, nullptr, s2, "tc.seg_state_dk");
+  // (dq / dk are zeroed for the atomic group sums on the stream of the pass
+  // that adds into them, after the fork, so that the two fills overlap)
+  cudaError_t eb = atomic ? cudaMemsetAsync(dk, 0, sizeof(float) * g.B * g.L * g.G * g.dk, s2) : cudaSuccess;
+  if (eb == cudaSuccess)
+    eb = run_states<true>(pb, dout, q, la, dhT, true, dh0, stB, aB, nullptr, s2, "tc.seg_state_dk");
   WalkOut okk{dkh ? dkh : dk, oslots, k, rk};
   if (eb == cudaSuccess) eb = run_walk<true>(pb, v, dout, q, la, stB, false, okk, atomic, s2, "tc.walk_dk");
   WalkOut ov{dv, (int)g.H, nullptr, nullptr};
@@ -1740,7 +1749,8 @@ cudaError_t bwd(const float *q, const float *k, const float *v, const float *la,
   }
   // pass A on s, meanwhile
   auto on_s = [&]() -> cudaError_t {
-    cudaError_t ea = run_states<false>(pa, v, k, la, h0, true, hT, stA, aA, nullptr, s, "tc.seg_state_dq");
+    cudaError_t ea = atomic ? cudaMemsetAsync(dq, 0, sizeof(float) * g.B * g.L * g.G * g.dk, s) : cudaSuccess;
+    if (ea == cudaSuccess) ea = run_states<false>(pa, v, k, la, h0, true, hT, stA, aA, nullptr, s, "tc.seg_state_dq");
     if (ea != cudaSuccess) return ea;
     WalkOut oq{dqh ? dqh : dq, oslots, q, rq};
     return run_walk<false>(pa, dout, v, k, la, stA, false, oq, atomic, s, "tc.walk_dq");
