@@ -27,6 +27,11 @@ SMALL = [
     (2, 300, 2, 8, 128, 128, 64, -3.0, True),
     (1, 129, 1, 1, 128, 64, 64, 0.0, True),
     (3, 77, 3, 3, 8, 8, 64, 0.0, True),
+    # one feature count a multiple of 32 and the other not (the tensor-core
+    # path's tile loads take one box per tile for the first, one per 32-feature
+    # block for the second), and three 32-feature blocks
+    (1, 150, 1, 2, 128, 40, 64, 0.0, True),
+    (2, 90, 1, 2, 40, 96, 64, -3.0, True),
 ]
 SIMT_ONLY = [
     (2, 50, 1, 2, 5, 3, 16, 0.0, True),
