@@ -237,10 +237,13 @@ SSD_API int ssd_get_path(void);
  * first backward), forked from and joined back into the caller's stream
  * inside the call, so the call stays ordered on `stream` like any other; the
  * intra-chunk dlog_alpha sums run on a second stream of the library's, and
- * the causal dq pass on `stream`, meanwhile.  Off runs every kernel on `stream` in turn (the same results up
- * to the order of the float atomic adds that sum a group's heads; for
- * profiling one kernel at a time).  The SIMT and sequential paths are not
- * affected.  ssd_set_overlap returns the previous setting. */
+ * the causal dq pass on `stream`, meanwhile.  With overlap on, the
+ * intra-chunk sums take the SMs the one-CTA-per-SM passes leave idle (when
+ * their work fits in the passes' time there), so they run beside them.  Off
+ * runs every kernel on `stream` in turn (the same results up to the order of
+ * the float atomic adds that sum a group's heads; for profiling one kernel
+ * at a time).  The SIMT and sequential paths are not affected.
+ * ssd_set_overlap returns the previous setting. */
 SSD_API int ssd_set_overlap(int on);
 SSD_API int ssd_get_overlap(void);
 
