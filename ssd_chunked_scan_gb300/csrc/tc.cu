@@ -475,6 +475,11 @@ __global__ void __launch_bounds__(NTH) k_seg_scan(float *__restrict__ st,
 // The entering state is read from Hseg as [dk' x dv'] (or [dv' x dk'] when
 // hseg_t).
 constexpr int WT = 384;
+// The walks with per-token dots (SPLIT) add a second epilogue warpgroup
+// (warps 12-15): each group takes half of every chunk's tokens, since their
+// epilogue, not the state chain, paced those walks.  All roles still fit 128
+// registers a thread at 512 threads.
+__host__ __device__ constexpr int walk_threads(bool split) { return split ? 512 : WT; }
 struct Fac {     // decay factors of one chunk, walk order
   float cs2[C];  // in-chunk inclusive prefix of la, times log2(e) (0 past the end)
   float qf[C];   // inter-term factor of query row t times the state scale
@@ -490,7 +495,7 @@ struct WalkOut {
 };
 
 template <bool REV, bool ATOMIC, bool SPLIT>
-__global__ void __launch_bounds__(WT, 1) k_walk(const __grid_constant__ CUtensorMap tmQ,
+__global__ void __launch_bounds__(walk_threads(SPLIT), 1) k_walk(const __grid_constant__ CUtensorMap tmQ,
                                               const __grid_constant__ CUtensorMap tmK,
                                               const __grid_constant__ CUtensorMap tmV,
                                               const float *__restrict__ la,
@@ -530,6 +535,7 @@ __global__ void __launch_bounds__(WT, 1) k_walk(const __grid_constant__ CUtensor
   const int dk = p.dk, dv = p.dv;
   auto chunk_of = [&](int ci) { return REV ? nc - 1 - ci : ci; };
   const int64_t n_la = p.B * p.L * p.H;  // element counts (debug-build index checks)
+  constexpr int NEG = SPLIT ? 2 : 1;     // epilogue warpgroups
 
   if (warp == 1) tmem_alloc(&tmem_base, 512);
   if (tid == 0) {
@@ -539,7 +545,7 @@ __global__ void __launch_bounds__(WT, 1) k_walk(const __grid_constant__ CUtensor
       mbar_init(&s_full[i], 1);
       mbar_init(&s_empty[i], 128);
       mbar_init(&xy_full[i], 1);
-      mbar_init(&x_empty[i], 128);
+      mbar_init(&x_empty[i], 128 * NEG);
       mbar_init(&wk_full[i], 128);
     }
     mbar_init(&p_full, 128);
@@ -551,7 +557,7 @@ __global__ void __launch_bounds__(WT, 1) k_walk(const __grid_constant__ CUtensor
     mbar_init(&never, 1);
     for (int i = 0; i < 4; ++i) {
       mbar_init(&fac_full[i], 32);
-      mbar_init(&fac_empty[i], 257);
+      mbar_init(&fac_empty[i], 129 + 128 * NEG);
     }
     abort_flag = 0;
     fence_mbar_init();
@@ -810,10 +816,14 @@ __global__ void __launch_bounds__(WT, 1) k_walk(const __grid_constant__ CUtensor
     }
   } else {
     // ---- epilogue --------------------------------------------------------------
-    const int et = tid - 256, wq = warp & 3;
+    // group eg (one with NEG = 1) takes steps g_lo .. g_hi - 1 (16 tokens
+    // each) of every chunk; group 0 also loads the entering state and does
+    // the occasional rescale
+    const int et = (tid - 256) & 127, eg = (tid - 256) >> 7, wq = warp & 3;
+    const int g_lo = eg * (4 / NEG), g_hi = g_lo + 4 / NEG;
     const int j = 32 * wq + lane;  // v' feature of this lane
     const uint32_t lb = (uint32_t)(32 * wq) << 16;
-    {  // entering state into tensor memory: lane j, column i = state[i][j]
+    if (eg == 0) {  // entering state into tensor memory: lane j, column i = state[i][j]
       const int64_t sz = (int64_t)dk * dv, h0 = (bh * p.nseg + seg) * sz, n_h = p.B * p.H * p.nseg * sz;
       for (int c0 = 0; c0 < p.dkp; c0 += 32) {
         float hv[32];
@@ -859,8 +869,8 @@ __global__ void __launch_bounds__(WT, 1) k_walk(const __grid_constant__ CUtensor
         for (int i = 0; i < 16; ++i) dst[i] = (j < dv && 16 * g + i < leny) ? LDC(oa.y, y0 + (16 * g + i) * ldy, n_y) : 0.f;
       }
     };
-    load_y(yr0, 0, 0);
-    load_y(yr1, 0, 1);
+    load_y(yr0, 0, g_lo);
+    load_y(yr1, 0, g_lo + 1);
     const int stall_at = g_test_stall ? (nc > 1 ? 1 : 0) : -1;
     for (int ci = 0; ci < nc; ++ci) {
       const int slot = ci & 3, xb = ci & 1;
@@ -874,7 +884,7 @@ __global__ void __launch_bounds__(WT, 1) k_walk(const __grid_constant__ CUtensor
         bool ok = mbar_wait(&fac_full[slot], (ci >> 2) & 1, ab);
         if (ok && ci == stall_at) ok = mbar_wait(&never, 0, ab);
         if (ok) ok = mbar_wait(&xy_full[xb], (ci >> 1) & 1, ab);
-        if (named_sync_or(2, 128, !ok)) break;
+        if (named_sync_or(2 + eg, 128, !ok)) break;
         __syncwarp();
       } else {
         if (!mbar_wait_all(&fac_full[slot], (ci >> 2) & 1, ab)) break;
@@ -885,7 +895,7 @@ __global__ void __launch_bounds__(WT, 1) k_walk(const __grid_constant__ CUtensor
       }
       tc_fence_after();
       const Fac &F = fac[slot];
-      if (F.rescale) {  // Hs <- alpha exp(A_c) Hs before the update is issued
+      if (F.rescale && eg == 0) {  // Hs <- alpha exp(A_c) Hs before the update is issued
         const float an = F.an;
         for (int c0 = 0; c0 < p.dkp; c0 += 32) {
           float hv[32];
@@ -903,7 +913,7 @@ __global__ void __launch_bounds__(WT, 1) k_walk(const __grid_constant__ CUtensor
       auto step = [&](const int g) {  // tokens 16 g .. 16 g + 15
         float xa[16], ya[16];
         tmem_ld16x2(T_X + xb * 64 + 16 * g + lb, T_Y + xb * 64 + 16 * g + lb, xa, ya);
-        if (g == 3) {
+        if (g == g_hi - 1) {
           tc_fence_before();
           mbar_arrive(&x_empty[xb]);
         }
@@ -921,7 +931,9 @@ __global__ void __launch_bounds__(WT, 1) k_walk(const __grid_constant__ CUtensor
         if constexpr (SPLIT) {  // shift the ring and load two steps ahead
 #pragma unroll
           for (int i = 0; i < 16; ++i) yr0[i] = yr1[i];
-          load_y(yr1, g + 2 < 4 ? ci : ci + 1, (g + 2) & 3);
+          // (two steps ahead in this group's sequence of steps)
+          if (NEG == 2) load_y(yr1, ci + 1, g);
+          else load_y(yr1, g + 2 < 4 ? ci : ci + 1, (g + 2) & 3);
         }
         if (j < dv) {
           const int64_t o16 = o0 + (int64_t)(16 * g) * ld;
@@ -959,10 +971,13 @@ __global__ void __launch_bounds__(WT, 1) k_walk(const __grid_constant__ CUtensor
         }
       };
 #pragma unroll 1
-      for (int g = 0; g < 4; ++g) step(g);
+      for (int g = g_lo; g < g_hi; ++g) step(g);
       if constexpr (SPLIT) {
-        named_sync(2, 128);
-        if (et < len) STC(oa.dcs, (b * p.L + t0 + et) * p.H + h, n_la, red[et] + red[C + et] + red[2 * C + et] + red[3 * C + et]);
+        named_sync(2 + eg, 128);
+        // this group's tokens: 16 g_lo .. 16 g_hi - 1
+        const int tk = 16 * g_lo + et;
+        if (et < 16 * (g_hi - g_lo) && tk < len)
+          STC(oa.dcs, (b * p.L + t0 + tk) * p.H + h, n_la, red[tk] + red[C + tk] + red[2 * C + tk] + red[3 * C + tk]);
       }
       mbar_arrive(&fac_empty[slot]);
     }
@@ -1523,7 +1538,8 @@ cudaError_t launch_walk(const CUtensorMap &mq, const CUtensorMap &mk, const CUte
   const size_t sm = walk_smem(p);
   if ((e = set_smem(k_walk<REV, ATOMIC, SPLIT>, sm)) != cudaSuccess) return e;
   const dim3 grid((unsigned)p.nseg, (unsigned)p.H, (unsigned)p.B);
-  return launch(k_walk<REV, ATOMIC, SPLIT>, grid, dim3(WT), sm, s, mq, mk, mv, la, states, states_t ? 1 : 0, oa, p);
+  return launch(k_walk<REV, ATOMIC, SPLIT>, grid, dim3(walk_threads(SPLIT)), sm, s, mq, mk, mv, la, states,
+                states_t ? 1 : 0, oa, p);
 }
 
 // The walk of one pass over every segment, from the entering states.
