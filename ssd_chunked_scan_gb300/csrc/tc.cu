@@ -442,7 +442,7 @@ __global__ void __launch_bounds__(NTH) k_seg_scan(float *__restrict__ st,
 // ===========================================================================
 // Walk over the chunks of one segment (left to right, or right to left when
 // REV) with the running state resident in tensor memory.  grid (nseg, H, B),
-// one CTA per SM, 384 threads in warp-specialised roles:
+// one CTA per SM, 384 threads (512 when SPLIT) in warp-specialised roles:
 //   warp 0      TMA producer: q', k' (K-major) and v' (MN-major) tiles of each
 //               chunk into a two-stage ring
 //   warp 1      state-chain MMAs of chunk c:  X = S^T q'^T (inter term),
@@ -456,6 +456,8 @@ __global__ void __launch_bounds__(NTH) k_seg_scan(float *__restrict__ st,
 //   warps 8-11  epilogue: out'_t = f_t X_t + Y_t to global memory (atomic
 //               add over a group's heads when ATOMIC), dcs_t = y_t . f_t X_t
 //               when SPLIT, and the occasional explicit state rescale
+//   warps 12-15 (SPLIT) a second epilogue group: each group takes two of a
+//               chunk's four 16-token steps
 // so the next chunk's scores and mask overlap the current chunk's products.
 //
 // Tensor memory (512 columns): S^T [0,128) (lane j = v' feature, column i =
