@@ -64,18 +64,18 @@ def load_peaks():
 # file in the tree no longer hashes to that, the group's figures no longer
 # describe the kernels and the bench line reports traffic null, saying why.
 TRAFFIC_GROUPS = {
-    "tc.": {"source": "ssd_chunked_scan_gb300/csrc/tc.cu", "sha16": "756bf550ab13a704", "commit": "2f50d5b",
+    "tc.": {"source": "ssd_chunked_scan_gb300/csrc/tc.cu", "sha16": "5a668854d1e62e34", "commit": "02a28d2",
             "bytes": {
-                "tc.seg_state": 172397824,
-                "tc.seg_state_dq": 169821952,
-                "tc.seg_state_dk": 169003520,
-                "tc.seg_scan": (10531072 + 8445184 + 10536448) // 3,  # mean of the three passes' scans
-                "tc.walk_out": 303323392,
-                "tc.walk_dq": 403194880,
-                "tc.walk_dk": 402319360,
-                "tc.walk_dv": 304078848,
-                "tc.dla_intra": 337567488,
-                "tc.dla": 15752448,
+                "tc.seg_state": 172689664,
+                "tc.seg_state_dq": 169597184,
+                "tc.seg_state_dk": 169251584,
+                "tc.seg_scan": (10531072 + 8445952 + 10536448) // 3,  # mean of the three passes' scans
+                "tc.walk_out": 303384576,
+                "tc.walk_dq": 403106816,
+                "tc.walk_dk": 402502656,
+                "tc.walk_dv": 304101888,
+                "tc.dla_intra": 337807360,
+                "tc.dla": 15751424,
             }},
     "simt.": {"source": "ssd_chunked_scan_gb300/csrc/simt.cu", "sha16": "5682068978fc8373", "commit": "02155b1",
               "bytes": {}},
