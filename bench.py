@@ -173,7 +173,10 @@ def kernel_costs(w, sms=152):
     for n in ("tc.walk_dq", "tc.walk_dk"):
         c[n] = (3 * qk + 2 * vv + 2 * la + sst, fw + BL * H * dk * 2, "hbm")
     c["tc.dla_intra"] = (2 * qk + 2 * vv + 2 * la, BL * (G * C * dk + H * C * dv + H * C), "hbm")
-    c["tc.dla"] = (4 * la + 2 * sst, BL * H * 4 + 2 * B * H * nseg * dk * dv, "hbm")
+    # dla: the in-segment suffix sums (B_t, rq, rk in, dla out); dla_carry: the
+    # segment carries, a dot of the two passes' states per segment
+    c["tc.dla"] = (4 * la + B * H * nseg * 8, BL * H * 4, "hbm")
+    c["tc.dla_carry"] = (2 * sst + B * H * nseg * 8, 2 * B * H * nseg * dk * dv, "hbm")
     # deterministic group sums (opt-in): read every head's share, write the group's
     c["tc.group_sum"] = (BL * H * dk * f + qk, BL * H * dk, "hbm")
     # sequential kernels (chunk = 1): fp32 state updates and reductions, one

@@ -1231,43 +1231,24 @@ __global__ void __launch_bounds__(DI_WG * NTH, 1) k_dla_intra(const __grid_const
 // elements).  For the last segment G_end is the final state's cotangent and
 // S_end the final state: Gfin and Sfin, both [dk x dv] per head, or no term
 // when Gfin is NULL.  grid (nseg, H, B).
-// The segment is taken in tiles of DT * DTPT tokens from its end; thread tid
-// owns DTPT consecutive tokens of a tile, and all of a tile's loads are issued
-// together (the first tile's before the carry's dot product, whose loads are
-// all in flight at once too), so a tile costs one memory round trip; the
-// suffix sums run in fp64.
+// The carry comes from k_dla_carry.  The segment is taken in tiles of
+// DT * DTPT tokens from its end; thread tid owns DTPT consecutive tokens of a
+// tile, and all of a tile's loads are issued together, so a tile costs one
+// memory round trip; the suffix sums run in fp64.
 constexpr int DT = 256;
 constexpr int DTPT = 8;
-__global__ void __launch_bounds__(DT) k_dla(const float *__restrict__ Bt,
-                                            const float *__restrict__ rq,
-                                            const float *__restrict__ rk,
-                                            const float *__restrict__ Gst,
-                                            const float *__restrict__ Sst,
-                                            const float *__restrict__ Gfin,
-                                            const float *__restrict__ Sfin, float *__restrict__ dla,
-                                            int64_t L, int64_t H, int64_t sz, int Ls, int nseg) {
-  constexpr int TILE = DT * DTPT;
+// The segment carries <G_end, S_end> (defined above), one per (segment, head,
+// batch) into carry[(b H + h) nseg + seg]: float4 loads eight pairs per thread
+// at a time, fp32 partial sums, fp64 across threads.  They need only the two
+// passes' scanned states, so the backward computes them on a side stream
+// beside the walks.  grid (nseg, H, B).
+__global__ void __launch_bounds__(DT) k_dla_carry(const float *__restrict__ Gst, const float *__restrict__ Sst,
+                                                  const float *__restrict__ Gfin, const float *__restrict__ Sfin,
+                                                  double *__restrict__ carry, int64_t H, int64_t sz, int nseg) {
   __shared__ double wred[DT / 32];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int64_t seg = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int64_t bh = b * H + h;
-  const int64_t n_tok = (int64_t)gridDim.z * L * H;  // element counts (debug-build index checks)
-  const int64_t s_begin = seg * (int64_t)Ls;
-  const int64_t s_end = imin64(L, s_begin + Ls);
-  float xq[DTPT], xk[DTPT], xb[DTPT];
-  auto load_tile = [&](int64_t hi) {  // tokens hi - TILE + tid DTPT + u (those >= s_begin)
-    const int64_t t0 = hi - TILE + (int64_t)tid * DTPT;
-#pragma unroll
-    for (int u = 0; u < DTPT; ++u) {
-      const bool ok = t0 + u >= s_begin;
-      const int64_t idx = (b * L + t0 + u) * H + h;
-      xq[u] = ok ? LDC(rq, idx, n_tok) : 0.f;
-      xk[u] = ok ? LDC(rk, idx, n_tok) : 0.f;
-      xb[u] = ok ? LDC(Bt, idx, n_tok) : 0.f;
-    }
-  };
-  load_tile(s_end);
-  // carry = <G_end, S_end>: float4 loads, fp32 partial sums, fp64 across threads
   float part = 0.f;
   const float4 *G = nullptr, *S = nullptr;
   int64_t g0 = 0, s0 = 0;        // float4 offsets of G and S
@@ -1304,10 +1285,41 @@ __global__ void __launch_bounds__(DT) k_dla(const float *__restrict__ Bt,
   for (int o = 16; o >= 1; o >>= 1) dp += __shfl_xor_sync(0xffffffffu, dp, o);
   if (lane == 0) wred[warp] = dp;
   __syncthreads();
-  double carry = 0.0;
+  if (tid == 0) {
+    double c = 0.0;
 #pragma unroll
-  for (int w2 = 0; w2 < DT / 32; ++w2) carry += wred[w2];
-  __syncthreads();
+    for (int w2 = 0; w2 < DT / 32; ++w2) c += wred[w2];
+    STC(carry, bh * nseg + seg, (int64_t)gridDim.z * H * nseg, c);
+  }
+}
+
+__global__ void __launch_bounds__(DT) k_dla(const float *__restrict__ Bt,
+                                            const float *__restrict__ rq,
+                                            const float *__restrict__ rk,
+                                            const double *__restrict__ carry_in, float *__restrict__ dla,
+                                            int64_t L, int64_t H, int Ls, int nseg) {
+  constexpr int TILE = DT * DTPT;
+  __shared__ double wred[DT / 32];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int64_t seg = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const int64_t bh = b * H + h;
+  const int64_t n_tok = (int64_t)gridDim.z * L * H;  // element counts (debug-build index checks)
+  const int64_t s_begin = seg * (int64_t)Ls;
+  const int64_t s_end = imin64(L, s_begin + Ls);
+  float xq[DTPT], xk[DTPT], xb[DTPT];
+  auto load_tile = [&](int64_t hi) {  // tokens hi - TILE + tid DTPT + u (those >= s_begin)
+    const int64_t t0 = hi - TILE + (int64_t)tid * DTPT;
+#pragma unroll
+    for (int u = 0; u < DTPT; ++u) {
+      const bool ok = t0 + u >= s_begin;
+      const int64_t idx = (b * L + t0 + u) * H + h;
+      xq[u] = ok ? LDC(rq, idx, n_tok) : 0.f;
+      xk[u] = ok ? LDC(rk, idx, n_tok) : 0.f;
+      xb[u] = ok ? LDC(Bt, idx, n_tok) : 0.f;
+    }
+  };
+  load_tile(s_end);
+  double carry = LDC(carry_in, bh * nseg + seg, (int64_t)gridDim.z * H * nseg);
   for (int64_t hi = s_end; hi > s_begin; hi -= TILE) {
     if (hi != s_end) load_tile(hi);
     double suf[DTPT], tot = 0.0;  // suffix sums over this thread's tokens
@@ -1581,6 +1593,7 @@ cudaError_t run_walk(const PassGeo &p, const float *qp, const float *kp, const f
 struct Side {
   cudaStream_t s2 = nullptr, s3 = nullptr;
   cudaEvent_t fork = nullptr, join = nullptr, join3 = nullptr;
+  cudaEvent_t scanA = nullptr, scanB = nullptr, walkA = nullptr, walkB = nullptr;  // a pass's scan / dot walk done
 };
 std::mutex g_side_mu;
 Side g_side[64];
@@ -1599,6 +1612,10 @@ cudaError_t get_side(Side **out) {
     if ((e = cudaEventCreateWithFlags(&sd.fork, cudaEventDisableTiming)) != cudaSuccess) return e;
     if ((e = cudaEventCreateWithFlags(&sd.join, cudaEventDisableTiming)) != cudaSuccess) return e;
     if ((e = cudaEventCreateWithFlags(&sd.join3, cudaEventDisableTiming)) != cudaSuccess) return e;
+    if ((e = cudaEventCreateWithFlags(&sd.scanA, cudaEventDisableTiming)) != cudaSuccess) return e;
+    if ((e = cudaEventCreateWithFlags(&sd.scanB, cudaEventDisableTiming)) != cudaSuccess) return e;
+    if ((e = cudaEventCreateWithFlags(&sd.walkA, cudaEventDisableTiming)) != cudaSuccess) return e;
+    if ((e = cudaEventCreateWithFlags(&sd.walkB, cudaEventDisableTiming)) != cudaSuccess) return e;
   }
   *out = &sd;
   return cudaSuccess;
@@ -1629,8 +1646,9 @@ size_t bwd_workspace_bytes(const Geo &g, bool det) {
   const size_t nst = state_floats(p), na = (size_t)(g.B * g.H * p.nseg);
   // deterministic group sums: per-head dq_h and dk_h, [B, L, H, dk] each
   const size_t per_head = (det && g.hpg > 1) ? 2 * (size_t)(g.B * g.L * g.H * g.dk) + 4 : 0;
+  // + the segment carries (fp64), 16-byte aligned after the rest
   return sizeof(float) * (2 * nst + 2 * na + 3 * (size_t)(g.B * g.L * g.H) +
-                          (size_t)(g.B * g.H * g.dk * g.dv) + per_head) + 256;
+                          (size_t)(g.B * g.H * g.dk * g.dv) + per_head) + 256 + sizeof(double) * na + 16;
 }
 
 cudaError_t fwd(const float *q, const float *k, const float *v, const float *la, const float *h0,
@@ -1687,6 +1705,12 @@ cudaError_t bwd(const float *q, const float *k, const float *v, const float *la,
     dqh = reinterpret_cast<float *>((a + 15) & ~uintptr_t(15));
     dkh = dqh + g.B * g.L * g.H * g.dk;
   }
+  // the segment carries of dlog_alpha, fp64, after everything above
+  double *carry = nullptr;
+  {
+    const float *end = dkh ? dkh + g.B * g.L * g.H * g.dk : Bt + g.B * g.L * g.H + g.B * g.H * g.dk * g.dv + 4;
+    carry = reinterpret_cast<double *>((reinterpret_cast<uintptr_t>(end) + 15) & ~uintptr_t(15));
+  }
   const int oslots = atomic ? (int)g.G : (int)g.H;
   // The dk / dv passes (pass B's states, both anti-causal walks) run on one
   // side stream and the intra-chunk dlog_alpha sums (inputs only) on another,
@@ -1740,14 +1764,26 @@ cudaError_t bwd(const float *q, const float *k, const float *v, const float *la,
                   (int64_t)g.N, (int64_t)g.G, dla_intra_worker_bytes(pi));
     }
   }
-  const cudaError_t ej3 = overlap ? cudaEventRecord(sd->join3, s3) : cudaSuccess;
+  // s3 is joined through join3, recorded after its last kernel: the
+  // dlog_alpha sums once both dot walks are done, or right away if the call
+  // stops early (whatever is enqueued on s3 is joined back before this returns)
+  bool rec3 = false;
+  cudaError_t ej3 = cudaSuccess;
+  auto record3 = [&]() {
+    if (overlap && !rec3) {
+      ej3 = cudaEventRecord(sd->join3, s3);
+      rec3 = true;
+    }
+  };
   // (dq / dk are zeroed for the atomic group sums on the stream of the pass
   // that adds into them, after the fork, so that the two fills overlap)
   cudaError_t eb = atomic ? cudaMemsetAsync(dk, 0, sizeof(float) * g.B * g.L * g.G * g.dk, s2) : cudaSuccess;
   if (eb == cudaSuccess)
     eb = run_states<true>(pb, dout, q, la, dhT, true, dh0, stB, aB, nullptr, s2, "tc.seg_state_dk");
+  if (eb == cudaSuccess && overlap) eb = cudaEventRecord(sd->scanB, s2);
   WalkOut okk{dkh ? dkh : dk, oslots, k, rk};
   if (eb == cudaSuccess) eb = run_walk<true>(pb, v, dout, q, la, stB, false, okk, atomic, s2, "tc.walk_dk");
+  if (eb == cudaSuccess && overlap) eb = cudaEventRecord(sd->walkB, s2);
   WalkOut ov{dv, (int)g.H, nullptr, nullptr};
   if (eb == cudaSuccess) eb = run_walk<true>(pc, k, q, dout, la, stB, true, ov, false, s2, "tc.walk_dv");
   // whatever was enqueued on s2 is joined back into s before this returns,
@@ -1755,6 +1791,7 @@ cudaError_t bwd(const float *q, const float *k, const float *v, const float *la,
   cudaError_t ej = overlap ? cudaEventRecord(sd->join, s2) : cudaSuccess;
   auto join = [&]() -> cudaError_t {
     if (!overlap) return cudaSuccess;
+    record3();
     if (ej != cudaSuccess) return ej;
     if (ej3 != cudaSuccess) return ej3;
     cudaError_t e1 = cudaStreamWaitEvent(s, sd->join, 0);
@@ -1769,11 +1806,40 @@ cudaError_t bwd(const float *q, const float *k, const float *v, const float *la,
   auto on_s = [&]() -> cudaError_t {
     cudaError_t ea = atomic ? cudaMemsetAsync(dq, 0, sizeof(float) * g.B * g.L * g.G * g.dk, s) : cudaSuccess;
     if (ea == cudaSuccess) ea = run_states<false>(pa, v, k, la, h0, true, hT, stA, aA, nullptr, s, "tc.seg_state_dq");
+    if (ea == cudaSuccess && overlap) ea = cudaEventRecord(sd->scanA, s);
     if (ea != cudaSuccess) return ea;
     WalkOut oq{dqh ? dqh : dq, oslots, q, rq};
-    return run_walk<false>(pa, dout, v, k, la, stA, false, oq, atomic, s, "tc.walk_dq");
+    ea = run_walk<false>(pa, dout, v, k, la, stA, false, oq, atomic, s, "tc.walk_dq");
+    if (ea == cudaSuccess && overlap) ea = cudaEventRecord(sd->walkA, s);
+    return ea;
   };
-  const cudaError_t ea = on_s();
+  cudaError_t ea = on_s();
+  // dlog_alpha: the segment carries <G_end, S_end> (pass B's states against
+  // pass A's) once both scans are done, then the in-segment suffix sums once
+  // both dot walks have written rq / rk.  On s3 they run beside the walks (the
+  // suffix sums beside the dv walk, on the SMs k_dla_intra leaves), or on s in
+  // turn.
+  if (ea == cudaSuccess) {
+    cudaStream_t sc = overlap ? s3 : s;
+    if (overlap) {
+      ea = cudaStreamWaitEvent(s3, sd->scanA, 0);
+      if (ea == cudaSuccess) ea = cudaStreamWaitEvent(s3, sd->scanB, 0);
+    }
+    if (ea == cudaSuccess) {
+      LaunchTrace lt("tc.dla_carry", sc);
+      ea = launch(k_dla_carry, dim3((unsigned)pa.nseg, (unsigned)g.H, (unsigned)g.B), dim3(DT), 0, sc, stB, stA, dhT,
+                  hT, carry, g.H, (int64_t)(DK * DV), pa.nseg);
+    }
+    if (ea == cudaSuccess && overlap) {
+      ea = cudaStreamWaitEvent(s3, sd->walkA, 0);
+      if (ea == cudaSuccess) ea = cudaStreamWaitEvent(s3, sd->walkB, 0);
+    }
+    if (ea == cudaSuccess) {
+      LaunchTrace lt("tc.dla", sc);
+      ea = launch(k_dla, dim3((unsigned)pa.nseg, (unsigned)g.H, (unsigned)g.B), dim3(DT), 0, sc, Bt, rq, rk,
+                  (const double *)carry, dla, g.L, g.H, pa.Ls, pa.nseg);
+    }
+  }
   if ((e = join()) != cudaSuccess) return e;
   if (ea != cudaSuccess) return ea;
   if (dqh) {  // the group sums, heads in order
@@ -1785,12 +1851,6 @@ cudaError_t bwd(const float *q, const float *k, const float *v, const float *la,
                       (int)g.hpg, (int)(g.dk / 4))) != cudaSuccess)
         return e;
     }
-  }
-  {  // pass A's states are S^T, pass B's are G^T: the carry is their plain dot
-    LaunchTrace lt("tc.dla", s);
-    if ((e = launch(k_dla, dim3((unsigned)pa.nseg, (unsigned)g.H, (unsigned)g.B), dim3(DT), 0, s, Bt, rq, rk, stB, stA,
-                    dhT, hT, dla, g.L, g.H, (int64_t)(DK * DV), pa.Ls, pa.nseg)) != cudaSuccess)
-      return e;
   }
   return cudaGetLastError();
 }
