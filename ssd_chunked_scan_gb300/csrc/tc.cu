@@ -1234,7 +1234,23 @@ __global__ void __launch_bounds__(DI_WG * NTH, 1) k_dla_intra(const __grid_const
 // The carry comes from k_dla_carry.  The segment is taken in tiles of
 // DT * DTPT tokens from its end; thread tid owns DTPT consecutive tokens of a
 // tile, and all of a tile's loads are issued together, so a tile costs one
-// memory round trip; the suffix sums run in fp64.
+// memory round trip.  The suffix sums run in double-float arithmetic (an
+// unevaluated pair hi + lo of fp32 values, added by Knuth's two-sum): about
+// fp64's accuracy on the fp32 pipes, since this part's fp64 rate is low.
+struct FF {
+  float hi, lo;
+};
+__device__ __forceinline__ FF ff_two_sum(float a, float b) {  // a + b exactly, as hi + lo
+  const float s = __fadd_rn(a, b);
+  const float bb = __fsub_rn(s, a);
+  return {s, __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb))};
+}
+__device__ __forceinline__ FF ff_add(FF a, FF b) {
+  const FF t = ff_two_sum(a.hi, b.hi);
+  const float lo = __fadd_rn(t.lo, __fadd_rn(a.lo, b.lo));
+  return ff_two_sum(t.hi, lo);
+}
+__device__ __forceinline__ FF ff_neg(FF a) { return {-a.hi, -a.lo}; }
 constexpr int DT = 256;
 constexpr int DTPT = 8;
 // The segment carries <G_end, S_end> (defined above), one per (segment, head,
@@ -1299,7 +1315,7 @@ __global__ void __launch_bounds__(DT) k_dla(const float *__restrict__ Bt,
                                             const double *__restrict__ carry_in, float *__restrict__ dla,
                                             int64_t L, int64_t H, int Ls, int nseg) {
   constexpr int TILE = DT * DTPT;
-  __shared__ double wred[DT / 32];
+  __shared__ FF wred[DT / 32];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int64_t seg = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int64_t bh = b * H + h;
@@ -1319,34 +1335,41 @@ __global__ void __launch_bounds__(DT) k_dla(const float *__restrict__ Bt,
     }
   };
   load_tile(s_end);
-  double carry = LDC(carry_in, bh * nseg + seg, (int64_t)gridDim.z * H * nseg);
+  FF carry;
+  {
+    const double c = LDC(carry_in, bh * nseg + seg, (int64_t)gridDim.z * H * nseg);
+    carry.hi = (float)c;
+    carry.lo = (float)(c - (double)carry.hi);
+  }
   for (int64_t hi = s_end; hi > s_begin; hi -= TILE) {
     if (hi != s_end) load_tile(hi);
-    double suf[DTPT], tot = 0.0;  // suffix sums over this thread's tokens
+    FF suf[DTPT], tot = {0.f, 0.f};  // suffix sums over this thread's tokens
 #pragma unroll
     for (int u = DTPT - 1; u >= 0; --u) {
-      tot += (double)xq[u] - (double)xk[u];
+      tot = ff_add(tot, ff_two_sum(xq[u], -xk[u]));
       suf[u] = tot;
     }
-    double x = tot;  // inclusive suffix of the thread totals within the warp
+    FF x = tot;  // inclusive suffix of the thread totals within the warp
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-      const double y = __shfl_down_sync(0xffffffffu, x, o);
-      if (lane + o < 32) x += y;
+      const FF y = {__shfl_down_sync(0xffffffffu, x.hi, o), __shfl_down_sync(0xffffffffu, x.lo, o)};
+      if (lane + o < 32) x = ff_add(x, y);
     }
     if (lane == 0) wred[warp] = x;  // warp total
     __syncthreads();
-    double after = carry + (x - tot);  // everything right of this thread's tokens
+    FF after = ff_add(carry, ff_add(x, ff_neg(tot)));  // everything right of this thread's tokens
 #pragma unroll
     for (int w2 = 0; w2 < DT / 32; ++w2)
-      if (w2 > warp) after += wred[w2];
+      if (w2 > warp) after = ff_add(after, wred[w2]);
     const int64_t t0 = hi - TILE + (int64_t)tid * DTPT;
 #pragma unroll
     for (int u = 0; u < DTPT; ++u)
-      if (t0 + u >= s_begin)
-        STC(dla, (b * L + t0 + u) * H + h, n_tok, (float)((double)xb[u] + suf[u] + after));
+      if (t0 + u >= s_begin) {
+        const FF r = ff_add(ff_add(suf[u], after), FF{xb[u], 0.f});
+        STC(dla, (b * L + t0 + u) * H + h, n_tok, __fadd_rn(r.hi, r.lo));
+      }
 #pragma unroll
-    for (int w2 = 0; w2 < DT / 32; ++w2) carry += wred[w2];
+    for (int w2 = 0; w2 < DT / 32; ++w2) carry = ff_add(carry, wred[w2]);
     __syncthreads();
   }
 }
