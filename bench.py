@@ -1,8 +1,10 @@
 #!/usr/bin/env python
 """Throughput of the chunked SSD scan (fwd + bwd) on one or more GPUs.
 
-A step is one forward and one backward pass (ssd_fwd then ssd_bwd, the whole
-hot path) over the g2h8_d128 L=8192 long-memory workload: B=4, G=2, H=8,
+A step is one forward and one backward pass (ssd_fwd_save then ssd_bwd_saved:
+the whole hot path, the backward reading the forward's segment states as a
+training step keeps them; --recompute times ssd_fwd then ssd_bwd, which keeps
+nothing) over the g2h8_d128 L=8192 long-memory workload: B=4, G=2, H=8,
 L=8192, dk=dv=128, chunk 64, fp32 storage, seeded synthetic inputs.  The
 metric is tokens/s with tokens = B*L*H per step.  Prints ONE JSON line
 (rank 0).
@@ -463,13 +465,13 @@ def _rel(x, ref):
     return num / den if den > 0 else num
 
 
-def oracle_accuracy(w, out, grads, ref=None, nb=None):
+def oracle_accuracy(w, out, grads, ref=None, nb=None, residual_mb=0.0):
     """The accuracy fields of a bench record, as the benchmark pages keep them
     beside each timing: rel_err = max|x - ref| / max|ref| of the output and of
     each gradient against the float64 oracle, on a sample of the workload,
-    computed outside the timed region; residual_mb = 0 (nothing is kept
-    between the forward and the backward: the backward recomputes its
-    states).  out / grads: the GPU results for the whole workload (host numpy
+    computed outside the timed region; residual_mb: what is kept between the
+    forward and the backward besides the inputs (the segment states and the
+    final state, or 0 when the backward recomputes them).  out / grads: the GPU results for the whole workload (host numpy
     arrays; grads None for a forward alone).  ref: the oracle's (out, grads)
     on batch entries 0..nb-1, when the CPU baseline has computed them; else
     the oracle runs here on one (batch 0, group 0) unit."""
@@ -500,7 +502,7 @@ def oracle_accuracy(w, out, grads, ref=None, nb=None):
     acc = {"rel_err": _rel(sel(out, "v"), r_out),
            "rel_err_grads": None if grads is None else
            {a: _rel(sel(grads[g], kinds[g]), r_g[g]) for a, g in GRAD_KEYS.items()},
-           "residual_mb": 0.0,
+           "residual_mb": residual_mb,
            "accuracy_sample": sample + ", float64 oracle, max|x - ref| / max|ref| per tensor"}
     return acc
 
@@ -973,6 +975,9 @@ def main():
                     help="tensor-core backward with deterministic group sums (ssd_set_deterministic)")
     ap.add_argument("--no-accuracy", action="store_true",
                     help="skip the rel_err fields (the float64 oracle on a sample of the workload)")
+    ap.add_argument("--recompute", action="store_true",
+                    help="fwd_bwd step as ssd_fwd + ssd_bwd (the backward recomputes the "
+                         "forward's segment states) instead of ssd_fwd_save + ssd_bwd_saved")
     ap.add_argument("--mode", default="fwd_bwd", choices=["fwd_bwd", "fwd", "max_len"],
                     help="fwd times ssd_fwd alone (a step is then one forward pass); "
                          "max_len finds the largest sequence length fwd_bwd runs at")
@@ -1021,11 +1026,21 @@ def main():
     grads = {"dq": torch.empty_like(q), "dk": torch.empty_like(k), "dv": torch.empty_like(v),
              "dlog_alpha": torch.empty_like(la), "dh0": torch.empty_like(h0)}
     stream = torch.cuda.current_stream(dev)
+    # the forward's segment states (and final state) kept for the backward
+    save = args.mode == "fwd_bwd" and not args.recompute
+    n_saved = ssd.ssd_saved_bytes(w.B, w.L, w.G, w.H, w.dk, w.dv, w.chunk) // 4 if save else 0
+    saved = torch.empty((n_saved,), device=dev) if n_saved else None
+    hT = torch.empty_like(h0) if save else None
+    residual_mb = ((n_saved + hT.numel()) * 4 / MiB) if save else 0.0
 
     def step():
-        ssd.ssd_fwd(q, k, v, la, h0, chunk=w.chunk, out=out)
-        if args.mode == "fwd_bwd":
-            ssd.ssd_bwd(q, k, v, la, h0, dout, chunk=w.chunk, grads=grads)
+        if not save:
+            ssd.ssd_fwd(q, k, v, la, h0, chunk=w.chunk, out=out)
+            if args.mode == "fwd_bwd":
+                ssd.ssd_bwd(q, k, v, la, h0, dout, chunk=w.chunk, grads=grads)
+            return
+        ssd.ssd_fwd_save(q, k, v, la, h0, chunk=w.chunk, out=out, hT=hT, saved=saved)
+        ssd.ssd_bwd_saved(q, k, v, la, h0, dout, None, hT, saved, chunk=w.chunk, grads=grads)
 
     def barrier():
         if world > 1:
@@ -1122,7 +1137,8 @@ def main():
                                     lambda: ssd.ssd_fwd(q, k, v, la, h0, chunk=w.chunk, out=out),
                                     resident_bytes(*dims, "fwd")) / MiB,
         "peak_mb_fwd_bwd": measure_peak(ssd, torch, dev, step,
-                                        resident_bytes(*dims, args.mode)) / MiB,
+                                        resident_bytes(*dims, args.mode) + residual_mb * MiB) / MiB,
+        "residual_mb": residual_mb,
         "resident_mb_fwd_bwd": resident_bytes(*dims, "fwd_bwd") / MiB,
         "workspace_mb_fwd": ssd.ssd_fwd_workspace_bytes(*dims, w.chunk) / MiB,
         "workspace_mb_bwd": ssd.ssd_bwd_workspace_bytes(*dims, w.chunk) / MiB,
@@ -1144,6 +1160,9 @@ def main():
         ins = [[torch.empty_like(t) for t in (q, k, v, la, h0, dout)] for _ in range(2)]
         outs = [torch.empty_like(out) for _ in range(2)]
         gsets = [{n: torch.empty_like(t) for n, t in grads.items()} for _ in range(2)]
+        # (the residual never leaves the device: one set per buffer set)
+        res = [(torch.empty_like(saved) if saved is not None else None,
+                torch.empty_like(hT) if hT is not None else None) for _ in range(2)]
         s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
         ev = lambda: torch.cuda.Event()
         in_ready, in_free = [ev(), ev()], [ev(), ev()]      # inputs landed / consumed
@@ -1160,9 +1179,14 @@ def main():
                 in_ready[b].record(s_in)
             stream.wait_event(in_ready[b])
             stream.wait_event(res_free[b])
-            ssd.ssd_fwd(*ins[b][:5], chunk=w.chunk, out=outs[b])
-            if fb:
-                ssd.ssd_bwd(*ins[b], chunk=w.chunk, grads=gsets[b])
+            if save:
+                ssd.ssd_fwd_save(*ins[b][:5], chunk=w.chunk, out=outs[b], hT=res[b][1], saved=res[b][0])
+                ssd.ssd_bwd_saved(*ins[b][:5], ins[b][5], None, res[b][1], res[b][0], chunk=w.chunk,
+                                  grads=gsets[b])
+            else:
+                ssd.ssd_fwd(*ins[b][:5], chunk=w.chunk, out=outs[b])
+                if fb:
+                    ssd.ssd_bwd(*ins[b], chunk=w.chunk, grads=gsets[b])
             in_free[b].record(stream)
             res_ready[b].record(stream)
             with torch.cuda.stream(s_out):
@@ -1237,6 +1261,7 @@ def main():
                    "H": w.H, "L": w.L, "dk": w.dk, "dv": w.dv, "chunk": w.chunk,
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "deterministic_group_sums": bool(args.deterministic),
+                   "saved_states": bool(save),
                    "l2": l2_note(resident_bytes(w.B, w.L, w.G, w.H, w.dk, w.dv, args.mode))},
         "roofline": roof,
         "step_roofline": {"bound": "hbm" if t_hbm >= t_tc else "tensor",
@@ -1266,9 +1291,9 @@ def main():
     if want_acc:
         if ref is not None:
             acc = oracle_accuracy(w, res_out, res_grads, ref=(ref[0], ref[1] if res_grads else None),
-                                  nb=ref_nb)
+                                  nb=ref_nb, residual_mb=residual_mb)
         else:
-            acc = oracle_accuracy(w, res_out, res_grads)
+            acc = oracle_accuracy(w, res_out, res_grads, residual_mb=residual_mb)
         line.update(acc)
     print(json.dumps(line), flush=True)
     if world > 1:

@@ -168,6 +168,51 @@ SSD_API int ssd_bwd_ex(const float *q, const float *k, const float *v,
                        ssd_stream_t stream);
 
 /*
+ * Saved segment states, for a training step (forward, then backward on the
+ * same inputs).  On the tensor-core path the backward's dq pass needs the
+ * forward recurrence's state entering every segment of the sequence (the
+ * chunked scan's passed states at segment boundaries, about one segment per
+ * SM in all), which ssd_bwd / ssd_bwd_ex recompute from k, v, log_alpha and
+ * h0: a contraction over the whole sequence and a scan, the same work the
+ * forward did.  ssd_fwd_save keeps the forward's copy in a caller buffer and
+ * ssd_bwd_saved reads it there instead.
+ *
+ * ssd_saved_bytes: the size of that buffer for the active path and the
+ *   current device (it depends on the SM count, like the workspace):
+ *   B*H*nseg*dk*dv*4 bytes on the tensor-core path (8 MiB at B=4, H=8,
+ *   L=8192, dk=dv=128 on 152 SMs), 0 on the CUDA-core and sequential
+ *   evaluations, whose backward always recomputes.  Same checks and return
+ *   values as ssd_fwd_workspace_bytes.
+ * ssd_fwd_save: as ssd_fwd_ex, and also writes
+ *   saved  ssd_saved_bytes bytes, 16-byte aligned: the states entering every
+ *          segment, transposed ([B, H, nseg, dv, dk]); may be NULL when
+ *          ssd_saved_bytes gives 0 (then identical to ssd_fwd_ex).
+ * ssd_bwd_saved: as ssd_bwd_ex, reading
+ *   saved  as ssd_fwd_save wrote it for the same q, k, v, log_alpha, h0,
+ *          shapes and chunk, on the same path and device, or NULL (then
+ *          identical to ssd_bwd_ex); the library does not check that it
+ *          matches, and a stale buffer gives wrong gradients.
+ *   hT     [B,H,dk,dv] the final state that ssd_fwd_save wrote; required
+ *          (SSD_ERR_ARG otherwise) when both saved and dhT are given,
+ *          ignored otherwise.
+ * Results equal those of ssd_bwd_ex up to rounding (the states come from the
+ * forward's products instead of the backward's own).  saved is only read, and
+ * must be complete in the stream order of the ssd_bwd_saved call.
+ */
+SSD_API int ssd_saved_bytes(int64_t B, int64_t L, int64_t G, int64_t H, int64_t dk, int64_t dv,
+                            int64_t chunk, size_t *bytes);
+SSD_API int ssd_fwd_save(const float *q, const float *k, const float *v,
+                         const float *log_alpha, const float *h0, float *out, float *hT,
+                         float *saved, int64_t B, int64_t L, int64_t G, int64_t H, int64_t dk,
+                         int64_t dv, int64_t chunk, ssd_stream_t stream);
+SSD_API int ssd_bwd_saved(const float *q, const float *k, const float *v,
+                          const float *log_alpha, const float *h0, const float *dout,
+                          const float *dhT, const float *hT, const float *saved, float *dq,
+                          float *dk, float *dv, float *dlog_alpha, float *dh0, int64_t B,
+                          int64_t L, int64_t G, int64_t H, int64_t dk_dim, int64_t dv_dim,
+                          int64_t chunk, ssd_stream_t stream);
+
+/*
  * Allocation-free forward.  The benchmark pages have no counterpart: this
  * entry point exists for callers that cannot allocate device memory at call
  * time -- code whose memory is fully reserved up front by a framework's own

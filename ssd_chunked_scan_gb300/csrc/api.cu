@@ -78,6 +78,88 @@ int ws_alloc(void **p, size_t bytes, cudaStream_t s) {
   return SSD_OK;
 }
 
+// ssd_fwd_ex / ssd_fwd_save: saved (may be NULL) is written by the
+// tensor-core path only.
+int fwd_impl(const float *q, const float *k, const float *v, const float *log_alpha, const float *h0,
+             float *out, float *hT, float *saved, int64_t B, int64_t L, int64_t G, int64_t H,
+             int64_t dk, int64_t dv, int64_t chunk, ssd_stream_t stream) {
+  int rc = check_common(B, L, G, H, dk, dv, chunk);
+  if (rc) return rc;
+  const int path = current_path();
+  rc = check_path_shape(path, B, L, dk, dv, chunk);
+  if (rc) return rc;
+  if (misaligned(q) || misaligned(k) || misaligned(v) || misaligned(log_alpha) ||
+      misaligned(h0) || misaligned(out) || misaligned(hT) || misaligned(saved))
+    return SSD_ERR_ALIGN;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (B == 0 || L == 0) {  // the final state is the initial one
+    if (!hT || B == 0) return SSD_OK;
+    const size_t bytes = sizeof(float) * B * H * dk * dv;
+    return from_cuda(h0 ? cudaMemcpyAsync(hT, h0, bytes, cudaMemcpyDeviceToDevice, s)
+                        : cudaMemsetAsync(hT, 0, bytes, s));
+  }
+  if (!q || !k || !v || !log_alpha || !out) return SSD_ERR_ARG;
+  const ssd::Geo g = make_geo(B, L, G, H, dk, dv, chunk);
+  const Impl im = impl_of(path, chunk);
+  if (im == Impl::SEQ) return from_cuda(ssd::seq::fwd(q, k, v, log_alpha, h0, out, hT, g, s));
+  const size_t wsb = im == Impl::SIMT ? ssd::simt::fwd_workspace_bytes(g)
+                                      : ssd::tc::fwd_workspace_bytes(g);
+  void *ws = nullptr;
+  rc = ws_alloc(&ws, wsb, s);
+  if (rc) return rc;
+  cudaError_t e = im == Impl::SIMT ? ssd::simt::fwd(q, k, v, log_alpha, h0, out, hT, g, ws, s)
+                                   : ssd::tc::fwd(q, k, v, log_alpha, h0, out, hT, saved, g, ws, s);
+  if (ws) cudaFreeAsync(ws, s);
+  return from_cuda(e);
+}
+
+// ssd_bwd_ex / ssd_bwd_saved: saved (may be NULL) is read by the tensor-core
+// path only, with hT_saved the final state when dhT is given.
+int bwd_impl(const float *q, const float *k, const float *v, const float *log_alpha, const float *h0,
+             const float *dout, const float *dhT, const float *hT_saved, const float *saved, float *dq,
+             float *dk, float *dv, float *dlog_alpha, float *dh0, int64_t B, int64_t L, int64_t G,
+             int64_t H, int64_t dk_dim, int64_t dv_dim, int64_t chunk, ssd_stream_t stream) {
+  int rc = check_common(B, L, G, H, dk_dim, dv_dim, chunk);
+  if (rc) return rc;
+  const int path = current_path();
+  rc = check_path_shape(path, B, L, dk_dim, dv_dim, chunk);
+  if (rc) return rc;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (misaligned(q) || misaligned(k) || misaligned(v) || misaligned(log_alpha) ||
+      misaligned(h0) || misaligned(dout) || misaligned(dhT) || misaligned(dq) ||
+      misaligned(dk) || misaligned(dv) || misaligned(dlog_alpha) || misaligned(dh0) ||
+      misaligned(hT_saved) || misaligned(saved))
+    return SSD_ERR_ALIGN;
+  if (B == 0 || L == 0) {  // dh0 = dhT (or zero)
+    if (!dh0 || B == 0) return SSD_OK;
+    const size_t bytes = sizeof(float) * B * H * dk_dim * dv_dim;
+    return from_cuda(dhT ? cudaMemcpyAsync(dh0, dhT, bytes, cudaMemcpyDeviceToDevice, s)
+                         : cudaMemsetAsync(dh0, 0, bytes, s));
+  }
+  if (!q || !k || !v || !log_alpha || !dout || !dq || !dk || !dv || !dlog_alpha)
+    return SSD_ERR_ARG;
+  const ssd::Geo g = make_geo(B, L, G, H, dk_dim, dv_dim, chunk);
+  const Impl im = impl_of(path, chunk);
+  if (im == Impl::TC && saved && dhT && !hT_saved) return SSD_ERR_ARG;
+  const bool det = ssd::tc::get_deterministic();  // read once: sizes the workspace and steers the call
+  const size_t wsb = im == Impl::SEQ    ? ssd::seq::bwd_workspace_bytes(g)
+                     : im == Impl::SIMT ? ssd::simt::bwd_workspace_bytes(g)
+                                        : ssd::tc::bwd_workspace_bytes(g, det);
+  void *ws = nullptr;
+  rc = ws_alloc(&ws, wsb, s);
+  if (rc) return rc;
+  cudaError_t e;
+  if (im == Impl::SEQ)
+    e = ssd::seq::bwd(q, k, v, log_alpha, h0, dout, dhT, dq, dk, dv, dlog_alpha, dh0, g, ws, s);
+  else if (im == Impl::SIMT)
+    e = ssd::simt::bwd(q, k, v, log_alpha, h0, dout, dhT, dq, dk, dv, dlog_alpha, dh0, g, ws, s);
+  else
+    e = ssd::tc::bwd(q, k, v, log_alpha, h0, dout, dhT, dq, dk, dv, dlog_alpha, dh0, saved, hT_saved, g, det,
+                     ws, s);
+  if (ws) cudaFreeAsync(ws, s);
+  return from_cuda(e);
+}
+
 }  // namespace
 
 extern "C" {
@@ -120,34 +202,13 @@ int ssd_get_deterministic(void) { return ssd::tc::get_deterministic() ? 1 : 0; }
 int ssd_fwd_ex(const float *q, const float *k, const float *v, const float *log_alpha,
                const float *h0, float *out, float *hT, int64_t B, int64_t L, int64_t G, int64_t H,
                int64_t dk, int64_t dv, int64_t chunk, ssd_stream_t stream) {
-  int rc = check_common(B, L, G, H, dk, dv, chunk);
-  if (rc) return rc;
-  const int path = current_path();
-  rc = check_path_shape(path, B, L, dk, dv, chunk);
-  if (rc) return rc;
-  if (misaligned(q) || misaligned(k) || misaligned(v) || misaligned(log_alpha) ||
-      misaligned(h0) || misaligned(out) || misaligned(hT))
-    return SSD_ERR_ALIGN;
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (B == 0 || L == 0) {  // the final state is the initial one
-    if (!hT || B == 0) return SSD_OK;
-    const size_t bytes = sizeof(float) * B * H * dk * dv;
-    return from_cuda(h0 ? cudaMemcpyAsync(hT, h0, bytes, cudaMemcpyDeviceToDevice, s)
-                        : cudaMemsetAsync(hT, 0, bytes, s));
-  }
-  if (!q || !k || !v || !log_alpha || !out) return SSD_ERR_ARG;
-  const ssd::Geo g = make_geo(B, L, G, H, dk, dv, chunk);
-  const Impl im = impl_of(path, chunk);
-  if (im == Impl::SEQ) return from_cuda(ssd::seq::fwd(q, k, v, log_alpha, h0, out, hT, g, s));
-  const size_t wsb = im == Impl::SIMT ? ssd::simt::fwd_workspace_bytes(g)
-                                      : ssd::tc::fwd_workspace_bytes(g);
-  void *ws = nullptr;
-  rc = ws_alloc(&ws, wsb, s);
-  if (rc) return rc;
-  cudaError_t e = im == Impl::SIMT ? ssd::simt::fwd(q, k, v, log_alpha, h0, out, hT, g, ws, s)
-                                   : ssd::tc::fwd(q, k, v, log_alpha, h0, out, hT, g, ws, s);
-  if (ws) cudaFreeAsync(ws, s);
-  return from_cuda(e);
+  return fwd_impl(q, k, v, log_alpha, h0, out, hT, nullptr, B, L, G, H, dk, dv, chunk, stream);
+}
+
+int ssd_fwd_save(const float *q, const float *k, const float *v, const float *log_alpha,
+                 const float *h0, float *out, float *hT, float *saved, int64_t B, int64_t L, int64_t G,
+                 int64_t H, int64_t dk, int64_t dv, int64_t chunk, ssd_stream_t stream) {
+  return fwd_impl(q, k, v, log_alpha, h0, out, hT, saved, B, L, G, H, dk, dv, chunk, stream);
 }
 
 int ssd_fwd(const float *q, const float *k, const float *v, const float *log_alpha,
@@ -160,42 +221,17 @@ int ssd_bwd_ex(const float *q, const float *k, const float *v, const float *log_
                const float *h0, const float *dout, const float *dhT, float *dq, float *dk,
                float *dv, float *dlog_alpha, float *dh0, int64_t B, int64_t L, int64_t G,
                int64_t H, int64_t dk_dim, int64_t dv_dim, int64_t chunk, ssd_stream_t stream) {
-  int rc = check_common(B, L, G, H, dk_dim, dv_dim, chunk);
-  if (rc) return rc;
-  const int path = current_path();
-  rc = check_path_shape(path, B, L, dk_dim, dv_dim, chunk);
-  if (rc) return rc;
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (misaligned(q) || misaligned(k) || misaligned(v) || misaligned(log_alpha) ||
-      misaligned(h0) || misaligned(dout) || misaligned(dhT) || misaligned(dq) ||
-      misaligned(dk) || misaligned(dv) || misaligned(dlog_alpha) || misaligned(dh0))
-    return SSD_ERR_ALIGN;
-  if (B == 0 || L == 0) {  // dh0 = dhT (or zero)
-    if (!dh0 || B == 0) return SSD_OK;
-    const size_t bytes = sizeof(float) * B * H * dk_dim * dv_dim;
-    return from_cuda(dhT ? cudaMemcpyAsync(dh0, dhT, bytes, cudaMemcpyDeviceToDevice, s)
-                         : cudaMemsetAsync(dh0, 0, bytes, s));
-  }
-  if (!q || !k || !v || !log_alpha || !dout || !dq || !dk || !dv || !dlog_alpha)
-    return SSD_ERR_ARG;
-  const ssd::Geo g = make_geo(B, L, G, H, dk_dim, dv_dim, chunk);
-  const Impl im = impl_of(path, chunk);
-  const bool det = ssd::tc::get_deterministic();  // read once: sizes the workspace and steers the call
-  const size_t wsb = im == Impl::SEQ    ? ssd::seq::bwd_workspace_bytes(g)
-                     : im == Impl::SIMT ? ssd::simt::bwd_workspace_bytes(g)
-                                        : ssd::tc::bwd_workspace_bytes(g, det);
-  void *ws = nullptr;
-  rc = ws_alloc(&ws, wsb, s);
-  if (rc) return rc;
-  cudaError_t e;
-  if (im == Impl::SEQ)
-    e = ssd::seq::bwd(q, k, v, log_alpha, h0, dout, dhT, dq, dk, dv, dlog_alpha, dh0, g, ws, s);
-  else if (im == Impl::SIMT)
-    e = ssd::simt::bwd(q, k, v, log_alpha, h0, dout, dhT, dq, dk, dv, dlog_alpha, dh0, g, ws, s);
-  else
-    e = ssd::tc::bwd(q, k, v, log_alpha, h0, dout, dhT, dq, dk, dv, dlog_alpha, dh0, g, det, ws, s);
-  if (ws) cudaFreeAsync(ws, s);
-  return from_cuda(e);
+  return bwd_impl(q, k, v, log_alpha, h0, dout, dhT, nullptr, nullptr, dq, dk, dv, dlog_alpha, dh0, B, L, G, H,
+                  dk_dim, dv_dim, chunk, stream);
+}
+
+int ssd_bwd_saved(const float *q, const float *k, const float *v, const float *log_alpha,
+                  const float *h0, const float *dout, const float *dhT, const float *hT,
+                  const float *saved, float *dq, float *dk, float *dv, float *dlog_alpha, float *dh0,
+                  int64_t B, int64_t L, int64_t G, int64_t H, int64_t dk_dim, int64_t dv_dim,
+                  int64_t chunk, ssd_stream_t stream) {
+  return bwd_impl(q, k, v, log_alpha, h0, dout, dhT, hT, saved, dq, dk, dv, dlog_alpha, dh0, B, L, G, H, dk_dim,
+                  dv_dim, chunk, stream);
 }
 
 int ssd_bwd(const float *q, const float *k, const float *v, const float *log_alpha,
@@ -239,6 +275,20 @@ int ssd_bwd_workspace_bytes(int64_t B, int64_t L, int64_t G, int64_t H, int64_t 
   *bytes = im == Impl::SEQ    ? ssd::seq::bwd_workspace_bytes(g)
            : im == Impl::SIMT ? ssd::simt::bwd_workspace_bytes(g)
                               : ssd::tc::bwd_workspace_bytes(g, ssd::tc::get_deterministic());
+  return SSD_OK;
+}
+
+int ssd_saved_bytes(int64_t B, int64_t L, int64_t G, int64_t H, int64_t dk, int64_t dv, int64_t chunk,
+                    size_t *bytes) {
+  if (!bytes) return SSD_ERR_ARG;
+  *bytes = 0;
+  int rc = check_common(B, L, G, H, dk, dv, chunk);
+  if (rc) return rc;
+  const int path = current_path();
+  rc = check_path_shape(path, B, L, dk, dv, chunk);
+  if (rc) return rc;
+  if (B == 0 || L == 0 || impl_of(path, chunk) != Impl::TC) return SSD_OK;
+  *bytes = sizeof(float) * ssd::tc::saved_floats(make_geo(B, L, G, H, dk, dv, chunk));
   return SSD_OK;
 }
 

@@ -382,7 +382,11 @@ __global__ void __launch_bounds__(SS_THREADS, 1) k_seg_state(const __grid_consta
 //                entering the last is init, or 0; the state left of segment 0
 //                goes to fin
 // init is read, and fin (if given) written, transposed when TRANS.  When stT
-// is given, every result is also written there transposed.
+// is given, every result is also written there transposed; with tfast (the
+// block's 4*NTH elements are R = 4*NTH/dv whole rows, R a multiple of 4 that
+// divides dk) through a shared-memory tile, so that each thread stores four
+// consecutive elements of one transposed row as a float4, else element by
+// element.
 // grid (B*H, ceil(dk*dv / (4*128))), dk*dv a multiple of 4
 constexpr int SU = 10;
 template <bool REV, bool TRANS>
@@ -390,11 +394,12 @@ __global__ void __launch_bounds__(NTH) k_seg_scan(float *__restrict__ st,
                                                   const float *__restrict__ Aseg,
                                                   const float *__restrict__ init,
                                                   float *__restrict__ fin,
-                                                  float *__restrict__ stT, PassGeo p) {
+                                                  float *__restrict__ stT, PassGeo p, int tfast) {
+  __shared__ float4 tile[NTH];
   const int64_t bh = blockIdx.x;
   const int64_t e0 = 4 * ((int64_t)blockIdx.y * NTH + threadIdx.x);
   const int64_t sz = (int64_t)p.dk * p.dv;
-  if (e0 >= sz) return;
+  if (e0 >= sz) return;  // (never with tfast: the blocks cover sz exactly)
   auto tpos = [&](int64_t e) { return (e % p.dv) * p.dk + e / p.dv; };  // transposed position
   float4 *q = reinterpret_cast<float4 *>(st);
   const int64_t sz4 = sz / 4, qb = (bh * p.nseg * sz + e0) / 4;  // (sz and e0 multiples of 4)
@@ -422,7 +427,20 @@ __global__ void __launch_bounds__(NTH) k_seg_scan(float *__restrict__ st,
       if (k < p.nseg) {
         const int s = REV ? p.nseg - 1 - k : k;
         STC(q, qb + (int64_t)s * sz4, n_st / 4, make_float4(run[0], run[1], run[2], run[3]));
-        if (stT) {
+        if (stT && tfast) {
+          // column jj of the block's R rows (from row i0): R / 4 float4s
+          const int R = 4 * NTH / p.dv, nq = R / 4;
+          const int jj = (int)threadIdx.x / nq, r4 = (int)threadIdx.x % nq;
+          const int64_t i0 = (int64_t)blockIdx.y * R;
+          __syncthreads();  // the previous segment's tile is read
+          tile[threadIdx.x] = make_float4(run[0], run[1], run[2], run[3]);
+          __syncthreads();
+          const float *tf = reinterpret_cast<const float *>(tile);
+          const float4 t4 = make_float4(tf[(4 * r4) * p.dv + jj], tf[(4 * r4 + 1) * p.dv + jj],
+                                        tf[(4 * r4 + 2) * p.dv + jj], tf[(4 * r4 + 3) * p.dv + jj]);
+          STC(reinterpret_cast<float4 *>(stT), (bh * p.nseg * sz + (int64_t)s * sz + jj * p.dk + i0 + 4 * r4) / 4,
+              n_st / 4, t4);
+        } else if (stT) {
 #pragma unroll
           for (int j = 0; j < 4; ++j) STC(stT, bh * p.nseg * sz + (int64_t)s * sz + tpos(e0 + j), n_st, run[j]);
         }
@@ -1560,8 +1578,10 @@ cudaError_t run_states(const PassGeo &p, const float *kp, const float *vp, const
   {
     LaunchTrace lt("tc.seg_scan", s);
     const dim3 sg((unsigned)(p.B * p.H), (unsigned)cdiv((int64_t)p.dk * p.dv, 4 * NTH));
-    e = trans ? launch(k_seg_scan<REV, true>, sg, dim3(NTH), 0, s, states, Aseg, h0, fin, statesT, p)
-              : launch(k_seg_scan<REV, false>, sg, dim3(NTH), 0, s, states, Aseg, h0, fin, statesT, p);
+    const int R = (4 * NTH) % p.dv == 0 ? 4 * NTH / p.dv : 0;
+    const int tfast = (R > 0 && R % 4 == 0 && p.dk % R == 0) ? 1 : 0;
+    e = trans ? launch(k_seg_scan<REV, true>, sg, dim3(NTH), 0, s, states, Aseg, h0, fin, statesT, p, tfast)
+              : launch(k_seg_scan<REV, false>, sg, dim3(NTH), 0, s, states, Aseg, h0, fin, statesT, p, tfast);
     if (e != cudaSuccess) return e;
   }
   return cudaGetLastError();
@@ -1657,6 +1677,10 @@ int check_shape(int64_t dk, int64_t dv, int64_t chunk) {
   return SSD_OK;
 }
 
+// The dq pass's states (its layout: [dv x dk] per head and segment) are the
+// forward's own states transposed; the forward can leave them for the backward.
+size_t saved_floats(const Geo &g) { return state_floats(make_pass(g, (int)g.dv, (int)g.dk, true, false)); }
+
 size_t fwd_workspace_bytes(const Geo &g) {
   const PassGeo p = make_pass(g, (int)g.dk, (int)g.dv, false, true);
   return sizeof(float) * (state_floats(p) + (size_t)(g.B * g.H * p.nseg));
@@ -1675,14 +1699,16 @@ size_t bwd_workspace_bytes(const Geo &g, bool det) {
 }
 
 cudaError_t fwd(const float *q, const float *k, const float *v, const float *la, const float *h0,
-                float *out, float *hT, const Geo &g, void *ws, cudaStream_t s) {
+                float *out, float *hT, float *saved, const Geo &g, void *ws, cudaStream_t s) {
   cudaError_t e = get_encoder();
   if (e != cudaSuccess) return e;
   if (g.B * g.L >= (int64_t)1 << 31) return cudaErrorNotSupported;
   const PassGeo p = make_pass(g, (int)g.dk, (int)g.dv, false, true);
   float *st = static_cast<float *>(ws);
   float *Aseg = st + state_floats(p);
-  if ((e = run_states<false>(p, k, v, la, h0, false, hT, st, Aseg, nullptr, s, "tc.seg_state")) != cudaSuccess)
+  // (saved: the scan also writes every segment's entering state transposed,
+  // the dq pass's states)
+  if ((e = run_states<false>(p, k, v, la, h0, false, hT, st, Aseg, saved, s, "tc.seg_state")) != cudaSuccess)
     return e;
   WalkOut oa{out, (int)g.H, nullptr, nullptr};
   return run_walk<false>(p, q, k, v, la, st, false, oa, false, s, "tc.walk_out");
@@ -1690,7 +1716,8 @@ cudaError_t fwd(const float *q, const float *k, const float *v, const float *la,
 
 cudaError_t bwd(const float *q, const float *k, const float *v, const float *la, const float *h0,
                 const float *dout, const float *dhT, float *dq, float *dk, float *dv, float *dla,
-                float *dh0, const Geo &g, bool det, void *ws, cudaStream_t s) {
+                float *dh0, const float *saved, const float *hT_saved, const Geo &g, bool det, void *ws,
+                cudaStream_t s) {
   cudaError_t e = get_encoder();
   if (e != cudaSuccess) return e;
   if (g.B * g.L >= (int64_t)1 << 31) return cudaErrorNotSupported;
@@ -1734,6 +1761,11 @@ cudaError_t bwd(const float *q, const float *k, const float *v, const float *la,
     const float *end = dkh ? dkh + g.B * g.L * g.H * g.dk : Bt + g.B * g.L * g.H + g.B * g.H * g.dk * g.dv + 4;
     carry = reinterpret_cast<double *>((reinterpret_cast<uintptr_t>(end) + 15) & ~uintptr_t(15));
   }
+  // pass A's states and final state: recomputed below into the workspace, or
+  // the forward's (saved; then hT_saved is the final state whenever dhT is
+  // given)
+  const float *stA_r = saved ? saved : stA;
+  const float *hT_r = saved ? hT_saved : hT;
   const int oslots = atomic ? (int)g.G : (int)g.H;
   // The dk / dv passes (pass B's states, both anti-causal walks) run on one
   // side stream and the intra-chunk dlog_alpha sums (inputs only) on another,
@@ -1798,6 +1830,8 @@ cudaError_t bwd(const float *q, const float *k, const float *v, const float *la,
       rec3 = true;
     }
   };
+  // (where dlog_alpha's segment carries run: see below)
+  const bool carry_on_s2 = overlap && saved;
   // (dq / dk are zeroed for the atomic group sums on the stream of the pass
   // that adds into them, after the fork, so that the two fills overlap)
   cudaError_t eb = atomic ? cudaMemsetAsync(dk, 0, sizeof(float) * g.B * g.L * g.G * g.dk, s2) : cudaSuccess;
@@ -1806,9 +1840,20 @@ cudaError_t bwd(const float *q, const float *k, const float *v, const float *la,
   if (eb == cudaSuccess && overlap) eb = cudaEventRecord(sd->scanB, s2);
   WalkOut okk{dkh ? dkh : dk, oslots, k, rk};
   if (eb == cudaSuccess) eb = run_walk<true>(pb, v, dout, q, la, stB, false, okk, atomic, s2, "tc.walk_dk");
-  if (eb == cudaSuccess && overlap) eb = cudaEventRecord(sd->walkB, s2);
+  if (eb == cudaSuccess && overlap && !carry_on_s2) eb = cudaEventRecord(sd->walkB, s2);
   WalkOut ov{dv, (int)g.H, nullptr, nullptr};
   if (eb == cudaSuccess) eb = run_walk<true>(pc, k, q, dout, la, stB, true, ov, false, s2, "tc.walk_dv");
+  // dlog_alpha's segment carries <G_end, S_end> (pass B's states against pass
+  // A's).  With overlap on and the forward's states given, k_dla_intra on s3
+  // outlasts the 128-SM chain, so they run here, at the end of the chain
+  // (pass A's states exist from the start); otherwise on s3 beside the walks,
+  // or on s in turn (below).
+  if (eb == cudaSuccess && carry_on_s2) {
+    LaunchTrace lt("tc.dla_carry", s2);
+    eb = launch(k_dla_carry, dim3((unsigned)pa.nseg, (unsigned)g.H, (unsigned)g.B), dim3(DT), 0, s2, stB, stA_r,
+                dhT, hT_r, carry, g.H, (int64_t)(DK * DV), pa.nseg);
+  }
+  if (eb == cudaSuccess && carry_on_s2) eb = cudaEventRecord(sd->walkB, s2);
   // whatever was enqueued on s2 is joined back into s before this returns,
   // even after an error (the caller frees the workspace on s)
   cudaError_t ej = overlap ? cudaEventRecord(sd->join, s2) : cudaSuccess;
@@ -1828,38 +1873,38 @@ cudaError_t bwd(const float *q, const float *k, const float *v, const float *la,
   // pass A on s, meanwhile
   auto on_s = [&]() -> cudaError_t {
     cudaError_t ea = atomic ? cudaMemsetAsync(dq, 0, sizeof(float) * g.B * g.L * g.G * g.dk, s) : cudaSuccess;
-    if (ea == cudaSuccess) ea = run_states<false>(pa, v, k, la, h0, true, hT, stA, aA, nullptr, s, "tc.seg_state_dq");
+    if (ea == cudaSuccess && !saved)
+      ea = run_states<false>(pa, v, k, la, h0, true, hT, stA, aA, nullptr, s, "tc.seg_state_dq");
     if (ea == cudaSuccess && overlap) ea = cudaEventRecord(sd->scanA, s);
     if (ea != cudaSuccess) return ea;
     WalkOut oq{dqh ? dqh : dq, oslots, q, rq};
-    ea = run_walk<false>(pa, dout, v, k, la, stA, false, oq, atomic, s, "tc.walk_dq");
-    if (ea == cudaSuccess && overlap) ea = cudaEventRecord(sd->walkA, s);
-    return ea;
+    return run_walk<false>(pa, dout, v, k, la, stA_r, false, oq, atomic, s, "tc.walk_dq");
   };
   cudaError_t ea = on_s();
-  // dlog_alpha: the segment carries <G_end, S_end> (pass B's states against
-  // pass A's) once both scans are done, then the in-segment suffix sums once
-  // both dot walks have written rq / rk.  On s3 they run beside the walks (the
-  // suffix sums beside the dv walk, on the SMs k_dla_intra leaves), or on s in
-  // turn.
-  if (ea == cudaSuccess) {
-    cudaStream_t sc = overlap ? s3 : s;
+  // dlog_alpha: the segment carries once both scans are done (on s3 beside
+  // the walks, or on s in turn, unless they ran on s2 above), then the
+  // in-segment suffix sums once both dot walks have written rq / rk, on s3
+  // after k_dla_intra (beside the dv walk, on the SMs it leaves).
+  if (ea == cudaSuccess && !carry_on_s2) {
     if (overlap) {
       ea = cudaStreamWaitEvent(s3, sd->scanA, 0);
       if (ea == cudaSuccess) ea = cudaStreamWaitEvent(s3, sd->scanB, 0);
     }
     if (ea == cudaSuccess) {
-      LaunchTrace lt("tc.dla_carry", sc);
-      ea = launch(k_dla_carry, dim3((unsigned)pa.nseg, (unsigned)g.H, (unsigned)g.B), dim3(DT), 0, sc, stB, stA, dhT,
-                  hT, carry, g.H, (int64_t)(DK * DV), pa.nseg);
+      LaunchTrace lt("tc.dla_carry", s3);
+      ea = launch(k_dla_carry, dim3((unsigned)pa.nseg, (unsigned)g.H, (unsigned)g.B), dim3(DT), 0, s3, stB, stA_r,
+                  dhT, hT_r, carry, g.H, (int64_t)(DK * DV), pa.nseg);
     }
+  }
+  if (ea == cudaSuccess) {
+    if (overlap) ea = cudaEventRecord(sd->walkA, s);  // the dq walk done
     if (ea == cudaSuccess && overlap) {
       ea = cudaStreamWaitEvent(s3, sd->walkA, 0);
       if (ea == cudaSuccess) ea = cudaStreamWaitEvent(s3, sd->walkB, 0);
     }
     if (ea == cudaSuccess) {
-      LaunchTrace lt("tc.dla", sc);
-      ea = launch(k_dla, dim3((unsigned)pa.nseg, (unsigned)g.H, (unsigned)g.B), dim3(DT), 0, sc, Bt, rq, rk,
+      LaunchTrace lt("tc.dla", s3);
+      ea = launch(k_dla, dim3((unsigned)pa.nseg, (unsigned)g.H, (unsigned)g.B), dim3(DT), 0, s3, Bt, rq, rk,
                   (const double *)carry, dla, g.L, g.H, pa.Ls, pa.nseg);
     }
   }

@@ -13,12 +13,20 @@ size_t fwd_workspace_bytes(const Geo &g);
 // must be given to bwd.
 size_t bwd_workspace_bytes(const Geo &g, bool det);
 
+// Floats of the states the forward can leave for the backward (see fwd).
+size_t saved_floats(const Geo &g);
+
 // hT (final state, written) and dhT (its cotangent, read) may be NULL.
+// saved (saved_floats(g), may be NULL): fwd also writes there the states
+// entering each segment, transposed, which are the backward's dq-pass states;
+// bwd then reads them instead of recomputing them, and hT_saved is the final
+// state fwd wrote (needed when dhT is given).
 cudaError_t fwd(const float *q, const float *k, const float *v, const float *la, const float *h0,
-                float *out, float *hT, const Geo &g, void *ws, cudaStream_t s);
+                float *out, float *hT, float *saved, const Geo &g, void *ws, cudaStream_t s);
 cudaError_t bwd(const float *q, const float *k, const float *v, const float *la, const float *h0,
                 const float *dout, const float *dhT, float *dq, float *dk, float *dv, float *dla,
-                float *dh0, const Geo &g, bool det, void *ws, cudaStream_t s);
+                float *dh0, const float *saved, const float *hT_saved, const Geo &g, bool det, void *ws,
+                cudaStream_t s);
 
 // Whether bwd runs its dk / dv passes on a side stream (see ssd_set_overlap);
 // set_overlap returns the previous setting.

@@ -34,7 +34,7 @@ EXPORTED = ("ssd_fwd", "ssd_bwd", "ssd_set_path", "ssd_get_path", "ssd_set_overl
             "ssd_last_device_error", "ssd_version", "ssd_launch_count", "ssd_trace_enable",
             "ssd_trace_collect", "ssd_trace_get", "ssd_trace_reset", "ssd_fwd_noalloc",
             "ssd_fwd_noalloc_scratch_bytes", "ssd_test_stall_walks", "ssd_set_deterministic",
-            "ssd_get_deterministic")
+            "ssd_get_deterministic", "ssd_saved_bytes", "ssd_fwd_save", "ssd_bwd_saved")
 
 
 class SSDError(RuntimeError):
@@ -56,6 +56,12 @@ def _load():
     lib.ssd_fwd_ex.restype = ctypes.c_int
     lib.ssd_bwd_ex.argtypes = [p] * 12 + [i64] * 7 + [p]
     lib.ssd_bwd_ex.restype = ctypes.c_int
+    lib.ssd_fwd_save.argtypes = [p] * 8 + [i64] * 7 + [p]
+    lib.ssd_fwd_save.restype = ctypes.c_int
+    lib.ssd_bwd_saved.argtypes = [p] * 14 + [i64] * 7 + [p]
+    lib.ssd_bwd_saved.restype = ctypes.c_int
+    lib.ssd_saved_bytes.argtypes = [i64] * 7 + [ctypes.POINTER(ctypes.c_size_t)]
+    lib.ssd_saved_bytes.restype = ctypes.c_int
     lib.ssd_bwd.restype = ctypes.c_int
     lib.ssd_set_path.argtypes = [ctypes.c_int]
     lib.ssd_set_path.restype = ctypes.c_int
@@ -336,6 +342,73 @@ def ssd_bwd_ex(q, k, v, log_alpha, h0, dout, dhT, chunk=64, want_dh0=True, grads
                         _stream(stream))
     if rc:
         raise SSDError(rc, "ssd_bwd_ex")
+    return g
+
+
+def ssd_saved_bytes(B, L, G, H, dk, dv, chunk=64) -> int:
+    """Bytes of the segment states ssd_fwd_save keeps for ssd_bwd_saved (0 when
+    the active path keeps none)."""
+    n = ctypes.c_size_t(0)
+    rc = LIB.ssd_saved_bytes(B, L, G, H, dk, dv, chunk, ctypes.byref(n))
+    if rc:
+        raise SSDError(rc, "ssd_saved_bytes")
+    return int(n.value)
+
+
+def _check_saved(saved, n, dev):
+    if saved is None:
+        return
+    if not isinstance(saved, torch.Tensor) or saved.dtype != torch.float32 or saved.dim() != 1:
+        raise TypeError("saved must be a 1-D float32 torch tensor")
+    _check("saved", saved, (n,), dev)
+
+
+def ssd_fwd_save(q, k, v, log_alpha, h0=None, chunk=64, out=None, hT=None, saved=None,
+                 stream=None):
+    """(out, hT, saved): ssd_fwd_ex, plus the segment states for ssd_bwd_saved
+    (a flat float32 tensor of ssd_saved_bytes // 4 elements, None when the
+    active path keeps none)."""
+    B, L, G, H, dk, dv = _dims(q, v)
+    dev = q.device
+    for n, t, s in (("q", q, (B, L, G, dk)), ("k", k, (B, L, G, dk)), ("v", v, (B, L, H, dv)),
+                    ("log_alpha", log_alpha, (B, L, H)), ("h0", h0, (B, H, dk, dv))):
+        _check(n, t, s, dev)
+    if out is None:
+        out = torch.empty((B, L, H, dv), dtype=torch.float32, device=dev)
+    if hT is None:
+        hT = torch.empty((B, H, dk, dv), dtype=torch.float32, device=dev)
+    n_saved = ssd_saved_bytes(B, L, G, H, dk, dv, chunk) // 4
+    if saved is None and n_saved:
+        saved = torch.empty((n_saved,), dtype=torch.float32, device=dev)
+    _check("out", out, (B, L, H, dv), dev)
+    _check("hT", hT, (B, H, dk, dv), dev)
+    _check_saved(saved, n_saved, dev)
+    rc = LIB.ssd_fwd_save(_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(h0), _ptr(out),
+                          _ptr(hT), _ptr(saved), B, L, G, H, dk, dv, int(chunk), _stream(stream))
+    if rc:
+        raise SSDError(rc, "ssd_fwd_save")
+    return out, hT, saved
+
+
+def ssd_bwd_saved(q, k, v, log_alpha, h0, dout, dhT, hT, saved, chunk=64, want_dh0=True,
+                  grads=None, stream=None):
+    """ssd_bwd_ex with the segment states ``saved`` (and final state ``hT``)
+    that ssd_fwd_save returned for the same inputs."""
+    B, L, G, H, dk, dv = _dims(q, v)
+    dev = q.device
+    for n, t, s in (("q", q, (B, L, G, dk)), ("k", k, (B, L, G, dk)), ("v", v, (B, L, H, dv)),
+                    ("log_alpha", log_alpha, (B, L, H)), ("h0", h0, (B, H, dk, dv)),
+                    ("dout", dout, (B, L, H, dv)), ("dhT", dhT, (B, H, dk, dv)),
+                    ("hT", hT, (B, H, dk, dv))):
+        _check(n, t, s, dev)
+    _check_saved(saved, ssd_saved_bytes(B, L, G, H, dk, dv, chunk) // 4 if saved is not None else 0, dev)
+    g = _grad_buffers(B, L, G, H, dk, dv, dev, want_dh0, grads)
+    rc = LIB.ssd_bwd_saved(_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(h0), _ptr(dout),
+                           _ptr(dhT), _ptr(hT), _ptr(saved), _ptr(g["dq"]), _ptr(g["dk"]),
+                           _ptr(g["dv"]), _ptr(g["dlog_alpha"]), _ptr(g["dh0"]), B, L, G, H, dk,
+                           dv, int(chunk), _stream(stream))
+    if rc:
+        raise SSDError(rc, "ssd_bwd_saved")
     return g
 
 

@@ -219,3 +219,51 @@ def test_mamba_host_checks(lib):
     assert lib.ssd_mamba_workspace_bytes(0, 4, 8192, 1024, 16, ctypes.byref(fwd_n)) == 0
     # forward: states + delta sums per segment; backward adds the u states
     assert 0 < fwd_n.value < n.value < 2 * fwd_n.value
+
+
+def _fwd_save(lib, ptrs=(0x1000,) * 8, B=1, L=8, G=1, H=1, dk=8, dv=8, chunk=64):
+    lib.ssd_fwd_save.argtypes = [ctypes.c_void_p] * 8 + [ctypes.c_int64] * 7 + [ctypes.c_void_p]
+    return lib.ssd_fwd_save(*[ctypes.c_void_p(x) for x in ptrs], B, L, G, H, dk, dv, chunk, None)
+
+
+def _bwd_saved(lib, ptrs=(0x1000,) * 14, B=1, L=8, G=1, H=1, dk=8, dv=8, chunk=64):
+    lib.ssd_bwd_saved.argtypes = [ctypes.c_void_p] * 14 + [ctypes.c_int64] * 7 + [ctypes.c_void_p]
+    return lib.ssd_bwd_saved(*[ctypes.c_void_p(x) for x in ptrs], B, L, G, H, dk, dv, chunk, None)
+
+
+def _saved_bytes(lib, B=1, L=8, G=1, H=1, dk=8, dv=8, chunk=64):
+    lib.ssd_saved_bytes.argtypes = [ctypes.c_int64] * 7 + [ctypes.POINTER(ctypes.c_size_t)]
+    n = ctypes.c_size_t(123)
+    rc = lib.ssd_saved_bytes(B, L, G, H, dk, dv, chunk, ctypes.byref(n))
+    return rc, n.value
+
+
+@pytest.mark.parametrize("path", [0, 1])
+def test_host_argument_checks_saved_states(lib, path):
+    assert lib.ssd_set_path(path) == 0
+    assert _fwd_save(lib, ptrs=(0x1000,) * 7 + (0x1008,)) == 2                  # saved misaligned
+    assert _bwd_saved(lib, ptrs=(0x1000,) * 8 + (0x1004,) + (0x1000,) * 5) == 2  # saved
+    assert _bwd_saved(lib, ptrs=(0x1000,) * 7 + (0x100c,) + (0x1000,) * 6) == 2  # hT
+    assert _fwd_save(lib, G=2, H=3) == 1
+    assert _bwd_saved(lib, dk=0) == 1
+    assert _fwd_save(lib, L=0, ptrs=(0,) * 8) == 0    # empty: nothing to keep
+    assert _bwd_saved(lib, L=0, ptrs=(0,) * 14) == 0
+    if path == 0:  # saved and dhT without the final state: refused before any launch
+        assert _bwd_saved(lib, ptrs=(0x1000,) * 7 + (0,) + (0x1000,) * 6) == 1
+    assert lib.ssd_set_path(0) == 0
+
+
+def test_saved_bytes(lib):
+    assert lib.ssd_set_path(0) == 0
+    rc, n = _saved_bytes(lib, B=4, L=8192, G=2, H=8, dk=128, dv=128)
+    # whole [dv x dk] states, one per (batch, head, segment), at least one segment
+    unit = 4 * 8 * 128 * 128 * 4
+    assert rc == 0 and n >= unit and n % unit == 0
+    assert _saved_bytes(lib, L=0) == (0, 0)
+    assert _saved_bytes(lib, chunk=1) == (0, 0)      # the sequential evaluation keeps none
+    assert _saved_bytes(lib, G=2, H=3)[0] == 1
+    assert lib.ssd_set_path(1) == 0
+    assert _saved_bytes(lib) == (0, 0)               # nor does the CUDA-core path
+    assert lib.ssd_set_path(0) == 0
+    lib.ssd_saved_bytes.argtypes = [ctypes.c_int64] * 7 + [ctypes.c_void_p]
+    assert lib.ssd_saved_bytes(1, 8, 1, 1, 8, 8, 64, None) == 1

@@ -1,5 +1,5 @@
 """The differentiable entry point ssd_scan: its forward and the gradients
-autograd returns are the library's ssd_fwd / ssd_bwd (and _ex) results on
+autograd returns are the library's ssd_fwd_save / ssd_bwd_saved results on
 the same inputs, the gradients agree with the float64 oracle, and tensors
 that are not on a CUDA device are refused (there is no CPU path)."""
 import os
@@ -62,13 +62,11 @@ def test_autograd_matches_library_calls(final, with_h0):
     loss.backward()
     torch.cuda.synchronize()
 
+    ref_out, ref_hT, saved = ssd.ssd_fwd_save(q, k, v, la, h0, chunk=64)
+    g = ssd.ssd_bwd_saved(q, k, v, la, h0, dout, dhT if final else None, ref_hT, saved, chunk=64,
+                          want_dh0=h0 is not None)
     if final:
-        ref_out, ref_hT = ssd.ssd_fwd_ex(q, k, v, la, h0, chunk=64)
-        g = ssd.ssd_bwd_ex(q, k, v, la, h0, dout, dhT, chunk=64, want_dh0=h0 is not None)
         assert _same(hT, ref_hT, exact=True)
-    else:
-        ref_out = ssd.ssd_fwd(q, k, v, la, h0, chunk=64)
-        g = ssd.ssd_bwd(q, k, v, la, h0, dout, chunk=64, want_dh0=h0 is not None)
     torch.cuda.synchronize()
     assert _same(out, ref_out, exact=True)
     grads = dict(zip(("dq", "dk", "dv", "dlog_alpha"), (t.grad for t in leaves)))
