@@ -1,10 +1,11 @@
 #!/usr/bin/env python
 """Throughput of the chunked SSD scan (fwd + bwd) on one or more GPUs.
 
-A step is one forward and one backward pass (ssd_fwd_save then ssd_bwd_saved:
-the whole hot path, the backward reading the forward's segment states as a
-training step keeps them; --recompute times ssd_fwd then ssd_bwd, which keeps
-nothing) over the g2h8_d128 L=8192 long-memory workload: B=4, G=2, H=8,
+A step is one forward and one backward pass (ssd_fwd then ssd_bwd: the whole
+hot path, the backward recomputing what it needs from the inputs, so nothing
+is kept between the two, as in the pages' chunked records; --saved-states
+times ssd_fwd_save then ssd_bwd_saved instead, the backward reading the
+forward's segment states) over the g2h8_d128 L=8192 long-memory workload: B=4, G=2, H=8,
 L=8192, dk=dv=128, chunk 64, fp32 storage, seeded synthetic inputs.  The
 metric is tokens/s with tokens = B*L*H per step.  Prints ONE JSON line
 (rank 0).
@@ -975,9 +976,10 @@ def main():
                     help="tensor-core backward with deterministic group sums (ssd_set_deterministic)")
     ap.add_argument("--no-accuracy", action="store_true",
                     help="skip the rel_err fields (the float64 oracle on a sample of the workload)")
-    ap.add_argument("--recompute", action="store_true",
-                    help="fwd_bwd step as ssd_fwd + ssd_bwd (the backward recomputes the "
-                         "forward's segment states) instead of ssd_fwd_save + ssd_bwd_saved")
+    ap.add_argument("--saved-states", action="store_true",
+                    help="fwd_bwd step as ssd_fwd_save + ssd_bwd_saved (the forward keeps its "
+                         "segment states for the backward: residual memory) instead of "
+                         "ssd_fwd + ssd_bwd (recompute, no residual)")
     ap.add_argument("--mode", default="fwd_bwd", choices=["fwd_bwd", "fwd", "max_len"],
                     help="fwd times ssd_fwd alone (a step is then one forward pass); "
                          "max_len finds the largest sequence length fwd_bwd runs at")
@@ -1027,7 +1029,7 @@ def main():
              "dlog_alpha": torch.empty_like(la), "dh0": torch.empty_like(h0)}
     stream = torch.cuda.current_stream(dev)
     # the forward's segment states (and final state) kept for the backward
-    save = args.mode == "fwd_bwd" and not args.recompute
+    save = args.mode == "fwd_bwd" and args.saved_states
     n_saved = ssd.ssd_saved_bytes(w.B, w.L, w.G, w.H, w.dk, w.dv, w.chunk) // 4 if save else 0
     saved = torch.empty((n_saved,), device=dev) if n_saved else None
     hT = torch.empty_like(h0) if save else None

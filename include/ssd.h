@@ -175,7 +175,10 @@ SSD_API int ssd_bwd_ex(const float *q, const float *k, const float *v,
  * SM in all), which ssd_bwd / ssd_bwd_ex recompute from k, v, log_alpha and
  * h0: a contraction over the whole sequence and a scan, the same work the
  * forward did.  ssd_fwd_save keeps the forward's copy in a caller buffer and
- * ssd_bwd_saved reads it there instead.
+ * ssd_bwd_saved reads it there instead.  The benchmark pages' chunked
+ * records keep nothing between the forward and the backward (residual 0 MB),
+ * as ssd_fwd / ssd_bwd do; this pair is an option for callers that can spare
+ * the buffer.
  *
  * ssd_saved_bytes: the size of that buffer for the active path and the
  *   current device (it depends on the SM count, like the workspace):

@@ -1,6 +1,6 @@
 """The differentiable entry point ssd_scan: its forward and the gradients
-autograd returns are the library's ssd_fwd_save / ssd_bwd_saved results on
-the same inputs, the gradients agree with the float64 oracle, and tensors
+autograd returns are the library's ssd_fwd_ex / ssd_bwd_ex results (with
+save_states, ssd_fwd_save / ssd_bwd_saved) on the same inputs, the gradients agree with the float64 oracle, and tensors
 that are not on a CUDA device are refused (there is no CPU path)."""
 import os
 
@@ -38,7 +38,8 @@ def _same(a, b, exact):
 @pytest.mark.gpu
 @pytest.mark.parametrize("final", [False, True])
 @pytest.mark.parametrize("with_h0", [True, False])
-def test_autograd_matches_library_calls(final, with_h0):
+@pytest.mark.parametrize("save_states", [False, True])
+def test_autograd_matches_library_calls(final, with_h0, save_states):
     import torch
     from oracle import ssd_bwd_ref
     from ssd_chunked_scan_gb300 import ssd
@@ -52,7 +53,7 @@ def test_autograd_matches_library_calls(final, with_h0):
     dhT = torch.from_numpy(np.random.default_rng(5).standard_normal((B, H, dk, dv)).astype(np.float32)).cuda()
     leaves = [t.clone().requires_grad_(True) for t in (q, k, v, la)]
     h0_leaf = h0.clone().requires_grad_(True) if h0 is not None else None
-    res = ssd_scan(*leaves, h0_leaf, chunk=64, return_final_state=final)
+    res = ssd_scan(*leaves, h0_leaf, chunk=64, return_final_state=final, save_states=save_states)
     if final:
         out, hT = res
         loss = (out * dout).sum() + (hT * dhT).sum()
@@ -62,9 +63,14 @@ def test_autograd_matches_library_calls(final, with_h0):
     loss.backward()
     torch.cuda.synchronize()
 
-    ref_out, ref_hT, saved = ssd.ssd_fwd_save(q, k, v, la, h0, chunk=64)
-    g = ssd.ssd_bwd_saved(q, k, v, la, h0, dout, dhT if final else None, ref_hT, saved, chunk=64,
-                          want_dh0=h0 is not None)
+    if save_states:
+        ref_out, ref_hT, saved = ssd.ssd_fwd_save(q, k, v, la, h0, chunk=64)
+        g = ssd.ssd_bwd_saved(q, k, v, la, h0, dout, dhT if final else None, ref_hT, saved, chunk=64,
+                              want_dh0=h0 is not None)
+    else:
+        ref_out, ref_hT = ssd.ssd_fwd_ex(q, k, v, la, h0, chunk=64)
+        g = ssd.ssd_bwd_ex(q, k, v, la, h0, dout, dhT if final else None, chunk=64,
+                           want_dh0=h0 is not None)
     if final:
         assert _same(hT, ref_hT, exact=True)
     torch.cuda.synchronize()
