@@ -382,11 +382,11 @@ __global__ void __launch_bounds__(SS_THREADS, 1) k_seg_state(const __grid_consta
 //                entering the last is init, or 0; the state left of segment 0
 //                goes to fin
 // init is read, and fin (if given) written, transposed when TRANS.  When stT
-// is given, every result is also written there transposed; with tfast (the
+// is given, every result is also written there transposed.  With tfast (the
 // block's 4*NTH elements are R = 4*NTH/dv whole rows, R a multiple of 4 that
-// divides dk) through a shared-memory tile, so that each thread stores four
-// consecutive elements of one transposed row as a float4, else element by
-// element.
+// divides dk) every transposed read or write (init, fin, stT) goes through a
+// shared-memory tile, so that each thread moves four consecutive elements of
+// one transposed row as a float4; otherwise element by element.
 // grid (B*H, ceil(dk*dv / (4*128))), dk*dv a multiple of 4
 constexpr int SU = 10;
 template <bool REV, bool TRANS>
@@ -404,14 +404,20 @@ __global__ void __launch_bounds__(NTH) k_seg_scan(float *__restrict__ st,
   float4 *q = reinterpret_cast<float4 *>(st);
   const int64_t sz4 = sz / 4, qb = (bh * p.nseg * sz + e0) / 4;  // (sz and e0 multiples of 4)
   const int64_t n_st = p.B * p.H * p.nseg * sz, n_a = p.B * p.H * p.nseg, n_h = p.B * p.H * sz;
-  float run[4] = {0.f, 0.f, 0.f, 0.f};
-  if (init) {
-#pragma unroll
-    for (int j = 0; j < 4; ++j) run[j] = LDC(init, bh * sz + (TRANS ? tpos(e0 + j) : e0 + j), n_h);
-  }
-  for (int k0 = 0; k0 < p.nseg; k0 += SU) {
-    float4 x[SU];
-    float d[SU];
+  // tfast: this thread's float4 of the transposed block is column jj, rows
+  // i0 + 4 r4 .. + 3 (offset tq from a matrix's start); the tile holds the
+  // block row-major, thread t's own four elements at tile[t]
+  const int R = tfast ? 4 * NTH / p.dv : 4, nq = R / 4;
+  const int jj = (int)threadIdx.x / nq, r4 = (int)threadIdx.x % nq;
+  const int64_t tq = (int64_t)jj * p.dk + (int64_t)blockIdx.y * R + 4 * r4;
+  float *tf = reinterpret_cast<float *>(tile);
+  auto col_of_tile = [&]() {
+    return make_float4(tf[(4 * r4) * p.dv + jj], tf[(4 * r4 + 1) * p.dv + jj], tf[(4 * r4 + 2) * p.dv + jj],
+                       tf[(4 * r4 + 3) * p.dv + jj]);
+  };
+  float4 x[SU];
+  float d[SU];
+  auto load_batch = [&](int k0) {
 #pragma unroll
     for (int u = 0; u < SU; ++u) {
       const int k = k0 + u;
@@ -421,6 +427,27 @@ __global__ void __launch_bounds__(NTH) k_seg_scan(float *__restrict__ st,
         d[u] = expf(LDC(Aseg, bh * p.nseg + s, n_a));
       }
     }
+  };
+  load_batch(0);  // (in flight while the initial state is fetched)
+  float run[4] = {0.f, 0.f, 0.f, 0.f};
+  if (init && TRANS && tfast) {  // a float4 of the transposed block, turned round in the tile
+    const float4 t4 = LDC(reinterpret_cast<const float4 *>(init), (bh * sz + tq) / 4, n_h / 4);
+    tf[(4 * r4) * p.dv + jj] = t4.x;
+    tf[(4 * r4 + 1) * p.dv + jj] = t4.y;
+    tf[(4 * r4 + 2) * p.dv + jj] = t4.z;
+    tf[(4 * r4 + 3) * p.dv + jj] = t4.w;
+    __syncthreads();
+    const float4 r = tile[threadIdx.x];
+    run[0] = r.x, run[1] = r.y, run[2] = r.z, run[3] = r.w;
+  } else if (init && TRANS) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) run[j] = LDC(init, bh * sz + tpos(e0 + j), n_h);
+  } else if (init) {
+    const float4 r = LDC(reinterpret_cast<const float4 *>(init), (bh * sz + e0) / 4, n_h / 4);
+    run[0] = r.x, run[1] = r.y, run[2] = r.z, run[3] = r.w;
+  }
+  for (int k0 = 0; k0 < p.nseg; k0 += SU) {
+    if (k0 > 0) load_batch(k0);
 #pragma unroll
     for (int u = 0; u < SU; ++u) {
       const int k = k0 + u;
@@ -428,18 +455,11 @@ __global__ void __launch_bounds__(NTH) k_seg_scan(float *__restrict__ st,
         const int s = REV ? p.nseg - 1 - k : k;
         STC(q, qb + (int64_t)s * sz4, n_st / 4, make_float4(run[0], run[1], run[2], run[3]));
         if (stT && tfast) {
-          // column jj of the block's R rows (from row i0): R / 4 float4s
-          const int R = 4 * NTH / p.dv, nq = R / 4;
-          const int jj = (int)threadIdx.x / nq, r4 = (int)threadIdx.x % nq;
-          const int64_t i0 = (int64_t)blockIdx.y * R;
-          __syncthreads();  // the previous segment's tile is read
+          __syncthreads();  // the tile's previous contents are read
           tile[threadIdx.x] = make_float4(run[0], run[1], run[2], run[3]);
           __syncthreads();
-          const float *tf = reinterpret_cast<const float *>(tile);
-          const float4 t4 = make_float4(tf[(4 * r4) * p.dv + jj], tf[(4 * r4 + 1) * p.dv + jj],
-                                        tf[(4 * r4 + 2) * p.dv + jj], tf[(4 * r4 + 3) * p.dv + jj]);
-          STC(reinterpret_cast<float4 *>(stT), (bh * p.nseg * sz + (int64_t)s * sz + jj * p.dk + i0 + 4 * r4) / 4,
-              n_st / 4, t4);
+          STC(reinterpret_cast<float4 *>(stT), (bh * p.nseg * sz + (int64_t)s * sz + tq) / 4, n_st / 4,
+              col_of_tile());
         } else if (stT) {
 #pragma unroll
           for (int j = 0; j < 4; ++j) STC(stT, bh * p.nseg * sz + (int64_t)s * sz + tpos(e0 + j), n_st, run[j]);
@@ -451,9 +471,16 @@ __global__ void __launch_bounds__(NTH) k_seg_scan(float *__restrict__ st,
       }
     }
   }
-  if (fin) {
+  if (fin && TRANS && tfast) {
+    __syncthreads();
+    tile[threadIdx.x] = make_float4(run[0], run[1], run[2], run[3]);
+    __syncthreads();
+    STC(reinterpret_cast<float4 *>(fin), (bh * sz + tq) / 4, n_h / 4, col_of_tile());
+  } else if (fin && TRANS) {
 #pragma unroll
-    for (int j = 0; j < 4; ++j) STC(fin, bh * sz + (TRANS ? tpos(e0 + j) : e0 + j), n_h, run[j]);
+    for (int j = 0; j < 4; ++j) STC(fin, bh * sz + tpos(e0 + j), n_h, run[j]);
+  } else if (fin) {
+    STC(reinterpret_cast<float4 *>(fin), (bh * sz + e0) / 4, n_h / 4, make_float4(run[0], run[1], run[2], run[3]));
   }
 }
 
