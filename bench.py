@@ -67,18 +67,19 @@ def load_peaks():
 # file in the tree no longer hashes to that, the group's figures no longer
 # describe the kernels and the bench line reports traffic null, saying why.
 TRAFFIC_GROUPS = {
-    "tc.": {"source": "ssd_chunked_scan_gb300/csrc/tc.cu", "sha16": "5a668854d1e62e34", "commit": "02a28d2",
+    "tc.": {"source": "ssd_chunked_scan_gb300/csrc/tc.cu", "sha16": "099217a7823d52e0", "commit": "65b9d9e",
             "bytes": {
-                "tc.seg_state": 172689664,
-                "tc.seg_state_dq": 169597184,
-                "tc.seg_state_dk": 169251584,
-                "tc.seg_scan": (10531072 + 8445952 + 10536448) // 3,  # mean of the three passes' scans
-                "tc.walk_out": 303384576,
-                "tc.walk_dq": 403106816,
-                "tc.walk_dk": 402502656,
-                "tc.walk_dv": 304101888,
-                "tc.dla_intra": 337807360,
-                "tc.dla": 15751424,
+                "tc.seg_state": 172368384,
+                "tc.seg_state_dq": 169227264,
+                "tc.seg_state_dk": 169054464,
+                "tc.seg_scan": (10548224 + 8460032 + 10553088) // 3,  # mean of the three passes' scans
+                "tc.walk_out": 303465216,
+                "tc.walk_dq": 403092992,
+                "tc.walk_dk": 402278656,
+                "tc.walk_dv": 304434688,
+                "tc.dla_intra": 337525760,
+                "tc.dla_carry": 12590080,
+                "tc.dla": 3171584,
             }},
     "simt.": {"source": "ssd_chunked_scan_gb300/csrc/simt.cu", "sha16": "5682068978fc8373", "commit": "02155b1",
               "bytes": {}},
