@@ -1795,10 +1795,11 @@ cudaError_t bwd(const float *q, const float *k, const float *v, const float *la,
   const float *hT_r = saved ? hT_saved : hT;
   const int oslots = atomic ? (int)g.G : (int)g.H;
   // The dk / dv passes (pass B's states, both anti-causal walks) run on one
-  // side stream and the intra-chunk dlog_alpha sums (inputs only) on another,
-  // both forked from s after the memsets and joined before k_dla (or all on s
-  // when overlap is off).  The walks take one CTA per SM and leave the rest
-  // of the SMs to the other streams' kernels.
+  // side stream (s2) and the intra-chunk dlog_alpha sums (inputs only) on
+  // another (s3), both forked from s and joined back into s before this
+  // returns (or all on s when overlap is off); the rest of dlog_alpha follows
+  // on s3 (below).  The walks take one CTA per SM and leave the rest of the
+  // SMs to the other streams' kernels.
   const bool overlap = g_overlap.load();
   std::unique_lock<std::mutex> lock(g_side_mu, std::defer_lock);
   Side *sd = nullptr;
