@@ -95,3 +95,41 @@ def test_saved_workload_parity(w):
                 "dv": _unit(g["dv"], b, hs), "dlog_alpha": _unit(g["dlog_alpha"], b, hs),
                 "dh0": np.ascontiguousarray(g["dh0"][b:b + 1, hs])}
         compare("tc", _unit(out, b, hs), mine, ref, rg, label=f"saved {w.name} unit b{b} g{gi}")
+
+
+@pytest.mark.parametrize("shape", [(2, 300, 2, 8, 128, 128), (2, 129, 3, 6, 48, 40)],
+                         ids=lambda s: "B{}L{}G{}H{}dk{}dv{}".format(*s))
+def test_saved_with_every_backward_mode(shape):
+    """The saved-state backward under each stream and group-sum mode: overlap
+    on and off, atomic and deterministic group sums; all against the oracle,
+    and the deterministic runs bitwise equal to each other."""
+    import torch
+    from ssd_chunked_scan_gb300 import ssd
+    B, L, G, H, dk, dv = shape
+    old = (ssd.ssd_get_path(), ssd.ssd_get_overlap(), ssd.ssd_get_deterministic())
+    ssd.ssd_set_path(ssd.SSD_PATH_TC)
+    try:
+        q, k, v, la, h0, dout = make_inputs(B, L, G, H, dk, dv, seed=sum(shape) + 3, la_mu=-3.0)
+        dhT = make_state_cotangent(B, H, dk, dv, seed=sum(shape))
+        tq, tk, tv, tla, th0, tdo, tdh = map(to_dev, (q, k, v, la, h0, dout, dhT))
+        out, hT, saved = ssd.ssd_fwd_save(tq, tk, tv, tla, th0, chunk=64)
+        rg = ssd_bwd_ref(q, k, v, la, h0, dout, dhT=dhT)
+        det_runs = []
+        for overlap in (True, False):
+            for det in (False, True):
+                ssd.ssd_set_overlap(overlap)
+                ssd.ssd_set_deterministic(det)
+                g = ssd.ssd_bwd_saved(tq, tk, tv, tla, th0, tdo, tdh, hT, saved, chunk=64)
+                torch.cuda.synchronize()
+                assert ssd.ssd_last_device_error() == 0
+                g = _np(g)
+                compare("tc", out.cpu().numpy(), g, ssd_fwd_ref(q, k, v, la, h0), rg,
+                        label=f"saved {shape} overlap={overlap} det={det}")
+                if det:
+                    det_runs.append(g)
+        for n in det_runs[0]:
+            assert np.array_equal(det_runs[0][n], det_runs[1][n]), n
+    finally:
+        ssd.ssd_set_path(old[0])
+        ssd.ssd_set_overlap(bool(old[1]))
+        ssd.ssd_set_deterministic(bool(old[2]))
