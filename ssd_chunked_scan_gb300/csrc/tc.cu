@@ -905,15 +905,27 @@ __global__ void __launch_bounds__(walk_threads(SPLIT), 1) k_walk(const __grid_co
     const int64_t n_out = p.B * p.L * ld, n_y = p.B * p.L * ldy;
     // SPLIT: the y values of 16-token step (chunk cy, step g), loaded two steps
     // before they are used (yr0: this step, yr1: the next; the ring runs
-    // across chunks), so the loads' latency hides behind the steps between
+    // across chunks), so the loads' latency hides behind the steps between.
+    // A lane pair (features fb, fb + 1) loads float2s: the even lane tokens
+    // 0-7 of the step, the odd lane tokens 8-15 (dst[2i], dst[2i + 1] = the
+    // two features of token i of its half); the step swaps the halves' other
+    // feature between the pair, so each load instruction brings two rows.
     float yr0[SPLIT ? 16 : 1], yr1[SPLIT ? 16 : 1];
     auto load_y = [&](float (&dst)[SPLIT ? 16 : 1], int cy, int g) {
       if constexpr (SPLIT) {
         const int64_t ty = s_begin + (int64_t)chunk_of(cy < nc ? cy : 0) * C;
         const int leny = cy < nc ? (int)imin64(C, s_end - ty) : 0;
-        const int64_t y0 = ((b * p.L + ty) * (p.H / p.hpg) + h / p.hpg) * (int64_t)dv + j;
+        const int odd = lane & 1, fb = j - odd;  // (dv is even: a pair is inside or past dv)
+        const int64_t y0 = ((b * p.L + ty) * (p.H / p.hpg) + h / p.hpg) * (int64_t)dv + fb;
+        const float2 *y2 = reinterpret_cast<const float2 *>(oa.y);
 #pragma unroll
-        for (int i = 0; i < 16; ++i) dst[i] = (j < dv && 16 * g + i < leny) ? LDC(oa.y, y0 + (16 * g + i) * ldy, n_y) : 0.f;
+        for (int i = 0; i < 8; ++i) {
+          const int t = 16 * g + 8 * odd + i;
+          const float2 v2 = (fb < dv && t < leny) ? LDC(y2, (y0 + (int64_t)t * ldy) / 2, n_y / 2)
+                                                  : make_float2(0.f, 0.f);
+          dst[2 * i] = v2.x;
+          dst[2 * i + 1] = v2.y;
+        }
       }
     };
     load_y(yr0, 0, g_lo);
@@ -968,12 +980,23 @@ __global__ void __launch_bounds__(walk_threads(SPLIT), 1) k_walk(const __grid_co
         // interleaving them with the (conditional) stores would serialise the
         // shuffle latencies
         const float qsrc = g < 2 ? qfA : qfB;
+        float yv[SPLIT ? 16 : 1];  // this lane's feature of the step's 16 tokens
+        if constexpr (SPLIT) {
+          const bool odd = (lane & 1) != 0;
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const float keep = odd ? yr0[2 * i + 1] : yr0[2 * i];
+            const float got = __shfl_xor_sync(0xffffffffu, odd ? yr0[2 * i] : yr0[2 * i + 1], 1);
+            yv[i] = odd ? got : keep;
+            yv[8 + i] = odd ? keep : got;
+          }
+        }
         float o[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
           const float xi = __shfl_sync(0xffffffffu, qsrc, (16 * g + i) & 31) * xa[i];
           o[i] = xi + ya[i];
-          if constexpr (SPLIT) xa[i] = xi * yr0[i];
+          if constexpr (SPLIT) xa[i] = xi * yv[i];
         }
         if constexpr (SPLIT) {  // shift the ring and load two steps ahead
 #pragma unroll
