@@ -67,20 +67,19 @@ def load_peaks():
 # file in the tree no longer hashes to that, the group's figures no longer
 # describe the kernels and the bench line reports traffic null, saying why.
 TRAFFIC_GROUPS = {
-    # (captured at 65b9d9e's tc.cu; the file has changed since in one comment only)
-    "tc.": {"source": "ssd_chunked_scan_gb300/csrc/tc.cu", "sha16": "8d6fbe99af3f8639", "commit": "65b9d9e",
+    "tc.": {"source": "ssd_chunked_scan_gb300/csrc/tc.cu", "sha16": "c7871499ec73c5ad", "commit": "0112b14",
             "bytes": {
-                "tc.seg_state": 172368384,
-                "tc.seg_state_dq": 169227264,
-                "tc.seg_state_dk": 169054464,
-                "tc.seg_scan": (10548224 + 8460032 + 10553088) // 3,  # mean of the three passes' scans
-                "tc.walk_out": 303465216,
-                "tc.walk_dq": 403092992,
-                "tc.walk_dk": 402278656,
-                "tc.walk_dv": 304434688,
-                "tc.dla_intra": 337525760,
-                "tc.dla_carry": 12590080,
-                "tc.dla": 3171584,
+                "tc.seg_state": 172355072,
+                "tc.seg_state_dq": 169376768,
+                "tc.seg_state_dk": 169300736,
+                "tc.seg_scan": (10550272 + 8458752 + 10553088) // 3,  # mean of the three passes' scans
+                "tc.walk_out": 303517696,
+                "tc.walk_dq": 403231232,
+                "tc.walk_dk": 401504256,
+                "tc.walk_dv": 304301056,
+                "tc.dla_intra": 338004480,
+                "tc.dla_carry": 12590336,
+                "tc.dla": 3171328,
             }},
     "simt.": {"source": "ssd_chunked_scan_gb300/csrc/simt.cu", "sha16": "5682068978fc8373", "commit": "02155b1",
               "bytes": {}},
